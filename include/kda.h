@@ -1,0 +1,176 @@
+/*
+ * kda.h -- C ABI of libkda, Kimi Delta Attention (KDA) on NVIDIA GB300 (sm_103a).
+ *
+ * The operations are those of the Kimi K3 technical report:
+ *   - bounded gate, section 2.1.1 Eq. 5 (the bias b of Eq. 2 sits inside the
+ *     logit, as in the flash-linear-attention `lower_bound` gate quoted by the
+ *     xuquant.com review of the report):
+ *         g = g_min * Sigmoid(exp(A_log[h]) * (z + b[h])),   alpha = exp(g)
+ *   - recurrence, section 2.1.1 Eq. 1 (decay before the delta update):
+ *         S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *         o_t = scale * S_t^T q_t              (scale = 1 in the report)
+ *   - chunkwise evaluation, section 2.1.1 Eq. 3 and Eq. 4 (parallel inside a
+ *     chunk, recurrent across chunks), and the single-token decode step of
+ *     section 5.4.2.
+ *
+ * Conventions shared by every entry point
+ *   - Memory: every tensor pointer is a DEVICE pointer on the current CUDA
+ *     device, owned by the caller.  The library allocates no device memory and
+ *     frees nothing; the prefill scratch ("workspace") is passed in by the caller
+ *     and sized by kda_chunk_fwd_workspace_size().  Tensors are dense,
+ *     row-major ("C-contiguous") with the shapes stated below, and 16-byte
+ *     aligned.
+ *   - Layout: token-major [T, H, d] for per-token vectors (T = all tokens of all
+ *     sequences packed back to back), [T, H] for beta, [H, d_k] for dt_bias,
+ *     [H] for A_log, and [N, H, d_k, d_v] for recurrent states (row = key
+ *     channel, column = value channel; each head's 128 x 128 state is one
+ *     contiguous block, as in the paged state layout of section 5.4.1).
+ *   - Types: kda_dtype_t selects the I/O type of q, k, v, z, beta and o (fp32 or
+ *     bf16).  dt_bias, A_log and states are always fp32.  Arithmetic is fp32.
+ *   - Streams: work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and returns before it finishes.
+ *   - Errors: every call validates its arguments on the host first and returns
+ *     a kda_status_t; on failure it launches nothing.  Nothing aborts, traps or
+ *     throws across this boundary.  Problems only visible on the device
+ *     (inconsistent cu_seqlens contents, an out-of-range state index) set a
+ *     device error word that kda_get_device_error() reads back and clears; the
+ *     affected work items are skipped.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+#define KDA_ABI_VERSION 1
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,       /* NULL where a tensor is required, negative size, bad g_min */
+    KDA_ERR_UNSUPPORTED_SHAPE = 2, /* head size or chunk size not built into this library */
+    KDA_ERR_UNSUPPORTED_DTYPE = 3,
+    KDA_ERR_MISALIGNED = 4,        /* a tensor pointer is not 16-byte aligned */
+    KDA_ERR_WORKSPACE = 5,         /* workspace NULL or smaller than required */
+    KDA_ERR_CUDA = 6,              /* a CUDA runtime call or launch failed */
+    KDA_ERR_BAD_SEQLENS = 7,       /* (device) cu_seqlens not 0 = c_0 <= c_1 <= ... <= c_N = T */
+    KDA_ERR_BAD_STATE_INDEX = 8,   /* (device) state_indices entry outside [0, num_slots) */
+    KDA_ERR_NO_DEVICE = 9,         /* no current CUDA device of compute capability 10.3 */
+    KDA_ERR_DEVICE_TIMEOUT = 10    /* (device) a bounded wait inside a kernel gave up */
+} kda_status_t;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
+
+/* ------------------------------------------------------------------ kda_gate
+ * Eq. 5 (section 2.1.1): per-channel log-decay g = g_min * Sigmoid(exp(A_log[h]) * (z + b[h]))
+ * for every token, optionally followed by the chunk-local cumulative sum of
+ * Eq. 3 in log space, G_r = sum_{i <= r} g_i, restarting at every chunk start
+ * (chunks of `chunk_size` tokens aligned to each sequence's first token).
+ */
+typedef struct {
+    int64_t T;                 /* tokens (all sequences packed) */
+    int64_t N;                 /* sequences (>= 1 when T > 0; ignored when chunk_size == 0) */
+    int32_t H;                 /* heads */
+    int32_t dk;                /* key channels (any value >= 1) */
+    kda_dtype_t dtype;         /* dtype of z */
+    const void *z;             /* [T, H, dk] decay logit without bias */
+    const float *dt_bias;      /* [H, dk] per-head bias b, or NULL for zero */
+    const float *A_log;        /* [H] per-head log-scale A, or NULL for zero */
+    float g_min;               /* lower bound of the log-decay, < 0 (the report uses -5) */
+    int32_t chunk_size;        /* 0: write g; > 0: write the chunk-local cumulative sum */
+    const int32_t *cu_seqlens; /* [N + 1] sequence starts, or NULL for N equal lengths T / N */
+    float *out;                /* [T, H, dk] fp32 output */
+} kda_gate_args;
+
+kda_status_t kda_gate(const kda_gate_args *args, struct CUstream_st *stream);
+
+/* ------------------------------------------------------------- kda_chunk_fwd
+ * Prefill: Eq. 1 over whole sequences, evaluated chunkwise as in Eq. 3 and
+ * Eq. 4 (section 2.1.1).  Inside each chunk of C = 64 tokens the UT transform
+ * yields U and W (pseudo-values V~ = U - W S), and outputs are
+ * O = (Gamma * Q) S + Tril[(Q * Gamma)(K / Gamma)^T] V~; across chunks the
+ * state is carried as S <- Diag(gamma^C) S + (K * gamma^C / Gamma)^T V~.
+ * The gate of Eq. 5 is fused.  Chunks start at each sequence's first token;
+ * the last chunk of a sequence may be shorter.
+ *
+ * Supported: d_k = d_v in {64, 128}; chunk_size 64 (0 selects 64).
+ * bf16 with d_k = d_v = 128 runs on the tensor cores (tcgen05); every other
+ * case runs on the fp32 CUDA-core path.
+ */
+typedef struct {
+    int64_t T;                     /* tokens (all sequences packed) */
+    int64_t N;                     /* sequences, >= 1 */
+    int32_t H, dk, dv;             /* heads, key channels, value channels */
+    kda_dtype_t dtype;             /* dtype of q, k, v, z, beta and o */
+    const void *q, *k, *z;         /* [T, H, dk] (q and k as given: the kernels do not normalise) */
+    const void *v;                 /* [T, H, dv] */
+    const void *beta;              /* [T, H] write strength in (0, 1), used as given */
+    const float *dt_bias;          /* [H, dk] or NULL (zero) */
+    const float *A_log;            /* [H] or NULL (zero) */
+    float g_min;                   /* < 0; the report uses -5 */
+    float scale;                   /* output scale; Eq. 1 has none (pass 1) */
+    const int32_t *cu_seqlens;     /* [N + 1] device, or NULL for N sequences of T / N tokens */
+    const int32_t *cu_seqlens_host;/* optional HOST copy of cu_seqlens (enables long-sequence
+                                      splitting across SMs); NULL = plan from T, N alone */
+    const float *initial_state;    /* [N, H, dk, dv] or NULL (zero state) */
+    float *final_state;            /* [N, H, dk, dv] or NULL; may alias initial_state */
+    void *o;                       /* [T, H, dv] output; must not alias an input */
+    int32_t chunk_size;            /* 64, or 0 for the default (64) */
+} kda_chunk_args;
+
+/* Bytes of device scratch kda_chunk_fwd needs for these sizes (0 on invalid sizes).
+ * Depends only on (T, N, H, dk, dv, dtype, chunk_size) and the presence of
+ * cu_seqlens_host (pass has_host_seqlens = 1 when it will be given). */
+size_t kda_chunk_fwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
+                                    kda_dtype_t dtype, int32_t chunk_size,
+                                    const int32_t *cu_seqlens_host);
+
+/* workspace: device memory of at least kda_chunk_fwd_workspace_size() bytes,
+ * 256-byte aligned, owned by the caller; its contents need no initialisation
+ * and are garbage afterwards.  Calls that share a workspace must not overlap. */
+kda_status_t kda_chunk_fwd(const kda_chunk_args *args, void *workspace, size_t workspace_bytes,
+                           struct CUstream_st *stream);
+
+/* -------------------------------------------------------- kda_recurrent_step
+ * Decode: one token per sequence, Eq. 1 applied once to each (sequence, head)
+ * state in place (section 5.4.2: the recurrent state is updated in place every
+ * step).  Evaluated as S' = Diag(alpha) S; e = beta (v - S'^T k);
+ * S <- S' + k e^T; o = scale * (S'^T q + (k . q) e), which equals Eq. 1.
+ * Supported: d_k = d_v in {64, 128}.
+ */
+typedef struct {
+    int64_t N;                     /* sequences in this step */
+    int32_t H, dk, dv;
+    kda_dtype_t dtype;             /* dtype of q, k, v, z, beta and o */
+    const void *q, *k, *z;         /* [N, H, dk] */
+    const void *v;                 /* [N, H, dv] */
+    const void *beta;              /* [N, H] */
+    const float *dt_bias;          /* [H, dk] or NULL */
+    const float *A_log;            /* [H] or NULL */
+    float g_min, scale;
+    float *state;                  /* [num_slots, H, dk, dv] fp32, read and written in place */
+    const int32_t *state_indices;  /* [N] state slot of each sequence, or NULL (slot = n) */
+    int64_t num_slots;             /* slots in `state` (0 means N) */
+    void *o;                       /* [N, H, dv] */
+} kda_step_args;
+
+kda_status_t kda_recurrent_step(const kda_step_args *args, struct CUstream_st *stream);
+
+/* ------------------------------------------------------------------ errors */
+const char *kda_status_string(kda_status_t status);
+
+/* Waits for `stream`, then returns and clears the first device-detected error
+ * (KDA_OK if none).  The word is per device and shared by all streams. */
+kda_status_t kda_get_device_error(struct CUstream_st *stream);
+
+int kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H_ */

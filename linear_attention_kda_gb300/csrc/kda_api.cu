@@ -1,0 +1,178 @@
+// C ABI of libkda: host-side validation and dispatch.  Nothing here allocates
+// device memory; failing validation launches nothing and returns a status.
+#include <math.h>
+#include <stdint.h>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+// One error word per device that loads this library (set by kernels with
+// atomicCAS, first error wins; read and cleared by kda_get_device_error).
+static __device__ int g_kda_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int *g_err_ptr[kMaxDevices];  // device address of g_kda_device_error, per device
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned_to(const void *p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+kda_status_t check_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_NO_DEVICE;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return KDA_ERR_NO_DEVICE;
+    if (major != 10 || minor != 3) return KDA_ERR_NO_DEVICE;
+    return KDA_OK;
+}
+
+bool dtype_ok(kda_dtype_t t) { return t == KDA_F32 || t == KDA_BF16; }
+size_t dtype_size(kda_dtype_t t) { return t == KDA_BF16 ? 2 : 4; }
+
+}  // namespace
+
+int *kda_device_error_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_kda_device_error) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = (int *)p;
+    }
+    return g_err_ptr[dev];
+}
+
+extern "C" {
+
+int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+const char *kda_status_string(kda_status_t s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (head size or chunk size)";
+        case KDA_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+        case KDA_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+        case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+        case KDA_ERR_CUDA: return "CUDA runtime error";
+        case KDA_ERR_BAD_SEQLENS: return "cu_seqlens is not 0 = c_0 <= ... <= c_N = T";
+        case KDA_ERR_BAD_STATE_INDEX: return "state index outside [0, num_slots)";
+        case KDA_ERR_NO_DEVICE: return "no current CUDA device of compute capability 10.3";
+        case KDA_ERR_DEVICE_TIMEOUT: return "bounded wait inside a kernel gave up";
+    }
+    return "unknown status";
+}
+
+kda_status_t kda_get_device_error(struct CUstream_st *stream) {
+    int *p = kda_device_error_ptr();
+    if (!p) return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KDA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_kda_device_error, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    const int zero = 0;
+    if (v != 0 && cudaMemcpyToSymbol(g_kda_device_error, &zero, sizeof(int)) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return (kda_status_t)v;
+}
+
+kda_status_t kda_gate(const kda_gate_args *a, struct CUstream_st *stream) {
+    if (!a) return KDA_ERR_INVALID_ARG;
+    if (a->T < 0 || a->H < 1 || a->dk < 1 || a->chunk_size < 0 || a->chunk_size > 256)
+        return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(a->dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (!(a->g_min < 0.f) || !isfinite(a->g_min)) return KDA_ERR_INVALID_ARG;
+    if (a->T == 0) return KDA_OK;
+    if (!a->z || !a->out) return KDA_ERR_INVALID_ARG;
+    if (a->chunk_size > 0) {
+        if (a->N < 1) return KDA_ERR_INVALID_ARG;
+        if (!a->cu_seqlens && a->T % a->N != 0) return KDA_ERR_INVALID_ARG;
+        if (a->cu_seqlens && !aligned_to(a->cu_seqlens, 4)) return KDA_ERR_MISALIGNED;
+    }
+    if (!aligned16(a->z) || !aligned16(a->out) || (a->dt_bias && !aligned16(a->dt_bias)) ||
+        (a->A_log && !aligned_to(a->A_log, 4)))
+        return KDA_ERR_MISALIGNED;
+    kda_status_t st = check_device();
+    if (st != KDA_OK) return st;
+    return kda_launch_gate(a, (cudaStream_t)stream);
+}
+
+static kda_status_t validate_chunk(const kda_chunk_args *a) {
+    if (!a) return KDA_ERR_INVALID_ARG;
+    if (a->T < 0 || a->N < 1 || a->H < 1) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(a->dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (a->dk != a->dv || (a->dk != 64 && a->dk != 128)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (a->chunk_size != 0 && a->chunk_size != 64) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!(a->g_min < 0.f) || !isfinite(a->g_min) || !isfinite(a->scale)) return KDA_ERR_INVALID_ARG;
+    if (!a->cu_seqlens && a->T % a->N != 0) return KDA_ERR_INVALID_ARG;
+    if (a->T > INT32_MAX) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (a->T > 0) {
+        if (!a->q || !a->k || !a->v || !a->z || !a->beta || !a->o) return KDA_ERR_INVALID_ARG;
+        if (a->o == a->q || a->o == a->k || a->o == a->v || a->o == a->z) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->z) ||
+            !aligned16(a->o) || !aligned_to(a->beta, dtype_size(a->dtype)))
+            return KDA_ERR_MISALIGNED;
+    }
+    if ((a->initial_state && !aligned16(a->initial_state)) ||
+        (a->final_state && !aligned16(a->final_state)) ||
+        (a->dt_bias && !aligned16(a->dt_bias)) || (a->A_log && !aligned_to(a->A_log, 4)) ||
+        (a->cu_seqlens && !aligned_to(a->cu_seqlens, 4)))
+        return KDA_ERR_MISALIGNED;
+    if (a->cu_seqlens_host) {
+        const int32_t *cu = a->cu_seqlens_host;
+        if (cu[0] != 0 || cu[a->N] != a->T) return KDA_ERR_INVALID_ARG;
+        for (int64_t n = 0; n < a->N; ++n)
+            if (cu[n + 1] < cu[n]) return KDA_ERR_INVALID_ARG;
+    }
+    return KDA_OK;
+}
+
+size_t kda_chunk_fwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
+                                    kda_dtype_t dtype, int32_t chunk_size,
+                                    const int32_t *cu_seqlens_host) {
+    (void)cu_seqlens_host;
+    if (T < 0 || N < 1 || H < 1 || !dtype_ok(dtype)) return 0;
+    if (dk != dv || (dk != 64 && dk != 128)) return 0;
+    if (chunk_size != 0 && chunk_size != 64) return 0;
+    kda_chunk_plan p;
+    if (!kda_make_chunk_plan(T, N, H, dk, dv, dtype, 64, &p)) return 0;
+    return p.total_bytes;
+}
+
+kda_status_t kda_chunk_fwd(const kda_chunk_args *a, void *workspace, size_t workspace_bytes,
+                           struct CUstream_st *stream) {
+    kda_status_t st = validate_chunk(a);
+    if (st != KDA_OK) return st;
+    kda_chunk_plan p;
+    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p))
+        return KDA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < p.total_bytes) return KDA_ERR_WORKSPACE;
+    if (!aligned_to(workspace, 256)) return KDA_ERR_MISALIGNED;
+    st = check_device();
+    if (st != KDA_OK) return st;
+    return kda_launch_chunk_simt(a, p, workspace, (cudaStream_t)stream);
+}
+
+kda_status_t kda_recurrent_step(const kda_step_args *a, struct CUstream_st *stream) {
+    if (!a) return KDA_ERR_INVALID_ARG;
+    if (a->N < 0 || a->H < 1 || a->num_slots < 0) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(a->dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (a->dk != a->dv || (a->dk != 64 && a->dk != 128)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!(a->g_min < 0.f) || !isfinite(a->g_min) || !isfinite(a->scale)) return KDA_ERR_INVALID_ARG;
+    if (a->N == 0) return KDA_OK;
+    if (a->N * (int64_t)a->H > INT32_MAX) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!a->q || !a->k || !a->v || !a->z || !a->beta || !a->o || !a->state) return KDA_ERR_INVALID_ARG;
+    if (!a->state_indices && a->num_slots != 0 && a->num_slots < a->N) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->z) ||
+        !aligned16(a->o) || !aligned16(a->state) || !aligned_to(a->beta, dtype_size(a->dtype)) ||
+        (a->dt_bias && !aligned16(a->dt_bias)) || (a->A_log && !aligned_to(a->A_log, 4)) ||
+        (a->state_indices && !aligned_to(a->state_indices, 4)))
+        return KDA_ERR_MISALIGNED;
+    kda_status_t st = check_device();
+    if (st != KDA_OK) return st;
+    return kda_launch_decode(a, (cudaStream_t)stream);
+}
+
+}  // extern "C"

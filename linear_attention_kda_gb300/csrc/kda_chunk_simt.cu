@@ -1,0 +1,291 @@
+// fp32 CUDA-core path of kda_chunk_fwd (any supported head size, fp32 or bf16
+// I/O).  It is the full-precision path: fp32 operands and fp32 accumulation
+// everywhere, so that fp32 I/O meets a 1e-4 relative error bound.
+//
+// Two kernels, following Eq. 3 and Eq. 4 of the Kimi K3 report (section 2.1.1):
+//
+// 1. intra (one CTA per (chunk, head), all chunks in parallel):
+//    g from Eq. 5, G = in-chunk cumulative log-decay (Eq. 3 in log space),
+//    L[r,i] = beta_r sum_c k_rc k_ic e^{G_rc - G_ic}  (i < r),
+//    A[r,i] =        sum_c q_rc k_ic e^{G_rc - G_ic}  (i <= r, diagonal kept),
+//    [W | U] = (I + L)^{-1} [diag(beta)(Gamma * K) | diag(beta) V]   (UT transform,
+//    by forward substitution, one column per thread),
+//    Q^ = Gamma * Q,  K~ = K * e^{G_last - G},  gamma^C = e^{G_last}.
+//    The relative decays are formed as e^{G_r - G_i} directly, never as a
+//    product of Gamma and 1/Gamma, so nothing overflows at any chunk length.
+// 2. chain (one CTA per (sequence, head, 32 value columns), chunks in order):
+//    V~ = U - W S;  O = scale (Q^ S + A V~);  S <- Diag(gamma^C) S + K~^T V~.
+//    Columns of S evolve independently (Eq. 1 acts on S from the left), so the
+//    value dimension is split across CTAs.
+// Tokens past the end of a sequence inside its last chunk are loaded as zeros
+// with g = 0 and beta = 0, which leaves every valid row and the state unchanged.
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+constexpr int SIMT_THREADS = 256;
+constexpr int SLICE = 32;  // value columns per chain CTA
+
+struct RecordView {
+    float *W, *U, *Q, *K, *A, *gam;
+};
+
+__device__ __forceinline__ RecordView record_view(char *base, size_t rec_bytes, int64_t slot, int H,
+                                                  int h, int C, int dk, int dv) {
+    float *r = (float *)(base + ((size_t)slot * H + h) * rec_bytes);
+    RecordView v;
+    v.W = r;
+    v.U = v.W + C * dk;
+    v.Q = v.U + C * dv;
+    v.K = v.Q + C * dk;
+    v.A = v.K + C * dk;
+    v.gam = v.A + C * C;
+    return v;
+}
+
+// Locates chunk slot -> (sequence n, first token t0, valid length len). Returns false past the end.
+__device__ __forceinline__ bool locate_chunk(const int32_t *chunk_start, const int32_t *cu, int64_t T,
+                                             int N, int C, int64_t slot, int &n, int64_t &t0, int &len) {
+    if (slot >= chunk_start[N]) return false;
+    int lo = 0, hi = N;  // largest n with chunk_start[n] <= slot
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (chunk_start[mid] <= slot) lo = mid; else hi = mid;
+    }
+    n = lo;
+    const int64_t s = cu ? (int64_t)cu[n] : (T / N) * n;
+    const int64_t e = cu ? (int64_t)cu[n + 1] : s + T / N;
+    t0 = s + (slot - chunk_start[n]) * (int64_t)C;
+    len = (int)min((int64_t)C, e - t0);
+    return true;
+}
+
+template <typename Tio>
+__global__ void __launch_bounds__(SIMT_THREADS)
+chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, const Tio *__restrict__ v,
+                        const Tio *__restrict__ z, const Tio *__restrict__ beta,
+                        const float *__restrict__ bias, const float *__restrict__ A_log, float g_min,
+                        int64_t T, int N, const int32_t *__restrict__ cu,
+                        const int32_t *__restrict__ chunk_start, int H, int dk, int dv, int C,
+                        char *__restrict__ records, size_t rec_bytes) {
+    extern __shared__ float sm[];
+    const int64_t slot = blockIdx.x;
+    const int h = blockIdx.y;
+    int n, len;
+    int64_t t0;
+    if (!locate_chunk(chunk_start, cu, T, N, C, slot, n, t0, len)) return;
+    const int tid = threadIdx.x;
+    const int PK = dk + 1, PV = dv + 1, PC = C + 1;
+    float *Ks = sm;               // [C][PK]
+    float *Qs = Ks + C * PK;      // [C][PK]
+    float *Gs = Qs + C * PK;      // [C][PK]
+    float *Vs = Gs + C * PK;      // [C][PV]
+    float *Ls = Vs + C * PV;      // [C][PC]
+    float *As = Ls + C * PC;      // [C][PC]
+    float *bet = As + C * PC;     // [C]
+
+    const float eA = A_log ? expf(A_log[h]) : 1.f;
+    for (int e = tid; e < C * dk; e += SIMT_THREADS) {
+        const int r = e / dk, c = e % dk;
+        const bool ok = r < len;
+        const int64_t idx = ((t0 + r) * H + h) * (int64_t)dk + c;
+        Ks[r * PK + c] = ok ? ld(k + idx) : 0.f;
+        Qs[r * PK + c] = ok ? ld(q + idx) : 0.f;
+        Gs[r * PK + c] = ok ? gate_logdecay(ld(z + idx), bias ? bias[h * dk + c] : 0.f, eA, g_min) : 0.f;
+    }
+    for (int e = tid; e < C * dv; e += SIMT_THREADS) {
+        const int r = e / dv, c = e % dv;
+        Vs[r * PV + c] = r < len ? ld(v + ((t0 + r) * H + h) * (int64_t)dv + c) : 0.f;
+    }
+    for (int r = tid; r < C; r += SIMT_THREADS) bet[r] = r < len ? ld(beta + (t0 + r) * H + h) : 0.f;
+    __syncthreads();
+    for (int c = tid; c < dk; c += SIMT_THREADS) {  // in-chunk cumulative log-decay (Eq. 3)
+        float acc = 0.f;
+        for (int r = 0; r < C; ++r) {
+            acc += Gs[r * PK + c];
+            Gs[r * PK + c] = acc;
+        }
+    }
+    __syncthreads();
+    for (int p = tid; p < C * C; p += SIMT_THREADS) {
+        const int r = p / C, i = p % C;
+        float sl = 0.f, sa = 0.f;
+        if (i <= r) {
+            for (int c = 0; c < dk; ++c) {
+                const float dec = expf(Gs[r * PK + c] - Gs[i * PK + c]);
+                const float ki = Ks[i * PK + c] * dec;
+                sl += Ks[r * PK + c] * ki;
+                sa += Qs[r * PK + c] * ki;
+            }
+        }
+        Ls[r * PC + i] = (i < r) ? bet[r] * sl : 0.f;
+        As[r * PC + i] = (i <= r) ? sa : 0.f;
+    }
+    __syncthreads();
+    RecordView rec = record_view(records, rec_bytes, slot, H, h, C, dk, dv);
+    for (int e = tid; e < C * C; e += SIMT_THREADS) rec.A[e] = As[(e / C) * PC + e % C];
+    for (int e = tid; e < C * dk; e += SIMT_THREADS) {
+        const int r = e / dk, c = e % dk;
+        const float G = Gs[r * PK + c], Gl = Gs[(C - 1) * PK + c];  // G is flat past len
+        rec.Q[e] = Qs[r * PK + c] * expf(G);
+        rec.K[e] = Ks[r * PK + c] * expf(Gl - G);
+        if (r == 0) rec.gam[c] = expf(Gl);
+    }
+    __syncthreads();
+    // right-hand sides of the UT transform, in place
+    for (int e = tid; e < C * dk; e += SIMT_THREADS) {
+        const int r = e / dk, c = e % dk;
+        Ks[r * PK + c] = bet[r] * Ks[r * PK + c] * expf(Gs[r * PK + c]);
+    }
+    for (int e = tid; e < C * dv; e += SIMT_THREADS) {
+        const int r = e / dv, c = e % dv;
+        Vs[r * PV + c] *= bet[r];
+    }
+    __syncthreads();
+    // forward substitution (I + L) X = RHS, one column per thread
+    for (int j = tid; j < dk + dv; j += SIMT_THREADS) {
+        float *X = j < dk ? Ks + j : Vs + (j - dk);
+        const int P = j < dk ? PK : PV;
+        for (int r = 1; r < C; ++r) {
+            float x = X[r * P];
+            for (int i = 0; i < r; ++i) x -= Ls[r * PC + i] * X[i * P];
+            X[r * P] = x;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < C * dk; e += SIMT_THREADS) rec.W[e] = Ks[(e / dk) * PK + e % dk];
+    for (int e = tid; e < C * dv; e += SIMT_THREADS) rec.U[e] = Vs[(e / dv) * PV + e % dv];
+}
+
+template <typename Tio>
+__global__ void __launch_bounds__(SIMT_THREADS)
+chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
+                        const int32_t *__restrict__ chunk_start, int H, int dk, int dv, int C,
+                        const char *__restrict__ records, size_t rec_bytes, float scale,
+                        const float *initial_state, float *final_state, Tio *__restrict__ o) {
+    extern __shared__ float sm[];
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const int j0 = blockIdx.y * SLICE;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NWARP = SIMT_THREADS / 32;
+    const int PK = dk + 1, PC = C + 1, PS = SLICE + 1;
+    float *Ws = sm;               // [C][PK]
+    float *Qs = Ws + C * PK;      // [C][PK]
+    float *Kt = Qs + C * PK;      // [C][PK]
+    float *As = Kt + C * PK;      // [C][PC]
+    float *Us = As + C * PC;      // [C][PS]
+    float *Vt = Us + C * PS;      // [C][PS]
+    float *Ss = Vt + C * PS;      // [dk][PS]
+    float *gam = Ss + dk * PS;    // [dk]
+
+    const size_t sbase = ((size_t)n * H + h) * (size_t)dk * dv;
+    for (int e = tid; e < dk * SLICE; e += SIMT_THREADS) {
+        const int c = e / SLICE, j = e % SLICE;
+        Ss[c * PS + j] = initial_state ? initial_state[sbase + (size_t)c * dv + j0 + j] : 0.f;
+    }
+    const int64_t s_tok = cu ? (int64_t)cu[n] : (T / N) * n;
+    const int64_t e_tok = cu ? (int64_t)cu[n + 1] : s_tok + T / N;
+    const int c0 = chunk_start[n], c1 = chunk_start[n + 1];
+    for (int cix = c0; cix < c1; ++cix) {
+        const int64_t t0 = s_tok + (int64_t)(cix - c0) * C;
+        const int len = (int)min((int64_t)C, e_tok - t0);
+        RecordView rec = record_view((char *)records, rec_bytes, cix, H, h, C, dk, dv);
+        __syncthreads();  // previous chunk done with the buffers
+        for (int e = tid; e < C * dk; e += SIMT_THREADS) {
+            const int r = e / dk, c = e % dk;
+            Ws[r * PK + c] = rec.W[e];
+            Qs[r * PK + c] = rec.Q[e];
+            Kt[r * PK + c] = rec.K[e];
+        }
+        for (int e = tid; e < C * C; e += SIMT_THREADS) As[(e / C) * PC + e % C] = rec.A[e];
+        for (int e = tid; e < C * SLICE; e += SIMT_THREADS) {
+            const int r = e / SLICE, j = e % SLICE;
+            Us[r * PS + j] = rec.U[r * dv + j0 + j];
+        }
+        for (int c = tid; c < dk; c += SIMT_THREADS) gam[c] = rec.gam[c];
+        __syncthreads();
+        // V~ = U - W S
+        for (int r = warp; r < C; r += NWARP) {
+            float acc = Us[r * PS + lane];
+            for (int c = 0; c < dk; ++c) acc -= Ws[r * PK + c] * Ss[c * PS + lane];
+            Vt[r * PS + lane] = acc;
+        }
+        __syncthreads();
+        // O = scale (Q^ S + A V~)
+        for (int r = warp; r < len; r += NWARP) {
+            float acc = 0.f;
+            for (int c = 0; c < dk; ++c) acc += Qs[r * PK + c] * Ss[c * PS + lane];
+            for (int i = 0; i <= r; ++i) acc += As[r * PC + i] * Vt[i * PS + lane];
+            st(o + ((t0 + r) * H + h) * (int64_t)dv + j0 + lane, scale * acc);
+        }
+        // S <- Diag(gamma^C) S + K~^T V~   (reads S only in its own column)
+        for (int c = warp; c < dk; c += NWARP) {
+            float acc = gam[c] * Ss[c * PS + lane];
+            for (int r = 0; r < len; ++r) acc += Kt[r * PK + c] * Vt[r * PS + lane];
+            // Other warps may still read S in the output pass: stage the new state in
+            // W's buffer (W is no longer read in this chunk) and copy after the barrier.
+            Ws[c * PS + lane] = acc;  // dk * PS <= C * PK floats
+        }
+        __syncthreads();
+        for (int c = warp; c < dk; c += NWARP) Ss[c * PS + lane] = Ws[c * PS + lane];
+    }
+    __syncthreads();
+    if (final_state) {
+        for (int e = tid; e < dk * SLICE; e += SIMT_THREADS) {
+            const int c = e / SLICE, j = e % SLICE;
+            final_state[sbase + (size_t)c * dv + j0 + j] = Ss[c * PS + j];
+        }
+    }
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+kda_status_t kda_launch_chunk_plan(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
+                                   cudaStream_t stream);
+
+kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
+                                   cudaStream_t stream) {
+    kda_status_t st = kda_launch_chunk_plan(a, p, ws, stream);
+    if (st != KDA_OK) return st;
+    const int C = p.C, dk = p.dk, dv = p.dv, H = p.H;
+    const int32_t *chunk_start = (const int32_t *)((char *)ws + p.off_chunk_start);
+    char *records = (char *)ws + p.off_records;
+    const size_t smem_intra =
+        sizeof(float) * ((size_t)3 * C * (dk + 1) + (size_t)C * (dv + 1) + 2 * (size_t)C * (C + 1) + C);
+    const size_t smem_chain = sizeof(float) * ((size_t)3 * C * (dk + 1) + (size_t)C * (C + 1) +
+                                               2 * (size_t)C * (SLICE + 1) + (size_t)dk * (SLICE + 1) + dk);
+    const bool b16 = a->dtype == KDA_BF16;
+    if (p.max_chunks > 0 && a->T > 0) {
+        dim3 grid((unsigned)p.max_chunks, (unsigned)H);
+        if (b16) {
+            cudaFuncSetAttribute(chunk_intra_simt_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_intra);
+            chunk_intra_simt_kernel<bf16><<<grid, SIMT_THREADS, smem_intra, stream>>>(
+                (const bf16 *)a->q, (const bf16 *)a->k, (const bf16 *)a->v, (const bf16 *)a->z,
+                (const bf16 *)a->beta, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
+                chunk_start, H, dk, dv, C, records, p.record_bytes);
+        } else {
+            cudaFuncSetAttribute(chunk_intra_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_intra);
+            chunk_intra_simt_kernel<float><<<grid, SIMT_THREADS, smem_intra, stream>>>(
+                (const float *)a->q, (const float *)a->k, (const float *)a->v, (const float *)a->z,
+                (const float *)a->beta, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
+                chunk_start, H, dk, dv, C, records, p.record_bytes);
+        }
+        if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    dim3 grid2((unsigned)(a->N * H), (unsigned)(dv / SLICE));
+    if (b16) {
+        cudaFuncSetAttribute(chunk_chain_simt_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_chain);
+        chunk_chain_simt_kernel<bf16><<<grid2, SIMT_THREADS, smem_chain, stream>>>(
+            a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, p.record_bytes,
+            a->scale, a->initial_state, a->final_state, (bf16 *)a->o);
+    } else {
+        cudaFuncSetAttribute(chunk_chain_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_chain);
+        chunk_chain_simt_kernel<float><<<grid2, SIMT_THREADS, smem_chain, stream>>>(
+            a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, p.record_bytes,
+            a->scale, a->initial_state, a->final_state, (float *)a->o);
+    }
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}

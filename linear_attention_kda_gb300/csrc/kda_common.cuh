@@ -1,0 +1,46 @@
+// Device helpers shared by the libkda kernels (sm_103a).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+using bf16 = __nv_bfloat16;
+
+template <typename T> __device__ __forceinline__ float ld(const T *p);
+template <> __device__ __forceinline__ float ld<float>(const float *p) { return *p; }
+template <> __device__ __forceinline__ float ld<bf16>(const bf16 *p) { return __bfloat162float(*p); }
+
+template <typename T> __device__ __forceinline__ void st(T *p, float x);
+template <> __device__ __forceinline__ void st<float>(float *p, float x) { *p = x; }
+template <> __device__ __forceinline__ void st<bf16>(bf16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Eq. 5 of the Kimi K3 report with the bias inside the logit:
+// g = g_min * Sigmoid(exp(A) * (z + b)).  expA = exp(A_log[h]) precomputed.
+__device__ __forceinline__ float gate_logdecay(float z, float b, float expA, float g_min) {
+    const float x = expA * (z + b);
+    return g_min / (1.0f + expf(-x));
+}
+
+// First device-detected error wins; later ones are dropped.
+__device__ __forceinline__ void set_error(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Sequence n containing token t: largest n with cu[n] <= t (cu has N + 1 entries).
+__device__ __forceinline__ int find_seq(const int32_t *cu, int N, int64_t t) {
+    int lo = 0, hi = N;  // invariant: cu[lo] <= t, answer in [lo, hi)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)cu[mid] <= t) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+}  // namespace kda
+
+// Host-side helpers (defined in kda_api.cu).
+int *kda_device_error_ptr();  // device address of this device's error word

@@ -1,0 +1,26 @@
+// Internal launchers behind the C ABI (host side).  Arguments are validated by
+// kda_api.cu before any of these is called.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "../../include/kda.h"
+
+kda_status_t kda_launch_gate(const kda_gate_args *a, cudaStream_t stream);
+kda_status_t kda_launch_decode(const kda_step_args *a, cudaStream_t stream);
+
+// Chunked prefill.  Workspace layout is owned by kda_chunk_plan.cu.
+struct kda_chunk_plan {
+    int64_t T, N;
+    int H, dk, dv, C;
+    int64_t max_chunks;    // upper bound on chunks over all sequences
+    int path;              // 0 = fp32 CUDA-core path, 1 = tensor-core path
+    size_t off_chunk_start;  // int32 [N + 1]: first chunk slot of each sequence
+    size_t off_records;      // per (chunk slot, head) intra-chunk records
+    size_t record_bytes;
+    size_t total_bytes;
+};
+
+bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_t dtype, int C,
+                         kda_chunk_plan *plan);
+kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
+                                   cudaStream_t stream);

@@ -1,0 +1,199 @@
+"""Thin ctypes binding of libkda (include/kda.h).
+
+Argument marshalling only: every step of KDA runs inside libkda's CUDA
+kernels.  PyTorch supplies device memory (outputs and the prefill workspace
+are allocated here with torch) and the current stream.  If libkda is not
+built or cannot be loaded, every call raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
+
+KDA_F32, KDA_BF16 = 0, 1
+_STATUS = {
+    0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
+    3: "KDA_ERR_UNSUPPORTED_DTYPE", 4: "KDA_ERR_MISALIGNED", 5: "KDA_ERR_WORKSPACE",
+    6: "KDA_ERR_CUDA", 7: "KDA_ERR_BAD_SEQLENS", 8: "KDA_ERR_BAD_STATE_INDEX",
+    9: "KDA_ERR_NO_DEVICE", 10: "KDA_ERR_DEVICE_TIMEOUT",
+}
+EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step",
+            "kda_status_string", "kda_get_device_error", "kda_abi_version"]
+
+_vp = ctypes.c_void_p
+_i64, _i32, _f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+
+
+class GateArgs(ctypes.Structure):
+    _fields_ = [("T", _i64), ("N", _i64), ("H", _i32), ("dk", _i32), ("dtype", ctypes.c_int),
+                ("z", _vp), ("dt_bias", _vp), ("A_log", _vp), ("g_min", _f32),
+                ("chunk_size", _i32), ("cu_seqlens", _vp), ("out", _vp)]
+
+
+class ChunkArgs(ctypes.Structure):
+    _fields_ = [("T", _i64), ("N", _i64), ("H", _i32), ("dk", _i32), ("dv", _i32),
+                ("dtype", ctypes.c_int), ("q", _vp), ("k", _vp), ("z", _vp), ("v", _vp),
+                ("beta", _vp), ("dt_bias", _vp), ("A_log", _vp), ("g_min", _f32), ("scale", _f32),
+                ("cu_seqlens", _vp), ("cu_seqlens_host", _vp), ("initial_state", _vp),
+                ("final_state", _vp), ("o", _vp), ("chunk_size", _i32)]
+
+
+class StepArgs(ctypes.Structure):
+    _fields_ = [("N", _i64), ("H", _i32), ("dk", _i32), ("dv", _i32), ("dtype", ctypes.c_int),
+                ("q", _vp), ("k", _vp), ("z", _vp), ("v", _vp), ("beta", _vp),
+                ("dt_bias", _vp), ("A_log", _vp), ("g_min", _f32), ("scale", _f32),
+                ("state", _vp), ("state_indices", _vp), ("num_slots", _i64), ("o", _vp)]
+
+
+class KDAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {_STATUS.get(int(code), code)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: Optional[str] = None):
+    """Loads libkda.so (raises if missing: build it with linear_attention_kda_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libkda is not built ({p} missing); run "
+                               "`python -m linear_attention_kda_gb300.build`")
+        L = ctypes.CDLL(p)
+        L.kda_gate.argtypes = [ctypes.POINTER(GateArgs), _vp]
+        L.kda_gate.restype = ctypes.c_int
+        L.kda_chunk_fwd.argtypes = [ctypes.POINTER(ChunkArgs), _vp, ctypes.c_size_t, _vp]
+        L.kda_chunk_fwd.restype = ctypes.c_int
+        L.kda_chunk_fwd_workspace_size.argtypes = [_i64, _i64, _i32, _i32, _i32, ctypes.c_int, _i32, _vp]
+        L.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
+        L.kda_recurrent_step.argtypes = [ctypes.POINTER(StepArgs), _vp]
+        L.kda_recurrent_step.restype = ctypes.c_int
+        L.kda_status_string.argtypes = [ctypes.c_int]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_get_device_error.argtypes = [_vp]
+        L.kda_get_device_error.restype = ctypes.c_int
+        L.kda_abi_version.restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(t: torch.Tensor):
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise KDAError(code, where)
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def gate(z: torch.Tensor, dt_bias=None, A_log=None, g_min: float = -5.0, chunk_size: int = 0,
+         cu_seqlens: Optional[torch.Tensor] = None, n_seq: int = 1, out=None) -> torch.Tensor:
+    """kda_gate: g = g_min * sigmoid(exp(A_log) (z + dt_bias)) (Eq. 5), or its chunk-local cumsum."""
+    L = load_library()
+    T, H, dk = z.shape
+    _contig(z, dt_bias, A_log, cu_seqlens)
+    if out is None:
+        out = torch.empty((T, H, dk), dtype=torch.float32, device=z.device)
+    a = GateArgs(T=T, N=(cu_seqlens.numel() - 1) if cu_seqlens is not None else n_seq, H=H, dk=dk,
+                 dtype=_dtype_code(z), z=_ptr(z), dt_bias=_ptr(dt_bias), A_log=_ptr(A_log),
+                 g_min=g_min, chunk_size=chunk_size, cu_seqlens=_ptr(cu_seqlens), out=_ptr(out))
+    _check(L.kda_gate(ctypes.byref(a), _stream(z)), "kda_gate")
+    return out
+
+
+def chunk_fwd_workspace_size(T, N, H, dk, dv, dtype: torch.dtype, chunk_size=64, cu_seqlens_host=None):
+    L = load_library()
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    hp = None
+    if cu_seqlens_host is not None:
+        hp = cu_seqlens_host.data_ptr()
+    return int(L.kda_chunk_fwd_workspace_size(T, N, H, dk, dv, code, chunk_size, hp))
+
+
+def chunk_fwd(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0, scale: float = 1.0,
+              cu_seqlens: Optional[torch.Tensor] = None, cu_seqlens_host: Optional[torch.Tensor] = None,
+              n_seq: int = 1, initial_state: Optional[torch.Tensor] = None,
+              output_final_state: bool = False, final_state: Optional[torch.Tensor] = None,
+              chunk_size: int = 64, workspace: Optional[torch.Tensor] = None,
+              out: Optional[torch.Tensor] = None):
+    """kda_chunk_fwd: chunkwise KDA prefill (Eq. 1 evaluated as Eq. 3-4).  Returns (o, final_state)."""
+    L = load_library()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    _contig(q, k, v, z, beta, dt_bias, A_log, cu_seqlens, initial_state)
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else n_seq
+    if cu_seqlens_host is not None:
+        cu_seqlens_host = cu_seqlens_host.to(dtype=torch.int32, device="cpu").contiguous()
+    o = out if out is not None else torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    fs = final_state
+    if fs is None and output_final_state:
+        fs = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    need = chunk_fwd_workspace_size(T, N, H, dk, dv, q.dtype, chunk_size, cu_seqlens_host)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
+    a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=_dtype_code(q), q=_ptr(q), k=_ptr(k), z=_ptr(z),
+                  v=_ptr(v), beta=_ptr(beta), dt_bias=_ptr(dt_bias), A_log=_ptr(A_log), g_min=g_min,
+                  scale=scale, cu_seqlens=_ptr(cu_seqlens),
+                  cu_seqlens_host=None if cu_seqlens_host is None else cu_seqlens_host.data_ptr(),
+                  initial_state=_ptr(initial_state), final_state=_ptr(fs), o=_ptr(o),
+                  chunk_size=chunk_size)
+    _check(L.kda_chunk_fwd(ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(q)),
+           "kda_chunk_fwd")
+    return o, fs
+
+
+def recurrent_step(q, k, v, z, beta, dt_bias, A_log, state, *, g_min: float = -5.0, scale: float = 1.0,
+                   state_indices: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None):
+    """kda_recurrent_step: one decode token per sequence; `state` is updated in place.  Returns o."""
+    L = load_library()
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    _contig(q, k, v, z, beta, dt_bias, A_log, state, state_indices)
+    o = out if out is not None else torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    a = StepArgs(N=N, H=H, dk=dk, dv=dv, dtype=_dtype_code(q), q=_ptr(q), k=_ptr(k), z=_ptr(z),
+                 v=_ptr(v), beta=_ptr(beta), dt_bias=_ptr(dt_bias), A_log=_ptr(A_log), g_min=g_min,
+                 scale=scale, state=_ptr(state), state_indices=_ptr(state_indices),
+                 num_slots=state.shape[0], o=_ptr(o))
+    _check(L.kda_recurrent_step(ctypes.byref(a), _stream(q)), "kda_recurrent_step")
+    return o
+
+
+def get_device_error(device=None) -> int:
+    """Waits for the current stream and returns (and clears) the device error code (0 = none)."""
+    L = load_library()
+    return int(L.kda_get_device_error(torch.cuda.current_stream(device).cuda_stream))
+
+
+def status_string(code: int) -> str:
+    return load_library().kda_status_string(int(code)).decode()

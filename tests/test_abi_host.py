@@ -1,0 +1,202 @@
+"""Host-only checks of the C ABI (no GPU needed, no kernel launched).
+
+* libkda.so loads and exports every function include/kda.h declares.
+* The ctypes mirrors of the argument structs match the C layout (checked by
+  compiling a small C program against include/kda.h with gcc).
+* Host validation rejects bad arguments with the documented status before any
+  launch: only cases that fail validation are sent through the ABI here, so no
+  fake pointer ever reaches a kernel.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from linear_attention_kda_gb300 import build as kbuild, kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kda.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(kda_[a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"kda_gate", "kda_chunk_fwd", "kda_recurrent_step"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"libkda does not export {n}"
+    assert set(kda.EXPORTED) <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", kbuild.LIB_PATH], capture_output=True, text=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}\b", out), f"{n} not a defined text symbol"
+
+
+def test_abi_version_and_strings(lib):
+    assert lib.kda_abi_version() == 1
+    for code, name in kda._STATUS.items():
+        s = lib.kda_status_string(code).decode()
+        assert s and s != "unknown status", name
+    assert lib.kda_status_string(999).decode() == "unknown status"
+
+
+_LAYOUT_C = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "kda.h"
+#define F(S, f) printf(#S " " #f " %zu\n", offsetof(S, f));
+int main(void) {
+  printf("kda_gate_args sizeof %zu\n", sizeof(kda_gate_args));
+  printf("kda_chunk_args sizeof %zu\n", sizeof(kda_chunk_args));
+  printf("kda_step_args sizeof %zu\n", sizeof(kda_step_args));
+  %FIELDS%
+  return 0;
+}
+"""
+
+
+def test_struct_layout_matches_header(tmp_path):
+    fields = []
+    for cname, cls in (("kda_gate_args", kda.GateArgs), ("kda_chunk_args", kda.ChunkArgs),
+                       ("kda_step_args", kda.StepArgs)):
+        for f, _ in cls._fields_:
+            fields.append(f"F({cname}, {f})")
+    src = tmp_path / "layout.c"
+    src.write_text(_LAYOUT_C.replace("%FIELDS%", "\n  ".join(fields)))
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {}
+    for ln in lines:
+        if ln.strip():
+            s, f, v = ln.split()
+            got[(s, f)] = int(v)
+    for cname, cls in (("kda_gate_args", kda.GateArgs), ("kda_chunk_args", kda.ChunkArgs),
+                       ("kda_step_args", kda.StepArgs)):
+        assert got[(cname, "sizeof")] == ctypes.sizeof(cls), cname
+        for f, _ in cls._fields_:
+            assert got[(cname, f)] == getattr(cls, f).offset, (cname, f)
+
+
+FAKE = 1 << 20  # 16-byte aligned fake device address; never dereferenced (validation fails first)
+
+
+def _chunk(**kw):
+    base = dict(T=128, N=1, H=2, dk=128, dv=128, dtype=kda.KDA_BF16, q=FAKE, k=FAKE + 1024,
+                z=FAKE + 2048, v=FAKE + 4096, beta=FAKE + 8192, dt_bias=None, A_log=None,
+                g_min=-5.0, scale=1.0, cu_seqlens=None, cu_seqlens_host=None, initial_state=None,
+                final_state=None, o=FAKE + 16384, chunk_size=64)
+    base.update(kw)
+    return kda.ChunkArgs(**base)
+
+
+def _call_chunk(lib, a, ws=FAKE, ws_bytes=1 << 40):
+    return lib.kda_chunk_fwd(ctypes.byref(a), ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dk=96, dv=96), 2),
+    (dict(dk=128, dv=64), 2),
+    (dict(chunk_size=32), 2),
+    (dict(dtype=7), 3),
+    (dict(N=0), 1),
+    (dict(T=-1), 1),
+    (dict(H=0), 1),
+    (dict(g_min=0.0), 1),
+    (dict(g_min=float("nan")), 1),
+    (dict(scale=float("inf")), 1),
+    (dict(T=130, N=4), 1),          # equal-length split must divide T
+    (dict(q=None), 1),
+    (dict(o=FAKE), 1),              # o aliases q
+    (dict(q=FAKE + 8), 4),
+    (dict(o=FAKE + 16392), 4),
+    (dict(initial_state=FAKE + 4), 4),
+])
+def test_chunk_fwd_rejects(lib, kw, code):
+    assert _call_chunk(lib, _chunk(**kw)) == code
+
+
+def test_chunk_fwd_workspace_checks(lib):
+    a = _chunk()
+    need = lib.kda_chunk_fwd_workspace_size(128, 1, 2, 128, 128, kda.KDA_BF16, 64, None)
+    assert need > 0
+    assert _call_chunk(lib, a, ws=None) == 5
+    assert _call_chunk(lib, a, ws_bytes=need - 1) == 5
+    assert _call_chunk(lib, a, ws=FAKE + 16, ws_bytes=need) == 4
+    assert lib.kda_chunk_fwd_workspace_size(128, 1, 2, 96, 96, kda.KDA_BF16, 64, None) == 0
+    assert lib.kda_chunk_fwd_workspace_size(128, 0, 2, 128, 128, kda.KDA_BF16, 64, None) == 0
+
+
+def test_chunk_fwd_host_seqlens_validated(lib):
+    cu = (ctypes.c_int32 * 3)(0, 100, 90)
+    a = _chunk(T=90, N=2, cu_seqlens=FAKE + 32768, cu_seqlens_host=ctypes.addressof(cu))
+    assert _call_chunk(lib, a) == 1
+    cu2 = (ctypes.c_int32 * 3)(0, 50, 128)
+    a = _chunk(T=100, N=2, cu_seqlens=FAKE + 32768, cu_seqlens_host=ctypes.addressof(cu2))
+    assert _call_chunk(lib, a) == 1
+
+
+def _step(**kw):
+    base = dict(N=4, H=2, dk=128, dv=128, dtype=kda.KDA_BF16, q=FAKE, k=FAKE + 1024, z=FAKE + 2048,
+                v=FAKE + 4096, beta=FAKE + 8192, dt_bias=None, A_log=None, g_min=-5.0, scale=1.0,
+                state=FAKE + 65536, state_indices=None, num_slots=0, o=FAKE + 16384)
+    base.update(kw)
+    return kda.StepArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dk=32, dv=32), 2),
+    (dict(dtype=5), 3),
+    (dict(H=0), 1),
+    (dict(state=None), 1),
+    (dict(num_slots=2), 1),        # fewer slots than sequences without an index map
+    (dict(state=FAKE + 65544), 4),
+    (dict(beta=FAKE + 8193), 4),
+    (dict(g_min=1.0), 1),
+])
+def test_recurrent_step_rejects(lib, kw, code):
+    assert lib.kda_recurrent_step(ctypes.byref(_step(**kw)), None) == code
+
+
+def test_gate_rejects(lib):
+    a = kda.GateArgs(T=8, N=1, H=1, dk=16, dtype=kda.KDA_F32, z=FAKE, dt_bias=None, A_log=None,
+                     g_min=-5.0, chunk_size=0, cu_seqlens=None, out=FAKE + 4096)
+    a.g_min = 0.5
+    assert lib.kda_gate(ctypes.byref(a), None) == 1
+    a.g_min = -5.0
+    a.z = FAKE + 2
+    assert lib.kda_gate(ctypes.byref(a), None) == 4
+    a.z = FAKE
+    a.chunk_size = 4
+    a.N = 3  # 8 tokens do not split into 3 equal sequences
+    assert lib.kda_gate(ctypes.byref(a), None) == 1
+    a.chunk_size = 1000
+    assert lib.kda_gate(ctypes.byref(a), None) == 1
+
+
+def test_empty_inputs_are_noops(lib):
+    # T = 0 gate / N = 0 decode return KDA_OK before touching any pointer or the device
+    a = kda.GateArgs(T=0, N=1, H=1, dk=16, dtype=kda.KDA_F32, z=None, dt_bias=None, A_log=None,
+                     g_min=-5.0, chunk_size=0, cu_seqlens=None, out=None)
+    assert lib.kda_gate(ctypes.byref(a), None) == 0
+    assert lib.kda_recurrent_step(ctypes.byref(_step(N=0, q=None)), None) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
+def test_valid_args_stop_at_device_check_without_gpu(lib):
+    # Passes validation, then finds no sm_103 device: nothing is launched.
+    assert _call_chunk(lib, _chunk()) == 9
+    assert lib.kda_recurrent_step(ctypes.byref(_step()), None) == 9

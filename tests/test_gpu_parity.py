@@ -1,0 +1,245 @@
+"""GPU parity of libkda against the fp64 oracle (through the C ABI).
+
+Tolerances (relative Frobenius error per (sequence, head), on outputs and
+final states): 1e-2 for bf16 I/O with fp32 accumulation, 1e-4 for the fp32
+path.  Inputs are the seeded synthetic workloads (same distributions as the
+benchmark), shortened where the oracle must run on every head.
+"""
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_kda_gb300 import kda, synthetic as syn
+from oracle import c_ref, numpy_ref as R
+from tests.gpu_util import TOL_BF16, TOL_F32, compare_prefill, oracle_prefill, rel_err, run_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _dev(cuda_ok):
+    torch.cuda.set_device(0)
+    kda.load_library()
+
+
+def _varlen(w, lengths, seed, s0_std=None):
+    d = syn.make_prefill(w, seed, T_override=1)
+    T = sum(lengths)
+    q, k, v, beta, z = syn.make_tokens(T, w.H, w.d, w.d, w.dtype, seed, z_std=w.z_std)
+    d.update(q=q, k=k, v=v, beta=beta, z=z, lengths=lengths, cu_seqlens=syn.cu_seqlens_of(lengths))
+    std = w.s0_std if s0_std is None else s0_std
+    d["initial_state"] = syn.make_state(len(lengths), w.H, w.d, w.d, std, seed) if std > 0 else None
+    return d
+
+
+# ----------------------------------------------------------------------------- gate
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gate_elementwise(dtype):
+    w = syn.PREFILL_4K
+    d = syn.make_prefill(syn.Workload("g", H=3, d=128, dtype=dtype, seq_len=100, z_std=3.0,
+                                      b_range=1.0, alog_std=0.5), seed=3)
+    g = kda.gate(d["z"].cuda(), d["dt_bias"].cuda(), d["A_log"].cuda(), g_min=-5.0).cpu().numpy()
+    ref = R.gate(d["z"].float().numpy(), d["dt_bias"].numpy()[None], d["A_log"].numpy()[None, :, None])
+    np.testing.assert_allclose(g, ref, rtol=1e-5, atol=1e-6)
+    assert np.all(g >= -5.0) and np.all(g <= 0.0)
+    assert w.H == 32
+
+
+def test_gate_chunk_cumsum_varlen():
+    lengths = [5, 0, 64, 65, 130, 1, 200]
+    w = syn.Workload("g", H=2, d=64, dtype="bf16", seq_len=None, z_std=1.5, b_range=1.0, alog_std=0.25)
+    T = sum(lengths)
+    q, k, v, beta, z = syn.make_tokens(T, 2, 64, 64, "bf16", 9, z_std=1.5)
+    b, a = syn.make_head_params(2, 64, 9, b_range=1.0, alog_std=0.25)
+    cu = syn.cu_seqlens_of(lengths)
+    G = kda.gate(z.cuda(), b.cuda(), a.cuda(), chunk_size=64, cu_seqlens=cu.cuda()).cpu().numpy()
+    assert kda.get_device_error() == 0
+    g = R.gate(z.float().numpy(), b.numpy()[None], a.numpy()[None, :, None])
+    ref = np.zeros_like(g)
+    for n in range(len(lengths)):
+        for c0 in range(int(cu[n]), int(cu[n + 1]), 64):
+            c1 = min(c0 + 64, int(cu[n + 1]))
+            ref[c0:c1] = np.cumsum(g[c0:c1], axis=0)
+    np.testing.assert_allclose(G, ref, rtol=1e-5, atol=2e-4)
+    assert w.d == 64
+
+
+def test_gate_bad_seqlens_sets_device_error():
+    z = torch.zeros((10, 1, 16), dtype=torch.float32, device="cuda")
+    cu = torch.tensor([0, 7, 3, 10], dtype=torch.int32, device="cuda")  # not monotone
+    kda.gate(z, chunk_size=4, cu_seqlens=cu)
+    assert kda.get_device_error() == 7
+    assert kda.get_device_error() == 0  # cleared
+
+
+# ----------------------------------------------------------------------------- decode
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_recurrent_step_matches_oracle(D, dtype):
+    w = syn.Workload("dec", H=3, d=D, dtype=dtype, n_seq=5, seq_len=1, z_std=1.5, b_range=1.0,
+                     alog_std=0.25, s0_std=0.02, decode_steps=6)
+    d = syn.make_decode(w, seed=11)
+    N, H, S = 5, 3, 6
+    # slots permuted, plus one spare slot that must stay untouched
+    slots = torch.tensor([3, 0, 5, 1, 2], dtype=torch.int32)
+    pool = torch.randn((6, H, D, D)) * 0.02
+    pool[slots.long()] = d["state"]
+    pool_gpu = pool.cuda()
+    outs = []
+    for s in range(S):
+        args = [d[n][s].contiguous().cuda() for n in ("q", "k", "v", "z", "beta")]
+        outs.append(kda.recurrent_step(*args, d["dt_bias"].cuda(), d["A_log"].cuda(), pool_gpu,
+                                       state_indices=slots.cuda()).float().cpu())
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    seq = lambda n: torch.stack([d[n][s] for s in range(S)], 1).reshape(N * S, H, *d[n].shape[3:])  # noqa: E731
+    cu = torch.arange(0, N * S + 1, S, dtype=torch.int32)
+    res, _ = c_ref.forward(seq("q"), seq("k"), seq("v"), seq("z"), seq("beta"), d["dt_bias"], d["A_log"],
+                           cu, S0=d["state"])
+    tol = TOL_F32 if dtype == "f32" else TOL_BF16
+    pool_out = pool_gpu.cpu()
+    for n in range(N):
+        for h in range(H):
+            o_ref, S_ref = res[(n, h)]
+            o_gpu = torch.stack([outs[s][n, h] for s in range(S)]).numpy()
+            assert rel_err(o_gpu, o_ref) <= tol
+            assert rel_err(pool_out[int(slots[n]), h].numpy(), S_ref) <= tol
+    assert torch.equal(pool_out[4], pool[4])  # unused slot untouched
+
+
+def test_recurrent_step_bad_index_reports_and_skips():
+    D, H = 64, 1
+    st = torch.zeros((2, H, D, D), device="cuda")
+    x = torch.zeros((1, H, D), device="cuda")
+    b = torch.zeros((1, H), device="cuda")
+    kda.recurrent_step(x, x, x, x, b, None, None, st, state_indices=torch.tensor([5], dtype=torch.int32, device="cuda"))
+    assert kda.get_device_error() == 8
+    assert torch.count_nonzero(st) == 0
+
+
+# ----------------------------------------------------------------------------- prefill
+
+def test_tiny_f32_workload():
+    """B=1, H=2, T=256, d=64, fp32, zero initial state: <= 1e-4 against the fp64 recurrence."""
+    d = syn.make_prefill(syn.TINY_F32, seed=0)
+    o, fs = run_prefill(d)
+    compare_prefill(d, o, fs, oracle_prefill(d), TOL_F32)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 128), ("bf16", 64), ("f32", 64)])
+def test_varlen_ragged_with_state(dtype, D):
+    """Ragged lengths (empty, 1, chunk +-1, multi-chunk tails) with a random initial state."""
+    w = syn.Workload("v", H=3, d=D, dtype=dtype, seq_len=None, z_std=1.5, b_range=1.0,
+                     alog_std=0.25, s0_std=0.02)
+    d = _varlen(w, [1, 63, 64, 0, 65, 130, 200, 7], seed=21)
+    o, fs = run_prefill(d)
+    compare_prefill(d, o, fs, oracle_prefill(d), TOL_F32 if dtype == "f32" else TOL_BF16)
+
+
+def test_prefill_4k_workload_full():
+    """The single-sequence bf16 workload at full size (T=4096, H=32, d=128), every head."""
+    d = syn.make_prefill(syn.PREFILL_4K, seed=1)
+    o, fs = run_prefill(d)
+    worst = compare_prefill(d, o, fs, oracle_prefill(d), TOL_BF16)
+    assert worst < TOL_BF16
+
+
+def test_equal_length_batch_without_cu_seqlens():
+    w = syn.Workload("b", H=2, d=128, dtype="bf16", n_seq=3, seq_len=100, z_std=1.5, b_range=1.0,
+                     alog_std=0.25, s0_std=0.02)
+    d = syn.make_prefill(w, seed=5)
+    dev = "cuda"
+    o, fs = kda.chunk_fwd(*(d[n].to(dev) for n in ("q", "k", "v", "z", "beta")), d["dt_bias"].to(dev),
+                          d["A_log"].to(dev), n_seq=3, initial_state=d["initial_state"].to(dev),
+                          output_final_state=True)
+    compare_prefill(d, o.float().cpu(), fs.cpu(), oracle_prefill(d), TOL_BF16)
+
+
+def test_final_state_aliases_initial_state():
+    w = syn.Workload("a", H=2, d=128, dtype="bf16", seq_len=None, z_std=1.5, b_range=1.0,
+                     alog_std=0.25, s0_std=0.02)
+    d = _varlen(w, [70, 3, 128], seed=6)
+    st = d["initial_state"].cuda().contiguous()
+    dev = "cuda"
+    o, fs = kda.chunk_fwd(*(d[n].to(dev) for n in ("q", "k", "v", "z", "beta")), d["dt_bias"].to(dev),
+                          d["A_log"].to(dev), cu_seqlens=d["cu_seqlens"].to(dev), initial_state=st,
+                          final_state=st)
+    torch.cuda.synchronize()
+    compare_prefill(d, o.float().cpu(), st.cpu(), oracle_prefill(d), TOL_BF16)
+
+
+@pytest.mark.parametrize("split", [1, 64, 100, 129])
+def test_split_resume_matches_one_pass(split):
+    """Final state of a prefix passed as the initial state of the rest equals one pass (prefix reuse)."""
+    w = syn.Workload("s", H=2, d=128, dtype="bf16", seq_len=300, z_std=1.5, b_range=1.0,
+                     alog_std=0.25, s0_std=0.02)
+    d = syn.make_prefill(w, seed=8)
+    o_full, fs_full = run_prefill(d)
+    d1 = dict(d, cu_seqlens=torch.tensor([0, split], dtype=torch.int32))
+    d2 = dict(d, cu_seqlens=torch.tensor([0, 300 - split], dtype=torch.int32))
+    for n in ("q", "k", "v", "z", "beta"):
+        d1[n] = d[n][:split].contiguous()
+        d2[n] = d[n][split:].contiguous()
+    o1, fs1 = run_prefill(d1)
+    d2["initial_state"] = fs1
+    o2, fs2 = run_prefill(d2)
+    o_cat = torch.cat([o1, o2])
+    for h in range(2):
+        assert rel_err(o_cat[:, h].numpy(), o_full[:, h].numpy()) <= TOL_BF16
+        assert rel_err(fs2[0, h].numpy(), fs_full[0, h].numpy()) <= TOL_BF16
+    compare_prefill(d, o_cat, fs2, oracle_prefill(d), TOL_BF16)
+
+
+def test_zero_state_identity_gate_limits():
+    """z -> -inf gives g = 0 (alpha = 1); with beta = 0 the state is carried unchanged."""
+    T, H, D = 130, 2, 128
+    q, k, v, beta, z = syn.make_tokens(T, H, D, D, "bf16", 12, z_std=1.0)
+    z = torch.full_like(z, -1e4)
+    beta = torch.zeros_like(beta)
+    S0 = torch.randn((1, H, D, D)) * 0.1
+    dev = "cuda"
+    o, fs = kda.chunk_fwd(q.to(dev), k.to(dev), v.to(dev), z.to(dev), beta.to(dev), None, None,
+                          initial_state=S0.to(dev), output_final_state=True)
+    torch.cuda.synchronize()
+    assert rel_err(fs.cpu().numpy(), S0.numpy()) <= 1e-6
+    o_ref = torch.einsum("thc,hcj->thj", q.float(), S0[0])
+    assert rel_err(o.float().cpu().numpy(), o_ref.numpy()) <= TOL_BF16
+
+
+def test_bad_cu_seqlens_reports_device_error():
+    w = syn.Workload("e", H=1, d=64, dtype="f32", seq_len=64)
+    d = syn.make_prefill(w, seed=1)
+    dev = "cuda"
+    cu = torch.tensor([0, 40, 30, 64], dtype=torch.int32, device=dev)
+    kda.chunk_fwd(*(d[n].to(dev) for n in ("q", "k", "v", "z", "beta")), None, None, cu_seqlens=cu,
+                  output_final_state=True)
+    assert kda.get_device_error() == 7
+
+
+def test_decode_equals_prefill_continuation():
+    """512 in-place decode steps equal kda_chunk_fwd over the same tokens from the same state
+    (decode workload, reduced to 8 sequences x 4 heads x 96 steps)."""
+    w = syn.DECODE_256
+    N, H, S = 8, 4, 96
+    d = syn.make_decode(w, seed=4, n_seq=N, steps=S)
+    hs = slice(0, H)
+    st = d["state"][:, hs].contiguous().cuda()
+    S0 = d["state"][:, hs].contiguous()
+    b, a = d["dt_bias"][hs].contiguous().cuda(), d["A_log"][hs].contiguous().cuda()
+    outs = []
+    for s in range(S):
+        args = [d[n][s, :, hs].contiguous().cuda() for n in ("q", "k", "v", "z", "beta")]
+        outs.append(kda.recurrent_step(*args, b, a, st))
+    o_dec = torch.stack(outs, 1).float().cpu()  # [N, S, H, D]
+    seq = lambda n: torch.stack([d[n][s, :, hs] for s in range(S)], 1).reshape(N * S, H, *d[n].shape[3:]).contiguous()  # noqa: E731
+    cu = torch.arange(0, N * S + 1, S, dtype=torch.int32)
+    o_pf, fs_pf = kda.chunk_fwd(*(seq(n).cuda() for n in ("q", "k", "v", "z", "beta")), b, a,
+                                cu_seqlens=cu.cuda(), initial_state=S0.cuda(), output_final_state=True)
+    torch.cuda.synchronize()
+    o_pf = o_pf.float().cpu().reshape(N, S, H, -1)
+    for n in range(N):
+        for h in range(H):
+            assert rel_err(o_dec[n, :, h].numpy(), o_pf[n, :, h].numpy()) <= TOL_BF16
+            assert rel_err(st[n, h].cpu().numpy(), fs_pf[n, h].cpu().numpy()) <= TOL_BF16
