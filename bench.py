@@ -1,0 +1,427 @@
+"""KDA benchmark: chunked prefill (tokens/s, TFLOP/s) and decode (GB/s) on one GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one kda_chunk_fwd pass over the single-sequence bf16 prefill
+workload (B=1, H=32, T=4096, d_k=d_v=128, C=64, fp32 state, final state
+written), inputs resident in HBM.  L2 is flushed (a 512 MiB write) before
+every timed step; each step is timed alone with CUDA events on the launching
+stream, and per-kernel times come from events the library records between
+its launches.  The decode numbers come from the decode workload (256
+sequences x 32 heads, 512 in-place steps) in the same run.  Under torchrun
+each rank runs its own copy of the workload (sequences are independent: no
+data-path collective); value = tokens of all ranks / max time over ranks.
+
+--impl reference times the fp64 CPU oracle (test infrastructure) on the same
+workload, on the host cores, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from linear_attention_kda_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "KDA chunked prefill tokens/s and TFLOP/s (% BF16 TC peak); decode GB/s (% HBM)"
+WORKLOAD = syn.PREFILL_4K
+DECODE = syn.DECODE_256
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def chunk_lengths(lengths, C):
+    out = []
+    for L in lengths:
+        full, tail = divmod(int(L), C)
+        out += [C] * full + ([tail] if tail else [])
+    return out
+
+
+def prefill_flops(lengths, H, dk, dv, C=64):
+    """Algorithmic FLOPs (2 per MAC, causal shapes) of the chunked form, split by kernel role.
+
+    intra (UT transform, A):  2 dk c(c+1) + dk c(c-1) + dv c(c+1) + c^3/3
+    inter (state, output):    6 c dk dv + dv c(c+1)
+    """
+    intra = inter = dense = 0.0
+    for c in chunk_lengths(lengths, C):
+        intra += 2 * dk * c * (c + 1) + dk * c * (c - 1) + dv * c * (c + 1) + c ** 3 / 3.0
+        inter += 6 * c * dk * dv + dv * c * (c + 1)
+        dense += 6 * C * dk * dv + 3 * (2 * C * C * dk) + 2 * (2 * C * C * dv) + C ** 3 / 3.0
+    return {"intra": intra * H, "inter": inter * H, "total": (intra + inter) * H, "dense_tile": dense * H}
+
+
+def prefill_bytes(T, N, H, dk, dv, io_bytes, with_s0, with_sT):
+    """Algorithmic HBM bytes: read q, k, z [dk], v [dv], beta; write o [dv]; states fp32."""
+    per_tok_in = (3 * dk + dv) * io_bytes + io_bytes
+    per_tok_out = dv * io_bytes
+    st = N * H * dk * dv * 4
+    return {"intra": T * H * per_tok_in,
+            "inter": T * H * per_tok_out + (st if with_s0 else 0) + (st if with_sT else 0),
+            "total": T * H * (per_tok_in + per_tok_out) + (st if with_s0 else 0) + (st if with_sT else 0)}
+
+
+def decode_bytes(N, H, d, io_bytes):
+    """Per step: state read + write (fp32), q, k, v, z, beta read, o written."""
+    return N * H * (2 * d * d * 4 + 4 * d * io_bytes + io_bytes + d * io_bytes)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling (100 ms) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kda_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [x.strip() for x in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_run(d, units=None, reps_target_s=10.0, max_reps=3):
+    """Times the fp64 C oracle (as it stands) on the workload; returns (token-heads/s, threads, secs)."""
+    from oracle import c_ref
+    c_ref.build()
+    nth = os.cpu_count() or 1
+    best = None
+    used = 1
+    total = 0.0
+    reps = 0
+    while reps < max_reps and (reps == 0 or total < reps_target_s):
+        _, info = c_ref.forward(d["q"], d["k"], d["v"], d["z"], d["beta"], d["dt_bias"], d["A_log"],
+                                d["cu_seqlens"], S0=d["initial_state"], units=units, nthreads=nth)
+        used = info["threads"]
+        total += info["seconds"]
+        best = info["seconds"] if best is None else min(best, info["seconds"])
+        reps += 1
+    return best, used, total, reps
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return
+    d = syn.make_prefill(WORKLOAD, seed=1, device="cpu")
+    T, H = sum(d["lengths"]), WORKLOAD.H
+    from oracle import c_ref
+    c_ref.build()
+    nth = os.cpu_count() or 1
+    times = []
+    used = 1
+    for i in range(args.warmup + args.steps):
+        _, info = c_ref.forward(d["q"], d["k"], d["v"], d["z"], d["beta"], d["dt_bias"], d["A_log"],
+                                d["cu_seqlens"], S0=d["initial_state"], nthreads=nth)
+        used = info["threads"]
+        if i >= args.warmup:
+            times.append(info["seconds"])
+    ms = 1e3 * sum(times) / len(times)
+    value = T / (ms / 1e3)
+    line = {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD.name, "tokens": T, "heads": H, "d": WORKLOAD.d, "chunk": 64,
+                   "io_dtype": "bf16", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": f"the full workload ({T} tokens x {H} heads) each step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, rank, ws, local):
+    from linear_attention_kda_gb300 import build as kbuild, kda
+    kbuild.build()
+    kda.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    # ---------------- prefill inputs resident in HBM
+    d = syn.make_prefill(WORKLOAD, seed=1 + rank, device=dev)
+    lengths = d["lengths"]
+    T, N, H, D = sum(lengths), len(lengths), WORKLOAD.H, WORKLOAD.d
+    cu_host = d["cu_seqlens"].cpu()
+    q, k, v, z, beta = (d[n] for n in ("q", "k", "v", "z", "beta"))
+    b, a = d["dt_bias"], d["A_log"]
+    o = torch.empty_like(v)
+    fs = torch.empty((N, H, D, D), dtype=torch.float32, device=dev)
+    wsz = kda.chunk_fwd_workspace_size(T, N, H, D, D, q.dtype, 64, cu_host)
+    work = torch.empty((wsz,), dtype=torch.uint8, device=dev)
+    flush = torch.empty((512 << 20,), dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.chunk_fwd(q, k, v, z, beta, b, a, g_min=d["g_min"], scale=d["scale"], cu_seqlens=d["cu_seqlens"],
+                      cu_seqlens_host=cu_host, final_state=fs, workspace=work, out=o)
+
+    nk = kda.chunk_fwd_kernel_count()
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    for row in ev:  # materialise the events before handing them to the library
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier(ws)
+        for i in range(args.steps):
+            flush.zero_()
+            kda.set_profile_events(ev[i])
+            step()
+        kda.set_profile_events([])
+        torch.cuda.synchronize()
+        barrier(ws)
+    clocks = clk.summary()
+    step_ms = [ev[i][0].elapsed_time(ev[i][nk]) for i in range(args.steps)]
+    kern_ms = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)] for j in range(nk)]
+    ms = sum(step_ms) / len(step_ms)
+    ms_max = max_over_ranks(ms, ws)
+    value = T * ws / (ms_max / 1e3)
+    fl = prefill_flops(lengths, H, D, D)
+    by = prefill_bytes(T, N, H, D, D, 2, False, True)
+    tflops = fl["total"] / (ms / 1e3) / 1e12
+    kern_avg = [sum(x) / len(x) for x in kern_ms]
+    names = ["chunk_plan", "chunk_intra", "chunk_inter"][:nk]
+    dom = max(range(nk), key=lambda j: kern_avg[j])
+    role = {"chunk_intra": "intra", "chunk_inter": "inter"}.get(names[dom], "intra")
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    tc = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    bytes_dom, flops_dom = by[role], fl[role]
+    t_dom = kern_avg[dom] / 1e3
+    # the kernel's algorithmic bound: whichever of its bytes or FLOPs takes longer at peak
+    if bytes_dom / (hbm * 1e9) >= flops_dom / (tc * 1e12):
+        roof = {"bound": "hbm", "achieved": bytes_dom / t_dom / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops_dom / t_dom / 1e12, "peak": tc, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = names[dom]
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json burst)" if peak_kind == "measured" else "fallback"
+
+    # ---------------- e2e through the same C ABI call with host buffers
+    pin = {n: d[n].cpu().pin_memory() for n in ("q", "k", "v", "z", "beta")}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    fs_host = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+    dev_in = {n: torch.empty_like(d[n]) for n in pin}
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = o_host.numel() * o_host.element_size() + fs_host.numel() * fs_host.element_size()
+
+    def e2e_step():
+        for n in pin:
+            dev_in[n].copy_(pin[n], non_blocking=True)
+        kda.chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["z"], dev_in["beta"], b, a,
+                      g_min=d["g_min"], scale=d["scale"], cu_seqlens=d["cu_seqlens"], cu_seqlens_host=cu_host,
+                      final_state=fs, workspace=work, out=o)
+        o_host.copy_(o, non_blocking=True)
+        fs_host.copy_(fs, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_times = []
+    barrier(ws)
+    for _ in range(args.steps):
+        flush.zero_()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e2e_times.append(e0.elapsed_time(e1))
+    e2e_ms = max_over_ranks(sum(e2e_times) / len(e2e_times), ws)
+    del dev_in, pin
+
+    # ---------------- decode workload (HBM-bound), 512 in-place steps
+    dec = None
+    if not args.no_decode:
+        dd = syn.make_decode(DECODE, seed=4 + rank, device=dev)
+        st = dd["state"]
+        nsteps = DECODE.decode_steps
+        od = torch.empty((DECODE.n_seq, DECODE.H, DECODE.d), dtype=torch.bfloat16, device=dev)
+        ins = [[dd[n][s] for n in ("q", "k", "v", "z", "beta")] for s in range(nsteps)]
+        for s in range(3):
+            kda.recurrent_step(*ins[s], dd["dt_bias"], dd["A_log"], st, out=od)
+        torch.cuda.synchronize()
+        dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nsteps)]
+        for e_a, e_b in dev_ev:
+            e_a.record(stream)
+            e_b.record(stream)
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk2:
+            for s in range(nsteps):
+                kda.set_profile_events(list(dev_ev[s]))
+                kda.recurrent_step(*ins[s], dd["dt_bias"], dd["A_log"], st, out=od)
+            kda.set_profile_events([])
+            torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        dts = [a_.elapsed_time(b_) for a_, b_ in dev_ev]
+        dms = sum(dts) / len(dts)
+        dbytes = decode_bytes(DECODE.n_seq, DECODE.H, DECODE.d, 2)
+        gbs = dbytes / (dms / 1e3) / 1e9
+        dec = {"workload": DECODE.name, "steps": nsteps, "us_per_step": dms * 1e3,
+               "GB_per_s": gbs, "bytes_per_step": dbytes,
+               "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                            "traffic": None, "kernel": "decode_step"},
+               "clocks": clk2.summary()}
+        del dd, ins, st
+
+    # ---------------- CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        dc = syn.make_prefill(WORKLOAD, seed=1, device="cpu")
+        secs, used, total, reps = cpu_oracle_run(dc)
+        cpu = {"value": T / secs, "unit": "tokens/s", "cores": used, "kind": "oracle",
+               "sample": f"the full workload ({T} tokens x {H} heads), best of {reps} runs, {total:.1f} s total"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD.name, "tokens": T, "sequences": N, "heads": H, "d_k": D,
+                       "d_v": D, "chunk": 64, "io_dtype": "bf16", "state_dtype": "f32",
+                       "final_state": True, "l2": "flushed (512 MiB write) before every timed step",
+                       "parallelism": f"replicas x{ws}"},
+            "tflops": tflops, "tflops_dense_tile": fl["dense_tile"] / (ms / 1e3) / 1e12,
+            "frac_bf16_peak": tflops / tc, "hbm_gbs_algorithmic": by["total"] / (ms / 1e3) / 1e9,
+            "kernels_ms": dict(zip(names, kern_avg)),
+            "roofline": roof,
+            "e2e": {"value": T * ws / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": nk * args.steps,
+            "clocks": clocks,
+            "decode": dec,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, ws, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, ws)
+    else:
+        run_ours(args, rank, ws, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

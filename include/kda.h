@@ -170,6 +170,18 @@ kda_status_t kda_get_device_error(struct CUstream_st *stream);
 
 int kda_abi_version(void);
 
+/* ------------------------------------------------------------ instrumentation
+ * Optional per-kernel timing.  While set (n_events > 0), kda_chunk_fwd records
+ * events[0] on its stream before its first kernel and events[i] right after its
+ * i-th kernel launch, for i < n_events; kda_recurrent_step records events[0]
+ * before and events[1] after its kernel.  `events` are cudaEvent_t handles
+ * created by the caller (timing enabled); the array is copied.  Pass
+ * (NULL, 0) to stop.  Process-wide setting: set it only while one thread calls
+ * into the library.  Returns the number of kernels kda_chunk_fwd launches for
+ * the given problem when queried with kda_chunk_fwd_kernel_count(). */
+kda_status_t kda_set_profile_events(void *const *events, int32_t n_events);
+int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *args);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,6 +34,16 @@ size_t dtype_size(kda_dtype_t t) { return t == KDA_BF16 ? 2 : 4; }
 
 }  // namespace
 
+namespace {
+constexpr int kMaxProfileEvents = 16;
+cudaEvent_t g_prof_events[kMaxProfileEvents];
+int g_prof_n = 0;
+}  // namespace
+
+void kda_profile_mark(int i, cudaStream_t stream) {
+    if (i < g_prof_n && g_prof_events[i]) cudaEventRecord(g_prof_events[i], stream);
+}
+
 int *kda_device_error_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -48,6 +58,19 @@ int *kda_device_error_ptr() {
 extern "C" {
 
 int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+kda_status_t kda_set_profile_events(void *const *events, int32_t n_events) {
+    if (n_events < 0 || n_events > kMaxProfileEvents || (n_events > 0 && !events))
+        return KDA_ERR_INVALID_ARG;
+    for (int i = 0; i < n_events; ++i) g_prof_events[i] = (cudaEvent_t)events[i];
+    g_prof_n = n_events;
+    return KDA_OK;
+}
+
+int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
+    if (!a) return 0;
+    return 3;  // chunk plan, intra-chunk transform, inter-chunk state/output pass
+}
 
 const char *kda_status_string(kda_status_t s) {
     switch (s) {

@@ -248,8 +248,10 @@ kda_status_t kda_launch_chunk_plan(const kda_chunk_args *a, const kda_chunk_plan
 
 kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
                                    cudaStream_t stream) {
+    kda_profile_mark(0, stream);
     kda_status_t st = kda_launch_chunk_plan(a, p, ws, stream);
     if (st != KDA_OK) return st;
+    kda_profile_mark(1, stream);
     const int C = p.C, dk = p.dk, dv = p.dv, H = p.H;
     const int32_t *chunk_start = (const int32_t *)((char *)ws + p.off_chunk_start);
     char *records = (char *)ws + p.off_records;
@@ -275,6 +277,7 @@ kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan
         }
         if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     }
+    kda_profile_mark(2, stream);
     dim3 grid2((unsigned)(a->N * H), (unsigned)(dv / SLICE));
     if (b16) {
         cudaFuncSetAttribute(chunk_chain_simt_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_chain);
@@ -287,5 +290,6 @@ kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan
             a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, p.record_bytes,
             a->scale, a->initial_state, a->final_state, (float *)a->o);
     }
+    kda_profile_mark(3, stream);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

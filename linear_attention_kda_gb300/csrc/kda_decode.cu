@@ -162,7 +162,9 @@ kda_status_t kda_launch_decode(const kda_step_args *a, cudaStream_t stream) {
     int *err = kda_device_error_ptr();
     if (!err) return KDA_ERR_CUDA;
     const bool b16 = a->dtype == KDA_BF16;
+    kda_profile_mark(0, stream);
     if (a->dk == 128) { if (b16) launch<128, bf16>(a, stream, err); else launch<128, float>(a, stream, err); }
     else { if (b16) launch<64, bf16>(a, stream, err); else launch<64, float>(a, stream, err); }
+    kda_profile_mark(1, stream);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

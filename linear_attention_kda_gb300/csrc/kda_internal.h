@@ -5,6 +5,9 @@
 
 #include "../../include/kda.h"
 
+// Records the i-th profiling event on `stream` when instrumentation is set.
+void kda_profile_mark(int i, cudaStream_t stream);
+
 kda_status_t kda_launch_gate(const kda_gate_args *a, cudaStream_t stream);
 kda_status_t kda_launch_decode(const kda_step_args *a, cudaStream_t stream);
 

@@ -25,7 +25,8 @@ _STATUS = {
     9: "KDA_ERR_NO_DEVICE", 10: "KDA_ERR_DEVICE_TIMEOUT",
 }
 EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step",
-            "kda_status_string", "kda_get_device_error", "kda_abi_version"]
+            "kda_status_string", "kda_get_device_error", "kda_abi_version",
+            "kda_set_profile_events", "kda_chunk_fwd_kernel_count"]
 
 _vp = ctypes.c_void_p
 _i64, _i32, _f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
@@ -86,6 +87,10 @@ def load_library(path: Optional[str] = None):
         L.kda_get_device_error.argtypes = [_vp]
         L.kda_get_device_error.restype = ctypes.c_int
         L.kda_abi_version.restype = ctypes.c_int
+        L.kda_set_profile_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), _i32]
+        L.kda_set_profile_events.restype = ctypes.c_int
+        L.kda_chunk_fwd_kernel_count.argtypes = [ctypes.POINTER(ChunkArgs)]
+        L.kda_chunk_fwd_kernel_count.restype = _i32
         _lib = L
         return L
 
@@ -197,3 +202,18 @@ def get_device_error(device=None) -> int:
 
 def status_string(code: int) -> str:
     return load_library().kda_status_string(int(code)).decode()
+
+
+def set_profile_events(events) -> None:
+    """Per-kernel timing: pass torch.cuda.Event objects (already recorded once), or [] to stop."""
+    L = load_library()
+    if not events:
+        _check(L.kda_set_profile_events(None, 0), "kda_set_profile_events")
+        return
+    arr = (ctypes.c_void_p * len(events))(*[int(e.cuda_event) for e in events])
+    _check(L.kda_set_profile_events(arr, len(events)), "kda_set_profile_events")
+
+
+def chunk_fwd_kernel_count() -> int:
+    a = ChunkArgs()
+    return int(load_library().kda_chunk_fwd_kernel_count(ctypes.byref(a)))
