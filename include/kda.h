@@ -136,6 +136,31 @@ size_t kda_chunk_fwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk,
 kda_status_t kda_chunk_fwd(const kda_chunk_args *args, void *workspace, size_t workspace_bytes,
                            struct CUstream_st *stream);
 
+/* --------------------------------------------------- kda_chunk_fwd_static_ws
+ * Not an operation of the paper (it has no counterpart there): the same
+ * prefill as kda_chunk_fwd, for callers that cannot allocate device memory at
+ * all -- for example engine plugins that receive only input and output
+ * pointers while the engine owns every other byte of device memory, or code
+ * that must not risk the device-wide synchronisation of cudaMalloc/cudaFree.
+ * Instead of a caller workspace it uses one scratch buffer of
+ * KDA_STATIC_WORKSPACE_BYTES that lives inside the library (a file-scope
+ * device array, held by every GPU that loads the library until the process
+ * exits).  The caller still owns and passes every input and output.
+ *   - Limit: problems whose kda_chunk_fwd_workspace_size() exceeds
+ *     KDA_STATIC_WORKSPACE_BYTES are rejected with KDA_ERR_WORKSPACE before
+ *     anything is launched (e.g. bf16, d = 128: about 440 chunk-heads, such as
+ *     T = 2048 tokens with 12 heads).
+ *   - Set-up: the first call on each device, made while that device is
+ *     current, looks up the buffer's device address; make that first call
+ *     before any stream capture.
+ *   - Sharing: every call on a device uses the same buffer, which keeps the
+ *     last call's contents.  Calls whose GPU work overlaps in time (different
+ *     streams, or different host threads) race on it and give wrong results:
+ *     serialise them.
+ * It allocates no device memory and calls no allocating routine. */
+#define KDA_STATIC_WORKSPACE_BYTES (64u << 20)
+kda_status_t kda_chunk_fwd_static_ws(const kda_chunk_args *args, struct CUstream_st *stream);
+
 /* -------------------------------------------------------- kda_recurrent_step
  * Decode: one token per sequence, Eq. 1 applied once to each (sequence, head)
  * state in place (section 5.4.2: the recurrent state is updated in place every

@@ -26,7 +26,8 @@ _STATUS = {
 }
 EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step",
             "kda_status_string", "kda_get_device_error", "kda_abi_version",
-            "kda_set_profile_events", "kda_chunk_fwd_kernel_count"]
+            "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws"]
+STATIC_WORKSPACE_BYTES = 64 << 20
 
 _vp = ctypes.c_void_p
 _i64, _i32, _f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
@@ -91,6 +92,8 @@ def load_library(path: Optional[str] = None):
         L.kda_set_profile_events.restype = ctypes.c_int
         L.kda_chunk_fwd_kernel_count.argtypes = [ctypes.POINTER(ChunkArgs)]
         L.kda_chunk_fwd_kernel_count.restype = _i32
+        L.kda_chunk_fwd_static_ws.argtypes = [ctypes.POINTER(ChunkArgs), _vp]
+        L.kda_chunk_fwd_static_ws.restype = ctypes.c_int
         _lib = L
         return L
 
@@ -217,3 +220,34 @@ def set_profile_events(events) -> None:
 def chunk_fwd_kernel_count() -> int:
     a = ChunkArgs()
     return int(load_library().kda_chunk_fwd_kernel_count(ctypes.byref(a)))
+
+
+def chunk_fwd_static_ws(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0,
+                        scale: float = 1.0, cu_seqlens: Optional[torch.Tensor] = None,
+                        cu_seqlens_host: Optional[torch.Tensor] = None, n_seq: int = 1,
+                        initial_state: Optional[torch.Tensor] = None,
+                        final_state: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None):
+    """kda_chunk_fwd_static_ws: prefill using the library's own fixed scratch buffer.
+
+    For callers that must not allocate device scratch: outputs (`out`,
+    `final_state`) are caller-provided tensors here (allocated by this helper only
+    when omitted); the library uses its internal buffer of STATIC_WORKSPACE_BYTES
+    and rejects larger problems (KDA_ERR_WORKSPACE).  Calls on one device share
+    that buffer, so they must not overlap in time.
+    """
+    L = load_library()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    _contig(q, k, v, z, beta, dt_bias, A_log, cu_seqlens, initial_state)
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else n_seq
+    if cu_seqlens_host is not None:
+        cu_seqlens_host = cu_seqlens_host.to(dtype=torch.int32, device="cpu").contiguous()
+    o = out if out is not None else torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=_dtype_code(q), q=_ptr(q), k=_ptr(k), z=_ptr(z),
+                  v=_ptr(v), beta=_ptr(beta), dt_bias=_ptr(dt_bias), A_log=_ptr(A_log), g_min=g_min,
+                  scale=scale, cu_seqlens=_ptr(cu_seqlens),
+                  cu_seqlens_host=None if cu_seqlens_host is None else cu_seqlens_host.data_ptr(),
+                  initial_state=_ptr(initial_state), final_state=_ptr(final_state), o=_ptr(o),
+                  chunk_size=64)
+    _check(L.kda_chunk_fwd_static_ws(ctypes.byref(a), _stream(q)), "kda_chunk_fwd_static_ws")
+    return o, final_state
