@@ -148,8 +148,8 @@ kda_status_t kda_chunk_fwd(const kda_chunk_args *args, void *workspace, size_t w
  * exits).  The caller still owns and passes every input and output.
  *   - Limit: problems whose kda_chunk_fwd_workspace_size() exceeds
  *     KDA_STATIC_WORKSPACE_BYTES are rejected with KDA_ERR_WORKSPACE before
- *     anything is launched (e.g. bf16, d = 128: about 440 chunk-heads, such as
- *     T = 2048 tokens with 12 heads).
+ *     anything is launched (bf16 with d = 128 needs about 74 KiB per chunk of
+ *     64 tokens per head, so e.g. T = 4096 tokens with 13 heads fit).
  *   - Set-up: the first call on each device, made while that device is
  *     current, looks up the buffer's device address; make that first call
  *     before any stream capture.

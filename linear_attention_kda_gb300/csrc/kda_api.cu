@@ -175,6 +175,7 @@ kda_status_t kda_chunk_fwd(const kda_chunk_args *a, void *workspace, size_t work
     if (!aligned_to(workspace, 256)) return KDA_ERR_MISALIGNED;
     st = check_device();
     if (st != KDA_OK) return st;
+    if (p.path == 1) return kda_launch_chunk_tc(a, p, workspace, (cudaStream_t)stream);
     return kda_launch_chunk_simt(a, p, workspace, (cudaStream_t)stream);
 }
 

@@ -78,13 +78,17 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
     if (T < 0 || N < 1 || H < 1 || C < 1) return false;
     p->T = T; p->N = N; p->H = H; p->dk = dk; p->dv = dv; p->C = C;
     p->max_chunks = (T + N * (int64_t)(C - 1)) / C;
-    p->path = 0;
-    // fp32 CUDA-core records: W, Q^, K~ [C, dk]; U [C, dv]; A [C, C]; gamma^C [dk]
-    p->record_bytes = align_up(sizeof(float) * ((size_t)C * (3 * dk + dv) + (size_t)C * C + dk), 256);
+    // bf16 with d_k = d_v = 128 runs on the tensor cores; everything else on the fp32 CUDA-core path
+    p->path = (dtype == KDA_BF16 && dk == 128 && dv == 128 && C == 64) ? 1 : 0;
+    if (p->path == 1) {
+        p->record_bytes = kda_tc_packet_stride();  // bf16 operand images + gamma^C
+    } else {
+        // fp32 CUDA-core records: W, Q^, K~ [C, dk]; U [C, dv]; A [C, C]; gamma^C [dk]
+        p->record_bytes = align_up(sizeof(float) * ((size_t)C * (3 * dk + dv) + (size_t)C * C + dk), 256);
+    }
     p->off_chunk_start = 0;
     p->off_records = align_up(sizeof(int32_t) * (size_t)(N + 1), 256);
     p->total_bytes = p->off_records + p->record_bytes * (size_t)p->max_chunks * (size_t)H;
-    (void)dtype;
     return true;
 }
 

@@ -27,3 +27,6 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
                          kda_chunk_plan *plan);
 kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
                                    cudaStream_t stream);
+kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
+                                 cudaStream_t stream);
+size_t kda_tc_packet_stride();  // bytes per (chunk, head) packet of the tensor-core path
