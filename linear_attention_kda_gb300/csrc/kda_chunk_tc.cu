@@ -5,7 +5,9 @@
 // (kind::f16, bf16 operands in shared memory, fp32 accumulators in tensor
 // memory); the scan-like and exponential work runs on the CUDA cores in fp32.
 //
-// 1. chunk_intra_tc (one CTA per (chunk, head); all chunks in parallel)
+// 1. chunk_intra_tc (persistent: one CTA of 256 threads per SM walks the
+//    (chunk, head) items; the q, k, v, z tiles of the next item are bulk-copied
+//    into a second buffer while the current one is computed)
 //    - g (Eq. 5) and the in-chunk cumulative log-decay G (Eq. 3), fp32.
 //    - A = Tril[(Q Gamma)(K / Gamma)^T] (diagonal kept) and the UT-transform
 //      matrix L = StrictTril[diag(beta)(K Gamma)(K / Gamma)^T].  Over a 64-token
@@ -25,18 +27,21 @@
 //    - Writes a per-(chunk, head) packet of ready-to-use operand images:
 //      W [64 x 128], Q^ = Q Gamma [64 x 128], K~^T = (K e^{G_last - G})^T [128 x 64],
 //      A [64 x 64], U^T [128 x 64] (plain), gamma^C [128] fp32.
-// 2. chunk_inter_tc (one CTA per (sequence, head); chunks in order)
+// 2. chunk_inter_tc (one CTA of 256 threads per (sequence, head); chunks in order)
 //    The state is kept transposed in tensor memory, S^T [d_v lanes x d_k
 //    columns] fp32, and as a bf16 operand image in shared memory.  Per chunk:
 //      V~^T = U^T - S^T W^T                      (MMA, M = 128, N = 64, K = 128)
 //      O^T  = S^T Q^^T + V~^T A^T                (MMA, K = 128 then K = 64)
 //      S^T <- S^T Diag(gamma^C) + V~^T K~        (scale in fp32, MMA N = 128, K = 64)
-//    Packets are streamed by 1-D bulk copies, double buffered.
+//    Warps w and w + 4 share TMEM lanes and split the columns.  Packets are
+//    streamed by 1-D bulk copies, double buffered.
 // Waits on mbarriers give up after about a second, set KDA_ERR_DEVICE_TIMEOUT,
 // and the kernel still releases its tensor memory before it returns.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "tc_util.cuh"
+
+#include <cuda.h>
 
 namespace kda {
 namespace tcp {
@@ -45,7 +50,6 @@ using namespace kda::tc;
 
 constexpr int C = 64;   // chunk
 constexpr int D = 128;  // d_k = d_v
-constexpr int NT = 128; // threads per CTA
 
 // packet layout (bytes)
 constexpr uint32_t PK_W = 0;          // W image, 64 rows x 128 K
@@ -57,35 +61,30 @@ constexpr uint32_t PK_G = 73728;      // gamma^C fp32 [128]
 constexpr uint32_t PK_BYTES = 74240;
 constexpr uint32_t PK_STRIDE = 75776; // multiple of 1024
 
-// intra kernel shared memory (offsets from a 1024-aligned base)
-constexpr uint32_t IS_G = 0;            // fp32 [64][128]
-constexpr uint32_t IS_SCR = 32768;      // 48 KB scratch, reused by phase
-constexpr uint32_t IS_ROW = IS_SCR;             // row image 128 x 128 (32 KB)
-constexpr uint32_t IS_KEY = IS_SCR + 32768;     // 4 key-block images 16 x 128 (4 KB each)
-constexpr uint32_t IS_L = IS_SCR;               // fp32 [64][65]
-constexpr uint32_t IS_T = IS_SCR + 16640;       // fp32 [64][65]
-constexpr uint32_t IS_P = IS_SCR + 33280;       // fp32 [3][16][16]
-constexpr uint32_t IS_TIMG = IS_SCR + 40960;    // T image 64 x 64 (8 KB)
-constexpr uint32_t IS_XT = IS_SCR;              // (beta Gamma K)^T image 128 x 64
-constexpr uint32_t IS_VT = IS_SCR + 16384;      // (beta V)^T image 128 x 64
-constexpr uint32_t IS_WST = IS_SCR;             // W staging image 64 x 128
-constexpr uint32_t IS_BETA = IS_SCR + 49152;    // fp32 [64]
-constexpr uint32_t IS_BAR = IS_BETA + 256;
-constexpr uint32_t IS_TSLOT = IS_BAR + 16;
-constexpr uint32_t IS_TOTAL = IS_BAR + 64 + 1024;  // + alignment slack
-
 // inter kernel shared memory
 constexpr uint32_t CS_STAGE0 = 0;
 constexpr uint32_t CS_STAGE1 = PK_STRIDE;
 constexpr uint32_t CS_SIMG = 2 * PK_STRIDE;            // S^T image 128 x 128 (32 KB)
 constexpr uint32_t CS_VIMG = CS_SIMG + 32768;          // V~^T image 128 x 64 (16 KB)
-constexpr uint32_t CS_BAR = CS_VIMG + 16384;           // 3 mbarriers
-constexpr uint32_t CS_TSLOT = CS_BAR + 32;
-constexpr uint32_t CS_TOTAL = CS_BAR + 64 + 1024;
+constexpr uint32_t CS_BAR = CS_VIMG + 16384;           // 8 mbarriers
+constexpr uint32_t CS_TSLOT = CS_BAR + 64;             // TMEM base, failure flag
+constexpr uint32_t CS_TOTAL = CS_BAR + 128 + 1024;
 
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
     const uint32_t s = smem_u32(p);
     return p + ((1024u - (s & 1023u)) & 1023u);
+}
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+// bar.red.popc over the 256 threads of named barrier 1.
+__device__ __forceinline__ int __syncthreads_count_named1(bool pred) {
+    int r;
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.popc.u32 %0, 1, 256, p;\n\t}\n"
+                 : "=r"(r) : "r"((unsigned)pred) : "memory");
+    return r;
 }
 
 __device__ __forceinline__ void sync_all() {
@@ -136,290 +135,527 @@ __device__ __forceinline__ bool locate(const int32_t *chunk_start, const int32_t
 }
 
 // =====================================================================================
-__global__ void __launch_bounds__(NT, 2)
-chunk_intra_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
-                      const bf16 *__restrict__ z, const bf16 *__restrict__ beta,
+// Persistent intra-chunk kernel: one CTA per SM walks (chunk, head) work items
+// w = slot * H + h.  Warp 8 is the producer: for each item it fetches the q, z, k, v
+// tiles (four TMA boxes of 64 tokens x 128 channels) and the item's beta, bias and
+// e^{A_log} into one half of a double buffer, while warps 0-7 compute the other item.
+//
+// Exponentials: per element only d = G_r - G_p(r) >= 0 (p(r) = last row of r's
+// 16-row block) is exponentiated, as E = e^d and E^-1 = e^-d; every other decay
+// factor is E or E^-1 times a per-(block, channel) factor:
+//   e^{G_r}           = E * e^{G_p}                    (Q^, beta Gamma K)
+//   e^{G_last - G_r}  = E^-1 * e^{G_last - G_p}        (K~)
+//   e^{G_p - G_r}     = E^-1                            (key-block image)
+//   e^{G_r - G_p'}    = E * e^{G_p(r) - G_p'}  (p' <= p(r), row images)
+constexpr int NT2 = 288;      // 8 consumer warps + 1 producer warp
+constexpr int NC2 = 256;      // consumer threads
+constexpr uint32_t I2_STG = 0;  // 2 stages x [Q | Z | K | V], plain [64][128] bf16 each
+constexpr uint32_t I2_STG_BYTES = 65536;
+constexpr uint32_t I2_TQ = 0, I2_TZ = 16384, I2_TK = 32768, I2_TV = 49152;
+// after the gate (Z dead) and the row-side caching (Q dead) the stage's first 32 KB
+// hold the second row image, and after the L/A products the X^T and (beta V)^T images
+constexpr uint32_t I2_G = 131072;             // fp32 [64][128]: G, then E in place
+constexpr uint32_t I2_SCR = 163840;           // 48 KB scratch
+constexpr uint32_t I2_ROW = I2_SCR;           // row image A (stage + 0 is row image B)
+constexpr uint32_t I2_KEY = I2_SCR + 32768;   // 4 key-block images
+constexpr int LS = 68;                        // row stride (floats) of the fp32 L and T matrices
+constexpr uint32_t I2_L = I2_SCR;             // fp32 [64][68]
+constexpr uint32_t I2_T = I2_SCR + 17408;     // fp32 [64][68]
+constexpr uint32_t I2_P = I2_SCR + 34816;     // fp32 [3][16][16]
+constexpr uint32_t I2_TIMG = I2_SCR + 40960;  // T image 64 x 64
+constexpr uint32_t I2_XT = 0;                 // relative to the stage
+constexpr uint32_t I2_VT = 16384;             // relative to the stage
+constexpr uint32_t I2_WST = I2_SCR;           // W staging image 64 x 128
+constexpr uint32_t I2_FAC = 212992;           // fp32 factor rows, [18][128]
+constexpr int FAC_GPR = 0, FAC_GPE = 4, FAC_FL = 8, FAC_F = 12;  // row indices
+constexpr uint32_t I2_BETA = I2_FAC + 18 * 512;   // 2 stages x fp32 [64]
+constexpr uint32_t I2_BIAS = I2_BETA + 512;       // 2 stages x fp32 [128]
+constexpr uint32_t I2_INFO = I2_BIAS + 1024;      // 2 stages x {int64 t0, len, h, slot; float eA}
+constexpr uint32_t I2_BAR = I2_INFO + 128;        // ld[2], free[2], mma[2]
+constexpr uint32_t I2_TSLOT = I2_BAR + 48;
+constexpr uint32_t I2_TOTAL = I2_BAR + 64 + 1024;
+
+__device__ __forceinline__ int fpair(int b, int bp) { return (b * (b - 1)) / 2 + bp; }  // b' < b
+
+__device__ __forceinline__ void unpack4(const uint2 &u, float *f) {
+    const __nv_bfloat162 *hh = reinterpret_cast<const __nv_bfloat162 *>(&u);
+    const float2 a = __bfloat1622float2(hh[0]), b = __bfloat1622float2(hh[1]);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+__device__ __forceinline__ uint2 pack4(const float *f) {
+    return make_uint2(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]));
+}
+
+struct TileMaps {
+    CUtensorMap q, k, v, z;
+};
+
+// Consumer-group barrier (warps 0-7, named barrier 1) with tcgen05 ordering.
+__device__ __forceinline__ void csync() {
+    fence_before_sync();
+    named_sync(1, NC2);
+    fence_after_sync();
+}
+__device__ __forceinline__ bool csync_and(bool pred) { return __syncthreads_count_named1(pred) == NC2; }
+// Waits on an mbarrier from every consumer thread; CTA-group-uniform result.
+__device__ __forceinline__ bool cwait(uint64_t *bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return csync_and(ok);
+}
+
+__global__ void __launch_bounds__(NT2, 1)
+chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restrict__ beta,
                       const float *__restrict__ bias, const float *__restrict__ A_log, float g_min,
                       int64_t T, int N, const int32_t *__restrict__ cu,
                       const int32_t *__restrict__ chunk_start, int H, unsigned char *__restrict__ packets,
                       int *err) {
     extern __shared__ unsigned char smem_raw[];
-    const int64_t slot = blockIdx.x;
-    const int h = blockIdx.y;
-    int n, len;
-    int64_t t0;
-    if (!locate(chunk_start, cu, T, N, slot, n, t0, len)) return;
-
     unsigned char *sm = align1024(smem_raw);
-    float *G = (float *)(sm + IS_G);
-    float *bet = (float *)(sm + IS_BETA);
-    uint64_t *bar = (uint64_t *)(sm + IS_BAR);
-    uint32_t *tslot = (uint32_t *)(sm + IS_TSLOT);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    unsigned char *pk = packets + ((size_t)slot * H + h) * PK_STRIDE;
-    const int64_t rowstride = (int64_t)H * D;  // elements between consecutive tokens
-    const bf16 *qh = q + (t0 * H + h) * D;
-    const bf16 *kh = k + (t0 * H + h) * D;
-    const bf16 *vh = v + (t0 * H + h) * D;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t W = (int64_t)chunk_start[N] * H;  // work items
+    if ((int64_t)blockIdx.x >= W) return;
+    float *G = (float *)(sm + I2_G);
+    float *FAC = (float *)(sm + I2_FAC);
+    uint64_t *bar_ld = (uint64_t *)(sm + I2_BAR);
+    uint64_t *bar_free = bar_ld + 2;
+    uint64_t *bar_mma = bar_ld + 4;  // one per row-image buffer: no barrier ever has two phases pending
+    uint32_t *tslot = (uint32_t *)(sm + I2_TSLOT);
 
-    if (tid == 0) mbar_init(bar, 1);
-    if (warp == 0) tmem_alloc(tslot, 256);
-    if (tid < C) bet[tid] = tid < len ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
-
-    // ---- phase 1: gate (Eq. 5) and in-chunk cumulative log-decay (Eq. 3), thread = channel
-    {
-        const int c = tid;
-        const float eA = A_log ? expf(A_log[h]) : 1.f;
-        const float bc = bias ? bias[h * D + c] : 0.f;
-        const bf16 *zc = z + (t0 * H + h) * D + c;
-        float acc = 0.f;
-#pragma unroll 4
-        for (int r0 = 0; r0 < C; r0 += 16) {
-            float zz[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                zz[i] = (r0 + i < len) ? __bfloat162float(zc[(int64_t)(r0 + i) * rowstride]) : 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float g = (r0 + i < len) ? gate_logdecay(zz[i], bc, eA, g_min) : 0.f;
-                acc += g;
-                G[(r0 + i) * D + c] = acc;
-            }
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_ld[i], 1);
+            mbar_init(&bar_free[i], 1);
+            mbar_init(&bar_mma[i], 1);
         }
     }
+    if (warp == 0) tmem_alloc(tslot, 256);
     fence_proxy_async();
     sync_all();
     const uint32_t tb = *tslot;
-    uint32_t mma_phase = 0;
-    bool ok = true;
 
-    // ---- phase 2: key-block images K^_b (reference = last token of the block) and Q^ = Q Gamma
-    for (int idx = tid; idx < C * 16; idx += NT) {
-        const int r = idx >> 4, j = idx & 15, c0 = j * 8;
-        const int p = (r | 15);
-        float kf[8], qf[8], Gr[8], Gp[8], o1[8], o2[8];
-        uint4 ku = make_uint4(0, 0, 0, 0), qu = make_uint4(0, 0, 0, 0);
-        if (r < len) {
-            ku = *reinterpret_cast<const uint4 *>(kh + (int64_t)r * rowstride + c0);
-            qu = *reinterpret_cast<const uint4 *>(qh + (int64_t)r * rowstride + c0);
-        }
-        unpack8(ku, kf);
-        unpack8(qu, qf);
+    if (warp == 8) {
+        // ------------------------------------------------ producer warp
+        bool ok = true;
+        for (int it = 0;; ++it) {
+            const int64_t w = (int64_t)blockIdx.x + (int64_t)it * gridDim.x;
+            if (w >= W) break;
+            const int s = it & 1;
+            if (it >= 2) {
+                ok = mbar_wait(&bar_free[s], ((it >> 1) - 1) & 1);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            const int64_t slot = w / H;
+            const int h = (int)(w % H);
+            int n = 0, len = 0;
+            int64_t t0 = 0;
+            locate(chunk_start, cu, T, N, slot, n, t0, len);
+            float *bet = (float *)(sm + I2_BETA) + 64 * s;
+            float *bia = (float *)(sm + I2_BIAS) + 128 * s;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            Gr[e] = G[r * D + c0 + e];
-            Gp[e] = G[p * D + c0 + e];
-        }
+            for (int r = lane; r < C; r += 32) bet[r] = r < len ? __bfloat162float(beta[(t0 + r) * H + h]) : 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            o1[e] = kf[e] * __expf(Gp[e] - Gr[e]);
-            o2[e] = qf[e] * __expf(Gr[e]);
-        }
-        *reinterpret_cast<uint4 *>(sm + IS_KEY + (r >> 4) * 4096 + img_chunk_off(16, r & 15, j)) = pack8(o1);
-        *reinterpret_cast<uint4 *>(pk + PK_Q + img_chunk_off(64, r, j)) = pack8(o2);
-    }
-
-    // ---- phase 3: row images per key block b, one M=128 (q rows | k rows), N=16, K=128 MMA each
-    const uint32_t idesc16 = idesc_bf16(128, 16);
-    for (int b = 0; b < 4; ++b) {
-        const int p = 16 * b + 15;
-        const int rlo = 16 * b;
-        if (b > 0) {  // rows of the previous block become zero for this key block
-            for (int idx = tid; idx < 32 * 16; idx += NT) {
-                const int rr = idx >> 4, j = idx & 15;
-                const int row = (rr < 16) ? (rlo - 16 + rr) : (64 + rlo - 16 + rr - 16);
-                *reinterpret_cast<uint4 *>(sm + IS_ROW + img_chunk_off(128, row, j)) = make_uint4(0, 0, 0, 0);
+            for (int c = lane; c < D; c += 32) bia[c] = bias ? bias[h * D + c] : 0.f;
+            if (lane == 0) {
+                int64_t *info = (int64_t *)(sm + I2_INFO + 64 * s);
+                info[0] = t0;
+                info[1] = len;
+                info[2] = h;
+                info[3] = slot;
+                *reinterpret_cast<float *>(info + 4) = A_log ? __expf(A_log[h]) : 1.f;
+            }
+            __threadfence_block();
+            __syncwarp();
+            if (lane == 0) {
+                unsigned char *stg = sm + I2_STG + s * I2_STG_BYTES;
+                mbar_arrive_expect_tx(&bar_ld[s], 4u * 16384u);
+                tma_load_3d(stg + I2_TQ, &tm.q, 0, h, (int)t0, &bar_ld[s]);
+                tma_load_3d(stg + I2_TZ, &tm.z, 0, h, (int)t0, &bar_ld[s]);
+                tma_load_3d(stg + I2_TK, &tm.k, 0, h, (int)t0, &bar_ld[s]);
+                tma_load_3d(stg + I2_TV, &tm.v, 0, h, (int)t0, &bar_ld[s]);
             }
         }
-        const int nrows = (C - rlo) * 2;
-        for (int idx = tid; idx < nrows * 16; idx += NT) {
-            const int rr = idx >> 4, j = idx & 15, c0 = j * 8;
-            const int side = rr / (C - rlo);            // 0 = q rows, 1 = k rows
-            const int r = rlo + rr % (C - rlo);
-            float xf[8], o[8];
-            uint4 xu = make_uint4(0, 0, 0, 0);
-            if (r < len) xu = *reinterpret_cast<const uint4 *>((side ? kh : qh) + (int64_t)r * rowstride + c0);
-            unpack8(xu, xf);
+        if (!ok && lane == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
+    } else {
+        // ------------------------------------------------ consumer warps 0-7
+        uint32_t mph[2] = {0, 0};
+        bool ok = true;
+        int it = 0;
+        for (;; ++it) {
+            const int64_t w = (int64_t)blockIdx.x + (int64_t)it * gridDim.x;
+            if (w >= W) break;
+            const int s = it & 1;
+            ok = cwait(&bar_ld[s], (it >> 1) & 1);
+            if (!ok) break;
+            const int64_t *info = (const int64_t *)(sm + I2_INFO + 64 * s);
+            const int len = (int)info[1];
+            const int h = (int)info[2];
+            const int64_t slot = info[3];
+            const float eA = *reinterpret_cast<const float *>(info + 4);
+            const float *bet = (const float *)(sm + I2_BETA) + 64 * s;
+            const float *bia = (const float *)(sm + I2_BIAS) + 128 * s;
+            unsigned char *stg = sm + I2_STG + s * I2_STG_BYTES;
+            unsigned char *pk = packets + ((size_t)slot * H + h) * PK_STRIDE;
+            if (len < C) {  // clear rows past the end of the sequence (uniform branch)
+                for (int idx = tid; idx < 4 * (C - len) * 16; idx += NC2) {
+                    const int tile = idx / ((C - len) * 16), rem = idx % ((C - len) * 16);
+                    const int r = len + rem / 16, u = rem % 16;
+                    reinterpret_cast<uint4 *>(stg + tile * 16384 + r * 256)[u] = make_uint4(0, 0, 0, 0);
+                }
+                csync();
+            }
+
+            // ---- phase 1: gate (Eq. 5) and in-chunk cumulative log-decay (Eq. 3): thread = (channel, half)
+            //      g = g_min / (1 + e^{-x}) with fast exp and division (a few ulp each)
+            {
+                const int c = tid & 127, r0 = (tid >> 7) * 32;
+                const float bc = bia[c];
+                const bf16 *Z = reinterpret_cast<const bf16 *>(stg + I2_TZ);
+                float gv[32];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = xf[e] * __expf(G[r * D + c0 + e] - G[p * D + c0 + e]);
-            *reinterpret_cast<uint4 *>(sm + IS_ROW + img_chunk_off(128, side * 64 + r, j)) = pack8(o);
-        }
-        fence_proxy_async();
-        sync_all();
-        if (ok) {  // ok is CTA-uniform
+                for (int i = 0; i < 32; ++i) {
+                    const float x = eA * (__bfloat162float(Z[(r0 + i) * D + c]) + bc);
+                    gv[i] = (r0 + i < len) ? __fdividef(g_min, 1.0f + __expf(-x)) : 0.f;
+                }
+#pragma unroll
+                for (int i = 1; i < 32; ++i) gv[i] += gv[i - 1];
+                if (r0 == 0) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) G[i * D + c] = gv[i];
+                }
+                csync();
+                if (r0 == 32) {
+                    const float base = G[31 * D + c];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) G[(32 + i) * D + c] = gv[i] + base;
+                }
+                csync();
+            }
+            // ---- phase 2a: per-(block, channel) factors
+            {
+                const int c = tid & 127;
+                if (tid < 128) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const float gp = G[(16 * b + 15) * D + c];
+                        FAC[(FAC_GPR + b) * D + c] = gp;
+                        FAC[(FAC_GPE + b) * D + c] = __expf(gp);
+                        FAC[(FAC_FL + b) * D + c] = __expf(G[63 * D + c] - gp);
+                    }
+                } else {
+#pragma unroll
+                    for (int b = 1; b < 4; ++b)
+#pragma unroll
+                        for (int bp = 0; bp < b; ++bp)
+                            FAC[(FAC_F + fpair(b, bp)) * D + c] =
+                                __expf(G[(16 * b + 15) * D + c] - G[(16 * bp + 15) * D + c]);
+                }
+                csync();
+            }
+            // ---- phase 2b: E in place of G; key-block images, Q^ and K~^T (packet)
+            {
+                const int rg = tid >> 5, c0 = (tid & 31) * 4, b = rg >> 1;
+                const bf16 *Q = reinterpret_cast<const bf16 *>(stg + I2_TQ);
+                const bf16 *K = reinterpret_cast<const bf16 *>(stg + I2_TK);
+                const float4 gp = *reinterpret_cast<const float4 *>(&FAC[(FAC_GPR + b) * D + c0]);
+                const float4 ge = *reinterpret_cast<const float4 *>(&FAC[(FAC_GPE + b) * D + c0]);
+                const float4 fl = *reinterpret_cast<const float4 *>(&FAC[(FAC_FL + b) * D + c0]);
+                const float gpv[4] = {gp.x, gp.y, gp.z, gp.w}, gev[4] = {ge.x, ge.y, ge.z, ge.w};
+                const float flv[4] = {fl.x, fl.y, fl.z, fl.w};
+                float kt[4][8];  // K~^T chunks: [channel][token]
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = rg * 8 + i;
+                    float kf[4], qf[4], Ev[4], kh[4], qh[4];
+                    unpack4(*reinterpret_cast<const uint2 *>(K + r * D + c0), kf);
+                    unpack4(*reinterpret_cast<const uint2 *>(Q + r * D + c0), qf);
+                    const float4 g4 = *reinterpret_cast<const float4 *>(&G[r * D + c0]);
+                    const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float d = gv[e] - gpv[e];
+                        const float E = __expf(d), Ei = __expf(-d);
+                        Ev[e] = E;
+                        kh[e] = kf[e] * Ei;
+                        qh[e] = qf[e] * E * gev[e];
+                        kt[e][i] = kf[e] * Ei * flv[e];
+                    }
+                    *reinterpret_cast<float4 *>(&G[r * D + c0]) = make_float4(Ev[0], Ev[1], Ev[2], Ev[3]);
+                    *reinterpret_cast<uint2 *>(sm + I2_KEY + b * 4096 + img_off(16, r & 15, c0)) = pack4(kh);
+                    *reinterpret_cast<uint2 *>(pk + PK_Q + img_off(64, r, c0)) = pack4(qh);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    *reinterpret_cast<uint4 *>(pk + PK_K + img_chunk_off(128, c0 + e, rg)) = pack8(kt[e]);
+                if (tid < 128) *reinterpret_cast<float *>(pk + PK_G + 4 * tid) = FAC[(FAC_GPE + 3) * D + tid];
+                if (tid == 0 && it > 0) bulk_wait_read0();  // previous item's W staging (row image A) was read
+                csync();
+            }
+            // ---- phase 3: row images for key block b' (rows r >= 16 b'), one MMA each.  Each thread
+            //      caches x_r e^{G_r - G_p(r)} for its 8 (side, row) items; block b' scales them by
+            //      e^{G_p(r) - G_p'}.  Rows r < 16 b' are left stale: every entry they produce lies above
+            //      the diagonal and is discarded by the causal mask.  Two image buffers alternate.
+            {
+                const int j = tid & 15, ri = tid >> 4, c0 = j * 8;
+                float xe[2][4][8];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int r = ri + 16 * m;
+                    float qf[8], kf[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(stg + I2_TQ + r * 256 + c0 * 2), qf);
+                    unpack8(*reinterpret_cast<const uint4 *>(stg + I2_TK + r * 256 + c0 * 2), kf);
+                    const float4 e0 = *reinterpret_cast<const float4 *>(&G[r * D + c0]);
+                    const float4 e1 = *reinterpret_cast<const float4 *>(&G[r * D + c0 + 4]);
+                    const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        xe[0][m][e] = qf[e] * ev[e];
+                        xe[1][m][e] = kf[e] * ev[e];
+                    }
+                }
+                csync();  // the Q tile (row image B) is about to be overwritten
+                const uint32_t idesc16 = idesc_bf16(128, 16);
+                auto build = [&](int bq, unsigned char *img) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        if (m < bq) continue;
+                        const int r = ri + 16 * m;
+                        float fv[8];
+                        if (m == bq) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) fv[e] = 1.f;
+                        } else {
+                            const float *F = &FAC[(FAC_F + fpair(m, bq)) * D + c0];
+                            const float4 f0 = *reinterpret_cast<const float4 *>(F);
+                            const float4 f1 = *reinterpret_cast<const float4 *>(F + 4);
+                            fv[0] = f0.x; fv[1] = f0.y; fv[2] = f0.z; fv[3] = f0.w;
+                            fv[4] = f1.x; fv[5] = f1.y; fv[6] = f1.z; fv[7] = f1.w;
+                        }
+#pragma unroll
+                        for (int side = 0; side < 2; ++side) {
+                            float o[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) o[e] = xe[side][m][e] * fv[e];
+                            *reinterpret_cast<uint4 *>(img + img_chunk_off(128, side * 64 + r, j)) = pack8(o);
+                        }
+                    }
+                };
+                unsigned char *imgA = sm + I2_ROW, *imgB = stg;
+#pragma unroll
+                for (int round = 0; round < 2; ++round) {
+                    if (round == 1) {  // both buffers are read by the first two MMAs
+                        const bool w0 = mbar_wait(&bar_mma[0], mph[0] & 1);
+                        const bool w1 = mbar_wait(&bar_mma[1], mph[1] & 1);
+                        ++mph[0];
+                        ++mph[1];
+                        ok = csync_and(ok && w0 && w1);
+                        fence_after_sync();
+                    }
+                    build(2 * round, imgA);
+                    build(2 * round + 1, imgB);
+                    fence_proxy_async();
+                    csync();
+                    if (ok && tid == 0) {
+                        mma_bf16_k(tb + 32 * round, smem_u32(imgA), 128, smem_u32(sm + I2_KEY + 2 * round * 4096),
+                                   16, 8, idesc16, false);
+                        mma_commit(&bar_mma[0]);
+                        mma_bf16_k(tb + 32 * round + 16, smem_u32(imgB), 128,
+                                   smem_u32(sm + I2_KEY + (2 * round + 1) * 4096), 16, 8, idesc16, false);
+                        mma_commit(&bar_mma[1]);
+                    }
+                }
+                const bool w0 = mbar_wait(&bar_mma[0], mph[0] & 1);
+                const bool w1 = mbar_wait(&bar_mma[1], mph[1] & 1);
+                ++mph[0];
+                ++mph[1];
+                ok = csync_and(ok && w0 && w1);
+                fence_after_sync();
+            }
+            if (!ok) break;
+            // ---- phase 4: A rows -> packet, L rows -> fp32 smem (warp w and w+4 split the 64 columns)
+            float *Lm = (float *)(sm + I2_L);
+            float *Tm = (float *)(sm + I2_T);
+            {
+                const int lq = warp & 3, cbase = (warp >> 2) * 32;
+                const int m = lq * 32 + lane;  // TMEM lane = row
+                float d[32];
+                tmem_ld32(tmem_addr(tb, lq * 32, cbase), d);
+                if (m < 64) {
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = (cbase + 8 * jj + e <= m) ? d[8 * jj + e] : 0.f;
+                        *reinterpret_cast<uint4 *>(pk + PK_A + img_chunk_off(64, m, cbase / 8 + jj)) = pack8(o);
+                    }
+                } else {
+                    const int r = m - 64;
+                    const float br = bet[r];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        float4 v4;
+                        v4.x = (cbase + i < r) ? br * d[i] : 0.f;
+                        v4.y = (cbase + i + 1 < r) ? br * d[i + 1] : 0.f;
+                        v4.z = (cbase + i + 2 < r) ? br * d[i + 2] : 0.f;
+                        v4.w = (cbase + i + 3 < r) ? br * d[i + 3] : 0.f;
+                        *reinterpret_cast<float4 *>(&Lm[r * LS + cbase + i]) = v4;
+                    }
+                }
+            }
+            csync();
+            // ---- phase 5 (warps 0-3: 16x16 diagonal blocks of (I + L)^{-1}) alongside
+            //      phase 6 (warps 4-7: (beta Gamma K)^T and (beta V)^T images in the stage)
+            if (warp < 4) {
+                if (lane < 16) {
+                    const int base = 16 * warp, c = lane;
+                    float x[16];
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) {
+                        float sacc = (r == c) ? 1.f : 0.f;
+#pragma unroll
+                        for (int i = 0; i < r; ++i) sacc -= Lm[(base + r) * LS + base + i] * x[i];
+                        x[r] = (r < c) ? 0.f : sacc;
+                    }
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) Tm[(base + r) * LS + base + c] = x[r];
+                }
+            } else {
+                const int u = tid - 128, rg = u >> 4, c0 = (u & 15) * 8, b = rg >> 1;
+                const float *gp = &FAC[(FAC_GPE + b) * D + c0];
+                const float4 g0 = *reinterpret_cast<const float4 *>(gp), g1 = *reinterpret_cast<const float4 *>(gp + 4);
+                const float gev[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                float xt[8][8], vt[8][8];  // [channel][token]
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = rg * 8 + i;
+                    float kf[8], vf[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(stg + I2_TK + r * 256 + c0 * 2), kf);
+                    unpack8(*reinterpret_cast<const uint4 *>(stg + I2_TV + r * 256 + c0 * 2), vf);
+                    const float4 e0 = *reinterpret_cast<const float4 *>(&G[r * D + c0]);
+                    const float4 e1 = *reinterpret_cast<const float4 *>(&G[r * D + c0 + 4]);
+                    const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+                    const float br = bet[r];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        xt[e][i] = br * kf[e] * ev[e] * gev[e];
+                        vt[e][i] = br * vf[e];
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    *reinterpret_cast<uint4 *>(stg + I2_XT + img_chunk_off(128, c0 + e, rg)) = pack8(xt[e]);
+                    *reinterpret_cast<uint4 *>(stg + I2_VT + img_chunk_off(128, c0 + e, rg)) = pack8(vt[e]);
+                }
+            }
+            csync();
+            // off-diagonal blocks, level d = i - j: P = sum_{m=j}^{i-1} L_im T_mj, then T_ij = -T_ii P.
+            // A thread owns 4 consecutive columns of one row of one block.
+            {
+                float *P = (float *)(sm + I2_P);
+#pragma unroll
+                for (int dlev = 1; dlev <= 3; ++dlev) {
+                    const int units = (4 - dlev) * 64;
+                    const int blk = tid >> 6, a = (tid >> 2) & 15, bq = (tid & 3) * 4;
+                    const int i = blk + dlev, jb = blk;
+                    if (tid < units) {
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float *Lrow = &Lm[(16 * i + a) * LS + 16 * jb];
+#pragma unroll 8
+                        for (int t = 0; t < 16 * dlev; ++t) {
+                            const float l = Lrow[t];
+                            const float4 tv = *reinterpret_cast<const float4 *>(&Tm[(16 * jb + t) * LS + 16 * jb + bq]);
+                            acc.x += l * tv.x; acc.y += l * tv.y; acc.z += l * tv.z; acc.w += l * tv.w;
+                        }
+                        *reinterpret_cast<float4 *>(&P[blk * 256 + a * 16 + bq]) = acc;
+                    }
+                    csync();
+                    if (tid < units) {
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float *Trow = &Tm[(16 * i + a) * LS + 16 * i];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            if (e <= a) {
+                                const float t = Trow[e];
+                                const float4 pv = *reinterpret_cast<const float4 *>(&P[blk * 256 + e * 16 + bq]);
+                                acc.x += t * pv.x; acc.y += t * pv.y; acc.z += t * pv.z; acc.w += t * pv.w;
+                            }
+                        }
+                        *reinterpret_cast<float4 *>(&Tm[(16 * i + a) * LS + 16 * jb + bq]) =
+                            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                    }
+                    csync();
+                }
+                for (int idx = tid; idx < 64 * 8; idx += NC2) {
+                    const int r = idx >> 3, jj = idx & 7;
+                    float o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = (8 * jj + e <= r) ? Tm[r * LS + 8 * jj + e] : 0.f;
+                    *reinterpret_cast<uint4 *>(sm + I2_TIMG + img_chunk_off(64, r, jj)) = pack8(o);
+                }
+            }
+            fence_proxy_async();
+            csync();
+            // ---- phase 7: W^T = X^T T^T (TMEM cols 64..127), U^T = (beta V)^T T^T (cols 128..191)
             if (tid == 0) {
-                mma_bf16_k(tb + 16 * b, smem_u32(sm + IS_ROW), 128, smem_u32(sm + IS_KEY + b * 4096), 16, 8,
-                           idesc16, false);
-                mma_commit(bar);
+                const uint32_t idesc64 = idesc_bf16(128, 64);
+                mma_bf16_k(tb + 64, smem_u32(stg + I2_XT), 128, smem_u32(sm + I2_TIMG), 64, 4, idesc64, false);
+                mma_bf16_k(tb + 128, smem_u32(stg + I2_VT), 128, smem_u32(sm + I2_TIMG), 64, 4, idesc64, false);
+                mma_commit(&bar_mma[0]);
             }
-            ok = wait_all(bar, mma_phase & 1);
-            ++mma_phase;
-        }
-        fence_after_sync();
-    }
-
-    // ---- phase 4: A rows (lanes 0..63) to the packet, L rows (lanes 64..127) to fp32 smem
-    float *Lm = (float *)(sm + IS_L);
-    float *Tm = (float *)(sm + IS_T);
-    if (ok) {
-        float d[64];
+            ok = cwait(&bar_mma[0], mph[0] & 1);
+            ++mph[0];
+            if (!ok) break;
+            fence_after_sync();
+            // ---- phase 8: W (through an smem image, one bulk store) and U^T rows to the packet
+            {
+                const int lq = warp & 3, rbase = (warp >> 2) * 32;
+                const int c = lq * 32 + lane;
+                float d[32];
+                tmem_ld32(tmem_addr(tb, lq * 32, 64 + rbase), d);
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tmem_addr(tb, warp * 32, c0), d + c0);
-        if (tid < 64) {
-            const int r = tid;
+                for (int i = 0; i < 32; ++i)
+                    *reinterpret_cast<bf16 *>(sm + I2_WST + img_off(64, rbase + i, c)) = __float2bfloat16_rn(d[i]);
+                tmem_ld32(tmem_addr(tb, lq * 32, 128 + rbase), d);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float o[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = (8 * j + e <= r) ? d[8 * j + e] : 0.f;
-                *reinterpret_cast<uint4 *>(pk + PK_A + img_chunk_off(64, r, j)) = pack8(o);
+                for (int jj = 0; jj < 4; ++jj)
+                    *reinterpret_cast<uint4 *>(pk + PK_U + c * 128 + rbase * 2 + jj * 16) = pack8(d + 8 * jj);
             }
-        } else {
-            const int r = tid - 64;
-            const float br = bet[r];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) Lm[r * 65 + i] = (i < r) ? br * d[i] : 0.f;
-        }
-    }
-    sync_all();
-
-    // ---- phase 5: T = (I + L)^{-1}, fp32.  Diagonal 16x16 blocks (warp w, lane = column) ...
-    if (ok) {
-        const int lane = tid & 31;
-        if (lane < 16) {
-            const int base = 16 * warp, c = lane;
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float s = (r == c) ? 1.f : 0.f;
-#pragma unroll
-                for (int i = 0; i < r; ++i) s -= Lm[(base + r) * 65 + base + i] * x[i];
-                x[r] = (r < c) ? 0.f : s;
+            fence_proxy_async();
+            csync();
+            if (tid == 0) {
+                bulk_s2g(pk + PK_W, sm + I2_WST, 16384);
+                bulk_commit();
+                mbar_arrive(&bar_free[s]);  // this stage may be refilled
             }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) Tm[(base + r) * 65 + base + c] = x[r];
         }
+        if (tid == 0) bulk_wait0();
+        if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     }
     __syncthreads();
-    // ... then off-diagonal blocks: T_ij = -T_ii sum_{m=j}^{i-1} L_im T_mj, level by level.
-    if (ok) {
-        float *P = (float *)(sm + IS_P);
-        for (int dlev = 1; dlev <= 3; ++dlev) {
-            const int nb = 4 - dlev;
-            for (int o = tid; o < nb * 256; o += NT) {
-                const int blk = o >> 8, a = (o >> 4) & 15, bb = o & 15;
-                const int i = blk + dlev, j = blk;
-                float s = 0.f;
-                for (int m = j; m < i; ++m)
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) s += Lm[(16 * i + a) * 65 + 16 * m + e] * Tm[(16 * m + e) * 65 + 16 * j + bb];
-                P[blk * 256 + a * 16 + bb] = s;
-            }
-            __syncthreads();
-            for (int o = tid; o < nb * 256; o += NT) {
-                const int blk = o >> 8, a = (o >> 4) & 15, bb = o & 15;
-                const int i = blk + dlev, j = blk;
-                float s = 0.f;
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    if (e <= a) s += Tm[(16 * i + a) * 65 + 16 * i + e] * P[blk * 256 + e * 16 + bb];
-                Tm[(16 * i + a) * 65 + 16 * j + bb] = -s;
-            }
-            __syncthreads();
-        }
-        // T image (64 rows r x 64 K = i), upper triangle zero
-        for (int idx = tid; idx < 64 * 8; idx += NT) {
-            const int r = idx >> 3, j = idx & 7;
-            float o[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = (8 * j + e <= r) ? Tm[r * 65 + 8 * j + e] : 0.f;
-            *reinterpret_cast<uint4 *>(sm + IS_TIMG + img_chunk_off(64, r, j)) = pack8(o);
-        }
-    }
-    fence_proxy_async();
-    sync_all();
-
-    // ---- phase 6: (beta Gamma K)^T and (beta V)^T images, K~^T image and gamma^C to the packet
-    {
-        const int c = tid;
-        const float Gl = G[(C - 1) * D + c];
-        *reinterpret_cast<float *>(pk + PK_G + 4 * c) = expf(Gl);
-        const bf16 *kc = kh + c;
-        const bf16 *vc = vh + c;
-#pragma unroll 1
-        for (int jr = 0; jr < 8; ++jr) {
-            float xo[8], vo[8], ko[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int r = 8 * jr + e;
-                const float kv = (r < len) ? __bfloat162float(kc[(int64_t)r * rowstride]) : 0.f;
-                const float vv = (r < len) ? __bfloat162float(vc[(int64_t)r * rowstride]) : 0.f;
-                const float Gr = G[r * D + c];
-                const float br = bet[r];
-                xo[e] = br * kv * __expf(Gr);
-                ko[e] = kv * __expf(Gl - Gr);
-                vo[e] = br * vv;
-            }
-            *reinterpret_cast<uint4 *>(sm + IS_XT + img_chunk_off(128, c, jr)) = pack8(xo);
-            *reinterpret_cast<uint4 *>(sm + IS_VT + img_chunk_off(128, c, jr)) = pack8(vo);
-            *reinterpret_cast<uint4 *>(pk + PK_K + img_chunk_off(128, c, jr)) = pack8(ko);
-        }
-    }
-    fence_proxy_async();
-    sync_all();
-
-    // ---- phase 7: W^T = X^T T^T (TMEM cols 64..127), U^T = (beta V)^T T^T (cols 128..191)
-    if (ok && tid == 0) {
-        const uint32_t idesc64 = idesc_bf16(128, 64);
-        mma_bf16_k(tb + 64, smem_u32(sm + IS_XT), 128, smem_u32(sm + IS_TIMG), 64, 4, idesc64, false);
-        mma_bf16_k(tb + 128, smem_u32(sm + IS_VT), 128, smem_u32(sm + IS_TIMG), 64, 4, idesc64, false);
-        mma_commit(bar);
-    }
-    if (ok) {
-        ok = wait_all(bar, mma_phase & 1);
-        ++mma_phase;
-    }
-    fence_after_sync();
-
-    // ---- phase 8: W (transposed through smem, bulk-stored) and U^T rows to the packet
-    if (ok) {
-        float d[64];
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tmem_addr(tb, warp * 32, 64 + c0), d + c0);
-        const int c = tid;
-#pragma unroll
-        for (int r = 0; r < 64; ++r)
-            *reinterpret_cast<bf16 *>(sm + IS_WST + img_off(64, r, c)) = __float2bfloat16_rn(d[r]);
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tmem_addr(tb, warp * 32, 128 + c0), d + c0);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4 *>(pk + PK_U + c * 128 + j * 16) = pack8(d + 8 * j);
-    }
-    fence_proxy_async();
-    sync_all();
-    if (ok && tid == 0) {
-        bulk_s2g(pk + PK_W, sm + IS_WST, 16384);
-        bulk_commit();
-        bulk_wait0();
-    }
-    if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
-    sync_all();
     if (warp == 0) tmem_dealloc(tb, 256);
 }
 
-// =====================================================================================
-__global__ void __launch_bounds__(NT, 1)
+constexpr int NT3 = 384;  // warps 0-7: state path; warps 8-11: output path
+// Warp roles.  Warps 0-7 carry the recurrence: per chunk V~ (after the V MMA), then the state
+// readout after the state MMA, writing the bf16 S^T image for the next chunk and the TMEM copy
+// scaled by the next chunk's gamma (warps w and w + 4 share TMEM lanes and split the columns).
+// Warps 8-11 move the outputs: after the output MMAs of chunk k complete they read O^T (double
+// buffered in TMEM), store it, and release the buffer and the packet stage.
+__global__ void __launch_bounds__(NT3, 1)
 chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
                       int H, const unsigned char *__restrict__ packets, float scale,
                       const float *initial_state, float *final_state, bf16 *__restrict__ o, int *err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1024(smem_raw);
     const int n = blockIdx.x / H, h = blockIdx.x % H;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    uint64_t *bar_ld = (uint64_t *)(sm + CS_BAR);      // [2]
-    uint64_t *bar_mma = (uint64_t *)(sm + CS_BAR + 16);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lq = warp & 3;
+    const int j = lq * 32 + lane;  // value channel = TMEM lane = S^T row
+    uint64_t *bar_ld = (uint64_t *)(sm + CS_BAR);             // [2] packet stage loaded
+    uint64_t *bar_v = bar_ld + 2, *bar_s = bar_ld + 3;        // V MMA, state MMA done
+    uint64_t *bar_o = bar_ld + 4;                             // [2] output MMAs of a chunk done
+    uint64_t *bar_free = bar_ld + 6;                          // [2] O buffer + packet stage released
     uint32_t *tslot = (uint32_t *)(sm + CS_TSLOT);
+    int *s_fail = (int *)(sm + CS_TSLOT + 8);
     const int c_begin = chunk_start[n], c_end = chunk_start[n + 1];
     const int nc = c_end - c_begin;
     const int64_t s_tok = cu ? (int64_t)cu[n] : (T / N) * n;
@@ -429,13 +665,19 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
     if (tid == 0) {
         mbar_init(&bar_ld[0], 1);
         mbar_init(&bar_ld[1], 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_v, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(&bar_o[0], 1);
+        mbar_init(&bar_o[1], 1);
+        mbar_init(&bar_free[0], 128);
+        mbar_init(&bar_free[1], 128);
+        *s_fail = 0;
     }
-    if (warp == 0) tmem_alloc(tslot, 256);
+    if (warp == 0) tmem_alloc(tslot, 512);
     fence_proxy_async();  // barrier init visible to the async proxy
     sync_all();
     const uint32_t tb = *tslot;
-    const uint32_t tS = tb, tV = tb + 128, tO = tb + 192;  // S^T: 128 cols, V~^T: 64, O^T: 64
+    const uint32_t tS = tb, tV = tb + 128, tO0 = tb + 192;  // S^T 128 cols, V~^T 64, O^T 2 x 64
     auto packet = [&](int kk) { return packets + ((size_t)(c_begin + kk) * H + h) * PK_STRIDE; };
     if (tid == 0) {
         for (int kk = 0; kk < 2 && kk < nc; ++kk) {
@@ -443,128 +685,145 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
             bulk_g2s(sm + (kk ? CS_STAGE1 : CS_STAGE0), packet(kk), PK_BYTES, &bar_ld[kk]);
         }
     }
-    // initial state: thread j owns S^T row j (value channel j)
-    const int j = tid;
-    {
-        float s[16];
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 16) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                s[e] = initial_state ? initial_state[st_off + (size_t)(c0 + e) * D + j] : 0.f;
-            tmem_st16(tmem_addr(tS, warp * 32, c0), s);
-            *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, c0 / 8)) = pack8(s);
-            *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(s + 8);
-        }
-        tmem_st_wait();
-    }
-    fence_proxy_async();
-    sync_all();
 
-    const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128);
-    uint32_t mph = 0;
-    bool ok = true;
-    for (int kk = 0; kk < nc && ok; ++kk) {
-        const int stage = kk & 1;
-        unsigned char *P = sm + (stage ? CS_STAGE1 : CS_STAGE0);
-        const int64_t t0 = s_tok + (int64_t)kk * C;
-        const int len = (int)min((int64_t)C, e_tok - t0);
-        ok = wait_all(&bar_ld[stage], (kk >> 1) & 1);
-        if (!ok) break;
-        fence_after_sync();
-        if (tid == 0) {
-            mma_bf16_k(tV, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_W), 64, 8, id64, false);
-            mma_bf16_k(tO, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_Q), 64, 8, id64, false);
-            mma_commit(bar_mma);
-        }
-        // S^T <- S^T Diag(gamma^C) (column c scaled by gamma_c), overlapping the MMAs above
-        {
-            const float *gam = (const float *)(P + PK_G);
-            float s[16];
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 16) {
-                tmem_ld16(tmem_addr(tS, warp * 32, c0), s);
+    if (warp >= 8) {
+        // ------------------------------------------------ output path (128 threads)
+        const int ot = tid - 256;
+        bool ok = true;
+        for (int kk = 0; kk < nc; ++kk) {
+            ok = ok && mbar_wait(&bar_o[kk & 1], (kk >> 1) & 1);
+            if (!ok) break;
+            fence_after_sync();
+            // every MMA of chunk kk has completed: packet stage kk & 1 can take chunk kk + 2
+            if (ot == 0 && kk + 2 < nc) {
+                mbar_arrive_expect_tx(&bar_ld[kk & 1], PK_BYTES);
+                bulk_g2s(sm + ((kk & 1) ? CS_STAGE1 : CS_STAGE0), packet(kk + 2), PK_BYTES, &bar_ld[kk & 1]);
+            }
+            const int64_t tp = s_tok + (int64_t)kk * C;
+            const int lenp = (int)min((int64_t)C, e_tok - tp);
+            bf16 *oj = o + (tp * H + h) * D + j;
+            const uint32_t tO = tO0 + 64 * (kk & 1);
+            float d[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) s[e] *= gam[c0 + e];
-                tmem_st16(tmem_addr(tS, warp * 32, c0), s);
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                tmem_ld32(tmem_addr(tO, lq * 32, c0), d);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (c0 + e < lenp) oj[(int64_t)(c0 + e) * H * D] = __float2bfloat16_rn(scale * d[e]);
+            }
+            fence_before_sync();
+            mbar_arrive(&bar_free[kk & 1]);  // O buffer kk & 1 may be overwritten
+        }
+        if (!ok) atomicExch(s_fail, 1);
+    } else {
+        // ------------------------------------------------ state path (256 threads)
+        const int hf = warp >> 2;  // column half
+        bool ok = true;
+        float sreg[64];
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+            sreg[e] = initial_state ? initial_state[st_off + (size_t)(64 * hf + e) * D + j] : 0.f;
+        if (nc > 0) ok = mbar_wait(&bar_ld[0], 0);
+        ok = (__syncthreads_count_named1(ok) == 256);
+        if (ok && nc > 0) {  // S_0 image; TMEM gets S_0 Diag(gamma_0)
+            const float *gam = (const float *)(sm + CS_STAGE0 + PK_G);
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 8)
+                *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, (64 * hf + c0) / 8)) = pack8(sreg + c0);
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                float sc[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) sc[e] = sreg[c0 + e] * gam[64 * hf + c0 + e];
+                tmem_st16(tmem_addr(tS, lq * 32, 64 * hf + c0), sc);
             }
             tmem_st_wait();
         }
-        ok = wait_all(bar_mma, mph & 1);
-        ++mph;
-        if (!ok) break;
+        fence_proxy_async();
+        fence_before_sync();
+        named_sync(1, 256);
         fence_after_sync();
-        // V~^T row j = U^T row j - (S^T W^T) row j, to the bf16 operand image
-        {
-            const uint4 *urow = reinterpret_cast<const uint4 *>(P + PK_U + j * 128);
-            float dv[16], u[8], vo[8];
-#pragma unroll 1
-            for (int c0 = 0; c0 < 64; c0 += 16) {
-                tmem_ld16(tmem_addr(tV, warp * 32, c0), dv);
+        const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128);
+        for (int kk = 0; kk < nc && ok; ++kk) {
+            // invariant: packet kk resident; S^T image = bf16(S_kk); TMEM S^T = S_kk^T Diag(gamma_kk)
+            unsigned char *P = sm + ((kk & 1) ? CS_STAGE1 : CS_STAGE0);
+            const uint32_t tO = tO0 + 64 * (kk & 1);
+            if (tid == 0) {
+                mma_bf16_k(tV, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_W), 64, 8, id64, false);
+                mma_commit(bar_v);
+                // O buffer kk & 1 was last read for chunk kk - 2
+                bool fr = (kk < 2) || mbar_wait(&bar_free[kk & 1], ((kk >> 1) - 1) & 1);
+                if (!fr) atomicExch(s_fail, 1);
+                fence_after_sync();
+                mma_bf16_k(tO, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_Q), 64, 8, id64, false);
+            }
+            ok = mbar_wait(bar_v, kk & 1);
+            ok = (__syncthreads_count_named1(ok) == 256) && (*(volatile int *)s_fail == 0);
+            if (!ok) break;
+            fence_after_sync();
+            // V~^T row j = U^T row j - (S^T W^T) row j, columns [32 hf, 32 hf + 32)
+            {
+                const uint4 *urow = reinterpret_cast<const uint4 *>(P + PK_U + j * 128);
+                float dv[32], u[8], vo[8];
+                tmem_ld32(tmem_addr(tV, lq * 32, 32 * hf), dv);
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    unpack8(urow[c0 / 8 + hh], u);
+                for (int hh = 0; hh < 4; ++hh) {
+                    unpack8(urow[4 * hf + hh], u);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) vo[e] = u[e] - dv[8 * hh + e];
-                    *reinterpret_cast<uint4 *>(sm + CS_VIMG + img_chunk_off(128, j, c0 / 8 + hh)) = pack8(vo);
+                    *reinterpret_cast<uint4 *>(sm + CS_VIMG + img_chunk_off(128, j, 4 * hf + hh)) = pack8(vo);
                 }
             }
-        }
-        fence_proxy_async();
-        sync_all();
-        if (tid == 0) {
-            mma_bf16_k(tS, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_K), 128, 4, id128, true);
-            mma_bf16_k(tO, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_A), 64, 4, id64, true);
-            mma_commit(bar_mma);
-        }
-        ok = wait_all(bar_mma, mph & 1);
-        ++mph;
-        if (!ok) break;
-        fence_after_sync();
-        // this stage is free again: prefetch chunk kk + 2 into it
-        if (tid == 0 && kk + 2 < nc) {
-            mbar_arrive_expect_tx(&bar_ld[stage], PK_BYTES);
-            bulk_g2s(P, packet(kk + 2), PK_BYTES, &bar_ld[stage]);
-        }
-        // outputs O^T row j -> o[t0 + r, h, j]
-        {
-            float d[16];
-            bf16 *oj = o + (t0 * H + h) * D + j;
-#pragma unroll 1
-            for (int c0 = 0; c0 < 64; c0 += 16) {
-                tmem_ld16(tmem_addr(tO, warp * 32, c0), d);
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    if (c0 + e < len) oj[(int64_t)(c0 + e) * H * D] = __float2bfloat16_rn(scale * d[e]);
+            fence_proxy_async();
+            fence_before_sync();
+            named_sync(1, 256);
+            fence_after_sync();
+            if (tid == 0) {
+                mma_bf16_k(tS, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_K), 128, 4, id128, true);
+                mma_commit(bar_s);
+                mma_bf16_k(tO, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_A), 64, 4, id64, true);
+                mma_commit(&bar_o[kk & 1]);
             }
-        }
-        // new state: bf16 operand image for the next chunk, or the final state
-        {
-            float s[16];
             const bool last = (kk == nc - 1);
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 16) {
-                tmem_ld16(tmem_addr(tS, warp * 32, c0), s);
-                if (last) {
-                    if (final_state)
+            bool okl = true;
+            if (!last) okl = mbar_wait(&bar_ld[(kk + 1) & 1], ((kk + 1) >> 1) & 1);
+            ok = mbar_wait(bar_s, kk & 1) && okl;
+            ok = (__syncthreads_count_named1(ok) == 256);
+            if (!ok) break;
+            fence_after_sync();
+            // S_{kk+1}: bf16 image and TMEM copy scaled by gamma_{kk+1} (or kept for the final state)
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) final_state[st_off + (size_t)(c0 + e) * D + j] = s[e];
-                } else {
-                    *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, c0 / 8)) = pack8(s);
-                    *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(s + 8);
+            for (int c0 = 0; c0 < 64; c0 += 32) tmem_ld32(tmem_addr(tS, lq * 32, 64 * hf + c0), sreg + c0);
+            if (!last) {
+                const float *gam = (const float *)(sm + (((kk + 1) & 1) ? CS_STAGE1 : CS_STAGE0) + PK_G);
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 8)
+                    *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, (64 * hf + c0) / 8)) =
+                        pack8(sreg + c0);
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 16) {
+                    float sc[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) sc[e] = sreg[c0 + e] * gam[64 * hf + c0 + e];
+                    tmem_st16(tmem_addr(tS, lq * 32, 64 * hf + c0), sc);
                 }
+                tmem_st_wait();
             }
+            fence_proxy_async();
+            fence_before_sync();
+            named_sync(1, 256);
+            fence_after_sync();
         }
-        fence_proxy_async();
-        sync_all();
+        if (ok && final_state) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) final_state[st_off + (size_t)(64 * hf + e) * D + j] = sreg[e];
+        }
+        if (!ok) atomicExch(s_fail, 1);
     }
-    if (ok && nc == 0 && final_state) {
-        for (int c = 0; c < D; ++c)
-            final_state[st_off + (size_t)c * D + j] = initial_state ? initial_state[st_off + (size_t)c * D + j] : 0.f;
-    }
-    if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
+    __syncthreads();
+    if (tid == 0 && *(volatile int *)s_fail) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     sync_all();
-    if (warp == 0) tmem_dealloc(tb, 256);
+    if (warp == 0) tmem_dealloc(tb, 512);
 }
 
 }  // namespace tcp
@@ -576,6 +835,38 @@ size_t kda_tc_packet_stride() { return tcp::PK_STRIDE; }
 
 kda_status_t kda_launch_chunk_plan(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
                                    cudaStream_t stream);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda dependency).
+typedef CUresult (*encode_tiled_fn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                    CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                    CUtensorMapFloatOOBfill);
+
+static encode_tiled_fn get_encode_tiled() {
+    static encode_tiled_fn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (encode_tiled_fn)p;
+    }
+    return fn;
+}
+
+// [T, H, 128] bf16 as a 3-D map (channel, head, token) with 128 x 1 x 64 boxes, no swizzle.
+static bool make_tile_map(CUtensorMap *m, const void *base, int64_t T, int H) {
+    encode_tiled_fn enc = get_encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)H * 256};
+    const cuuint32_t box[3] = {128, 1, 64};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
                                  cudaStream_t stream) {
@@ -589,18 +880,25 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     unsigned char *packets = (unsigned char *)ws + p.off_records;
     if (p.max_chunks > 0 && a->T > 0) {
         cudaFuncSetAttribute(tcp::chunk_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tcp::IS_TOTAL);
-        dim3 grid((unsigned)p.max_chunks, (unsigned)p.H);
-        tcp::chunk_intra_tc_kernel<<<grid, tcp::NT, tcp::IS_TOTAL, stream>>>(
-            (const bf16 *)a->q, (const bf16 *)a->k, (const bf16 *)a->v, (const bf16 *)a->z,
-            (const bf16 *)a->beta, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
+                             (int)tcp::I2_TOTAL);
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int64_t items = p.max_chunks * (int64_t)p.H;
+        const unsigned grid = (unsigned)(items < sms ? items : sms);
+        tcp::TileMaps tm;
+        if (!make_tile_map(&tm.q, a->q, a->T, p.H) || !make_tile_map(&tm.k, a->k, a->T, p.H) ||
+            !make_tile_map(&tm.v, a->v, a->T, p.H) || !make_tile_map(&tm.z, a->z, a->T, p.H))
+            return KDA_ERR_CUDA;
+        tcp::chunk_intra_tc_kernel<<<grid, tcp::NT2, tcp::I2_TOTAL, stream>>>(
+            tm, (const bf16 *)a->beta, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
             chunk_start, p.H, packets, err);
         if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     }
     kda_profile_mark(2, stream);
     cudaFuncSetAttribute(tcp::chunk_inter_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)tcp::CS_TOTAL);
-    tcp::chunk_inter_tc_kernel<<<(unsigned)(a->N * p.H), tcp::NT, tcp::CS_TOTAL, stream>>>(
+    tcp::chunk_inter_tc_kernel<<<(unsigned)(a->N * p.H), tcp::NT3, tcp::CS_TOTAL, stream>>>(
         a->T, (int)a->N, a->cu_seqlens, chunk_start, p.H, packets, a->scale, a->initial_state,
         a->final_state, (bf16 *)a->o, err);
     kda_profile_mark(3, stream);
