@@ -253,7 +253,7 @@ def run_ours(args, rank, ws, local):
         kda.chunk_fwd(q, k, v, z, beta, b, a, g_min=d["g_min"], scale=d["scale"], cu_seqlens=d["cu_seqlens"],
                       cu_seqlens_host=cu_host, final_state=fs, workspace=work, out=o)
 
-    nk = kda.chunk_fwd_kernel_count()
+    nk = kda.chunk_fwd_kernel_count(T, N, H, D, D, q.dtype, cu_host)
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -286,9 +286,10 @@ def run_ours(args, rank, ws, local):
     by = prefill_bytes(T, N, H, D, D, 2, False, True)
     tflops = fl["total"] / (ms / 1e3) / 1e12
     kern_avg = [sum(x) / len(x) for x in kern_ms]
-    names = ["chunk_plan", "chunk_intra", "chunk_inter"][:nk]
+    names = (["chunk_plan", "chunk_intra", "chunk_inter"] if nk == 3 else
+             ["chunk_plan", "chunk_intra", "chunk_segsum", "chunk_fold", "chunk_inter"])
     dom = max(range(nk), key=lambda j: kern_avg[j])
-    role = {"chunk_intra": "intra", "chunk_inter": "inter"}.get(names[dom], "intra")
+    role = {"chunk_intra": "intra"}.get(names[dom], "inter")
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     tc = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     bytes_dom, flops_dom = by[role], fl[role]

@@ -69,7 +69,12 @@ kda_status_t kda_set_profile_events(void *const *events, int32_t n_events) {
 
 int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
     if (!a) return 0;
-    return 3;  // chunk plan, intra-chunk transform, inter-chunk state/output pass
+    kda_chunk_plan p;
+    if (!kda_make_chunk_plan(a->T, a->N > 0 ? a->N : 1, a->H > 0 ? a->H : 1, a->dk, a->dv, a->dtype, 64, &p,
+                             a->cu_seqlens_host))
+        return 0;
+    // chunk plan, intra-chunk transform, [segment summaries, fold,] state/output pass
+    return p.split ? 5 : 3;
 }
 
 const char *kda_status_string(kda_status_t s) {
@@ -160,7 +165,7 @@ size_t kda_chunk_fwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk,
     if (dk != dv || (dk != 64 && dk != 128)) return 0;
     if (chunk_size != 0 && chunk_size != 64) return 0;
     kda_chunk_plan p;
-    if (!kda_make_chunk_plan(T, N, H, dk, dv, dtype, 64, &p)) return 0;
+    if (!kda_make_chunk_plan(T, N, H, dk, dv, dtype, 64, &p, cu_seqlens_host)) return 0;
     return p.total_bytes;
 }
 
@@ -169,7 +174,7 @@ kda_status_t kda_chunk_fwd(const kda_chunk_args *a, void *workspace, size_t work
     kda_status_t st = validate_chunk(a);
     if (st != KDA_OK) return st;
     kda_chunk_plan p;
-    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p))
+    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p, a->cu_seqlens_host))
         return KDA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < p.total_bytes) return KDA_ERR_WORKSPACE;
     if (!aligned_to(workspace, 256)) return KDA_ERR_MISALIGNED;

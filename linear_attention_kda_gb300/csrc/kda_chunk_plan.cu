@@ -14,7 +14,8 @@ namespace kda {
 
 __global__ void __launch_bounds__(1024)
 chunk_plan_kernel(const int32_t *__restrict__ cu, int64_t T, int N, int C,
-                  int32_t *__restrict__ chunk_start, int *err) {
+                  int32_t *__restrict__ chunk_start, int64_t seg_len, int32_t *__restrict__ seg_start,
+                  int *err) {
     __shared__ int s_bad;
     __shared__ int s_warp[32];
     __shared__ int s_carry;
@@ -31,7 +32,10 @@ chunk_plan_kernel(const int32_t *__restrict__ cu, int64_t T, int N, int C,
     __syncthreads();
     if (s_bad) {
         if (tid == 0) set_error(err, KDA_ERR_BAD_SEQLENS);
-        for (int n = tid; n <= N; n += blockDim.x) chunk_start[n] = 0;  // no chunk runs
+        for (int n = tid; n <= N; n += blockDim.x) {
+            chunk_start[n] = 0;  // no chunk runs
+            if (seg_start) seg_start[n] = 0;
+        }
         return;
     }
     const int64_t len_eq = cu ? 0 : T / N;
@@ -67,14 +71,92 @@ chunk_plan_kernel(const int32_t *__restrict__ cu, int64_t T, int N, int C,
         __syncthreads();
     }
     if (tid == 0) chunk_start[0] = 0;
+    if (!seg_start) return;
+    // segments per sequence: max(1, ceil(chunks / seg_len)) (an empty sequence keeps one segment,
+    // which writes its final state)
+    __syncthreads();
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    for (int base = 0; base < N; base += blockDim.x) {
+        const int n = base + tid;
+        int cnt = 0;
+        if (n < N) {
+            const int64_t nc = (int64_t)chunk_start[n + 1] - chunk_start[n];
+            cnt = (int)max((int64_t)1, (nc + seg_len - 1) / seg_len);
+        }
+        int x = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) s_warp[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = (lane < (int)(blockDim.x >> 5)) ? s_warp[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += y;
+            }
+            s_warp[lane] = w;
+        }
+        __syncthreads();
+        const int incl = x + (warp > 0 ? s_warp[warp - 1] : 0) + s_carry;
+        if (n < N) seg_start[n + 1] = incl;
+        __syncthreads();
+        if (tid == blockDim.x - 1) s_carry = incl;
+        __syncthreads();
+    }
+    if (tid == 0) seg_start[0] = 0;
 }
 
 }  // namespace kda
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Segment length of the split-sequence state pass, from a latency model of the tensor-core
+// kernels: a chain step costs t, a summary step 1.3 t (two states), a fold step ~1 t; one CTA per
+// SM.  Candidate lengths are compared with the unsplit pass; splitting is used only if it wins by
+// more than 15 %.  Uses per-sequence lengths when the host copy of cu_seqlens is given.
+static int64_t choose_seg_len(int64_t T, int64_t N, int H, int C, const int32_t *cu_host, int sms) {
+    if (T == 0) return 1 << 30;
+    int64_t total = 0, longest = 0;
+    auto chunks_of = [&](int64_t n) -> int64_t {
+        const int64_t len = cu_host ? (int64_t)cu_host[n + 1] - cu_host[n] : T / N;
+        return (len + C - 1) / C;
+    };
+    for (int64_t n = 0; n < N; ++n) {
+        const int64_t c = chunks_of(n);
+        total += c;
+        longest = c > longest ? c : longest;
+    }
+    auto waves = [&](int64_t ctas) { return (double)((ctas + sms - 1) / sms); };
+    const double unsplit = (double)longest > (double)total * H / sms ? (double)longest
+                                                                      : (double)total * H / sms;
+    double best = unsplit * 0.85;
+    int64_t best_len = 1 << 30;
+    for (int64_t L = 8; L <= (1 << 14); L *= 2) {
+        if (L >= longest) break;
+        int64_t segs = 0, segs_sum = 0, max_nseg = 0;
+        for (int64_t n = 0; n < N; ++n) {
+            const int64_t c = chunks_of(n);
+            const int64_t ns = c > 0 ? (c + L - 1) / L : 1;
+            segs += ns;
+            segs_sum += ns - 1;
+            max_nseg = ns > max_nseg ? ns : max_nseg;
+        }
+        const double cost = 1.3 * L * waves(segs_sum * H) + 1.0 * (max_nseg - 1) + L * waves(segs * H) + 8.0;
+        if (cost < best) {
+            best = cost;
+            best_len = L;
+        }
+    }
+    return best_len;
+}
+
 bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_t dtype, int C,
-                         kda_chunk_plan *p) {
+                         kda_chunk_plan *p, const int32_t *cu_seqlens_host) {
     if (T < 0 || N < 1 || H < 1 || C < 1) return false;
     p->T = T; p->N = N; p->H = H; p->dk = dk; p->dv = dv; p->C = C;
     p->max_chunks = (T + N * (int64_t)(C - 1)) / C;
@@ -88,7 +170,27 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
     }
     p->off_chunk_start = 0;
     p->off_records = align_up(sizeof(int32_t) * (size_t)(N + 1), 256);
-    p->total_bytes = p->off_records + p->record_bytes * (size_t)p->max_chunks * (size_t)H;
+    size_t end = p->off_records + p->record_bytes * (size_t)p->max_chunks * (size_t)H;
+    p->split = 0;
+    p->seg_len = (int64_t)1 << 30;
+    p->max_segs = N;
+    if (p->path == 1) {
+        int dev = 0, sms = 152;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 152;
+        p->seg_len = choose_seg_len(T, N, H, C, cu_seqlens_host, sms);
+        p->split = p->seg_len < ((int64_t)1 << 30) ? 1 : 0;
+        p->max_segs = p->split ? p->max_chunks / p->seg_len + N : N;
+    }
+    p->off_seg_start = align_up(end, 256);
+    end = p->off_seg_start + sizeof(int32_t) * (size_t)(N + 1);
+    p->off_seg_sum = align_up(end, 1024);
+    p->off_seg_in = p->off_seg_sum;
+    if (p->split) {
+        p->off_seg_in = p->off_seg_sum + (size_t)p->max_segs * H * 2 * 128 * 128 * sizeof(float);
+        end = p->off_seg_in + (size_t)p->max_segs * H * 128 * 128 * sizeof(float);
+    }
+    p->total_bytes = align_up(end, 256);
     return true;
 }
 
@@ -97,6 +199,8 @@ kda_status_t kda_launch_chunk_plan(const kda_chunk_args *a, const kda_chunk_plan
     int *err = kda_device_error_ptr();
     if (!err) return KDA_ERR_CUDA;
     int32_t *chunk_start = (int32_t *)((char *)ws + p.off_chunk_start);
-    kda::chunk_plan_kernel<<<1, 1024, 0, stream>>>(a->cu_seqlens, a->T, (int)a->N, p.C, chunk_start, err);
+    int32_t *seg_start = p.path == 1 ? (int32_t *)((char *)ws + p.off_seg_start) : nullptr;
+    kda::chunk_plan_kernel<<<1, 1024, 0, stream>>>(a->cu_seqlens, a->T, (int)a->N, p.C, chunk_start,
+                                                    p.seg_len, seg_start, err);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

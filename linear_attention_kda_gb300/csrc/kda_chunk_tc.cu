@@ -642,11 +642,25 @@ constexpr int NT3 = 384;  // warps 0-7: state path; warps 8-11: output path
 // buffered in TMEM), store it, and release the buffer and the packet stage.
 __global__ void __launch_bounds__(NT3, 1)
 chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
+                      const int32_t *__restrict__ seg_start, int64_t seg_len, const float *__restrict__ seg_in,
                       int H, const unsigned char *__restrict__ packets, float scale,
                       const float *initial_state, float *final_state, bf16 *__restrict__ o, int *err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1024(smem_raw);
-    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    // segment g of sequence n, head h: chunks [kk0, kk0 + nc) of the sequence
+    const int g = blockIdx.x, h = blockIdx.y;
+    if (g >= seg_start[N]) return;
+    int n = 0;
+    {
+        int lo = 0, hi = N;  // largest n with seg_start[n] <= g
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (seg_start[mid] <= g) lo = mid; else hi = mid;
+        }
+        n = lo;
+    }
+    const int seg_i = g - seg_start[n], nseg = seg_start[n + 1] - seg_start[n];
+    const bool last_seg = (seg_i == nseg - 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lq = warp & 3;
     const int j = lq * 32 + lane;  // value channel = TMEM lane = S^T row
@@ -656,11 +670,16 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
     uint64_t *bar_free = bar_ld + 6;                          // [2] O buffer + packet stage released
     uint32_t *tslot = (uint32_t *)(sm + CS_TSLOT);
     int *s_fail = (int *)(sm + CS_TSLOT + 8);
-    const int c_begin = chunk_start[n], c_end = chunk_start[n + 1];
-    const int nc = c_end - c_begin;
-    const int64_t s_tok = cu ? (int64_t)cu[n] : (T / N) * n;
-    const int64_t e_tok = cu ? (int64_t)cu[n + 1] : s_tok + T / N;
+    const int64_t kk0 = (int64_t)seg_i * seg_len;
+    const int nc_seq = chunk_start[n + 1] - chunk_start[n];
+    const int c_begin = chunk_start[n] + (int)kk0;
+    const int nc = (int)max((int64_t)0, min(seg_len, (int64_t)nc_seq - kk0));
+    const int64_t s_tok = (cu ? (int64_t)cu[n] : (T / N) * n) + kk0 * C;
+    const int64_t e_tok = cu ? (int64_t)cu[n + 1] : (T / N) * (n + 1);
     const size_t st_off = ((size_t)n * H + h) * D * D;
+    // entering state: the sequence's initial state for a lone segment; otherwise the fold's output
+    // (segment 0 included), so that final_state may alias initial_state
+    const float *s_in = (nseg > 1) ? seg_in + ((size_t)g * H + h) * D * D : nullptr;  // S^T rows
 
     if (tid == 0) {
         mbar_init(&bar_ld[0], 1);
@@ -720,9 +739,17 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
         const int hf = warp >> 2;  // column half
         bool ok = true;
         float sreg[64];
+        if (s_in) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e)
-            sreg[e] = initial_state ? initial_state[st_off + (size_t)(64 * hf + e) * D + j] : 0.f;
+            for (int e = 0; e < 64; e += 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(s_in + (size_t)j * D + 64 * hf + e);
+                sreg[e] = v4.x; sreg[e + 1] = v4.y; sreg[e + 2] = v4.z; sreg[e + 3] = v4.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+                sreg[e] = initial_state ? initial_state[st_off + (size_t)(64 * hf + e) * D + j] : 0.f;
+        }
         if (nc > 0) ok = mbar_wait(&bar_ld[0], 0);
         ok = (__syncthreads_count_named1(ok) == 256);
         if (ok && nc > 0) {  // S_0 image; TMEM gets S_0 Diag(gamma_0)
@@ -814,7 +841,7 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
             named_sync(1, 256);
             fence_after_sync();
         }
-        if (ok && final_state) {
+        if (ok && final_state && last_seg) {
 #pragma unroll
             for (int e = 0; e < 64; ++e) final_state[st_off + (size_t)(64 * hf + e) * D + j] = sreg[e];
         }
@@ -824,6 +851,287 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
     if (tid == 0 && *(volatile int *)s_fail) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     sync_all();
     if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+
+// =====================================================================================
+// Segment summaries (section 5.1.2, Eq. 17, used inside one device): for every segment but
+// the last of its sequence, run the state recurrence over the segment's chunks on the pair
+// [S~ | M] from [0 | I]: S~ with the segment's values, M with values zero.  Then for any
+// entering state, S_out = M S_in + S~.  Both are kept transposed in TMEM exactly like the
+// state of the output pass; Q^ and A are not needed, so a compact packet stage is loaded.
+constexpr uint32_t SS_STAGE_BYTES = 50176;
+constexpr uint32_t SS_W = 0, SS_K = 16384, SS_U = 32768, SS_G = 49152;
+constexpr uint32_t SS_SIMG = 2 * SS_STAGE_BYTES;       // S~^T image 128 x 128
+constexpr uint32_t SS_MIMG = SS_SIMG + 32768;          // M^T image
+constexpr uint32_t SS_VSIMG = SS_MIMG + 32768;         // V~_S^T image 128 x 64
+constexpr uint32_t SS_VMIMG = SS_VSIMG + 16384;        // V~_M^T image
+constexpr uint32_t SS_BAR = SS_VMIMG + 16384;
+constexpr uint32_t SS_TSLOT = SS_BAR + 64;
+constexpr uint32_t SS_TOTAL = SS_BAR + 128 + 1024;
+constexpr uint32_t SS_TX = 16384 + 16384 + 16896;
+
+__global__ void __launch_bounds__(256, 1)
+chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int32_t *__restrict__ seg_start,
+                       int64_t seg_len, int H, const unsigned char *__restrict__ packets,
+                       float *__restrict__ seg_sum, int *err) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = align1024(smem_raw);
+    const int g = blockIdx.x, h = blockIdx.y;
+    if (g >= seg_start[N]) return;
+    int n = 0;
+    {
+        int lo = 0, hi = N;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (seg_start[mid] <= g) lo = mid; else hi = mid;
+        }
+        n = lo;
+    }
+    const int seg_i = g - seg_start[n], nseg = seg_start[n + 1] - seg_start[n];
+    if (seg_i == nseg - 1) return;  // the last segment of a sequence needs no summary
+    const int64_t kk0 = (int64_t)seg_i * seg_len;
+    const int c_begin = chunk_start[n] + (int)kk0;
+    const int nc = (int)min(seg_len, (int64_t)(chunk_start[n + 1] - chunk_start[n]) - kk0);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lq = warp & 3, hf = warp >> 2;
+    const int j = lq * 32 + lane;
+    uint64_t *bar_ld = (uint64_t *)(sm + SS_BAR);
+    uint64_t *bar_v = bar_ld + 2, *bar_s = bar_ld + 3;
+    uint32_t *tslot = (uint32_t *)(sm + SS_TSLOT);
+    if (tid == 0) {
+        mbar_init(&bar_ld[0], 1);
+        mbar_init(&bar_ld[1], 1);
+        mbar_init(bar_v, 1);
+        mbar_init(bar_s, 1);
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    fence_proxy_async();
+    sync_all();
+    const uint32_t tb = *tslot;
+    const uint32_t tSt = tb, tMt = tb + 128, tVS = tb + 256, tVM = tb + 320;
+    auto issue = [&](int kk, int st) {
+        const unsigned char *pk = packets + ((size_t)(c_begin + kk) * H + h) * PK_STRIDE;
+        unsigned char *dst = sm + st * SS_STAGE_BYTES;
+        mbar_arrive_expect_tx(&bar_ld[st], SS_TX);
+        bulk_g2s(dst + SS_W, pk + PK_W, 16384, &bar_ld[st]);
+        bulk_g2s(dst + SS_K, pk + PK_K, 16384, &bar_ld[st]);
+        bulk_g2s(dst + SS_U, pk + PK_U, 16896, &bar_ld[st]);
+    };
+    if (tid == 0) {
+        issue(0, 0);
+        if (nc > 1) issue(1, 1);
+    }
+    bool ok = wait_all(&bar_ld[0], 0);
+    fence_after_sync();
+    if (ok) {  // [S~ | M] = [0 | I]; TMEM copies scaled by gamma_0 (column scale)
+        const float *gam = (const float *)(sm + SS_G);
+#pragma unroll
+        for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 16) {
+            float z16[16], m16[16], ms[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                z16[e] = 0.f;
+                m16[e] = (c0 + e == j) ? 1.f : 0.f;
+                ms[e] = m16[e] * gam[c0 + e];
+            }
+            tmem_st16(tmem_addr(tSt, lq * 32, c0), z16);
+            tmem_st16(tmem_addr(tMt, lq * 32, c0), ms);
+            *reinterpret_cast<uint4 *>(sm + SS_SIMG + img_chunk_off(128, j, c0 / 8)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(sm + SS_SIMG + img_chunk_off(128, j, c0 / 8 + 1)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(sm + SS_MIMG + img_chunk_off(128, j, c0 / 8)) = pack8(m16);
+            *reinterpret_cast<uint4 *>(sm + SS_MIMG + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(m16 + 8);
+        }
+        tmem_st_wait();
+    }
+    fence_proxy_async();
+    sync_all();
+    const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128);
+    for (int kk = 0; kk < nc && ok; ++kk) {
+        unsigned char *P = sm + (kk & 1) * SS_STAGE_BYTES;
+        if (tid == 0) {
+            mma_bf16_k(tVS, smem_u32(sm + SS_SIMG), 128, smem_u32(P + SS_W), 64, 8, id64, false);
+            mma_bf16_k(tVM, smem_u32(sm + SS_MIMG), 128, smem_u32(P + SS_W), 64, 8, id64, false);
+            mma_commit(bar_v);
+        }
+        ok = wait_all(bar_v, kk & 1);
+        if (!ok) break;
+        fence_after_sync();
+        {
+            const uint4 *urow = reinterpret_cast<const uint4 *>(P + SS_U + j * 128);
+            float dvs[32], dvm[32], u[8], o1[8], o2[8];
+            tmem_ld32(tmem_addr(tVS, lq * 32, 32 * hf), dvs);
+            tmem_ld32(tmem_addr(tVM, lq * 32, 32 * hf), dvm);
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+                unpack8(urow[4 * hf + hh], u);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    o1[e] = u[e] - dvs[8 * hh + e];
+                    o2[e] = -dvm[8 * hh + e];
+                }
+                *reinterpret_cast<uint4 *>(sm + SS_VSIMG + img_chunk_off(128, j, 4 * hf + hh)) = pack8(o1);
+                *reinterpret_cast<uint4 *>(sm + SS_VMIMG + img_chunk_off(128, j, 4 * hf + hh)) = pack8(o2);
+            }
+        }
+        fence_proxy_async();
+        sync_all();
+        if (tid == 0) {
+            mma_bf16_k(tSt, smem_u32(sm + SS_VSIMG), 128, smem_u32(P + SS_K), 128, 4, id128, true);
+            mma_bf16_k(tMt, smem_u32(sm + SS_VMIMG), 128, smem_u32(P + SS_K), 128, 4, id128, true);
+            mma_commit(bar_s);
+        }
+        const bool last = (kk == nc - 1);
+        bool okl = true;
+        if (!last) okl = mbar_wait(&bar_ld[(kk + 1) & 1], ((kk + 1) >> 1) & 1);
+        ok = mbar_wait(bar_s, kk & 1) && okl;
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        if (!ok) break;
+        fence_after_sync();
+        const float *gam = (const float *)(sm + ((kk + 1) & 1) * SS_STAGE_BYTES + SS_G);
+        float *out = seg_sum + ((size_t)g * H + h) * 2 * D * D;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const uint32_t tX = which ? tMt : tSt;
+            unsigned char *img = sm + (which ? SS_MIMG : SS_SIMG);
+#pragma unroll
+            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
+                float x[32];
+                tmem_ld32(tmem_addr(tX, lq * 32, c0), x);
+                if (!last) {
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        *reinterpret_cast<uint4 *>(img + img_chunk_off(128, j, c0 / 8 + q8)) = pack8(x + 8 * q8);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] *= gam[c0 + e];
+                    tmem_st16(tmem_addr(tX, lq * 32, c0), x);
+                    tmem_st16(tmem_addr(tX, lq * 32, c0 + 16), x + 16);
+                } else if (which == 0) {  // S~^T row j
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(out + (size_t)j * D + c0 + e) =
+                            make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+                } else {  // M row-major: M[c][j] = M^T[j][c]
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) out[D * D + (size_t)(c0 + e) * D + j] = x[e];
+                }
+            }
+        }
+        if (!last) tmem_st_wait();
+        fence_proxy_async();
+        sync_all();
+        if (tid == 0 && kk + 2 < nc) issue(kk + 2, kk & 1);
+    }
+    if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
+    sync_all();
+    if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+// =====================================================================================
+// Fold of the segment summaries of each (sequence, head) in order (section 5.1.2: the
+// rank-level updates compose associatively): S_in(i+1) = M_i S_in(i) + S~_i, starting from
+// the sequence's initial state.  Transposed: S^T <- S~^T + S^T M^T, an MMA with A = S^T and
+// B = M (rows c, K = m).  Both operands are split into bf16 high and low parts and three
+// products are accumulated (hi*hi + hi*lo + lo*hi), which keeps the fold near fp32 accuracy.
+constexpr uint32_t FD_AHI = 0, FD_ALO = 32768, FD_BHI = 65536, FD_BLO = 98304;
+constexpr uint32_t FD_BAR = 131072;
+constexpr uint32_t FD_TSLOT = FD_BAR + 16;
+constexpr uint32_t FD_TOTAL = FD_BAR + 64 + 1024;
+
+__global__ void __launch_bounds__(256, 1)
+chunk_fold_tc_kernel(int N, const int32_t *__restrict__ seg_start, int H, const float *initial_state,
+                     const float *__restrict__ seg_sum, float *__restrict__ seg_in, int *err) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = align1024(smem_raw);
+    const int n = blockIdx.x, h = blockIdx.y;
+    const int g0 = seg_start[n], nseg = seg_start[n + 1] - g0;
+    if (nseg <= 1) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lq = warp & 3, hf = warp >> 2;
+    const int j = lq * 32 + lane;
+    uint64_t *bar = (uint64_t *)(sm + FD_BAR);
+    uint32_t *tslot = (uint32_t *)(sm + FD_TSLOT);
+    if (tid == 0) mbar_init(bar, 1);
+    if (warp == 0) tmem_alloc(tslot, 128);
+    fence_proxy_async();
+    sync_all();
+    const uint32_t tD = *tslot;
+    const size_t st_off = ((size_t)n * H + h) * D * D;
+    float sreg[64];  // S^T row j, columns [64 hf, 64 hf + 64)
+#pragma unroll
+    for (int e = 0; e < 64; ++e) sreg[e] = initial_state ? initial_state[st_off + (size_t)(64 * hf + e) * D + j] : 0.f;
+    {
+        float *dst0 = seg_in + ((size_t)g0 * H + h) * D * D;  // segment 0 enters with S0
+#pragma unroll
+        for (int e = 0; e < 64; e += 4)
+            *reinterpret_cast<float4 *>(dst0 + (size_t)j * D + 64 * hf + e) =
+                make_float4(sreg[e], sreg[e + 1], sreg[e + 2], sreg[e + 3]);
+    }
+    bool ok = true;
+    const uint32_t id128 = idesc_bf16(128, 128);
+    for (int i = 0; i < nseg - 1 && ok; ++i) {
+        const float *sum = seg_sum + ((size_t)(g0 + i) * H + h) * 2 * D * D;
+        // D <- S~^T (row j); A images from S^T; B images from M (row c = j)
+#pragma unroll
+        for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 16) {
+            float t16[16], hi[16], lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(sum + (size_t)j * D + c0 + e);
+                t16[e] = v4.x; t16[e + 1] = v4.y; t16[e + 2] = v4.z; t16[e + 3] = v4.w;
+            }
+            tmem_st16(tmem_addr(tD, lq * 32, c0), t16);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                hi[e] = __bfloat162float(__float2bfloat16_rn(sreg[c0 - 64 * hf + e]));
+                lo[e] = sreg[c0 - 64 * hf + e] - hi[e];
+            }
+            *reinterpret_cast<uint4 *>(sm + FD_AHI + img_chunk_off(128, j, c0 / 8)) = pack8(hi);
+            *reinterpret_cast<uint4 *>(sm + FD_AHI + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(hi + 8);
+            *reinterpret_cast<uint4 *>(sm + FD_ALO + img_chunk_off(128, j, c0 / 8)) = pack8(lo);
+            *reinterpret_cast<uint4 *>(sm + FD_ALO + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(lo + 8);
+            float m16[16];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(sum + D * D + (size_t)j * D + c0 + e);
+                m16[e] = v4.x; m16[e + 1] = v4.y; m16[e + 2] = v4.z; m16[e + 3] = v4.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                hi[e] = __bfloat162float(__float2bfloat16_rn(m16[e]));
+                lo[e] = m16[e] - hi[e];
+            }
+            *reinterpret_cast<uint4 *>(sm + FD_BHI + img_chunk_off(128, j, c0 / 8)) = pack8(hi);
+            *reinterpret_cast<uint4 *>(sm + FD_BHI + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(hi + 8);
+            *reinterpret_cast<uint4 *>(sm + FD_BLO + img_chunk_off(128, j, c0 / 8)) = pack8(lo);
+            *reinterpret_cast<uint4 *>(sm + FD_BLO + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(lo + 8);
+        }
+        tmem_st_wait();
+        fence_proxy_async();
+        sync_all();
+        if (tid == 0) {
+            mma_bf16_k(tD, smem_u32(sm + FD_AHI), 128, smem_u32(sm + FD_BHI), 128, 8, id128, true);
+            mma_bf16_k(tD, smem_u32(sm + FD_AHI), 128, smem_u32(sm + FD_BLO), 128, 8, id128, true);
+            mma_bf16_k(tD, smem_u32(sm + FD_ALO), 128, smem_u32(sm + FD_BHI), 128, 8, id128, true);
+            mma_commit(bar);
+        }
+        ok = wait_all(bar, i & 1);
+        if (!ok) break;
+        fence_after_sync();
+        float *dst = seg_in + ((size_t)(g0 + i + 1) * H + h) * D * D;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+            tmem_ld32(tmem_addr(tD, lq * 32, 64 * hf + c0), sreg + c0);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4 *>(dst + (size_t)j * D + 64 * hf + c0 + e) =
+                    make_float4(sreg[c0 + e], sreg[c0 + e + 1], sreg[c0 + e + 2], sreg[c0 + e + 3]);
+        }
+        sync_all();
+    }
+    if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
+    sync_all();
+    if (warp == 0) tmem_dealloc(tD, 128);
 }
 
 }  // namespace tcp
@@ -896,11 +1204,29 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
         if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     }
     kda_profile_mark(2, stream);
+    const int32_t *seg_start = (const int32_t *)((char *)ws + p.off_seg_start);
+    float *seg_sum = (float *)((char *)ws + p.off_seg_sum);
+    float *seg_in = (float *)((char *)ws + p.off_seg_in);
+    int mark = 3;
+    if (p.split) {
+        cudaFuncSetAttribute(tcp::chunk_segsum_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tcp::SS_TOTAL);
+        tcp::chunk_segsum_tc_kernel<<<dim3((unsigned)p.max_segs, (unsigned)p.H), 256, tcp::SS_TOTAL, stream>>>(
+            (int)a->N, chunk_start, seg_start, p.seg_len, p.H, packets, seg_sum, err);
+        if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+        kda_profile_mark(mark++, stream);
+        cudaFuncSetAttribute(tcp::chunk_fold_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tcp::FD_TOTAL);
+        tcp::chunk_fold_tc_kernel<<<dim3((unsigned)a->N, (unsigned)p.H), 256, tcp::FD_TOTAL, stream>>>(
+            (int)a->N, seg_start, p.H, a->initial_state, seg_sum, seg_in, err);
+        if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+        kda_profile_mark(mark++, stream);
+    }
     cudaFuncSetAttribute(tcp::chunk_inter_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)tcp::CS_TOTAL);
-    tcp::chunk_inter_tc_kernel<<<(unsigned)(a->N * p.H), tcp::NT3, tcp::CS_TOTAL, stream>>>(
-        a->T, (int)a->N, a->cu_seqlens, chunk_start, p.H, packets, a->scale, a->initial_state,
-        a->final_state, (bf16 *)a->o, err);
-    kda_profile_mark(3, stream);
+    tcp::chunk_inter_tc_kernel<<<dim3((unsigned)p.max_segs, (unsigned)p.H), tcp::NT3, tcp::CS_TOTAL, stream>>>(
+        a->T, (int)a->N, a->cu_seqlens, chunk_start, seg_start, p.seg_len, seg_in, p.H, packets, a->scale,
+        a->initial_state, a->final_state, (bf16 *)a->o, err);
+    kda_profile_mark(mark, stream);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

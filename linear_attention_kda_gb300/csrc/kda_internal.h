@@ -20,11 +20,21 @@ struct kda_chunk_plan {
     size_t off_chunk_start;  // int32 [N + 1]: first chunk slot of each sequence
     size_t off_records;      // per (chunk slot, head) intra-chunk records
     size_t record_bytes;
+    // Split-sequence state pass (tensor-core path): sequences are cut into segments of seg_len
+    // chunks; every segment but the last of its sequence gets a summary (S~, M) with
+    // S_out = M S_in + S~, the summaries are folded in order, and each segment then runs from its
+    // true entering state.  seg_len >= max chunks per sequence means one segment per sequence.
+    int split;               // 1 if the segment summary and fold passes run
+    int64_t seg_len;         // chunks per segment
+    int64_t max_segs;        // upper bound on segments over all sequences
+    size_t off_seg_start;    // int32 [N + 1]: first segment of each sequence
+    size_t off_seg_sum;      // per (segment, head): S~^T [128][128] and M [128][128], fp32
+    size_t off_seg_in;       // per (segment, head): entering state S^T [128][128], fp32
     size_t total_bytes;
 };
 
 bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_t dtype, int C,
-                         kda_chunk_plan *plan);
+                         kda_chunk_plan *plan, const int32_t *cu_seqlens_host = nullptr);
 kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
                                    cudaStream_t stream);
 kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,

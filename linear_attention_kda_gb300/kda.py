@@ -217,8 +217,13 @@ def set_profile_events(events) -> None:
     _check(L.kda_set_profile_events(arr, len(events)), "kda_set_profile_events")
 
 
-def chunk_fwd_kernel_count() -> int:
-    a = ChunkArgs()
+def chunk_fwd_kernel_count(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, cu_seqlens_host=None) -> int:
+    """Kernels kda_chunk_fwd launches for these sizes (the split-sequence state pass adds two)."""
+    cu = None
+    if cu_seqlens_host is not None:
+        cu = cu_seqlens_host.to(dtype=torch.int32, device="cpu").contiguous()
+    a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=KDA_BF16 if dtype == torch.bfloat16 else KDA_F32,
+                  cu_seqlens_host=None if cu is None else cu.data_ptr(), chunk_size=64)
     return int(load_library().kda_chunk_fwd_kernel_count(ctypes.byref(a)))
 
 

@@ -243,3 +243,39 @@ def test_decode_equals_prefill_continuation():
         for h in range(H):
             assert rel_err(o_dec[n, :, h].numpy(), o_pf[n, :, h].numpy()) <= TOL_BF16
             assert rel_err(st[n, h].cpu().numpy(), fs_pf[n, h].cpu().numpy()) <= TOL_BF16
+
+
+@pytest.mark.parametrize("T", [8192, 8192 + 37])
+def test_split_sequence_state_pass(T):
+    """Long sequences with few heads take the split-sequence state pass (segment summaries,
+    fold, per-segment output); checked against the oracle like any other case."""
+    w = syn.Workload("cp", H=2, d=128, dtype="bf16", seq_len=T, z_std=1.5, b_range=1.0,
+                     alog_std=0.25, s0_std=0.02)
+    d = syn.make_prefill(w, seed=41)
+    assert kda.chunk_fwd_kernel_count(T, 1, 2, 128, 128, torch.bfloat16, d["cu_seqlens"]) == 5
+    o, fs = run_prefill(d)
+    compare_prefill(d, o, fs, oracle_prefill(d), TOL_BF16)
+
+
+def test_split_sequence_varlen_mix():
+    """Split state pass with sequences of very different lengths, one of them empty."""
+    w = syn.Workload("cpv", H=2, d=128, dtype="bf16", seq_len=None, z_std=1.5, b_range=1.0,
+                     alog_std=0.25, s0_std=0.02)
+    d = _varlen(w, [8192, 100, 0, 3000, 5000, 64], seed=42)
+    assert kda.chunk_fwd_kernel_count(sum(d["lengths"]), 6, 2, 128, 128, torch.bfloat16, d["cu_seqlens"]) == 5
+    o, fs = run_prefill(d)
+    compare_prefill(d, o, fs, oracle_prefill(d), TOL_BF16)
+
+
+def test_split_sequence_final_state_aliases_initial_state():
+    w = syn.Workload("cpa", H=2, d=128, dtype="bf16", seq_len=None, z_std=1.5, b_range=1.0,
+                     alog_std=0.25, s0_std=0.02)
+    d = _varlen(w, [8192, 300], seed=43)
+    assert kda.chunk_fwd_kernel_count(sum(d["lengths"]), 2, 2, 128, 128, torch.bfloat16, d["cu_seqlens"]) == 5
+    st = d["initial_state"].cuda().contiguous()
+    dev = "cuda"
+    o, _ = kda.chunk_fwd(*(d[n].to(dev) for n in ("q", "k", "v", "z", "beta")), d["dt_bias"].to(dev),
+                         d["A_log"].to(dev), cu_seqlens=d["cu_seqlens"].to(dev), cu_seqlens_host=d["cu_seqlens"],
+                         initial_state=st, final_state=st)
+    torch.cuda.synchronize()
+    compare_prefill(d, o.float().cpu(), st.cpu(), oracle_prefill(d), TOL_BF16)
