@@ -78,6 +78,29 @@ def decode_bytes(N, H, d, io_bytes):
     return N * H * (2 * d * d * 4 + 4 * d * io_bytes + io_bytes + d * io_bytes)
 
 
+def chunk_lengths_count(lengths, C=64):
+    return [(int(L) + C - 1) // C for L in lengths]
+
+
+def measured_traffic(kernel, p_items):
+    """DRAM bytes per launch of `kernel` from the committed ncu record (profiles/traffic_*.json),
+    scaled by the (chunk, head) items of this launch; None if no record exists or the kernel
+    source changed since the capture (sha256 prefix mismatch)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != rec["source_sha256_16"]:
+            return None
+    return rec["dram_bytes_per_item"] * p_items
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -90,29 +113,75 @@ def load_peaks():
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi sampling (100 ms) during the timed region."""
+    """Samples SM clock, power and clock-event reasons during the timed region (read-only).
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Uses NVML through ctypes every 2 ms (the timed regions are tens of milliseconds); falls back
+    to `nvidia-smi -lms 100` when NVML cannot be loaded.  Nothing here changes any GPU setting.
+    """
 
-    def __init__(self, index=0):
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index=0, period_s=0.002):
         self.index = index
+        self.period = period_s
+        self.rows = []
         self.proc = None
-        self.path = os.path.join("/tmp", f"kda_clocks_{os.getpid()}.csv")
+        self.nvml = None
+        self.thread = None
+        self.stop = None
+
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            return None
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return lib, h, reasons
+
+    def _poll(self):
+        import ctypes
+        lib, h, reasons = self.nvml
+        clk, mx, pw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+        while not self.stop.is_set():
+            lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk))  # NVML_CLOCK_SM
+            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+            reasons(h, ctypes.byref(rs))
+            self.rows.append((float(clk.value), float(mx.value), pw.value / 1000.0, int(rs.value)))
+            time.sleep(self.period)
 
     def __enter__(self):
+        import threading
+        try:
+            self.nvml = self._nvml_open()
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return self
+        self.path = os.path.join("/tmp", f"kda_clocks_{os.getpid()}.csv")
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
-                stderr=subprocess.DEVNULL)
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def __exit__(self, *exc):
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -120,26 +189,21 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.fh.close()
+            with open(self.path) as f:
+                for ln in f:
+                    parts = [x.strip() for x in ln.split(",")]
+                    try:
+                        self.rows.append((float(parts[0]), float(parts[1]), float(parts[2]), int(parts[3], 16)))
+                    except (ValueError, IndexError):
+                        continue
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        with open(self.path) as f:
-            for ln in f:
-                parts = [x.strip() for x in ln.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
-                except ValueError:
-                    continue
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"]}
+        reasons = sorted({name for r in self.rows for bit, name in self.REASONS.items() if r[3] & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in self.rows), "sm_max_mhz": max(r[1] for r in self.rows),
+                "power_w_max": max(r[2] for r in self.rows), "samples": len(self.rows),
+                "source": "nvml" if self.nvml is not None else "nvidia-smi", "reasons": reasons}
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -300,7 +364,7 @@ def run_ours(args, rank, ws, local):
     else:
         roof = {"bound": "tensor", "achieved": flops_dom / t_dom / 1e12, "peak": tc, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(names[dom], p_items=sum(chunk_lengths_count(lengths)) * H)
     roof["kernel"] = names[dom]
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json burst)" if peak_kind == "measured" else "fallback"
 
@@ -402,6 +466,35 @@ def run_ours(args, rank, ws, local):
         print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """Small fixed cases for profiler captures (a few untimed launches, then a one-line summary).
+
+    prefill_small: B=1, H=8, T=16384, bf16, d=128 (inputs 33.6 MB, packets 155 MB: above L2).
+    decode_small:  N=64 sequences x H=32 heads, d=128, fp32 state 268 MB (above L2), 8 steps.
+    """
+    from linear_attention_kda_gb300 import build as kbuild, kda
+    kbuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.case == "prefill_small":
+        w = syn.Workload("prefill_small_bf16_T16384_H8_d128", H=8, d=128, dtype="bf16", seq_len=16384,
+                         z_std=1.5, b_range=1.0, alog_std=0.25)
+        d = syn.make_prefill(w, seed=1, device=dev)
+        for _ in range(3):
+            kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["dt_bias"], d["A_log"],
+                          cu_seqlens=d["cu_seqlens"], cu_seqlens_host=d["cu_seqlens"].cpu(),
+                          output_final_state=True)
+    else:
+        w = syn.Workload("decode_small_bf16_N64_H32_d128", H=32, d=128, dtype="bf16", n_seq=64, seq_len=1,
+                         z_std=1.5, b_range=1.0, alog_std=0.25, s0_std=0.02, decode_steps=8)
+        d = syn.make_decode(w, seed=4, device=dev)
+        for s_ in range(8):
+            kda.recurrent_step(d["q"][s_], d["k"][s_], d["v"][s_], d["z"][s_], d["beta"][s_], d["dt_bias"],
+                               d["A_log"], d["state"])
+    torch.cuda.synchronize()
+    print(json.dumps({"case": args.case, "workload": w.name, "device_error": kda.get_device_error()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,7 +503,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--case", choices=["prefill_small", "decode_small"], default=None,
+                    help="run a small fixed case for profiler captures instead of the benchmark")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     rank, ws, local = dist_setup()

@@ -56,7 +56,7 @@ constexpr uint32_t PK_W = 0;          // W image, 64 rows x 128 K
 constexpr uint32_t PK_Q = 16384;      // Q^ image, 64 x 128
 constexpr uint32_t PK_K = 32768;      // K~^T image, 128 x 64
 constexpr uint32_t PK_A = 49152;      // A image, 64 x 64
-constexpr uint32_t PK_U = 57344;      // U^T plain bf16 [128][64]
+constexpr uint32_t PK_U = 57344;      // U^T bf16 [128][64], 16-byte chunk j of row r at chunk j ^ (r % 8)
 constexpr uint32_t PK_G = 73728;      // gamma^C fp32 [128]
 constexpr uint32_t PK_BYTES = 74240;
 constexpr uint32_t PK_STRIDE = 75776; // multiple of 1024
@@ -66,8 +66,8 @@ constexpr uint32_t CS_STAGE0 = 0;
 constexpr uint32_t CS_STAGE1 = PK_STRIDE;
 constexpr uint32_t CS_SIMG = 2 * PK_STRIDE;            // S^T image 128 x 128 (32 KB)
 constexpr uint32_t CS_VIMG = CS_SIMG + 32768;          // V~^T image 128 x 64 (16 KB)
-constexpr uint32_t CS_BAR = CS_VIMG + 16384;           // 8 mbarriers
-constexpr uint32_t CS_TSLOT = CS_BAR + 64;             // TMEM base, failure flag
+constexpr uint32_t CS_BAR = CS_VIMG + 16384;           // 10 mbarriers
+constexpr uint32_t CS_TSLOT = CS_BAR + 96;             // TMEM base, failure flag
 constexpr uint32_t CS_TOTAL = CS_BAR + 128 + 1024;
 
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
@@ -519,7 +519,7 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
                     for (int r = 0; r < 16; ++r) Tm[(base + r) * LS + base + c] = x[r];
                 }
             } else {
-                const int u = tid - 128, rg = u >> 4, c0 = (u & 15) * 8, b = rg >> 1;
+                const int u = tid - 128, rg = u & 7, c0 = (u >> 3) * 8, b = rg >> 1;
                 const float *gp = &FAC[(FAC_GPE + b) * D + c0];
                 const float4 g0 = *reinterpret_cast<const float4 *>(gp), g1 = *reinterpret_cast<const float4 *>(gp + 4);
                 const float gev[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
@@ -617,7 +617,7 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
                 tmem_ld32(tmem_addr(tb, lq * 32, 128 + rbase), d);
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
-                    *reinterpret_cast<uint4 *>(pk + PK_U + c * 128 + rbase * 2 + jj * 16) = pack8(d + 8 * jj);
+                    *reinterpret_cast<uint4 *>(pk + PK_U + img_chunk_off(128, c, rbase / 8 + jj)) = pack8(d + 8 * jj);
             }
             fence_proxy_async();
             csync();
@@ -634,12 +634,18 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
     if (warp == 0) tmem_dealloc(tb, 256);
 }
 
-constexpr int NT3 = 384;  // warps 0-7: state path; warps 8-11: output path
-// Warp roles.  Warps 0-7 carry the recurrence: per chunk V~ (after the V MMA), then the state
-// readout after the state MMA, writing the bf16 S^T image for the next chunk and the TMEM copy
-// scaled by the next chunk's gamma (warps w and w + 4 share TMEM lanes and split the columns).
-// Warps 8-11 move the outputs: after the output MMAs of chunk k complete they read O^T (double
-// buffered in TMEM), store it, and release the buffer and the packet stage.
+constexpr int NT3 = 416;  // warps 0-7: state path; 8-11: output path; 12: MMA issue
+// Warp roles.
+//  - Warp 12 (one thread) issues every tcgen05.mma in program order: per chunk the V product
+//    (needs the S^T image), the Q^ product (output), then after V~ is ready the state update and
+//    the A product.  Issuing costs ~45 cycles per instruction, so keeping it off the SIMT warps
+//    removes it from their critical path.
+//  - Warps 0-7 carry the recurrence: V~ after the V product, then the state readout after the
+//    state MMA, writing the bf16 S^T image for the next chunk and the TMEM copy scaled by the
+//    next chunk's gamma (warps w and w + 4 share TMEM lanes and split the columns).
+//  - Warps 8-11 move the outputs: after the output MMAs of chunk k complete they read O^T (double
+//    buffered in TMEM), store it, release the buffer, and refill the packet stage.
+// In-order execution of one thread's MMAs makes each commit cover everything issued before it.
 __global__ void __launch_bounds__(NT3, 1)
 chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
                       const int32_t *__restrict__ seg_start, int64_t seg_len, const float *__restrict__ seg_in,
@@ -665,9 +671,10 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
     const int lq = warp & 3;
     const int j = lq * 32 + lane;  // value channel = TMEM lane = S^T row
     uint64_t *bar_ld = (uint64_t *)(sm + CS_BAR);             // [2] packet stage loaded
-    uint64_t *bar_v = bar_ld + 2, *bar_s = bar_ld + 3;        // V MMA, state MMA done
-    uint64_t *bar_o = bar_ld + 4;                             // [2] output MMAs of a chunk done
-    uint64_t *bar_free = bar_ld + 6;                          // [2] O buffer + packet stage released
+    uint64_t *bar_v = bar_ld + 2, *bar_s = bar_ld + 3;        // V product / state update done
+    uint64_t *bar_o = bar_ld + 4;                             // [2] all MMAs of a chunk done
+    uint64_t *bar_free = bar_ld + 6;                          // [2] O buffer released by the output path
+    uint64_t *bar_simg = bar_ld + 8, *bar_vimg = bar_ld + 9;  // S^T / V~^T images ready
     uint32_t *tslot = (uint32_t *)(sm + CS_TSLOT);
     int *s_fail = (int *)(sm + CS_TSLOT + 8);
     const int64_t kk0 = (int64_t)seg_i * seg_len;
@@ -690,6 +697,8 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
         mbar_init(&bar_o[1], 1);
         mbar_init(&bar_free[0], 128);
         mbar_init(&bar_free[1], 128);
+        mbar_init(bar_simg, 1);
+        mbar_init(bar_vimg, 1);
         *s_fail = 0;
     }
     if (warp == 0) tmem_alloc(tslot, 512);
@@ -705,7 +714,34 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
         }
     }
 
-    if (warp >= 8) {
+    if (warp == 12) {
+        // ------------------------------------------------ MMA issue (one thread)
+        if (lane == 0) {
+            const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128);
+            bool ok = true;
+            for (int kk = 0; kk < nc && ok; ++kk) {
+                unsigned char *P = sm + ((kk & 1) ? CS_STAGE1 : CS_STAGE0);
+                const uint32_t tO = tO0 + 64 * (kk & 1);
+                ok = mbar_wait(bar_simg, kk & 1);  // S^T image of S_kk written, packet kk resident
+                if (!ok) break;
+                fence_after_sync();
+                mma_bf16_k(tV, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_W), 64, 8, id64, false);
+                mma_commit(bar_v);
+                if (kk >= 2) ok = mbar_wait(&bar_free[kk & 1], ((kk >> 1) - 1) & 1);  // O buffer read
+                if (!ok) break;
+                fence_after_sync();
+                mma_bf16_k(tO, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_Q), 64, 8, id64, false);
+                ok = mbar_wait(bar_vimg, kk & 1);  // V~^T image written, TMEM S scaled by gamma_kk
+                if (!ok) break;
+                fence_after_sync();
+                mma_bf16_k(tS, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_K), 128, 4, id128, true);
+                mma_commit(bar_s);
+                mma_bf16_k(tO, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_A), 64, 4, id64, true);
+                mma_commit(&bar_o[kk & 1]);
+            }
+            if (!ok) atomicExch(s_fail, 1);
+        }
+    } else if (warp >= 8) {
         // ------------------------------------------------ output path (128 threads)
         const int ot = tid - 256;
         bool ok = true;
@@ -738,91 +774,27 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
         // ------------------------------------------------ state path (256 threads)
         const int hf = warp >> 2;  // column half
         bool ok = true;
-        float sreg[64];
-        if (s_in) {
+        {
+            float sreg[64];
+            if (s_in) {
 #pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(s_in + (size_t)j * D + 64 * hf + e);
-                sreg[e] = v4.x; sreg[e + 1] = v4.y; sreg[e + 2] = v4.z; sreg[e + 3] = v4.w;
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 64; ++e)
-                sreg[e] = initial_state ? initial_state[st_off + (size_t)(64 * hf + e) * D + j] : 0.f;
-        }
-        if (nc > 0) ok = mbar_wait(&bar_ld[0], 0);
-        ok = (__syncthreads_count_named1(ok) == 256);
-        if (ok && nc > 0) {  // S_0 image; TMEM gets S_0 Diag(gamma_0)
-            const float *gam = (const float *)(sm + CS_STAGE0 + PK_G);
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 8)
-                *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, (64 * hf + c0) / 8)) = pack8(sreg + c0);
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16) {
-                float sc[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) sc[e] = sreg[c0 + e] * gam[64 * hf + c0 + e];
-                tmem_st16(tmem_addr(tS, lq * 32, 64 * hf + c0), sc);
-            }
-            tmem_st_wait();
-        }
-        fence_proxy_async();
-        fence_before_sync();
-        named_sync(1, 256);
-        fence_after_sync();
-        const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128);
-        for (int kk = 0; kk < nc && ok; ++kk) {
-            // invariant: packet kk resident; S^T image = bf16(S_kk); TMEM S^T = S_kk^T Diag(gamma_kk)
-            unsigned char *P = sm + ((kk & 1) ? CS_STAGE1 : CS_STAGE0);
-            const uint32_t tO = tO0 + 64 * (kk & 1);
-            if (tid == 0) {
-                mma_bf16_k(tV, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_W), 64, 8, id64, false);
-                mma_commit(bar_v);
-                // O buffer kk & 1 was last read for chunk kk - 2
-                bool fr = (kk < 2) || mbar_wait(&bar_free[kk & 1], ((kk >> 1) - 1) & 1);
-                if (!fr) atomicExch(s_fail, 1);
-                fence_after_sync();
-                mma_bf16_k(tO, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_Q), 64, 8, id64, false);
-            }
-            ok = mbar_wait(bar_v, kk & 1);
-            ok = (__syncthreads_count_named1(ok) == 256) && (*(volatile int *)s_fail == 0);
-            if (!ok) break;
-            fence_after_sync();
-            // V~^T row j = U^T row j - (S^T W^T) row j, columns [32 hf, 32 hf + 32)
-            {
-                const uint4 *urow = reinterpret_cast<const uint4 *>(P + PK_U + j * 128);
-                float dv[32], u[8], vo[8];
-                tmem_ld32(tmem_addr(tV, lq * 32, 32 * hf), dv);
-#pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {
-                    unpack8(urow[4 * hf + hh], u);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) vo[e] = u[e] - dv[8 * hh + e];
-                    *reinterpret_cast<uint4 *>(sm + CS_VIMG + img_chunk_off(128, j, 4 * hf + hh)) = pack8(vo);
+                for (int e = 0; e < 64; e += 4) {
+                    const float4 v4 = *reinterpret_cast<const float4 *>(s_in + (size_t)j * D + 64 * hf + e);
+                    sreg[e] = v4.x; sreg[e + 1] = v4.y; sreg[e + 2] = v4.z; sreg[e + 3] = v4.w;
                 }
-            }
-            fence_proxy_async();
-            fence_before_sync();
-            named_sync(1, 256);
-            fence_after_sync();
-            if (tid == 0) {
-                mma_bf16_k(tS, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_K), 128, 4, id128, true);
-                mma_commit(bar_s);
-                mma_bf16_k(tO, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_A), 64, 4, id64, true);
-                mma_commit(&bar_o[kk & 1]);
-            }
-            const bool last = (kk == nc - 1);
-            bool okl = true;
-            if (!last) okl = mbar_wait(&bar_ld[(kk + 1) & 1], ((kk + 1) >> 1) & 1);
-            ok = mbar_wait(bar_s, kk & 1) && okl;
-            ok = (__syncthreads_count_named1(ok) == 256);
-            if (!ok) break;
-            fence_after_sync();
-            // S_{kk+1}: bf16 image and TMEM copy scaled by gamma_{kk+1} (or kept for the final state)
+            } else {
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) tmem_ld32(tmem_addr(tS, lq * 32, 64 * hf + c0), sreg + c0);
-            if (!last) {
-                const float *gam = (const float *)(sm + (((kk + 1) & 1) ? CS_STAGE1 : CS_STAGE0) + PK_G);
+                for (int e = 0; e < 64; ++e)
+                    sreg[e] = initial_state ? initial_state[st_off + (size_t)(64 * hf + e) * D + j] : 0.f;
+            }
+            if (nc > 0) ok = mbar_wait(&bar_ld[0], 0);
+            ok = (__syncthreads_count_named1(ok) == 256);
+            if (nc == 0 && ok && final_state && last_seg) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) final_state[st_off + (size_t)(64 * hf + e) * D + j] = sreg[e];
+            }
+            if (ok && nc > 0) {  // S_0 image; TMEM gets S_0 Diag(gamma_0)
+                const float *gam = (const float *)(sm + CS_STAGE0 + PK_G);
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 8)
                     *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, (64 * hf + c0) / 8)) =
@@ -836,14 +808,66 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
                 }
                 tmem_st_wait();
             }
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        named_sync(1, 256);
+        if (tid == 0 && nc > 0) mbar_arrive(bar_simg);
+        for (int kk = 0; kk < nc && ok; ++kk) {
+            // invariant: packet kk resident; S^T image = bf16(S_kk); TMEM S^T = S_kk^T Diag(gamma_kk)
+            unsigned char *P = sm + ((kk & 1) ? CS_STAGE1 : CS_STAGE0);
+            ok = mbar_wait(bar_v, kk & 1);
+            ok = (__syncthreads_count_named1(ok) == 256) && (*(volatile int *)s_fail == 0);
+            if (!ok) break;
+            fence_after_sync();
+            // V~^T row j = U^T row j - (S^T W^T) row j, columns [32 hf, 32 hf + 32)
+            {
+                float dv[32], u[8], vo[8];
+                tmem_ld32(tmem_addr(tV, lq * 32, 32 * hf), dv);
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) {
+                    unpack8(*reinterpret_cast<const uint4 *>(P + PK_U + img_chunk_off(128, j, 4 * hf + hh)), u);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) vo[e] = u[e] - dv[8 * hh + e];
+                    *reinterpret_cast<uint4 *>(sm + CS_VIMG + img_chunk_off(128, j, 4 * hf + hh)) = pack8(vo);
+                }
+            }
             fence_proxy_async();
             fence_before_sync();
             named_sync(1, 256);
+            if (tid == 0) mbar_arrive(bar_vimg);
+            const bool last = (kk == nc - 1);
+            bool okl = true;
+            if (!last) okl = mbar_wait(&bar_ld[(kk + 1) & 1], ((kk + 1) >> 1) & 1);
+            ok = mbar_wait(bar_s, kk & 1) && okl;
+            ok = (__syncthreads_count_named1(ok) == 256);
+            if (!ok) break;
             fence_after_sync();
-        }
-        if (ok && final_state && last_seg) {
+            // S_{kk+1}: bf16 image and TMEM copy scaled by gamma_{kk+1}; or the final state
+            const float *gam = (const float *)(sm + (((kk + 1) & 1) ? CS_STAGE1 : CS_STAGE0) + PK_G);
 #pragma unroll
-            for (int e = 0; e < 64; ++e) final_state[st_off + (size_t)(64 * hf + e) * D + j] = sreg[e];
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                float x[32];
+                tmem_ld32(tmem_addr(tS, lq * 32, 64 * hf + c0), x);
+                if (!last) {
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, (64 * hf + c0) / 8 + q8)) =
+                            pack8(x + 8 * q8);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] *= gam[64 * hf + c0 + e];
+                    tmem_st16(tmem_addr(tS, lq * 32, 64 * hf + c0), x);
+                    tmem_st16(tmem_addr(tS, lq * 32, 64 * hf + c0 + 16), x + 16);
+                } else if (final_state && last_seg) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) final_state[st_off + (size_t)(64 * hf + c0 + e) * D + j] = x[e];
+                }
+            }
+            if (!last) tmem_st_wait();
+            fence_proxy_async();
+            fence_before_sync();
+            named_sync(1, 256);
+            if (tid == 0 && !last) mbar_arrive(bar_simg);
         }
         if (!ok) atomicExch(s_fail, 1);
     }
@@ -852,7 +876,6 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
     sync_all();
     if (warp == 0) tmem_dealloc(tb, 512);
 }
-
 
 // =====================================================================================
 // Segment summaries (section 5.1.2, Eq. 17, used inside one device): for every segment but
@@ -958,13 +981,12 @@ chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int
         if (!ok) break;
         fence_after_sync();
         {
-            const uint4 *urow = reinterpret_cast<const uint4 *>(P + SS_U + j * 128);
             float dvs[32], dvm[32], u[8], o1[8], o2[8];
             tmem_ld32(tmem_addr(tVS, lq * 32, 32 * hf), dvs);
             tmem_ld32(tmem_addr(tVM, lq * 32, 32 * hf), dvm);
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh) {
-                unpack8(urow[4 * hf + hh], u);
+                unpack8(*reinterpret_cast<const uint4 *>(P + SS_U + img_chunk_off(128, j, 4 * hf + hh)), u);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     o1[e] = u[e] - dvs[8 * hh + e];
