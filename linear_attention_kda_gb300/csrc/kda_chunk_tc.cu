@@ -1,40 +1,23 @@
 // Tensor-core path of kda_chunk_fwd: bf16 I/O, d_k = d_v = 128, C = 64.
 //
-// Two kernels (plus the chunk plan) evaluate Eq. 3 and Eq. 4 of the Kimi K3
+// The kernels below (plus the chunk plan) evaluate Eq. 3 and Eq. 4 of the Kimi K3
 // report (section 2.1.1).  Every dense contraction runs on tcgen05.mma
 // (kind::f16, bf16 operands in shared memory, fp32 accumulators in tensor
 // memory); the scan-like and exponential work runs on the CUDA cores in fp32.
 //
-// 1. chunk_intra_tc (persistent: one CTA of 256 threads per SM walks the
-//    (chunk, head) items; the q, k, v, z tiles of the next item are bulk-copied
-//    into a second buffer while the current one is computed)
-//    - g (Eq. 5) and the in-chunk cumulative log-decay G (Eq. 3), fp32.
-//    - A = Tril[(Q Gamma)(K / Gamma)^T] (diagonal kept) and the UT-transform
-//      matrix L = StrictTril[diag(beta)(K Gamma)(K / Gamma)^T].  Over a 64-token
-//      chunk 1/Gamma reaches e^{320} and overflows even fp32, so the key axis is
-//      cut into 16-token blocks, as the report's bounded-gate argument allows
-//      (over 16 tokens the log-decay lies in (-80, 0), inside bf16 range).  Key
-//      block b (tokens 16b..16b+15, reference p = 16b+15) is scaled as
-//      k_i e^{G_p - G_i} (exponent in [-75, 0]); rows r >= 16b as
-//      x_r e^{G_r - G_p} (exponent <= 75), rows r < 16b are zero.  Each block is
-//      one MMA with M = 128 (64 query rows stacked over 64 key rows), N = 16,
-//      K = 128, so both A and L come out of the same four MMAs, diagonal tiles
-//      included.  No operand exceeds e^{75} and masked entries stay finite.
-//    - T = (I + L)^{-1} in fp32: 16x16 diagonal blocks by substitution, then
-//      the off-diagonal blocks level by level.
-//    - W^T = (diag(beta) Gamma K)^T T^T and U^T = (diag(beta) V)^T T^T on the
-//      tensor cores (M = 128 channels, N = 64, K = 64).
-//    - Writes a per-(chunk, head) packet of ready-to-use operand images:
-//      W [64 x 128], Q^ = Q Gamma [64 x 128], K~^T = (K e^{G_last - G})^T [128 x 64],
-//      A [64 x 64], U^T [128 x 64] (plain), gamma^C [128] fp32.
-// 2. chunk_inter_tc (one CTA of 256 threads per (sequence, head); chunks in order)
+// 1. chunk_intra_tc (persistent, one CTA per SM over the (chunk, head) items)
+//    computes the gate, the decays, A, the UT transform T = (I + L)^{-1}, W and U
+//    of each chunk and writes a per-(chunk, head) packet of ready-to-use operand
+//    images: W^T [128 x 64], Q^ = Q Gamma [64 x 128], K~ = K e^{G_last - G}
+//    [64 x 128], A [64 x 64], U^T [128 x 64], gamma^C [128] fp32.
+// 2. chunk_inter_tc (one CTA per (segment, head); chunks in order)
 //    The state is kept transposed in tensor memory, S^T [d_v lanes x d_k
 //    columns] fp32, and as a bf16 operand image in shared memory.  Per chunk:
 //      V~^T = U^T - S^T W^T                      (MMA, M = 128, N = 64, K = 128)
 //      O^T  = S^T Q^^T + V~^T A^T                (MMA, K = 128 then K = 64)
 //      S^T <- S^T Diag(gamma^C) + V~^T K~        (scale in fp32, MMA N = 128, K = 64)
-//    Warps w and w + 4 share TMEM lanes and split the columns.  Packets are
-//    streamed by 1-D bulk copies, double buffered.
+//    Packets are streamed by 1-D bulk copies, double buffered.
+// 3. chunk_segsum_tc / chunk_fold_tc: the split-sequence state pass (section 5.1.2).
 // Waits on mbarriers give up after about a second, set KDA_ERR_DEVICE_TIMEOUT,
 // and the kernel still releases its tensor memory before it returns.
 #include "kda_common.cuh"
@@ -52,23 +35,28 @@ constexpr int C = 64;   // chunk
 constexpr int D = 128;  // d_k = d_v
 
 // packet layout (bytes)
-constexpr uint32_t PK_W = 0;          // W image, 64 rows x 128 K
+constexpr uint32_t PK_W = 0;          // W^T bf16 [128 channels][64 tokens], read as an MN-major B operand
 constexpr uint32_t PK_Q = 16384;      // Q^ image, 64 x 128
-constexpr uint32_t PK_K = 32768;      // K~^T image, 128 x 64
+constexpr uint32_t PK_K = 32768;      // K~ bf16 [64 tokens][128 channels] (two 64-channel halves), MN-major B
 constexpr uint32_t PK_A = 49152;      // A image, 64 x 64
 constexpr uint32_t PK_U = 57344;      // U^T bf16 [128][64], 16-byte chunk j of row r at chunk j ^ (r % 8)
 constexpr uint32_t PK_G = 73728;      // gamma^C fp32 [128]
-constexpr uint32_t PK_BYTES = 74240;
 constexpr uint32_t PK_STRIDE = 75776; // multiple of 1024
 
 // inter kernel shared memory
-constexpr uint32_t CS_STAGE0 = 0;
-constexpr uint32_t CS_STAGE1 = PK_STRIDE;
-constexpr uint32_t CS_SIMG = 2 * PK_STRIDE;            // S^T image 128 x 128 (32 KB)
+// Three packet stages hold the MMA operands of a chunk (W^T, Q^, K~, A) and gamma; U^T is read by the
+// CUDA cores straight from global memory into registers, two chunks ahead.
+constexpr uint32_t CS_NST = 3;
+constexpr uint32_t CS_PK_MMA = PK_A + 8192;            // bytes [0, PK_A + 8 KB) of a packet: W, Q^, K~, A
+constexpr uint32_t CS_G = CS_PK_MMA;                   // gamma inside a stage
+constexpr uint32_t CS_ST_TX = CS_PK_MMA + 512;
+constexpr uint32_t CS_ST_BYTES = 58368;                // stage stride (multiple of 1024)
+constexpr uint32_t CS_SIMG = CS_NST * CS_ST_BYTES;     // S^T image 128 x 128 (32 KB)
 constexpr uint32_t CS_VIMG = CS_SIMG + 32768;          // V~^T image 128 x 64 (16 KB)
-constexpr uint32_t CS_BAR = CS_VIMG + 16384;           // 10 mbarriers
+constexpr uint32_t CS_BAR = CS_VIMG + 16384;           // 11 mbarriers
 constexpr uint32_t CS_TSLOT = CS_BAR + 96;             // TMEM base, failure flag
 constexpr uint32_t CS_TOTAL = CS_BAR + 128 + 1024;
+static_assert(CS_ST_TX <= CS_ST_BYTES, "stage");
 
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
     const uint32_t s = smem_u32(p);
@@ -135,47 +123,73 @@ __device__ __forceinline__ bool locate(const int32_t *chunk_start, const int32_t
 }
 
 // =====================================================================================
-// Persistent intra-chunk kernel: one CTA per SM walks (chunk, head) work items
-// w = slot * H + h.  Warp 8 is the producer: for each item it fetches the q, z, k, v
-// tiles (four TMA boxes of 64 tokens x 128 channels) and the item's beta, bias and
-// e^{A_log} into one half of a double buffer, while warps 0-7 compute the other item.
+// Persistent intra-chunk kernel: one CTA per SM walks the (chunk, head) work items
+// w = slot * H + h.  Warp 16 is the producer: for each item it fetches the q, z, k, v tiles
+// (128-byte-swizzled TMA boxes of 64 tokens x 64 channels, two per tile) and the item's beta,
+// bias and e^{A_log} into one half of a double buffer, while warps 0-15 compute the other item.
 //
-// Exponentials: per element only d = G_r - G_p(r) >= 0 (p(r) = last row of r's
-// 16-row block) is exponentiated, as E = e^d and E^-1 = e^-d; every other decay
-// factor is E or E^-1 times a per-(block, channel) factor:
-//   e^{G_r}           = E * e^{G_p}                    (Q^, beta Gamma K)
-//   e^{G_last - G_r}  = E^-1 * e^{G_last - G_p}        (K~)
-//   e^{G_p - G_r}     = E^-1                            (key-block image)
-//   e^{G_r - G_p'}    = E * e^{G_p(r) - G_p'}  (p' <= p(r), row images)
-constexpr int NT2 = 288;      // 8 consumer warps + 1 producer warp
-constexpr int NC2 = 256;      // consumer threads
-constexpr uint32_t I2_STG = 0;  // 2 stages x [Q | Z | K | V], plain [64][128] bf16 each
-constexpr uint32_t I2_STG_BYTES = 65536;
-constexpr uint32_t I2_TQ = 0, I2_TZ = 16384, I2_TK = 32768, I2_TV = 49152;
-// after the gate (Z dead) and the row-side caching (Q dead) the stage's first 32 KB
-// hold the second row image, and after the L/A products the X^T and (beta V)^T images
-constexpr uint32_t I2_G = 131072;             // fp32 [64][128]: G, then E in place
-constexpr uint32_t I2_SCR = 163840;           // 48 KB scratch
-constexpr uint32_t I2_ROW = I2_SCR;           // row image A (stage + 0 is row image B)
-constexpr uint32_t I2_KEY = I2_SCR + 32768;   // 4 key-block images
-constexpr int LS = 68;                        // row stride (floats) of the fp32 L and T matrices
-constexpr uint32_t I2_L = I2_SCR;             // fp32 [64][68]
-constexpr uint32_t I2_T = I2_SCR + 17408;     // fp32 [64][68]
-constexpr uint32_t I2_P = I2_SCR + 34816;     // fp32 [3][16][16]
-constexpr uint32_t I2_TIMG = I2_SCR + 40960;  // T image 64 x 64
-constexpr uint32_t I2_XT = 0;                 // relative to the stage
-constexpr uint32_t I2_VT = 16384;             // relative to the stage
-constexpr uint32_t I2_WST = I2_SCR;           // W staging image 64 x 128
-constexpr uint32_t I2_FAC = 212992;           // fp32 factor rows, [18][128]
-constexpr int FAC_GPR = 0, FAC_GPE = 4, FAC_FL = 8, FAC_F = 12;  // row indices
-constexpr uint32_t I2_BETA = I2_FAC + 18 * 512;   // 2 stages x fp32 [64]
-constexpr uint32_t I2_BIAS = I2_BETA + 512;       // 2 stages x fp32 [128]
-constexpr uint32_t I2_INFO = I2_BIAS + 1024;      // 2 stages x {int64 t0, len, h, slot; float eA}
-constexpr uint32_t I2_BAR = I2_INFO + 128;        // ld[2], free[2], mma[2]
-constexpr uint32_t I2_TSLOT = I2_BAR + 48;
-constexpr uint32_t I2_TOTAL = I2_BAR + 64 + 1024;
+// Tiles stay token-major ([token][channel], the TMA layout) from load to packet: tcgen05 reads a
+// token-major tile as a K-major operand when the contraction runs over channels and, through an
+// MN-major descriptor, as its transpose when it runs over tokens.  Per item:
+//   G1   gate (Eq. 5) and in-chunk cumulative log-decay G (Eq. 3); thread = (channel, half).
+//   G2   element pass; thread = (4 channels, tokens tg + 8 i): every decay factor and operand
+//        image.  Q^ = Q Gamma overwrites q, X = Gamma K overwrites k, K~ = K e^{G_63 - G} takes
+//        the place of z; the row image and two key images feed the next step.
+//   MMA  A = Tril[(Q Gamma)(K / Gamma)^T] and L = StrictTril[diag(beta)(K Gamma)(K / Gamma)^T]:
+//        one product with M = 128 (64 query rows over 64 key rows), N = 96 (keys scaled to either
+//        reference), K = 128 channels.
+//   INV  T = (I + L)^{-1} in fp32: 16 x 16 diagonal blocks by substitution, then one 16-row and
+//        one 32-row block merge, T21 = -T22 L21 T11.
+//   MMA  W^T = X^T (T diag beta)^T and U^T = V^T (T diag beta)^T, X and V read MN-major.
+//   OUT  packet by bulk copies: W^T, Q^, K~, A, U^T, gamma.
+//
+// Warps 0-15 split every phase (16 consumer warps keep the latency-bound phases fed).
+//
+// Exponent safety.  Each log-decay step lies in (g_min, 0) = (-5, 0), so 16 tokens span less than
+// 80 in the exponent, inside the fp32 / bf16 range of e^{+-88}.  The chunk is cut into two
+// 32-token halves with references p0 = 15 and p1 = 47, 16 tokens from either end of their half.
+// Rows r of half b are scaled by E_r = e^{G_r - G_pb} (|exponent| <= 80).  Keys of half 0 are
+// scaled by e^{G_p0 - G_i} for the products with rows of half 0 (<= e^{80}), and every key by
+// e^{G_p1 - G_i} for the products with rows of half 1 (<= 1 for keys of half 0).  Each factor is
+// the exponential of its own exponent, never a product of two large and small factors, so a key
+// factor that underflows loses at most e^{75 - 87} of a term.  Entries above the diagonal may
+// overflow to inf; they are discarded by selects and never multiplied.
+constexpr int NT2 = 544;      // 16 consumer warps + 1 producer warp
+constexpr int NC2 = 512;      // consumer threads
+constexpr int PRODUCER = 16;  // producer warp
+constexpr uint32_t J_STG_BYTES = 65536;  // 2 stages x [Q | Z | K | V], [64][128] bf16 each (SW128)
+constexpr uint32_t J_TQ = 0, J_TZ = 16384, J_TK = 32768, J_TV = 49152;
+constexpr uint32_t J_G = 2 * J_STG_BYTES;   // fp32 G [64][128]; float4 slot s of row t at s ^ (t % 8)
+constexpr uint32_t J_IMG = J_G + 32768;     // 56 KB working region
+constexpr uint32_t J_ROW = J_IMG;           // row image: q rows over k rows, 128 x 128
+constexpr uint32_t J_KEY = J_IMG + 32768;   // key image, 96 x 128: rows 0-31 = keys 0-31 scaled to p0,
+                                            // rows 32-95 = keys 0-63 scaled to p1
+constexpr int LS = 68;                      // row stride (floats) of the fp32 L and T matrices
+constexpr uint32_t J_L = J_IMG;             // after the A / L product: fp32 L [64][LS]
+constexpr uint32_t J_T = J_IMG + 17408;     // fp32 T [64][LS]
+constexpr uint32_t J_TIMG = J_IMG + 34816;  // (T diag beta) image 64 x 64
+constexpr uint32_t J_AIMG = J_IMG + 43008;  // A image 64 x 64
+constexpr uint32_t J_GAM = J_IMG + 57344;   // gamma fp32 [128]
+constexpr uint32_t J_QTOT = J_GAM + 512;    // G at tokens 15, 31, 47: fp32 [3][128]
+constexpr uint32_t J_BETA = J_QTOT + 2048;  // 2 stages x fp32 [64]
+constexpr uint32_t J_BIAS = J_BETA + 512;   // 2 stages x fp32 [128]
+constexpr uint32_t J_INFO = J_BIAS + 1024;  // 2 stages x {int64 t0, len, h, slot; float eA}
+constexpr uint32_t J_BAR = J_INFO + 128;    // ld[2], free[2], mma
+constexpr uint32_t J_TSLOT = J_BAR + 48;
+constexpr uint32_t J_TOTAL = J_BAR + 64 + 1024;
+// TMEM columns: A / L product (96), W^T (64), U^T (64)
+constexpr uint32_t TM_DA = 0, TM_DB = 32, TM_DW = 96, TM_DU = 160;
 
-__device__ __forceinline__ int fpair(int b, int bp) { return (b * (b - 1)) / 2 + bp; }  // b' < b
+constexpr float LOG2E = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// float index of G[t][c] in the swizzled fp32 G tile
+__device__ __forceinline__ int gsw(int t, int c) { return t * 128 + ((((c >> 2) ^ (t & 7)) << 2) | (c & 3)); }
 
 __device__ __forceinline__ void unpack4(const uint2 &u, float *f) {
     const __nv_bfloat162 *hh = reinterpret_cast<const __nv_bfloat162 *>(&u);
@@ -190,17 +204,100 @@ struct TileMaps {
     CUtensorMap q, k, v, z;
 };
 
-// Consumer-group barrier (warps 0-7, named barrier 1) with tcgen05 ordering.
+// Consumer-group barrier (warps 0-15, named barrier 1) with tcgen05 ordering.
 __device__ __forceinline__ void csync() {
     fence_before_sync();
     named_sync(1, NC2);
     fence_after_sync();
 }
-__device__ __forceinline__ bool csync_and(bool pred) { return __syncthreads_count_named1(pred) == NC2; }
-// Waits on an mbarrier from every consumer thread; CTA-group-uniform result.
+__device__ __forceinline__ bool csync_and(bool pred) {
+    int r;
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.popc.u32 %0, 1, %2, p;\n\t}\n"
+                 : "=r"(r) : "r"((unsigned)pred), "n"(NC2) : "memory");
+    return r == NC2;
+}
+// Waits on an mbarrier from every consumer thread; consumer-uniform result.
 __device__ __forceinline__ bool cwait(uint64_t *bar, uint32_t parity) {
     const bool ok = mbar_wait(bar, parity);
     return csync_and(ok);
+}
+
+// Partial products of the block merges of the UT-transform inverse.  Level 1: P[q + 4 a][jc] =
+// L[ro + q + 4 a][co .. co + 15] . T[co .. co + 15][co + jc], starting at column K0 <= jc (T is zero
+// above the diagonal).  Level 2: the lower-left 32 x 32 block, rows 32 + q + 16 a.
+template <int K0>
+__device__ __forceinline__ void inv_l1_partial(const float *Lm, const float *Tm, int ro, int co, int q, int jc,
+                                               float *p) {
+    float tc[16];
+#pragma unroll
+    for (int k = K0; k < 16; ++k) tc[k] = Tm[(co + k) * LS + co + jc];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const float *lr = Lm + (ro + q + 4 * a) * LS + co;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = K0; k < 16; k += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(lr + k);
+            acc += l4.x * tc[k] + l4.y * tc[k + 1] + l4.z * tc[k + 2] + l4.w * tc[k + 3];
+        }
+        p[a] = acc;
+    }
+}
+template <int K0>
+__device__ __forceinline__ void inv_l2_partial(const float *Lm, const float *Tm, int q, int jc, float *p) {
+    float tc[32];
+#pragma unroll
+    for (int k = K0; k < 32; ++k) tc[k] = Tm[k * LS + jc];
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+        const float *lr = Lm + (32 + q + 16 * a) * LS;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = K0; k < 32; k += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(lr + k);
+            acc += l4.x * tc[k] + l4.y * tc[k + 1] + l4.z * tc[k + 2] + l4.w * tc[k + 3];
+        }
+        p[a] = acc;
+    }
+}
+
+// Element pass for 4 tokens t = tg + 8 i (i = 4 H1 .. 4 H1 + 3) and channels c0 .. c0 + 3.
+template <bool H1>
+__device__ __forceinline__ void element_pass(unsigned char *sm, unsigned char *stg, const float *Gs, int tg,
+                                             int c0, const float *G15, const float *G47, const float *eg15,
+                                             const float *eg47, const float *f63) {
+    const int s4 = c0 >> 2;
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+        const int t = tg + 8 * (4 * H1 + ii);
+        const float4 g4 = *reinterpret_cast<const float4 *>(Gs + t * 128 + ((s4 ^ tg) << 2));
+        const float gt[4] = {g4.x, g4.y, g4.z, g4.w};
+        float qf[4], kf[4];
+        unpack4(*reinterpret_cast<const uint2 *>(stg + J_TQ + img_off(64, t, c0)), qf);
+        unpack4(*reinterpret_cast<const uint2 *>(stg + J_TK + img_off(64, t, c0)), kf);
+        float rq[4], rk[4], k0[4], k1[4], qh[4], xk[4], kt[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float dd = (gt[e] - (H1 ? G47[e] : G15[e])) * LOG2E;
+            const float E = ex2_approx(dd);                         // e^{G_t - G_p}
+            const float f1 = ex2_approx((G47[e] - gt[e]) * LOG2E);  // e^{G_p1 - G_t}
+            rq[e] = qf[e] * E;
+            rk[e] = kf[e] * E;
+            k1[e] = kf[e] * f1;
+            k0[e] = H1 ? 0.f : kf[e] * ex2_approx(-dd);             // e^{G_p0 - G_t}
+            const float eg = E * (H1 ? eg47[e] : eg15[e]);           // e^{G_t}
+            qh[e] = qf[e] * eg;
+            xk[e] = kf[e] * eg;
+            kt[e] = kf[e] * (f1 * f63[e]);                           // e^{G_63 - G_t}
+        }
+        *reinterpret_cast<uint2 *>(sm + J_ROW + img_off(128, t, c0)) = pack4(rq);
+        *reinterpret_cast<uint2 *>(sm + J_ROW + img_off(128, 64 + t, c0)) = pack4(rk);
+        *reinterpret_cast<uint2 *>(sm + J_KEY + img_off(96, 32 + t, c0)) = pack4(k1);
+        if (!H1) *reinterpret_cast<uint2 *>(sm + J_KEY + img_off(96, t, c0)) = pack4(k0);
+        *reinterpret_cast<uint2 *>(stg + J_TQ + img_off(64, t, c0)) = pack4(qh);
+        *reinterpret_cast<uint2 *>(stg + J_TK + img_off(64, t, c0)) = pack4(xk);
+        *reinterpret_cast<uint2 *>(stg + J_TZ + img_off(64, t, c0)) = pack4(kt);
+    }
 }
 
 __global__ void __launch_bounds__(NT2, 1)
@@ -214,26 +311,25 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t W = (int64_t)chunk_start[N] * H;  // work items
     if ((int64_t)blockIdx.x >= W) return;
-    float *G = (float *)(sm + I2_G);
-    float *FAC = (float *)(sm + I2_FAC);
-    uint64_t *bar_ld = (uint64_t *)(sm + I2_BAR);
+    float *Gs = (float *)(sm + J_G);
+    uint64_t *bar_ld = (uint64_t *)(sm + J_BAR);
     uint64_t *bar_free = bar_ld + 2;
-    uint64_t *bar_mma = bar_ld + 4;  // one per row-image buffer: no barrier ever has two phases pending
-    uint32_t *tslot = (uint32_t *)(sm + I2_TSLOT);
+    uint64_t *bar_mma = bar_ld + 4;
+    uint32_t *tslot = (uint32_t *)(sm + J_TSLOT);
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_ld[i], 1);
             mbar_init(&bar_free[i], 1);
-            mbar_init(&bar_mma[i], 1);
         }
+        mbar_init(bar_mma, 1);
     }
     if (warp == 0) tmem_alloc(tslot, 256);
     fence_proxy_async();
     sync_all();
     const uint32_t tb = *tslot;
 
-    if (warp == 8) {
+    if (warp == PRODUCER) {
         // ------------------------------------------------ producer warp
         bool ok = true;
         for (int it = 0;; ++it) {
@@ -249,14 +345,14 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
             int n = 0, len = 0;
             int64_t t0 = 0;
             locate(chunk_start, cu, T, N, slot, n, t0, len);
-            float *bet = (float *)(sm + I2_BETA) + 64 * s;
-            float *bia = (float *)(sm + I2_BIAS) + 128 * s;
+            float *bet = (float *)(sm + J_BETA) + 64 * s;
+            float *bia = (float *)(sm + J_BIAS) + 128 * s;
 #pragma unroll
             for (int r = lane; r < C; r += 32) bet[r] = r < len ? __bfloat162float(beta[(t0 + r) * H + h]) : 0.f;
 #pragma unroll
             for (int c = lane; c < D; c += 32) bia[c] = bias ? bias[h * D + c] : 0.f;
             if (lane == 0) {
-                int64_t *info = (int64_t *)(sm + I2_INFO + 64 * s);
+                int64_t *info = (int64_t *)(sm + J_INFO + 64 * s);
                 info[0] = t0;
                 info[1] = len;
                 info[2] = h;
@@ -266,18 +362,20 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
             __threadfence_block();
             __syncwarp();
             if (lane == 0) {
-                unsigned char *stg = sm + I2_STG + s * I2_STG_BYTES;
-                mbar_arrive_expect_tx(&bar_ld[s], 4u * 16384u);
-                tma_load_3d(stg + I2_TQ, &tm.q, 0, h, (int)t0, &bar_ld[s]);
-                tma_load_3d(stg + I2_TZ, &tm.z, 0, h, (int)t0, &bar_ld[s]);
-                tma_load_3d(stg + I2_TK, &tm.k, 0, h, (int)t0, &bar_ld[s]);
-                tma_load_3d(stg + I2_TV, &tm.v, 0, h, (int)t0, &bar_ld[s]);
+                unsigned char *stg = sm + s * J_STG_BYTES;
+                mbar_arrive_expect_tx(&bar_ld[s], J_STG_BYTES);
+                const CUtensorMap *maps[4] = {&tm.q, &tm.z, &tm.k, &tm.v};
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    tma_load_3d(stg + 16384 * x, maps[x], 0, h, (int)t0, &bar_ld[s]);
+                    tma_load_3d(stg + 16384 * x + 8192, maps[x], 64, h, (int)t0, &bar_ld[s]);
+                }
             }
         }
         if (!ok && lane == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     } else {
-        // ------------------------------------------------ consumer warps 0-7
-        uint32_t mph[2] = {0, 0};
+        // ------------------------------------------------ consumer warps 0-15
+        uint32_t mph = 0;
         bool ok = true;
         int it = 0;
         for (;; ++it) {
@@ -286,345 +384,269 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
             const int s = it & 1;
             ok = cwait(&bar_ld[s], (it >> 1) & 1);
             if (!ok) break;
-            const int64_t *info = (const int64_t *)(sm + I2_INFO + 64 * s);
+            const int64_t *info = (const int64_t *)(sm + J_INFO + 64 * s);
             const int len = (int)info[1];
             const int h = (int)info[2];
             const int64_t slot = info[3];
             const float eA = *reinterpret_cast<const float *>(info + 4);
-            const float *bet = (const float *)(sm + I2_BETA) + 64 * s;
-            const float *bia = (const float *)(sm + I2_BIAS) + 128 * s;
-            unsigned char *stg = sm + I2_STG + s * I2_STG_BYTES;
+            const float *bet = (const float *)(sm + J_BETA) + 64 * s;
+            const float *bia = (const float *)(sm + J_BIAS) + 128 * s;
+            unsigned char *stg = sm + s * J_STG_BYTES;
             unsigned char *pk = packets + ((size_t)slot * H + h) * PK_STRIDE;
-            if (len < C) {  // clear rows past the end of the sequence (uniform branch)
-                for (int idx = tid; idx < 4 * (C - len) * 16; idx += NC2) {
-                    const int tile = idx / ((C - len) * 16), rem = idx % ((C - len) * 16);
-                    const int r = len + rem / 16, u = rem % 16;
-                    reinterpret_cast<uint4 *>(stg + tile * 16384 + r * 256)[u] = make_uint4(0, 0, 0, 0);
-                }
-                csync();
-            }
 
-            // ---- phase 1: gate (Eq. 5) and in-chunk cumulative log-decay (Eq. 3): thread = (channel, half)
-            //      g = g_min / (1 + e^{-x}) with fast exp and division (a few ulp each)
+            // ---- G1: gate (Eq. 5) and in-chunk cumulative log-decay (Eq. 3), thread = (channel,
+            //      16-token quarter).  Tokens past the end of the sequence get g = 0 (an exact no-op).
             {
-                const int c = tid & 127, r0 = (tid >> 7) * 32;
+                const int c = tid & 127, qt = tid >> 7;
                 const float bc = bia[c];
-                const bf16 *Z = reinterpret_cast<const bf16 *>(stg + I2_TZ);
-                float gv[32];
+                float gv[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float x = eA * (__bfloat162float(Z[(r0 + i) * D + c]) + bc);
-                    gv[i] = (r0 + i < len) ? __fdividef(g_min, 1.0f + __expf(-x)) : 0.f;
+                for (int i = 0; i < 16; ++i) {
+                    const float zf =
+                        __bfloat162float(*reinterpret_cast<const bf16 *>(stg + J_TZ + img_off(64, 16 * qt + i, c)));
+                    gv[i] = __fdividef(g_min, 1.0f + __expf(-eA * (zf + bc)));
+                }
+                if (len < C) {  // ragged tail (uniform branch, outside the arithmetic above)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (16 * qt + i >= len) gv[i] = 0.f;
                 }
 #pragma unroll
-                for (int i = 1; i < 32; ++i) gv[i] += gv[i - 1];
-                if (r0 == 0) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) G[i * D + c] = gv[i];
-                }
+                for (int i = 1; i < 16; ++i) gv[i] += gv[i - 1];
+                float *qtot = (float *)(sm + J_QTOT);
+                if (qt < 3) qtot[qt * 128 + c] = gv[15];
                 csync();
-                if (r0 == 32) {
-                    const float base = G[31 * D + c];
+                float base = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) G[(32 + i) * D + c] = gv[i] + base;
-                }
-                csync();
-            }
-            // ---- phase 2a: per-(block, channel) factors
-            {
-                const int c = tid & 127;
-                if (tid < 128) {
+                for (int u = 0; u < 3; ++u)
+                    if (u < qt) base += qtot[u * 128 + c];
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        const float gp = G[(16 * b + 15) * D + c];
-                        FAC[(FAC_GPR + b) * D + c] = gp;
-                        FAC[(FAC_GPE + b) * D + c] = __expf(gp);
-                        FAC[(FAC_FL + b) * D + c] = __expf(G[63 * D + c] - gp);
-                    }
-                } else {
-#pragma unroll
-                    for (int b = 1; b < 4; ++b)
-#pragma unroll
-                        for (int bp = 0; bp < b; ++bp)
-                            FAC[(FAC_F + fpair(b, bp)) * D + c] =
-                                __expf(G[(16 * b + 15) * D + c] - G[(16 * bp + 15) * D + c]);
+                for (int i = 0; i < 16; ++i) Gs[gsw(16 * qt + i, c)] = gv[i] + base;
+                if (tid == 0 && it > 0) {  // the previous item's packet copies have read their sources
+                    bulk_wait_read0();
+                    mbar_arrive(&bar_free[s ^ 1]);
                 }
                 csync();
             }
-            // ---- phase 2b: E in place of G; key-block images, Q^ and K~^T (packet)
+            // ---- G2: element pass, thread = (channels c0..c0+3, tokens tg + 8 i, one chunk half)
             {
-                const int rg = tid >> 5, c0 = (tid & 31) * 4, b = rg >> 1;
-                const bf16 *Q = reinterpret_cast<const bf16 *>(stg + I2_TQ);
-                const bf16 *K = reinterpret_cast<const bf16 *>(stg + I2_TK);
-                const float4 gp = *reinterpret_cast<const float4 *>(&FAC[(FAC_GPR + b) * D + c0]);
-                const float4 ge = *reinterpret_cast<const float4 *>(&FAC[(FAC_GPE + b) * D + c0]);
-                const float4 fl = *reinterpret_cast<const float4 *>(&FAC[(FAC_FL + b) * D + c0]);
-                const float gpv[4] = {gp.x, gp.y, gp.z, gp.w}, gev[4] = {ge.x, ge.y, ge.z, ge.w};
-                const float flv[4] = {fl.x, fl.y, fl.z, fl.w};
-                float kt[4][8];  // K~^T chunks: [channel][token]
+                const int tg = lane & 7, cgl = lane >> 3, th = warp >> 3;
+                const int c0 = 16 * (warp & 7) + 4 * cgl, s4 = c0 >> 2;
+                const float4 a15 = *reinterpret_cast<const float4 *>(Gs + 15 * 128 + ((s4 ^ 7) << 2));
+                const float4 a47 = *reinterpret_cast<const float4 *>(Gs + 47 * 128 + ((s4 ^ 7) << 2));
+                const float4 a63 = *reinterpret_cast<const float4 *>(Gs + 63 * 128 + ((s4 ^ 7) << 2));
+                const float G15[4] = {a15.x, a15.y, a15.z, a15.w}, G47[4] = {a47.x, a47.y, a47.z, a47.w};
+                const float G63[4] = {a63.x, a63.y, a63.z, a63.w};
+                float eg15[4], eg47[4], f63[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = rg * 8 + i;
-                    float kf[4], qf[4], Ev[4], kh[4], qh[4];
-                    unpack4(*reinterpret_cast<const uint2 *>(K + r * D + c0), kf);
-                    unpack4(*reinterpret_cast<const uint2 *>(Q + r * D + c0), qf);
-                    const float4 g4 = *reinterpret_cast<const float4 *>(&G[r * D + c0]);
-                    const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float d = gv[e] - gpv[e];
-                        const float E = __expf(d), Ei = __expf(-d);
-                        Ev[e] = E;
-                        kh[e] = kf[e] * Ei;
-                        qh[e] = qf[e] * E * gev[e];
-                        kt[e][i] = kf[e] * Ei * flv[e];
-                    }
-                    *reinterpret_cast<float4 *>(&G[r * D + c0]) = make_float4(Ev[0], Ev[1], Ev[2], Ev[3]);
-                    *reinterpret_cast<uint2 *>(sm + I2_KEY + b * 4096 + img_off(16, r & 15, c0)) = pack4(kh);
-                    *reinterpret_cast<uint2 *>(pk + PK_Q + img_off(64, r, c0)) = pack4(qh);
+                for (int e = 0; e < 4; ++e) {
+                    eg15[e] = ex2_approx(G15[e] * LOG2E);
+                    eg47[e] = ex2_approx(G47[e] * LOG2E);
+                    f63[e] = ex2_approx((G63[e] - G47[e]) * LOG2E);
                 }
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    *reinterpret_cast<uint4 *>(pk + PK_K + img_chunk_off(128, c0 + e, rg)) = pack8(kt[e]);
-                if (tid < 128) *reinterpret_cast<float *>(pk + PK_G + 4 * tid) = FAC[(FAC_GPE + 3) * D + tid];
-                if (tid == 0 && it > 0) bulk_wait_read0();  // previous item's W staging (row image A) was read
-                csync();
-            }
-            // ---- phase 3: row images for key block b' (rows r >= 16 b'), one MMA each.  Each thread
-            //      caches x_r e^{G_r - G_p(r)} for its 8 (side, row) items; block b' scales them by
-            //      e^{G_p(r) - G_p'}.  Rows r < 16 b' are left stale: every entry they produce lies above
-            //      the diagonal and is discarded by the causal mask.  Two image buffers alternate.
-            {
-                const int j = tid & 15, ri = tid >> 4, c0 = j * 8;
-                float xe[2][4][8];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int r = ri + 16 * m;
-                    float qf[8], kf[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(stg + I2_TQ + r * 256 + c0 * 2), qf);
-                    unpack8(*reinterpret_cast<const uint4 *>(stg + I2_TK + r * 256 + c0 * 2), kf);
-                    const float4 e0 = *reinterpret_cast<const float4 *>(&G[r * D + c0]);
-                    const float4 e1 = *reinterpret_cast<const float4 *>(&G[r * D + c0 + 4]);
-                    const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        xe[0][m][e] = qf[e] * ev[e];
-                        xe[1][m][e] = kf[e] * ev[e];
-                    }
-                }
-                csync();  // the Q tile (row image B) is about to be overwritten
-                const uint32_t idesc16 = idesc_bf16(128, 16);
-                auto build = [&](int bq, unsigned char *img) {
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        if (m < bq) continue;
-                        const int r = ri + 16 * m;
-                        float fv[8];
-                        if (m == bq) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) fv[e] = 1.f;
-                        } else {
-                            const float *F = &FAC[(FAC_F + fpair(m, bq)) * D + c0];
-                            const float4 f0 = *reinterpret_cast<const float4 *>(F);
-                            const float4 f1 = *reinterpret_cast<const float4 *>(F + 4);
-                            fv[0] = f0.x; fv[1] = f0.y; fv[2] = f0.z; fv[3] = f0.w;
-                            fv[4] = f1.x; fv[5] = f1.y; fv[6] = f1.z; fv[7] = f1.w;
-                        }
-#pragma unroll
-                        for (int side = 0; side < 2; ++side) {
-                            float o[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) o[e] = xe[side][m][e] * fv[e];
-                            *reinterpret_cast<uint4 *>(img + img_chunk_off(128, side * 64 + r, j)) = pack8(o);
-                        }
-                    }
-                };
-                unsigned char *imgA = sm + I2_ROW, *imgB = stg;
-#pragma unroll
-                for (int round = 0; round < 2; ++round) {
-                    if (round == 1) {  // both buffers are read by the first two MMAs
-                        const bool w0 = mbar_wait(&bar_mma[0], mph[0] & 1);
-                        const bool w1 = mbar_wait(&bar_mma[1], mph[1] & 1);
-                        ++mph[0];
-                        ++mph[1];
-                        ok = csync_and(ok && w0 && w1);
-                        fence_after_sync();
-                    }
-                    build(2 * round, imgA);
-                    build(2 * round + 1, imgB);
-                    fence_proxy_async();
-                    csync();
-                    if (ok && tid == 0) {
-                        mma_bf16_k(tb + 32 * round, smem_u32(imgA), 128, smem_u32(sm + I2_KEY + 2 * round * 4096),
-                                   16, 8, idesc16, false);
-                        mma_commit(&bar_mma[0]);
-                        mma_bf16_k(tb + 32 * round + 16, smem_u32(imgB), 128,
-                                   smem_u32(sm + I2_KEY + (2 * round + 1) * 4096), 16, 8, idesc16, false);
-                        mma_commit(&bar_mma[1]);
-                    }
-                }
-                const bool w0 = mbar_wait(&bar_mma[0], mph[0] & 1);
-                const bool w1 = mbar_wait(&bar_mma[1], mph[1] & 1);
-                ++mph[0];
-                ++mph[1];
-                ok = csync_and(ok && w0 && w1);
-                fence_after_sync();
-            }
-            if (!ok) break;
-            // ---- phase 4: A rows -> packet, L rows -> fp32 smem (warp w and w+4 split the 64 columns)
-            float *Lm = (float *)(sm + I2_L);
-            float *Tm = (float *)(sm + I2_T);
-            {
-                const int lq = warp & 3, cbase = (warp >> 2) * 32;
-                const int m = lq * 32 + lane;  // TMEM lane = row
-                float d[32];
-                tmem_ld32(tmem_addr(tb, lq * 32, cbase), d);
-                if (m < 64) {
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        float o[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = (cbase + 8 * jj + e <= m) ? d[8 * jj + e] : 0.f;
-                        *reinterpret_cast<uint4 *>(pk + PK_A + img_chunk_off(64, m, cbase / 8 + jj)) = pack8(o);
-                    }
-                } else {
-                    const int r = m - 64;
-                    const float br = bet[r];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        float4 v4;
-                        v4.x = (cbase + i < r) ? br * d[i] : 0.f;
-                        v4.y = (cbase + i + 1 < r) ? br * d[i + 1] : 0.f;
-                        v4.z = (cbase + i + 2 < r) ? br * d[i + 2] : 0.f;
-                        v4.w = (cbase + i + 3 < r) ? br * d[i + 3] : 0.f;
-                        *reinterpret_cast<float4 *>(&Lm[r * LS + cbase + i]) = v4;
-                    }
-                }
-            }
-            csync();
-            // ---- phase 5 (warps 0-3: 16x16 diagonal blocks of (I + L)^{-1}) alongside
-            //      phase 6 (warps 4-7: (beta Gamma K)^T and (beta V)^T images in the stage)
-            if (warp < 4) {
-                if (lane < 16) {
-                    const int base = 16 * warp, c = lane;
-                    float x[16];
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        float sacc = (r == c) ? 1.f : 0.f;
-#pragma unroll
-                        for (int i = 0; i < r; ++i) sacc -= Lm[(base + r) * LS + base + i] * x[i];
-                        x[r] = (r < c) ? 0.f : sacc;
-                    }
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) Tm[(base + r) * LS + base + c] = x[r];
-                }
-            } else {
-                const int u = tid - 128, rg = u & 7, c0 = (u >> 3) * 8, b = rg >> 1;
-                const float *gp = &FAC[(FAC_GPE + b) * D + c0];
-                const float4 g0 = *reinterpret_cast<const float4 *>(gp), g1 = *reinterpret_cast<const float4 *>(gp + 4);
-                const float gev[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-                float xt[8][8], vt[8][8];  // [channel][token]
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = rg * 8 + i;
-                    float kf[8], vf[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(stg + I2_TK + r * 256 + c0 * 2), kf);
-                    unpack8(*reinterpret_cast<const uint4 *>(stg + I2_TV + r * 256 + c0 * 2), vf);
-                    const float4 e0 = *reinterpret_cast<const float4 *>(&G[r * D + c0]);
-                    const float4 e1 = *reinterpret_cast<const float4 *>(&G[r * D + c0 + 4]);
-                    const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-                    const float br = bet[r];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        xt[e][i] = br * kf[e] * ev[e] * gev[e];
-                        vt[e][i] = br * vf[e];
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    *reinterpret_cast<uint4 *>(stg + I2_XT + img_chunk_off(128, c0 + e, rg)) = pack8(xt[e]);
-                    *reinterpret_cast<uint4 *>(stg + I2_VT + img_chunk_off(128, c0 + e, rg)) = pack8(vt[e]);
-                }
-            }
-            csync();
-            // off-diagonal blocks, level d = i - j: P = sum_{m=j}^{i-1} L_im T_mj, then T_ij = -T_ii P.
-            // A thread owns 4 consecutive columns of one row of one block.
-            {
-                float *P = (float *)(sm + I2_P);
-#pragma unroll
-                for (int dlev = 1; dlev <= 3; ++dlev) {
-                    const int units = (4 - dlev) * 64;
-                    const int blk = tid >> 6, a = (tid >> 2) & 15, bq = (tid & 3) * 4;
-                    const int i = blk + dlev, jb = blk;
-                    if (tid < units) {
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        const float *Lrow = &Lm[(16 * i + a) * LS + 16 * jb];
-#pragma unroll 8
-                        for (int t = 0; t < 16 * dlev; ++t) {
-                            const float l = Lrow[t];
-                            const float4 tv = *reinterpret_cast<const float4 *>(&Tm[(16 * jb + t) * LS + 16 * jb + bq]);
-                            acc.x += l * tv.x; acc.y += l * tv.y; acc.z += l * tv.z; acc.w += l * tv.w;
-                        }
-                        *reinterpret_cast<float4 *>(&P[blk * 256 + a * 16 + bq]) = acc;
-                    }
-                    csync();
-                    if (tid < units) {
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        const float *Trow = &Tm[(16 * i + a) * LS + 16 * i];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            if (e <= a) {
-                                const float t = Trow[e];
-                                const float4 pv = *reinterpret_cast<const float4 *>(&P[blk * 256 + e * 16 + bq]);
-                                acc.x += t * pv.x; acc.y += t * pv.y; acc.z += t * pv.z; acc.w += t * pv.w;
-                            }
-                        }
-                        *reinterpret_cast<float4 *>(&Tm[(16 * i + a) * LS + 16 * jb + bq]) =
-                            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-                    }
-                    csync();
-                }
-                for (int idx = tid; idx < 64 * 8; idx += NC2) {
-                    const int r = idx >> 3, jj = idx & 7;
-                    float o[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] = (8 * jj + e <= r) ? Tm[r * LS + 8 * jj + e] : 0.f;
-                    *reinterpret_cast<uint4 *>(sm + I2_TIMG + img_chunk_off(64, r, jj)) = pack8(o);
-                }
+                if (tg == 0 && th == 0)
+                    *reinterpret_cast<float4 *>(sm + J_GAM + 4 * c0) =
+                        make_float4(ex2_approx(G63[0] * LOG2E), ex2_approx(G63[1] * LOG2E),
+                                    ex2_approx(G63[2] * LOG2E), ex2_approx(G63[3] * LOG2E));
+                if (th) element_pass<true>(sm, stg, Gs, tg, c0, G15, G47, eg15, eg47, f63);
+                else element_pass<false>(sm, stg, Gs, tg, c0, G15, G47, eg15, eg47, f63);
             }
             fence_proxy_async();
             csync();
-            // ---- phase 7: W^T = X^T T^T (TMEM cols 64..127), U^T = (beta V)^T T^T (cols 128..191)
             if (tid == 0) {
-                const uint32_t idesc64 = idesc_bf16(128, 64);
-                mma_bf16_k(tb + 64, smem_u32(stg + I2_XT), 128, smem_u32(sm + I2_TIMG), 64, 4, idesc64, false);
-                mma_bf16_k(tb + 128, smem_u32(stg + I2_VT), 128, smem_u32(sm + I2_TIMG), 64, 4, idesc64, false);
-                mma_commit(&bar_mma[0]);
+                // one product, N = 96: columns 0-31 against keys scaled to p0, 32-95 against keys scaled to p1
+                mma_bf16_k(tb + TM_DA, smem_u32(sm + J_ROW), 128, smem_u32(sm + J_KEY), 96, 8, idesc_bf16(128, 96),
+                           false);
+                mma_commit(bar_mma);
+                bulk_s2g(pk + PK_Q, stg + J_TQ, 16384);
+                bulk_s2g(pk + PK_K, stg + J_TZ, 16384);
+                bulk_commit();
             }
-            ok = cwait(&bar_mma[0], mph[0] & 1);
-            ++mph[0];
+            ok = cwait(bar_mma, mph & 1);
+            ++mph;
             if (!ok) break;
             fence_after_sync();
-            // ---- phase 8: W (through an smem image, one bulk store) and U^T rows to the packet
+            // ---- A rows -> A image (causal, diagonal kept); L rows -> fp32 (strictly lower, times beta).
+            //      Rows of the first half take keys 0-31 from columns 0-31, rows of the second half keys
+            //      0-63 from columns 32-95; the four warps of a TMEM lane quarter split the columns.
+            float *Lm = (float *)(sm + J_L);
+            float *Tm = (float *)(sm + J_T);
             {
-                const int lq = warp & 3, rbase = (warp >> 2) * 32;
-                const int c = lq * 32 + lane;
-                float d[32];
-                tmem_ld32(tmem_addr(tb, lq * 32, 64 + rbase), d);
+                const int lq = warp & 3, cp = warp >> 2;
+                const int r = (32 * lq + lane) & 63;  // token row
+                if ((lq & 1) == 0) {
+                    float d[8];
+                    tmem_ld8(tmem_addr(tb + TM_DA, 32 * lq, 8 * cp), d);
+                    if (lq == 0) {
+                        float o[8];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    *reinterpret_cast<bf16 *>(sm + I2_WST + img_off(64, rbase + i, c)) = __float2bfloat16_rn(d[i]);
-                tmem_ld32(tmem_addr(tb, lq * 32, 128 + rbase), d);
+                        for (int e = 0; e < 8; ++e) o[e] = (8 * cp + e <= r) ? d[e] : 0.f;
+                        *reinterpret_cast<uint4 *>(sm + J_AIMG + img_chunk_off(64, r, cp)) = pack8(o);
+                        *reinterpret_cast<uint4 *>(sm + J_AIMG + img_chunk_off(64, r, 4 + cp)) = make_uint4(0, 0, 0, 0);
+                    } else {
+                        const float br = bet[r];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                    *reinterpret_cast<uint4 *>(pk + PK_U + img_chunk_off(128, c, rbase / 8 + jj)) = pack8(d + 8 * jj);
+                        for (int e = 0; e < 8; e += 4) {
+                            const int i = 8 * cp + e;
+                            *reinterpret_cast<float4 *>(&Lm[r * LS + i]) =
+                                make_float4((i < r) ? br * d[e] : 0.f, (i + 1 < r) ? br * d[e + 1] : 0.f,
+                                            (i + 2 < r) ? br * d[e + 2] : 0.f, (i + 3 < r) ? br * d[e + 3] : 0.f);
+                        }
+                    }
+                } else {
+                    float d[16];
+                    tmem_ld16(tmem_addr(tb + TM_DB, 32 * lq, 16 * cp), d);
+                    if (lq == 1) {
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int cj = 2 * cp + jj;
+                            float o[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) o[e] = (8 * cj + e <= r) ? d[8 * jj + e] : 0.f;
+                            *reinterpret_cast<uint4 *>(sm + J_AIMG + img_chunk_off(64, r, cj)) = pack8(o);
+                        }
+                    } else {
+                        const float br = bet[r];
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4) {
+                            const int i = 16 * cp + e;
+                            *reinterpret_cast<float4 *>(&Lm[r * LS + i]) =
+                                make_float4((i < r) ? br * d[e] : 0.f, (i + 1 < r) ? br * d[e + 1] : 0.f,
+                                            (i + 2 < r) ? br * d[e + 2] : 0.f, (i + 3 < r) ? br * d[e + 3] : 0.f);
+                        }
+                    }
+                }
+            }
+            csync();
+            // ---- T = (I + L)^{-1}.  Level 0: the four 16 x 16 diagonal blocks, one column per thread,
+            //      by forward substitution; the blocks above the diagonal inside each 32-row half are
+            //      zeroed so that the merges below can run full-length dot products.
+            if (tid < 64) {
+                const int b = tid >> 4, jc = tid & 15, o0 = 16 * b;
+                float x[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) x[r] = (r == jc) ? 1.f : 0.f;
+#pragma unroll
+                for (int i = 0; i < 15; ++i) {
+                    const float xi = x[i];
+#pragma unroll
+                    for (int r = i + 1; r < 16; ++r) x[r] -= Lm[(o0 + r) * LS + o0 + i] * xi;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tm[(o0 + r) * LS + o0 + jc] = x[r];
+                if ((b & 1) == 0) {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) Tm[(o0 + r) * LS + o0 + 16 + jc] = 0.f;
+                }
+            }
+            csync();
+            // Level 1: T_10 = -T_11 L_10 T_00 inside each 32-row half.  Thread = (half mg, column jc,
+            // rows q + 4 a); the four threads of a column share their partial products by shuffles.
+            // T_00 column jc is zero above row jc and T_11 is lower triangular, so the dot products
+            // start at the warp's lowest column and stop at the row.
+            if (tid < 128) {
+                const int mg = tid >> 6, q = lane & 3;
+                const int jc = ((tid >> 5) & 1) * 8 + (lane >> 2);
+                const int ro = 32 * mg + 16, co = 32 * mg;
+                float p[4];
+                if (warp & 1) inv_l1_partial<8>(Lm, Tm, ro, co, q, jc, p);
+                else inv_l1_partial<0>(Lm, Tm, ro, co, q, jc, p);
+                float pc[16];  // P[:, jc], row q2 + 4 a from lane q2
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) pc[q2 + 4 * a] = __shfl_sync(0xffffffffu, p[a], (lane & ~3) | q2);
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const float *tr = Tm + (ro + q + 4 * a) * LS + ro;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 4 * (a + 1); k += 4) {
+                        const float4 t4 = *reinterpret_cast<const float4 *>(tr + k);
+                        acc += t4.x * pc[k] + t4.y * pc[k + 1] + t4.z * pc[k + 2] + t4.w * pc[k + 3];
+                    }
+                    Tm[(ro + q + 4 * a) * LS + co + jc] = -acc;
+                }
+            }
+            csync();
+            // Level 2: T_[23][01] = -T_[23][23] L_[23][01] T_[01][01] on 32 x 32 blocks.  Thread =
+            // (column jc, rows q + 16 a); the sixteen threads of a column share partial products.
+            {
+                const int q = lane & 15, jc = 2 * warp + (lane >> 4);
+                float p[2];
+                switch (warp >> 1) {
+                    case 0: inv_l2_partial<0>(Lm, Tm, q, jc, p); break;
+                    case 1: inv_l2_partial<4>(Lm, Tm, q, jc, p); break;
+                    case 2: inv_l2_partial<8>(Lm, Tm, q, jc, p); break;
+                    case 3: inv_l2_partial<12>(Lm, Tm, q, jc, p); break;
+                    case 4: inv_l2_partial<16>(Lm, Tm, q, jc, p); break;
+                    case 5: inv_l2_partial<20>(Lm, Tm, q, jc, p); break;
+                    case 6: inv_l2_partial<24>(Lm, Tm, q, jc, p); break;
+                    default: inv_l2_partial<28>(Lm, Tm, q, jc, p); break;
+                }
+                float pc[32];
+#pragma unroll
+                for (int q2 = 0; q2 < 16; ++q2)
+#pragma unroll
+                    for (int a = 0; a < 2; ++a) pc[q2 + 16 * a] = __shfl_sync(0xffffffffu, p[a], (lane & ~15) | q2);
+#pragma unroll
+                for (int a = 0; a < 2; ++a) {
+                    const float *tr = Tm + (32 + q + 16 * a) * LS + 32;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 16 * (a + 1); k += 4) {
+                        const float4 t4 = *reinterpret_cast<const float4 *>(tr + k);
+                        acc += t4.x * pc[k] + t4.y * pc[k + 1] + t4.z * pc[k + 2] + t4.w * pc[k + 3];
+                    }
+                    Tm[(32 + q + 16 * a) * LS + jc] = -acc;
+                }
+            }
+            csync();
+            // (T diag beta) image: row r, keys 8 jj .. 8 jj + 7; entries above the diagonal are zero
+            {
+                const int r = tid >> 3, jj = tid & 7;
+                const float4 t0v = *reinterpret_cast<const float4 *>(Tm + r * LS + 8 * jj);
+                const float4 t1v = *reinterpret_cast<const float4 *>(Tm + r * LS + 8 * jj + 4);
+                const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = (8 * jj + e <= r) ? tv[e] * bet[8 * jj + e] : 0.f;
+                *reinterpret_cast<uint4 *>(sm + J_TIMG + img_chunk_off(64, r, jj)) = pack8(o);
             }
             fence_proxy_async();
             csync();
             if (tid == 0) {
-                bulk_s2g(pk + PK_W, sm + I2_WST, 16384);
+                const uint32_t id = idesc_bf16(128, 64, true, false);
+                mma_bf16_mnk(tb + TM_DW, smem_u32(stg + J_TK), 8192, smem_u32(sm + J_TIMG), 64, 4, id, false);
+                mma_bf16_mnk(tb + TM_DU, smem_u32(stg + J_TV), 8192, smem_u32(sm + J_TIMG), 64, 4, id, false);
+                mma_commit(bar_mma);
+            }
+            ok = cwait(bar_mma, mph & 1);
+            ++mph;
+            if (!ok) break;
+            fence_after_sync();
+            // ---- W^T and U^T rows (channel-major images) into the dead X and V tiles
+            {
+                const int lq = warp & 3, cq = warp >> 2;
+                const int c = 32 * lq + lane;
+                float d[16];
+                tmem_ld16(tmem_addr(tb + TM_DW, 32 * lq, 16 * cq), d);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+                    *reinterpret_cast<uint4 *>(stg + J_TK + img_chunk_off(128, c, 2 * cq + jj)) = pack8(d + 8 * jj);
+                tmem_ld16(tmem_addr(tb + TM_DU, 32 * lq, 16 * cq), d);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+                    *reinterpret_cast<uint4 *>(stg + J_TV + img_chunk_off(128, c, 2 * cq + jj)) = pack8(d + 8 * jj);
+            }
+            fence_proxy_async();
+            csync();
+            if (tid == 0) {
+                bulk_s2g(pk + PK_W, stg + J_TK, 16384);
+                bulk_s2g(pk + PK_U, stg + J_TV, 16384);
+                bulk_s2g(pk + PK_A, sm + J_AIMG, 8192);
+                bulk_s2g(pk + PK_G, sm + J_GAM, 512);
                 bulk_commit();
-                mbar_arrive(&bar_free[s]);  // this stage may be refilled
             }
         }
         if (tid == 0) bulk_wait0();
@@ -670,11 +692,11 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lq = warp & 3;
     const int j = lq * 32 + lane;  // value channel = TMEM lane = S^T row
-    uint64_t *bar_ld = (uint64_t *)(sm + CS_BAR);             // [2] packet stage loaded
-    uint64_t *bar_v = bar_ld + 2, *bar_s = bar_ld + 3;        // V product / state update done
-    uint64_t *bar_o = bar_ld + 4;                             // [2] all MMAs of a chunk done
-    uint64_t *bar_free = bar_ld + 6;                          // [2] O buffer released by the output path
-    uint64_t *bar_simg = bar_ld + 8, *bar_vimg = bar_ld + 9;  // S^T / V~^T images ready
+    uint64_t *bar_ld = (uint64_t *)(sm + CS_BAR);              // [3] packet stage loaded
+    uint64_t *bar_v = bar_ld + 3, *bar_s = bar_ld + 4;         // V product / state update done
+    uint64_t *bar_o = bar_ld + 5;                              // [2] all MMAs of a chunk done
+    uint64_t *bar_free = bar_ld + 7;                           // [2] O buffer released by the output path
+    uint64_t *bar_simg = bar_ld + 9, *bar_vimg = bar_ld + 10;  // S^T / V~^T images ready
     uint32_t *tslot = (uint32_t *)(sm + CS_TSLOT);
     int *s_fail = (int *)(sm + CS_TSLOT + 8);
     const int64_t kk0 = (int64_t)seg_i * seg_len;
@@ -691,6 +713,7 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
     if (tid == 0) {
         mbar_init(&bar_ld[0], 1);
         mbar_init(&bar_ld[1], 1);
+        mbar_init(&bar_ld[2], 1);
         mbar_init(bar_v, 1);
         mbar_init(bar_s, 1);
         mbar_init(&bar_o[0], 1);
@@ -707,25 +730,30 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
     const uint32_t tb = *tslot;
     const uint32_t tS = tb, tV = tb + 128, tO0 = tb + 192;  // S^T 128 cols, V~^T 64, O^T 2 x 64
     auto packet = [&](int kk) { return packets + ((size_t)(c_begin + kk) * H + h) * PK_STRIDE; };
+    auto stage = [&](int kk) { return sm + (kk % CS_NST) * CS_ST_BYTES; };
+    auto load_stage = [&](int kk) {
+        uint64_t *b = &bar_ld[kk % CS_NST];
+        mbar_arrive_expect_tx(b, CS_ST_TX);
+        bulk_g2s(stage(kk), packet(kk), CS_PK_MMA, b);
+        bulk_g2s(stage(kk) + CS_G, packet(kk) + PK_G, 512, b);
+    };
     if (tid == 0) {
-        for (int kk = 0; kk < 2 && kk < nc; ++kk) {
-            mbar_arrive_expect_tx(&bar_ld[kk], PK_BYTES);
-            bulk_g2s(sm + (kk ? CS_STAGE1 : CS_STAGE0), packet(kk), PK_BYTES, &bar_ld[kk]);
-        }
+        for (int kk = 0; kk < (int)CS_NST && kk < nc; ++kk) load_stage(kk);
     }
 
     if (warp == 12) {
         // ------------------------------------------------ MMA issue (one thread)
         if (lane == 0) {
-            const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128);
+            const uint32_t id64 = idesc_bf16(128, 64), id64mn = idesc_bf16(128, 64, false, true);
+            const uint32_t id128mn = idesc_bf16(128, 128, false, true);
             bool ok = true;
             for (int kk = 0; kk < nc && ok; ++kk) {
-                unsigned char *P = sm + ((kk & 1) ? CS_STAGE1 : CS_STAGE0);
+                unsigned char *P = stage(kk);
                 const uint32_t tO = tO0 + 64 * (kk & 1);
                 ok = mbar_wait(bar_simg, kk & 1);  // S^T image of S_kk written, packet kk resident
                 if (!ok) break;
                 fence_after_sync();
-                mma_bf16_k(tV, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_W), 64, 8, id64, false);
+                mma_bf16_kmn(tV, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_W), 8192, 8, id64mn, false);
                 mma_commit(bar_v);
                 if (kk >= 2) ok = mbar_wait(&bar_free[kk & 1], ((kk >> 1) - 1) & 1);  // O buffer read
                 if (!ok) break;
@@ -734,7 +762,7 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
                 ok = mbar_wait(bar_vimg, kk & 1);  // V~^T image written, TMEM S scaled by gamma_kk
                 if (!ok) break;
                 fence_after_sync();
-                mma_bf16_k(tS, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_K), 128, 4, id128, true);
+                mma_bf16_kmn(tS, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_K), 8192, 4, id128mn, true);
                 mma_commit(bar_s);
                 mma_bf16_k(tO, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_A), 64, 4, id64, true);
                 mma_commit(&bar_o[kk & 1]);
@@ -749,11 +777,8 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
             ok = ok && mbar_wait(&bar_o[kk & 1], (kk >> 1) & 1);
             if (!ok) break;
             fence_after_sync();
-            // every MMA of chunk kk has completed: packet stage kk & 1 can take chunk kk + 2
-            if (ot == 0 && kk + 2 < nc) {
-                mbar_arrive_expect_tx(&bar_ld[kk & 1], PK_BYTES);
-                bulk_g2s(sm + ((kk & 1) ? CS_STAGE1 : CS_STAGE0), packet(kk + 2), PK_BYTES, &bar_ld[kk & 1]);
-            }
+            // every MMA of chunk kk has completed: its packet stage can take chunk kk + 3
+            if (ot == 0 && kk + (int)CS_NST < nc) load_stage(kk + CS_NST);
             const int64_t tp = s_tok + (int64_t)kk * C;
             const int lenp = (int)min((int64_t)C, e_tok - tp);
             bf16 *oj = o + (tp * H + h) * D + j;
@@ -794,7 +819,7 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
                 for (int e = 0; e < 64; ++e) final_state[st_off + (size_t)(64 * hf + e) * D + j] = sreg[e];
             }
             if (ok && nc > 0) {  // S_0 image; TMEM gets S_0 Diag(gamma_0)
-                const float *gam = (const float *)(sm + CS_STAGE0 + PK_G);
+                const float *gam = (const float *)(stage(0) + CS_G);
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 8)
                     *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, (64 * hf + c0) / 8)) =
@@ -813,9 +838,18 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
         fence_before_sync();
         named_sync(1, 256);
         if (tid == 0 && nc > 0) mbar_arrive(bar_simg);
+        // U^T row j, columns [32 hf, 32 hf + 32) of chunks kk and kk + 1 (read-only global loads)
+        auto load_u = [&](int kk, uint4 *u4) {
+            const unsigned char *src = packet(kk) + PK_U;
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh)
+                u4[hh] = __ldg(reinterpret_cast<const uint4 *>(src + img_chunk_off(128, j, 4 * hf + hh)));
+        };
+        uint4 ua[4], ub[4];
+        if (nc > 0) load_u(0, ua);
+        if (nc > 1) load_u(1, ub);
         for (int kk = 0; kk < nc && ok; ++kk) {
             // invariant: packet kk resident; S^T image = bf16(S_kk); TMEM S^T = S_kk^T Diag(gamma_kk)
-            unsigned char *P = sm + ((kk & 1) ? CS_STAGE1 : CS_STAGE0);
             ok = mbar_wait(bar_v, kk & 1);
             ok = (__syncthreads_count_named1(ok) == 256) && (*(volatile int *)s_fail == 0);
             if (!ok) break;
@@ -826,11 +860,14 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
                 tmem_ld32(tmem_addr(tV, lq * 32, 32 * hf), dv);
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
-                    unpack8(*reinterpret_cast<const uint4 *>(P + PK_U + img_chunk_off(128, j, 4 * hf + hh)), u);
+                    unpack8(ua[hh], u);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) vo[e] = u[e] - dv[8 * hh + e];
                     *reinterpret_cast<uint4 *>(sm + CS_VIMG + img_chunk_off(128, j, 4 * hf + hh)) = pack8(vo);
                 }
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) ua[hh] = ub[hh];
+                if (kk + 2 < nc) load_u(kk + 2, ub);
             }
             fence_proxy_async();
             fence_before_sync();
@@ -838,13 +875,13 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
             if (tid == 0) mbar_arrive(bar_vimg);
             const bool last = (kk == nc - 1);
             bool okl = true;
-            if (!last) okl = mbar_wait(&bar_ld[(kk + 1) & 1], ((kk + 1) >> 1) & 1);
+            if (!last) okl = mbar_wait(&bar_ld[(kk + 1) % CS_NST], ((kk + 1) / CS_NST) & 1);
             ok = mbar_wait(bar_s, kk & 1) && okl;
             ok = (__syncthreads_count_named1(ok) == 256);
             if (!ok) break;
             fence_after_sync();
             // S_{kk+1}: bf16 image and TMEM copy scaled by gamma_{kk+1}; or the final state
-            const float *gam = (const float *)(sm + (((kk + 1) & 1) ? CS_STAGE1 : CS_STAGE0) + PK_G);
+            const float *gam = (const float *)(stage(kk + 1) + CS_G);
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 float x[32];
@@ -883,16 +920,18 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
 // [S~ | M] from [0 | I]: S~ with the segment's values, M with values zero.  Then for any
 // entering state, S_out = M S_in + S~.  Both are kept transposed in TMEM exactly like the
 // state of the output pass; Q^ and A are not needed, so a compact packet stage is loaded.
-constexpr uint32_t SS_STAGE_BYTES = 50176;
-constexpr uint32_t SS_W = 0, SS_K = 16384, SS_U = 32768, SS_G = 49152;
-constexpr uint32_t SS_SIMG = 2 * SS_STAGE_BYTES;       // S~^T image 128 x 128
+// Three stages of W^T, K~ and gamma; U^T goes from global memory to registers two chunks ahead.
+constexpr uint32_t SS_NST = 3;
+constexpr uint32_t SS_STAGE_BYTES = 33792;
+constexpr uint32_t SS_W = 0, SS_K = 16384, SS_G = 32768;
+constexpr uint32_t SS_SIMG = SS_NST * SS_STAGE_BYTES;  // S~^T image 128 x 128
 constexpr uint32_t SS_MIMG = SS_SIMG + 32768;          // M^T image
 constexpr uint32_t SS_VSIMG = SS_MIMG + 32768;         // V~_S^T image 128 x 64
 constexpr uint32_t SS_VMIMG = SS_VSIMG + 16384;        // V~_M^T image
 constexpr uint32_t SS_BAR = SS_VMIMG + 16384;
 constexpr uint32_t SS_TSLOT = SS_BAR + 64;
 constexpr uint32_t SS_TOTAL = SS_BAR + 128 + 1024;
-constexpr uint32_t SS_TX = 16384 + 16384 + 16896;
+constexpr uint32_t SS_TX = 16384 + 16384 + 512;
 
 __global__ void __launch_bounds__(256, 1)
 chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int32_t *__restrict__ seg_start,
@@ -919,12 +958,13 @@ chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lq = warp & 3, hf = warp >> 2;
     const int j = lq * 32 + lane;
-    uint64_t *bar_ld = (uint64_t *)(sm + SS_BAR);
-    uint64_t *bar_v = bar_ld + 2, *bar_s = bar_ld + 3;
+    uint64_t *bar_ld = (uint64_t *)(sm + SS_BAR);  // [3]
+    uint64_t *bar_v = bar_ld + 3, *bar_s = bar_ld + 4;
     uint32_t *tslot = (uint32_t *)(sm + SS_TSLOT);
     if (tid == 0) {
         mbar_init(&bar_ld[0], 1);
         mbar_init(&bar_ld[1], 1);
+        mbar_init(&bar_ld[2], 1);
         mbar_init(bar_v, 1);
         mbar_init(bar_s, 1);
     }
@@ -939,11 +979,10 @@ chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int
         mbar_arrive_expect_tx(&bar_ld[st], SS_TX);
         bulk_g2s(dst + SS_W, pk + PK_W, 16384, &bar_ld[st]);
         bulk_g2s(dst + SS_K, pk + PK_K, 16384, &bar_ld[st]);
-        bulk_g2s(dst + SS_U, pk + PK_U, 16896, &bar_ld[st]);
+        bulk_g2s(dst + SS_G, pk + PK_G, 512, &bar_ld[st]);
     };
     if (tid == 0) {
-        issue(0, 0);
-        if (nc > 1) issue(1, 1);
+        for (int kk = 0; kk < (int)SS_NST && kk < nc; ++kk) issue(kk, kk);
     }
     bool ok = wait_all(&bar_ld[0], 0);
     fence_after_sync();
@@ -969,12 +1008,22 @@ chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int
     }
     fence_proxy_async();
     sync_all();
-    const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128);
+    // W^T and K~ are MN-major B operands (K rows of 128 bytes)
+    const uint32_t id64 = idesc_bf16(128, 64, false, true), id128 = idesc_bf16(128, 128, false, true);
+    auto load_u = [&](int kk, uint4 *u4) {  // U^T row j, columns [32 hf, 32 hf + 32)
+        const unsigned char *src = packets + ((size_t)(c_begin + kk) * H + h) * PK_STRIDE + PK_U;
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+            u4[hh] = __ldg(reinterpret_cast<const uint4 *>(src + img_chunk_off(128, j, 4 * hf + hh)));
+    };
+    uint4 ua[4], ub[4];
+    if (nc > 0) load_u(0, ua);
+    if (nc > 1) load_u(1, ub);
     for (int kk = 0; kk < nc && ok; ++kk) {
-        unsigned char *P = sm + (kk & 1) * SS_STAGE_BYTES;
+        unsigned char *P = sm + (kk % SS_NST) * SS_STAGE_BYTES;
         if (tid == 0) {
-            mma_bf16_k(tVS, smem_u32(sm + SS_SIMG), 128, smem_u32(P + SS_W), 64, 8, id64, false);
-            mma_bf16_k(tVM, smem_u32(sm + SS_MIMG), 128, smem_u32(P + SS_W), 64, 8, id64, false);
+            mma_bf16_kmn(tVS, smem_u32(sm + SS_SIMG), 128, smem_u32(P + SS_W), 8192, 8, id64, false);
+            mma_bf16_kmn(tVM, smem_u32(sm + SS_MIMG), 128, smem_u32(P + SS_W), 8192, 8, id64, false);
             mma_commit(bar_v);
         }
         ok = wait_all(bar_v, kk & 1);
@@ -986,7 +1035,7 @@ chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int
             tmem_ld32(tmem_addr(tVM, lq * 32, 32 * hf), dvm);
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh) {
-                unpack8(*reinterpret_cast<const uint4 *>(P + SS_U + img_chunk_off(128, j, 4 * hf + hh)), u);
+                unpack8(ua[hh], u);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     o1[e] = u[e] - dvs[8 * hh + e];
@@ -995,22 +1044,25 @@ chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int
                 *reinterpret_cast<uint4 *>(sm + SS_VSIMG + img_chunk_off(128, j, 4 * hf + hh)) = pack8(o1);
                 *reinterpret_cast<uint4 *>(sm + SS_VMIMG + img_chunk_off(128, j, 4 * hf + hh)) = pack8(o2);
             }
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) ua[hh] = ub[hh];
+            if (kk + 2 < nc) load_u(kk + 2, ub);
         }
         fence_proxy_async();
         sync_all();
         if (tid == 0) {
-            mma_bf16_k(tSt, smem_u32(sm + SS_VSIMG), 128, smem_u32(P + SS_K), 128, 4, id128, true);
-            mma_bf16_k(tMt, smem_u32(sm + SS_VMIMG), 128, smem_u32(P + SS_K), 128, 4, id128, true);
+            mma_bf16_kmn(tSt, smem_u32(sm + SS_VSIMG), 128, smem_u32(P + SS_K), 8192, 4, id128, true);
+            mma_bf16_kmn(tMt, smem_u32(sm + SS_VMIMG), 128, smem_u32(P + SS_K), 8192, 4, id128, true);
             mma_commit(bar_s);
         }
         const bool last = (kk == nc - 1);
         bool okl = true;
-        if (!last) okl = mbar_wait(&bar_ld[(kk + 1) & 1], ((kk + 1) >> 1) & 1);
+        if (!last) okl = mbar_wait(&bar_ld[(kk + 1) % SS_NST], ((kk + 1) / SS_NST) & 1);
         ok = mbar_wait(bar_s, kk & 1) && okl;
         ok = __syncthreads_and(ok ? 1 : 0) != 0;
         if (!ok) break;
         fence_after_sync();
-        const float *gam = (const float *)(sm + ((kk + 1) & 1) * SS_STAGE_BYTES + SS_G);
+        const float *gam = (const float *)(sm + ((kk + 1) % SS_NST) * SS_STAGE_BYTES + SS_G);
         float *out = seg_sum + ((size_t)g * H + h) * 2 * D * D;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
@@ -1033,16 +1085,27 @@ chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int
                     for (int e = 0; e < 32; e += 4)
                         *reinterpret_cast<float4 *>(out + (size_t)j * D + c0 + e) =
                             make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-                } else {  // M row-major: M[c][j] = M^T[j][c]
+                } else {  // M^T row j as bf16 high / low parts, 128-byte-swizzled rows (the fold's operand)
+                    unsigned char *mimg = reinterpret_cast<unsigned char *>(out + D * D);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) out[D * D + (size_t)(c0 + e) * D + j] = x[e];
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        float hi[8], lo[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            hi[e] = __bfloat162float(__float2bfloat16_rn(x[8 * q8 + e]));
+                            lo[e] = x[8 * q8 + e] - hi[e];
+                        }
+                        const uint32_t off = img_chunk_off(128, j, c0 / 8 + q8);
+                        *reinterpret_cast<uint4 *>(mimg + off) = pack8(hi);
+                        *reinterpret_cast<uint4 *>(mimg + 32768 + off) = pack8(lo);
+                    }
                 }
             }
         }
         if (!last) tmem_st_wait();
         fence_proxy_async();
         sync_all();
-        if (tid == 0 && kk + 2 < nc) issue(kk + 2, kk & 1);
+        if (tid == 0 && kk + (int)SS_NST < nc) issue(kk + SS_NST, kk % SS_NST);
     }
     if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     sync_all();
@@ -1052,13 +1115,18 @@ chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int
 // =====================================================================================
 // Fold of the segment summaries of each (sequence, head) in order (section 5.1.2: the
 // rank-level updates compose associatively): S_in(i+1) = M_i S_in(i) + S~_i, starting from
-// the sequence's initial state.  Transposed: S^T <- S~^T + S^T M^T, an MMA with A = S^T and
-// B = M (rows c, K = m).  Both operands are split into bf16 high and low parts and three
-// products are accumulated (hi*hi + hi*lo + lo*hi), which keeps the fold near fp32 accuracy.
-constexpr uint32_t FD_AHI = 0, FD_ALO = 32768, FD_BHI = 65536, FD_BLO = 98304;
-constexpr uint32_t FD_BAR = 131072;
-constexpr uint32_t FD_TSLOT = FD_BAR + 16;
+// the sequence's initial state.  Transposed: S^T <- S~^T + S^T M^T, an MMA with A = S^T (K-major
+// image) and B = M^T (read MN-major from the rows the summary pass wrote).  Both factors are
+// split into bf16 high and low parts and hi*hi + hi*lo + lo*hi is accumulated (near-fp32
+// accuracy): one N = 256 product A_hi [M^T_hi | M^T_lo] and one N = 128 product A_lo M^T_hi.
+// The M^T images of step i + 2 are bulk-copied while step i runs; S~^T of step i + 1 is read into
+// registers during step i and placed in tensor memory, where the readout adds it.
+constexpr uint32_t FD_STG = 0;                 // 2 stages x [M^T hi | M^T lo] (64 KB each)
+constexpr uint32_t FD_AHI = 131072, FD_ALO = FD_AHI + 32768;  // S^T hi / lo images (32 KB each)
+constexpr uint32_t FD_BAR = FD_ALO + 32768;    // ld[2], mma
+constexpr uint32_t FD_TSLOT = FD_BAR + 32;
 constexpr uint32_t FD_TOTAL = FD_BAR + 64 + 1024;
+constexpr uint32_t TF_D = 0, TF_ST = 256;      // TMEM: products (256 columns), S~^T (128 columns)
 
 __global__ void __launch_bounds__(256, 1)
 chunk_fold_tc_kernel(int N, const int32_t *__restrict__ seg_start, int H, const float *initial_state,
@@ -1068,16 +1136,31 @@ chunk_fold_tc_kernel(int N, const int32_t *__restrict__ seg_start, int H, const 
     const int n = blockIdx.x, h = blockIdx.y;
     const int g0 = seg_start[n], nseg = seg_start[n + 1] - g0;
     if (nseg <= 1) return;
+    const int steps = nseg - 1;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lq = warp & 3, hf = warp >> 2;
-    const int j = lq * 32 + lane;
-    uint64_t *bar = (uint64_t *)(sm + FD_BAR);
+    const int j = lq * 32 + lane;  // S^T row (value channel) = TMEM lane
+    uint64_t *bar_ld = (uint64_t *)(sm + FD_BAR);
+    uint64_t *bar_mma = bar_ld + 2;
     uint32_t *tslot = (uint32_t *)(sm + FD_TSLOT);
-    if (tid == 0) mbar_init(bar, 1);
-    if (warp == 0) tmem_alloc(tslot, 128);
+    auto summary = [&](int i) { return seg_sum + ((size_t)(g0 + i) * H + h) * 2 * D * D; };
+    auto issue = [&](int i) {  // M^T hi / lo images of step i into stage i & 1
+        mbar_arrive_expect_tx(&bar_ld[i & 1], 65536);
+        bulk_g2s(sm + FD_STG + (i & 1) * 65536, summary(i) + D * D, 65536, &bar_ld[i & 1]);
+    };
+    if (tid == 0) {
+        mbar_init(&bar_ld[0], 1);
+        mbar_init(&bar_ld[1], 1);
+        mbar_init(bar_mma, 1);
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
     fence_proxy_async();
     sync_all();
-    const uint32_t tD = *tslot;
+    const uint32_t tb = *tslot;
+    if (tid == 0) {
+        issue(0);
+        if (steps > 1) issue(1);
+    }
     const size_t st_off = ((size_t)n * H + h) * D * D;
     float sreg[64];  // S^T row j, columns [64 hf, 64 hf + 64)
 #pragma unroll
@@ -1089,71 +1172,73 @@ chunk_fold_tc_kernel(int N, const int32_t *__restrict__ seg_start, int H, const 
             *reinterpret_cast<float4 *>(dst0 + (size_t)j * D + 64 * hf + e) =
                 make_float4(sreg[e], sreg[e + 1], sreg[e + 2], sreg[e + 3]);
     }
+    float nxt[64];  // S~^T row j of the current step
+#pragma unroll
+    for (int e = 0; e < 64; e += 4) {
+        const float4 v4 = *reinterpret_cast<const float4 *>(summary(0) + (size_t)j * D + 64 * hf + e);
+        nxt[e] = v4.x; nxt[e + 1] = v4.y; nxt[e + 2] = v4.z; nxt[e + 3] = v4.w;
+    }
     bool ok = true;
-    const uint32_t id128 = idesc_bf16(128, 128);
-    for (int i = 0; i < nseg - 1 && ok; ++i) {
-        const float *sum = seg_sum + ((size_t)(g0 + i) * H + h) * 2 * D * D;
-        // D <- S~^T (row j); A images from S^T; B images from M (row c = j)
+    const uint32_t id256 = idesc_bf16(128, 256, false, true), id128 = idesc_bf16(128, 128, false, true);
+    for (int i = 0; i < steps && ok; ++i) {
+        // S~^T into TMEM; S_in^T hi / lo images
 #pragma unroll
-        for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 16) {
-            float t16[16], hi[16], lo[16];
+        for (int c0 = 0; c0 < 64; c0 += 16) tmem_st16(tmem_addr(tb + TF_ST, lq * 32, 64 * hf + c0), nxt + c0);
 #pragma unroll
-            for (int e = 0; e < 16; e += 4) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(sum + (size_t)j * D + c0 + e);
-                t16[e] = v4.x; t16[e + 1] = v4.y; t16[e + 2] = v4.z; t16[e + 3] = v4.w;
+        for (int c0 = 0; c0 < 64; c0 += 8) {
+            float hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                hi[e] = __bfloat162float(__float2bfloat16_rn(sreg[c0 + e]));
+                lo[e] = sreg[c0 + e] - hi[e];
             }
-            tmem_st16(tmem_addr(tD, lq * 32, c0), t16);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                hi[e] = __bfloat162float(__float2bfloat16_rn(sreg[c0 - 64 * hf + e]));
-                lo[e] = sreg[c0 - 64 * hf + e] - hi[e];
-            }
-            *reinterpret_cast<uint4 *>(sm + FD_AHI + img_chunk_off(128, j, c0 / 8)) = pack8(hi);
-            *reinterpret_cast<uint4 *>(sm + FD_AHI + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(hi + 8);
-            *reinterpret_cast<uint4 *>(sm + FD_ALO + img_chunk_off(128, j, c0 / 8)) = pack8(lo);
-            *reinterpret_cast<uint4 *>(sm + FD_ALO + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(lo + 8);
-            float m16[16];
-#pragma unroll
-            for (int e = 0; e < 16; e += 4) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(sum + D * D + (size_t)j * D + c0 + e);
-                m16[e] = v4.x; m16[e + 1] = v4.y; m16[e + 2] = v4.z; m16[e + 3] = v4.w;
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                hi[e] = __bfloat162float(__float2bfloat16_rn(m16[e]));
-                lo[e] = m16[e] - hi[e];
-            }
-            *reinterpret_cast<uint4 *>(sm + FD_BHI + img_chunk_off(128, j, c0 / 8)) = pack8(hi);
-            *reinterpret_cast<uint4 *>(sm + FD_BHI + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(hi + 8);
-            *reinterpret_cast<uint4 *>(sm + FD_BLO + img_chunk_off(128, j, c0 / 8)) = pack8(lo);
-            *reinterpret_cast<uint4 *>(sm + FD_BLO + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(lo + 8);
+            const uint32_t off = img_chunk_off(128, j, (64 * hf + c0) / 8);
+            *reinterpret_cast<uint4 *>(sm + FD_AHI + off) = pack8(hi);
+            *reinterpret_cast<uint4 *>(sm + FD_ALO + off) = pack8(lo);
         }
         tmem_st_wait();
         fence_proxy_async();
-        sync_all();
-        if (tid == 0) {
-            mma_bf16_k(tD, smem_u32(sm + FD_AHI), 128, smem_u32(sm + FD_BHI), 128, 8, id128, true);
-            mma_bf16_k(tD, smem_u32(sm + FD_AHI), 128, smem_u32(sm + FD_BLO), 128, 8, id128, true);
-            mma_bf16_k(tD, smem_u32(sm + FD_ALO), 128, smem_u32(sm + FD_BHI), 128, 8, id128, true);
-            mma_commit(bar);
-        }
-        ok = wait_all(bar, i & 1);
+        ok = wait_all(&bar_ld[i & 1], (i >> 1) & 1);
         if (!ok) break;
         fence_after_sync();
+        if (tid == 0) {
+            const uint32_t B = smem_u32(sm + FD_STG + (i & 1) * 65536);
+            mma_bf16_kmn(tb + TF_D, smem_u32(sm + FD_AHI), 128, B, 16384, 8, id256, false);
+            mma_bf16_kmn(tb + TF_D, smem_u32(sm + FD_ALO), 128, B, 16384, 8, id128, true);
+            mma_commit(bar_mma);
+        }
+        if (i + 1 < steps) {
+#pragma unroll
+            for (int e = 0; e < 64; e += 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(summary(i + 1) + (size_t)j * D + 64 * hf + e);
+                nxt[e] = v4.x; nxt[e + 1] = v4.y; nxt[e + 2] = v4.z; nxt[e + 3] = v4.w;
+            }
+        }
+        ok = wait_all(bar_mma, i & 1);
+        if (!ok) break;
+        fence_after_sync();
+        if (tid == 0 && i + 2 < steps) issue(i + 2);  // stage i & 1 has been read
         float *dst = seg_in + ((size_t)(g0 + i + 1) * H + h) * D * D;
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-            tmem_ld32(tmem_addr(tD, lq * 32, 64 * hf + c0), sreg + c0);
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+            float a[16], b[16], c[16];
+            tmem_ld16(tmem_addr(tb + TF_D, lq * 32, 64 * hf + c0), a);
+            tmem_ld16(tmem_addr(tb + TF_D, lq * 32, 128 + 64 * hf + c0), b);
+            tmem_ld16(tmem_addr(tb + TF_ST, lq * 32, 64 * hf + c0), c);
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
+            for (int e = 0; e < 16; ++e) sreg[c0 + e] = a[e] + b[e] + c[e];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
                 *reinterpret_cast<float4 *>(dst + (size_t)j * D + 64 * hf + c0 + e) =
                     make_float4(sreg[c0 + e], sreg[c0 + e + 1], sreg[c0 + e + 2], sreg[c0 + e + 3]);
         }
-        sync_all();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
     }
     if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     sync_all();
-    if (warp == 0) tmem_dealloc(tD, 128);
+    if (warp == 0) tmem_dealloc(tb, 512);
 }
 
 }  // namespace tcp
@@ -1185,16 +1270,18 @@ static encode_tiled_fn get_encode_tiled() {
     return fn;
 }
 
-// [T, H, 128] bf16 as a 3-D map (channel, head, token) with 128 x 1 x 64 boxes, no swizzle.
+// [T, H, 128] bf16 as a 3-D map (channel, head, token) with 64 x 1 x 64 boxes (128 bytes per
+// token row) and 128-byte swizzle: a box lands as the [64 tokens][64 channels] half of an operand
+// tile.  Tokens past T read as zeros.
 static bool make_tile_map(CUtensorMap *m, const void *base, int64_t T, int H) {
     encode_tiled_fn enc = get_encode_tiled();
     if (!enc) return false;
     const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
     const cuuint64_t strides[2] = {256, (cuuint64_t)H * 256};
-    const cuuint32_t box[3] = {128, 1, 64};
+    const cuuint32_t box[3] = {64, 1, 64};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1210,7 +1297,7 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     unsigned char *packets = (unsigned char *)ws + p.off_records;
     if (p.max_chunks > 0 && a->T > 0) {
         cudaFuncSetAttribute(tcp::chunk_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tcp::I2_TOTAL);
+                             (int)tcp::J_TOTAL);
         int dev = 0, sms = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1220,7 +1307,7 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
         if (!make_tile_map(&tm.q, a->q, a->T, p.H) || !make_tile_map(&tm.k, a->k, a->T, p.H) ||
             !make_tile_map(&tm.v, a->v, a->T, p.H) || !make_tile_map(&tm.z, a->z, a->T, p.H))
             return KDA_ERR_CUDA;
-        tcp::chunk_intra_tc_kernel<<<grid, tcp::NT2, tcp::I2_TOTAL, stream>>>(
+        tcp::chunk_intra_tc_kernel<<<grid, tcp::NT2, tcp::J_TOTAL, stream>>>(
             tm, (const bf16 *)a->beta, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
             chunk_start, p.H, packets, err);
         if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;

@@ -28,7 +28,8 @@ struct kda_chunk_plan {
     int64_t seg_len;         // chunks per segment
     int64_t max_segs;        // upper bound on segments over all sequences
     size_t off_seg_start;    // int32 [N + 1]: first segment of each sequence
-    size_t off_seg_sum;      // per (segment, head): S~^T [128][128] and M [128][128], fp32
+    size_t off_seg_sum;      // per (segment, head), 128 KB: S~^T [128][128] fp32, then M^T as bf16 high and
+                             // low operand images (32 KB each)
     size_t off_seg_in;       // per (segment, head): entering state S^T [128][128], fp32
     size_t total_bytes;
 };

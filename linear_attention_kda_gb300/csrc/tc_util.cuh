@@ -45,9 +45,24 @@ __device__ __forceinline__ uint64_t desc_kstep(uint32_t base, int R, int s) {
     return desc_sw128(base + (uint32_t)((s >> 2) * (R * 128) + (s & 3) * 32));
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, dense.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Descriptor of an MN-major ("transposed") SW128 operand kept token-major: rows of 128 bytes hold
+// 64 consecutive elements along M (or N), consecutive rows are consecutive K, 8-row atoms are
+// 1024 bytes apart (SBO) and further 64-element groups along M (or N) lbo bytes apart (LBO).  A
+// [rows][128] tile stored as two [rows][64] halves is read this way with lbo = rows * 128.
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, dense; A / B K-major unless a_mn / b_mn.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn = false, bool b_mn = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // D[tmem] (+)= A(smem desc) * B(smem desc)^T, issued by one thread.
@@ -67,6 +82,28 @@ __device__ __forceinline__ void mma_bf16_k(uint32_t d_tmem, uint32_t a_base, int
 #pragma unroll
     for (int s = 0; s < ksteps; ++s)
         mma_bf16(d_tmem, da + (uint64_t)((((s >> 2) * RA * 128) + (s & 3) * 32) >> 4),
+                 db + (uint64_t)((((s >> 2) * RB * 128) + (s & 3) * 32) >> 4), idesc,
+                 (accumulate || s > 0) ? 1u : 0u);
+}
+
+// Full product over K = 16 * ksteps with A K-major (image with RA rows) and B MN-major (K-step s
+// starts 16 rows = 2048 bytes further; N-groups b_lbo bytes apart).
+__device__ __forceinline__ void mma_bf16_kmn(uint32_t d_tmem, uint32_t a_base, int RA, uint32_t b_base,
+                                             uint32_t b_lbo, int ksteps, uint32_t idesc, bool accumulate) {
+    const uint64_t da = desc_sw128(a_base), db = desc_sw128_mn(b_base, b_lbo);
+#pragma unroll
+    for (int s = 0; s < ksteps; ++s)
+        mma_bf16(d_tmem, da + (uint64_t)((((s >> 2) * RA * 128) + (s & 3) * 32) >> 4),
+                 db + (uint64_t)((2048 * s) >> 4), idesc, (accumulate || s > 0) ? 1u : 0u);
+}
+// Full product over K = 16 * ksteps with A MN-major (groups along M a_lbo bytes apart) and B K-major
+// (image with RB rows).
+__device__ __forceinline__ void mma_bf16_mnk(uint32_t d_tmem, uint32_t a_base, uint32_t a_lbo, uint32_t b_base,
+                                             int RB, int ksteps, uint32_t idesc, bool accumulate) {
+    const uint64_t da = desc_sw128_mn(a_base, a_lbo), db = desc_sw128(b_base);
+#pragma unroll
+    for (int s = 0; s < ksteps; ++s)
+        mma_bf16(d_tmem, da + (uint64_t)((2048 * s) >> 4),
                  db + (uint64_t)((((s >> 2) * RB * 128) + (s & 3) * 32) >> 4), idesc,
                  (accumulate || s > 0) ? 1u : 0u);
 }
@@ -117,6 +154,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 8 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
     asm volatile(
