@@ -193,6 +193,11 @@ const char *kda_status_string(kda_status_t status);
  * (KDA_OK if none).  The word is per device and shared by all streams. */
 kda_status_t kda_get_device_error(struct CUstream_st *stream);
 
+/* The CUDA runtime error code (a cudaError_t value) behind the last
+ * KDA_ERR_CUDA returned to the calling host thread, 0 if none; reading it
+ * clears it. */
+int32_t kda_last_cuda_error(void);
+
 int kda_abi_version(void);
 
 /* ------------------------------------------------------------ instrumentation

@@ -55,6 +55,14 @@ int *kda_device_error_ptr() {
     return g_err_ptr[dev];
 }
 
+static thread_local int g_last_cuda_error = 0;
+
+kda_status_t kda_cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return KDA_OK;
+    g_last_cuda_error = (int)e;
+    return KDA_ERR_CUDA;
+}
+
 extern "C" {
 
 int kda_abi_version(void) { return KDA_ABI_VERSION; }
@@ -92,6 +100,12 @@ const char *kda_status_string(kda_status_t s) {
         case KDA_ERR_DEVICE_TIMEOUT: return "bounded wait inside a kernel gave up";
     }
     return "unknown status";
+}
+
+int32_t kda_last_cuda_error(void) {
+    const int v = g_last_cuda_error;
+    g_last_cuda_error = 0;
+    return v;
 }
 
 kda_status_t kda_get_device_error(struct CUstream_st *stream) {

@@ -202,5 +202,5 @@ kda_status_t kda_launch_chunk_plan(const kda_chunk_args *a, const kda_chunk_plan
     int32_t *seg_start = p.path == 1 ? (int32_t *)((char *)ws + p.off_seg_start) : nullptr;
     kda::chunk_plan_kernel<<<1, 1024, 0, stream>>>(a->cu_seqlens, a->T, (int)a->N, p.C, chunk_start,
                                                     p.seg_len, seg_start, err);
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return kda_cuda_status(cudaGetLastError());
 }

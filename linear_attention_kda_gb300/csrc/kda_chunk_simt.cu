@@ -275,7 +275,10 @@ kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan
                 (const float *)a->beta, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
                 chunk_start, H, dk, dv, C, records, p.record_bytes);
         }
-        if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+        {
+            const kda_status_t cst = kda_cuda_status(cudaGetLastError());
+            if (cst != KDA_OK) return cst;
+        }
     }
     kda_profile_mark(2, stream);
     dim3 grid2((unsigned)(a->N * H), (unsigned)(dv / SLICE));
@@ -291,5 +294,5 @@ kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan
             a->scale, a->initial_state, a->final_state, (float *)a->o);
     }
     kda_profile_mark(3, stream);
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return kda_cuda_status(cudaGetLastError());
 }

@@ -35,27 +35,31 @@ constexpr int C = 64;   // chunk
 constexpr int D = 128;  // d_k = d_v
 
 // packet layout (bytes)
-constexpr uint32_t PK_W = 0;          // W^T bf16 [128 channels][64 tokens], read as an MN-major B operand
-constexpr uint32_t PK_Q = 16384;      // Q^ image, 64 x 128
-constexpr uint32_t PK_K = 32768;      // K~ bf16 [64 tokens][128 channels] (two 64-channel halves), MN-major B
-constexpr uint32_t PK_A = 49152;      // A image, 64 x 64
-constexpr uint32_t PK_U = 57344;      // U^T bf16 [128][64], 16-byte chunk j of row r at chunk j ^ (r % 8)
+// Every operand is token-major ([token][channel] rows of 128 bytes, 128-byte swizzle).
+constexpr uint32_t PK_WQ = 0;         // [W; Q^]: one K-major 128-row image (rows 0-63 W, rows 64-127 Q^),
+                                      // 16 KB per 64-channel block
+constexpr uint32_t PK_K = 32768;      // K~ [64 tokens][128 channels] (two 64-channel halves)
+constexpr uint32_t PK_A = 49152;      // A [64 query rows][64 keys]; with the K~ half before it, a 128-row
+                                      // operand whose rows 64-127 are A
+constexpr uint32_t PK_U = 57344;      // U [64 tokens][128 channels] (two halves)
 constexpr uint32_t PK_G = 73728;      // gamma^C fp32 [128]
 constexpr uint32_t PK_STRIDE = 75776; // multiple of 1024
 
 // inter kernel shared memory
-// Three packet stages hold the MMA operands of a chunk (W^T, Q^, K~, A) and gamma; U^T is read by the
-// CUDA cores straight from global memory into registers, two chunks ahead.
-constexpr uint32_t CS_NST = 3;
-constexpr uint32_t CS_PK_MMA = PK_A + 8192;            // bytes [0, PK_A + 8 KB) of a packet: W, Q^, K~, A
+// Output pass: two packet stages hold the MMA operands of a chunk ([W; Q^], K~, A) and gamma (the
+// packet after them is prefetched into L2); U is read by the CUDA cores from global memory into
+// registers, one chunk ahead.
+constexpr uint32_t CS_NST = 2;
+constexpr uint32_t CS_PK_MMA = PK_A + 8192;            // bytes [0, PK_A + 8 KB) of a packet
 constexpr uint32_t CS_G = CS_PK_MMA;                   // gamma inside a stage
 constexpr uint32_t CS_ST_TX = CS_PK_MMA + 512;
 constexpr uint32_t CS_ST_BYTES = 58368;                // stage stride (multiple of 1024)
-constexpr uint32_t CS_SIMG = CS_NST * CS_ST_BYTES;     // S^T image 128 x 128 (32 KB)
-constexpr uint32_t CS_VIMG = CS_SIMG + 32768;          // V~^T image 128 x 64 (16 KB)
-constexpr uint32_t CS_BAR = CS_VIMG + 16384;           // 11 mbarriers
-constexpr uint32_t CS_TSLOT = CS_BAR + 96;             // TMEM base, failure flag
-constexpr uint32_t CS_TOTAL = CS_BAR + 128 + 1024;
+constexpr uint32_t CS_SIMG = CS_NST * CS_ST_BYTES;     // S image, 128 rows (d_k) x 128 (d_v), 2 x 16 KB
+constexpr uint32_t CS_VIMG = CS_SIMG + 32768;          // V~ image, 64 tokens x 128 (d_v), 2 x 8 KB
+constexpr uint32_t CS_OIMG = CS_VIMG + 16384;          // o staging, 64 tokens x 128, 2 x 8 KB
+constexpr uint32_t CS_BAR = CS_OIMG + 16384;           // 14 mbarriers
+constexpr uint32_t CS_TSLOT = CS_BAR + 128;            // TMEM base, failure flag
+constexpr uint32_t CS_TOTAL = CS_BAR + 192 + 1024;
 static_assert(CS_ST_TX <= CS_ST_BYTES, "stage");
 
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
@@ -63,8 +67,21 @@ __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
     return p + ((1024u - (s & 1023u)) & 1023u);
 }
 
+// Float offset of element (i, c) of a 128 x 128 fp32 matrix kept in the workspace in "lane-major"
+// order: float4 (c / 4) of row i at ((c / 4) * 128 + i) * 4, so that the 32 rows of a warp (one row per
+// thread) read or write 512 contiguous bytes per float4 column.
+__device__ __forceinline__ size_t ll_off(int i, int c) { return ((size_t)(c >> 2) * 128 + i) * 4 + (c & 3); }
+
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+// bar.red.popc over the n threads of named barrier id: the number of them with pred set.
+__device__ __forceinline__ int bar_red_popc(int id, int n, bool pred) {
+    int r;
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.popc.u32 %0, %2, %3, p;\n\t}\n"
+                 : "=r"(r) : "r"((unsigned)pred), "r"(id), "r"(n) : "memory");
+    return r;
 }
 
 // bar.red.popc over the 256 threads of named barrier 1.
@@ -140,8 +157,8 @@ __device__ __forceinline__ bool locate(const int32_t *chunk_start, const int32_t
 //        reference), K = 128 channels.
 //   INV  T = (I + L)^{-1} in fp32: 16 x 16 diagonal blocks by substitution, then one 16-row and
 //        one 32-row block merge, T21 = -T22 L21 T11.
-//   MMA  W^T = X^T (T diag beta)^T and U^T = V^T (T diag beta)^T, X and V read MN-major.
-//   OUT  packet by bulk copies: W^T, Q^, K~, A, U^T, gamma.
+//   MMA  [W | U] = (T diag beta) [X | V], X and V read MN-major (one N = 256 product).
+//   OUT  packet by bulk copies: [W; Q^], K~, A, U, gamma.
 //
 // Warps 0-15 split every phase (16 consumer warps keep the latency-bound phases fed).
 //
@@ -177,8 +194,8 @@ constexpr uint32_t J_INFO = J_BIAS + 1024;  // 2 stages x {int64 t0, len, h, slo
 constexpr uint32_t J_BAR = J_INFO + 128;    // ld[2], free[2], mma
 constexpr uint32_t J_TSLOT = J_BAR + 48;
 constexpr uint32_t J_TOTAL = J_BAR + 64 + 1024;
-// TMEM columns: A / L product (96), W^T (64), U^T (64)
-constexpr uint32_t TM_DA = 0, TM_DB = 32, TM_DW = 96, TM_DU = 160;
+// TMEM columns: A / L product (96); later [W | U] (256, lanes 0-63)
+constexpr uint32_t TM_DA = 0, TM_DB = 32, TM_DWU = 0;
 
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -458,7 +475,8 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
                 mma_bf16_k(tb + TM_DA, smem_u32(sm + J_ROW), 128, smem_u32(sm + J_KEY), 96, 8, idesc_bf16(128, 96),
                            false);
                 mma_commit(bar_mma);
-                bulk_s2g(pk + PK_Q, stg + J_TQ, 16384);
+                bulk_s2g(pk + PK_WQ + 8192, stg + J_TQ, 8192);           // Q^ rows of the [W; Q^] image
+                bulk_s2g(pk + PK_WQ + 24576, stg + J_TQ + 8192, 8192);
                 bulk_s2g(pk + PK_K, stg + J_TZ, 16384);
                 bulk_commit();
             }
@@ -616,33 +634,36 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
             fence_proxy_async();
             csync();
             if (tid == 0) {
-                const uint32_t id = idesc_bf16(128, 64, true, false);
-                mma_bf16_mnk(tb + TM_DW, smem_u32(stg + J_TK), 8192, smem_u32(sm + J_TIMG), 64, 4, id, false);
-                mma_bf16_mnk(tb + TM_DU, smem_u32(stg + J_TV), 8192, smem_u32(sm + J_TIMG), 64, 4, id, false);
+                // [W | U] = (T diag beta) [X | V]: A = the T image read as 128 rows (rows 64-127 are the A
+                // image behind it and land in unused TMEM lanes), B = X and V as one MN-major operand of
+                // 256 columns (the k and v tiles are adjacent)
+                mma_bf16_kmn(tb + TM_DWU, smem_u32(sm + J_TIMG), 128, smem_u32(stg + J_TK), 8192, 4,
+                             idesc_bf16(128, 256, false, true), false);
                 mma_commit(bar_mma);
             }
             ok = cwait(bar_mma, mph & 1);
             ++mph;
             if (!ok) break;
             fence_after_sync();
-            // ---- W^T and U^T rows (channel-major images) into the dead X and V tiles
-            {
-                const int lq = warp & 3, cq = warp >> 2;
-                const int c = 32 * lq + lane;
-                float d[16];
-                tmem_ld16(tmem_addr(tb + TM_DW, 32 * lq, 16 * cq), d);
+            // ---- W and U rows (token-major, TMEM lanes 0-63) into the dead X and V tiles
+            if ((warp & 3) < 2) {
+                const int r = 32 * (warp & 3) + lane, cq = warp >> 2;  // columns [64 cq, 64 cq + 64)
+                unsigned char *dst = stg + (cq < 2 ? J_TK : J_TV);
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj)
-                    *reinterpret_cast<uint4 *>(stg + J_TK + img_chunk_off(128, c, 2 * cq + jj)) = pack8(d + 8 * jj);
-                tmem_ld16(tmem_addr(tb + TM_DU, 32 * lq, 16 * cq), d);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    float d[32];
+                    tmem_ld32(tmem_addr(tb + TM_DWU, 32 * (warp & 3), 64 * cq + 32 * h2), d);
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj)
-                    *reinterpret_cast<uint4 *>(stg + J_TV + img_chunk_off(128, c, 2 * cq + jj)) = pack8(d + 8 * jj);
+                    for (int jj = 0; jj < 4; ++jj)
+                        *reinterpret_cast<uint4 *>(dst + img_chunk_off(64, r, 8 * (cq & 1) + 4 * h2 + jj)) =
+                            pack8(d + 8 * jj);
+                }
             }
             fence_proxy_async();
             csync();
             if (tid == 0) {
-                bulk_s2g(pk + PK_W, stg + J_TK, 16384);
+                bulk_s2g(pk + PK_WQ, stg + J_TK, 8192);
+                bulk_s2g(pk + PK_WQ + 16384, stg + J_TK + 8192, 8192);
                 bulk_s2g(pk + PK_U, stg + J_TV, 16384);
                 bulk_s2g(pk + PK_A, sm + J_AIMG, 8192);
                 bulk_s2g(pk + PK_G, sm + J_GAM, 512);
@@ -656,23 +677,27 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
     if (warp == 0) tmem_dealloc(tb, 256);
 }
 
-constexpr int NT3 = 416;  // warps 0-7: state path; 8-11: output path; 12: MMA issue
-// Warp roles.
-//  - Warp 12 (one thread) issues every tcgen05.mma in program order: per chunk the V product
-//    (needs the S^T image), the Q^ product (output), then after V~ is ready the state update and
-//    the A product.  Issuing costs ~45 cycles per instruction, so keeping it off the SIMT warps
-//    removes it from their critical path.
-//  - Warps 0-7 carry the recurrence: V~ after the V product, then the state readout after the
-//    state MMA, writing the bf16 S^T image for the next chunk and the TMEM copy scaled by the
-//    next chunk's gamma (warps w and w + 4 share TMEM lanes and split the columns).
-//  - Warps 8-11 move the outputs: after the output MMAs of chunk k complete they read O^T (double
-//    buffered in TMEM), store it, release the buffer, and refill the packet stage.
-// In-order execution of one thread's MMAs makes each commit cover everything issued before it.
+constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 10, 11, 14, 15: output; 9, 12, 13 idle
+// The state is kept as S [d_k lanes x d_v columns] fp32 in tensor memory and as a bf16 image in shared
+// memory (rows d_k, read MN-major).  Per chunk k (one thread of warp 8 issues every MMA, in order):
+//   MMA1  D = [W; Q^] S                 rows 0-63: W S, rows 64-127: Q^ S   (M = 128, N = 128, K = 128)
+//   V~    = U - W S                     TMEM lanes 0-63, token-major image
+//   MMA3  S <- Diag(gamma) S + K~^T V~  A = K~, B = V~ (both MN-major); the decay was applied to the
+//                                       TMEM copy when S was read out, as a per-lane scalar
+//   MMA2  D rows 64-127 += A V~         A operand = [K~ half; A] read as 128 rows -> O = Q^ S + A V~
+//   S     readout: bf16 image of S_{k+1}; TMEM copy scaled by gamma_{k+1}
+// Columns of S (value channels) never mix, so the recurrence runs as two independent column halves
+// (warps 0-3: d_v 0-63, warps 4-7: d_v 64-127), each with its own barriers and N = 64 products; the
+// issuer interleaves them so that one half's CUDA-core phase overlaps the other half's MMAs.
+// The recurrence never waits for the outputs: the output warps (the four that reach TMEM lanes
+// 64-127) read O of chunk k once its MMAs are done, release the D buffer (double buffered), refill
+// the packet stage and store o through a staging tile and TMA.
 __global__ void __launch_bounds__(NT3, 1)
-chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
-                      const int32_t *__restrict__ seg_start, int64_t seg_len, const float *__restrict__ seg_in,
-                      int H, const unsigned char *__restrict__ packets, float scale,
-                      const float *initial_state, float *final_state, bf16 *__restrict__ o, int *err) {
+chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N, const int32_t *__restrict__ cu,
+                      const int32_t *__restrict__ chunk_start, const int32_t *__restrict__ seg_start,
+                      int64_t seg_len, const float *__restrict__ seg_in, int H,
+                      const unsigned char *__restrict__ packets, float scale, const float *initial_state,
+                      float *final_state, bf16 *__restrict__ o, int *err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1024(smem_raw);
     // segment g of sequence n, head h: chunks [kk0, kk0 + nc) of the sequence
@@ -690,13 +715,13 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
     const int seg_i = g - seg_start[n], nseg = seg_start[n + 1] - seg_start[n];
     const bool last_seg = (seg_i == nseg - 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int lq = warp & 3;
-    const int j = lq * 32 + lane;  // value channel = TMEM lane = S^T row
-    uint64_t *bar_ld = (uint64_t *)(sm + CS_BAR);              // [3] packet stage loaded
-    uint64_t *bar_v = bar_ld + 3, *bar_s = bar_ld + 4;         // V product / state update done
-    uint64_t *bar_o = bar_ld + 5;                              // [2] all MMAs of a chunk done
-    uint64_t *bar_free = bar_ld + 7;                           // [2] O buffer released by the output path
-    uint64_t *bar_simg = bar_ld + 9, *bar_vimg = bar_ld + 10;  // S^T / V~^T images ready
+    const int lq = warp & 3, cg = (warp >> 2) & 1;  // TMEM lane quarter, 64-column half
+    const int row = 32 * lq + lane;                  // TMEM lane: d_k row of S; token of D
+    uint64_t *bar_ld = (uint64_t *)(sm + CS_BAR);  // [2] packet stage loaded
+    uint64_t *bar_o = bar_ld + 2;                  // [2] MMA2 (all MMAs of a chunk) done
+    uint64_t *bar_free = bar_ld + 4;               // [2] D buffer read by the output warps
+    uint64_t *bar_v = bar_ld + 6, *bar_s = bar_ld + 8;         // [2 halves] MMA1 / MMA3 done
+    uint64_t *bar_simg = bar_ld + 10, *bar_vimg = bar_ld + 12;  // [2 halves] S / V~ image halves ready
     uint32_t *tslot = (uint32_t *)(sm + CS_TSLOT);
     int *s_fail = (int *)(sm + CS_TSLOT + 8);
     const int64_t kk0 = (int64_t)seg_i * seg_len;
@@ -708,203 +733,238 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
     const size_t st_off = ((size_t)n * H + h) * D * D;
     // entering state: the sequence's initial state for a lone segment; otherwise the fold's output
     // (segment 0 included), so that final_state may alias initial_state
-    const float *s_in = (nseg > 1) ? seg_in + ((size_t)g * H + h) * D * D : nullptr;  // S^T rows
+    // (lane-major, see ll_off) or, for a lone segment, the user's row-major initial state
+    const bool s_in_ll = (nseg > 1);
+    const float *s_in = s_in_ll ? seg_in + ((size_t)g * H + h) * D * D
+                                : (initial_state ? initial_state + st_off : nullptr);
 
     if (tid == 0) {
-        mbar_init(&bar_ld[0], 1);
-        mbar_init(&bar_ld[1], 1);
-        mbar_init(&bar_ld[2], 1);
-        mbar_init(bar_v, 1);
-        mbar_init(bar_s, 1);
-        mbar_init(&bar_o[0], 1);
-        mbar_init(&bar_o[1], 1);
-        mbar_init(&bar_free[0], 128);
-        mbar_init(&bar_free[1], 128);
-        mbar_init(bar_simg, 1);
-        mbar_init(bar_vimg, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_ld[i], 1);
+            mbar_init(&bar_o[i], 1);
+            mbar_init(&bar_free[i], 128);
+            mbar_init(&bar_v[i], 1);
+            mbar_init(&bar_s[i], 1);
+            mbar_init(&bar_simg[i], 1);
+            mbar_init(&bar_vimg[i], 1);
+        }
         *s_fail = 0;
     }
     if (warp == 0) tmem_alloc(tslot, 512);
     fence_proxy_async();  // barrier init visible to the async proxy
     sync_all();
     const uint32_t tb = *tslot;
-    const uint32_t tS = tb, tV = tb + 128, tO0 = tb + 192;  // S^T 128 cols, V~^T 64, O^T 2 x 64
+    const uint32_t tS = tb;  // S: 128 columns; D buffers at tb + 128 and tb + 256
+    auto tDbuf = [&](int kk) { return tb + 128 + 128 * (uint32_t)(kk & 1); };
     auto packet = [&](int kk) { return packets + ((size_t)(c_begin + kk) * H + h) * PK_STRIDE; };
-    auto stage = [&](int kk) { return sm + (kk % CS_NST) * CS_ST_BYTES; };
+    auto stage = [&](int kk) { return sm + (kk & 1) * CS_ST_BYTES; };
     auto load_stage = [&](int kk) {
-        uint64_t *b = &bar_ld[kk % CS_NST];
+        uint64_t *b = &bar_ld[kk & 1];
         mbar_arrive_expect_tx(b, CS_ST_TX);
         bulk_g2s(stage(kk), packet(kk), CS_PK_MMA, b);
         bulk_g2s(stage(kk) + CS_G, packet(kk) + PK_G, 512, b);
     };
     if (tid == 0) {
-        for (int kk = 0; kk < (int)CS_NST && kk < nc; ++kk) load_stage(kk);
+        for (int kk = 0; kk < 2 && kk < nc; ++kk) load_stage(kk);
+        if (nc > 2) bulk_prefetch_l2(packet(2), PK_G + 512);
     }
 
-    if (warp == 12) {
+    if (warp == 8) {
         // ------------------------------------------------ MMA issue (one thread)
         if (lane == 0) {
-            const uint32_t id64 = idesc_bf16(128, 64), id64mn = idesc_bf16(128, 64, false, true);
-            const uint32_t id128mn = idesc_bf16(128, 128, false, true);
+            const uint32_t idD = idesc_bf16(128, 128, false, true);
+            const uint32_t idD64 = idesc_bf16(128, 64, false, true), idS64 = idesc_bf16(128, 64, true, true);
             bool ok = true;
             for (int kk = 0; kk < nc && ok; ++kk) {
                 unsigned char *P = stage(kk);
-                const uint32_t tO = tO0 + 64 * (kk & 1);
-                ok = mbar_wait(bar_simg, kk & 1);  // S^T image of S_kk written, packet kk resident
+                const uint32_t tD = tDbuf(kk);
+                if (kk >= 2) ok = mbar_wait_spin(&bar_free[kk & 1], ((kk >> 1) - 1) & 1);  // O of chunk kk - 2 read
+                for (int hv = 0; hv < 2 && ok; ++hv) {  // MMA1 per column half: D[:, half] = [W; Q^] S[:, half]
+                    ok = mbar_wait_spin(&bar_simg[hv], kk & 1);  // S image half of S_kk written, packet kk resident
+                    if (!ok) break;
+                    fence_after_sync();
+                    mma_bf16_kmn(tD + 64 * hv, smem_u32(P + PK_WQ), 128, smem_u32(sm + CS_SIMG + 16384 * hv), 16384,
+                                 8, idD64, false);
+                    mma_commit(&bar_v[hv]);
+                }
+                for (int hv = 0; hv < 2 && ok; ++hv) {  // MMA3 per column half: S[:, half] += K~^T V~[:, half]
+                    ok = mbar_wait_spin(&bar_vimg[hv], kk & 1);  // V~ half written, TMEM S half scaled by gamma_kk
+                    if (!ok) break;
+                    fence_after_sync();
+                    mma_bf16_mnmn(tS + 64 * hv, smem_u32(P + PK_K), 8192, smem_u32(sm + CS_VIMG + 8192 * hv), 8192,
+                                  4, idS64, true);
+                    mma_commit(&bar_s[hv]);
+                }
                 if (!ok) break;
-                fence_after_sync();
-                mma_bf16_kmn(tV, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_W), 8192, 8, id64mn, false);
-                mma_commit(bar_v);
-                if (kk >= 2) ok = mbar_wait(&bar_free[kk & 1], ((kk >> 1) - 1) & 1);  // O buffer read
-                if (!ok) break;
-                fence_after_sync();
-                mma_bf16_k(tO, smem_u32(sm + CS_SIMG), 128, smem_u32(P + PK_Q), 64, 8, id64, false);
-                ok = mbar_wait(bar_vimg, kk & 1);  // V~^T image written, TMEM S scaled by gamma_kk
-                if (!ok) break;
-                fence_after_sync();
-                mma_bf16_kmn(tS, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_K), 8192, 4, id128mn, true);
-                mma_commit(bar_s);
-                mma_bf16_k(tO, smem_u32(sm + CS_VIMG), 128, smem_u32(P + PK_A), 64, 4, id64, true);
+                mma_bf16_kmn(tD, smem_u32(P + PK_A - 8192), 128, smem_u32(sm + CS_VIMG), 8192, 4, idD, true);
                 mma_commit(&bar_o[kk & 1]);
             }
             if (!ok) atomicExch(s_fail, 1);
         }
-    } else if (warp >= 8) {
-        // ------------------------------------------------ output path (128 threads)
-        const int ot = tid - 256;
+    } else if (warp >= 10 && lq >= 2) {
+        // ------------------------------------------------ output warps 10, 11, 14, 15 (128 threads)
+        const int ot = (warp >= 14 ? 64 : 0) + (warp & 1) * 32 + lane;  // 0..127
+        const int t = row - 64;                                         // token of TMEM lane `row`
         bool ok = true;
-        for (int kk = 0; kk < nc; ++kk) {
-            ok = ok && mbar_wait(&bar_o[kk & 1], (kk >> 1) & 1);
+        for (int kk = 0; kk < nc && ok; ++kk) {
+            ok = mbar_wait(&bar_o[kk & 1], (kk >> 1) & 1);
+            ok = bar_red_popc(2, 128, ok) == 128;
             if (!ok) break;
             fence_after_sync();
-            // every MMA of chunk kk has completed: its packet stage can take chunk kk + 3
-            if (ot == 0 && kk + (int)CS_NST < nc) load_stage(kk + CS_NST);
+            if (ot == 0) {  // all MMAs of chunk kk are done: its stage takes chunk kk + 2
+                if (kk + 2 < nc) load_stage(kk + 2);
+                if (kk + 3 < nc) bulk_prefetch_l2(packet(kk + 3), PK_G + 512);
+            }
             const int64_t tp = s_tok + (int64_t)kk * C;
             const int lenp = (int)min((int64_t)C, e_tok - tp);
-            bf16 *oj = o + (tp * H + h) * D + j;
-            const uint32_t tO = tO0 + 64 * (kk & 1);
-            float d[32];
+            uint4 pk8[8];
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                tmem_ld32(tmem_addr(tO, lq * 32, c0), d);
+            for (int h2 = 0; h2 < 2; ++h2) {
+                float d[32];
+                tmem_ld32(tmem_addr(tDbuf(kk), 32 * lq, 64 * cg + 32 * h2), d);
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if (c0 + e < lenp) oj[(int64_t)(c0 + e) * H * D] = __float2bfloat16_rn(scale * d[e]);
+                for (int jj = 0; jj < 4; ++jj) {
+                    float v8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v8[e] = scale * d[8 * jj + e];
+                    pk8[4 * h2 + jj] = pack8(v8);
+                }
             }
             fence_before_sync();
-            mbar_arrive(&bar_free[kk & 1]);  // O buffer kk & 1 may be overwritten
+            mbar_arrive(&bar_free[kk & 1]);  // TMEM buffer read
+            if (lenp == C) {  // full chunk: two 64 x 64 swizzled tiles, two TMA stores
+                if (ot == 0) bulk_wait_read0();  // the previous tile has left the staging buffer
+                named_sync(2, 128);
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                    *reinterpret_cast<uint4 *>(sm + CS_OIMG + img_chunk_off(64, t, 8 * cg + jj)) = pk8[jj];
+                fence_proxy_async();
+                named_sync(2, 128);
+                if (ot == 0) {
+                    tma_store_3d(&omap, sm + CS_OIMG, 0, h, (int)tp);
+                    tma_store_3d(&omap, sm + CS_OIMG + 8192, 64, h, (int)tp);
+                    bulk_commit();
+                }
+            } else if (t < lenp) {  // the ragged last chunk of a sequence: rows past its end stay untouched
+                bf16 *dst = o + ((tp + t) * H + h) * D + 64 * cg;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) *reinterpret_cast<uint4 *>(dst + 8 * jj) = pk8[jj];
+            }
         }
+        if (ot == 0) bulk_wait0();
         if (!ok) atomicExch(s_fail, 1);
-    } else {
-        // ------------------------------------------------ state path (256 threads)
-        const int hf = warp >> 2;  // column half
+    } else if (warp < 8) {
+        // ------------------------------------------------ recurrence warps 0-7: half cg = warps 4 cg .. 4 cg + 3
+        const int nbar = cg ? 3 : 1;  // named barrier of this half (128 threads)
+        const int ht = tid & 127;     // thread within the half
         bool ok = true;
         {
-            float sreg[64];
+            float x[64];  // S_0 row `row`, columns [64 cg, 64 cg + 64)
             if (s_in) {
 #pragma unroll
                 for (int e = 0; e < 64; e += 4) {
-                    const float4 v4 = *reinterpret_cast<const float4 *>(s_in + (size_t)j * D + 64 * hf + e);
-                    sreg[e] = v4.x; sreg[e + 1] = v4.y; sreg[e + 2] = v4.z; sreg[e + 3] = v4.w;
+                    const float4 v4 = *reinterpret_cast<const float4 *>(
+                        s_in + (s_in_ll ? ll_off(row, 64 * cg + e) : (size_t)row * D + 64 * cg + e));
+                    x[e] = v4.x; x[e + 1] = v4.y; x[e + 2] = v4.z; x[e + 3] = v4.w;
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 64; ++e)
-                    sreg[e] = initial_state ? initial_state[st_off + (size_t)(64 * hf + e) * D + j] : 0.f;
+                for (int e = 0; e < 64; ++e) x[e] = 0.f;
             }
             if (nc > 0) ok = mbar_wait(&bar_ld[0], 0);
-            ok = (__syncthreads_count_named1(ok) == 256);
+            ok = bar_red_popc(nbar, 128, ok) == 128;
             if (nc == 0 && ok && final_state && last_seg) {
 #pragma unroll
-                for (int e = 0; e < 64; ++e) final_state[st_off + (size_t)(64 * hf + e) * D + j] = sreg[e];
+                for (int e = 0; e < 64; e += 4)
+                    *reinterpret_cast<float4 *>(final_state + st_off + (size_t)row * D + 64 * cg + e) =
+                        make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
             }
-            if (ok && nc > 0) {  // S_0 image; TMEM gets S_0 Diag(gamma_0)
-                const float *gam = (const float *)(stage(0) + CS_G);
+            if (ok && nc > 0) {  // S_0 image; TMEM gets Diag(gamma_0) S_0
 #pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 8)
-                    *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, (64 * hf + c0) / 8)) =
-                        pack8(sreg + c0);
+                for (int jj = 0; jj < 8; ++jj)
+                    *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, row, 8 * cg + jj)) = pack8(x + 8 * jj);
+                const float gr = reinterpret_cast<const float *>(stage(0) + CS_G)[row];
 #pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 16) {
-                    float sc[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) sc[e] = sreg[c0 + e] * gam[64 * hf + c0 + e];
-                    tmem_st16(tmem_addr(tS, lq * 32, 64 * hf + c0), sc);
-                }
+                for (int e = 0; e < 64; ++e) x[e] *= gr;
+                tmem_st32(tmem_addr(tS, 32 * lq, 64 * cg), x);
+                tmem_st32(tmem_addr(tS, 32 * lq, 64 * cg + 32), x + 32);
                 tmem_st_wait();
             }
         }
         fence_proxy_async();
         fence_before_sync();
-        named_sync(1, 256);
-        if (tid == 0 && nc > 0) mbar_arrive(bar_simg);
-        // U^T row j, columns [32 hf, 32 hf + 32) of chunks kk and kk + 1 (read-only global loads)
+        named_sync(nbar, 128);
+        if (ht == 0 && nc > 0) mbar_arrive(&bar_simg[cg]);
+        // U row `row` (a token; lane quarters 0, 1), columns [64 cg, 64 cg + 64), one chunk ahead
         auto load_u = [&](int kk, uint4 *u4) {
             const unsigned char *src = packet(kk) + PK_U;
 #pragma unroll
-            for (int hh = 0; hh < 4; ++hh)
-                u4[hh] = __ldg(reinterpret_cast<const uint4 *>(src + img_chunk_off(128, j, 4 * hf + hh)));
+            for (int jj = 0; jj < 8; ++jj)
+                u4[jj] = __ldg(reinterpret_cast<const uint4 *>(src + img_chunk_off(64, row, 8 * cg + jj)));
         };
-        uint4 ua[4], ub[4];
-        if (nc > 0) load_u(0, ua);
-        if (nc > 1) load_u(1, ub);
+        uint4 ua[8];
+        if (lq < 2 && nc > 0) load_u(0, ua);
         for (int kk = 0; kk < nc && ok; ++kk) {
-            // invariant: packet kk resident; S^T image = bf16(S_kk); TMEM S^T = S_kk^T Diag(gamma_kk)
-            ok = mbar_wait(bar_v, kk & 1);
-            ok = (__syncthreads_count_named1(ok) == 256) && (*(volatile int *)s_fail == 0);
+            // invariant: packet kk resident; S image = bf16(S_kk); TMEM S = Diag(gamma_kk) S_kk
+            if (ht == 0) ok = mbar_wait_spin(&bar_v[cg], kk & 1);  // one thread polls, the barrier releases
+            ok = (bar_red_popc(nbar, 128, ok) == 128) && (*(volatile int *)s_fail == 0);
             if (!ok) break;
             fence_after_sync();
-            // V~^T row j = U^T row j - (S^T W^T) row j, columns [32 hf, 32 hf + 32)
-            {
-                float dv[32], u[8], vo[8];
-                tmem_ld32(tmem_addr(tV, lq * 32, 32 * hf), dv);
+            if (lq < 2) {  // V~ row `row` = U - W S
 #pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {
-                    unpack8(ua[hh], u);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    float dv[32], u[8], vo[8];
+                    tmem_ld32(tmem_addr(tDbuf(kk), 32 * lq, 64 * cg + 32 * h2), dv);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) vo[e] = u[e] - dv[8 * hh + e];
-                    *reinterpret_cast<uint4 *>(sm + CS_VIMG + img_chunk_off(128, j, 4 * hf + hh)) = pack8(vo);
+                    for (int jj = 0; jj < 4; ++jj) {
+                        unpack8(ua[4 * h2 + jj], u);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) vo[e] = u[e] - dv[8 * jj + e];
+                        *reinterpret_cast<uint4 *>(sm + CS_VIMG + img_chunk_off(64, row, 8 * cg + 4 * h2 + jj)) =
+                            pack8(vo);
+                    }
                 }
-#pragma unroll
-                for (int hh = 0; hh < 4; ++hh) ua[hh] = ub[hh];
-                if (kk + 2 < nc) load_u(kk + 2, ub);
+                if (kk + 1 < nc) load_u(kk + 1, ua);
             }
             fence_proxy_async();
             fence_before_sync();
-            named_sync(1, 256);
-            if (tid == 0) mbar_arrive(bar_vimg);
+            named_sync(nbar, 128);
+            if (ht == 0) mbar_arrive(&bar_vimg[cg]);
             const bool last = (kk == nc - 1);
-            bool okl = true;
-            if (!last) okl = mbar_wait(&bar_ld[(kk + 1) % CS_NST], ((kk + 1) / CS_NST) & 1);
-            ok = mbar_wait(bar_s, kk & 1) && okl;
-            ok = (__syncthreads_count_named1(ok) == 256);
+            if (ht == 0) {
+                const bool okl = last || mbar_wait_spin(&bar_ld[(kk + 1) & 1], ((kk + 1) >> 1) & 1);
+                ok = mbar_wait_spin(&bar_s[cg], kk & 1) && okl;
+            }
+            ok = bar_red_popc(nbar, 128, ok) == 128;
             if (!ok) break;
             fence_after_sync();
             // S_{kk+1}: bf16 image and TMEM copy scaled by gamma_{kk+1}; or the final state
-            const float *gam = (const float *)(stage(kk + 1) + CS_G);
+            const float gr = last ? 1.f : reinterpret_cast<const float *>(stage(kk + 1) + CS_G)[row];
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
+            for (int h2 = 0; h2 < 2; ++h2) {
                 float x[32];
-                tmem_ld32(tmem_addr(tS, lq * 32, 64 * hf + c0), x);
+                const int c0 = 64 * cg + 32 * h2;
+                tmem_ld32(tmem_addr(tS, 32 * lq, c0), x);
                 if (!last) {
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8)
-                        *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, j, (64 * hf + c0) / 8 + q8)) =
-                            pack8(x + 8 * q8);
+                    for (int jj = 0; jj < 4; ++jj)
+                        *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, row, c0 / 8 + jj)) =
+                            pack8(x + 8 * jj);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] *= gam[64 * hf + c0 + e];
-                    tmem_st16(tmem_addr(tS, lq * 32, 64 * hf + c0), x);
-                    tmem_st16(tmem_addr(tS, lq * 32, 64 * hf + c0 + 16), x + 16);
+                    for (int e = 0; e < 32; ++e) x[e] *= gr;
+                    tmem_st32(tmem_addr(tS, 32 * lq, c0), x);
                 } else if (final_state && last_seg) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) final_state[st_off + (size_t)(64 * hf + c0 + e) * D + j] = x[e];
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(final_state + st_off + (size_t)row * D + c0 + e) =
+                            make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
                 }
             }
             if (!last) tmem_st_wait();
             fence_proxy_async();
             fence_before_sync();
-            named_sync(1, 256);
-            if (tid == 0 && !last) mbar_arrive(bar_simg);
+            named_sync(nbar, 128);
+            if (ht == 0 && !last) mbar_arrive(&bar_simg[cg]);
         }
         if (!ok) atomicExch(s_fail, 1);
     }
@@ -918,22 +978,29 @@ chunk_inter_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const in
 // Segment summaries (section 5.1.2, Eq. 17, used inside one device): for every segment but
 // the last of its sequence, run the state recurrence over the segment's chunks on the pair
 // [S~ | M] from [0 | I]: S~ with the segment's values, M with values zero.  Then for any
-// entering state, S_out = M S_in + S~.  Both are kept transposed in TMEM exactly like the
-// state of the output pass; Q^ and A are not needed, so a compact packet stage is loaded.
-// Three stages of W^T, K~ and gamma; U^T goes from global memory to registers two chunks ahead.
+// entering state, S_out = M S_in + S~.  [S~ | M] is kept like the state of the output pass
+// (d_k lanes; 256 columns), so per chunk:
+//   MMA1  D = W [S~ | M]                       (M = 128 with rows 64-127 unused, K = 128)
+//   V~    = [U - W S~ | -W M]                  (TMEM lanes 0-63), token-major images
+//   MMA2  [S~ | M] <- Diag(gamma) [S~ | M] + K~^T [V~_S | V~_M]   (K = 64)
+// S~ and M are independent chains (N = 128 each) run by separate warp groups.
+// A stage holds [W half 0 | K~ half 0 | W half 1 | K~ half 1 | gamma]: read as a 128-row K-major image
+// it is W (rows 64-127 are K~ and land in unused lanes); K~ is read MN-major with its halves 16 KB
+// apart.  U goes from global memory to registers one chunk ahead.
 constexpr uint32_t SS_NST = 3;
 constexpr uint32_t SS_STAGE_BYTES = 33792;
-constexpr uint32_t SS_W = 0, SS_K = 16384, SS_G = 32768;
-constexpr uint32_t SS_SIMG = SS_NST * SS_STAGE_BYTES;  // S~^T image 128 x 128
-constexpr uint32_t SS_MIMG = SS_SIMG + 32768;          // M^T image
-constexpr uint32_t SS_VSIMG = SS_MIMG + 32768;         // V~_S^T image 128 x 64
-constexpr uint32_t SS_VMIMG = SS_VSIMG + 16384;        // V~_M^T image
-constexpr uint32_t SS_BAR = SS_VMIMG + 16384;
+constexpr uint32_t SS_G = 32768;
+constexpr uint32_t SS_SIMG = SS_NST * SS_STAGE_BYTES;  // [S~ | M] image: rows d_k, 4 x 64 columns (16 KB each)
+constexpr uint32_t SS_VIMG = SS_SIMG + 65536;          // [V~_S | V~_M] token-major image, 4 x 8 KB
+constexpr uint32_t SS_BAR = SS_VIMG + 32768;
 constexpr uint32_t SS_TSLOT = SS_BAR + 64;
 constexpr uint32_t SS_TOTAL = SS_BAR + 128 + 1024;
-constexpr uint32_t SS_TX = 16384 + 16384 + 512;
+constexpr uint32_t SS_TX = 4 * 8192 + 512;
+// Summary record per (segment, head): S~ fp32 (lane-major, see ll_off), then M as bf16 high and low
+// K-major images.
+constexpr size_t SUM_M_HI = 65536, SUM_M_LO = 98304;
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(512, 1)
 chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int32_t *__restrict__ seg_start,
                        int64_t seg_len, int H, const unsigned char *__restrict__ packets,
                        float *__restrict__ seg_sum, int *err) {
@@ -956,156 +1023,164 @@ chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int
     const int c_begin = chunk_start[n] + (int)kk0;
     const int nc = (int)min(seg_len, (int64_t)(chunk_start[n + 1] - chunk_start[n]) - kk0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int lq = warp & 3, hf = warp >> 2;
-    const int j = lq * 32 + lane;
+    const int lq = warp & 3, cg = warp >> 2;  // TMEM lane quarter; 64-column group of 256
+    const int row = 32 * lq + lane;
     uint64_t *bar_ld = (uint64_t *)(sm + SS_BAR);  // [3]
-    uint64_t *bar_v = bar_ld + 3, *bar_s = bar_ld + 4;
+    uint64_t *bar_v = bar_ld + 3, *bar_s = bar_ld + 5;  // [2 chains] each
     uint32_t *tslot = (uint32_t *)(sm + SS_TSLOT);
     if (tid == 0) {
-        mbar_init(&bar_ld[0], 1);
-        mbar_init(&bar_ld[1], 1);
-        mbar_init(&bar_ld[2], 1);
-        mbar_init(bar_v, 1);
-        mbar_init(bar_s, 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&bar_ld[i], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_v[i], 1);
+            mbar_init(&bar_s[i], 1);
+        }
     }
     if (warp == 0) tmem_alloc(tslot, 512);
     fence_proxy_async();
     sync_all();
     const uint32_t tb = *tslot;
-    const uint32_t tSt = tb, tMt = tb + 128, tVS = tb + 256, tVM = tb + 320;
-    auto issue = [&](int kk, int st) {
-        const unsigned char *pk = packets + ((size_t)(c_begin + kk) * H + h) * PK_STRIDE;
-        unsigned char *dst = sm + st * SS_STAGE_BYTES;
-        mbar_arrive_expect_tx(&bar_ld[st], SS_TX);
-        bulk_g2s(dst + SS_W, pk + PK_W, 16384, &bar_ld[st]);
-        bulk_g2s(dst + SS_K, pk + PK_K, 16384, &bar_ld[st]);
-        bulk_g2s(dst + SS_G, pk + PK_G, 512, &bar_ld[st]);
+    const uint32_t tSM = tb, tDV = tb + 256;  // [S~ | M] (256 columns); D (256 columns, lanes 0-63)
+    auto packet = [&](int kk) { return packets + ((size_t)(c_begin + kk) * H + h) * PK_STRIDE; };
+    auto issue = [&](int kk) {
+        unsigned char *dst = sm + (kk % SS_NST) * SS_STAGE_BYTES;
+        uint64_t *b = &bar_ld[kk % SS_NST];
+        const unsigned char *pk = packet(kk);
+        mbar_arrive_expect_tx(b, SS_TX);
+        bulk_g2s(dst, pk + PK_WQ, 8192, b);
+        bulk_g2s(dst + 8192, pk + PK_K, 8192, b);
+        bulk_g2s(dst + 16384, pk + PK_WQ + 16384, 8192, b);
+        bulk_g2s(dst + 24576, pk + PK_K + 8192, 8192, b);
+        bulk_g2s(dst + SS_G, pk + PK_G, 512, b);
     };
     if (tid == 0) {
-        for (int kk = 0; kk < (int)SS_NST && kk < nc; ++kk) issue(kk, kk);
+        for (int kk = 0; kk < (int)SS_NST && kk < nc; ++kk) issue(kk);
     }
     bool ok = wait_all(&bar_ld[0], 0);
     fence_after_sync();
-    if (ok) {  // [S~ | M] = [0 | I]; TMEM copies scaled by gamma_0 (column scale)
-        const float *gam = (const float *)(sm + SS_G);
+    if (ok) {  // [S~ | M] = [0 | I]: image, and TMEM scaled by gamma_0 (a per-row scale)
+        const float gr = reinterpret_cast<const float *>(sm + SS_G)[row];
 #pragma unroll
-        for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 16) {
-            float z16[16], m16[16], ms[16];
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+            float x[16], xs[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-                z16[e] = 0.f;
-                m16[e] = (c0 + e == j) ? 1.f : 0.f;
-                ms[e] = m16[e] * gam[c0 + e];
+                const int c = 64 * cg + c0 + e;
+                x[e] = (c >= 128 && c - 128 == row) ? 1.f : 0.f;
+                xs[e] = x[e] * gr;
             }
-            tmem_st16(tmem_addr(tSt, lq * 32, c0), z16);
-            tmem_st16(tmem_addr(tMt, lq * 32, c0), ms);
-            *reinterpret_cast<uint4 *>(sm + SS_SIMG + img_chunk_off(128, j, c0 / 8)) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(sm + SS_SIMG + img_chunk_off(128, j, c0 / 8 + 1)) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(sm + SS_MIMG + img_chunk_off(128, j, c0 / 8)) = pack8(m16);
-            *reinterpret_cast<uint4 *>(sm + SS_MIMG + img_chunk_off(128, j, c0 / 8 + 1)) = pack8(m16 + 8);
+            tmem_st16(tmem_addr(tSM, 32 * lq, 64 * cg + c0), xs);
+            *reinterpret_cast<uint4 *>(sm + SS_SIMG + img_chunk_off(128, row, (64 * cg + c0) / 8)) = pack8(x);
+            *reinterpret_cast<uint4 *>(sm + SS_SIMG + img_chunk_off(128, row, (64 * cg + c0) / 8 + 1)) = pack8(x + 8);
         }
         tmem_st_wait();
     }
     fence_proxy_async();
     sync_all();
-    // W^T and K~ are MN-major B operands (K rows of 128 bytes)
-    const uint32_t id64 = idesc_bf16(128, 64, false, true), id128 = idesc_bf16(128, 128, false, true);
-    auto load_u = [&](int kk, uint4 *u4) {  // U^T row j, columns [32 hf, 32 hf + 32)
-        const unsigned char *src = packets + ((size_t)(c_begin + kk) * H + h) * PK_STRIDE + PK_U;
+    // Two independent chains: warps 0-7 carry S~ (columns 0-127 of [S~ | M]), warps 8-15 carry M
+    // (columns 128-255); each issues its own MMAs and synchronises on its own barriers, so one chain's
+    // CUDA-core phases overlap the other's products.
+    const int ch = warp >> 3, nb = 1 + ch, ct = tid & 255;
+    // U row `row` (a token), columns [64 cg, 64 cg + 64) for warps with lq < 2 and cg < 2
+    const bool vrow = (lq < 2), uneed = vrow && (cg < 2);
+    uint4 ua[8];
+    auto load_u = [&](int kk) {
+        const unsigned char *src = packet(kk) + PK_U;
 #pragma unroll
-        for (int hh = 0; hh < 4; ++hh)
-            u4[hh] = __ldg(reinterpret_cast<const uint4 *>(src + img_chunk_off(128, j, 4 * hf + hh)));
+        for (int jj = 0; jj < 8; ++jj)
+            ua[jj] = __ldg(reinterpret_cast<const uint4 *>(src + img_chunk_off(64, row, 8 * cg + jj)));
     };
-    uint4 ua[4], ub[4];
-    if (nc > 0) load_u(0, ua);
-    if (nc > 1) load_u(1, ub);
+    if (uneed && nc > 0) load_u(0);
+    const uint32_t id1 = idesc_bf16(128, 128, false, true), id2 = idesc_bf16(128, 128, true, true);
     for (int kk = 0; kk < nc && ok; ++kk) {
         unsigned char *P = sm + (kk % SS_NST) * SS_STAGE_BYTES;
-        if (tid == 0) {
-            mma_bf16_kmn(tVS, smem_u32(sm + SS_SIMG), 128, smem_u32(P + SS_W), 8192, 8, id64, false);
-            mma_bf16_kmn(tVM, smem_u32(sm + SS_MIMG), 128, smem_u32(P + SS_W), 8192, 8, id64, false);
-            mma_commit(bar_v);
+        if (ct == 0) {  // D[:, chain] = W [S~ | M][:, chain]
+            fence_after_sync();
+            mma_bf16_kmn(tDV + 128 * ch, smem_u32(P), 128, smem_u32(sm + SS_SIMG + 32768 * ch), 16384, 8, id1, false);
+            mma_commit(&bar_v[ch]);
+            ok = mbar_wait_spin(&bar_v[ch], kk & 1);
         }
-        ok = wait_all(bar_v, kk & 1);
+        ok = bar_red_popc(nb, 256, ok) == 256;
         if (!ok) break;
         fence_after_sync();
-        {
-            float dvs[32], dvm[32], u[8], o1[8], o2[8];
-            tmem_ld32(tmem_addr(tVS, lq * 32, 32 * hf), dvs);
-            tmem_ld32(tmem_addr(tVM, lq * 32, 32 * hf), dvm);
+        if (vrow) {  // V~ row `row`: columns [64 cg, 64 cg + 64) of [U - W S~ | -W M]
 #pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-                unpack8(ua[hh], u);
+            for (int h2 = 0; h2 < 2; ++h2) {
+                float d[32], u[8], vo[8];
+                tmem_ld32(tmem_addr(tDV, 32 * lq, 64 * cg + 32 * h2), d);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    o1[e] = u[e] - dvs[8 * hh + e];
-                    o2[e] = -dvm[8 * hh + e];
+                for (int jj = 0; jj < 4; ++jj) {
+                    if (uneed) {
+                        unpack8(ua[4 * h2 + jj], u);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) vo[e] = u[e] - d[8 * jj + e];
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) vo[e] = -d[8 * jj + e];
+                    }
+                    *reinterpret_cast<uint4 *>(sm + SS_VIMG + img_chunk_off(64, row, 8 * cg + 4 * h2 + jj)) = pack8(vo);
                 }
-                *reinterpret_cast<uint4 *>(sm + SS_VSIMG + img_chunk_off(128, j, 4 * hf + hh)) = pack8(o1);
-                *reinterpret_cast<uint4 *>(sm + SS_VMIMG + img_chunk_off(128, j, 4 * hf + hh)) = pack8(o2);
             }
-#pragma unroll
-            for (int hh = 0; hh < 4; ++hh) ua[hh] = ub[hh];
-            if (kk + 2 < nc) load_u(kk + 2, ub);
+            if (uneed && kk + 1 < nc) load_u(kk + 1);
         }
         fence_proxy_async();
-        sync_all();
-        if (tid == 0) {
-            mma_bf16_kmn(tSt, smem_u32(sm + SS_VSIMG), 128, smem_u32(P + SS_K), 8192, 4, id128, true);
-            mma_bf16_kmn(tMt, smem_u32(sm + SS_VMIMG), 128, smem_u32(P + SS_K), 8192, 4, id128, true);
-            mma_commit(bar_s);
-        }
+        fence_before_sync();
+        named_sync(nb, 256);
         const bool last = (kk == nc - 1);
-        bool okl = true;
-        if (!last) okl = mbar_wait(&bar_ld[(kk + 1) % SS_NST], ((kk + 1) / SS_NST) & 1);
-        ok = mbar_wait(bar_s, kk & 1) && okl;
-        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        if (ct == 0) {  // [S~ | M][:, chain] += K~^T V~[:, chain]
+            fence_after_sync();
+            mma_bf16_mnmn(tSM + 128 * ch, smem_u32(P + 8192), 16384, smem_u32(sm + SS_VIMG + 16384 * ch), 8192, 4, id2,
+                          true);
+            mma_commit(&bar_s[ch]);
+            const bool okl = last || mbar_wait_spin(&bar_ld[(kk + 1) % SS_NST], ((kk + 1) / SS_NST) & 1);
+            ok = mbar_wait_spin(&bar_s[ch], kk & 1) && okl;
+        }
+        ok = bar_red_popc(nb, 256, ok) == 256;
         if (!ok) break;
         fence_after_sync();
-        const float *gam = (const float *)(sm + ((kk + 1) % SS_NST) * SS_STAGE_BYTES + SS_G);
+        const float gr = reinterpret_cast<const float *>(sm + ((kk + 1) % SS_NST) * SS_STAGE_BYTES + SS_G)[row];
         float *out = seg_sum + ((size_t)g * H + h) * 2 * D * D;
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            const uint32_t tX = which ? tMt : tSt;
-            unsigned char *img = sm + (which ? SS_MIMG : SS_SIMG);
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int c0 = 64 * cg + 32 * h2;  // column in [S~ | M]
+            float x[32];
+            tmem_ld32(tmem_addr(tSM, 32 * lq, c0), x);
+            if (!last) {
 #pragma unroll
-            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
-                float x[32];
-                tmem_ld32(tmem_addr(tX, lq * 32, c0), x);
-                if (!last) {
+                for (int q8 = 0; q8 < 4; ++q8)
+                    *reinterpret_cast<uint4 *>(sm + SS_SIMG + img_chunk_off(128, row, c0 / 8 + q8)) = pack8(x + 8 * q8);
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8)
-                        *reinterpret_cast<uint4 *>(img + img_chunk_off(128, j, c0 / 8 + q8)) = pack8(x + 8 * q8);
+                for (int e = 0; e < 32; ++e) x[e] *= gr;
+                tmem_st32(tmem_addr(tSM, 32 * lq, c0), x);
+            } else if (c0 < 128) {  // S~ row `row`, fp32
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] *= gam[c0 + e];
-                    tmem_st16(tmem_addr(tX, lq * 32, c0), x);
-                    tmem_st16(tmem_addr(tX, lq * 32, c0 + 16), x + 16);
-                } else if (which == 0) {  // S~^T row j
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(out + ll_off(row, c0 + e)) =
+                        make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+            } else {  // M row `row` as bf16 high / low parts of a K-major image (the fold's A operand)
+                unsigned char *mimg = reinterpret_cast<unsigned char *>(out);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4 *>(out + (size_t)j * D + c0 + e) =
-                            make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-                } else {  // M^T row j as bf16 high / low parts, 128-byte-swizzled rows (the fold's operand)
-                    unsigned char *mimg = reinterpret_cast<unsigned char *>(out + D * D);
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    float hi[8], lo[8];
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        float hi[8], lo[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            hi[e] = __bfloat162float(__float2bfloat16_rn(x[8 * q8 + e]));
-                            lo[e] = x[8 * q8 + e] - hi[e];
-                        }
-                        const uint32_t off = img_chunk_off(128, j, c0 / 8 + q8);
-                        *reinterpret_cast<uint4 *>(mimg + off) = pack8(hi);
-                        *reinterpret_cast<uint4 *>(mimg + 32768 + off) = pack8(lo);
+                    for (int e = 0; e < 8; ++e) {
+                        hi[e] = __bfloat162float(__float2bfloat16_rn(x[8 * q8 + e]));
+                        lo[e] = x[8 * q8 + e] - hi[e];
                     }
+                    const uint32_t off = img_chunk_off(128, row, (c0 - 128) / 8 + q8);
+                    *reinterpret_cast<uint4 *>(mimg + SUM_M_HI + off) = pack8(hi);
+                    *reinterpret_cast<uint4 *>(mimg + SUM_M_LO + off) = pack8(lo);
                 }
             }
         }
         if (!last) tmem_st_wait();
         fence_proxy_async();
-        sync_all();
-        if (tid == 0 && kk + (int)SS_NST < nc) issue(kk + SS_NST, kk % SS_NST);
+        fence_before_sync();
+        named_sync(nb, 256);
+        // stage kk is free once both chains' products of chunk kk are done
+        if (ch == 1 && ct == 0 && kk + (int)SS_NST < nc) {
+            if (mbar_wait_spin(&bar_s[0], kk & 1)) issue(kk + SS_NST);
+            else ok = false;
+        }
     }
     if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     sync_all();
@@ -1115,18 +1190,18 @@ chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int
 // =====================================================================================
 // Fold of the segment summaries of each (sequence, head) in order (section 5.1.2: the
 // rank-level updates compose associatively): S_in(i+1) = M_i S_in(i) + S~_i, starting from
-// the sequence's initial state.  Transposed: S^T <- S~^T + S^T M^T, an MMA with A = S^T (K-major
-// image) and B = M^T (read MN-major from the rows the summary pass wrote).  Both factors are
-// split into bf16 high and low parts and hi*hi + hi*lo + lo*hi is accumulated (near-fp32
-// accuracy): one N = 256 product A_hi [M^T_hi | M^T_lo] and one N = 128 product A_lo M^T_hi.
-// The M^T images of step i + 2 are bulk-copied while step i runs; S~^T of step i + 1 is read into
-// registers during step i and placed in tensor memory, where the readout adds it.
-constexpr uint32_t FD_STG = 0;                 // 2 stages x [M^T hi | M^T lo] (64 KB each)
-constexpr uint32_t FD_AHI = 131072, FD_ALO = FD_AHI + 32768;  // S^T hi / lo images (32 KB each)
-constexpr uint32_t FD_BAR = FD_ALO + 32768;    // ld[2], mma
+// the sequence's initial state.  An MMA with A = M (K-major high / low images written by the summary
+// pass) and B = S_in (rows d_k, read MN-major); both factors are split into bf16 high and low parts
+// and hi*hi + hi*lo + lo*hi is accumulated (near-fp32 accuracy): one N = 256 product
+// M_hi [S_hi | S_lo] and one N = 128 product M_lo S_hi.  The M images of step i + 2 are bulk-copied
+// while step i runs; S~ of step i + 1 is read into registers during step i and placed in tensor
+// memory, where the readout adds it.
+constexpr uint32_t FD_STG = 0;                 // 2 stages x [M hi | M lo] (64 KB each)
+constexpr uint32_t FD_B = 131072;              // [S_in hi | S_in lo] image: rows d_k, 4 x 64 columns (64 KB)
+constexpr uint32_t FD_BAR = FD_B + 65536;      // ld[2], mma
 constexpr uint32_t FD_TSLOT = FD_BAR + 32;
 constexpr uint32_t FD_TOTAL = FD_BAR + 64 + 1024;
-constexpr uint32_t TF_D = 0, TF_ST = 256;      // TMEM: products (256 columns), S~^T (128 columns)
+constexpr uint32_t TF_D = 0, TF_ST = 256;      // TMEM: products (256 columns), S~ (128 columns)
 
 __global__ void __launch_bounds__(256, 1)
 chunk_fold_tc_kernel(int N, const int32_t *__restrict__ seg_start, int H, const float *initial_state,
@@ -1139,14 +1214,15 @@ chunk_fold_tc_kernel(int N, const int32_t *__restrict__ seg_start, int H, const 
     const int steps = nseg - 1;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lq = warp & 3, hf = warp >> 2;
-    const int j = lq * 32 + lane;  // S^T row (value channel) = TMEM lane
+    const int row = lq * 32 + lane;  // d_k row of S = TMEM lane
     uint64_t *bar_ld = (uint64_t *)(sm + FD_BAR);
     uint64_t *bar_mma = bar_ld + 2;
     uint32_t *tslot = (uint32_t *)(sm + FD_TSLOT);
     auto summary = [&](int i) { return seg_sum + ((size_t)(g0 + i) * H + h) * 2 * D * D; };
-    auto issue = [&](int i) {  // M^T hi / lo images of step i into stage i & 1
+    auto issue = [&](int i) {  // M hi / lo images of step i into stage i & 1
         mbar_arrive_expect_tx(&bar_ld[i & 1], 65536);
-        bulk_g2s(sm + FD_STG + (i & 1) * 65536, summary(i) + D * D, 65536, &bar_ld[i & 1]);
+        bulk_g2s(sm + FD_STG + (i & 1) * 65536, reinterpret_cast<const unsigned char *>(summary(i)) + SUM_M_HI,
+                 65536, &bar_ld[i & 1]);
     };
     if (tid == 0) {
         mbar_init(&bar_ld[0], 1);
@@ -1162,26 +1238,30 @@ chunk_fold_tc_kernel(int N, const int32_t *__restrict__ seg_start, int H, const 
         if (steps > 1) issue(1);
     }
     const size_t st_off = ((size_t)n * H + h) * D * D;
-    float sreg[64];  // S^T row j, columns [64 hf, 64 hf + 64)
+    float sreg[64];  // S row `row`, columns [64 hf, 64 hf + 64)
 #pragma unroll
-    for (int e = 0; e < 64; ++e) sreg[e] = initial_state ? initial_state[st_off + (size_t)(64 * hf + e) * D + j] : 0.f;
+    for (int e = 0; e < 64; e += 4) {
+        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (initial_state) v4 = *reinterpret_cast<const float4 *>(initial_state + st_off + (size_t)row * D + 64 * hf + e);
+        sreg[e] = v4.x; sreg[e + 1] = v4.y; sreg[e + 2] = v4.z; sreg[e + 3] = v4.w;
+    }
     {
         float *dst0 = seg_in + ((size_t)g0 * H + h) * D * D;  // segment 0 enters with S0
 #pragma unroll
         for (int e = 0; e < 64; e += 4)
-            *reinterpret_cast<float4 *>(dst0 + (size_t)j * D + 64 * hf + e) =
+            *reinterpret_cast<float4 *>(dst0 + ll_off(row, 64 * hf + e)) =
                 make_float4(sreg[e], sreg[e + 1], sreg[e + 2], sreg[e + 3]);
     }
-    float nxt[64];  // S~^T row j of the current step
+    float nxt[64];  // S~ row `row` of the current step
 #pragma unroll
     for (int e = 0; e < 64; e += 4) {
-        const float4 v4 = *reinterpret_cast<const float4 *>(summary(0) + (size_t)j * D + 64 * hf + e);
+        const float4 v4 = *reinterpret_cast<const float4 *>(summary(0) + ll_off(row, 64 * hf + e));
         nxt[e] = v4.x; nxt[e + 1] = v4.y; nxt[e + 2] = v4.z; nxt[e + 3] = v4.w;
     }
     bool ok = true;
     const uint32_t id256 = idesc_bf16(128, 256, false, true), id128 = idesc_bf16(128, 128, false, true);
     for (int i = 0; i < steps && ok; ++i) {
-        // S~^T into TMEM; S_in^T hi / lo images
+        // S~ into TMEM; S_in hi / lo images (rows d_k)
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 16) tmem_st16(tmem_addr(tb + TF_ST, lq * 32, 64 * hf + c0), nxt + c0);
 #pragma unroll
@@ -1192,9 +1272,9 @@ chunk_fold_tc_kernel(int N, const int32_t *__restrict__ seg_start, int H, const 
                 hi[e] = __bfloat162float(__float2bfloat16_rn(sreg[c0 + e]));
                 lo[e] = sreg[c0 + e] - hi[e];
             }
-            const uint32_t off = img_chunk_off(128, j, (64 * hf + c0) / 8);
-            *reinterpret_cast<uint4 *>(sm + FD_AHI + off) = pack8(hi);
-            *reinterpret_cast<uint4 *>(sm + FD_ALO + off) = pack8(lo);
+            const uint32_t off = img_chunk_off(128, row, (64 * hf + c0) / 8);
+            *reinterpret_cast<uint4 *>(sm + FD_B + off) = pack8(hi);
+            *reinterpret_cast<uint4 *>(sm + FD_B + 32768 + off) = pack8(lo);
         }
         tmem_st_wait();
         fence_proxy_async();
@@ -1202,15 +1282,15 @@ chunk_fold_tc_kernel(int N, const int32_t *__restrict__ seg_start, int H, const 
         if (!ok) break;
         fence_after_sync();
         if (tid == 0) {
-            const uint32_t B = smem_u32(sm + FD_STG + (i & 1) * 65536);
-            mma_bf16_kmn(tb + TF_D, smem_u32(sm + FD_AHI), 128, B, 16384, 8, id256, false);
-            mma_bf16_kmn(tb + TF_D, smem_u32(sm + FD_ALO), 128, B, 16384, 8, id128, true);
+            const uint32_t A = smem_u32(sm + FD_STG + (i & 1) * 65536);
+            mma_bf16_kmn(tb + TF_D, A, 128, smem_u32(sm + FD_B), 16384, 8, id256, false);
+            mma_bf16_kmn(tb + TF_D, A + 32768, 128, smem_u32(sm + FD_B), 16384, 8, id128, true);
             mma_commit(bar_mma);
         }
         if (i + 1 < steps) {
 #pragma unroll
             for (int e = 0; e < 64; e += 4) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(summary(i + 1) + (size_t)j * D + 64 * hf + e);
+                const float4 v4 = *reinterpret_cast<const float4 *>(summary(i + 1) + ll_off(row, 64 * hf + e));
                 nxt[e] = v4.x; nxt[e + 1] = v4.y; nxt[e + 2] = v4.z; nxt[e + 3] = v4.w;
             }
         }
@@ -1229,7 +1309,7 @@ chunk_fold_tc_kernel(int N, const int32_t *__restrict__ seg_start, int H, const 
             for (int e = 0; e < 16; ++e) sreg[c0 + e] = a[e] + b[e] + c[e];
 #pragma unroll
             for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<float4 *>(dst + (size_t)j * D + 64 * hf + c0 + e) =
+                *reinterpret_cast<float4 *>(dst + ll_off(row, 64 * hf + c0 + e)) =
                     make_float4(sreg[c0 + e], sreg[c0 + e + 1], sreg[c0 + e + 2], sreg[c0 + e + 3]);
         }
         fence_before_sync();
@@ -1296,8 +1376,11 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     const int32_t *chunk_start = (const int32_t *)((char *)ws + p.off_chunk_start);
     unsigned char *packets = (unsigned char *)ws + p.off_records;
     if (p.max_chunks > 0 && a->T > 0) {
-        cudaFuncSetAttribute(tcp::chunk_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tcp::J_TOTAL);
+        {
+            const kda_status_t cst = kda_cuda_status(cudaFuncSetAttribute(tcp::chunk_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                                          (int)tcp::J_TOTAL));
+            if (cst != KDA_OK) return cst;
+        }
         int dev = 0, sms = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1310,7 +1393,10 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
         tcp::chunk_intra_tc_kernel<<<grid, tcp::NT2, tcp::J_TOTAL, stream>>>(
             tm, (const bf16 *)a->beta, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
             chunk_start, p.H, packets, err);
-        if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+        {
+            const kda_status_t cst = kda_cuda_status(cudaGetLastError());
+            if (cst != KDA_OK) return cst;
+        }
     }
     kda_profile_mark(2, stream);
     const int32_t *seg_start = (const int32_t *)((char *)ws + p.off_seg_start);
@@ -1318,24 +1404,41 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     float *seg_in = (float *)((char *)ws + p.off_seg_in);
     int mark = 3;
     if (p.split) {
-        cudaFuncSetAttribute(tcp::chunk_segsum_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tcp::SS_TOTAL);
-        tcp::chunk_segsum_tc_kernel<<<dim3((unsigned)p.max_segs, (unsigned)p.H), 256, tcp::SS_TOTAL, stream>>>(
+        {
+            const kda_status_t cst = kda_cuda_status(cudaFuncSetAttribute(tcp::chunk_segsum_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                                          (int)tcp::SS_TOTAL));
+            if (cst != KDA_OK) return cst;
+        }
+        tcp::chunk_segsum_tc_kernel<<<dim3((unsigned)p.max_segs, (unsigned)p.H), 512, tcp::SS_TOTAL, stream>>>(
             (int)a->N, chunk_start, seg_start, p.seg_len, p.H, packets, seg_sum, err);
-        if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+        {
+            const kda_status_t cst = kda_cuda_status(cudaGetLastError());
+            if (cst != KDA_OK) return cst;
+        }
         kda_profile_mark(mark++, stream);
-        cudaFuncSetAttribute(tcp::chunk_fold_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tcp::FD_TOTAL);
+        {
+            const kda_status_t cst = kda_cuda_status(cudaFuncSetAttribute(tcp::chunk_fold_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                                          (int)tcp::FD_TOTAL));
+            if (cst != KDA_OK) return cst;
+        }
         tcp::chunk_fold_tc_kernel<<<dim3((unsigned)a->N, (unsigned)p.H), 256, tcp::FD_TOTAL, stream>>>(
             (int)a->N, seg_start, p.H, a->initial_state, seg_sum, seg_in, err);
-        if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+        {
+            const kda_status_t cst = kda_cuda_status(cudaGetLastError());
+            if (cst != KDA_OK) return cst;
+        }
         kda_profile_mark(mark++, stream);
     }
-    cudaFuncSetAttribute(tcp::chunk_inter_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)tcp::CS_TOTAL);
+    {
+        const kda_status_t cst = kda_cuda_status(cudaFuncSetAttribute(tcp::chunk_inter_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                                      (int)tcp::CS_TOTAL));
+        if (cst != KDA_OK) return cst;
+    }
+    CUtensorMap omap;
+    if (!make_tile_map(&omap, a->o, a->T, p.H)) return KDA_ERR_CUDA;
     tcp::chunk_inter_tc_kernel<<<dim3((unsigned)p.max_segs, (unsigned)p.H), tcp::NT3, tcp::CS_TOTAL, stream>>>(
-        a->T, (int)a->N, a->cu_seqlens, chunk_start, seg_start, p.seg_len, seg_in, p.H, packets, a->scale,
+        omap, a->T, (int)a->N, a->cu_seqlens, chunk_start, seg_start, p.seg_len, seg_in, p.H, packets, a->scale,
         a->initial_state, a->final_state, (bf16 *)a->o, err);
     kda_profile_mark(mark, stream);
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return kda_cuda_status(cudaGetLastError());
 }

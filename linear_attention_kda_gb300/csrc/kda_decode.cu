@@ -166,5 +166,5 @@ kda_status_t kda_launch_decode(const kda_step_args *a, cudaStream_t stream) {
     if (a->dk == 128) { if (b16) launch<128, bf16>(a, stream, err); else launch<128, float>(a, stream, err); }
     else { if (b16) launch<64, bf16>(a, stream, err); else launch<64, float>(a, stream, err); }
     kda_profile_mark(1, stream);
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return kda_cuda_status(cudaGetLastError());
 }

@@ -114,5 +114,5 @@ kda_status_t kda_launch_gate(const kda_gate_args *a, cudaStream_t stream) {
                 (const float *)a->z, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
                 a->H, a->dk, C, a->out, err);
     }
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return kda_cuda_status(cudaGetLastError());
 }

@@ -7,6 +7,8 @@
 
 // Records the i-th profiling event on `stream` when instrumentation is set.
 void kda_profile_mark(int i, cudaStream_t stream);
+// KDA_OK for cudaSuccess; otherwise records the code for kda_last_cuda_error() and returns KDA_ERR_CUDA.
+kda_status_t kda_cuda_status(cudaError_t e);
 
 kda_status_t kda_launch_gate(const kda_gate_args *a, cudaStream_t stream);
 kda_status_t kda_launch_decode(const kda_step_args *a, cudaStream_t stream);
@@ -28,9 +30,9 @@ struct kda_chunk_plan {
     int64_t seg_len;         // chunks per segment
     int64_t max_segs;        // upper bound on segments over all sequences
     size_t off_seg_start;    // int32 [N + 1]: first segment of each sequence
-    size_t off_seg_sum;      // per (segment, head), 128 KB: S~^T [128][128] fp32, then M^T as bf16 high and
-                             // low operand images (32 KB each)
-    size_t off_seg_in;       // per (segment, head): entering state S^T [128][128], fp32
+    size_t off_seg_sum;      // per (segment, head), 128 KB: S~ [128][128] fp32 (lane-major), then M as bf16
+                             // high and low operand images (32 KB each)
+    size_t off_seg_in;       // per (segment, head): entering state S [128][128] fp32 (lane-major)
     size_t total_bytes;
 };
 

@@ -108,6 +108,19 @@ __device__ __forceinline__ void mma_bf16_mnk(uint32_t d_tmem, uint32_t a_base, u
                  (accumulate || s > 0) ? 1u : 0u);
 }
 
+// Full product over K = 16 * ksteps with both operands MN-major (K-step s starts 2048 bytes further in
+// each; groups along M / N a_lbo / b_lbo bytes apart).
+__device__ __forceinline__ void mma_bf16_mnmn(uint32_t d_tmem, uint32_t a_base, uint32_t a_lbo, uint32_t b_base,
+                                              uint32_t b_lbo, int ksteps, uint32_t idesc, bool accumulate) {
+    const uint64_t da = desc_sw128_mn(a_base, a_lbo), db = desc_sw128_mn(b_base, b_lbo);
+#pragma unroll
+    for (int s = 0; s < ksteps; ++s)
+        mma_bf16(d_tmem, da + (uint64_t)((2048 * s) >> 4), db + (uint64_t)((2048 * s) >> 4), idesc,
+                 (accumulate || s > 0) ? 1u : 0u);
+}
+// 32 consecutive fp32 columns into TMEM.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v);
+
 // 32 / 64 consecutive fp32 columns of this thread's TMEM lane in one load.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
     uint32_t r[32];
@@ -176,6 +189,10 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
            "r"(__float_as_uint(v[15]))
         : "memory");
 }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+    tmem_st16(taddr, v);
+    tmem_st16(taddr + 16, v + 16);
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // TMEM address of (lane, column) relative to an allocation base.
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int lane, int col) {
@@ -217,6 +234,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     }
 }
 
+// Non-blocking test of a phase; mbar_wait_spin polls it (no suspension between polls), for waits on
+// the critical path of a recurrence where the wake-up delay of a suspended try_wait would show.  Also
+// gives up after ~1 s.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 256; ++i)
+            if (mbar_test_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > 1000000000ull) return false;
+    }
+}
+
 // ---------------------------------------------------------------- bulk copies (1-D, 16-byte granules)
 __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -229,6 +266,16 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, in
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
         :: "r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2),
            "r"(smem_u32(bar)) : "memory");
+}
+// Tiled TMA store of one box of a 3-D tensor map from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const void *tmap, const void *smem_src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+// Prefetch of a global range into L2 (size a multiple of 16 bytes).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(gsrc), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void bulk_s2g(void *gdst, const void *smem_src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"

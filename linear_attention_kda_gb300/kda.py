@@ -26,7 +26,8 @@ _STATUS = {
 }
 EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step",
             "kda_status_string", "kda_get_device_error", "kda_abi_version",
-            "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws"]
+            "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws",
+            "kda_last_cuda_error"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 _vp = ctypes.c_void_p
@@ -94,6 +95,8 @@ def load_library(path: Optional[str] = None):
         L.kda_chunk_fwd_kernel_count.restype = _i32
         L.kda_chunk_fwd_static_ws.argtypes = [ctypes.POINTER(ChunkArgs), _vp]
         L.kda_chunk_fwd_static_ws.restype = ctypes.c_int
+        L.kda_last_cuda_error.argtypes = []
+        L.kda_last_cuda_error.restype = _i32
         _lib = L
         return L
 
@@ -116,6 +119,8 @@ def _stream(t: torch.Tensor):
 
 def _check(code: int, where: str):
     if code != 0:
+        if code == 6 and _lib is not None:  # KDA_ERR_CUDA
+            where = f"{where} (cudaError_t {int(_lib.kda_last_cuda_error())})"
         raise KDAError(code, where)
 
 
