@@ -362,10 +362,10 @@ def run_ours(args, rank, ws, local):
     by = prefill_bytes(T, N, H, D, D, 2, False, True)
     tflops = fl["total"] / (ms / 1e3) / 1e12
     kern_avg = [sum(x) / len(x) for x in kern_ms]
-    names = (["chunk_plan", "chunk_intra", "chunk_inter"] if nk == 3 else
-             ["chunk_plan", "chunk_intra", "chunk_segsum", "chunk_fold", "chunk_inter"])
+    names = {2: ["chunk_plan", "chunk_fused"], 3: ["chunk_plan", "chunk_intra", "chunk_inter"],
+             5: ["chunk_plan", "chunk_intra", "chunk_segsum", "chunk_fold", "chunk_inter"]}[nk]
     dom = max(range(nk), key=lambda j: kern_avg[j])
-    role = {"chunk_intra": "intra"}.get(names[dom], "inter")
+    role = {"chunk_intra": "intra", "chunk_fused": "total"}.get(names[dom], "inter")
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     tc = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     bytes_dom, flops_dom = by[role], fl[role]

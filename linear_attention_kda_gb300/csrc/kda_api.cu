@@ -81,7 +81,9 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
     if (!kda_make_chunk_plan(a->T, a->N > 0 ? a->N : 1, a->H > 0 ? a->H : 1, a->dk, a->dv, a->dtype, 64, &p,
                              a->cu_seqlens_host))
         return 0;
-    // chunk plan, intra-chunk transform, [segment summaries, fold,] state/output pass
+    // chunk plan, then either one fused launch (intra-chunk transform and output pass together) or
+    // intra-chunk transform, [segment summaries, fold,] output pass
+    if (p.fused) return 2;
     return p.split ? 5 : 3;
 }
 

@@ -10,6 +10,8 @@
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
+#include <cmath>
+
 namespace kda {
 
 __global__ void __launch_bounds__(1024)
@@ -115,12 +117,23 @@ chunk_plan_kernel(const int32_t *__restrict__ cu, int64_t T, int N, int C,
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Segment length of the split-sequence state pass, from a latency model of the tensor-core
-// kernels: a chain step costs t, a summary step 1.3 t (two states), a fold step ~1 t; one CTA per
-// SM.  Candidate lengths are compared with the unsplit pass; splitting is used only if it wins by
-// more than 15 %.  Uses per-sequence lengths when the host copy of cu_seqlens is given.
-static int64_t choose_seg_len(int64_t T, int64_t N, int H, int C, const int32_t *cu_host, int sms) {
-    if (T == 0) return 1 << 30;
+// Schedule of the tensor-core path, from a latency model of its kernels (microseconds): an
+// intra-chunk item costs T_ITEM on one SM; a chain step of the output pass T_STEP, a summary step
+// 1.3 T_STEP, a fold step ~T_STEP; one CTA per SM; T_LAUNCH per kernel boundary.  Three schedules:
+//  - separate kernels, one segment per sequence;
+//  - separate kernels with the split-sequence state pass (segments of L chunks);
+//  - fused: chains (one per sequence and head) and intra-chunk producers share one launch.
+// Uses per-sequence lengths when the host copy of cu_seqlens is given.
+constexpr double T_ITEM = 6.0, T_STEP = 1.8, T_LAUNCH = 4.0;
+
+struct tc_schedule {
+    int64_t seg_len;  // 1 << 30: no split
+    bool fused;
+};
+
+static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int32_t *cu_host, int sms) {
+    tc_schedule r{(int64_t)1 << 30, false};
+    if (T == 0) return r;
     int64_t total = 0, longest = 0;
     auto chunks_of = [&](int64_t n) -> int64_t {
         const int64_t len = cu_host ? (int64_t)cu_host[n + 1] - cu_host[n] : T / N;
@@ -132,10 +145,11 @@ static int64_t choose_seg_len(int64_t T, int64_t N, int H, int C, const int32_t 
         longest = c > longest ? c : longest;
     }
     auto waves = [&](int64_t ctas) { return (double)((ctas + sms - 1) / sms); };
-    const double unsplit = (double)longest > (double)total * H / sms ? (double)longest
-                                                                      : (double)total * H / sms;
-    double best = unsplit * 0.85;
-    int64_t best_len = 1 << 30;
+    const double items = (double)total * H;
+    const double intra = waves((int64_t)items) * T_ITEM;
+    // unsplit output pass: the longest chain, or the chains' total over the SMs
+    const double unsplit = (double)longest > items / sms ? (double)longest : items / sms;
+    double best = intra + unsplit * T_STEP + 2 * T_LAUNCH;
     for (int64_t L = 8; L <= (1 << 14); L *= 2) {
         if (L >= longest) break;
         int64_t segs = 0, segs_sum = 0, max_nseg = 0;
@@ -146,13 +160,26 @@ static int64_t choose_seg_len(int64_t T, int64_t N, int H, int C, const int32_t 
             segs_sum += ns - 1;
             max_nseg = ns > max_nseg ? ns : max_nseg;
         }
-        const double cost = 1.3 * L * waves(segs_sum * H) + 1.0 * (max_nseg - 1) + L * waves(segs * H) + 8.0;
-        if (cost < best) {
+        const double steps = 1.3 * L * waves(segs_sum * H) + 1.0 * (max_nseg - 1) + L * waves(segs * H);
+        const double cost = intra + steps * T_STEP + 4 * T_LAUNCH;
+        if (cost < 0.85 * best) {  // split only for a clear gain
             best = cost;
-            best_len = L;
+            r.seg_len = L;
         }
     }
-    return best_len;
+    const int64_t n_chain = N * H;
+    if (n_chain + 16 <= sms) {
+        const double producers = (double)(sms - n_chain);
+        const double fused = (items / producers > (double)longest * T_STEP / T_ITEM
+                                  ? std::ceil(items / producers) * T_ITEM
+                                  : (double)longest * T_STEP) +
+                             T_ITEM + T_LAUNCH;
+        if (fused < best) {
+            r.fused = true;
+            r.seg_len = (int64_t)1 << 30;
+        }
+    }
+    return r;
 }
 
 bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_t dtype, int C,
@@ -172,13 +199,16 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
     p->off_records = align_up(sizeof(int32_t) * (size_t)(N + 1), 256);
     size_t end = p->off_records + p->record_bytes * (size_t)p->max_chunks * (size_t)H;
     p->split = 0;
+    p->fused = 0;
     p->seg_len = (int64_t)1 << 30;
     p->max_segs = N;
     if (p->path == 1) {
         int dev = 0, sms = 152;
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 152;
-        p->seg_len = choose_seg_len(T, N, H, C, cu_seqlens_host, sms);
+        const tc_schedule sch = choose_schedule(T, N, H, C, cu_seqlens_host, sms);
+        p->seg_len = sch.seg_len;
+        p->fused = sch.fused ? 1 : 0;
         p->split = p->seg_len < ((int64_t)1 << 30) ? 1 : 0;
         p->max_segs = p->split ? p->max_chunks / p->seg_len + N : N;
     }
@@ -190,6 +220,8 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
         p->off_seg_in = p->off_seg_sum + (size_t)p->max_segs * H * 2 * 128 * 128 * sizeof(float);
         end = p->off_seg_in + (size_t)p->max_segs * H * 128 * 128 * sizeof(float);
     }
+    p->off_flags = align_up(end, 256);
+    end = p->off_flags + sizeof(int32_t) * (size_t)p->max_chunks * (size_t)H;
     p->total_bytes = align_up(end, 256);
     return true;
 }

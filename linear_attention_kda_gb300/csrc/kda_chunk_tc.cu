@@ -46,15 +46,11 @@ constexpr uint32_t PK_G = 73728;      // gamma^C fp32 [128]
 constexpr uint32_t PK_STRIDE = 75776; // multiple of 1024
 
 // inter kernel shared memory
-// Output pass: two packet stages hold the MMA operands of a chunk ([W; Q^], K~, A) and gamma (the
-// packet after them is prefetched into L2); U is read by the CUDA cores from global memory into
-// registers, one chunk ahead.
-constexpr uint32_t CS_NST = 2;
-constexpr uint32_t CS_PK_MMA = PK_A + 8192;            // bytes [0, PK_A + 8 KB) of a packet
-constexpr uint32_t CS_G = CS_PK_MMA;                   // gamma inside a stage
-constexpr uint32_t CS_ST_TX = CS_PK_MMA + 512;
-constexpr uint32_t CS_ST_BYTES = 58368;                // stage stride (multiple of 1024)
-constexpr uint32_t CS_SIMG = CS_NST * CS_ST_BYTES;     // S image, 128 rows (d_k) x 128 (d_v), 2 x 16 KB
+// Output pass: two stages hold whole packets (one bulk copy each); the packet after them is
+// prefetched into L2.
+constexpr uint32_t CS_ST_TX = PK_G + 512;              // packet bytes
+constexpr uint32_t CS_ST_BYTES = PK_STRIDE;            // stage stride (multiple of 1024)
+constexpr uint32_t CS_SIMG = 2 * CS_ST_BYTES;          // S image, 128 rows (d_k) x 128 (d_v), 2 x 16 KB
 constexpr uint32_t CS_VIMG = CS_SIMG + 32768;          // V~ image, 64 tokens x 128 (d_v), 2 x 8 KB
 constexpr uint32_t CS_OIMG = CS_VIMG + 16384;          // o staging, 64 tokens x 128, 2 x 8 KB
 constexpr uint32_t CS_BAR = CS_OIMG + 16384;           // 14 mbarriers
@@ -317,17 +313,40 @@ __device__ __forceinline__ void element_pass(unsigned char *sm, unsigned char *s
     }
 }
 
-__global__ void __launch_bounds__(NT2, 1)
-chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restrict__ beta,
-                      const float *__restrict__ bias, const float *__restrict__ A_log, float g_min,
-                      int64_t T, int N, const int32_t *__restrict__ cu,
-                      const int32_t *__restrict__ chunk_start, int H, unsigned char *__restrict__ packets,
-                      int *err) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = align1024(smem_raw);
+// Packet publication between CTAs of one (cooperative) launch: the producer releases a flag once the
+// packet's bulk writes have completed; the consumer acquires it before its bulk reads.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ void flag_release(int *f) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" :: "l"(f), "r"(1) : "memory");
+}
+__device__ __forceinline__ int flag_acquire(const int *f) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+// Bounded wait (~1 s) for a packet flag.
+__device__ __forceinline__ bool flag_wait(const int *f) {
+    if (flag_acquire(f)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (flag_acquire(f)) return true;
+        if (globaltimer_ns() - t0 > 1000000000ull) return false;
+    }
+}
+
+// The intra-chunk work of one CTA: worker `worker` of `nworkers` takes items worker, worker +
+// nworkers, ...  With `flags`, each item's packet is published (flags[item] = 1) once its writes
+// have completed.
+__device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm, const bf16 *__restrict__ beta,
+                                           const float *__restrict__ bias, const float *__restrict__ A_log,
+                                           float g_min, int64_t T, int N, const int32_t *__restrict__ cu,
+                                           const int32_t *__restrict__ chunk_start, int H,
+                                           unsigned char *__restrict__ packets, int *err, int worker, int nworkers,
+                                           int *flags) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t W = (int64_t)chunk_start[N] * H;  // work items
-    if ((int64_t)blockIdx.x >= W) return;
+    if ((int64_t)worker >= W) return;
     float *Gs = (float *)(sm + J_G);
     uint64_t *bar_ld = (uint64_t *)(sm + J_BAR);
     uint64_t *bar_free = bar_ld + 2;
@@ -350,7 +369,7 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
         // ------------------------------------------------ producer warp
         bool ok = true;
         for (int it = 0;; ++it) {
-            const int64_t w = (int64_t)blockIdx.x + (int64_t)it * gridDim.x;
+            const int64_t w = (int64_t)worker + (int64_t)it * nworkers;
             if (w >= W) break;
             const int s = it & 1;
             if (it >= 2) {
@@ -396,7 +415,7 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
         bool ok = true;
         int it = 0;
         for (;; ++it) {
-            const int64_t w = (int64_t)blockIdx.x + (int64_t)it * gridDim.x;
+            const int64_t w = (int64_t)worker + (int64_t)it * nworkers;
             if (w >= W) break;
             const int s = it & 1;
             ok = cwait(&bar_ld[s], (it >> 1) & 1);
@@ -444,6 +463,11 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
                     mbar_arrive(&bar_free[s ^ 1]);
                 }
                 csync();
+            }
+            if (flags && tid == 0 && it > 0) {  // the previous item's packet is complete: publish it
+                bulk_wait0();
+                fence_proxy_async_global();
+                flag_release(flags + (w - nworkers));
             }
             // ---- G2: element pass, thread = (channels c0..c0+3, tokens tg + 8 i, one chunk half)
             {
@@ -671,10 +695,25 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
             }
         }
         if (tid == 0) bulk_wait0();
+        if (flags && ok && tid == 0 && it > 0) {  // the last item's packet
+            fence_proxy_async_global();
+            flag_release(flags + ((int64_t)worker + (int64_t)(it - 1) * nworkers));
+        }
         if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 256);
+}
+
+__global__ void __launch_bounds__(NT2, 1)
+chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restrict__ beta,
+                      const float *__restrict__ bias, const float *__restrict__ A_log, float g_min,
+                      int64_t T, int N, const int32_t *__restrict__ cu,
+                      const int32_t *__restrict__ chunk_start, int H, unsigned char *__restrict__ packets,
+                      int *err) {
+    extern __shared__ unsigned char smem_raw[];
+    intra_role(align1024(smem_raw), tm, beta, bias, A_log, g_min, T, N, cu, chunk_start, H, packets, err,
+               (int)blockIdx.x, (int)gridDim.x, nullptr);
 }
 
 constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 10, 11, 14, 15: output; 9, 12, 13 idle
@@ -692,16 +731,16 @@ constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 10, 11, 14, 15
 // The recurrence never waits for the outputs: the output warps (the four that reach TMEM lanes
 // 64-127) read O of chunk k once its MMAs are done, release the D buffer (double buffered), refill
 // the packet stage and store o through a staging tile and TMA.
-__global__ void __launch_bounds__(NT3, 1)
-chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N, const int32_t *__restrict__ cu,
-                      const int32_t *__restrict__ chunk_start, const int32_t *__restrict__ seg_start,
-                      int64_t seg_len, const float *__restrict__ seg_in, int H,
-                      const unsigned char *__restrict__ packets, float scale, const float *initial_state,
-                      float *final_state, bf16 *__restrict__ o, int *err) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = align1024(smem_raw);
+// The output pass of segment g, head h in one CTA (threads 0-511).  With `flags`, a packet is loaded
+// only after its producer has published it.
+__device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap &omap, int64_t T, int N,
+                                           const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
+                                           const int32_t *__restrict__ seg_start, int64_t seg_len,
+                                           const float *__restrict__ seg_in, int H,
+                                           const unsigned char *__restrict__ packets, float scale,
+                                           const float *initial_state, float *final_state, bf16 *__restrict__ o,
+                                           int *err, int g, int h, const int *flags) {
     // segment g of sequence n, head h: chunks [kk0, kk0 + nc) of the sequence
-    const int g = blockIdx.x, h = blockIdx.y;
     if (g >= seg_start[N]) return;
     int n = 0;
     {
@@ -758,15 +797,20 @@ chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N
     auto tDbuf = [&](int kk) { return tb + 128 + 128 * (uint32_t)(kk & 1); };
     auto packet = [&](int kk) { return packets + ((size_t)(c_begin + kk) * H + h) * PK_STRIDE; };
     auto stage = [&](int kk) { return sm + (kk & 1) * CS_ST_BYTES; };
-    auto load_stage = [&](int kk) {
+    auto load_stage = [&](int kk) {  // returns false if the packet was never published
+        if (flags) {
+            if (!flag_wait(flags + ((size_t)(c_begin + kk) * H + h))) return false;
+            fence_proxy_async_global();
+        }
         uint64_t *b = &bar_ld[kk & 1];
         mbar_arrive_expect_tx(b, CS_ST_TX);
-        bulk_g2s(stage(kk), packet(kk), CS_PK_MMA, b);
-        bulk_g2s(stage(kk) + CS_G, packet(kk) + PK_G, 512, b);
+        bulk_g2s(stage(kk), packet(kk), CS_ST_TX, b);
+        return true;
     };
     if (tid == 0) {
-        for (int kk = 0; kk < 2 && kk < nc; ++kk) load_stage(kk);
-        if (nc > 2) bulk_prefetch_l2(packet(2), PK_G + 512);
+        for (int kk = 0; kk < 2 && kk < nc; ++kk)
+            if (!load_stage(kk)) atomicExch(s_fail, 1);
+        if (nc > 2 && !flags) bulk_prefetch_l2(packet(2), CS_ST_TX);
     }
 
     if (warp == 8) {
@@ -812,8 +856,8 @@ chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N
             if (!ok) break;
             fence_after_sync();
             if (ot == 0) {  // all MMAs of chunk kk are done: its stage takes chunk kk + 2
-                if (kk + 2 < nc) load_stage(kk + 2);
-                if (kk + 3 < nc) bulk_prefetch_l2(packet(kk + 3), PK_G + 512);
+                if (kk + 2 < nc && !load_stage(kk + 2)) atomicExch(s_fail, 1);
+                if (kk + 3 < nc && !flags) bulk_prefetch_l2(packet(kk + 3), CS_ST_TX);
             }
             const int64_t tp = s_tok + (int64_t)kk * C;
             const int lenp = (int)min((int64_t)C, e_tok - tp);
@@ -883,7 +927,7 @@ chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj)
                     *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, row, 8 * cg + jj)) = pack8(x + 8 * jj);
-                const float gr = reinterpret_cast<const float *>(stage(0) + CS_G)[row];
+                const float gr = reinterpret_cast<const float *>(stage(0) + PK_G)[row];
 #pragma unroll
                 for (int e = 0; e < 64; ++e) x[e] *= gr;
                 tmem_st32(tmem_addr(tS, 32 * lq, 64 * cg), x);
@@ -895,15 +939,6 @@ chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N
         fence_before_sync();
         named_sync(nbar, 128);
         if (ht == 0 && nc > 0) mbar_arrive(&bar_simg[cg]);
-        // U row `row` (a token; lane quarters 0, 1), columns [64 cg, 64 cg + 64), one chunk ahead
-        auto load_u = [&](int kk, uint4 *u4) {
-            const unsigned char *src = packet(kk) + PK_U;
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-                u4[jj] = __ldg(reinterpret_cast<const uint4 *>(src + img_chunk_off(64, row, 8 * cg + jj)));
-        };
-        uint4 ua[8];
-        if (lq < 2 && nc > 0) load_u(0, ua);
         for (int kk = 0; kk < nc && ok; ++kk) {
             // invariant: packet kk resident; S image = bf16(S_kk); TMEM S = Diag(gamma_kk) S_kk
             if (ht == 0) ok = mbar_wait_spin(&bar_v[cg], kk & 1);  // one thread polls, the barrier releases
@@ -917,14 +952,15 @@ chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N
                     tmem_ld32(tmem_addr(tDbuf(kk), 32 * lq, 64 * cg + 32 * h2), dv);
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
-                        unpack8(ua[4 * h2 + jj], u);
+                        unpack8(*reinterpret_cast<const uint4 *>(stage(kk) + PK_U +
+                                                                 img_chunk_off(64, row, 8 * cg + 4 * h2 + jj)),
+                                u);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) vo[e] = u[e] - dv[8 * jj + e];
                         *reinterpret_cast<uint4 *>(sm + CS_VIMG + img_chunk_off(64, row, 8 * cg + 4 * h2 + jj)) =
                             pack8(vo);
                     }
                 }
-                if (kk + 1 < nc) load_u(kk + 1, ua);
             }
             fence_proxy_async();
             fence_before_sync();
@@ -939,7 +975,7 @@ chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N
             if (!ok) break;
             fence_after_sync();
             // S_{kk+1}: bf16 image and TMEM copy scaled by gamma_{kk+1}; or the final state
-            const float gr = last ? 1.f : reinterpret_cast<const float *>(stage(kk + 1) + CS_G)[row];
+            const float gr = last ? 1.f : reinterpret_cast<const float *>(stage(kk + 1) + PK_G)[row];
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 float x[32];
@@ -972,6 +1008,41 @@ chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N
     if (tid == 0 && *(volatile int *)s_fail) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     sync_all();
     if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+__global__ void __launch_bounds__(NT3, 1)
+chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N, const int32_t *__restrict__ cu,
+                      const int32_t *__restrict__ chunk_start, const int32_t *__restrict__ seg_start,
+                      int64_t seg_len, const float *__restrict__ seg_in, int H,
+                      const unsigned char *__restrict__ packets, float scale, const float *initial_state,
+                      float *final_state, bf16 *__restrict__ o, int *err) {
+    extern __shared__ unsigned char smem_raw[];
+    chain_role(align1024(smem_raw), omap, T, N, cu, chunk_start, seg_start, seg_len, seg_in, H, packets, scale,
+               initial_state, final_state, o, err, (int)blockIdx.x, (int)blockIdx.y, nullptr);
+}
+
+// =====================================================================================
+// Intra-chunk work and the output pass in one launch, for inputs whose chains (one per sequence and
+// head) are few: CTAs [0, n_chain) run the chains (no segment split), the others produce packets in
+// chunk order and publish them through `flags`; a chain waits for each packet before loading it.
+// Launched cooperatively, so every CTA is resident and the producers always make progress; every
+// wait is bounded.
+__global__ void __launch_bounds__(NT2, 1)
+chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant__ CUtensorMap omap,
+                      const bf16 *__restrict__ beta, const float *__restrict__ bias, const float *__restrict__ A_log,
+                      float g_min, int64_t T, int N, const int32_t *__restrict__ cu,
+                      const int32_t *__restrict__ chunk_start, const int32_t *__restrict__ seg_start, int H,
+                      unsigned char *__restrict__ packets, float scale, const float *initial_state,
+                      float *final_state, bf16 *__restrict__ o, int *err, int n_chain, int *flags) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = align1024(smem_raw);
+    const int b = (int)blockIdx.x;
+    if (b < n_chain)
+        chain_role(sm, omap, T, N, cu, chunk_start, seg_start, (int64_t)1 << 30, nullptr, H, packets, scale,
+                   initial_state, final_state, o, err, b / H, b % H, flags);
+    else
+        intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, chunk_start, H, packets, err, b - n_chain,
+                   (int)gridDim.x - n_chain, flags);
 }
 
 // =====================================================================================
@@ -1365,6 +1436,45 @@ static bool make_tile_map(CUtensorMap *m, const void *base, int64_t T, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+static kda_status_t set_smem(const void *kernel, uint32_t bytes) {
+    return kda_cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
+}
+
+// The fused schedule: one cooperative launch of chains + producers.  Returns false (and clears the
+// launch error) when the device refuses to make every CTA resident; the caller then runs the
+// separate kernels, which need the same workspace.
+static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws, cudaStream_t stream,
+                         const tcp::TileMaps &tm, const CUtensorMap &omap, int sms, int *err) {
+    const uint32_t smem = tcp::J_TOTAL > tcp::CS_TOTAL ? tcp::J_TOTAL : tcp::CS_TOTAL;
+    if (set_smem((const void *)tcp::chunk_fused_tc_kernel, smem) != KDA_OK) return false;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tcp::chunk_fused_tc_kernel, tcp::NT2, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+        return false;
+    int *flags = (int *)((char *)ws + p.off_flags);
+    if (cudaMemsetAsync(flags, 0, sizeof(int) * (size_t)p.max_chunks * p.H, stream) != cudaSuccess) return false;
+    const int32_t *chunk_start = (const int32_t *)((char *)ws + p.off_chunk_start);
+    const int32_t *seg_start = (const int32_t *)((char *)ws + p.off_seg_start);
+    unsigned char *packets = (unsigned char *)ws + p.off_records;
+    const bf16 *beta = (const bf16 *)a->beta;
+    const float *bias = a->dt_bias, *A_log = a->A_log, *init = a->initial_state;
+    float g_min = a->g_min, scale = a->scale;
+    int64_t T = a->T;
+    int N = (int)a->N, H = p.H, n_chain = (int)(a->N * p.H);
+    const int32_t *cu = a->cu_seqlens;
+    float *fin = a->final_state;
+    bf16 *o = (bf16 *)a->o;
+    void *args[] = {(void *)&tm, (void *)&omap, &beta, &bias, &A_log, &g_min, &T, &N, &cu, &chunk_start,
+                    &seg_start, &H, &packets, &scale, &init, &fin, &o, &err, &n_chain, &flags};
+    if (cudaLaunchCooperativeKernel((const void *)tcp::chunk_fused_tc_kernel, dim3((unsigned)sms), dim3(tcp::NT2),
+                                    args, smem, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
 kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
                                  cudaStream_t stream) {
     int *err = kda_device_error_ptr();
@@ -1375,28 +1485,29 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     kda_profile_mark(1, stream);
     const int32_t *chunk_start = (const int32_t *)((char *)ws + p.off_chunk_start);
     unsigned char *packets = (unsigned char *)ws + p.off_records;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    tcp::TileMaps tm;
+    CUtensorMap omap;
+    if (!make_tile_map(&tm.q, a->q, a->T, p.H) || !make_tile_map(&tm.k, a->k, a->T, p.H) ||
+        !make_tile_map(&tm.v, a->v, a->T, p.H) || !make_tile_map(&tm.z, a->z, a->T, p.H) ||
+        !make_tile_map(&omap, a->o, a->T, p.H))
+        return KDA_ERR_CUDA;
+    if (p.fused && p.max_chunks > 0 && a->T > 0 && launch_fused(a, p, ws, stream, tm, omap, sms, err)) {
+        kda_profile_mark(2, stream);
+        return kda_cuda_status(cudaGetLastError());
+    }
     if (p.max_chunks > 0 && a->T > 0) {
-        {
-            const kda_status_t cst = kda_cuda_status(cudaFuncSetAttribute(tcp::chunk_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                                          (int)tcp::J_TOTAL));
-            if (cst != KDA_OK) return cst;
-        }
-        int dev = 0, sms = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        st = set_smem((const void *)tcp::chunk_intra_tc_kernel, tcp::J_TOTAL);
+        if (st != KDA_OK) return st;
         const int64_t items = p.max_chunks * (int64_t)p.H;
         const unsigned grid = (unsigned)(items < sms ? items : sms);
-        tcp::TileMaps tm;
-        if (!make_tile_map(&tm.q, a->q, a->T, p.H) || !make_tile_map(&tm.k, a->k, a->T, p.H) ||
-            !make_tile_map(&tm.v, a->v, a->T, p.H) || !make_tile_map(&tm.z, a->z, a->T, p.H))
-            return KDA_ERR_CUDA;
         tcp::chunk_intra_tc_kernel<<<grid, tcp::NT2, tcp::J_TOTAL, stream>>>(
             tm, (const bf16 *)a->beta, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
             chunk_start, p.H, packets, err);
-        {
-            const kda_status_t cst = kda_cuda_status(cudaGetLastError());
-            if (cst != KDA_OK) return cst;
-        }
+        st = kda_cuda_status(cudaGetLastError());
+        if (st != KDA_OK) return st;
     }
     kda_profile_mark(2, stream);
     const int32_t *seg_start = (const int32_t *)((char *)ws + p.off_seg_start);
@@ -1404,38 +1515,23 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     float *seg_in = (float *)((char *)ws + p.off_seg_in);
     int mark = 3;
     if (p.split) {
-        {
-            const kda_status_t cst = kda_cuda_status(cudaFuncSetAttribute(tcp::chunk_segsum_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                                          (int)tcp::SS_TOTAL));
-            if (cst != KDA_OK) return cst;
-        }
+        st = set_smem((const void *)tcp::chunk_segsum_tc_kernel, tcp::SS_TOTAL);
+        if (st != KDA_OK) return st;
         tcp::chunk_segsum_tc_kernel<<<dim3((unsigned)p.max_segs, (unsigned)p.H), 512, tcp::SS_TOTAL, stream>>>(
             (int)a->N, chunk_start, seg_start, p.seg_len, p.H, packets, seg_sum, err);
-        {
-            const kda_status_t cst = kda_cuda_status(cudaGetLastError());
-            if (cst != KDA_OK) return cst;
-        }
+        st = kda_cuda_status(cudaGetLastError());
+        if (st != KDA_OK) return st;
         kda_profile_mark(mark++, stream);
-        {
-            const kda_status_t cst = kda_cuda_status(cudaFuncSetAttribute(tcp::chunk_fold_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                                          (int)tcp::FD_TOTAL));
-            if (cst != KDA_OK) return cst;
-        }
+        st = set_smem((const void *)tcp::chunk_fold_tc_kernel, tcp::FD_TOTAL);
+        if (st != KDA_OK) return st;
         tcp::chunk_fold_tc_kernel<<<dim3((unsigned)a->N, (unsigned)p.H), 256, tcp::FD_TOTAL, stream>>>(
             (int)a->N, seg_start, p.H, a->initial_state, seg_sum, seg_in, err);
-        {
-            const kda_status_t cst = kda_cuda_status(cudaGetLastError());
-            if (cst != KDA_OK) return cst;
-        }
+        st = kda_cuda_status(cudaGetLastError());
+        if (st != KDA_OK) return st;
         kda_profile_mark(mark++, stream);
     }
-    {
-        const kda_status_t cst = kda_cuda_status(cudaFuncSetAttribute(tcp::chunk_inter_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                                      (int)tcp::CS_TOTAL));
-        if (cst != KDA_OK) return cst;
-    }
-    CUtensorMap omap;
-    if (!make_tile_map(&omap, a->o, a->T, p.H)) return KDA_ERR_CUDA;
+    st = set_smem((const void *)tcp::chunk_inter_tc_kernel, tcp::CS_TOTAL);
+    if (st != KDA_OK) return st;
     tcp::chunk_inter_tc_kernel<<<dim3((unsigned)p.max_segs, (unsigned)p.H), tcp::NT3, tcp::CS_TOTAL, stream>>>(
         omap, a->T, (int)a->N, a->cu_seqlens, chunk_start, seg_start, p.seg_len, seg_in, p.H, packets, a->scale,
         a->initial_state, a->final_state, (bf16 *)a->o, err);

@@ -33,6 +33,11 @@ struct kda_chunk_plan {
     size_t off_seg_sum;      // per (segment, head), 128 KB: S~ [128][128] fp32 (lane-major), then M as bf16
                              // high and low operand images (32 KB each)
     size_t off_seg_in;       // per (segment, head): entering state S [128][128] fp32 (lane-major)
+    // Fused launch (tensor-core path, no split): the output pass of every (sequence, head) and the
+    // intra-chunk work run concurrently in one cooperative launch; packets are published through
+    // int32 flags, one per (chunk slot, head).
+    int fused;
+    size_t off_flags;
     size_t total_bytes;
 };
 
