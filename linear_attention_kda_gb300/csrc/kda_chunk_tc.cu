@@ -187,9 +187,9 @@ constexpr uint32_t J_QTOT = J_GAM + 512;    // G at tokens 15, 31, 47: fp32 [3][
 constexpr uint32_t J_BETA = J_QTOT + 2048;  // 2 stages x fp32 [64]
 constexpr uint32_t J_BIAS = J_BETA + 512;   // 2 stages x fp32 [128]
 constexpr uint32_t J_INFO = J_BIAS + 1024;  // 2 stages x {int64 t0, len, h, slot; float eA}
-constexpr uint32_t J_BAR = J_INFO + 128;    // ld[2], free[2], mma
-constexpr uint32_t J_TSLOT = J_BAR + 48;
-constexpr uint32_t J_TOTAL = J_BAR + 64 + 1024;
+constexpr uint32_t J_BAR = J_INFO + 128;    // ld[2], pq[2], pw[2], mma, rd
+constexpr uint32_t J_TSLOT = J_BAR + 64;
+constexpr uint32_t J_TOTAL = J_BAR + 128 + 1024;
 // TMEM columns: A / L product (96); later [W | U] (256, lanes 0-63)
 constexpr uint32_t TM_DA = 0, TM_DB = 32, TM_DWU = 0;
 
@@ -348,17 +348,21 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
     const int64_t W = (int64_t)chunk_start[N] * H;  // work items
     if ((int64_t)worker >= W) return;
     float *Gs = (float *)(sm + J_G);
-    uint64_t *bar_ld = (uint64_t *)(sm + J_BAR);
-    uint64_t *bar_free = bar_ld + 2;
-    uint64_t *bar_mma = bar_ld + 4;
+    uint64_t *bar_ld = (uint64_t *)(sm + J_BAR);  // [2] stage loaded
+    uint64_t *bar_pq = bar_ld + 2;                // [2] Q^ and K~ tiles of the stage's item written
+    uint64_t *bar_pw = bar_ld + 4;                // [2] rest of the item's packet written (item done)
+    uint64_t *bar_rd = bar_ld + 7;                // the packet copies of the last item have read shared memory
+    uint64_t *bar_mma = bar_ld + 6;
     uint32_t *tslot = (uint32_t *)(sm + J_TSLOT);
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_ld[i], 1);
-            mbar_init(&bar_free[i], 1);
+            mbar_init(&bar_pq[i], 1);
+            mbar_init(&bar_pw[i], 1);
         }
         mbar_init(bar_mma, 1);
+        mbar_init(bar_rd, 1);
     }
     if (warp == 0) tmem_alloc(tslot, 256);
     fence_proxy_async();
@@ -366,16 +370,12 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
     const uint32_t tb = *tslot;
 
     if (warp == PRODUCER) {
-        // ------------------------------------------------ producer warp
-        bool ok = true;
-        for (int it = 0;; ++it) {
+        // ------------------------------------------------ producer warp: loads items into the two stages and
+        // writes their packets (bulk copies from shared memory), publishing each through `flags` once its
+        // writes have completed; a stage is refilled as soon as the copies of its item have read it.
+        auto load_item = [&](int it) {
             const int64_t w = (int64_t)worker + (int64_t)it * nworkers;
-            if (w >= W) break;
             const int s = it & 1;
-            if (it >= 2) {
-                ok = mbar_wait(&bar_free[s], ((it >> 1) - 1) & 1);
-                if (!__all_sync(0xffffffffu, ok)) break;
-            }
             const int64_t slot = w / H;
             const int h = (int)(w % H);
             int n = 0, len = 0;
@@ -407,6 +407,45 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
                     tma_load_3d(stg + 16384 * x + 8192, maps[x], 64, h, (int)t0, &bar_ld[s]);
                 }
             }
+        };
+        const int n_items = (int)((W - worker + nworkers - 1) / nworkers);
+        if (n_items > 0) load_item(0);
+        if (n_items > 1) load_item(1);
+        bool ok = true;
+        for (int it = 0; it < n_items && ok; ++it) {
+            const int s = it & 1;
+            const int64_t w = (int64_t)worker + (int64_t)it * nworkers;
+            unsigned char *stg = sm + s * J_STG_BYTES;
+            unsigned char *pk = packets + (size_t)w * PK_STRIDE;  // item w = slot * H + h
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_pq[s], (it >> 1) & 1));
+            if (!ok) break;
+            if (lane == 0) {
+                bulk_s2g(pk + PK_WQ + 8192, stg + J_TQ, 8192);  // Q^ rows of the [W; Q^] image
+                bulk_s2g(pk + PK_WQ + 24576, stg + J_TQ + 8192, 8192);
+                bulk_s2g(pk + PK_K, stg + J_TZ, 16384);
+                bulk_commit();
+            }
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_pw[s], (it >> 1) & 1));
+            if (!ok) break;
+            if (lane == 0) {
+                bulk_s2g(pk + PK_WQ, stg + J_TK, 8192);
+                bulk_s2g(pk + PK_WQ + 16384, stg + J_TK + 8192, 8192);
+                bulk_s2g(pk + PK_U, stg + J_TV, 16384);
+                bulk_s2g(pk + PK_A, sm + J_AIMG, 8192);
+                bulk_s2g(pk + PK_G, sm + J_GAM, 512);
+                bulk_commit();
+                bulk_wait_read0();
+                mbar_arrive(bar_rd);  // the A image and gamma may be overwritten
+            }
+            if (lane == 0) {  // publish before refilling the stage: a chain may be waiting for this packet
+                bulk_wait0();
+                if (flags) {
+                    fence_proxy_async_global();
+                    flag_release(flags + w);
+                }
+            }
+            __syncwarp();
+            if (it + 2 < n_items) load_item(it + 2);
         }
         if (!ok && lane == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     } else {
@@ -422,13 +461,10 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
             if (!ok) break;
             const int64_t *info = (const int64_t *)(sm + J_INFO + 64 * s);
             const int len = (int)info[1];
-            const int h = (int)info[2];
-            const int64_t slot = info[3];
             const float eA = *reinterpret_cast<const float *>(info + 4);
             const float *bet = (const float *)(sm + J_BETA) + 64 * s;
             const float *bia = (const float *)(sm + J_BIAS) + 128 * s;
             unsigned char *stg = sm + s * J_STG_BYTES;
-            unsigned char *pk = packets + ((size_t)slot * H + h) * PK_STRIDE;
 
             // ---- G1: gate (Eq. 5) and in-chunk cumulative log-decay (Eq. 3), thread = (channel,
             //      16-token quarter).  Tokens past the end of the sequence get g = 0 (an exact no-op).
@@ -458,17 +494,11 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
                     if (u < qt) base += qtot[u * 128 + c];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) Gs[gsw(16 * qt + i, c)] = gv[i] + base;
-                if (tid == 0 && it > 0) {  // the previous item's packet copies have read their sources
-                    bulk_wait_read0();
-                    mbar_arrive(&bar_free[s ^ 1]);
-                }
-                csync();
+                // the previous item's packet copies have read the A image and gamma buffers
+                if (tid == 0 && it > 0) ok = mbar_wait(bar_rd, (it - 1) & 1);
+                ok = csync_and(ok);
             }
-            if (flags && tid == 0 && it > 0) {  // the previous item's packet is complete: publish it
-                bulk_wait0();
-                fence_proxy_async_global();
-                flag_release(flags + (w - nworkers));
-            }
+            if (!ok) break;
             // ---- G2: element pass, thread = (channels c0..c0+3, tokens tg + 8 i, one chunk half)
             {
                 const int tg = lane & 7, cgl = lane >> 3, th = warp >> 3;
@@ -499,10 +529,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
                 mma_bf16_k(tb + TM_DA, smem_u32(sm + J_ROW), 128, smem_u32(sm + J_KEY), 96, 8, idesc_bf16(128, 96),
                            false);
                 mma_commit(bar_mma);
-                bulk_s2g(pk + PK_WQ + 8192, stg + J_TQ, 8192);           // Q^ rows of the [W; Q^] image
-                bulk_s2g(pk + PK_WQ + 24576, stg + J_TQ + 8192, 8192);
-                bulk_s2g(pk + PK_K, stg + J_TZ, 16384);
-                bulk_commit();
+                mbar_arrive(&bar_pq[s]);  // Q^ and K~ are in the stage: the producer copies them out
             }
             ok = cwait(bar_mma, mph & 1);
             ++mph;
@@ -685,19 +712,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
             }
             fence_proxy_async();
             csync();
-            if (tid == 0) {
-                bulk_s2g(pk + PK_WQ, stg + J_TK, 8192);
-                bulk_s2g(pk + PK_WQ + 16384, stg + J_TK + 8192, 8192);
-                bulk_s2g(pk + PK_U, stg + J_TV, 16384);
-                bulk_s2g(pk + PK_A, sm + J_AIMG, 8192);
-                bulk_s2g(pk + PK_G, sm + J_GAM, 512);
-                bulk_commit();
-            }
-        }
-        if (tid == 0) bulk_wait0();
-        if (flags && ok && tid == 0 && it > 0) {  // the last item's packet
-            fence_proxy_async_global();
-            flag_release(flags + ((int64_t)worker + (int64_t)(it - 1) * nworkers));
+            if (tid == 0) mbar_arrive(&bar_pw[s]);  // the item is done: the producer writes its packet
         }
         if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     }
@@ -974,33 +989,46 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
             ok = bar_red_popc(nbar, 128, ok) == 128;
             if (!ok) break;
             fence_after_sync();
-            // S_{kk+1}: bf16 image and TMEM copy scaled by gamma_{kk+1}; or the final state
-            const float gr = last ? 1.f : reinterpret_cast<const float *>(stage(kk + 1) + PK_G)[row];
+            // S_{kk+1}: bf16 image first (MMA1 of the next chunk needs it), then the TMEM copy scaled by
+            // gamma_{kk+1} (the next MMA3 needs it, and is issued only after this half's next V~ image)
+            if (!last) {
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                float x[32];
-                const int c0 = 64 * cg + 32 * h2;
-                tmem_ld32(tmem_addr(tS, 32 * lq, c0), x);
-                if (!last) {
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    float x[32];
+                    const int c0 = 64 * cg + 32 * h2;
+                    tmem_ld32(tmem_addr(tS, 32 * lq, c0), x);
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
                         *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, row, c0 / 8 + jj)) =
                             pack8(x + 8 * jj);
+                }
+                fence_proxy_async();
+                fence_before_sync();
+                named_sync(nbar, 128);
+                if (ht == 0) mbar_arrive(&bar_simg[cg]);
+                const float gr = reinterpret_cast<const float *>(stage(kk + 1) + PK_G)[row];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    float x[32];
+                    const int c0 = 64 * cg + 32 * h2;
+                    tmem_ld32(tmem_addr(tS, 32 * lq, c0), x);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[e] *= gr;
                     tmem_st32(tmem_addr(tS, 32 * lq, c0), x);
-                } else if (final_state && last_seg) {
+                }
+                tmem_st_wait();
+            } else if (final_state && last_seg) {
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    float x[32];
+                    const int c0 = 64 * cg + 32 * h2;
+                    tmem_ld32(tmem_addr(tS, 32 * lq, c0), x);
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
                         *reinterpret_cast<float4 *>(final_state + st_off + (size_t)row * D + c0 + e) =
                             make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
                 }
             }
-            if (!last) tmem_st_wait();
-            fence_proxy_async();
-            fence_before_sync();
-            named_sync(nbar, 128);
-            if (ht == 0 && !last) mbar_arrive(&bar_simg[cg]);
         }
         if (!ok) atomicExch(s_fail, 1);
     }
