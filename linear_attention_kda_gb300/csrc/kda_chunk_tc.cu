@@ -50,10 +50,9 @@ constexpr uint32_t PK_STRIDE = 75776; // multiple of 1024
 // prefetched into L2.
 constexpr uint32_t CS_ST_TX = PK_G + 512;              // packet bytes
 constexpr uint32_t CS_ST_BYTES = PK_STRIDE;            // stage stride (multiple of 1024)
-constexpr uint32_t CS_SIMG = 2 * CS_ST_BYTES;          // S image, 128 rows (d_k) x 128 (d_v), 2 x 16 KB
-constexpr uint32_t CS_VIMG = CS_SIMG + 32768;          // V~ image, 64 tokens x 128 (d_v), 2 x 8 KB
-constexpr uint32_t CS_OIMG = CS_VIMG + 16384;          // o staging, 64 tokens x 128, 2 x 8 KB
-constexpr uint32_t CS_BAR = CS_OIMG + 16384;           // 14 mbarriers
+constexpr uint32_t CS_NI = 2 * CS_ST_BYTES;            // [-I; 0] operand image, 128 rows x 64, 16 KB
+constexpr uint32_t CS_OIMG = CS_NI + 16384;            // o staging, 2 buffers x (64 tokens x 128, 2 x 8 KB)
+constexpr uint32_t CS_BAR = CS_OIMG + 32768;           // 10 mbarriers
 constexpr uint32_t CS_TSLOT = CS_BAR + 128;            // TMEM base, failure flag
 constexpr uint32_t CS_TOTAL = CS_BAR + 192 + 1024;
 static_assert(CS_ST_TX <= CS_ST_BYTES, "stage");
@@ -731,21 +730,23 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
                (int)blockIdx.x, (int)gridDim.x, nullptr);
 }
 
-constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 10, 11, 14, 15: output; 9, 12, 13 idle
-// The state is kept as S [d_k lanes x d_v columns] fp32 in tensor memory and as a bf16 image in shared
-// memory (rows d_k, read MN-major).  Per chunk k (one thread of warp 8 issues every MMA, in order):
-//   MMA1  D = [W; Q^] S                 rows 0-63: W S, rows 64-127: Q^ S   (M = 128, N = 128, K = 128)
-//   V~    = U - W S                     TMEM lanes 0-63, token-major image
-//   MMA3  S <- Diag(gamma) S + K~^T V~  A = K~, B = V~ (both MN-major); the decay was applied to the
-//                                       TMEM copy when S was read out, as a per-lane scalar
-//   MMA2  D rows 64-127 += A V~         A operand = [K~ half; A] read as 128 rows -> O = Q^ S + A V~
-//   S     readout: bf16 image of S_{k+1}; TMEM copy scaled by gamma_{k+1}
-// Columns of S (value channels) never mix, so the recurrence runs as two independent column halves
-// (warps 0-3: d_v 0-63, warps 4-7: d_v 64-127), each with its own barriers and N = 64 products; the
-// issuer interleaves them so that one half's CUDA-core phase overlaps the other half's MMAs.
-// The recurrence never waits for the outputs: the output warps (the four that reach TMEM lanes
-// 64-127) read O of chunk k once its MMAs are done, release the D buffer (double buffered), refill
-// the packet stage and store o through a staging tile and TMA.
+constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 9: packet loads; 12-15: output; 10, 11 idle
+// The state is kept transposed: S^T [d_v lanes x d_k columns] fp32 in tensor memory.  Its bf16 copy
+// and V~^T (bf16 pairs per 32-bit column) are the A operands of the MMAs, read from tensor memory, so
+// that the recurrence moves no operand through shared memory.  Per chunk k (one thread of warp 8
+// issues every MMA, in order; D is one of two 128-column buffers):
+//   MMA_U  D  = U^T [-I; 0]^T          D[:, 0:64] = -U^T, D[:, 64:128] = 0     (A = U, MN-major)
+//   MMA1   D += S^T [W; Q^]^T          D[:, 0:64] = (W S - U)^T = -V~^T, D[:, 64:128] = (Q^ S)^T
+//   V~     -D[:, 0:64] as bf16 pairs into tensor memory
+//   MMA3   S^T += V~^T K~              the decay Diag(gamma) was applied to S^T by the CUDA cores
+//   MMA2   D[:, 64:128] += V~^T A^T    O^T = (Q^ S + A V~)^T
+//   S      bf16 copy of S_{k+1}^T, then S^T scaled by gamma_{k+1} (per column)
+// MMA_U needs only the packet and runs ahead of the recurrence; the output warps read O^T of chunk k
+// once its MMAs are done, release the D buffer, and store o through a staging tile and TMA.
+// Tensor memory columns: S^T fp32 [0, 128), D buffers [128, 384), bf16 S^T [384, 448), bf16 V~^T
+// [448, 480).
+constexpr uint32_t TM_S = 0, TM_D0 = 128, TM_SB = 384, TM_VT = 448;
+
 // The output pass of segment g, head h in one CTA (threads 0-511).  With `flags`, a packet is loaded
 // only after its producer has published it.
 __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap &omap, int64_t T, int N,
@@ -769,13 +770,15 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
     const int seg_i = g - seg_start[n], nseg = seg_start[n + 1] - seg_start[n];
     const bool last_seg = (seg_i == nseg - 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int lq = warp & 3, cg = (warp >> 2) & 1;  // TMEM lane quarter, 64-column half
-    const int row = 32 * lq + lane;                  // TMEM lane: d_k row of S; token of D
+    const int lq = warp & 3;           // TMEM lane quarter
+    const int v = 32 * lq + lane;      // TMEM lane: d_v channel
     uint64_t *bar_ld = (uint64_t *)(sm + CS_BAR);  // [2] packet stage loaded
-    uint64_t *bar_o = bar_ld + 2;                  // [2] MMA2 (all MMAs of a chunk) done
-    uint64_t *bar_free = bar_ld + 4;               // [2] D buffer read by the output warps
-    uint64_t *bar_v = bar_ld + 6, *bar_s = bar_ld + 8;         // [2 halves] MMA1 / MMA3 done
-    uint64_t *bar_simg = bar_ld + 10, *bar_vimg = bar_ld + 12;  // [2 halves] S / V~ image halves ready
+    uint64_t *bar_o = bar_ld + 2;                  // [2] all MMAs of a chunk done
+    uint64_t *bar_free = bar_ld + 4;               // [2] O^T of a D buffer read by the output warps
+    uint64_t *bar_v = bar_ld + 6;                  // MMA1 done
+    uint64_t *bar_s = bar_ld + 7;                  // MMA3 done
+    uint64_t *bar_sb = bar_ld + 8;                 // bf16 S^T written (one arrival per recurrence warp)
+    uint64_t *bar_vt = bar_ld + 9;                 // V~^T written (one arrival per recurrence warp)
     uint32_t *tslot = (uint32_t *)(sm + CS_TSLOT);
     int *s_fail = (int *)(sm + CS_TSLOT + 8);
     const int64_t kk0 = (int64_t)seg_i * seg_len;
@@ -786,8 +789,7 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
     const int64_t e_tok = cu ? (int64_t)cu[n + 1] : (T / N) * (n + 1);
     const size_t st_off = ((size_t)n * H + h) * D * D;
     // entering state: the sequence's initial state for a lone segment; otherwise the fold's output
-    // (segment 0 included), so that final_state may alias initial_state
-    // (lane-major, see ll_off) or, for a lone segment, the user's row-major initial state
+    // (segment 0 included, lane-major, see ll_off), so that final_state may alias initial_state
     const bool s_in_ll = (nseg > 1);
     const float *s_in = s_in_ll ? seg_in + ((size_t)g * H + h) * D * D
                                 : (initial_state ? initial_state + st_off : nullptr);
@@ -797,19 +799,28 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
             mbar_init(&bar_ld[i], 1);
             mbar_init(&bar_o[i], 1);
             mbar_init(&bar_free[i], 128);
-            mbar_init(&bar_v[i], 1);
-            mbar_init(&bar_s[i], 1);
-            mbar_init(&bar_simg[i], 1);
-            mbar_init(&bar_vimg[i], 1);
         }
+        mbar_init(bar_v, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_sb, 8);
+        mbar_init(bar_vt, 8);
         *s_fail = 0;
     }
+    // [-I; 0]: 128 rows x 64, K-major (one 16 KB swizzled block); 16-byte chunk e holds row e / 8
+    for (int e = tid; e < 1024; e += blockDim.x) {
+        const int r = e >> 3, j = (e & 7) ^ (r & 7);
+        const bool diag = (r < 64 && (r >> 3) == j);
+        const uint32_t m = (r & 1) ? 0xBF800000u : 0x0000BF80u;  // bf16 -1.0 in the half of element r
+        const int wi = (r & 7) >> 1;
+        reinterpret_cast<uint4 *>(sm + CS_NI)[e] =
+            make_uint4(diag && wi == 0 ? m : 0u, diag && wi == 1 ? m : 0u, diag && wi == 2 ? m : 0u,
+                       diag && wi == 3 ? m : 0u);
+    }
     if (warp == 0) tmem_alloc(tslot, 512);
-    fence_proxy_async();  // barrier init visible to the async proxy
+    fence_proxy_async();  // barrier init and the [-I; 0] image visible to the async proxy
     sync_all();
     const uint32_t tb = *tslot;
-    const uint32_t tS = tb;  // S: 128 columns; D buffers at tb + 128 and tb + 256
-    auto tDbuf = [&](int kk) { return tb + 128 + 128 * (uint32_t)(kk & 1); };
+    auto tDbuf = [&](int kk) { return tb + TM_D0 + 128 * (uint32_t)(kk & 1); };
     auto packet = [&](int kk) { return packets + ((size_t)(c_begin + kk) * H + h) * PK_STRIDE; };
     auto stage = [&](int kk) { return sm + (kk & 1) * CS_ST_BYTES; };
     auto load_stage = [&](int kk) {  // returns false if the packet was never published
@@ -822,211 +833,197 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
         bulk_g2s(stage(kk), packet(kk), CS_ST_TX, b);
         return true;
     };
-    if (tid == 0) {
-        for (int kk = 0; kk < 2 && kk < nc; ++kk)
-            if (!load_stage(kk)) atomicExch(s_fail, 1);
-        if (nc > 2 && !flags) bulk_prefetch_l2(packet(2), CS_ST_TX);
-    }
 
     if (warp == 8) {
         // ------------------------------------------------ MMA issue (one thread)
         if (lane == 0) {
-            const uint32_t idD = idesc_bf16(128, 128, false, true);
-            const uint32_t idD64 = idesc_bf16(128, 64, false, true), idS64 = idesc_bf16(128, 64, true, true);
+            const uint32_t idU = idesc_bf16(128, 128, true, false);   // A = U (MN-major), B = [-I; 0]
+            const uint32_t id1 = idesc_bf16(128, 128, false, false);  // A = bf16 S^T, B = [W; Q^] (K-major)
+            const uint32_t id3 = idesc_bf16(128, 128, false, true);   // A = V~^T, B = K~ (MN-major)
+            const uint32_t id2 = idesc_bf16(128, 64, false, false);   // A = V~^T, B = A (K-major)
             bool ok = true;
             for (int kk = 0; kk < nc && ok; ++kk) {
                 unsigned char *P = stage(kk);
                 const uint32_t tD = tDbuf(kk);
                 if (kk >= 2) ok = mbar_wait_spin(&bar_free[kk & 1], ((kk >> 1) - 1) & 1);  // O of chunk kk - 2 read
-                for (int hv = 0; hv < 2 && ok; ++hv) {  // MMA1 per column half: D[:, half] = [W; Q^] S[:, half]
-                    ok = mbar_wait_spin(&bar_simg[hv], kk & 1);  // S image half of S_kk written, packet kk resident
-                    if (!ok) break;
-                    fence_after_sync();
-                    mma_bf16_kmn(tD + 64 * hv, smem_u32(P + PK_WQ), 128, smem_u32(sm + CS_SIMG + 16384 * hv), 16384,
-                                 8, idD64, false);
-                    mma_commit(&bar_v[hv]);
-                }
-                for (int hv = 0; hv < 2 && ok; ++hv) {  // MMA3 per column half: S[:, half] += K~^T V~[:, half]
-                    ok = mbar_wait_spin(&bar_vimg[hv], kk & 1);  // V~ half written, TMEM S half scaled by gamma_kk
-                    if (!ok) break;
-                    fence_after_sync();
-                    mma_bf16_mnmn(tS + 64 * hv, smem_u32(P + PK_K), 8192, smem_u32(sm + CS_VIMG + 8192 * hv), 8192,
-                                  4, idS64, true);
-                    mma_commit(&bar_s[hv]);
-                }
+                ok = ok && mbar_wait_spin(&bar_ld[kk & 1], (kk >> 1) & 1);                // packet kk resident
                 if (!ok) break;
-                mma_bf16_kmn(tD, smem_u32(P + PK_A - 8192), 128, smem_u32(sm + CS_VIMG), 8192, 4, idD, true);
+                fence_after_sync();
+                mma_bf16_mnk(tD, smem_u32(P + PK_U), 8192, smem_u32(sm + CS_NI), 128, 4, idU, false);
+                ok = mbar_wait_spin(bar_sb, kk & 1);  // bf16 S_kk^T written
+                if (!ok) break;
+                fence_after_sync();
+                mma_ts_k(tD, tb + TM_SB, smem_u32(P + PK_WQ), 128, 8, id1, true);
+                mma_commit(bar_v);
+                ok = mbar_wait_spin(bar_vt, kk & 1);  // V~^T written, S^T scaled by gamma_kk
+                if (!ok) break;
+                fence_after_sync();
+                mma_ts_mn(tb + TM_S, tb + TM_VT, smem_u32(P + PK_K), 8192, 4, id3, true);
+                mma_commit(bar_s);
+                mma_ts_k(tD + 64, tb + TM_VT, smem_u32(P + PK_A), 64, 4, id2, true);
                 mma_commit(&bar_o[kk & 1]);
             }
             if (!ok) atomicExch(s_fail, 1);
         }
-    } else if (warp >= 10 && lq >= 2) {
-        // ------------------------------------------------ output warps 10, 11, 14, 15 (128 threads)
-        const int ot = (warp >= 14 ? 64 : 0) + (warp & 1) * 32 + lane;  // 0..127
-        const int t = row - 64;                                         // token of TMEM lane `row`
+    } else if (warp == 9) {
+        // ------------------------------------------------ packet loads (one thread)
+        if (lane == 0) {
+            bool ok = true;
+            for (int kk = 0; kk < 2 && kk < nc && ok; ++kk) ok = load_stage(kk);
+            if (ok && nc > 2 && !flags) bulk_prefetch_l2(packet(2), CS_ST_TX);
+            for (int kk = 0; kk + 2 < nc && ok; ++kk) {
+                ok = mbar_wait(&bar_o[kk & 1], (kk >> 1) & 1);  // all MMAs of chunk kk done: its stage takes kk + 2
+                if (!ok) break;
+                ok = load_stage(kk + 2);
+                if (ok && kk + 3 < nc && !flags) bulk_prefetch_l2(packet(kk + 3), CS_ST_TX);
+            }
+            if (!ok) atomicExch(s_fail, 1);
+        }
+    } else if (warp >= 12 && warp < 16) {
+        // ------------------------------------------------ output warps 12-15 (128 threads, one d_v lane each)
+        const int ot = tid - 384;
+        // byte offset of (token t, channel v) in the staging tile (two 64-channel SW128 halves): row part
+        const uint32_t vh = (uint32_t)(v >> 6) * 8192 + ((uint32_t)(v & 7) << 1);
+        const int vc = (v & 63) >> 3;
         bool ok = true;
         for (int kk = 0; kk < nc && ok; ++kk) {
             ok = mbar_wait(&bar_o[kk & 1], (kk >> 1) & 1);
-            ok = bar_red_popc(2, 128, ok) == 128;
             if (!ok) break;
             fence_after_sync();
-            if (ot == 0) {  // all MMAs of chunk kk are done: its stage takes chunk kk + 2
-                if (kk + 2 < nc && !load_stage(kk + 2)) atomicExch(s_fail, 1);
-                if (kk + 3 < nc && !flags) bulk_prefetch_l2(packet(kk + 3), CS_ST_TX);
-            }
-            const int64_t tp = s_tok + (int64_t)kk * C;
-            const int lenp = (int)min((int64_t)C, e_tok - tp);
-            uint4 pk8[8];
+            uint32_t ob[32];  // O^T[v][2i], O^T[v][2i + 1] as bf16 pairs
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 float d[32];
-                tmem_ld32(tmem_addr(tDbuf(kk), 32 * lq, 64 * cg + 32 * h2), d);
+                tmem_ld32(tDbuf(kk) + ((uint32_t)(32 * lq) << 16) + 64 + 32 * h2, d);
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    float v8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v8[e] = scale * d[8 * jj + e];
-                    pk8[4 * h2 + jj] = pack8(v8);
-                }
+                for (int i = 0; i < 16; ++i) ob[16 * h2 + i] = pack_bf16(scale * d[2 * i], scale * d[2 * i + 1]);
             }
             fence_before_sync();
             mbar_arrive(&bar_free[kk & 1]);  // TMEM buffer read
-            if (lenp == C) {  // full chunk: two 64 x 64 swizzled tiles, two TMA stores
-                if (ot == 0) bulk_wait_read0();  // the previous tile has left the staging buffer
+            const int64_t tp = s_tok + (int64_t)kk * C;
+            const int lenp = (int)min((int64_t)C, e_tok - tp);
+            if (lenp == C) {  // full chunk: two 64 x 64 swizzled tiles, two TMA stores (double-buffered)
+                unsigned char *stg = sm + CS_OIMG + 16384 * (kk & 1);
+                if (ot == 0 && kk >= 2) bulk_wait_read1();  // the store of chunk kk - 2 has left this buffer
                 named_sync(2, 128);
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj)
-                    *reinterpret_cast<uint4 *>(sm + CS_OIMG + img_chunk_off(64, t, 8 * cg + jj)) = pk8[jj];
+                for (int t = 0; t < 64; ++t) {
+                    const uint32_t w = ob[t >> 1];
+                    *reinterpret_cast<uint16_t *>(stg + vh + t * 128 + ((vc ^ (t & 7)) << 4)) =
+                        (uint16_t)((t & 1) ? (w >> 16) : (w & 0xFFFFu));
+                }
                 fence_proxy_async();
                 named_sync(2, 128);
                 if (ot == 0) {
-                    tma_store_3d(&omap, sm + CS_OIMG, 0, h, (int)tp);
-                    tma_store_3d(&omap, sm + CS_OIMG + 8192, 64, h, (int)tp);
+                    tma_store_3d(&omap, stg, 0, h, (int)tp);
+                    tma_store_3d(&omap, stg + 8192, 64, h, (int)tp);
                     bulk_commit();
                 }
-            } else if (t < lenp) {  // the ragged last chunk of a sequence: rows past its end stay untouched
-                bf16 *dst = o + ((tp + t) * H + h) * D + 64 * cg;
+            } else {  // the ragged last chunk of a sequence: rows past its end stay untouched
+                bf16 *dst = o + (tp * H + h) * D + v;
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) *reinterpret_cast<uint4 *>(dst + 8 * jj) = pk8[jj];
+                for (int t = 0; t < 64; ++t) {
+                    const uint32_t w = ob[t >> 1];
+                    if (t < lenp)
+                        *reinterpret_cast<uint16_t *>(dst + (size_t)t * H * D) =
+                            (uint16_t)((t & 1) ? (w >> 16) : (w & 0xFFFFu));
+                }
             }
         }
         if (ot == 0) bulk_wait0();
         if (!ok) atomicExch(s_fail, 1);
     } else if (warp < 8) {
-        // ------------------------------------------------ recurrence warps 0-7: half cg = warps 4 cg .. 4 cg + 3
-        const int nbar = cg ? 3 : 1;  // named barrier of this half (128 threads)
-        const int ht = tid & 127;     // thread within the half
+        // ------------------------------------------------ recurrence warps 0-7: lanes of quarter lq,
+        // d_k columns [64 j, 64 j + 64) of S^T and tokens [32 j, 32 j + 32) of V~^T
+        const int j = warp >> 2;
         bool ok = true;
-        {
-            float x[64];  // S_0 row `row`, columns [64 cg, 64 cg + 64)
-            if (s_in) {
+        if (nc > 0) ok = mbar_wait_spin(&bar_ld[0], 0);
+        // S_0^T, 32 columns at a time: bf16 copy, and the fp32 state scaled by gamma_0
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2 && ok; ++h2) {
+            const int c0 = 64 * j + 32 * h2;
+            float x[32];
 #pragma unroll
-                for (int e = 0; e < 64; e += 4) {
-                    const float4 v4 = *reinterpret_cast<const float4 *>(
-                        s_in + (s_in_ll ? ll_off(row, 64 * cg + e) : (size_t)row * D + 64 * cg + e));
-                    x[e] = v4.x; x[e + 1] = v4.y; x[e + 2] = v4.z; x[e + 3] = v4.w;
+            for (int e = 0; e < 32; ++e)
+                x[e] = s_in ? s_in[s_in_ll ? ll_off(c0 + e, v) : (size_t)(c0 + e) * D + v] : 0.f;
+            if (nc == 0) {
+                if (final_state && last_seg) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) final_state[st_off + (size_t)(c0 + e) * D + v] = x[e];
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 64; ++e) x[e] = 0.f;
+                continue;
             }
-            if (nc > 0) ok = mbar_wait(&bar_ld[0], 0);
-            ok = bar_red_popc(nbar, 128, ok) == 128;
-            if (nc == 0 && ok && final_state && last_seg) {
+            uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 64; e += 4)
-                    *reinterpret_cast<float4 *>(final_state + st_off + (size_t)row * D + 64 * cg + e) =
-                        make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-            }
-            if (ok && nc > 0) {  // S_0 image; TMEM gets Diag(gamma_0) S_0
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(x[2 * i], x[2 * i + 1]);
+            tmem_st16u(tmem_addr(tb + TM_SB, 32 * lq, c0 / 2), pk);
+            const float *gam = reinterpret_cast<const float *>(stage(0) + PK_G) + c0;
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj)
-                    *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, row, 8 * cg + jj)) = pack8(x + 8 * jj);
-                const float gr = reinterpret_cast<const float *>(stage(0) + PK_G)[row];
+            for (int e = 0; e < 32; ++e) x[e] *= gam[e];
+            tmem_st32(tmem_addr(tb + TM_S, 32 * lq, c0), x);
+        }
+        tmem_st_wait();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0 && nc > 0 && ok) mbar_arrive(bar_sb);
+        for (int kk = 0; kk < nc && ok; ++kk) {
+            // invariant: packet kk resident; bf16 S_kk^T written; TMEM S^T = (Diag(gamma_kk) S_kk)^T
+            ok = mbar_wait_spin(bar_v, kk & 1) && (*(volatile int *)s_fail == 0);
+            if (!ok) break;
+            fence_after_sync();
+            {
+                float d[32];
+                tmem_ld32(tmem_addr(tDbuf(kk), 32 * lq, 32 * j), d);
+                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 64; ++e) x[e] *= gr;
-                tmem_st32(tmem_addr(tS, 32 * lq, 64 * cg), x);
-                tmem_st32(tmem_addr(tS, 32 * lq, 64 * cg + 32), x + 32);
+                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(-d[2 * i], -d[2 * i + 1]);
+                tmem_st16u(tmem_addr(tb + TM_VT, 32 * lq, 16 * j), pk);
                 tmem_st_wait();
             }
-        }
-        fence_proxy_async();
-        fence_before_sync();
-        named_sync(nbar, 128);
-        if (ht == 0 && nc > 0) mbar_arrive(&bar_simg[cg]);
-        for (int kk = 0; kk < nc && ok; ++kk) {
-            // invariant: packet kk resident; S image = bf16(S_kk); TMEM S = Diag(gamma_kk) S_kk
-            if (ht == 0) ok = mbar_wait_spin(&bar_v[cg], kk & 1);  // one thread polls, the barrier releases
-            ok = (bar_red_popc(nbar, 128, ok) == 128) && (*(volatile int *)s_fail == 0);
-            if (!ok) break;
-            fence_after_sync();
-            if (lq < 2) {  // V~ row `row` = U - W S
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    float dv[32], u[8], vo[8];
-                    tmem_ld32(tmem_addr(tDbuf(kk), 32 * lq, 64 * cg + 32 * h2), dv);
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        unpack8(*reinterpret_cast<const uint4 *>(stage(kk) + PK_U +
-                                                                 img_chunk_off(64, row, 8 * cg + 4 * h2 + jj)),
-                                u);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) vo[e] = u[e] - dv[8 * jj + e];
-                        *reinterpret_cast<uint4 *>(sm + CS_VIMG + img_chunk_off(64, row, 8 * cg + 4 * h2 + jj)) =
-                            pack8(vo);
-                    }
-                }
-            }
-            fence_proxy_async();
             fence_before_sync();
-            named_sync(nbar, 128);
-            if (ht == 0) mbar_arrive(&bar_vimg[cg]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_vt);
             const bool last = (kk == nc - 1);
-            if (ht == 0) {
-                const bool okl = last || mbar_wait_spin(&bar_ld[(kk + 1) & 1], ((kk + 1) >> 1) & 1);
-                ok = mbar_wait_spin(&bar_s[cg], kk & 1) && okl;
-            }
-            ok = bar_red_popc(nbar, 128, ok) == 128;
+            ok = mbar_wait_spin(bar_s, kk & 1);
+            if (ok && !last) ok = mbar_wait_spin(&bar_ld[(kk + 1) & 1], ((kk + 1) >> 1) & 1);
             if (!ok) break;
             fence_after_sync();
-            // S_{kk+1}: bf16 image first (MMA1 of the next chunk needs it), then the TMEM copy scaled by
-            // gamma_{kk+1} (the next MMA3 needs it, and is issued only after this half's next V~ image)
             if (!last) {
+                // bf16 S_{kk+1}^T first (MMA1 of the next chunk waits for it), then the fp32 copy scaled
+                // by gamma_{kk+1} (MMA3 of the next chunk, issued after this warp's next V~, needs it)
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c0 = 64 * j + 32 * h2;
                     float x[32];
-                    const int c0 = 64 * cg + 32 * h2;
-                    tmem_ld32(tmem_addr(tS, 32 * lq, c0), x);
+                    tmem_ld32(tmem_addr(tb + TM_S, 32 * lq, c0), x);
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        *reinterpret_cast<uint4 *>(sm + CS_SIMG + img_chunk_off(128, row, c0 / 8 + jj)) =
-                            pack8(x + 8 * jj);
+                    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(x[2 * i], x[2 * i + 1]);
+                    tmem_st16u(tmem_addr(tb + TM_SB, 32 * lq, c0 / 2), pk);
                 }
-                fence_proxy_async();
+                tmem_st_wait();
                 fence_before_sync();
-                named_sync(nbar, 128);
-                if (ht == 0) mbar_arrive(&bar_simg[cg]);
-                const float gr = reinterpret_cast<const float *>(stage(kk + 1) + PK_G)[row];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_sb);
+                const float *gam = reinterpret_cast<const float *>(stage(kk + 1) + PK_G);
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c0 = 64 * j + 32 * h2;
                     float x[32];
-                    const int c0 = 64 * cg + 32 * h2;
-                    tmem_ld32(tmem_addr(tS, 32 * lq, c0), x);
+                    tmem_ld32(tmem_addr(tb + TM_S, 32 * lq, c0), x);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] *= gr;
-                    tmem_st32(tmem_addr(tS, 32 * lq, c0), x);
+                    for (int e = 0; e < 32; ++e) x[e] *= gam[c0 + e];
+                    tmem_st32(tmem_addr(tb + TM_S, 32 * lq, c0), x);
                 }
                 tmem_st_wait();
             } else if (final_state && last_seg) {
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c0 = 64 * j + 32 * h2;
                     float x[32];
-                    const int c0 = 64 * cg + 32 * h2;
-                    tmem_ld32(tmem_addr(tS, 32 * lq, c0), x);
+                    tmem_ld32(tmem_addr(tb + TM_S, 32 * lq, c0), x);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4 *>(final_state + st_off + (size_t)row * D + c0 + e) =
-                            make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+                    for (int e = 0; e < 32; ++e) final_state[st_off + (size_t)(c0 + e) * D + v] = x[e];
                 }
             }
         }

@@ -121,6 +121,34 @@ __device__ __forceinline__ void mma_bf16_mnmn(uint32_t d_tmem, uint32_t a_base, 
 // 32 consecutive fp32 columns into TMEM.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v);
 
+// D[tmem] (+)= A(tmem) * B(smem desc)^T, issued by one thread.  A sits in tensor memory with row m in
+// lane m and bf16 pairs packed per 32-bit column (element 2j in the low half of column j), so that
+// one K-step of 16 elements is 8 columns.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+// Full product over K = 16 * ksteps, A in tensor memory, B a K-major image with RB rows.
+__device__ __forceinline__ void mma_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, int RB, int ksteps,
+                                         uint32_t idesc, bool accumulate) {
+    const uint64_t db = desc_sw128(b_base);
+#pragma unroll
+    for (int s = 0; s < ksteps; ++s)
+        mma_ts(d_tmem, a_tmem + 8 * s, db + (uint64_t)((((s >> 2) * RB * 128) + (s & 3) * 32) >> 4), idesc,
+               (accumulate || s > 0) ? 1u : 0u);
+}
+// Full product over K = 16 * ksteps, A in tensor memory, B MN-major (groups along N b_lbo bytes apart).
+__device__ __forceinline__ void mma_ts_mn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, uint32_t b_lbo,
+                                          int ksteps, uint32_t idesc, bool accumulate) {
+    const uint64_t db = desc_sw128_mn(b_base, b_lbo);
+#pragma unroll
+    for (int s = 0; s < ksteps; ++s)
+        mma_ts(d_tmem, a_tmem + 8 * s, db + (uint64_t)((2048 * s) >> 4), idesc, (accumulate || s > 0) ? 1u : 0u);
+}
+
 // 32 / 64 consecutive fp32 columns of this thread's TMEM lane in one load.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
     uint32_t r[32];
@@ -187,6 +215,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
            "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
            "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
            "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+// 16 consecutive 32-bit columns (e.g. bf16 pairs) into TMEM.
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+           "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
@@ -283,6 +319,7 @@ __device__ __forceinline__ void bulk_s2g(void *gdst, const void *smem_src, uint3
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
