@@ -483,15 +483,19 @@ def run_case(args):
     """Small fixed cases for profiler captures (a few untimed launches, then a one-line summary).
 
     prefill_small: B=1, H=8, T=16384, bf16, d=128 (inputs 33.6 MB, packets 155 MB: above L2).
+    prefill_4k:    the benchmark's prefill workload, B=1, H=32, T=4096, bf16, d=128.
     decode_small:  N=64 sequences x H=32 heads, d=128, fp32 state 268 MB (above L2), 8 steps.
     """
     from linear_attention_kda_gb300 import build as kbuild, kda
     kbuild.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.case == "prefill_small":
-        w = syn.Workload("prefill_small_bf16_T16384_H8_d128", H=8, d=128, dtype="bf16", seq_len=16384,
-                         z_std=1.5, b_range=1.0, alog_std=0.25)
+    if args.case in ("prefill_small", "prefill_4k"):
+        if args.case == "prefill_small":
+            w = syn.Workload("prefill_small_bf16_T16384_H8_d128", H=8, d=128, dtype="bf16", seq_len=16384,
+                             z_std=1.5, b_range=1.0, alog_std=0.25)
+        else:
+            w = syn.PREFILL_4K
         d = syn.make_prefill(w, seed=1, device=dev)
         for _ in range(3):
             kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["dt_bias"], d["A_log"],
@@ -516,7 +520,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--case", choices=["prefill_small", "decode_small"], default=None,
+    ap.add_argument("--case", choices=["prefill_small", "prefill_4k", "decode_small"], default=None,
                     help="run a small fixed case for profiler captures instead of the benchmark")
     args = ap.parse_args()
     if args.case:

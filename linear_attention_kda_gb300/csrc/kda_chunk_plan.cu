@@ -10,6 +10,7 @@
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
+#include <algorithm>
 #include <cmath>
 
 namespace kda {
@@ -117,22 +118,25 @@ chunk_plan_kernel(const int32_t *__restrict__ cu, int64_t T, int N, int C,
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Schedule of the tensor-core path, from a latency model of its kernels (microseconds): an
-// intra-chunk item costs T_ITEM on one SM; a chain step of the output pass T_STEP, a summary step
-// 1.3 T_STEP, a fold step ~T_STEP; one CTA per SM; T_LAUNCH per kernel boundary.  Three schedules:
+// Schedule of the tensor-core path, from a latency model of its kernels (microseconds, one CTA per
+// SM): an intra-chunk item costs T_ITEM, plus T_COLD for the first item of a CTA; a step of the
+// output pass T_CHAIN, of a segment summary T_SUM, of the fold T_FOLD; T_LAUNCH per kernel boundary.
+// Three schedules:
 //  - separate kernels, one segment per sequence;
 //  - separate kernels with the split-sequence state pass (segments of L chunks);
-//  - fused: chains (one per sequence and head) and intra-chunk producers share one launch.
+//  - fused: chains (one per sequence and head) and intra-chunk producers share one launch; each
+//    chain first produces its own first kpre chunks, the producers the rest.
 // Uses per-sequence lengths when the host copy of cu_seqlens is given.
-constexpr double T_ITEM = 6.0, T_STEP = 1.8, T_LAUNCH = 4.0;
+constexpr double T_ITEM = 6.5, T_COLD = 13.5, T_CHAIN = 1.15, T_SUM = 2.3, T_FOLD = 1.8, T_LAUNCH = 4.0;
 
 struct tc_schedule {
     int64_t seg_len;  // 1 << 30: no split
     bool fused;
+    int kpre;
 };
 
 static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int32_t *cu_host, int sms) {
-    tc_schedule r{(int64_t)1 << 30, false};
+    tc_schedule r{(int64_t)1 << 30, false, 0};
     if (T == 0) return r;
     int64_t total = 0, longest = 0;
     auto chunks_of = [&](int64_t n) -> int64_t {
@@ -144,12 +148,12 @@ static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int
         total += c;
         longest = c > longest ? c : longest;
     }
-    auto waves = [&](int64_t ctas) { return (double)((ctas + sms - 1) / sms); };
+    auto waves = [&](double ctas, double width) { return std::ceil(ctas / width); };
     const double items = (double)total * H;
-    const double intra = waves((int64_t)items) * T_ITEM;
+    const double intra = T_COLD + waves(items, sms) * T_ITEM;
     // unsplit output pass: the longest chain, or the chains' total over the SMs
     const double unsplit = (double)longest > items / sms ? (double)longest : items / sms;
-    double best = intra + unsplit * T_STEP + 2 * T_LAUNCH;
+    double best = intra + unsplit * T_CHAIN + 2 * T_LAUNCH;
     for (int64_t L = 8; L <= (1 << 14); L *= 2) {
         if (L >= longest) break;
         int64_t segs = 0, segs_sum = 0, max_nseg = 0;
@@ -160,23 +164,33 @@ static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int
             segs_sum += ns - 1;
             max_nseg = ns > max_nseg ? ns : max_nseg;
         }
-        const double steps = 1.3 * L * waves(segs_sum * H) + 1.0 * (max_nseg - 1) + L * waves(segs * H);
-        const double cost = intra + steps * T_STEP + 4 * T_LAUNCH;
+        const double steps = T_SUM * L * waves((double)segs_sum * H, sms) + T_FOLD * (max_nseg - 1) +
+                             T_CHAIN * L * waves((double)segs * H, sms);
+        const double cost = intra + steps + 4 * T_LAUNCH;
         if (cost < 0.85 * best) {  // split only for a clear gain
             best = cost;
             r.seg_len = L;
         }
     }
     const int64_t n_chain = N * H;
-    if (n_chain + 16 <= sms) {
+    if (n_chain + 16 <= sms && N <= KDA_FUSED_MAX_SEQS) {
         const double producers = (double)(sms - n_chain);
-        const double fused = (items / producers > (double)longest * T_STEP / T_ITEM
-                                  ? std::ceil(items / producers) * T_ITEM
-                                  : (double)longest * T_STEP) +
-                             T_ITEM + T_LAUNCH;
-        if (fused < best) {
-            r.fused = true;
-            r.seg_len = (int64_t)1 << 30;
+        for (int kp = 0; kp <= 8; ++kp) {
+            double items_p = 0;
+            for (int64_t n = 0; n < N; ++n) {
+                const int64_t c = chunks_of(n) - kp;
+                items_p += c > 0 ? (double)c * H : 0.0;
+            }
+            const double pm = items_p > 0 ? T_COLD + waves(items_p, producers) * T_ITEM : 0.0;
+            const double first = T_COLD + (kp > 0 ? (double)(kp < longest ? kp : longest) : 1.0) * T_ITEM;
+            const double chain_end = std::max(first + (double)longest * T_CHAIN, pm + 2 * T_CHAIN);
+            const double cost = std::max(pm, chain_end) + T_LAUNCH;
+            if (cost < best) {
+                best = cost;
+                r.fused = true;
+                r.kpre = kp;
+                r.seg_len = (int64_t)1 << 30;
+            }
         }
     }
     return r;
@@ -200,6 +214,7 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
     size_t end = p->off_records + p->record_bytes * (size_t)p->max_chunks * (size_t)H;
     p->split = 0;
     p->fused = 0;
+    p->kpre = 0;
     p->seg_len = (int64_t)1 << 30;
     p->max_segs = N;
     if (p->path == 1) {
@@ -209,6 +224,7 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
         const tc_schedule sch = choose_schedule(T, N, H, C, cu_seqlens_host, sms);
         p->seg_len = sch.seg_len;
         p->fused = sch.fused ? 1 : 0;
+        p->kpre = sch.kpre;
         p->split = p->seg_len < ((int64_t)1 << 30) ? 1 : 0;
         p->max_segs = p->split ? p->max_chunks / p->seg_len + N : N;
     }

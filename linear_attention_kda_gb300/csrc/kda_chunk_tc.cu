@@ -35,27 +35,29 @@ constexpr int C = 64;   // chunk
 constexpr int D = 128;  // d_k = d_v
 
 // packet layout (bytes)
-// Every operand is token-major ([token][channel] rows of 128 bytes, 128-byte swizzle).
+// Operands are token-major ([token][channel] rows of 128 bytes, 128-byte swizzle), except U, kept
+// as U^T (rows are value channels).  Part 1
+// ([W; Q^], U, gamma) is what a chunk's first MMAs and the decay of the state before it read; part 2
+// (K~, A) is read last, so the output pass loads and releases the two parts separately.
 constexpr uint32_t PK_WQ = 0;         // [W; Q^]: one K-major 128-row image (rows 0-63 W, rows 64-127 Q^),
                                       // 16 KB per 64-channel block
-constexpr uint32_t PK_K = 32768;      // K~ [64 tokens][128 channels] (two 64-channel halves)
-constexpr uint32_t PK_A = 49152;      // A [64 query rows][64 keys]; with the K~ half before it, a 128-row
-                                      // operand whose rows 64-127 are A
-constexpr uint32_t PK_U = 57344;      // U [64 tokens][128 channels] (two halves)
-constexpr uint32_t PK_G = 73728;      // gamma^C fp32 [128]
-constexpr uint32_t PK_STRIDE = 75776; // multiple of 1024
+constexpr uint32_t PK_U = 32768;      // U^T [128 channels][64 tokens]: K-major image, rows d_v
+constexpr uint32_t PK_G = 49152;      // gamma^C fp32 [128]
+constexpr uint32_t PK_K = 50176;      // K~ [64 tokens][128 channels] (two halves)
+constexpr uint32_t PK_A = 66560;      // A [64 query rows][64 keys]
+constexpr uint32_t PK_STRIDE = 74752; // multiple of 1024
+constexpr uint32_t PK_P1 = PK_G + 512;        // bytes of part 1 (at 0)
+constexpr uint32_t PK_P2 = PK_STRIDE - PK_K;  // bytes of part 2 (at PK_K)
 
 // inter kernel shared memory
-// Output pass: two stages hold whole packets (one bulk copy each); the packet after them is
-// prefetched into L2.
-constexpr uint32_t CS_ST_TX = PK_G + 512;              // packet bytes
+// Output pass: two stages hold whole packets (two bulk copies each, one per part); without flags
+// the packet after them is prefetched into L2.
 constexpr uint32_t CS_ST_BYTES = PK_STRIDE;            // stage stride (multiple of 1024)
-constexpr uint32_t CS_NI = 2 * CS_ST_BYTES;            // [-I; 0] operand image, 128 rows x 64, 16 KB
-constexpr uint32_t CS_OIMG = CS_NI + 16384;            // o staging, 2 buffers x (64 tokens x 128, 2 x 8 KB)
-constexpr uint32_t CS_BAR = CS_OIMG + 32768;           // 10 mbarriers
+constexpr uint32_t CS_OIMG = 2 * CS_ST_BYTES;          // o staging, 2 buffers x (64 tokens x 128, 2 x 8 KB)
+constexpr uint32_t CS_BAR = CS_OIMG + 32768;           // 12 mbarriers
 constexpr uint32_t CS_TSLOT = CS_BAR + 128;            // TMEM base, failure flag
 constexpr uint32_t CS_TOTAL = CS_BAR + 192 + 1024;
-static_assert(CS_ST_TX <= CS_ST_BYTES, "stage");
+static_assert(PK_P1 <= PK_K && PK_P1 % 16 == 0 && PK_P2 % 16 == 0, "packet parts");
 
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
     const uint32_t s = smem_u32(p);
@@ -188,9 +190,11 @@ constexpr uint32_t J_BIAS = J_BETA + 512;   // 2 stages x fp32 [128]
 constexpr uint32_t J_INFO = J_BIAS + 1024;  // 2 stages x {int64 t0, len, h, slot; float eA}
 constexpr uint32_t J_BAR = J_INFO + 128;    // ld[2], pq[2], pw[2], mma, rd
 constexpr uint32_t J_TSLOT = J_BAR + 64;
-constexpr uint32_t J_TOTAL = J_BAR + 128 + 1024;
+constexpr uint32_t J_TBL = J_BAR + 128;     // int32 [J_TBL_N + 1]: producer chunks before each sequence
+constexpr int J_TBL_N = KDA_FUSED_MAX_SEQS;  // sequences the table holds
+constexpr uint32_t J_TOTAL = J_TBL + 4 * (J_TBL_N + 1) + 1024;
 // TMEM columns: A / L product (96); later [W | U] (256, lanes 0-63)
-constexpr uint32_t TM_DA = 0, TM_DB = 32, TM_DWU = 0;
+constexpr uint32_t TM_DA = 0, TM_DB = 32, TM_DW = 0, TM_DUT = 128;
 
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -334,18 +338,60 @@ __device__ __forceinline__ bool flag_wait(const int *f) {
     }
 }
 
-// The intra-chunk work of one CTA: worker `worker` of `nworkers` takes items worker, worker +
-// nworkers, ...  With `flags`, each item's packet is published (flags[item] = 1) once its writes
-// have completed.
+// The intra-chunk work of one CTA.  Items (chunk slot, head) are numbered w = slot * H + h.
+//  - own_n < 0, kpre == 0: worker `worker` of `nworkers` takes items worker, worker + nworkers, ...
+//  - own_n < 0, kpre > 0: the same over the items left once the first kpre chunks of every
+//    sequence are taken away (in the same order);
+//  - own_n >= 0: the first kpre chunks of sequence own_n for head own_h.
+// With `flags`, each item's packet is published (flags[item] = 1) once its writes have completed.
+// In the last mode the CTA keeps its right to allocate tensor memory (its chain runs next).
 __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm, const bf16 *__restrict__ beta,
                                            const float *__restrict__ bias, const float *__restrict__ A_log,
                                            float g_min, int64_t T, int N, const int32_t *__restrict__ cu,
                                            const int32_t *__restrict__ chunk_start, int H,
                                            unsigned char *__restrict__ packets, int *err, int worker, int nworkers,
-                                           int *flags) {
+                                           int *flags, int kpre, int own_n, int own_h) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t W = (int64_t)chunk_start[N] * H;  // work items
-    if ((int64_t)worker >= W) return;
+    int32_t *tbl = (int32_t *)(sm + J_TBL);  // kpre > 0: tbl[n] = producer chunks of sequences before n
+    int n_items = 0;
+    if (own_n >= 0) {
+        n_items = min(kpre, chunk_start[own_n + 1] - chunk_start[own_n]);
+    } else if (kpre > 0) {
+        if (warp == 0) {
+            int carry = 0;
+            if (lane == 0) tbl[0] = 0;
+            for (int base = 0; base < N; base += 32) {
+                const int m = base + lane;
+                int x = m < N ? max(0, chunk_start[m + 1] - chunk_start[m] - kpre) : 0;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, x, off);
+                    if (lane >= off) x += y;
+                }
+                if (m < N) tbl[m + 1] = carry + x;
+                carry += __shfl_sync(0xffffffffu, x, 31);
+            }
+        }
+        __syncthreads();
+        const int64_t Wp = (int64_t)tbl[N] * H;
+        n_items = worker < Wp ? (int)((Wp - worker + nworkers - 1) / nworkers) : 0;
+    } else {
+        const int64_t W = (int64_t)chunk_start[N] * H;
+        n_items = worker < W ? (int)((W - worker + nworkers - 1) / nworkers) : 0;
+    }
+    if (n_items == 0) return;
+    auto w_of = [&](int it) -> int64_t {  // global item index of this CTA's it-th item
+        if (own_n >= 0) return (int64_t)(chunk_start[own_n] + it) * H + own_h;
+        const int64_t k = (int64_t)worker + (int64_t)it * nworkers;
+        if (kpre <= 0) return k;
+        const int64_t kk = k / H;
+        int lo = 0, hi = N;  // the sequence holding producer chunk kk: largest n with tbl[n] <= kk
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (tbl[mid] <= kk) lo = mid; else hi = mid;
+        }
+        return (int64_t)(chunk_start[lo] + kpre + (kk - tbl[lo])) * H + (int)(k % H);
+    };
     float *Gs = (float *)(sm + J_G);
     uint64_t *bar_ld = (uint64_t *)(sm + J_BAR);  // [2] stage loaded
     uint64_t *bar_pq = bar_ld + 2;                // [2] Q^ and K~ tiles of the stage's item written
@@ -363,7 +409,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
         mbar_init(bar_mma, 1);
         mbar_init(bar_rd, 1);
     }
-    if (warp == 0) tmem_alloc(tslot, 256);
+    if (warp == 0) tmem_alloc(tslot, 256, own_n < 0);
     fence_proxy_async();
     sync_all();
     const uint32_t tb = *tslot;
@@ -373,7 +419,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
         // writes their packets (bulk copies from shared memory), publishing each through `flags` once its
         // writes have completed; a stage is refilled as soon as the copies of its item have read it.
         auto load_item = [&](int it) {
-            const int64_t w = (int64_t)worker + (int64_t)it * nworkers;
+            const int64_t w = w_of(it);
             const int s = it & 1;
             const int64_t slot = w / H;
             const int h = (int)(w % H);
@@ -407,13 +453,12 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
                 }
             }
         };
-        const int n_items = (int)((W - worker + nworkers - 1) / nworkers);
         if (n_items > 0) load_item(0);
         if (n_items > 1) load_item(1);
         bool ok = true;
         for (int it = 0; it < n_items && ok; ++it) {
             const int s = it & 1;
-            const int64_t w = (int64_t)worker + (int64_t)it * nworkers;
+            const int64_t w = w_of(it);
             unsigned char *stg = sm + s * J_STG_BYTES;
             unsigned char *pk = packets + (size_t)w * PK_STRIDE;  // item w = slot * H + h
             ok = __all_sync(0xffffffffu, mbar_wait(&bar_pq[s], (it >> 1) & 1));
@@ -453,8 +498,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
         bool ok = true;
         int it = 0;
         for (;; ++it) {
-            const int64_t w = (int64_t)worker + (int64_t)it * nworkers;
-            if (w >= W) break;
+            if (it >= n_items) break;
             const int s = it & 1;
             ok = cwait(&bar_ld[s], (it >> 1) & 1);
             if (!ok) break;
@@ -684,30 +728,35 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
             fence_proxy_async();
             csync();
             if (tid == 0) {
-                // [W | U] = (T diag beta) [X | V]: A = the T image read as 128 rows (rows 64-127 are the A
-                // image behind it and land in unused TMEM lanes), B = X and V as one MN-major operand of
-                // 256 columns (the k and v tiles are adjacent)
-                mma_bf16_kmn(tb + TM_DWU, smem_u32(sm + J_TIMG), 128, smem_u32(stg + J_TK), 8192, 4,
-                             idesc_bf16(128, 256, false, true), false);
+                // W = (T diag beta) X: A = the T image read as 128 rows (rows 64-127 are the A image behind
+                // it and land in unused TMEM lanes), B = X (MN-major).  U^T = V^T (T diag beta)^T: A = V
+                // (MN-major, M = d_v), B = the T image (K-major, 64 rows).
+                mma_bf16_kmn(tb + TM_DW, smem_u32(sm + J_TIMG), 128, smem_u32(stg + J_TK), 8192, 4,
+                             idesc_bf16(128, 128, false, true), false);
+                mma_bf16_mnk(tb + TM_DUT, smem_u32(stg + J_TV), 8192, smem_u32(sm + J_TIMG), 64, 4,
+                             idesc_bf16(128, 64, true, false), false);
                 mma_commit(bar_mma);
             }
             ok = cwait(bar_mma, mph & 1);
             ++mph;
             if (!ok) break;
             fence_after_sync();
-            // ---- W and U rows (token-major, TMEM lanes 0-63) into the dead X and V tiles
+            // ---- W rows (token-major, TMEM lanes 0-63) into the dead X tile, U^T rows (value channels,
+            //      all lanes) into the dead V tile
             if ((warp & 3) < 2) {
-                const int r = 32 * (warp & 3) + lane, cq = warp >> 2;  // columns [64 cq, 64 cq + 64)
-                unsigned char *dst = stg + (cq < 2 ? J_TK : J_TV);
+                const int r = 32 * (warp & 3) + lane, cq = warp >> 2;  // columns [32 cq, 32 cq + 32)
+                float d[32];
+                tmem_ld32(tmem_addr(tb + TM_DW, 32 * (warp & 3), 32 * cq), d);
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    float d[32];
-                    tmem_ld32(tmem_addr(tb + TM_DWU, 32 * (warp & 3), 64 * cq + 32 * h2), d);
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        *reinterpret_cast<uint4 *>(dst + img_chunk_off(64, r, 8 * (cq & 1) + 4 * h2 + jj)) =
-                            pack8(d + 8 * jj);
-                }
+                for (int jj = 0; jj < 4; ++jj)
+                    *reinterpret_cast<uint4 *>(stg + J_TK + img_chunk_off(64, r, 4 * cq + jj)) = pack8(d + 8 * jj);
+            }
+            {
+                const int vr = 32 * (warp & 3) + lane, tq = warp >> 2;  // tokens [16 tq, 16 tq + 16)
+                float d[16];
+                tmem_ld16(tmem_addr(tb + TM_DUT, 32 * (warp & 3), 16 * tq), d);
+                *reinterpret_cast<uint4 *>(stg + J_TV + img_chunk_off(128, vr, 2 * tq)) = pack8(d);
+                *reinterpret_cast<uint4 *>(stg + J_TV + img_chunk_off(128, vr, 2 * tq + 1)) = pack8(d + 8);
             }
             fence_proxy_async();
             csync();
@@ -727,7 +776,7 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
                       int *err) {
     extern __shared__ unsigned char smem_raw[];
     intra_role(align1024(smem_raw), tm, beta, bias, A_log, g_min, T, N, cu, chunk_start, H, packets, err,
-               (int)blockIdx.x, (int)gridDim.x, nullptr);
+               (int)blockIdx.x, (int)gridDim.x, nullptr, 0, -1, 0);
 }
 
 constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 9: packet loads; 12-15: output; 10, 11 idle
@@ -735,16 +784,16 @@ constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 9: packet load
 // and V~^T (bf16 pairs per 32-bit column) are the A operands of the MMAs, read from tensor memory, so
 // that the recurrence moves no operand through shared memory.  Per chunk k (one thread of warp 8
 // issues every MMA, in order; D is one of two 128-column buffers):
-//   MMA_U  D  = U^T [-I; 0]^T          D[:, 0:64] = -U^T, D[:, 64:128] = 0     (A = U, MN-major)
-//   MMA1   D += S^T [W; Q^]^T          D[:, 0:64] = (W S - U)^T = -V~^T, D[:, 64:128] = (Q^ S)^T
-//   V~     -D[:, 0:64] as bf16 pairs into tensor memory
+//   MMA1   D = S^T [W; Q^]^T           D[:, 0:64] = (W S)^T, D[:, 64:128] = (Q^ S)^T
+//   V~     V~^T = U^T - D[:, 0:64] (U^T from the packet) as bf16 pairs into tensor memory
 //   MMA3   S^T += V~^T K~              the decay Diag(gamma) was applied to S^T by the CUDA cores
-//   MMA2   D[:, 64:128] += V~^T A^T    O^T = (Q^ S + A V~)^T
 //   S      bf16 copy of S_{k+1}^T, then S^T scaled by gamma_{k+1} (per column)
-// MMA_U needs only the packet and runs ahead of the recurrence; the output warps read O^T of chunk k
-// once its MMAs are done, release the D buffer, and store o through a staging tile and TMA.
+//   MMA2   D[:, 64:128] += V~^T A^T    O^T = (Q^ S + A V~)^T, issued after MMA1 of chunk k + 1 so that
+//                                      the in-order tensor pipe runs it during the next V~ phase
+// The output warps read O^T of chunk k once its MMAs are done, release the D buffer, and store o
+// through a staging tile and TMA.
 // Tensor memory columns: S^T fp32 [0, 128), D buffers [128, 384), bf16 S^T [384, 448), bf16 V~^T
-// [448, 480).
+// buffers [448, 512).
 constexpr uint32_t TM_S = 0, TM_D0 = 128, TM_SB = 384, TM_VT = 448;
 
 // The output pass of segment g, head h in one CTA (threads 0-511).  With `flags`, a packet is loaded
@@ -772,13 +821,14 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lq = warp & 3;           // TMEM lane quarter
     const int v = 32 * lq + lane;      // TMEM lane: d_v channel
-    uint64_t *bar_ld = (uint64_t *)(sm + CS_BAR);  // [2] packet stage loaded
-    uint64_t *bar_o = bar_ld + 2;                  // [2] all MMAs of a chunk done
-    uint64_t *bar_free = bar_ld + 4;               // [2] O^T of a D buffer read by the output warps
-    uint64_t *bar_v = bar_ld + 6;                  // MMA1 done
-    uint64_t *bar_s = bar_ld + 7;                  // MMA3 done
-    uint64_t *bar_sb = bar_ld + 8;                 // bf16 S^T written (one arrival per recurrence warp)
-    uint64_t *bar_vt = bar_ld + 9;                 // V~^T written (one arrival per recurrence warp)
+    uint64_t *bar_ld1 = (uint64_t *)(sm + CS_BAR);  // [2] part 1 of a packet stage loaded
+    uint64_t *bar_ld2 = bar_ld1 + 2;                // [2] part 2 loaded
+    uint64_t *bar_o = bar_ld1 + 4;                  // [2] all MMAs of a chunk done
+    uint64_t *bar_free = bar_ld1 + 6;               // [2] O^T of a D buffer read by the output warps
+    uint64_t *bar_v = bar_ld1 + 8;                  // MMA1 done
+    uint64_t *bar_s = bar_ld1 + 9;                  // MMA3 done
+    uint64_t *bar_sb = bar_ld1 + 10;                // bf16 S^T written (one arrival per recurrence warp)
+    uint64_t *bar_vt = bar_ld1 + 11;                // V~^T written (one arrival per recurrence warp)
     uint32_t *tslot = (uint32_t *)(sm + CS_TSLOT);
     int *s_fail = (int *)(sm + CS_TSLOT + 8);
     const int64_t kk0 = (int64_t)seg_i * seg_len;
@@ -796,7 +846,8 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar_ld[i], 1);
+            mbar_init(&bar_ld1[i], 1);
+            mbar_init(&bar_ld2[i], 1);
             mbar_init(&bar_o[i], 1);
             mbar_init(&bar_free[i], 128);
         }
@@ -806,76 +857,84 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
         mbar_init(bar_vt, 8);
         *s_fail = 0;
     }
-    // [-I; 0]: 128 rows x 64, K-major (one 16 KB swizzled block); 16-byte chunk e holds row e / 8
-    for (int e = tid; e < 1024; e += blockDim.x) {
-        const int r = e >> 3, j = (e & 7) ^ (r & 7);
-        const bool diag = (r < 64 && (r >> 3) == j);
-        const uint32_t m = (r & 1) ? 0xBF800000u : 0x0000BF80u;  // bf16 -1.0 in the half of element r
-        const int wi = (r & 7) >> 1;
-        reinterpret_cast<uint4 *>(sm + CS_NI)[e] =
-            make_uint4(diag && wi == 0 ? m : 0u, diag && wi == 1 ? m : 0u, diag && wi == 2 ? m : 0u,
-                       diag && wi == 3 ? m : 0u);
-    }
     if (warp == 0) tmem_alloc(tslot, 512);
-    fence_proxy_async();  // barrier init and the [-I; 0] image visible to the async proxy
+    fence_proxy_async();  // barrier init visible to the async proxy
     sync_all();
     const uint32_t tb = *tslot;
     auto tDbuf = [&](int kk) { return tb + TM_D0 + 128 * (uint32_t)(kk & 1); };
     auto packet = [&](int kk) { return packets + ((size_t)(c_begin + kk) * H + h) * PK_STRIDE; };
     auto stage = [&](int kk) { return sm + (kk & 1) * CS_ST_BYTES; };
-    auto load_stage = [&](int kk) {  // returns false if the packet was never published
+    auto acquire = [&](int kk) {  // the packet of chunk kk is published (false: it never was)
         if (flags) {
             if (!flag_wait(flags + ((size_t)(c_begin + kk) * H + h))) return false;
             fence_proxy_async_global();
         }
-        uint64_t *b = &bar_ld[kk & 1];
-        mbar_arrive_expect_tx(b, CS_ST_TX);
-        bulk_g2s(stage(kk), packet(kk), CS_ST_TX, b);
         return true;
+    };
+    auto load_part1 = [&](int kk) {
+        uint64_t *b = &bar_ld1[kk & 1];
+        mbar_arrive_expect_tx(b, PK_P1);
+        bulk_g2s(stage(kk), packet(kk), PK_P1, b);
+    };
+    auto load_part2 = [&](int kk) {
+        uint64_t *b = &bar_ld2[kk & 1];
+        mbar_arrive_expect_tx(b, PK_P2);
+        bulk_g2s(stage(kk) + PK_K, packet(kk) + PK_K, PK_P2, b);
     };
 
     if (warp == 8) {
         // ------------------------------------------------ MMA issue (one thread)
         if (lane == 0) {
-            const uint32_t idU = idesc_bf16(128, 128, true, false);   // A = U (MN-major), B = [-I; 0]
             const uint32_t id1 = idesc_bf16(128, 128, false, false);  // A = bf16 S^T, B = [W; Q^] (K-major)
             const uint32_t id3 = idesc_bf16(128, 128, false, true);   // A = V~^T, B = K~ (MN-major)
             const uint32_t id2 = idesc_bf16(128, 64, false, false);   // A = V~^T, B = A (K-major)
             bool ok = true;
+            auto mma2 = [&](int kk) {  // O^T of chunk kk += V~^T A^T
+                mma_ts_k(tDbuf(kk) + 64, tb + TM_VT + 32 * (kk & 1), smem_u32(stage(kk) + PK_A), 64, 4, id2, true);
+                mma_commit(&bar_o[kk & 1]);
+            };
             for (int kk = 0; kk < nc && ok; ++kk) {
                 unsigned char *P = stage(kk);
-                const uint32_t tD = tDbuf(kk);
                 if (kk >= 2) ok = mbar_wait_spin(&bar_free[kk & 1], ((kk >> 1) - 1) & 1);  // O of chunk kk - 2 read
-                ok = ok && mbar_wait_spin(&bar_ld[kk & 1], (kk >> 1) & 1);                // packet kk resident
+                ok = ok && mbar_wait_spin(&bar_ld1[kk & 1], (kk >> 1) & 1);               // part 1 of packet kk
+                ok = ok && mbar_wait_spin(bar_sb, kk & 1);                                  // bf16 S_kk^T written
                 if (!ok) break;
                 fence_after_sync();
-                mma_bf16_mnk(tD, smem_u32(P + PK_U), 8192, smem_u32(sm + CS_NI), 128, 4, idU, false);
-                ok = mbar_wait_spin(bar_sb, kk & 1);  // bf16 S_kk^T written
-                if (!ok) break;
-                fence_after_sync();
-                mma_ts_k(tD, tb + TM_SB, smem_u32(P + PK_WQ), 128, 8, id1, true);
+                mma_ts_k(tDbuf(kk), tb + TM_SB, smem_u32(P + PK_WQ), 128, 8, id1, false);
                 mma_commit(bar_v);
+                if (kk > 0) mma2(kk - 1);
                 ok = mbar_wait_spin(bar_vt, kk & 1);  // V~^T written, S^T scaled by gamma_kk
+                ok = ok && mbar_wait_spin(&bar_ld2[kk & 1], (kk >> 1) & 1);  // part 2 of packet kk
                 if (!ok) break;
                 fence_after_sync();
-                mma_ts_mn(tb + TM_S, tb + TM_VT, smem_u32(P + PK_K), 8192, 4, id3, true);
+                mma_ts_mn(tb + TM_S, tb + TM_VT + 32 * (kk & 1), smem_u32(P + PK_K), 8192, 4, id3, true);
                 mma_commit(bar_s);
-                mma_ts_k(tD + 64, tb + TM_VT, smem_u32(P + PK_A), 64, 4, id2, true);
-                mma_commit(&bar_o[kk & 1]);
             }
+            if (ok && nc > 0) mma2(nc - 1);
             if (!ok) atomicExch(s_fail, 1);
         }
     } else if (warp == 9) {
         // ------------------------------------------------ packet loads (one thread)
         if (lane == 0) {
             bool ok = true;
-            for (int kk = 0; kk < 2 && kk < nc && ok; ++kk) ok = load_stage(kk);
-            if (ok && nc > 2 && !flags) bulk_prefetch_l2(packet(2), CS_ST_TX);
+            for (int kk = 0; kk < 2 && kk < nc && ok; ++kk) {
+                ok = acquire(kk);
+                if (ok) {
+                    load_part1(kk);
+                    load_part2(kk);
+                }
+            }
+            if (ok && nc > 2 && !flags) bulk_prefetch_l2(packet(2), PK_STRIDE);
             for (int kk = 0; kk + 2 < nc && ok; ++kk) {
-                ok = mbar_wait(&bar_o[kk & 1], (kk >> 1) & 1);  // all MMAs of chunk kk done: its stage takes kk + 2
+                // MMA_U and MMA1 of chunk kk done and gamma_kk read (V~^T of chunk kk written): part 1 of
+                // its stage takes chunk kk + 2
+                ok = mbar_wait_spin(bar_vt, kk & 1) && acquire(kk + 2);
                 if (!ok) break;
-                ok = load_stage(kk + 2);
-                if (ok && kk + 3 < nc && !flags) bulk_prefetch_l2(packet(kk + 3), CS_ST_TX);
+                load_part1(kk + 2);
+                ok = mbar_wait_spin(&bar_o[kk & 1], (kk >> 1) & 1);  // all MMAs of chunk kk done: part 2
+                if (!ok) break;
+                load_part2(kk + 2);
+                if (kk + 3 < nc && !flags) bulk_prefetch_l2(packet(kk + 3), PK_STRIDE);
             }
             if (!ok) atomicExch(s_fail, 1);
         }
@@ -937,7 +996,7 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
         // d_k columns [64 j, 64 j + 64) of S^T and tokens [32 j, 32 j + 32) of V~^T
         const int j = warp >> 2;
         bool ok = true;
-        if (nc > 0) ok = mbar_wait_spin(&bar_ld[0], 0);
+        if (nc > 0) ok = mbar_wait_spin(&bar_ld1[0], 0);
         // S_0^T, 32 columns at a time: bf16 copy, and the fp32 state scaled by gamma_0
 #pragma unroll 1
         for (int h2 = 0; h2 < 2 && ok; ++h2) {
@@ -967,17 +1026,29 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
         __syncwarp();
         if (lane == 0 && nc > 0 && ok) mbar_arrive(bar_sb);
         for (int kk = 0; kk < nc && ok; ++kk) {
-            // invariant: packet kk resident; bf16 S_kk^T written; TMEM S^T = (Diag(gamma_kk) S_kk)^T
+            // invariant: part 1 of packet kk resident; bf16 S_kk^T written; TMEM S^T = (Diag(gamma_kk) S_kk)^T
+            uint4 ua[4];  // U^T row v, tokens [32 j, 32 j + 32), read before MMA1 is done
+            {
+                const unsigned char *ut = stage(kk) + PK_U + v * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) ua[q] = *reinterpret_cast<const uint4 *>(ut + (((4 * j + q) ^ (v & 7)) << 4));
+            }
             ok = mbar_wait_spin(bar_v, kk & 1) && (*(volatile int *)s_fail == 0);
             if (!ok) break;
             fence_after_sync();
-            {
+            {  // V~^T row v, tokens [32 j, 32 j + 32) = U^T - (W S)^T
                 float d[32];
                 tmem_ld32(tmem_addr(tDbuf(kk), 32 * lq, 32 * j), d);
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(-d[2 * i], -d[2 * i + 1]);
-                tmem_st16u(tmem_addr(tb + TM_VT, 32 * lq, 16 * j), pk);
+                for (int q = 0; q < 4; ++q) {
+                    float u[8];
+                    unpack8(ua[q], u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        pk[4 * q + e] = pack_bf16(u[2 * e] - d[8 * q + 2 * e], u[2 * e + 1] - d[8 * q + 2 * e + 1]);
+                }
+                tmem_st16u(tmem_addr(tb + TM_VT + 32 * (kk & 1), 32 * lq, 16 * j), pk);
                 tmem_st_wait();
             }
             fence_before_sync();
@@ -985,12 +1056,12 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
             if (lane == 0) mbar_arrive(bar_vt);
             const bool last = (kk == nc - 1);
             ok = mbar_wait_spin(bar_s, kk & 1);
-            if (ok && !last) ok = mbar_wait_spin(&bar_ld[(kk + 1) & 1], ((kk + 1) >> 1) & 1);
             if (!ok) break;
             fence_after_sync();
             if (!last) {
                 // bf16 S_{kk+1}^T first (MMA1 of the next chunk waits for it), then the fp32 copy scaled
-                // by gamma_{kk+1} (MMA3 of the next chunk, issued after this warp's next V~, needs it)
+                // by gamma_{kk+1} from packet kk + 1 (MMA3 of the next chunk, issued after this warp's next
+                // V~, needs it)
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int c0 = 64 * j + 32 * h2;
@@ -1005,6 +1076,8 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_sb);
+                ok = mbar_wait_spin(&bar_ld1[(kk + 1) & 1], ((kk + 1) >> 1) & 1);
+                if (!ok) break;
                 const float *gam = reinterpret_cast<const float *>(stage(kk + 1) + PK_G);
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
@@ -1058,16 +1131,23 @@ chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant
                       float g_min, int64_t T, int N, const int32_t *__restrict__ cu,
                       const int32_t *__restrict__ chunk_start, const int32_t *__restrict__ seg_start, int H,
                       unsigned char *__restrict__ packets, float scale, const float *initial_state,
-                      float *final_state, bf16 *__restrict__ o, int *err, int n_chain, int *flags) {
+                      float *final_state, bf16 *__restrict__ o, int *err, int n_chain, int *flags, int kpre) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1024(smem_raw);
     const int b = (int)blockIdx.x;
-    if (b < n_chain)
+    if (b < n_chain) {
+        // the chain of (sequence b / H, head b % H) first produces its own first kpre chunks
+        if (kpre > 0) {
+            intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, chunk_start, H, packets, err, 0, 1, flags, kpre,
+                       b / H, b % H);
+            __syncthreads();
+        }
         chain_role(sm, omap, T, N, cu, chunk_start, seg_start, (int64_t)1 << 30, nullptr, H, packets, scale,
                    initial_state, final_state, o, err, b / H, b % H, flags);
-    else
+    } else {
         intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, chunk_start, H, packets, err, b - n_chain,
-                   (int)gridDim.x - n_chain, flags);
+                   (int)gridDim.x - n_chain, flags, kpre, -1, 0);
+    }
 }
 
 // =====================================================================================
@@ -1082,7 +1162,7 @@ chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant
 // S~ and M are independent chains (N = 128 each) run by separate warp groups.
 // A stage holds [W half 0 | K~ half 0 | W half 1 | K~ half 1 | gamma]: read as a 128-row K-major image
 // it is W (rows 64-127 are K~ and land in unused lanes); K~ is read MN-major with its halves 16 KB
-// apart.  U goes from global memory to registers one chunk ahead.
+// apart.  U (kept as U^T in the packet) goes from global memory to registers one chunk ahead.
 constexpr uint32_t SS_NST = 3;
 constexpr uint32_t SS_STAGE_BYTES = 33792;
 constexpr uint32_t SS_G = 32768;
@@ -1179,11 +1259,20 @@ chunk_segsum_tc_kernel(int N, const int32_t *__restrict__ chunk_start, const int
     // U row `row` (a token), columns [64 cg, 64 cg + 64) for warps with lq < 2 and cg < 2
     const bool vrow = (lq < 2), uneed = vrow && (cg < 2);
     uint4 ua[8];
-    auto load_u = [&](int kk) {
+    auto load_u = [&](int kk) {  // from the U^T image (rows are channels): one bf16 per load, coalesced
         const unsigned char *src = packet(kk) + PK_U;
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-            ua[jj] = __ldg(reinterpret_cast<const uint4 *>(src + img_chunk_off(64, row, 8 * cg + jj)));
+        for (int jj = 0; jj < 8; ++jj) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = 64 * cg + 8 * jj + 2 * e;
+                const uint32_t lo = __ldg(reinterpret_cast<const unsigned short *>(src + img_off(128, c, row)));
+                const uint32_t hi = __ldg(reinterpret_cast<const unsigned short *>(src + img_off(128, c + 1, row)));
+                w[e] = lo | (hi << 16);
+            }
+            ua[jj] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
     };
     if (uneed && nc > 0) load_u(0);
     const uint32_t id1 = idesc_bf16(128, 128, false, true), id2 = idesc_bf16(128, 128, true, true);
@@ -1490,8 +1579,9 @@ static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void 
     const int32_t *cu = a->cu_seqlens;
     float *fin = a->final_state;
     bf16 *o = (bf16 *)a->o;
+    int kpre = p.kpre;
     void *args[] = {(void *)&tm, (void *)&omap, &beta, &bias, &A_log, &g_min, &T, &N, &cu, &chunk_start,
-                    &seg_start, &H, &packets, &scale, &init, &fin, &o, &err, &n_chain, &flags};
+                    &seg_start, &H, &packets, &scale, &init, &fin, &o, &err, &n_chain, &flags, &kpre};
     if (cudaLaunchCooperativeKernel((const void *)tcp::chunk_fused_tc_kernel, dim3((unsigned)sms), dim3(tcp::NT2),
                                     args, smem, stream) != cudaSuccess) {
         (void)cudaGetLastError();

@@ -14,6 +14,7 @@ kda_status_t kda_launch_gate(const kda_gate_args *a, cudaStream_t stream);
 kda_status_t kda_launch_decode(const kda_step_args *a, cudaStream_t stream);
 
 // Chunked prefill.  Workspace layout is owned by kda_chunk_plan.cu.
+constexpr int KDA_FUSED_MAX_SEQS = 159;  // sequences the fused schedule's producer item map holds
 struct kda_chunk_plan {
     int64_t T, N;
     int H, dk, dv, C;
@@ -36,7 +37,8 @@ struct kda_chunk_plan {
     // Fused launch (tensor-core path, no split): the output pass of every (sequence, head) and the
     // intra-chunk work run concurrently in one cooperative launch; packets are published through
     // int32 flags, one per (chunk slot, head).
-    int fused;
+    int fused;               // (at most KDA_FUSED_MAX_SEQS sequences)
+    int kpre;                // fused: chunks at the start of every sequence that its chains produce themselves
     size_t off_flags;
     size_t total_bytes;
 };

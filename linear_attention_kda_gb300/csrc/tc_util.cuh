@@ -174,11 +174,12 @@ __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence
 // Makes generic-proxy shared-memory writes visible to the async proxy (MMA, bulk copies).
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// TMEM allocation: executed by one full warp.
-__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+// TMEM allocation: executed by one full warp.  With `relinquish`, the CTA then gives up the right
+// to allocate again (other CTAs on the SM need not wait for it).
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols, bool relinquish = true) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (relinquish) asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
