@@ -362,7 +362,7 @@ def run_ours(args, rank, ws, local):
     by = prefill_bytes(T, N, H, D, D, 2, False, True)
     tflops = fl["total"] / (ms / 1e3) / 1e12
     kern_avg = [sum(x) / len(x) for x in kern_ms]
-    names = {2: ["chunk_plan", "chunk_fused"], 3: ["chunk_plan", "chunk_intra", "chunk_inter"],
+    names = {1: ["chunk_fused"], 3: ["chunk_plan", "chunk_intra", "chunk_inter"],
              5: ["chunk_plan", "chunk_intra", "chunk_segsum", "chunk_fold", "chunk_inter"]}[nk]
     dom = max(range(nk), key=lambda j: kern_avg[j])
     role = {"chunk_intra": "intra", "chunk_fused": "total"}.get(names[dom], "inter")

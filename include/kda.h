@@ -212,6 +212,16 @@ int kda_abi_version(void);
 kda_status_t kda_set_profile_events(void *const *events, int32_t n_events);
 int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *args);
 
+/* The schedule kda_chunk_fwd picks for these arguments (host only: reads the
+ * sizes, dtype and cu_seqlens_host, launches nothing).  out (caller-owned, 4
+ * entries): out[0] = 1 for the fused launch (intra-chunk transform and output
+ * pass in one cooperative kernel), else 0; out[1] = chunks at the start of every
+ * sequence that its own output-pass CTAs produce in the fused launch; out[2] =
+ * segment length in chunks of the split-sequence state pass (section 5.1.2,
+ * Eq. 17 of the Kimi Linear report), 0 when the pass does not run; out[3] =
+ * kernels launched.  KDA_ERR_INVALID_ARG on NULL pointers or invalid sizes. */
+kda_status_t kda_chunk_fwd_schedule(const kda_chunk_args *args, int64_t *out);
+
 #ifdef __cplusplus
 }
 #endif

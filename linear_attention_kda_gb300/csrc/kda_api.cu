@@ -81,10 +81,22 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
     if (!kda_make_chunk_plan(a->T, a->N > 0 ? a->N : 1, a->H > 0 ? a->H : 1, a->dk, a->dv, a->dtype, 64, &p,
                              a->cu_seqlens_host))
         return 0;
-    // chunk plan, then either one fused launch (intra-chunk transform and output pass together) or
-    // intra-chunk transform, [segment summaries, fold,] output pass
-    if (p.fused) return 2;
+    // either one fused launch (intra-chunk transform and output pass together) or the chunk plan,
+    // then intra-chunk transform, [segment summaries, fold,] output pass
+    if (p.fused) return 1;
     return p.split ? 5 : 3;
+}
+
+kda_status_t kda_chunk_fwd_schedule(const kda_chunk_args *a, int64_t *out) {
+    if (!a || !out || a->T < 0 || a->N < 1 || a->H < 1) return KDA_ERR_INVALID_ARG;
+    kda_chunk_plan p;
+    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p, a->cu_seqlens_host))
+        return KDA_ERR_INVALID_ARG;
+    out[0] = p.fused;
+    out[1] = p.fused ? p.kpre : 0;
+    out[2] = p.split ? p.seg_len : 0;
+    out[3] = kda_chunk_fwd_kernel_count(a);
+    return KDA_OK;
 }
 
 const char *kda_status_string(kda_status_t s) {

@@ -237,7 +237,7 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
         end = p->off_seg_in + (size_t)p->max_segs * H * 128 * 128 * sizeof(float);
     }
     p->off_flags = align_up(end, 256);
-    end = p->off_flags + sizeof(int32_t) * (size_t)p->max_chunks * (size_t)H;
+    end = p->off_flags + sizeof(uint64_t) * (size_t)p->max_chunks * (size_t)H;
     p->total_bytes = align_up(end, 256);
     return true;
 }

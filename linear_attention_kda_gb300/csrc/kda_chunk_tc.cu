@@ -26,6 +26,9 @@
 
 #include <cuda.h>
 
+#include <atomic>
+#include <chrono>
+
 namespace kda {
 namespace tcp {
 
@@ -192,7 +195,9 @@ constexpr uint32_t J_BAR = J_INFO + 128;    // ld[2], pq[2], pw[2], mma, rd
 constexpr uint32_t J_TSLOT = J_BAR + 64;
 constexpr uint32_t J_TBL = J_BAR + 128;     // int32 [J_TBL_N + 1]: producer chunks before each sequence
 constexpr int J_TBL_N = KDA_FUSED_MAX_SEQS;  // sequences the table holds
-constexpr uint32_t J_TOTAL = J_TBL + 4 * (J_TBL_N + 1) + 1024;
+constexpr uint32_t J_CS = J_TBL + 4 * (J_TBL_N + 1);  // fused launch: chunk_start [N + 1]
+constexpr uint32_t J_SS = J_CS + 4 * (J_TBL_N + 1);   //               seg_start [N + 1], then a flag
+constexpr uint32_t J_TOTAL = J_SS + 4 * (J_TBL_N + 2) + 1024;
 // TMEM columns: A / L product (96); later [W | U] (256, lanes 0-63)
 constexpr uint32_t TM_DA = 0, TM_DB = 32, TM_DW = 0, TM_DUT = 128;
 
@@ -319,21 +324,23 @@ __device__ __forceinline__ void element_pass(unsigned char *sm, unsigned char *s
 // Packet publication between CTAs of one (cooperative) launch: the producer releases a flag once the
 // packet's bulk writes have completed; the consumer acquires it before its bulk reads.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-__device__ __forceinline__ void flag_release(int *f) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" :: "l"(f), "r"(1) : "memory");
+// Flags hold the epoch of the launch that published them (a per-process counter that never repeats),
+// so a workspace needs no clearing between launches.
+__device__ __forceinline__ void flag_release(uint64_t *f, uint64_t epoch) {
+    asm volatile("st.release.gpu.global.b64 [%0], %1;" :: "l"(f), "l"(epoch) : "memory");
 }
-__device__ __forceinline__ int flag_acquire(const int *f) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+__device__ __forceinline__ uint64_t flag_acquire(const uint64_t *f) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
     return v;
 }
-// Bounded wait (~1 s) for a packet flag.
-__device__ __forceinline__ bool flag_wait(const int *f) {
-    if (flag_acquire(f)) return true;
+// Bounded wait (~1 s) for a packet flag to reach this launch's epoch.
+__device__ __forceinline__ bool flag_wait(const uint64_t *f, uint64_t epoch) {
+    if (flag_acquire(f) == epoch) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         for (int i = 0; i < 64; ++i)
-            if (flag_acquire(f)) return true;
+            if (flag_acquire(f) == epoch) return true;
         if (globaltimer_ns() - t0 > 1000000000ull) return false;
     }
 }
@@ -343,14 +350,14 @@ __device__ __forceinline__ bool flag_wait(const int *f) {
 //  - own_n < 0, kpre > 0: the same over the items left once the first kpre chunks of every
 //    sequence are taken away (in the same order);
 //  - own_n >= 0: the first kpre chunks of sequence own_n for head own_h.
-// With `flags`, each item's packet is published (flags[item] = 1) once its writes have completed.
+// With `flags`, each item's packet is published (flags[item] = epoch) once its writes have completed.
 // In the last mode the CTA keeps its right to allocate tensor memory (its chain runs next).
 __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm, const bf16 *__restrict__ beta,
                                            const float *__restrict__ bias, const float *__restrict__ A_log,
                                            float g_min, int64_t T, int N, const int32_t *__restrict__ cu,
                                            const int32_t *__restrict__ chunk_start, int H,
                                            unsigned char *__restrict__ packets, int *err, int worker, int nworkers,
-                                           int *flags, int kpre, int own_n, int own_h) {
+                                           uint64_t *flags, uint64_t epoch, int kpre, int own_n, int own_h) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t *tbl = (int32_t *)(sm + J_TBL);  // kpre > 0: tbl[n] = producer chunks of sequences before n
     int n_items = 0;
@@ -485,7 +492,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
                 bulk_wait0();
                 if (flags) {
                     fence_proxy_async_global();
-                    flag_release(flags + w);
+                    flag_release(flags + w, epoch);
                 }
             }
             __syncwarp();
@@ -776,7 +783,7 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
                       int *err) {
     extern __shared__ unsigned char smem_raw[];
     intra_role(align1024(smem_raw), tm, beta, bias, A_log, g_min, T, N, cu, chunk_start, H, packets, err,
-               (int)blockIdx.x, (int)gridDim.x, nullptr, 0, -1, 0);
+               (int)blockIdx.x, (int)gridDim.x, nullptr, 0, 0, -1, 0);
 }
 
 constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 9: packet loads; 12-15: output; 10, 11 idle
@@ -804,7 +811,7 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                                            const float *__restrict__ seg_in, int H,
                                            const unsigned char *__restrict__ packets, float scale,
                                            const float *initial_state, float *final_state, bf16 *__restrict__ o,
-                                           int *err, int g, int h, const int *flags) {
+                                           int *err, int g, int h, const uint64_t *flags, uint64_t epoch) {
     // segment g of sequence n, head h: chunks [kk0, kk0 + nc) of the sequence
     if (g >= seg_start[N]) return;
     int n = 0;
@@ -866,7 +873,7 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
     auto stage = [&](int kk) { return sm + (kk & 1) * CS_ST_BYTES; };
     auto acquire = [&](int kk) {  // the packet of chunk kk is published (false: it never was)
         if (flags) {
-            if (!flag_wait(flags + ((size_t)(c_begin + kk) * H + h))) return false;
+            if (!flag_wait(flags + ((size_t)(c_begin + kk) * H + h), epoch)) return false;
             fence_proxy_async_global();
         }
         return true;
@@ -1116,37 +1123,77 @@ chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N
                       float *final_state, bf16 *__restrict__ o, int *err) {
     extern __shared__ unsigned char smem_raw[];
     chain_role(align1024(smem_raw), omap, T, N, cu, chunk_start, seg_start, seg_len, seg_in, H, packets, scale,
-               initial_state, final_state, o, err, (int)blockIdx.x, (int)blockIdx.y, nullptr);
+               initial_state, final_state, o, err, (int)blockIdx.x, (int)blockIdx.y, nullptr, 0);
 }
 
 // =====================================================================================
 // Intra-chunk work and the output pass in one launch, for inputs whose chains (one per sequence and
-// head) are few: CTAs [0, n_chain) run the chains (no segment split), the others produce packets in
-// chunk order and publish them through `flags`; a chain waits for each packet before loading it.
-// Launched cooperatively, so every CTA is resident and the producers always make progress; every
-// wait is bounded.
+// head) are few: CTAs [0, n_chain) run the chains (no segment split), each first producing the first
+// kpre chunks of its own sequence and head; the others produce the remaining packets in chunk order
+// and publish them through `flags`; a chain waits for each packet before loading it.  Every CTA
+// derives the chunk layout from cu_seqlens itself (at most KDA_FUSED_MAX_SEQS sequences), so the launch
+// needs no planning kernel.  Launched cooperatively, so every CTA is resident and the producers always
+// make progress; every wait is bounded.
 __global__ void __launch_bounds__(NT2, 1)
 chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant__ CUtensorMap omap,
                       const bf16 *__restrict__ beta, const float *__restrict__ bias, const float *__restrict__ A_log,
-                      float g_min, int64_t T, int N, const int32_t *__restrict__ cu,
-                      const int32_t *__restrict__ chunk_start, const int32_t *__restrict__ seg_start, int H,
+                      float g_min, int64_t T, int N, const int32_t *__restrict__ cu, int H,
                       unsigned char *__restrict__ packets, float scale, const float *initial_state,
-                      float *final_state, bf16 *__restrict__ o, int *err, int n_chain, int *flags, int kpre) {
+                      float *final_state, bf16 *__restrict__ o, int *err, int n_chain, uint64_t *flags,
+                      uint64_t epoch, int kpre) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1024(smem_raw);
-    const int b = (int)blockIdx.x;
+    const int b = (int)blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int32_t *cs = (int32_t *)(sm + J_CS);  // chunk_start [N + 1]
+    int32_t *ss = (int32_t *)(sm + J_SS);  // seg_start [N + 1]: one segment per sequence
+    int *s_bad = (int *)(sm + J_SS + 4 * (J_TBL_N + 1));
+    if (warp == 0) {  // validate cu_seqlens (0 = c_0 <= ... <= c_N = T) and count chunks per sequence
+        bool bad = false;
+        if (cu) {
+            for (int n = lane; n <= N; n += 32) {
+                const int64_t x = cu[n];
+                bad = bad || (n == 0 && x != 0) || (n == N && x != T) || (n > 0 && x < (int64_t)cu[n - 1]);
+            }
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        int carry = 0;
+        for (int base = 0; base < N; base += 32) {
+            const int m = base + lane;
+            int x = 0;
+            if (m < N && !bad) {
+                const int64_t len = cu ? (int64_t)cu[m + 1] - cu[m] : T / N;
+                x = (int)((len + C - 1) / C);
+            }
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            if (m < N) cs[m + 1] = carry + x;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        for (int n = lane; n <= N; n += 32) ss[n] = n;
+        if (lane == 0) {
+            cs[0] = 0;
+            *s_bad = bad ? 1 : 0;
+        }
+    }
+    __syncthreads();
+    if (*(volatile int *)s_bad) {
+        if (b == 0 && tid == 0) set_error(err, KDA_ERR_BAD_SEQLENS);
+        return;
+    }
     if (b < n_chain) {
-        // the chain of (sequence b / H, head b % H) first produces its own first kpre chunks
         if (kpre > 0) {
-            intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, chunk_start, H, packets, err, 0, 1, flags, kpre,
+            intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, cs, H, packets, err, 0, 1, flags, epoch, kpre,
                        b / H, b % H);
             __syncthreads();
         }
-        chain_role(sm, omap, T, N, cu, chunk_start, seg_start, (int64_t)1 << 30, nullptr, H, packets, scale,
-                   initial_state, final_state, o, err, b / H, b % H, flags);
+        chain_role(sm, omap, T, N, cu, cs, ss, (int64_t)1 << 30, nullptr, H, packets, scale, initial_state,
+                   final_state, o, err, b / H, b % H, flags, epoch);
     } else {
-        intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, chunk_start, H, packets, err, b - n_chain,
-                   (int)gridDim.x - n_chain, flags, kpre, -1, 0);
+        intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, cs, H, packets, err, b - n_chain,
+                   (int)gridDim.x - n_chain, flags, epoch, kpre, -1, 0);
     }
 }
 
@@ -1559,6 +1606,7 @@ static kda_status_t set_smem(const void *kernel, uint32_t bytes) {
 // separate kernels, which need the same workspace.
 static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws, cudaStream_t stream,
                          const tcp::TileMaps &tm, const CUtensorMap &omap, int sms, int *err) {
+    static std::atomic<uint64_t> next_epoch{0};
     const uint32_t smem = tcp::J_TOTAL > tcp::CS_TOTAL ? tcp::J_TOTAL : tcp::CS_TOTAL;
     if (set_smem((const void *)tcp::chunk_fused_tc_kernel, smem) != KDA_OK) return false;
     int per_sm = 0;
@@ -1566,22 +1614,24 @@ static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void 
             cudaSuccess ||
         per_sm < 1)
         return false;
-    int *flags = (int *)((char *)ws + p.off_flags);
-    if (cudaMemsetAsync(flags, 0, sizeof(int) * (size_t)p.max_chunks * p.H, stream) != cudaSuccess) return false;
-    const int32_t *chunk_start = (const int32_t *)((char *)ws + p.off_chunk_start);
-    const int32_t *seg_start = (const int32_t *)((char *)ws + p.off_seg_start);
+    uint64_t expected = 0;  // first use: start the epochs at a value unlikely to sit in fresh memory
+    if (next_epoch.load() == 0)
+        next_epoch.compare_exchange_strong(
+            expected, ((uint64_t)std::chrono::steady_clock::now().time_since_epoch().count() << 20) | 1u);
+    uint64_t epoch = next_epoch.fetch_add(1);
+    if (epoch == 0) epoch = next_epoch.fetch_add(1);
+    uint64_t *flags = (uint64_t *)((char *)ws + p.off_flags);
     unsigned char *packets = (unsigned char *)ws + p.off_records;
     const bf16 *beta = (const bf16 *)a->beta;
     const float *bias = a->dt_bias, *A_log = a->A_log, *init = a->initial_state;
     float g_min = a->g_min, scale = a->scale;
     int64_t T = a->T;
-    int N = (int)a->N, H = p.H, n_chain = (int)(a->N * p.H);
+    int N = (int)a->N, H = p.H, n_chain = (int)(a->N * p.H), kpre = p.kpre;
     const int32_t *cu = a->cu_seqlens;
     float *fin = a->final_state;
     bf16 *o = (bf16 *)a->o;
-    int kpre = p.kpre;
-    void *args[] = {(void *)&tm, (void *)&omap, &beta, &bias, &A_log, &g_min, &T, &N, &cu, &chunk_start,
-                    &seg_start, &H, &packets, &scale, &init, &fin, &o, &err, &n_chain, &flags, &kpre};
+    void *args[] = {(void *)&tm, (void *)&omap, &beta, &bias, &A_log, &g_min, &T, &N, &cu, &H, &packets,
+                    &scale, &init, &fin, &o, &err, &n_chain, &flags, &epoch, &kpre};
     if (cudaLaunchCooperativeKernel((const void *)tcp::chunk_fused_tc_kernel, dim3((unsigned)sms), dim3(tcp::NT2),
                                     args, smem, stream) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -1594,10 +1644,6 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
                                  cudaStream_t stream) {
     int *err = kda_device_error_ptr();
     if (!err) return KDA_ERR_CUDA;
-    kda_profile_mark(0, stream);
-    kda_status_t st = kda_launch_chunk_plan(a, p, ws, stream);
-    if (st != KDA_OK) return st;
-    kda_profile_mark(1, stream);
     const int32_t *chunk_start = (const int32_t *)((char *)ws + p.off_chunk_start);
     unsigned char *packets = (unsigned char *)ws + p.off_records;
     int dev = 0, sms = 0;
@@ -1609,10 +1655,15 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
         !make_tile_map(&tm.v, a->v, a->T, p.H) || !make_tile_map(&tm.z, a->z, a->T, p.H) ||
         !make_tile_map(&omap, a->o, a->T, p.H))
         return KDA_ERR_CUDA;
+    kda_profile_mark(0, stream);
     if (p.fused && p.max_chunks > 0 && a->T > 0 && launch_fused(a, p, ws, stream, tm, omap, sms, err)) {
-        kda_profile_mark(2, stream);
+        kda_profile_mark(1, stream);
         return kda_cuda_status(cudaGetLastError());
     }
+    // separate kernels (also the fallback when the fused launch cannot make every CTA resident)
+    kda_status_t st = kda_launch_chunk_plan(a, p, ws, stream);
+    if (st != KDA_OK) return st;
+    kda_profile_mark(1, stream);
     if (p.max_chunks > 0 && a->T > 0) {
         st = set_smem((const void *)tcp::chunk_intra_tc_kernel, tcp::J_TOTAL);
         if (st != KDA_OK) return st;

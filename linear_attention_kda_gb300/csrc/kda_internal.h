@@ -35,8 +35,8 @@ struct kda_chunk_plan {
                              // high and low operand images (32 KB each)
     size_t off_seg_in;       // per (segment, head): entering state S [128][128] fp32 (lane-major)
     // Fused launch (tensor-core path, no split): the output pass of every (sequence, head) and the
-    // intra-chunk work run concurrently in one cooperative launch; packets are published through
-    // int32 flags, one per (chunk slot, head).
+    // intra-chunk work run concurrently in one cooperative launch (no planning kernel); packets are
+    // published through 64-bit epoch flags, one per (chunk slot, head).
     int fused;               // (at most KDA_FUSED_MAX_SEQS sequences)
     int kpre;                // fused: chunks at the start of every sequence that its chains produce themselves
     size_t off_flags;

@@ -27,7 +27,7 @@ _STATUS = {
 EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step",
             "kda_status_string", "kda_get_device_error", "kda_abi_version",
             "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws",
-            "kda_last_cuda_error"]
+            "kda_last_cuda_error", "kda_chunk_fwd_schedule"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 _vp = ctypes.c_void_p
@@ -93,6 +93,8 @@ def load_library(path: Optional[str] = None):
         L.kda_set_profile_events.restype = ctypes.c_int
         L.kda_chunk_fwd_kernel_count.argtypes = [ctypes.POINTER(ChunkArgs)]
         L.kda_chunk_fwd_kernel_count.restype = _i32
+        L.kda_chunk_fwd_schedule.argtypes = [ctypes.POINTER(ChunkArgs), ctypes.POINTER(_i64)]
+        L.kda_chunk_fwd_schedule.restype = ctypes.c_int
         L.kda_chunk_fwd_static_ws.argtypes = [ctypes.POINTER(ChunkArgs), _vp]
         L.kda_chunk_fwd_static_ws.restype = ctypes.c_int
         L.kda_last_cuda_error.argtypes = []
@@ -230,6 +232,18 @@ def chunk_fwd_kernel_count(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, 
     a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=KDA_BF16 if dtype == torch.bfloat16 else KDA_F32,
                   cu_seqlens_host=None if cu is None else cu.data_ptr(), chunk_size=64)
     return int(load_library().kda_chunk_fwd_kernel_count(ctypes.byref(a)))
+
+
+def chunk_fwd_schedule(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, cu_seqlens_host=None) -> dict:
+    """The schedule kda_chunk_fwd picks for these sizes (see kda_chunk_fwd_schedule in kda.h)."""
+    cu = None
+    if cu_seqlens_host is not None:
+        cu = cu_seqlens_host.to(dtype=torch.int32, device="cpu").contiguous()
+    a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=KDA_BF16 if dtype == torch.bfloat16 else KDA_F32,
+                  cu_seqlens_host=None if cu is None else cu.data_ptr(), chunk_size=64)
+    out = (_i64 * 4)()
+    _check(load_library().kda_chunk_fwd_schedule(ctypes.byref(a), out), "kda_chunk_fwd_schedule")
+    return {"fused": bool(out[0]), "own_chunks": int(out[1]), "seg_len": int(out[2]), "kernels": int(out[3])}
 
 
 def chunk_fwd_static_ws(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0,

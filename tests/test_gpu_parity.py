@@ -208,6 +208,30 @@ def test_zero_state_identity_gate_limits():
     assert rel_err(o.float().cpu().numpy(), o_ref.numpy()) <= TOL_BF16
 
 
+def test_fused_schedule_varlen_own_chunks():
+    """Fused launch on a batch with an empty sequence where each chain first produces its own first
+    chunks and the producers take the rest (their item map skips those chunks per sequence)."""
+    w = syn.Workload("f", H=16, d=128, dtype="bf16", seq_len=None, z_std=1.5, b_range=1.0,
+                     alog_std=0.25, s0_std=0.02)
+    d = _varlen(w, [1000, 0, 700, 5], seed=23)
+    sch = kda.chunk_fwd_schedule(sum(d["lengths"]), 4, 16, 128, 128, torch.bfloat16, d["cu_seqlens"])
+    assert sch["fused"] and sch["own_chunks"] >= 1 and sch["kernels"] == 1
+    o, fs = run_prefill(d)
+    compare_prefill(d, o, fs, oracle_prefill(d), TOL_BF16)
+
+
+def test_fused_bad_cu_seqlens_reports_device_error():
+    """The fused launch validates cu_seqlens itself (no planning kernel runs before it)."""
+    w = syn.Workload("e", H=2, d=128, dtype="bf16", seq_len=64)
+    d = syn.make_prefill(w, seed=1)
+    cu = torch.tensor([0, 40, 30, 64], dtype=torch.int32)
+    assert kda.chunk_fwd_schedule(64, 3, 2, 128, 128, torch.bfloat16, None)["fused"]
+    dev = "cuda"
+    kda.chunk_fwd(*(d[n].to(dev) for n in ("q", "k", "v", "z", "beta")), None, None, cu_seqlens=cu.to(dev),
+                  output_final_state=True)
+    assert kda.get_device_error() == 7
+
+
 def test_bad_cu_seqlens_reports_device_error():
     w = syn.Workload("e", H=1, d=64, dtype="f32", seq_len=64)
     d = syn.make_prefill(w, seed=1)
