@@ -57,7 +57,7 @@ constexpr uint32_t PK_P2 = PK_STRIDE - PK_K;  // bytes of part 2 (at PK_K)
 // the packet after them is prefetched into L2.
 constexpr uint32_t CS_ST_BYTES = PK_STRIDE;            // stage stride (multiple of 1024)
 constexpr uint32_t CS_OIMG = 2 * CS_ST_BYTES;          // o staging, 2 buffers x (64 tokens x 128, 2 x 8 KB)
-constexpr uint32_t CS_BAR = CS_OIMG + 32768;           // 12 mbarriers
+constexpr uint32_t CS_BAR = CS_OIMG + 32768;           // 13 mbarriers
 constexpr uint32_t CS_TSLOT = CS_BAR + 128;            // TMEM base, failure flag
 constexpr uint32_t CS_TOTAL = CS_BAR + 192 + 1024;
 static_assert(PK_P1 <= PK_K && PK_P1 % 16 == 0 && PK_P2 % 16 == 0, "packet parts");
@@ -243,9 +243,9 @@ __device__ __forceinline__ bool cwait(uint64_t *bar, uint32_t parity) {
     return csync_and(ok);
 }
 
-// Partial products of the block merges of the UT-transform inverse.  Level 1: P[q + 4 a][jc] =
+// Partial products of the level-1 block merges of the UT-transform inverse: P[q + 4 a][jc] =
 // L[ro + q + 4 a][co .. co + 15] . T[co .. co + 15][co + jc], starting at column K0 <= jc (T is zero
-// above the diagonal).  Level 2: the lower-left 32 x 32 block, rows 32 + q + 16 a.
+// above the diagonal).
 template <int K0>
 __device__ __forceinline__ void inv_l1_partial(const float *Lm, const float *Tm, int ro, int co, int q, int jc,
                                                float *p) {
@@ -258,23 +258,6 @@ __device__ __forceinline__ void inv_l1_partial(const float *Lm, const float *Tm,
         float acc = 0.f;
 #pragma unroll
         for (int k = K0; k < 16; k += 4) {
-            const float4 l4 = *reinterpret_cast<const float4 *>(lr + k);
-            acc += l4.x * tc[k] + l4.y * tc[k + 1] + l4.z * tc[k + 2] + l4.w * tc[k + 3];
-        }
-        p[a] = acc;
-    }
-}
-template <int K0>
-__device__ __forceinline__ void inv_l2_partial(const float *Lm, const float *Tm, int q, int jc, float *p) {
-    float tc[32];
-#pragma unroll
-    for (int k = K0; k < 32; ++k) tc[k] = Tm[k * LS + jc];
-#pragma unroll
-    for (int a = 0; a < 2; ++a) {
-        const float *lr = Lm + (32 + q + 16 * a) * LS;
-        float acc = 0.f;
-#pragma unroll
-        for (int k = K0; k < 32; k += 4) {
             const float4 l4 = *reinterpret_cast<const float4 *>(lr + k);
             acc += l4.x * tc[k] + l4.y * tc[k + 1] + l4.z * tc[k + 2] + l4.w * tc[k + 3];
         }
@@ -688,36 +671,51 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
                 }
             }
             csync();
-            // Level 2: T_[23][01] = -T_[23][23] L_[23][01] T_[01][01] on 32 x 32 blocks.  Thread =
-            // (column jc, rows q + 16 a); the sixteen threads of a column share partial products.
+            // Level 2: T_[23][01] = -T_[23][23] L_[23][01] T_[01][01] on 32 x 32 blocks, as two products
+            // through shared memory: P = L_[23][01] T_[01][01], then T_[23][01] = -T_[23][23] P.  Warps 0-7,
+            // thread = (row i, columns 4 jq .. 4 jq + 3), float4 loads.  The triangular factors hold zeros
+            // above their diagonals, so full-length dot products are exact.  P goes to the (not yet
+            // written) T-image area.
             {
-                const int q = lane & 15, jc = 2 * warp + (lane >> 4);
-                float p[2];
-                switch (warp >> 1) {
-                    case 0: inv_l2_partial<0>(Lm, Tm, q, jc, p); break;
-                    case 1: inv_l2_partial<4>(Lm, Tm, q, jc, p); break;
-                    case 2: inv_l2_partial<8>(Lm, Tm, q, jc, p); break;
-                    case 3: inv_l2_partial<12>(Lm, Tm, q, jc, p); break;
-                    case 4: inv_l2_partial<16>(Lm, Tm, q, jc, p); break;
-                    case 5: inv_l2_partial<20>(Lm, Tm, q, jc, p); break;
-                    case 6: inv_l2_partial<24>(Lm, Tm, q, jc, p); break;
-                    default: inv_l2_partial<28>(Lm, Tm, q, jc, p); break;
-                }
-                float pc[32];
+                float *Pm = (float *)(sm + J_TIMG);  // P [32][36]
+                const int jq = tid & 7, i = tid >> 3;
+                if (tid < 256) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float *lr = Lm + (32 + i) * LS;
 #pragma unroll
-                for (int q2 = 0; q2 < 16; ++q2)
+                    for (int k = 0; k < 32; k += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4 *>(lr + k);
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                    for (int a = 0; a < 2; ++a) pc[q2 + 16 * a] = __shfl_sync(0xffffffffu, p[a], (lane & ~15) | q2);
-#pragma unroll
-                for (int a = 0; a < 2; ++a) {
-                    const float *tr = Tm + (32 + q + 16 * a) * LS + 32;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int k = 0; k < 16 * (a + 1); k += 4) {
-                        const float4 t4 = *reinterpret_cast<const float4 *>(tr + k);
-                        acc += t4.x * pc[k] + t4.y * pc[k + 1] + t4.z * pc[k + 2] + t4.w * pc[k + 3];
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 t4 = *reinterpret_cast<const float4 *>(Tm + (k + e) * LS + 4 * jq);
+                            acc.x = fmaf(lv[e], t4.x, acc.x);
+                            acc.y = fmaf(lv[e], t4.y, acc.y);
+                            acc.z = fmaf(lv[e], t4.z, acc.z);
+                            acc.w = fmaf(lv[e], t4.w, acc.w);
+                        }
                     }
-                    Tm[(32 + q + 16 * a) * LS + jc] = -acc;
+                    *reinterpret_cast<float4 *>(Pm + i * 36 + 4 * jq) = acc;
+                }
+                csync();
+                if (tid < 256) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float *tr = Tm + (32 + i) * LS + 32;
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4) {
+                        const float4 t4 = *reinterpret_cast<const float4 *>(tr + k);
+                        const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 p4 = *reinterpret_cast<const float4 *>(Pm + (k + e) * 36 + 4 * jq);
+                            acc.x = fmaf(tv[e], p4.x, acc.x);
+                            acc.y = fmaf(tv[e], p4.y, acc.y);
+                            acc.z = fmaf(tv[e], p4.z, acc.z);
+                            acc.w = fmaf(tv[e], p4.w, acc.w);
+                        }
+                    }
+                    *reinterpret_cast<float4 *>(Tm + (32 + i) * LS + 4 * jq) =
+                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                 }
             }
             csync();
@@ -835,7 +833,10 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
     uint64_t *bar_v = bar_ld1 + 8;                  // MMA1 done
     uint64_t *bar_s = bar_ld1 + 9;                  // MMA3 done
     uint64_t *bar_sb = bar_ld1 + 10;                // bf16 S^T written (one arrival per recurrence warp)
-    uint64_t *bar_vt = bar_ld1 + 11;                // V~^T written (one arrival per recurrence warp)
+    uint64_t *bar_vt = bar_ld1 + 11;                // [2] V~^T of chunk kk written (one arrival per
+                                                    // recurrence warp); double-buffered so that the
+                                                    // loader, which also waits on it, can never see a
+                                                    // phase two ahead
     uint32_t *tslot = (uint32_t *)(sm + CS_TSLOT);
     int *s_fail = (int *)(sm + CS_TSLOT + 8);
     const int64_t kk0 = (int64_t)seg_i * seg_len;
@@ -861,7 +862,8 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
         mbar_init(bar_v, 1);
         mbar_init(bar_s, 1);
         mbar_init(bar_sb, 8);
-        mbar_init(bar_vt, 8);
+        mbar_init(&bar_vt[0], 8);
+        mbar_init(&bar_vt[1], 8);
         *s_fail = 0;
     }
     if (warp == 0) tmem_alloc(tslot, 512);
@@ -910,7 +912,7 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                 mma_ts_k(tDbuf(kk), tb + TM_SB, smem_u32(P + PK_WQ), 128, 8, id1, false);
                 mma_commit(bar_v);
                 if (kk > 0) mma2(kk - 1);
-                ok = mbar_wait_spin(bar_vt, kk & 1);  // V~^T written, S^T scaled by gamma_kk
+                ok = mbar_wait_spin(&bar_vt[kk & 1], (kk >> 1) & 1);  // V~^T written, S^T scaled by gamma_kk
                 ok = ok && mbar_wait_spin(&bar_ld2[kk & 1], (kk >> 1) & 1);  // part 2 of packet kk
                 if (!ok) break;
                 fence_after_sync();
@@ -935,7 +937,7 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
             for (int kk = 0; kk + 2 < nc && ok; ++kk) {
                 // MMA_U and MMA1 of chunk kk done and gamma_kk read (V~^T of chunk kk written): part 1 of
                 // its stage takes chunk kk + 2
-                ok = mbar_wait_spin(bar_vt, kk & 1) && acquire(kk + 2);
+                ok = mbar_wait_spin(&bar_vt[kk & 1], (kk >> 1) & 1) && acquire(kk + 2);
                 if (!ok) break;
                 load_part1(kk + 2);
                 ok = mbar_wait_spin(&bar_o[kk & 1], (kk >> 1) & 1);  // all MMAs of chunk kk done: part 2
@@ -1060,7 +1062,7 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
             }
             fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_vt);
+            if (lane == 0) mbar_arrive(&bar_vt[kk & 1]);
             const bool last = (kk == nc - 1);
             ok = mbar_wait_spin(bar_s, kk & 1);
             if (!ok) break;
