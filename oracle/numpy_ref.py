@@ -15,6 +15,9 @@ passage of the Kimi K3 technical report (section 2.1.1 unless stated):
                      test that it equals ``recurrence``.
 * ``segment_maps``-- section 5.1.2, Eq. 17: a segment's cumulative transition
                      M and its zero-start state S~, so that S_out = M S_in + S~.
+* ``output_gate`` -- Eq. 6 without the projections W_o and W_g: the per-head
+                     RMSNorm of the recurrent output, then the output gate
+                     Sigmoid(g) with g = W_g x given.
 
 All arithmetic is fp64; inputs are upcast as given.  Layout of one head:
 q, k [T, d_k]; v [T, d_v]; g [T, d_k]; beta [T]; state S [d_k, d_v]
@@ -147,3 +150,22 @@ def forward(q, k, v, z, beta, dt_bias, A_log, cu_seqlens, S0=None, g_min=-5.0, s
                                              np.asarray(v, np.float64)[a:b, h], g,
                                              np.asarray(beta, np.float64)[a:b, h], s0, scale)
     return o, ST
+
+
+def output_gate(o, g, w=None, eps=1e-6):
+    """Eq. 6 (section 2.1.1) without the projections: y = Sigmoid(g) * RMSNorm(o~), where the RMSNorm
+    is taken per head (the report: a per-head RMSNorm of the recurrent output),
+        RMSNorm(o~)_c = w_c * o~_c / sqrt(mean_{c'} o~_{c'}^2 + eps)
+    over the d_v value channels of one (token, head).
+
+    o, g: [..., d_v] (the last axis is one head's value channels); w: RMSNorm weight broadcastable
+    to o (ones when None); eps > 0 (the report gives no value: a parameter).  Returns fp64 y.
+    """
+    o = np.asarray(o, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    ms = np.mean(o * o, axis=-1, keepdims=True)
+    normed = o / np.sqrt(ms + eps)
+    if w is not None:
+        normed = normed * np.asarray(w, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return normed / (1.0 + np.exp(-g))

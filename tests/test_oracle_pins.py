@@ -375,3 +375,57 @@ def test_pins_catch_planted_mistakes(mutant):
         if not (np.allclose(o, o_exp, atol=1e-12) and np.allclose(S, S_exp, atol=1e-12)):
             failures += 1
     assert failures >= 1, "a planted mistake passed every golden fixture"
+
+
+# ----------------------------------------------------------------------------- output epilogue (Eq. 6)
+
+def _output_gate_rows():
+    rows = read_table("output_gate_eq6.txt")
+    assert len(rows) == 5
+    return [(r[0], r[1:5], r[5:9], r[9:13], r[13:17]) for r in rows]
+
+
+def test_output_gate_golden():
+    for eps, o, g, w, y in _output_gate_rows():
+        assert np.allclose(R.output_gate(o, g, w, eps), y, rtol=1e-14, atol=1e-15)
+
+
+def test_output_gate_constant_vector_closed_form():
+    """o = c (all channels) with eps = 0: RMSNorm(o) = sign(c), so y = Sigmoid(g) * w * sign(c)."""
+    rng = np.random.default_rng(3)
+    for c in (-2.5, 0.125, 7.0):
+        g, w = rng.normal(size=16), rng.normal(size=16)
+        y = R.output_gate(np.full(16, c), g, w, 0.0)
+        assert np.allclose(y, np.sign(c) * w / (1.0 + np.exp(-g)), rtol=1e-14, atol=1e-15)
+
+
+def test_output_gate_scale_invariant_and_per_head():
+    """With eps = 0 the result does not depend on the scale of o; the norm of one head uses only
+    that head's channels."""
+    rng = np.random.default_rng(4)
+    o, g, w = rng.normal(size=(5, 3, 8)), rng.normal(size=(5, 3, 8)), rng.normal(size=(3, 8))
+    y = R.output_gate(o, g, w, 0.0)
+    assert np.allclose(R.output_gate(o * 37.0, g, w, 0.0), y, rtol=1e-13)
+    o2 = o.copy()
+    o2[:, 1] *= 5.0
+    o2[:, 2] += 1.0
+    y2 = R.output_gate(o2, g, w, 0.0)
+    assert np.array_equal(y2[:, 0], y[:, 0])
+    assert np.allclose(y2[:, 1], y[:, 1], rtol=1e-13)
+
+
+_OG_MUTANTS = {
+    "no_square_root": lambda o, g, w, e: np.asarray(o) / (np.mean(np.square(o)) + e) * w / (1 + np.exp(-np.asarray(g))),
+    "sum_not_mean": lambda o, g, w, e: np.asarray(o) / np.sqrt(np.sum(np.square(o)) + e) * w / (1 + np.exp(-np.asarray(g))),
+    "gate_sign_flipped": lambda o, g, w, e: np.asarray(o) / np.sqrt(np.mean(np.square(o)) + e) * w / (1 + np.exp(np.asarray(g))),
+    "eps_outside_root": lambda o, g, w, e: np.asarray(o) / (np.sqrt(np.mean(np.square(o))) + e) * w / (1 + np.exp(-np.asarray(g))),
+    "weight_dropped": lambda o, g, w, e: np.asarray(o) / np.sqrt(np.mean(np.square(o)) + e) / (1 + np.exp(-np.asarray(g))),
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(_OG_MUTANTS))
+def test_output_gate_fixture_catches_planted_mistakes(mutant):
+    f = _OG_MUTANTS[mutant]
+    failures = sum(not np.allclose(f(np.array(o), g, np.array(w), eps), y, rtol=1e-12, atol=1e-12)
+                   for eps, o, g, w, y in _output_gate_rows())
+    assert failures >= 1, "a planted mistake passed every output-gate fixture"
