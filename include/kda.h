@@ -48,7 +48,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
 
-#define KDA_ABI_VERSION 1
+#define KDA_ABI_VERSION 2
 
 typedef enum {
     KDA_OK = 0,
@@ -121,6 +121,13 @@ typedef struct {
     float *final_state;            /* [N, H, dk, dv] or NULL; may alias initial_state */
     void *o;                       /* [T, H, dv] output; must not alias an input */
     int32_t chunk_size;            /* 64, or 0 for the default (64) */
+    /* Optional output epilogue (Eq. 6 without its projections; see kda_output_gate): when out_gate
+     * is set, o receives Sigmoid(out_gate) * RMSNorm(o~) instead of the recurrent output o~.  On the
+     * tensor-core path it is applied before o leaves the chip; elsewhere by a kda_output_gate launch
+     * on o. */
+    const void *out_gate;          /* [T, H, dv], dtype of o, 16-byte aligned, or NULL (no epilogue) */
+    const float *out_norm_weight;  /* [H, dv] RMSNorm weight, 16-byte aligned, or NULL (ones) */
+    float out_norm_eps;            /* RMSNorm epsilon, > 0 when out_gate is set */
 } kda_chunk_args;
 
 /* Bytes of device scratch kda_chunk_fwd needs for these sizes (0 on invalid sizes).
@@ -135,6 +142,26 @@ size_t kda_chunk_fwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk,
  * and are garbage afterwards.  Calls that share a workspace must not overlap. */
 kda_status_t kda_chunk_fwd(const kda_chunk_args *args, void *workspace, size_t workspace_bytes,
                            struct CUstream_st *stream);
+
+/* ----------------------------------------------------------- kda_output_gate
+ * The output epilogue of Eq. 6 (section 2.1.1), y_t = W_o[Sigmoid(W_g x_t) * RMSNorm(o~_t)], without
+ * the two projections: for every token t and head h,
+ *     y[t,h,c] = Sigmoid(g[t,h,c]) * w[h,c] * o[t,h,c] / sqrt(mean_c' o[t,h,c']^2 + eps),
+ * the RMSNorm taken per head over its dv value channels, g = W_g x_t given.  fp32 arithmetic.
+ * Supported: dv in {32, 64, 128, 256}.  Pointers are device pointers, 16-byte aligned.
+ */
+typedef struct {
+    int64_t T;                  /* tokens */
+    int32_t H, dv;              /* heads, value channels */
+    kda_dtype_t dtype;          /* dtype of o, g and y */
+    const void *o;              /* [T, H, dv] recurrent output o~ */
+    const void *g;              /* [T, H, dv] gate pre-activation W_g x */
+    const float *norm_weight;   /* [H, dv] RMSNorm weight, or NULL (ones) */
+    float eps;                  /* RMSNorm epsilon, > 0 (the report gives no value) */
+    void *y;                    /* [T, H, dv] output; may alias o, must not alias g */
+} kda_output_gate_args;
+
+kda_status_t kda_output_gate(const kda_output_gate_args *args, struct CUstream_st *stream);
 
 /* --------------------------------------------------- kda_chunk_fwd_static_ws
  * Not an operation of the paper (it has no counterpart there): the same

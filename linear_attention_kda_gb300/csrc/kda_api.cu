@@ -84,7 +84,8 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
     // either one fused launch (intra-chunk transform and output pass together) or the chunk plan,
     // then intra-chunk transform, [segment summaries, fold,] output pass
     if (p.fused) return 1;
-    return p.split ? 5 : 3;
+    const int extra = (p.path == 0 && a->out_gate) ? 1 : 0;  // the fp32 path's separate epilogue pass
+    return (p.split ? 5 : 3) + extra;
 }
 
 kda_status_t kda_chunk_fwd_schedule(const kda_chunk_args *a, int64_t *out) {
@@ -176,6 +177,12 @@ static kda_status_t validate_chunk(const kda_chunk_args *a) {
         (a->dt_bias && !aligned16(a->dt_bias)) || (a->A_log && !aligned_to(a->A_log, 4)) ||
         (a->cu_seqlens && !aligned_to(a->cu_seqlens, 4)))
         return KDA_ERR_MISALIGNED;
+    if (a->out_gate) {  // output epilogue (Eq. 6)
+        if (!(a->out_norm_eps > 0.f) || !isfinite(a->out_norm_eps)) return KDA_ERR_INVALID_ARG;
+        if (a->out_gate == a->o) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(a->out_gate) || (a->out_norm_weight && !aligned16(a->out_norm_weight)))
+            return KDA_ERR_MISALIGNED;
+    }
     if (a->cu_seqlens_host) {
         const int32_t *cu = a->cu_seqlens_host;
         if (cu[0] != 0 || cu[a->N] != a->T) return KDA_ERR_INVALID_ARG;
@@ -209,7 +216,29 @@ kda_status_t kda_chunk_fwd(const kda_chunk_args *a, void *workspace, size_t work
     st = check_device();
     if (st != KDA_OK) return st;
     if (p.path == 1) return kda_launch_chunk_tc(a, p, workspace, (cudaStream_t)stream);
-    return kda_launch_chunk_simt(a, p, workspace, (cudaStream_t)stream);
+    st = kda_launch_chunk_simt(a, p, workspace, (cudaStream_t)stream);
+    if (st != KDA_OK || !a->out_gate) return st;
+    // the fp32 CUDA-core path applies the output epilogue as a separate pass over o, in place
+    kda_output_gate_args og{a->T, a->H, a->dv, a->dtype, a->o, a->out_gate, a->out_norm_weight,
+                            a->out_norm_eps, a->o};
+    return kda_launch_output_gate(&og, (cudaStream_t)stream);
+}
+
+kda_status_t kda_output_gate(const kda_output_gate_args *a, struct CUstream_st *stream) {
+    if (!a) return KDA_ERR_INVALID_ARG;
+    if (a->T < 0 || a->H < 1) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(a->dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (a->dv != 32 && a->dv != 64 && a->dv != 128 && a->dv != 256) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!(a->eps > 0.f) || !isfinite(a->eps)) return KDA_ERR_INVALID_ARG;
+    if (a->T == 0) return KDA_OK;
+    if (!a->o || !a->g || !a->y || a->y == a->g) return KDA_ERR_INVALID_ARG;
+    if (a->T * (int64_t)a->H > ((int64_t)INT32_MAX) * 8) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(a->o) || !aligned16(a->g) || !aligned16(a->y) ||
+        (a->norm_weight && !aligned16(a->norm_weight)))
+        return KDA_ERR_MISALIGNED;
+    kda_status_t st = check_device();
+    if (st != KDA_OK) return st;
+    return kda_launch_output_gate(a, (cudaStream_t)stream);
 }
 
 kda_status_t kda_recurrent_step(const kda_step_args *a, struct CUstream_st *stream) {

@@ -11,6 +11,7 @@ void kda_profile_mark(int i, cudaStream_t stream);
 kda_status_t kda_cuda_status(cudaError_t e);
 
 kda_status_t kda_launch_gate(const kda_gate_args *a, cudaStream_t stream);
+kda_status_t kda_launch_output_gate(const kda_output_gate_args *a, cudaStream_t stream);
 kda_status_t kda_launch_decode(const kda_step_args *a, cudaStream_t stream);
 
 // Chunked prefill.  Workspace layout is owned by kda_chunk_plan.cu.

@@ -27,7 +27,7 @@ _STATUS = {
 EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step",
             "kda_status_string", "kda_get_device_error", "kda_abi_version",
             "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws",
-            "kda_last_cuda_error", "kda_chunk_fwd_schedule"]
+            "kda_last_cuda_error", "kda_chunk_fwd_schedule", "kda_output_gate"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 _vp = ctypes.c_void_p
@@ -45,7 +45,13 @@ class ChunkArgs(ctypes.Structure):
                 ("dtype", ctypes.c_int), ("q", _vp), ("k", _vp), ("z", _vp), ("v", _vp),
                 ("beta", _vp), ("dt_bias", _vp), ("A_log", _vp), ("g_min", _f32), ("scale", _f32),
                 ("cu_seqlens", _vp), ("cu_seqlens_host", _vp), ("initial_state", _vp),
-                ("final_state", _vp), ("o", _vp), ("chunk_size", _i32)]
+                ("final_state", _vp), ("o", _vp), ("chunk_size", _i32),
+                ("out_gate", _vp), ("out_norm_weight", _vp), ("out_norm_eps", _f32)]
+
+
+class OutputGateArgs(ctypes.Structure):
+    _fields_ = [("T", _i64), ("H", _i32), ("dv", _i32), ("dtype", ctypes.c_int), ("o", _vp), ("g", _vp),
+                ("norm_weight", _vp), ("eps", _f32), ("y", _vp)]
 
 
 class StepArgs(ctypes.Structure):
@@ -97,6 +103,8 @@ def load_library(path: Optional[str] = None):
         L.kda_chunk_fwd_schedule.restype = ctypes.c_int
         L.kda_chunk_fwd_static_ws.argtypes = [ctypes.POINTER(ChunkArgs), _vp]
         L.kda_chunk_fwd_static_ws.restype = ctypes.c_int
+        L.kda_output_gate.argtypes = [ctypes.POINTER(OutputGateArgs), _vp]
+        L.kda_output_gate.restype = ctypes.c_int
         L.kda_last_cuda_error.argtypes = []
         L.kda_last_cuda_error.restype = _i32
         _lib = L
@@ -161,12 +169,16 @@ def chunk_fwd(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0
               n_seq: int = 1, initial_state: Optional[torch.Tensor] = None,
               output_final_state: bool = False, final_state: Optional[torch.Tensor] = None,
               chunk_size: int = 64, workspace: Optional[torch.Tensor] = None,
-              out: Optional[torch.Tensor] = None):
-    """kda_chunk_fwd: chunkwise KDA prefill (Eq. 1 evaluated as Eq. 3-4).  Returns (o, final_state)."""
+              out: Optional[torch.Tensor] = None, out_gate: Optional[torch.Tensor] = None,
+              out_norm_weight: Optional[torch.Tensor] = None, out_norm_eps: float = 1e-6):
+    """kda_chunk_fwd: chunkwise KDA prefill (Eq. 1 evaluated as Eq. 3-4).  Returns (o, final_state).
+
+    With out_gate ([T, H, dv], the gate pre-activation W_g x), o holds the output epilogue of Eq. 6,
+    Sigmoid(out_gate) * RMSNorm(o~) (per-head RMSNorm with weight out_norm_weight [H, dv], eps)."""
     L = load_library()
     T, H, dk = q.shape
     dv = v.shape[2]
-    _contig(q, k, v, z, beta, dt_bias, A_log, cu_seqlens, initial_state)
+    _contig(q, k, v, z, beta, dt_bias, A_log, cu_seqlens, initial_state, out_gate, out_norm_weight)
     N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else n_seq
     if cu_seqlens_host is not None:
         cu_seqlens_host = cu_seqlens_host.to(dtype=torch.int32, device="cpu").contiguous()
@@ -182,10 +194,24 @@ def chunk_fwd(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0
                   scale=scale, cu_seqlens=_ptr(cu_seqlens),
                   cu_seqlens_host=None if cu_seqlens_host is None else cu_seqlens_host.data_ptr(),
                   initial_state=_ptr(initial_state), final_state=_ptr(fs), o=_ptr(o),
-                  chunk_size=chunk_size)
+                  chunk_size=chunk_size, out_gate=_ptr(out_gate), out_norm_weight=_ptr(out_norm_weight),
+                  out_norm_eps=out_norm_eps)
     _check(L.kda_chunk_fwd(ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(q)),
            "kda_chunk_fwd")
     return o, fs
+
+
+def output_gate(o, g, norm_weight=None, eps: float = 1e-6, *, out: Optional[torch.Tensor] = None):
+    """kda_output_gate: Sigmoid(g) * RMSNorm(o) per (token, head) (Eq. 6 without projections).
+    o, g: [T, H, dv]; norm_weight: [H, dv] fp32 or None; out may be o (in place)."""
+    L = load_library()
+    T, H, dv = o.shape
+    _contig(o, g, norm_weight)
+    y = out if out is not None else torch.empty_like(o)
+    a = OutputGateArgs(T=T, H=H, dv=dv, dtype=_dtype_code(o), o=_ptr(o), g=_ptr(g),
+                       norm_weight=_ptr(norm_weight), eps=eps, y=_ptr(y))
+    _check(L.kda_output_gate(ctypes.byref(a), _stream(o)), "kda_output_gate")
+    return y
 
 
 def recurrent_step(q, k, v, z, beta, dt_bias, A_log, state, *, g_min: float = -5.0, scale: float = 1.0,

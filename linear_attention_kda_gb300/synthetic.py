@@ -116,6 +116,16 @@ def make_tokens(T: int, H: int, d_k: int, d_v: int, dtype: str, seed: int, *,
     return q, k, v, beta, z
 
 
+def make_output_gate_inputs(T: int, H: int, d_v: int, dtype: str, seed: int, device="cpu"):
+    """Inputs of the output epilogue (Eq. 6 without projections): the gate pre-activation
+    g = W_g x ~ N(0, 1) [T, H, d_v] in the I/O dtype, and the per-head RMSNorm weight
+    w = 1 + 0.1 N(0, 1) [H, d_v] fp32.  Draw order: g, w."""
+    gen = _gen(seed, device)
+    g = torch.randn((T, H, d_v), generator=gen, device=device, dtype=torch.float32).to(_DTYPES[dtype])
+    w = 1.0 + 0.1 * torch.randn((H, d_v), generator=gen, device=device, dtype=torch.float32)
+    return g, w
+
+
 def make_head_params(H: int, d_k: int, seed: int, *, b_range: float, alog_std: float):
     """dt_bias [H, d_k] fp32 and A_log [H] fp32 (CPU)."""
     g = _gen(seed + 104729, "cpu")

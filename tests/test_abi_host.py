@@ -46,7 +46,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.kda_abi_version() == 1
+    assert lib.kda_abi_version() == 2
     for code, name in kda._STATUS.items():
         s = lib.kda_status_string(code).decode()
         assert s and s != "unknown status", name
@@ -62,6 +62,7 @@ int main(void) {
   printf("kda_gate_args sizeof %zu\n", sizeof(kda_gate_args));
   printf("kda_chunk_args sizeof %zu\n", sizeof(kda_chunk_args));
   printf("kda_step_args sizeof %zu\n", sizeof(kda_step_args));
+  printf("kda_output_gate_args sizeof %zu\n", sizeof(kda_output_gate_args));
   %FIELDS%
   return 0;
 }
@@ -71,7 +72,7 @@ int main(void) {
 def test_struct_layout_matches_header(tmp_path):
     fields = []
     for cname, cls in (("kda_gate_args", kda.GateArgs), ("kda_chunk_args", kda.ChunkArgs),
-                       ("kda_step_args", kda.StepArgs)):
+                       ("kda_step_args", kda.StepArgs), ("kda_output_gate_args", kda.OutputGateArgs)):
         for f, _ in cls._fields_:
             fields.append(f"F({cname}, {f})")
     src = tmp_path / "layout.c"
@@ -85,7 +86,7 @@ def test_struct_layout_matches_header(tmp_path):
             s, f, v = ln.split()
             got[(s, f)] = int(v)
     for cname, cls in (("kda_gate_args", kda.GateArgs), ("kda_chunk_args", kda.ChunkArgs),
-                       ("kda_step_args", kda.StepArgs)):
+                       ("kda_step_args", kda.StepArgs), ("kda_output_gate_args", kda.OutputGateArgs)):
         assert got[(cname, "sizeof")] == ctypes.sizeof(cls), cname
         for f, _ in cls._fields_:
             assert got[(cname, f)] == getattr(cls, f).offset, (cname, f)
@@ -124,6 +125,10 @@ def _call_chunk(lib, a, ws=FAKE, ws_bytes=1 << 40):
     (dict(q=FAKE + 8), 4),
     (dict(o=FAKE + 16392), 4),
     (dict(initial_state=FAKE + 4), 4),
+    (dict(out_gate=FAKE + 32768, out_norm_eps=0.0), 1),          # epilogue needs eps > 0
+    (dict(out_gate=FAKE + 16384, out_norm_eps=1e-6), 1),         # gate aliases o
+    (dict(out_gate=FAKE + 32776, out_norm_eps=1e-6), 4),
+    (dict(out_gate=FAKE + 32768, out_norm_weight=FAKE + 40964, out_norm_eps=1e-6), 4),
 ])
 def test_chunk_fwd_rejects(lib, kw, code):
     assert _call_chunk(lib, _chunk(**kw)) == code
@@ -187,12 +192,36 @@ def test_gate_rejects(lib):
     assert lib.kda_gate(ctypes.byref(a), None) == 1
 
 
+def _og(**kw):
+    base = dict(T=16, H=2, dv=128, dtype=kda.KDA_BF16, o=FAKE, g=FAKE + 8192, norm_weight=None, eps=1e-6,
+                y=FAKE + 16384)
+    base.update(kw)
+    return kda.OutputGateArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dv=96), 2),
+    (dict(dtype=4), 3),
+    (dict(H=0), 1),
+    (dict(T=-1), 1),
+    (dict(eps=0.0), 1),
+    (dict(eps=float("nan")), 1),
+    (dict(g=None), 1),
+    (dict(y=FAKE + 8192), 1),       # y aliases g
+    (dict(o=FAKE + 8), 4),
+    (dict(norm_weight=FAKE + 32772), 4),
+])
+def test_output_gate_rejects(lib, kw, code):
+    assert lib.kda_output_gate(ctypes.byref(_og(**kw)), None) == code
+
+
 def test_empty_inputs_are_noops(lib):
     # T = 0 gate / N = 0 decode return KDA_OK before touching any pointer or the device
     a = kda.GateArgs(T=0, N=1, H=1, dk=16, dtype=kda.KDA_F32, z=None, dt_bias=None, A_log=None,
                      g_min=-5.0, chunk_size=0, cu_seqlens=None, out=None)
     assert lib.kda_gate(ctypes.byref(a), None) == 0
     assert lib.kda_recurrent_step(ctypes.byref(_step(N=0, q=None)), None) == 0
+    assert lib.kda_output_gate(ctypes.byref(_og(T=0, o=None, g=None, y=None)), None) == 0
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
@@ -200,3 +229,4 @@ def test_valid_args_stop_at_device_check_without_gpu(lib):
     # Passes validation, then finds no sm_103 device: nothing is launched.
     assert _call_chunk(lib, _chunk()) == 9
     assert lib.kda_recurrent_step(ctypes.byref(_step()), None) == 9
+    assert lib.kda_output_gate(ctypes.byref(_og()), None) == 9

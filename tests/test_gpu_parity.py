@@ -303,3 +303,73 @@ def test_split_sequence_final_state_aliases_initial_state():
                          initial_state=st, final_state=st)
     torch.cuda.synchronize()
     compare_prefill(d, o.float().cpu(), st.cpu(), oracle_prefill(d), TOL_BF16)
+
+
+# ----------------------------------------------------------------------------- output epilogue (Eq. 6)
+
+EPS = 1e-6
+
+
+def _epilogue_ref(d, res, g, w):
+    """Oracle: per (sequence, head), the recurrence's output followed by the Eq. 6 epilogue."""
+    cu = [int(x) for x in d["cu_seqlens"]]
+    out = {}
+    for (n, h), (o_ref, S_ref) in res.items():
+        gg = g[cu[n]:cu[n + 1], h].double().numpy()
+        out[(n, h)] = (R.output_gate(o_ref, gg, w[h].double().numpy(), EPS), S_ref)
+    return out
+
+
+@pytest.mark.parametrize("dtype,dv", [("bf16", 128), ("bf16", 64), ("f32", 128), ("f32", 32), ("bf16", 256)])
+def test_output_gate_standalone(dtype, dv):
+    T, H = 301, 3
+    o = syn.make_tokens(T, H, dv, dv, dtype, 31, z_std=1.0)[2] * 3.0
+    g, w = syn.make_output_gate_inputs(T, H, dv, dtype, 32)
+    ref = R.output_gate(o.double().numpy(), g.double().numpy(), w.double().numpy()[None], EPS)
+    tol = TOL_BF16 if dtype == "bf16" else 1e-5
+    y = kda.output_gate(o.cuda(), g.cuda(), w.cuda(), EPS).float().cpu()
+    y_now = kda.output_gate(o.cuda(), g.cuda(), None, EPS).float().cpu()
+    ref_now = R.output_gate(o.double().numpy(), g.double().numpy(), None, EPS)
+    oc = o.cuda().contiguous()
+    kda.output_gate(oc, g.cuda(), w.cuda(), EPS, out=oc)  # in place
+    for h in range(H):
+        assert rel_err(y[:, h].numpy(), ref[:, h]) <= tol
+        assert rel_err(y_now[:, h].numpy(), ref_now[:, h]) <= tol
+        assert rel_err(oc[:, h].float().cpu().numpy(), ref[:, h]) <= tol
+
+
+def test_prefill_4k_with_fused_output_epilogue():
+    """The benchmark workload with the epilogue fused into the tensor-core output pass."""
+    d = syn.make_prefill(syn.PREFILL_4K, seed=1)
+    g, w = syn.make_output_gate_inputs(4096, 32, 128, "bf16", 33)
+    o, fs = run_prefill(d, out_gate=g.cuda(), out_norm_weight=w.cuda(), out_norm_eps=EPS)
+    compare_prefill(d, o, fs, _epilogue_ref(d, oracle_prefill(d), g, w), TOL_BF16)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64)])
+def test_varlen_ragged_with_output_epilogue(dtype, D):
+    """Ragged lengths (empty, 1, chunk +-1, tails): the fused epilogue on the tensor-core path,
+    the separate epilogue pass on the fp32 path."""
+    w_ = syn.Workload("ve", H=3, d=D, dtype=dtype, seq_len=None, z_std=1.5, b_range=1.0,
+                      alog_std=0.25, s0_std=0.02)
+    d = _varlen(w_, [1, 63, 64, 0, 65, 130, 200, 7], seed=24)
+    T = sum(d["lengths"])
+    g, w = syn.make_output_gate_inputs(T, 3, D, dtype, 34)
+    o, fs = run_prefill(d, out_gate=g.cuda(), out_norm_weight=w.cuda(), out_norm_eps=EPS)
+    compare_prefill(d, o, fs, _epilogue_ref(d, oracle_prefill(d), g, w),
+                    TOL_F32 if dtype == "f32" else TOL_BF16)
+
+
+def test_fused_epilogue_equals_separate_pass():
+    """Epilogue inside the output pass == plain prefill followed by kda_output_gate (bf16 rounding
+    of both)."""
+    w_ = syn.Workload("fe", H=4, d=128, dtype="bf16", seq_len=None, z_std=1.5, b_range=1.0,
+                      alog_std=0.25, s0_std=0.02)
+    d = _varlen(w_, [700, 64, 333], seed=25)
+    T = sum(d["lengths"])
+    g, w = syn.make_output_gate_inputs(T, 4, 128, "bf16", 35)
+    o_f, _ = run_prefill(d, out_gate=g.cuda(), out_norm_weight=w.cuda(), out_norm_eps=EPS)
+    o_p, _ = run_prefill(d)
+    o_s = kda.output_gate(o_p.to(torch.bfloat16).cuda(), g.cuda(), w.cuda(), EPS).float().cpu()
+    for h in range(4):
+        assert rel_err(o_f[:, h].numpy(), o_s[:, h].numpy()) <= 5e-3
