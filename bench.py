@@ -413,6 +413,50 @@ def run_ours(args, rank, ws, local):
     e2e_ms = max_over_ranks(sum(e2e_times) / len(e2e_times), ws)
     del dev_in, pin
 
+    # ---------------- output epilogue of Eq. 6: through kda_chunk_fwd, and the pass alone
+    epi = None
+    if not args.no_epilogue:
+        g_in, w_in = syn.make_output_gate_inputs(T, H, D, "bf16", 33 + rank, device=dev)
+        o2 = torch.empty_like(v)
+
+        def step_epi():
+            kda.chunk_fwd(q, k, v, z, beta, b, a, g_min=d["g_min"], scale=d["scale"], cu_seqlens=d["cu_seqlens"],
+                          cu_seqlens_host=cu_host, final_state=fs, workspace=work, out=o2, out_gate=g_in,
+                          out_norm_weight=w_in, out_norm_eps=1e-6)
+
+        def sep_pass():
+            kda.output_gate(o, g_in, w_in, 1e-6, out=o2)
+
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def timed(fn, n):
+            ts = []
+            for _ in range(n):
+                flush.zero_()
+                ea.record(stream)
+                fn()
+                eb.record(stream)
+                eb.synchronize()
+                ts.append(ea.elapsed_time(eb))
+            return sum(ts) / len(ts)
+
+        for _ in range(3):
+            flush.zero_()
+            step_epi()
+            sep_pass()
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        ms_fused = timed(step_epi, args.steps)
+        ms_sep = timed(sep_pass, args.steps)
+        ob = 3 * T * H * D * 2 + H * D * 4  # o and g read, y written (bf16), weight
+        gb = ob / (ms_sep / 1e3) / 1e9
+        epi = {"what": "o <- Sigmoid(g) * RMSNorm(o) per (token, head) (Eq. 6 without projections)",
+               "prefill_with_epilogue_ms_per_step": ms_fused, "epilogue_overhead_ms": ms_fused - ms,
+               "epilogue_pass_ms": ms_sep,
+               "roofline": {"bound": "hbm", "achieved": gb, "peak": hbm, "unit": "GB/s",
+                            "frac": gb / hbm, "bytes": ob, "kernel": "output_gate"}}
+        del g_in, w_in, o2
+
     # ---------------- decode workload (HBM-bound), 512 in-place steps
     dec = None
     if not args.no_decode:
@@ -474,6 +518,7 @@ def run_ours(args, rank, ws, local):
             "gpu_launches": nk * args.steps,
             "clocks": clocks,
             "decode": dec,
+            "epilogue": epi,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -520,6 +565,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-epilogue", action="store_true")
     ap.add_argument("--case", choices=["prefill_small", "prefill_4k", "decode_small"], default=None,
                     help="run a small fixed case for profiler captures instead of the benchmark")
     args = ap.parse_args()

@@ -122,9 +122,8 @@ typedef struct {
     void *o;                       /* [T, H, dv] output; must not alias an input */
     int32_t chunk_size;            /* 64, or 0 for the default (64) */
     /* Optional output epilogue (Eq. 6 without its projections; see kda_output_gate): when out_gate
-     * is set, o receives Sigmoid(out_gate) * RMSNorm(o~) instead of the recurrent output o~.  On the
-     * tensor-core path it is applied before o leaves the chip; elsewhere by a kda_output_gate launch
-     * on o. */
+     * is set, o receives Sigmoid(out_gate) * RMSNorm(o~) instead of the recurrent output o~, by a
+     * kda_output_gate pass over o (in place) after the recurrence. */
     const void *out_gate;          /* [T, H, dv], dtype of o, 16-byte aligned, or NULL (no epilogue) */
     const float *out_norm_weight;  /* [H, dv] RMSNorm weight, 16-byte aligned, or NULL (ones) */
     float out_norm_eps;            /* RMSNorm epsilon, > 0 when out_gate is set */

@@ -83,8 +83,8 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
         return 0;
     // either one fused launch (intra-chunk transform and output pass together) or the chunk plan,
     // then intra-chunk transform, [segment summaries, fold,] output pass
-    if (p.fused) return 1;
-    const int extra = (p.path == 0 && a->out_gate) ? 1 : 0;  // the fp32 path's separate epilogue pass
+    const int extra = a->out_gate ? 1 : 0;  // the output epilogue's pass
+    if (p.fused) return 1 + extra;
     return (p.split ? 5 : 3) + extra;
 }
 
@@ -215,10 +215,11 @@ kda_status_t kda_chunk_fwd(const kda_chunk_args *a, void *workspace, size_t work
     if (!aligned_to(workspace, 256)) return KDA_ERR_MISALIGNED;
     st = check_device();
     if (st != KDA_OK) return st;
-    if (p.path == 1) return kda_launch_chunk_tc(a, p, workspace, (cudaStream_t)stream);
-    st = kda_launch_chunk_simt(a, p, workspace, (cudaStream_t)stream);
+    st = p.path == 1 ? kda_launch_chunk_tc(a, p, workspace, (cudaStream_t)stream)
+                     : kda_launch_chunk_simt(a, p, workspace, (cudaStream_t)stream);
     if (st != KDA_OK || !a->out_gate) return st;
-    // the fp32 CUDA-core path applies the output epilogue as a separate pass over o, in place
+    // the output epilogue runs as its own HBM-bound pass over o, in place, on all SMs (inside the
+    // output pass it would lengthen the latency-bound chain more than the round trip of o costs)
     kda_output_gate_args og{a->T, a->H, a->dv, a->dtype, a->o, a->out_gate, a->out_norm_weight,
                             a->out_norm_eps, a->o};
     return kda_launch_output_gate(&og, (cudaStream_t)stream);

@@ -57,19 +57,9 @@ constexpr uint32_t PK_P2 = PK_STRIDE - PK_K;  // bytes of part 2 (at PK_K)
 // the packet after them is prefetched into L2.
 constexpr uint32_t CS_ST_BYTES = PK_STRIDE;            // stage stride (multiple of 1024)
 constexpr uint32_t CS_OIMG = 2 * CS_ST_BYTES;          // o staging, 2 buffers x (64 tokens x 128, 2 x 8 KB)
-constexpr uint32_t CS_GIMG = CS_OIMG + 32768;          // output-gate tiles (epilogue), 2 buffers, same layout
-constexpr uint32_t CS_BAR = CS_GIMG + 32768;           // 15 mbarriers
+constexpr uint32_t CS_BAR = CS_OIMG + 32768;           // 13 mbarriers
 constexpr uint32_t CS_TSLOT = CS_BAR + 128;            // TMEM base, failure flag
-constexpr uint32_t CS_RED = CS_BAR + 256;              // epilogue: sums of squares [2][64] fp32
-constexpr uint32_t CS_TOTAL = CS_RED + 512 + 1024;
-
-// Output epilogue of Eq. 6 without its projections: o <- Sigmoid(gate) * RMSNorm(o) per (token, head),
-// the gate tiles read through a tensor map like o's.
-struct OutEpi {
-    const float *w;  // [H, 128] RMSNorm weight or nullptr (ones)
-    float eps;
-    int on;          // 0: plain output
-};
+constexpr uint32_t CS_TOTAL = CS_BAR + 192 + 1024;
 static_assert(PK_P1 <= PK_K && PK_P1 % 16 == 0 && PK_P2 % 16 == 0, "packet parts");
 
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
@@ -819,8 +809,7 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                                            const float *__restrict__ seg_in, int H,
                                            const unsigned char *__restrict__ packets, float scale,
                                            const float *initial_state, float *final_state, bf16 *__restrict__ o,
-                                           int *err, int g, int h, const uint64_t *flags, uint64_t epoch,
-                                           const CUtensorMap &gmap, const OutEpi &epi) {
+                                           int *err, int g, int h, const uint64_t *flags, uint64_t epoch) {
     // segment g of sequence n, head h: chunks [kk0, kk0 + nc) of the sequence
     if (g >= seg_start[N]) return;
     int n = 0;
@@ -844,7 +833,6 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
     uint64_t *bar_v = bar_ld1 + 8;                  // MMA1 done
     uint64_t *bar_s = bar_ld1 + 9;                  // MMA3 done
     uint64_t *bar_sb = bar_ld1 + 10;                // bf16 S^T written (one arrival per recurrence warp)
-    uint64_t *bar_g = bar_ld1 + 13;                 // [2] output-gate tile of a chunk loaded (epilogue)
     uint64_t *bar_vt = bar_ld1 + 11;                // [2] V~^T of chunk kk written (one arrival per
                                                     // recurrence warp); double-buffered so that the
                                                     // loader, which also waits on it, can never see a
@@ -876,8 +864,6 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
         mbar_init(bar_sb, 8);
         mbar_init(&bar_vt[0], 8);
         mbar_init(&bar_vt[1], 8);
-        mbar_init(&bar_g[0], 1);
-        mbar_init(&bar_g[1], 1);
         *s_fail = 0;
     }
     if (warp == 0) tmem_alloc(tslot, 512);
@@ -968,17 +954,6 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
         const uint32_t vh = (uint32_t)(v >> 6) * 8192 + ((uint32_t)(v & 7) << 1);
         const int vc = (v & 63) >> 3;
         bool ok = true;
-        int g_last = -1;  // last chunk whose gate tile was requested (loads alternate the two buffers)
-        auto load_gate = [&](int kk) {  // one thread
-            uint64_t *bg = &bar_g[kk & 1];
-            unsigned char *gdst = sm + CS_GIMG + 16384 * (kk & 1);
-            const int tok = (int)(s_tok + (int64_t)kk * C);
-            mbar_arrive_expect_tx(bg, 16384);
-            tma_load_3d(gdst, &gmap, 0, h, tok, bg);
-            tma_load_3d(gdst + 8192, &gmap, 64, h, tok, bg);
-            g_last = kk;
-        };
-        if (epi.on && ot == 0 && nc > 0) load_gate(0);
         for (int kk = 0; kk < nc && ok; ++kk) {
             ok = mbar_wait(&bar_o[kk & 1], (kk >> 1) & 1);
             if (!ok) break;
@@ -995,60 +970,16 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
             mbar_arrive(&bar_free[kk & 1]);  // TMEM buffer read
             const int64_t tp = s_tok + (int64_t)kk * C;
             const int lenp = (int)min((int64_t)C, e_tok - tp);
-            // o of the chunk into the staging tile (two 64 x 64 swizzled halves, double-buffered)
-            unsigned char *stg = sm + CS_OIMG + 16384 * (kk & 1);
-            if (ot == 0 && kk >= 2) bulk_wait_read1();  // the store of chunk kk - 2 has left this buffer
-            named_sync(2, 128);
-#pragma unroll
-            for (int t = 0; t < 64; ++t) {
-                const uint32_t w = ob[t >> 1];
-                *reinterpret_cast<uint16_t *>(stg + vh + t * 128 + ((vc ^ (t & 7)) << 4)) =
-                    (uint16_t)((t & 1) ? (w >> 16) : (w & 0xFFFFu));
-            }
-            named_sync(2, 128);
-            // thread = (token tt, 64-channel half hf): its row of the tile is 8 chunks of 16 bytes
-            const int tt = ot & 63, hf = ot >> 6;
-            unsigned char *row = stg + 8192 * hf + tt * 128;
-            if (epi.on) {  // o <- Sigmoid(g) * w * o / sqrt(mean o^2 + eps), in place in the tile
-                float *red = (float *)(sm + CS_RED);
-                if (ot == 0 && kk + 1 < nc) {  // the next chunk's gate tile; its buffer was last read
-                    fence_proxy_async();         // before the previous chunk's final barrier
-                    load_gate(kk + 1);
-                }
-                float ss = 0.f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float f[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(row + ((j ^ (tt & 7)) << 4)), f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-                }
-                red[hf * 64 + tt] = ss;
-                ok = mbar_wait(&bar_g[kk & 1], (kk >> 1) & 1);  // this chunk's gate tile
+            if (lenp == C) {  // full chunk: two 64 x 64 swizzled tiles, two TMA stores (double-buffered)
+                unsigned char *stg = sm + CS_OIMG + 16384 * (kk & 1);
+                if (ot == 0 && kk >= 2) bulk_wait_read1();  // the store of chunk kk - 2 has left this buffer
                 named_sync(2, 128);
-                const float r = rsqrtf((red[tt] + red[64 + tt]) * (1.0f / D) + epi.eps);
-                const unsigned char *grow = sm + CS_GIMG + 16384 * (kk & 1) + 8192 * hf + tt * 128;
-                const float *wr = epi.w ? epi.w + (size_t)h * D + 64 * hf : nullptr;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t off = (uint32_t)((j ^ (tt & 7)) << 4);
-                    float f[8], gv[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(row + off), f);
-                    unpack8(*reinterpret_cast<const uint4 *>(grow + off), gv);
-                    float4 w0 = make_float4(1.f, 1.f, 1.f, 1.f), w1 = w0;
-                    if (wr) {
-                        w0 = __ldg(reinterpret_cast<const float4 *>(wr + 8 * j));
-                        w1 = __ldg(reinterpret_cast<const float4 *>(wr + 8 * j + 4));
-                    }
-                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = f[e] * r * wv[e] / (1.0f + __expf(-gv[e]));
-                    *reinterpret_cast<uint4 *>(row + off) = pack8(f);
+                for (int t = 0; t < 64; ++t) {
+                    const uint32_t w = ob[t >> 1];
+                    *reinterpret_cast<uint16_t *>(stg + vh + t * 128 + ((vc ^ (t & 7)) << 4)) =
+                        (uint16_t)((t & 1) ? (w >> 16) : (w & 0xFFFFu));
                 }
-                ok = (bar_red_popc(2, 128, ok) == 128) && ok;
-                if (!ok) break;
-            }
-            if (lenp == C) {  // full chunk: two TMA stores
                 fence_proxy_async();
                 named_sync(2, 128);
                 if (ot == 0) {
@@ -1057,22 +988,17 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                     bulk_commit();
                 }
             } else {  // the ragged last chunk of a sequence: rows past its end stay untouched
-                named_sync(2, 128);
-                if (tt < lenp) {
-                    bf16 *dst = o + ((tp + tt) * H + h) * D + 64 * hf;
+                bf16 *dst = o + (tp * H + h) * D + v;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<uint4 *>(dst + 8 * j) =
-                            *reinterpret_cast<const uint4 *>(row + ((j ^ (tt & 7)) << 4));
+                for (int t = 0; t < 64; ++t) {
+                    const uint32_t w = ob[t >> 1];
+                    if (t < lenp)
+                        *reinterpret_cast<uint16_t *>(dst + (size_t)t * H * D) =
+                            (uint16_t)((t & 1) ? (w >> 16) : (w & 0xFFFFu));
                 }
             }
         }
-        if (ot == 0) {
-            bulk_wait0();
-            // no copy into shared memory may outlive the CTA: the last two requests (completed phases
-            // return at once; no later phase exists, so the parity is unambiguous)
-            for (int c = g_last; c >= 0 && c >= g_last - 1; --c) (void)mbar_wait(&bar_g[c & 1], (c >> 1) & 1);
-        }
+        if (ot == 0) bulk_wait0();
         if (!ok) atomicExch(s_fail, 1);
     } else if (warp < 8) {
         // ------------------------------------------------ recurrence warps 0-7: lanes of quarter lq,
@@ -1196,11 +1122,10 @@ chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N
                       const int32_t *__restrict__ chunk_start, const int32_t *__restrict__ seg_start,
                       int64_t seg_len, const float *__restrict__ seg_in, int H,
                       const unsigned char *__restrict__ packets, float scale, const float *initial_state,
-                      float *final_state, bf16 *__restrict__ o, int *err,
-                      const __grid_constant__ CUtensorMap gmap, OutEpi epi) {
+                      float *final_state, bf16 *__restrict__ o, int *err) {
     extern __shared__ unsigned char smem_raw[];
     chain_role(align1024(smem_raw), omap, T, N, cu, chunk_start, seg_start, seg_len, seg_in, H, packets, scale,
-               initial_state, final_state, o, err, (int)blockIdx.x, (int)blockIdx.y, nullptr, 0, gmap, epi);
+               initial_state, final_state, o, err, (int)blockIdx.x, (int)blockIdx.y, nullptr, 0);
 }
 
 // =====================================================================================
@@ -1217,7 +1142,7 @@ chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant
                       float g_min, int64_t T, int N, const int32_t *__restrict__ cu, int H,
                       unsigned char *__restrict__ packets, float scale, const float *initial_state,
                       float *final_state, bf16 *__restrict__ o, int *err, int n_chain, uint64_t *flags,
-                      uint64_t epoch, int kpre, const __grid_constant__ CUtensorMap gmap, OutEpi epi) {
+                      uint64_t epoch, int kpre) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1024(smem_raw);
     const int b = (int)blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1267,7 +1192,7 @@ chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant
             __syncthreads();
         }
         chain_role(sm, omap, T, N, cu, cs, ss, (int64_t)1 << 30, nullptr, H, packets, scale, initial_state,
-                   final_state, o, err, b / H, b % H, flags, epoch, gmap, epi);
+                   final_state, o, err, b / H, b % H, flags, epoch);
     } else {
         intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, cs, H, packets, err, b - n_chain,
                    (int)gridDim.x - n_chain, flags, epoch, kpre, -1, 0);
@@ -1682,8 +1607,7 @@ static kda_status_t set_smem(const void *kernel, uint32_t bytes) {
 // launch error) when the device refuses to make every CTA resident; the caller then runs the
 // separate kernels, which need the same workspace.
 static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws, cudaStream_t stream,
-                         const tcp::TileMaps &tm, const CUtensorMap &omap, const CUtensorMap &gmap,
-                         tcp::OutEpi epi, int sms, int *err) {
+                         const tcp::TileMaps &tm, const CUtensorMap &omap, int sms, int *err) {
     static std::atomic<uint64_t> next_epoch{0};
     const uint32_t smem = tcp::J_TOTAL > tcp::CS_TOTAL ? tcp::J_TOTAL : tcp::CS_TOTAL;
     if (set_smem((const void *)tcp::chunk_fused_tc_kernel, smem) != KDA_OK) return false;
@@ -1709,7 +1633,7 @@ static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void 
     float *fin = a->final_state;
     bf16 *o = (bf16 *)a->o;
     void *args[] = {(void *)&tm, (void *)&omap, &beta, &bias, &A_log, &g_min, &T, &N, &cu, &H, &packets,
-                    &scale, &init, &fin, &o, &err, &n_chain, &flags, &epoch, &kpre, (void *)&gmap, &epi};
+                    &scale, &init, &fin, &o, &err, &n_chain, &flags, &epoch, &kpre};
     if (cudaLaunchCooperativeKernel((const void *)tcp::chunk_fused_tc_kernel, dim3((unsigned)sms), dim3(tcp::NT2),
                                     args, smem, stream) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -1733,13 +1657,8 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
         !make_tile_map(&tm.v, a->v, a->T, p.H) || !make_tile_map(&tm.z, a->z, a->T, p.H) ||
         !make_tile_map(&omap, a->o, a->T, p.H))
         return KDA_ERR_CUDA;
-    // output epilogue: the gate tensor's map (same shape as o); without it the map is unused
-    CUtensorMap gmap = omap;
-    if (a->out_gate && !make_tile_map(&gmap, a->out_gate, a->T, p.H)) return KDA_ERR_CUDA;
-    const tcp::OutEpi epi{a->out_norm_weight, a->out_norm_eps, a->out_gate ? 1 : 0};
     kda_profile_mark(0, stream);
-    if (p.fused && p.max_chunks > 0 && a->T > 0 &&
-        launch_fused(a, p, ws, stream, tm, omap, gmap, epi, sms, err)) {
+    if (p.fused && p.max_chunks > 0 && a->T > 0 && launch_fused(a, p, ws, stream, tm, omap, sms, err)) {
         kda_profile_mark(1, stream);
         return kda_cuda_status(cudaGetLastError());
     }
@@ -1783,7 +1702,7 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     if (st != KDA_OK) return st;
     tcp::chunk_inter_tc_kernel<<<dim3((unsigned)p.max_segs, (unsigned)p.H), tcp::NT3, tcp::CS_TOTAL, stream>>>(
         omap, a->T, (int)a->N, a->cu_seqlens, chunk_start, seg_start, p.seg_len, seg_in, p.H, packets, a->scale,
-        a->initial_state, a->final_state, (bf16 *)a->o, err, gmap, epi);
+        a->initial_state, a->final_state, (bf16 *)a->o, err);
     kda_profile_mark(mark, stream);
     return kda_cuda_status(cudaGetLastError());
 }

@@ -2,8 +2,9 @@
 //     y[t,h,c] = Sigmoid(g[t,h,c]) * w[h,c] * o[t,h,c] / sqrt(mean_c' o[t,h,c']^2 + eps),
 // the per-head RMSNorm of the recurrent output followed by the data-dependent output gate.
 //
-// One warp per (token, head) row; each lane holds VPL = dv / 32 consecutive channels (one vector
-// load per tensor), the sum of squares is a warp-shuffle reduction.  HBM-bound: o and g are read
+// One warp per RPW (token, head) rows; each lane holds VPL = dv / 32 consecutive channels of a row (one
+// vector load per tensor), the sum of squares is a warp-shuffle reduction.  All of a warp's loads are
+// issued before the first is used, so that enough bytes are in flight to cover HBM latency.  HBM-bound: o and g are read
 // once, y written once (y may alias o: every element is read before it is written, by the same
 // thread).
 #include "kda_common.cuh"
@@ -70,43 +71,54 @@ __device__ __forceinline__ void pack(const float *f, uint32_t *w) {
     }
 }
 
+constexpr int RPW = 4;  // rows per warp: their loads are all issued before any is used
+
 template <typename T, int VPL>
 __global__ void __launch_bounds__(256) output_gate_kernel(const T *__restrict__ o, const T *__restrict__ g,
                                                           const float *__restrict__ w, float eps, int64_t rows,
                                                           int H, T *y) {
-    constexpr int DV = 32 * VPL, BYTES = VPL * (int)sizeof(T);
+    constexpr int DV = 32 * VPL, BYTES = VPL * (int)sizeof(T), WORDS = (BYTES + 3) / 4;
     const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (row >= rows) return;
-    const int h = (int)(row % H);
-    const size_t base = (size_t)row * DV + (size_t)VPL * lane;
-    uint32_t ow[(BYTES + 3) / 4], gw[(BYTES + 3) / 4];
-    ld_bytes<BYTES>(o + base, ow);
-    ld_bytes<BYTES>(g + base, gw);
-    float ov[VPL], gv[VPL];
-    unpack<T, VPL>(ow, ov);
-    unpack<T, VPL>(gw, gv);
-    float ss = 0.f;
+    const int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * RPW;
+    uint32_t ow[RPW][WORDS], gw[RPW][WORDS];
 #pragma unroll
-    for (int e = 0; e < VPL; ++e) ss = fmaf(ov[e], ov[e], ss);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float r = rsqrtf(ss * (1.0f / DV) + eps);
-    float yv[VPL];
-#pragma unroll
-    for (int e = 0; e < VPL; ++e) {
-        const float wv = w ? w[(size_t)h * DV + VPL * lane + e] : 1.f;
-        yv[e] = ov[e] * r * wv / (1.0f + __expf(-gv[e]));
+    for (int i = 0; i < RPW; ++i) {
+        if (row0 + i < rows) {
+            const size_t base = (size_t)(row0 + i) * DV + (size_t)VPL * lane;
+            ld_bytes<BYTES>(o + base, ow[i]);
+            ld_bytes<BYTES>(g + base, gw[i]);
+        }
     }
-    uint32_t yw[(BYTES + 3) / 4];
-    pack<T, VPL>(yv, yw);
-    st_bytes<BYTES>(y + base, yw);
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        const int64_t row = row0 + i;
+        if (row >= rows) break;  // warp-uniform
+        const int h = (int)(row % H);
+        float ov[VPL], gv[VPL];
+        unpack<T, VPL>(ow[i], ov);
+        unpack<T, VPL>(gw[i], gv);
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < VPL; ++e) ss = fmaf(ov[e], ov[e], ss);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float r = rsqrtf(ss * (1.0f / DV) + eps);
+        float yv[VPL];
+#pragma unroll
+        for (int e = 0; e < VPL; ++e) {
+            const float wv = w ? __ldg(w + (size_t)h * DV + VPL * lane + e) : 1.f;
+            yv[e] = __fdividef(ov[e] * r * wv, 1.0f + __expf(-gv[e]));  // 1 + e^{-g} >= 1; inf gives 0
+        }
+        uint32_t yw[WORDS];
+        pack<T, VPL>(yv, yw);
+        st_bytes<BYTES>(y + (size_t)row * DV + (size_t)VPL * lane, yw);
+    }
 }
 
 template <typename T>
 static kda_status_t launch_t(const kda_output_gate_args *a, cudaStream_t stream) {
     const int64_t rows = a->T * (int64_t)a->H;
-    const unsigned grid = (unsigned)((rows + 7) / 8);
+    const unsigned grid = (unsigned)((rows + 8 * RPW - 1) / (8 * RPW));
     const T *o = (const T *)a->o, *g = (const T *)a->g;
     T *y = (T *)a->y;
     switch (a->dv) {
