@@ -15,6 +15,9 @@ passage of the Kimi K3 technical report (section 2.1.1 unless stated):
                      test that it equals ``recurrence``.
 * ``segment_maps``-- section 5.1.2, Eq. 17: a segment's cumulative transition
                      M and its zero-start state S~, so that S_out = M S_in + S~.
+* ``replay``      -- section 5.4 (KDA decode): speculative decoding with replay,
+                     the committed state advanced over accepted cached drafts
+                     and committed new tokens, outputs for every new token.
 * ``output_gate`` -- Eq. 6 without the projections W_o and W_g: the per-head
                      RMSNorm of the recurrent output, then the output gate
                      Sigmoid(g) with g = W_g x given.
@@ -169,3 +172,23 @@ def output_gate(o, g, w=None, eps=1e-6):
         normed = normed * np.asarray(w, dtype=np.float64)
     with np.errstate(over="ignore"):
         return normed / (1.0 + np.exp(-g))
+
+
+def replay(cached, n_replay, new, n_commit, S0, scale=1.0):
+    """Section 5.4 (KDA decode): speculative decoding with replay, one (sequence, head).
+
+    cached, new: tuples (q, k, v, g, beta) of the cached draft window and of the new tokens (bonus
+    token, then the next drafts), token-major.  From the committed state S0: the first n_replay cached
+    tokens are replayed (Eq. 1), then every new token runs (Eq. 1) and yields an output; the committed
+    state is the one reached after the replayed tokens and the first n_commit new tokens (S0 itself when
+    there are none).  Returns (o_new [M, d_v], S_committed [d_k, d_v]).
+    """
+    parts = [np.concatenate([np.asarray(cached[i], np.float64)[:n_replay], np.asarray(new[i], np.float64)])
+             for i in range(5)]
+    o, _ = recurrence(*parts, S0=S0, scale=scale)
+    m = n_replay + n_commit
+    if m == 0:
+        S = np.array(S0, dtype=np.float64)
+    else:
+        _, S = recurrence(*(x[:m] for x in parts), S0=S0, scale=scale)
+    return o[n_replay:], S

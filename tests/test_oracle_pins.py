@@ -429,3 +429,42 @@ def test_output_gate_fixture_catches_planted_mistakes(mutant):
     failures = sum(not np.allclose(f(np.array(o), g, np.array(w), eps), y, rtol=1e-12, atol=1e-12)
                    for eps, o, g, w, y in _output_gate_rows())
     assert failures >= 1, "a planted mistake passed every output-gate fixture"
+
+
+# ----------------------------------------------------------------------------- speculative replay (section 5.4)
+
+def _tokens(rng, T, dk, dv):
+    k = rng.normal(size=(T, dk))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    return (rng.normal(size=(T, dk)), k, rng.normal(size=(T, dv)), -rng.uniform(0.0, 1.0, size=(T, dk)),
+            rng.uniform(0.1, 0.9, size=T))
+
+
+def test_replay_without_cache_is_the_recurrence():
+    rng = np.random.default_rng(11)
+    new = _tokens(rng, 5, 4, 3)
+    S0 = rng.normal(size=(4, 3))
+    o, S = R.replay(_tokens(rng, 0, 4, 3), 0, new, 5, S0)
+    o_ref, S_ref = R.recurrence(*new, S0=S0)
+    assert np.allclose(o, o_ref, rtol=1e-14, atol=1e-14) and np.allclose(S, S_ref, rtol=1e-14, atol=1e-14)
+
+
+def test_replay_commit_is_a_prefix_state_and_drafts_leave_it():
+    """The committed state equals the recurrence over accepted cached tokens then committed new ones,
+    i.e. the state a one-token-at-a-time decoder would hold; outputs of the new tokens do not depend on
+    how many are committed; nothing replayed or committed leaves S0 untouched."""
+    rng = np.random.default_rng(12)
+    cached, new = _tokens(rng, 4, 5, 3), _tokens(rng, 3, 5, 3)
+    S0 = rng.normal(size=(5, 3))
+    S = S0.copy()
+    for t in range(2):  # two accepted cached drafts, one token at a time
+        _, S = R.recurrence(*(x[t:t + 1] for x in cached), S0=S)
+    o_ref, _ = R.recurrence(*new, S0=S)
+    _, S_after_bonus = R.recurrence(*(x[:1] for x in new), S0=S)
+    for nc in range(4):
+        o, Sc = R.replay(cached, 2, new, nc, S0)
+        assert np.allclose(o, o_ref, rtol=1e-13, atol=1e-13)
+    o1, S1 = R.replay(cached, 2, new, 1, S0)
+    assert np.allclose(S1, S_after_bonus, rtol=1e-13, atol=1e-13)
+    _, Sz = R.replay(cached, 0, new, 0, S0)
+    assert np.array_equal(Sz, S0)
