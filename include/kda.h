@@ -61,7 +61,8 @@ typedef enum {
     KDA_ERR_BAD_SEQLENS = 7,       /* (device) cu_seqlens not 0 = c_0 <= c_1 <= ... <= c_N = T */
     KDA_ERR_BAD_STATE_INDEX = 8,   /* (device) state_indices entry outside [0, num_slots) */
     KDA_ERR_NO_DEVICE = 9,         /* no current CUDA device of compute capability 10.3 */
-    KDA_ERR_DEVICE_TIMEOUT = 10    /* (device) a bounded wait inside a kernel gave up */
+    KDA_ERR_DEVICE_TIMEOUT = 10,   /* (device) a bounded wait inside a kernel gave up */
+    KDA_ERR_BAD_TOKEN_COUNT = 11   /* (device) n_replay / n_commit entry outside its range */
 } kda_status_t;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
@@ -141,6 +142,48 @@ size_t kda_chunk_fwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk,
  * and are garbage afterwards.  Calls that share a workspace must not overlap. */
 kda_status_t kda_chunk_fwd(const kda_chunk_args *args, void *workspace, size_t workspace_bytes,
                            struct CUstream_st *stream);
+
+/* ------------------------------------------------------ kda_recurrent_replay
+ * Speculative decoding with replay (section 5.4, KDA decode kernel): instead of
+ * keeping a state snapshot per draft position, only the draft tokens' projected
+ * inputs are cached; the state of the accepted drafts is rebuilt on chip from
+ * them, and the replayed tokens, the bonus token and the next draft window run
+ * in one loop.  Per (sequence n, head h), starting from the committed state
+ * S = state[slot(n), h]:
+ *   1. replay tokens 0 .. n_replay[n] - 1 of the cached window (Eq. 1; no outputs);
+ *   2. run the M new tokens in order (Eq. 1), writing o for each;
+ *   3. write back the state reached after the replayed tokens and the first
+ *      n_commit[n] new tokens (typically the bonus token); later new tokens are
+ *      drafts: their outputs are written, their state is not.  When
+ *      n_replay[n] + n_commit[n] = 0 the state is left untouched.
+ * The state crosses HBM once (read) plus once (write) per call, whatever the
+ * number of tokens.  Counts outside [0, R] / [0, M] set KDA_ERR_BAD_TOKEN_COUNT
+ * on the device and skip that sequence.  Shapes as kda_recurrent_step.
+ */
+typedef struct {
+    int64_t N;                     /* sequences */
+    int32_t H, dk, dv;             /* heads; dk = dv in {64, 128} */
+    kda_dtype_t dtype;             /* dtype of every token input and of o */
+    int32_t R;                     /* cached tokens per sequence (replay window), >= 0 */
+    const void *rq, *rk, *rz;      /* [N, R, H, dk] cached inputs (may be NULL when R == 0) */
+    const void *rv;                /* [N, R, H, dv] */
+    const void *rbeta;             /* [N, R, H] */
+    const int32_t *n_replay;       /* [N] device: accepted cached tokens to replay, 0 .. R */
+    int32_t M;                     /* new tokens per sequence (bonus token, then drafts), >= 1 */
+    const void *q, *k, *z;         /* [N, M, H, dk] */
+    const void *v;                 /* [N, M, H, dv] */
+    const void *beta;              /* [N, M, H] */
+    const int32_t *n_commit;       /* [N] device: new tokens whose state is committed, 0 .. M */
+    const float *dt_bias;          /* [H, dk] or NULL */
+    const float *A_log;            /* [H] or NULL */
+    float g_min, scale;            /* as kda_recurrent_step */
+    float *state;                  /* [num_slots, H, dk, dv] committed states, updated in place */
+    const int32_t *state_indices;  /* [N] slot of each sequence, or NULL (slot n) */
+    int64_t num_slots;             /* 0 = N */
+    void *o;                       /* [N, M, H, dv] outputs of the new tokens */
+} kda_replay_args;
+
+kda_status_t kda_recurrent_replay(const kda_replay_args *args, struct CUstream_st *stream);
 
 /* ----------------------------------------------------------- kda_output_gate
  * The output epilogue of Eq. 6 (section 2.1.1), y_t = W_o[Sigmoid(W_g x_t) * RMSNorm(o~_t)], without

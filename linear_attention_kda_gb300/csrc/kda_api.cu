@@ -113,6 +113,7 @@ const char *kda_status_string(kda_status_t s) {
         case KDA_ERR_BAD_STATE_INDEX: return "state index outside [0, num_slots)";
         case KDA_ERR_NO_DEVICE: return "no current CUDA device of compute capability 10.3";
         case KDA_ERR_DEVICE_TIMEOUT: return "bounded wait inside a kernel gave up";
+        case KDA_ERR_BAD_TOKEN_COUNT: return "n_replay or n_commit entry outside its range";
     }
     return "unknown status";
 }
@@ -260,6 +261,34 @@ kda_status_t kda_recurrent_step(const kda_step_args *a, struct CUstream_st *stre
     kda_status_t st = check_device();
     if (st != KDA_OK) return st;
     return kda_launch_decode(a, (cudaStream_t)stream);
+}
+
+kda_status_t kda_recurrent_replay(const kda_replay_args *a, struct CUstream_st *stream) {
+    if (!a) return KDA_ERR_INVALID_ARG;
+    if (a->N < 0 || a->H < 1 || a->num_slots < 0 || a->R < 0 || a->M < 1) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(a->dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (a->dk != a->dv || (a->dk != 64 && a->dk != 128)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!(a->g_min < 0.f) || !isfinite(a->g_min) || !isfinite(a->scale)) return KDA_ERR_INVALID_ARG;
+    if (a->N == 0) return KDA_OK;
+    if (a->N * (int64_t)a->H > INT32_MAX || a->N * (int64_t)(a->R > a->M ? a->R : a->M) * a->H > INT32_MAX)
+        return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!a->q || !a->k || !a->v || !a->z || !a->beta || !a->o || !a->state || !a->n_commit)
+        return KDA_ERR_INVALID_ARG;
+    if (a->R > 0 && (!a->rq || !a->rk || !a->rv || !a->rz || !a->rbeta || !a->n_replay))
+        return KDA_ERR_INVALID_ARG;
+    if (!a->state_indices && a->num_slots != 0 && a->num_slots < a->N) return KDA_ERR_INVALID_ARG;
+    const size_t es = dtype_size(a->dtype);
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->z) || !aligned16(a->o) ||
+        !aligned16(a->state) || !aligned_to(a->beta, es) || !aligned_to(a->n_commit, 4) ||
+        (a->dt_bias && !aligned16(a->dt_bias)) || (a->A_log && !aligned_to(a->A_log, 4)) ||
+        (a->state_indices && !aligned_to(a->state_indices, 4)))
+        return KDA_ERR_MISALIGNED;
+    if (a->R > 0 && (!aligned16(a->rq) || !aligned16(a->rk) || !aligned16(a->rv) || !aligned16(a->rz) ||
+                     !aligned_to(a->rbeta, es) || !aligned_to(a->n_replay, 4)))
+        return KDA_ERR_MISALIGNED;
+    kda_status_t st = check_device();
+    if (st != KDA_OK) return st;
+    return kda_launch_replay(a, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -13,6 +13,7 @@ kda_status_t kda_cuda_status(cudaError_t e);
 kda_status_t kda_launch_gate(const kda_gate_args *a, cudaStream_t stream);
 kda_status_t kda_launch_output_gate(const kda_output_gate_args *a, cudaStream_t stream);
 kda_status_t kda_launch_decode(const kda_step_args *a, cudaStream_t stream);
+kda_status_t kda_launch_replay(const kda_replay_args *a, cudaStream_t stream);
 
 // Chunked prefill.  Workspace layout is owned by kda_chunk_plan.cu.
 constexpr int KDA_FUSED_MAX_SEQS = 159;  // sequences the fused schedule's producer item map holds

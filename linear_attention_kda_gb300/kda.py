@@ -22,12 +22,12 @@ _STATUS = {
     0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
     3: "KDA_ERR_UNSUPPORTED_DTYPE", 4: "KDA_ERR_MISALIGNED", 5: "KDA_ERR_WORKSPACE",
     6: "KDA_ERR_CUDA", 7: "KDA_ERR_BAD_SEQLENS", 8: "KDA_ERR_BAD_STATE_INDEX",
-    9: "KDA_ERR_NO_DEVICE", 10: "KDA_ERR_DEVICE_TIMEOUT",
+    9: "KDA_ERR_NO_DEVICE", 10: "KDA_ERR_DEVICE_TIMEOUT", 11: "KDA_ERR_BAD_TOKEN_COUNT",
 }
 EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step",
             "kda_status_string", "kda_get_device_error", "kda_abi_version",
             "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws",
-            "kda_last_cuda_error", "kda_chunk_fwd_schedule", "kda_output_gate"]
+            "kda_last_cuda_error", "kda_chunk_fwd_schedule", "kda_output_gate", "kda_recurrent_replay"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 _vp = ctypes.c_void_p
@@ -47,6 +47,14 @@ class ChunkArgs(ctypes.Structure):
                 ("cu_seqlens", _vp), ("cu_seqlens_host", _vp), ("initial_state", _vp),
                 ("final_state", _vp), ("o", _vp), ("chunk_size", _i32),
                 ("out_gate", _vp), ("out_norm_weight", _vp), ("out_norm_eps", _f32)]
+
+
+class ReplayArgs(ctypes.Structure):
+    _fields_ = [("N", _i64), ("H", _i32), ("dk", _i32), ("dv", _i32), ("dtype", ctypes.c_int), ("R", _i32),
+                ("rq", _vp), ("rk", _vp), ("rz", _vp), ("rv", _vp), ("rbeta", _vp), ("n_replay", _vp),
+                ("M", _i32), ("q", _vp), ("k", _vp), ("z", _vp), ("v", _vp), ("beta", _vp), ("n_commit", _vp),
+                ("dt_bias", _vp), ("A_log", _vp), ("g_min", _f32), ("scale", _f32), ("state", _vp),
+                ("state_indices", _vp), ("num_slots", _i64), ("o", _vp)]
 
 
 class OutputGateArgs(ctypes.Structure):
@@ -103,6 +111,8 @@ def load_library(path: Optional[str] = None):
         L.kda_chunk_fwd_schedule.restype = ctypes.c_int
         L.kda_chunk_fwd_static_ws.argtypes = [ctypes.POINTER(ChunkArgs), _vp]
         L.kda_chunk_fwd_static_ws.restype = ctypes.c_int
+        L.kda_recurrent_replay.argtypes = [ctypes.POINTER(ReplayArgs), _vp]
+        L.kda_recurrent_replay.restype = ctypes.c_int
         L.kda_output_gate.argtypes = [ctypes.POINTER(OutputGateArgs), _vp]
         L.kda_output_gate.restype = ctypes.c_int
         L.kda_last_cuda_error.argtypes = []
@@ -227,6 +237,36 @@ def recurrent_step(q, k, v, z, beta, dt_bias, A_log, state, *, g_min: float = -5
                  scale=scale, state=_ptr(state), state_indices=_ptr(state_indices),
                  num_slots=state.shape[0], o=_ptr(o))
     _check(L.kda_recurrent_step(ctypes.byref(a), _stream(q)), "kda_recurrent_step")
+    return o
+
+
+def recurrent_replay(cached, n_replay, new, n_commit, dt_bias, A_log, state, *, g_min: float = -5.0,
+                     scale: float = 1.0, state_indices: Optional[torch.Tensor] = None,
+                     out: Optional[torch.Tensor] = None):
+    """kda_recurrent_replay: speculative decoding with replay (section 5.4).
+
+    cached: (q, k, z, v, beta) of the cached draft window, [N, R, H, d] / [N, R, H] (or None: R = 0);
+    new: (q, k, z, v, beta) of the new tokens, [N, M, H, d] / [N, M, H]; n_replay, n_commit: int32 [N]
+    on the device.  Replays the accepted cached tokens, runs the new ones (outputs returned,
+    [N, M, H, dv]) and writes back the state after the first n_commit new tokens, in place."""
+    L = load_library()
+    q, k, z, v, beta = new
+    N, M, H, dk = q.shape
+    dv = v.shape[3]
+    if cached is None:
+        rq = rk = rz = rv = rb = None
+        R = 0
+    else:
+        rq, rk, rz, rv, rb = cached
+        R = rq.shape[1]
+    _contig(q, k, z, v, beta, rq, rk, rz, rv, rb, n_replay, n_commit, dt_bias, A_log, state, state_indices)
+    o = out if out is not None else torch.empty((N, M, H, dv), dtype=q.dtype, device=q.device)
+    a = ReplayArgs(N=N, H=H, dk=dk, dv=dv, dtype=_dtype_code(q), R=R, rq=_ptr(rq), rk=_ptr(rk), rz=_ptr(rz),
+                   rv=_ptr(rv), rbeta=_ptr(rb), n_replay=_ptr(n_replay), M=M, q=_ptr(q), k=_ptr(k), z=_ptr(z),
+                   v=_ptr(v), beta=_ptr(beta), n_commit=_ptr(n_commit), dt_bias=_ptr(dt_bias),
+                   A_log=_ptr(A_log), g_min=g_min, scale=scale, state=_ptr(state),
+                   state_indices=_ptr(state_indices), num_slots=state.shape[0], o=_ptr(o))
+    _check(L.kda_recurrent_replay(ctypes.byref(a), _stream(q)), "kda_recurrent_replay")
     return o
 
 

@@ -63,6 +63,7 @@ int main(void) {
   printf("kda_chunk_args sizeof %zu\n", sizeof(kda_chunk_args));
   printf("kda_step_args sizeof %zu\n", sizeof(kda_step_args));
   printf("kda_output_gate_args sizeof %zu\n", sizeof(kda_output_gate_args));
+  printf("kda_replay_args sizeof %zu\n", sizeof(kda_replay_args));
   %FIELDS%
   return 0;
 }
@@ -72,7 +73,8 @@ int main(void) {
 def test_struct_layout_matches_header(tmp_path):
     fields = []
     for cname, cls in (("kda_gate_args", kda.GateArgs), ("kda_chunk_args", kda.ChunkArgs),
-                       ("kda_step_args", kda.StepArgs), ("kda_output_gate_args", kda.OutputGateArgs)):
+                       ("kda_step_args", kda.StepArgs), ("kda_output_gate_args", kda.OutputGateArgs),
+                       ("kda_replay_args", kda.ReplayArgs)):
         for f, _ in cls._fields_:
             fields.append(f"F({cname}, {f})")
     src = tmp_path / "layout.c"
@@ -86,7 +88,8 @@ def test_struct_layout_matches_header(tmp_path):
             s, f, v = ln.split()
             got[(s, f)] = int(v)
     for cname, cls in (("kda_gate_args", kda.GateArgs), ("kda_chunk_args", kda.ChunkArgs),
-                       ("kda_step_args", kda.StepArgs), ("kda_output_gate_args", kda.OutputGateArgs)):
+                       ("kda_step_args", kda.StepArgs), ("kda_output_gate_args", kda.OutputGateArgs),
+                       ("kda_replay_args", kda.ReplayArgs)):
         assert got[(cname, "sizeof")] == ctypes.sizeof(cls), cname
         for f, _ in cls._fields_:
             assert got[(cname, f)] == getattr(cls, f).offset, (cname, f)
@@ -215,6 +218,33 @@ def test_output_gate_rejects(lib, kw, code):
     assert lib.kda_output_gate(ctypes.byref(_og(**kw)), None) == code
 
 
+def _rp(**kw):
+    base = dict(N=4, H=2, dk=128, dv=128, dtype=kda.KDA_BF16, R=3, rq=FAKE, rk=FAKE + 1024, rz=FAKE + 2048,
+                rv=FAKE + 4096, rbeta=FAKE + 8192, n_replay=FAKE + 12288, M=2, q=FAKE + 16384, k=FAKE + 20480,
+                z=FAKE + 24576, v=FAKE + 28672, beta=FAKE + 32768, n_commit=FAKE + 36864, dt_bias=None,
+                A_log=None, g_min=-5.0, scale=1.0, state=FAKE + 65536, state_indices=None, num_slots=0,
+                o=FAKE + 40960)
+    base.update(kw)
+    return kda.ReplayArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dk=96, dv=96), 2),
+    (dict(dtype=5), 3),
+    (dict(M=0), 1),
+    (dict(R=-1), 1),
+    (dict(n_commit=None), 1),
+    (dict(n_replay=None), 1),        # R > 0 needs the replay counts
+    (dict(rq=None), 1),
+    (dict(state=FAKE + 65544), 4),
+    (dict(rq=FAKE + 8), 4),
+    (dict(n_commit=FAKE + 36866), 4),
+    (dict(g_min=1.0), 1),
+])
+def test_recurrent_replay_rejects(lib, kw, code):
+    assert lib.kda_recurrent_replay(ctypes.byref(_rp(**kw)), None) == code
+
+
 def test_empty_inputs_are_noops(lib):
     # T = 0 gate / N = 0 decode return KDA_OK before touching any pointer or the device
     a = kda.GateArgs(T=0, N=1, H=1, dk=16, dtype=kda.KDA_F32, z=None, dt_bias=None, A_log=None,
@@ -222,6 +252,7 @@ def test_empty_inputs_are_noops(lib):
     assert lib.kda_gate(ctypes.byref(a), None) == 0
     assert lib.kda_recurrent_step(ctypes.byref(_step(N=0, q=None)), None) == 0
     assert lib.kda_output_gate(ctypes.byref(_og(T=0, o=None, g=None, y=None)), None) == 0
+    assert lib.kda_recurrent_replay(ctypes.byref(_rp(N=0, q=None)), None) == 0
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
@@ -230,3 +261,4 @@ def test_valid_args_stop_at_device_check_without_gpu(lib):
     assert _call_chunk(lib, _chunk()) == 9
     assert lib.kda_recurrent_step(ctypes.byref(_step()), None) == 9
     assert lib.kda_output_gate(ctypes.byref(_og()), None) == 9
+    assert lib.kda_recurrent_replay(ctypes.byref(_rp()), None) == 9

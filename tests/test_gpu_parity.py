@@ -371,3 +371,90 @@ def test_epilogue_through_prefill_equals_separate_call():
     o_s = kda.output_gate(o_p.to(torch.bfloat16).cuda(), g.cuda(), w.cuda(), EPS).float().cpu()
     for h in range(4):
         assert rel_err(o_f[:, h].numpy(), o_s[:, h].numpy()) <= 1e-6
+
+
+# ----------------------------------------------------------------------------- speculative replay (section 5.4)
+
+def _replay_inputs(D, dtype, N, H, Rw, M, seed):
+    w = syn.Workload("rp", H=H, d=D, dtype=dtype, n_seq=N, seq_len=1, z_std=1.5, b_range=1.0,
+                     alog_std=0.25, s0_std=0.02, decode_steps=Rw + M)
+    d = syn.make_decode(w, seed=seed)
+    win = lambda name, a, b: d[name][a:b].transpose(0, 1).contiguous()  # noqa: E731  [N, L, H, ...]
+    cached = tuple(win(n, 0, Rw) for n in ("q", "k", "z", "v", "beta"))
+    new = tuple(win(n, Rw, Rw + M) for n in ("q", "k", "z", "v", "beta"))
+    return d, cached, new
+
+
+def _replay_oracle(d, cached, new, nr, nc, n, h):
+    def tup(t):
+        q, k, z, v, beta = (x[n, :, h].double().numpy() for x in t)
+        g = R.gate(z, d["dt_bias"][h].double().numpy(), float(d["A_log"][h]), d["g_min"])
+        return q, k, v, g, beta
+    return R.replay(tup(cached), nr, tup(new), nc, d["state"][n, h].double().numpy())
+
+
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "f32"), (128, "f32"), (64, "bf16")])
+def test_recurrent_replay_matches_oracle(D, dtype):
+    """Accepted cached drafts replayed, bonus and new drafts run; every replay / commit count from 0 to
+    the window, permuted state slots with a spare slot left untouched."""
+    N, H, Rw, M = 6, 3, 4, 3
+    d, cached, new = _replay_inputs(D, dtype, N, H, Rw, M, seed=13)
+    nr = torch.tensor([0, 4, 2, 1, 3, 4], dtype=torch.int32)
+    nc = torch.tensor([1, 0, 3, 1, 2, 1], dtype=torch.int32)
+    slots = torch.tensor([5, 0, 3, 1, 2, 6], dtype=torch.int32)
+    pool = torch.randn((7, H, D, D)) * 0.02
+    pool[slots.long()] = d["state"]
+    pool_gpu = pool.cuda()
+    o = kda.recurrent_replay(tuple(x.cuda() for x in cached), nr.cuda(), tuple(x.cuda() for x in new), nc.cuda(),
+                             d["dt_bias"].cuda(), d["A_log"].cuda(), pool_gpu, state_indices=slots.cuda())
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    tol = TOL_F32 if dtype == "f32" else TOL_BF16
+    out = pool_gpu.cpu()
+    for n in range(N):
+        for h in range(H):
+            o_ref, S_ref = _replay_oracle(d, cached, new, int(nr[n]), int(nc[n]), n, h)
+            assert rel_err(o[n, :, h].float().cpu().numpy(), o_ref) <= tol, (n, h)
+            assert rel_err(out[int(slots[n]), h].numpy(), S_ref) <= tol, (n, h)
+    assert torch.equal(out[4], pool[4])  # spare slot untouched
+
+
+def test_recurrent_replay_equals_single_steps():
+    """Replaying the accepted drafts and committing the bonus token leaves the state that one decode
+    step per token would leave; the new tokens' outputs are those of continued single steps."""
+    D, N, H, Rw, M = 128, 4, 2, 3, 4
+    d, cached, new = _replay_inputs(D, "bf16", N, H, Rw, M, seed=14)
+    nr = torch.full((N,), Rw, dtype=torch.int32)
+    nc = torch.ones((N,), dtype=torch.int32)
+    st_r = d["state"].clone().cuda()
+    o_r = kda.recurrent_replay(tuple(x.cuda() for x in cached), nr.cuda(), tuple(x.cuda() for x in new),
+                               nc.cuda(), d["dt_bias"].cuda(), d["A_log"].cuda(), st_r)
+    st_s = d["state"].clone().cuda()
+    outs = []
+    for s in range(Rw + M):
+        args = [d[n][s].contiguous().cuda() for n in ("q", "k", "v", "z", "beta")]
+        outs.append(kda.recurrent_step(*args, d["dt_bias"].cuda(), d["A_log"].cuda(), st_s).float().cpu())
+        if s == Rw:  # after the bonus token: the committed state
+            st_commit = st_s.clone()
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    for n in range(N):
+        for h in range(H):
+            assert rel_err(st_r[n, h].cpu().numpy(), st_commit[n, h].cpu().numpy()) <= 1e-5
+            o_steps = torch.stack([outs[Rw + j][n, h] for j in range(M)]).numpy()
+            assert rel_err(o_r[n, :, h].float().cpu().numpy(), o_steps) <= 1e-2
+
+
+def test_recurrent_replay_nothing_committed_and_bad_counts():
+    D, N, H = 64, 2, 2
+    d, cached, new = _replay_inputs(D, "f32", N, H, 2, 2, seed=15)
+    st = d["state"].clone().cuda()
+    kda.recurrent_replay(tuple(x.cuda() for x in cached), torch.zeros(N, dtype=torch.int32, device="cuda"),
+                         tuple(x.cuda() for x in new), torch.zeros(N, dtype=torch.int32, device="cuda"),
+                         d["dt_bias"].cuda(), d["A_log"].cuda(), st)
+    assert kda.get_device_error() == 0
+    assert torch.equal(st.cpu(), d["state"])  # nothing replayed or committed: untouched
+    kda.recurrent_replay(tuple(x.cuda() for x in cached), torch.tensor([0, 3], dtype=torch.int32, device="cuda"),
+                         tuple(x.cuda() for x in new), torch.zeros(N, dtype=torch.int32, device="cuda"),
+                         d["dt_bias"].cuda(), d["A_log"].cuda(), st)
+    assert kda.get_device_error() == 11
