@@ -6,7 +6,8 @@
 //
 // Layout and per-token algebra are those of the decode step (kda_decode.cu): one CTA per (sequence,
 // head) state, 2 D threads, warp w holding rows [16 w, 16 w + 16), lane l holding D / 32 consecutive
-// columns; per token
+// columns.  The inputs of up to 8 tokens at a time (they do not depend on the state) are staged in
+// shared memory with all their loads in flight together; per token
 //     S' = Diag(alpha) S,  p = S'^T k,  r = S'^T q,  e = beta (v - p),
 //     S <- S' + k e^T,     o = scale (r + (k . q) e)
 // (Eq. 1, section 2.1.1).  The state is read once and written at most once per call, after the last
@@ -39,7 +40,7 @@ template <typename Tio> struct Tokens {
 };
 
 template <int D, typename Tio>
-__global__ void __launch_bounds__(2 * D)
+__global__ void __launch_bounds__(2 * D, 2)
 replay_kernel(Tokens<Tio> rt, const int32_t *__restrict__ n_replay, Tokens<Tio> nt,
               const int32_t *__restrict__ n_commit, const float *__restrict__ bias,
               const float *__restrict__ A_log, float g_min, float scale, float *__restrict__ state,
@@ -52,9 +53,11 @@ replay_kernel(Tokens<Tio> rt, const int32_t *__restrict__ n_replay, Tokens<Tio> 
     using VT = typename V::T;
     static_assert(RPW == 16, "layout assumes 16 rows per warp");
 
-    __shared__ float s_alpha[D], s_k[D], s_q[D], s_v[D], s_e[D];
-    __shared__ float s_p[NW][D], s_r[NW][D];
-    __shared__ float s_kq, s_beta;
+    constexpr int G = 8;          // tokens whose inputs are staged at a time
+    constexpr int IT = G * D / NT;  // staging iterations: thread t holds channel t % D of tokens 2 i + t / D
+    constexpr int KQP = D / 32;     // per-warp partial sums of k . q per token
+    __shared__ float s_alpha[G][D], s_k[G][D], s_q[G][D], s_v[G][D], s_beta[G], s_kqp[G][KQP];
+    __shared__ float s_p[NW][D], s_r[NW][D], s_e[D];
 
     const int64_t bid = blockIdx.x;
     const int64_t n = bid / H;
@@ -78,82 +81,121 @@ replay_kernel(Tokens<Tio> rt, const int32_t *__restrict__ n_replay, Tokens<Tio> 
     float *Sh = state + (slot * H + h) * (int64_t)(D * D);
     const int row0 = warp * RPW;
     const int col0 = lane * VW;
+    const int c_in = tid % D;  // the channel this thread stages
+    const float b_in = bias ? bias[h * D + c_in] : 0.f;
+    const float eA = A_log ? expf(A_log[h]) : 1.f;
+    const int total = nr + nt.L, last_commit = nr + nc - 1;
 
+    // raw inputs of one group, all loads issued before any is used
+    float zr[IT], kr_[IT], qr_[IT], vr[IT], br = 0.f;
+    auto fetch = [&](int g0) {
+        const int gn = min(G, total - g0);
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int jj = it * (NT / D) + tid / D, j = g0 + jj;
+            if (jj < gn) {
+                const bool is_new = j >= nr;
+                const int64_t tok = (n * (is_new ? nt.L : rt.L) + (is_new ? j - nr : j)) * H + h;  // [N, L, H]
+                zr[it] = ld((is_new ? nt.z : rt.z) + tok * D + c_in);
+                kr_[it] = ld((is_new ? nt.k : rt.k) + tok * D + c_in);
+                qr_[it] = ld((is_new ? nt.q : rt.q) + tok * D + c_in);
+                vr[it] = ld((is_new ? nt.v : rt.v) + tok * D + c_in);
+            }
+        }
+        if (tid < gn) {
+            const int j = g0 + tid;
+            const bool is_new = j >= nr;
+            const int64_t tok = (n * (is_new ? nt.L : rt.L) + (is_new ? j - nr : j)) * H + h;
+            br = ld((is_new ? nt.beta : rt.beta) + tok);
+        }
+    };
+    auto stage = [&](int g0) {
+        const int gn = min(G, total - g0);
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int jj = it * (NT / D) + tid / D;
+            if (jj < gn) {  // warp-uniform: D is a multiple of 32
+                s_alpha[jj][c_in] = expf(gate_logdecay(zr[it], b_in, eA, g_min));
+                s_k[jj][c_in] = kr_[it];
+                s_q[jj][c_in] = qr_[it];
+                s_v[jj][c_in] = vr[it];
+                float kq = kr_[it] * qr_[it];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+                if (lane == 0) s_kqp[jj][c_in / 32] = kq;
+            }
+        }
+        if (tid < gn) s_beta[tid] = br;
+    };
+
+    if (total > 0) fetch(0);  // the first group's inputs are in flight with the state
     VT s[RPW];
 #pragma unroll
     for (int i = 0; i < RPW; ++i)
         s[i] = __ldcs(reinterpret_cast<const VT *>(Sh + (row0 + i) * D + col0));
-    const float eA = A_log ? expf(A_log[h]) : 1.f;
-    const float b = (bias && tid < D) ? bias[h * D + tid] : 0.f;
 
-    const int total = nr + nt.L, last_commit = nr + nc - 1;
-    for (int j = 0; j < total; ++j) {
-        const bool is_new = j >= nr;
-        const int64_t tok = (n * (is_new ? nt.L : rt.L) + (is_new ? j - nr : j)) * H + h;  // [N, L, H] index
-        if (tid < D) {
-            s_alpha[tid] = expf(gate_logdecay(ld((is_new ? nt.z : rt.z) + tok * D + tid), b, eA, g_min));
-            s_k[tid] = ld((is_new ? nt.k : rt.k) + tok * D + tid);
-            s_q[tid] = ld((is_new ? nt.q : rt.q) + tok * D + tid);
-            s_v[tid] = ld((is_new ? nt.v : rt.v) + tok * D + tid);
-        }
-        if (tid == 0) s_beta = ld((is_new ? nt.beta : rt.beta) + tok);
+    for (int g0 = 0; g0 < total; g0 += G) {
+        const int gn = min(G, total - g0);
+        if (g0 > 0) fetch(g0);
+        stage(g0);
         __syncthreads();
-        if (warp == 0 && is_new) {  // k . q (only outputs use it)
-            float acc = 0.f;
+        for (int jj = 0; jj < gn; ++jj) {
+            const int j = g0 + jj;
+            const bool is_new = j >= nr;
+            float p[VW], r[VW];
 #pragma unroll
-            for (int i = lane; i < D; i += 32) acc += s_k[i] * s_q[i];
+            for (int c = 0; c < VW; ++c) p[c] = r[c] = 0.f;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (lane == 0) s_kq = acc;
-        }
-        float p[VW], r[VW];
+            for (int i = 0; i < RPW; ++i) {
+                const int row = row0 + i;
+                V::scale(s[i], s_alpha[jj][row]);
+                const float kr = s_k[jj][row], qr = s_q[jj][row];
 #pragma unroll
-        for (int c = 0; c < VW; ++c) p[c] = r[c] = 0.f;
-#pragma unroll
-        for (int i = 0; i < RPW; ++i) {
-            const int row = row0 + i;
-            V::scale(s[i], s_alpha[row]);
-            const float kr = s_k[row], qr = s_q[row];
+                for (int c = 0; c < VW; ++c) {
+                    const float x = V::get(s[i], c);
+                    p[c] += x * kr;
+                    r[c] += x * qr;
+                }
+            }
 #pragma unroll
             for (int c = 0; c < VW; ++c) {
-                const float x = V::get(s[i], c);
-                p[c] += x * kr;
-                r[c] += x * qr;
+                s_p[warp][col0 + c] = p[c];
+                s_r[warp][col0 + c] = r[c];
+            }
+            __syncthreads();  // partial sums of token j complete
+            if (tid < D) {
+                float P = 0.f, R = 0.f;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    P += s_p[w][tid];
+                    R += s_r[w][tid];
+                }
+                const float e = s_beta[jj] * (s_v[jj][tid] - P);
+                s_e[tid] = e;
+                if (is_new) {
+                    float kq = 0.f;
+#pragma unroll
+                    for (int w = 0; w < KQP; ++w) kq += s_kqp[jj][w];
+                    const int64_t tok = (n * nt.L + (j - nr)) * H + h;
+                    st(o + tok * D + tid, scale * (R + kq * e));
+                }
+            }
+            __syncthreads();  // e of token j complete; the partial sums were all read before it
+            float e[VW];
+#pragma unroll
+            for (int c = 0; c < VW; ++c) e[c] = s_e[col0 + c];
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const float kr = s_k[jj][row0 + i];
+#pragma unroll
+                for (int c = 0; c < VW; ++c) V::add(s[i], c, kr * e[c]);
+            }
+            if (j == last_commit) {  // the committed state: accepted drafts and the committed new tokens
+#pragma unroll
+                for (int i = 0; i < RPW; ++i) __stcs(reinterpret_cast<VT *>(Sh + (row0 + i) * D + col0), s[i]);
             }
         }
-#pragma unroll
-        for (int c = 0; c < VW; ++c) {
-            s_p[warp][col0 + c] = p[c];
-            s_r[warp][col0 + c] = r[c];
-        }
-        __syncthreads();
-        if (tid < D) {
-            float P = 0.f, R = 0.f;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                P += s_p[w][tid];
-                R += s_r[w][tid];
-            }
-            const float e = s_beta * (s_v[tid] - P);
-            s_e[tid] = e;
-            if (is_new) st(o + tok * D + tid, scale * (R + s_kq * e));
-        }
-        __syncthreads();
-        float e[VW];
-#pragma unroll
-        for (int c = 0; c < VW; ++c) e[c] = s_e[col0 + c];
-#pragma unroll
-        for (int i = 0; i < RPW; ++i) {
-            const float kr = s_k[row0 + i];
-#pragma unroll
-            for (int c = 0; c < VW; ++c) V::add(s[i], c, kr * e[c]);
-        }
-        if (j == last_commit) {  // the committed state: accepted drafts and the committed new tokens
-#pragma unroll
-            for (int i = 0; i < RPW; ++i) __stcs(reinterpret_cast<VT *>(Sh + (row0 + i) * D + col0), s[i]);
-        }
-        // the shared inputs of token j are overwritten only after every thread has used them
-        __syncthreads();
+        __syncthreads();  // the group's staged inputs and e are read before the next group overwrites them
     }
 }
 
