@@ -445,6 +445,52 @@ def test_recurrent_replay_equals_single_steps():
             assert rel_err(o_r[n, :, h].float().cpu().numpy(), o_steps) <= 1e-2
 
 
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "f32")])
+def test_recurrent_replay_long_windows_many_states(D, dtype):
+    """Windows of up to 19 tokens (several staging groups of 8) over more (sequence, head) states than
+    the device keeps resident, so that each CTA runs several states back to back."""
+    N, H, Rw, M = 48, 16, 10, 9
+    d, cached, new = _replay_inputs(D, dtype, N, H, Rw, M, seed=16)
+    g = torch.Generator().manual_seed(17)
+    nr = torch.randint(0, Rw + 1, (N,), generator=g, dtype=torch.int32)
+    nc = torch.randint(0, M + 1, (N,), generator=g, dtype=torch.int32)
+    nr[0], nc[0], nr[1], nc[1] = Rw, M, 0, 0  # the longest window; nothing committed
+    st = d["state"].clone().cuda()
+    o = kda.recurrent_replay(tuple(x.cuda() for x in cached), nr.cuda(), tuple(x.cuda() for x in new), nc.cuda(),
+                             d["dt_bias"].cuda(), d["A_log"].cuda(), st)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    tol = TOL_F32 if dtype == "f32" else TOL_BF16
+    out, o = st.cpu(), o.float().cpu()
+    for n in range(N):
+        for h in range(H):
+            o_ref, S_ref = _replay_oracle(d, cached, new, int(nr[n]), int(nc[n]), n, h)
+            assert rel_err(o[n, :, h].numpy(), o_ref) <= tol, (n, h)
+            assert rel_err(out[n, h].numpy(), S_ref) <= tol, (n, h)
+
+
+def test_recurrent_replay_bad_sequence_leaves_the_others_intact():
+    """A sequence with an out-of-range count is skipped with KDA_ERR_BAD_TOKEN_COUNT; the states
+    around it in the same launch are still computed."""
+    D, N, H, Rw, M = 128, 40, 8, 3, 4
+    d, cached, new = _replay_inputs(D, "bf16", N, H, Rw, M, seed=18)
+    nr = torch.full((N,), 2, dtype=torch.int32)
+    nc = torch.ones((N,), dtype=torch.int32)
+    nr[17] = Rw + 1
+    st = d["state"].clone().cuda()
+    o = kda.recurrent_replay(tuple(x.cuda() for x in cached), nr.cuda(), tuple(x.cuda() for x in new), nc.cuda(),
+                             d["dt_bias"].cuda(), d["A_log"].cuda(), st)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 11
+    out, o = st.cpu(), o.float().cpu()
+    assert torch.equal(out[17], d["state"][17])
+    for n in (0, 16, 18, 39):
+        for h in range(H):
+            o_ref, S_ref = _replay_oracle(d, cached, new, int(nr[n]), int(nc[n]), n, h)
+            assert rel_err(o[n, :, h].numpy(), o_ref) <= TOL_BF16, (n, h)
+            assert rel_err(out[n, h].numpy(), S_ref) <= TOL_BF16, (n, h)
+
+
 def test_recurrent_replay_nothing_committed_and_bad_counts():
     D, N, H = 64, 2, 2
     d, cached, new = _replay_inputs(D, "f32", N, H, 2, 2, seed=15)
