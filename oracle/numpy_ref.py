@@ -6,6 +6,8 @@ passage of the Kimi K3 technical report (section 2.1.1 unless stated):
 
 * ``gate``        -- Eq. 5, with the per-head bias b of Eq. 2 inside the
                      logit: g = g_min * Sigmoid(exp(A_h) * (z + b)).
+* ``gate_softplus`` -- the unbounded gate of the earlier Kimi Linear design that
+                     section 2.1.1 contrasts Eq. 5 with: g = -exp(A_h) * Softplus(z + b).
 * ``recurrence``  -- Eq. 1 token by token, decay before the delta update,
                      output read from the updated state.
 * ``chunked``     -- Eq. 3 and Eq. 4: chunkwise parallel form with the UT
@@ -41,6 +43,19 @@ def gate(z, b, A_log, g_min=-5.0):
     x = np.exp(np.asarray(A_log, dtype=np.float64)) * (z + np.asarray(b, dtype=np.float64))
     with np.errstate(over="ignore"):  # exp(-x) = inf for x << 0 gives g = -0, the exact limit
         return g_min / (1.0 + np.exp(-x))
+
+
+def gate_softplus(z, b, A_log):
+    """The gate Eq. 5 replaces (section 2.1.1: the earlier design's log-decay is unbounded below):
+    g = -exp(A_log) * Softplus(z + b), Softplus(x) = ln(1 + e^x), so g lies in (-inf, 0).  The bias
+    sits inside, as in the reading of Eq. 5.  Softplus is evaluated as max(x, 0) + ln(1 + e^{-|x|}),
+    which equals ln(1 + e^x) and overflows for no x.
+
+    z: [..., d_k]; b broadcastable to z; A_log broadcastable to z[..., :1].  Returns fp64 g.
+    """
+    x = np.asarray(z, dtype=np.float64) + np.asarray(b, dtype=np.float64)
+    sp = np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+    return -np.exp(np.asarray(A_log, dtype=np.float64)) * sp
 
 
 def recurrence(q, k, v, g, beta, S0=None, scale=1.0):
@@ -127,8 +142,9 @@ def segment_maps(k, g, beta, v):
 
 
 def forward(q, k, v, z, beta, dt_bias, A_log, cu_seqlens, S0=None, g_min=-5.0, scale=1.0,
-            heads=None):
-    """Packed multi-sequence, multi-head oracle (small cases).
+            heads=None, gate_kind="lower_bound"):
+    """Packed multi-sequence, multi-head oracle (small cases).  gate_kind "lower_bound" is Eq. 5
+    (``gate``), "softplus" the unbounded gate (``gate_softplus``, g_min unused).
 
     q, k, z [T, H, d_k]; v [T, H, d_v]; beta [T, H]; dt_bias [H, d_k];
     A_log [H]; cu_seqlens [N + 1]; S0 [N, H, d_k, d_v] or None.
@@ -146,8 +162,9 @@ def forward(q, k, v, z, beta, dt_bias, A_log, cu_seqlens, S0=None, g_min=-5.0, s
     for n in range(N):
         a, b = cu[n], cu[n + 1]
         for h in hs:
-            g = gate(np.asarray(z, np.float64)[a:b, h], np.asarray(dt_bias, np.float64)[h],
-                     float(np.asarray(A_log, np.float64)[h]), g_min)
+            zh, bh, ah = np.asarray(z, np.float64)[a:b, h], np.asarray(dt_bias, np.float64)[h], \
+                float(np.asarray(A_log, np.float64)[h])
+            g = gate_softplus(zh, bh, ah) if gate_kind == "softplus" else gate(zh, bh, ah, g_min)
             s0 = None if S0 is None else np.asarray(S0, np.float64)[n, h]
             o[a:b, h], ST[n, h] = recurrence(q[a:b, h], np.asarray(k, np.float64)[a:b, h],
                                              np.asarray(v, np.float64)[a:b, h], g,

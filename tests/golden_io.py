@@ -9,12 +9,12 @@ _SYMS = {"ln3": math.log(3.0), "ln2": math.log(2.0)}
 
 
 def num(tok: str) -> float:
-    """Parses '3/4', '-31/20', 'ln3/2', 'ln3-1', '-ln3' into a float."""
+    """Parses '3/4', '-31/20', 'ln3/2', 'ln3-1', '-ln3', 'ln3-2*ln2' into a float."""
     t = tok.strip()
-    for name, val in _SYMS.items():
-        if name in t:
-            expr = t.replace(name, repr(val))
-            return float(eval(expr, {"__builtins__": {}}))  # fixture-only arithmetic
+    if any(name in t for name in _SYMS):
+        for name, val in _SYMS.items():
+            t = t.replace(name, repr(val))
+        return float(eval(t, {"__builtins__": {}}))  # fixture-only arithmetic
     return float(Fraction(t))
 
 

@@ -50,6 +50,63 @@ def test_gate_bounds_symmetry_monotone():
     assert R.gate(np.array([800.0]), 0, 0, G_MIN)[0] == G_MIN
 
 
+# ----------------------------------------------------------------------------- unbounded softplus gate
+
+def test_gate_softplus_golden():
+    rows = read_table("gate_softplus.txt")
+    assert len(rows) == 8
+    for z, b, a, g_exp in rows:
+        g = float(R.gate_softplus(np.array([z]), np.array([b]), a)[0])
+        assert g == pytest.approx(g_exp, rel=1e-14, abs=1e-300)
+
+
+def test_gate_softplus_identities_and_unbounded():
+    rng = np.random.default_rng(3)
+    x = rng.normal(0, 4, size=4096)
+    for a in (-0.5, 0.0, 0.8):
+        g, gm = R.gate_softplus(x, 0.0, a), R.gate_softplus(-x, 0.0, a)
+        # Softplus(x) - Softplus(-x) = x  =>  g(x) - g(-x) = -e^A x
+        np.testing.assert_allclose(g - gm, -math.exp(a) * x, rtol=0, atol=1e-12)
+        assert np.all(g < 0)
+        assert np.all(np.diff(R.gate_softplus(np.sort(x), 0.3, a)) <= 0)  # decreasing in z
+    # unbounded below: 0 <= Softplus(x) - x = ln(1 + e^-x) <= e^-x, so g ~ -e^A x and no g_min holds
+    for xv in (10.0, 100.0, 1e4):
+        g = float(R.gate_softplus(np.array([xv]), 0.0, 0.0)[0])
+        assert 0.0 <= -g - xv <= math.exp(-xv) * (1 + 1e-12)
+    assert float(R.gate_softplus(np.array([1e4]), 0.0, 0.0)[0]) < 1000 * G_MIN
+
+
+_SP_MUTANTS = {
+    "sign_flipped": lambda z, b, a: np.exp(a) * np.logaddexp(0.0, z + b),
+    "scale_inside": lambda z, b, a: -np.logaddexp(0.0, np.exp(a) * (z + b)),
+    "bias_outside": lambda z, b, a: -np.exp(a) * (np.logaddexp(0.0, z) + b),
+    "log_without_one": lambda z, b, a: -np.exp(a) * (z + b),
+    "exp_not_softplus": lambda z, b, a: -np.exp(a) * np.exp(z + b),
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(_SP_MUTANTS))
+def test_gate_softplus_fixture_catches_planted_mistakes(mutant):
+    f = _SP_MUTANTS[mutant]
+    failures = sum(not np.isclose(f(z, b, a), g, rtol=1e-12, atol=1e-300)
+                   for z, b, a, g in read_table("gate_softplus.txt"))
+    assert failures >= 1, "a planted mistake passed every softplus-gate fixture"
+
+
+def test_recurrence_total_forgetting():
+    """A log-decay far below any bound (alpha = e^g underflows to 0, as the unbounded gate allows)
+    erases the state: S_t = beta_t k_t v_t^T and o_t = beta_t (k_t . q_t) v_t, with no inf or NaN."""
+    rng = np.random.default_rng(21)
+    T, dk, dv = 5, 4, 3
+    q, k, v = rng.normal(size=(T, dk)), rng.normal(size=(T, dk)), rng.normal(size=(T, dv))
+    beta = rng.uniform(0.2, 0.9, size=T)
+    g = np.full((T, dk), -2000.0)
+    o, S = R.recurrence(q, k, v, g, beta, S0=rng.normal(size=(dk, dv)))
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
+    np.testing.assert_allclose(S, beta[-1] * np.outer(k[-1], v[-1]), rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(o, (beta * np.einsum("tc,tc->t", k, q))[:, None] * v, rtol=1e-13, atol=1e-13)
+
+
 def test_gate_bound_on_workload_distribution():
     """Every gate value of the bf16 workloads' distribution obeys alpha > e^-5 (Eq. 5)."""
     import torch
