@@ -48,7 +48,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
 
-#define KDA_ABI_VERSION 2
+#define KDA_ABI_VERSION 3
 
 typedef enum {
     KDA_OK = 0,
@@ -67,9 +67,20 @@ typedef enum {
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
 
+/* Gate of the log-decay g (section 2.1.1).  Every entry point that takes z takes a gate_kind.
+ *   KDA_GATE_LOWER_BOUND (0): Eq. 5, g = g_min * Sigmoid(exp(A_log[h]) * (z + b[h])) in (g_min, 0).
+ *     The bound keeps every in-chunk decay factor inside bf16 range, which is what lets the
+ *     bf16 d = 128 prefill run as dense tensor-core products.
+ *   KDA_GATE_SOFTPLUS (1): the unbounded gate of the earlier design that Eq. 5 replaces,
+ *     g = -exp(A_log[h]) * Softplus(z + b[h]) in (-inf, 0); g_min is ignored.  The prefill then
+ *     runs on the fp32 CUDA-core path, which forms each in-chunk decay as exp(G_r - G_i) <= 1
+ *     from the cumulative log-decays (never as a product of Gamma and 1 / Gamma), so no value
+ *     of the gate overflows; a decay that underflows erases the state, as it should. */
+typedef enum { KDA_GATE_LOWER_BOUND = 0, KDA_GATE_SOFTPLUS = 1 } kda_gate_kind_t;
+
 /* ------------------------------------------------------------------ kda_gate
  * Eq. 5 (section 2.1.1): per-channel log-decay g = g_min * Sigmoid(exp(A_log[h]) * (z + b[h]))
- * for every token, optionally followed by the chunk-local cumulative sum of
+ * (or the softplus gate, see kda_gate_kind_t) for every token, optionally followed by the chunk-local cumulative sum of
  * Eq. 3 in log space, G_r = sum_{i <= r} g_i, restarting at every chunk start
  * (chunks of `chunk_size` tokens aligned to each sequence's first token).
  */
@@ -82,10 +93,12 @@ typedef struct {
     const void *z;             /* [T, H, dk] decay logit without bias */
     const float *dt_bias;      /* [H, dk] per-head bias b, or NULL for zero */
     const float *A_log;        /* [H] per-head log-scale A, or NULL for zero */
-    float g_min;               /* lower bound of the log-decay, < 0 (the report uses -5) */
+    float g_min;               /* lower bound of the log-decay, < 0 (the report uses -5); unused by
+                                  KDA_GATE_SOFTPLUS */
     int32_t chunk_size;        /* 0: write g; > 0: write the chunk-local cumulative sum */
     const int32_t *cu_seqlens; /* [N + 1] sequence starts, or NULL for N equal lengths T / N */
     float *out;                /* [T, H, dk] fp32 output */
+    int32_t gate_kind;         /* kda_gate_kind_t (0: Eq. 5) */
 } kda_gate_args;
 
 kda_status_t kda_gate(const kda_gate_args *args, struct CUstream_st *stream);
@@ -113,7 +126,7 @@ typedef struct {
     const void *beta;              /* [T, H] write strength in (0, 1), used as given */
     const float *dt_bias;          /* [H, dk] or NULL (zero) */
     const float *A_log;            /* [H] or NULL (zero) */
-    float g_min;                   /* < 0; the report uses -5 */
+    float g_min;                   /* < 0; the report uses -5 (unused by KDA_GATE_SOFTPLUS) */
     float scale;                   /* output scale; Eq. 1 has none (pass 1) */
     const int32_t *cu_seqlens;     /* [N + 1] device, or NULL for N sequences of T / N tokens */
     const int32_t *cu_seqlens_host;/* optional HOST copy of cu_seqlens (enables long-sequence
@@ -128,6 +141,7 @@ typedef struct {
     const void *out_gate;          /* [T, H, dv], dtype of o, 16-byte aligned, or NULL (no epilogue) */
     const float *out_norm_weight;  /* [H, dv] RMSNorm weight, 16-byte aligned, or NULL (ones) */
     float out_norm_eps;            /* RMSNorm epsilon, > 0 when out_gate is set */
+    int32_t gate_kind;             /* kda_gate_kind_t (0: Eq. 5; KDA_GATE_SOFTPLUS runs the fp32 path) */
 } kda_chunk_args;
 
 /* Bytes of device scratch kda_chunk_fwd needs for these sizes (0 on invalid sizes).
@@ -136,6 +150,11 @@ typedef struct {
 size_t kda_chunk_fwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
                                     kda_dtype_t dtype, int32_t chunk_size,
                                     const int32_t *cu_seqlens_host);
+/* The same for a given gate kind (kda_chunk_fwd_workspace_size is gate_kind 0; the softplus gate
+ * takes the fp32 path, whose records are larger for bf16 d = 128). */
+size_t kda_chunk_fwd_workspace_size_gate(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
+                                         kda_dtype_t dtype, int32_t chunk_size,
+                                         const int32_t *cu_seqlens_host, int32_t gate_kind);
 
 /* workspace: device memory of at least kda_chunk_fwd_workspace_size() bytes,
  * 256-byte aligned, owned by the caller; its contents need no initialisation
@@ -181,6 +200,7 @@ typedef struct {
     const int32_t *state_indices;  /* [N] slot of each sequence, or NULL (slot n) */
     int64_t num_slots;             /* 0 = N */
     void *o;                       /* [N, M, H, dv] outputs of the new tokens */
+    int32_t gate_kind;             /* kda_gate_kind_t (0: Eq. 5) */
 } kda_replay_args;
 
 kda_status_t kda_recurrent_replay(const kda_replay_args *args, struct CUstream_st *stream);
@@ -251,6 +271,7 @@ typedef struct {
     const int32_t *state_indices;  /* [N] state slot of each sequence, or NULL (slot = n) */
     int64_t num_slots;             /* slots in `state` (0 means N) */
     void *o;                       /* [N, H, dv] */
+    int32_t gate_kind;             /* kda_gate_kind_t (0: Eq. 5) */
 } kda_step_args;
 
 kda_status_t kda_recurrent_step(const kda_step_args *args, struct CUstream_st *stream);

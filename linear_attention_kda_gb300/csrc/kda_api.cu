@@ -15,6 +15,11 @@ namespace {
 constexpr int kMaxDevices = 64;
 int *g_err_ptr[kMaxDevices];  // device address of g_kda_device_error, per device
 
+// gate_kind is a kda_gate_kind_t; g_min matters (finite, < 0) for the bounded gate only
+bool gate_ok(int32_t kind, float g_min) {
+    if (kind == KDA_GATE_SOFTPLUS) return true;
+    return kind == KDA_GATE_LOWER_BOUND && g_min < 0.f && isfinite(g_min);
+}
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 bool aligned_to(const void *p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
@@ -79,7 +84,7 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
     if (!a) return 0;
     kda_chunk_plan p;
     if (!kda_make_chunk_plan(a->T, a->N > 0 ? a->N : 1, a->H > 0 ? a->H : 1, a->dk, a->dv, a->dtype, 64, &p,
-                             a->cu_seqlens_host))
+                             a->cu_seqlens_host, a->gate_kind))
         return 0;
     // either one fused launch (intra-chunk transform and output pass together) or the chunk plan,
     // then intra-chunk transform, [segment summaries, fold,] output pass
@@ -91,7 +96,7 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
 kda_status_t kda_chunk_fwd_schedule(const kda_chunk_args *a, int64_t *out) {
     if (!a || !out || a->T < 0 || a->N < 1 || a->H < 1) return KDA_ERR_INVALID_ARG;
     kda_chunk_plan p;
-    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p, a->cu_seqlens_host))
+    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p, a->cu_seqlens_host, a->gate_kind))
         return KDA_ERR_INVALID_ARG;
     out[0] = p.fused;
     out[1] = p.fused ? p.kpre : 0;
@@ -141,7 +146,7 @@ kda_status_t kda_gate(const kda_gate_args *a, struct CUstream_st *stream) {
     if (a->T < 0 || a->H < 1 || a->dk < 1 || a->chunk_size < 0 || a->chunk_size > 256)
         return KDA_ERR_INVALID_ARG;
     if (!dtype_ok(a->dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
-    if (!(a->g_min < 0.f) || !isfinite(a->g_min)) return KDA_ERR_INVALID_ARG;
+    if (!gate_ok(a->gate_kind, a->g_min)) return KDA_ERR_INVALID_ARG;
     if (a->T == 0) return KDA_OK;
     if (!a->z || !a->out) return KDA_ERR_INVALID_ARG;
     if (a->chunk_size > 0) {
@@ -163,7 +168,7 @@ static kda_status_t validate_chunk(const kda_chunk_args *a) {
     if (!dtype_ok(a->dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
     if (a->dk != a->dv || (a->dk != 64 && a->dk != 128)) return KDA_ERR_UNSUPPORTED_SHAPE;
     if (a->chunk_size != 0 && a->chunk_size != 64) return KDA_ERR_UNSUPPORTED_SHAPE;
-    if (!(a->g_min < 0.f) || !isfinite(a->g_min) || !isfinite(a->scale)) return KDA_ERR_INVALID_ARG;
+    if (!gate_ok(a->gate_kind, a->g_min) || !isfinite(a->scale)) return KDA_ERR_INVALID_ARG;
     if (!a->cu_seqlens && a->T % a->N != 0) return KDA_ERR_INVALID_ARG;
     if (a->T > INT32_MAX) return KDA_ERR_UNSUPPORTED_SHAPE;
     if (a->T > 0) {
@@ -193,16 +198,23 @@ static kda_status_t validate_chunk(const kda_chunk_args *a) {
     return KDA_OK;
 }
 
-size_t kda_chunk_fwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
-                                    kda_dtype_t dtype, int32_t chunk_size,
-                                    const int32_t *cu_seqlens_host) {
-    (void)cu_seqlens_host;
+size_t kda_chunk_fwd_workspace_size_gate(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
+                                         kda_dtype_t dtype, int32_t chunk_size,
+                                         const int32_t *cu_seqlens_host, int32_t gate_kind) {
     if (T < 0 || N < 1 || H < 1 || !dtype_ok(dtype)) return 0;
     if (dk != dv || (dk != 64 && dk != 128)) return 0;
     if (chunk_size != 0 && chunk_size != 64) return 0;
+    if (gate_kind != KDA_GATE_LOWER_BOUND && gate_kind != KDA_GATE_SOFTPLUS) return 0;
     kda_chunk_plan p;
-    if (!kda_make_chunk_plan(T, N, H, dk, dv, dtype, 64, &p, cu_seqlens_host)) return 0;
+    if (!kda_make_chunk_plan(T, N, H, dk, dv, dtype, 64, &p, cu_seqlens_host, gate_kind)) return 0;
     return p.total_bytes;
+}
+
+size_t kda_chunk_fwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
+                                    kda_dtype_t dtype, int32_t chunk_size,
+                                    const int32_t *cu_seqlens_host) {
+    return kda_chunk_fwd_workspace_size_gate(T, N, H, dk, dv, dtype, chunk_size, cu_seqlens_host,
+                                             KDA_GATE_LOWER_BOUND);
 }
 
 kda_status_t kda_chunk_fwd(const kda_chunk_args *a, void *workspace, size_t workspace_bytes,
@@ -210,7 +222,7 @@ kda_status_t kda_chunk_fwd(const kda_chunk_args *a, void *workspace, size_t work
     kda_status_t st = validate_chunk(a);
     if (st != KDA_OK) return st;
     kda_chunk_plan p;
-    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p, a->cu_seqlens_host))
+    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p, a->cu_seqlens_host, a->gate_kind))
         return KDA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < p.total_bytes) return KDA_ERR_WORKSPACE;
     if (!aligned_to(workspace, 256)) return KDA_ERR_MISALIGNED;
@@ -248,7 +260,7 @@ kda_status_t kda_recurrent_step(const kda_step_args *a, struct CUstream_st *stre
     if (a->N < 0 || a->H < 1 || a->num_slots < 0) return KDA_ERR_INVALID_ARG;
     if (!dtype_ok(a->dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
     if (a->dk != a->dv || (a->dk != 64 && a->dk != 128)) return KDA_ERR_UNSUPPORTED_SHAPE;
-    if (!(a->g_min < 0.f) || !isfinite(a->g_min) || !isfinite(a->scale)) return KDA_ERR_INVALID_ARG;
+    if (!gate_ok(a->gate_kind, a->g_min) || !isfinite(a->scale)) return KDA_ERR_INVALID_ARG;
     if (a->N == 0) return KDA_OK;
     if (a->N * (int64_t)a->H > INT32_MAX) return KDA_ERR_UNSUPPORTED_SHAPE;
     if (!a->q || !a->k || !a->v || !a->z || !a->beta || !a->o || !a->state) return KDA_ERR_INVALID_ARG;
@@ -268,7 +280,7 @@ kda_status_t kda_recurrent_replay(const kda_replay_args *a, struct CUstream_st *
     if (a->N < 0 || a->H < 1 || a->num_slots < 0 || a->R < 0 || a->M < 1) return KDA_ERR_INVALID_ARG;
     if (!dtype_ok(a->dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
     if (a->dk != a->dv || (a->dk != 64 && a->dk != 128)) return KDA_ERR_UNSUPPORTED_SHAPE;
-    if (!(a->g_min < 0.f) || !isfinite(a->g_min) || !isfinite(a->scale)) return KDA_ERR_INVALID_ARG;
+    if (!gate_ok(a->gate_kind, a->g_min) || !isfinite(a->scale)) return KDA_ERR_INVALID_ARG;
     if (a->N == 0) return KDA_OK;
     if (a->N * (int64_t)a->H > INT32_MAX || a->N * (int64_t)(a->R > a->M ? a->R : a->M) * a->H > INT32_MAX)
         return KDA_ERR_UNSUPPORTED_SHAPE;

@@ -5,14 +5,16 @@
 // Two kernels, following Eq. 3 and Eq. 4 of the Kimi K3 report (section 2.1.1):
 //
 // 1. intra (one CTA per (chunk, head), all chunks in parallel):
-//    g from Eq. 5, G = in-chunk cumulative log-decay (Eq. 3 in log space),
+//    g from Eq. 5 (or the unbounded softplus gate: this path is the one that gate
+//    takes, see below), G = in-chunk cumulative log-decay (Eq. 3 in log space),
 //    L[r,i] = beta_r sum_c k_rc k_ic e^{G_rc - G_ic}  (i < r),
 //    A[r,i] =        sum_c q_rc k_ic e^{G_rc - G_ic}  (i <= r, diagonal kept),
 //    [W | U] = (I + L)^{-1} [diag(beta)(Gamma * K) | diag(beta) V]   (UT transform,
 //    by forward substitution, one column per thread),
 //    Q^ = Gamma * Q,  K~ = K * e^{G_last - G},  gamma^C = e^{G_last}.
 //    The relative decays are formed as e^{G_r - G_i} directly, never as a
-//    product of Gamma and 1/Gamma, so nothing overflows at any chunk length.
+//    product of Gamma and 1/Gamma, so nothing overflows at any chunk length or
+//    for any gate value: every factor is <= 1 and a deep decay underflows to 0.
 // 2. chain (one CTA per (sequence, head, 32 value columns), chunks in order):
 //    V~ = U - W S;  O = scale (Q^ S + A V~);  S <- Diag(gamma^C) S + K~^T V~.
 //    Columns of S evolve independently (Eq. 1 acts on S from the left), so the
@@ -66,7 +68,7 @@ __global__ void __launch_bounds__(SIMT_THREADS)
 chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, const Tio *__restrict__ v,
                         const Tio *__restrict__ z, const Tio *__restrict__ beta,
                         const float *__restrict__ bias, const float *__restrict__ A_log, float g_min,
-                        int64_t T, int N, const int32_t *__restrict__ cu,
+                        int kind, int64_t T, int N, const int32_t *__restrict__ cu,
                         const int32_t *__restrict__ chunk_start, int H, int dk, int dv, int C,
                         char *__restrict__ records, size_t rec_bytes) {
     extern __shared__ float sm[];
@@ -92,7 +94,7 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
         const int64_t idx = ((t0 + r) * H + h) * (int64_t)dk + c;
         Ks[r * PK + c] = ok ? ld(k + idx) : 0.f;
         Qs[r * PK + c] = ok ? ld(q + idx) : 0.f;
-        Gs[r * PK + c] = ok ? gate_logdecay(ld(z + idx), bias ? bias[h * dk + c] : 0.f, eA, g_min) : 0.f;
+        Gs[r * PK + c] = ok ? gate_log(kind, ld(z + idx), bias ? bias[h * dk + c] : 0.f, eA, g_min) : 0.f;
     }
     for (int e = tid; e < C * dv; e += SIMT_THREADS) {
         const int r = e / dv, c = e % dv;
@@ -266,13 +268,13 @@ kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan
             cudaFuncSetAttribute(chunk_intra_simt_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_intra);
             chunk_intra_simt_kernel<bf16><<<grid, SIMT_THREADS, smem_intra, stream>>>(
                 (const bf16 *)a->q, (const bf16 *)a->k, (const bf16 *)a->v, (const bf16 *)a->z,
-                (const bf16 *)a->beta, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
+                (const bf16 *)a->beta, a->dt_bias, a->A_log, a->g_min, a->gate_kind, a->T, (int)a->N, a->cu_seqlens,
                 chunk_start, H, dk, dv, C, records, p.record_bytes);
         } else {
             cudaFuncSetAttribute(chunk_intra_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_intra);
             chunk_intra_simt_kernel<float><<<grid, SIMT_THREADS, smem_intra, stream>>>(
                 (const float *)a->q, (const float *)a->k, (const float *)a->v, (const float *)a->z,
-                (const float *)a->beta, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
+                (const float *)a->beta, a->dt_bias, a->A_log, a->g_min, a->gate_kind, a->T, (int)a->N, a->cu_seqlens,
                 chunk_start, H, dk, dv, C, records, p.record_bytes);
         }
         {

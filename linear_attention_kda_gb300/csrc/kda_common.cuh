@@ -25,6 +25,17 @@ __device__ __forceinline__ float gate_logdecay(float z, float b, float expA, flo
     return g_min / (1.0f + expf(-x));
 }
 
+// The gate selected by kind (kda_gate_kind_t): Eq. 5 above, or the unbounded softplus gate of the
+// earlier design, g = -expA * Softplus(z + b) with Softplus(x) = max(x, 0) + ln(1 + e^{-|x|})
+// (= ln(1 + e^x), no overflow for any x).
+__device__ __forceinline__ float gate_log(int kind, float z, float b, float expA, float g_min) {
+    if (kind == KDA_GATE_SOFTPLUS) {
+        const float x = z + b;
+        return -expA * (fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))));
+    }
+    return gate_logdecay(z, b, expA, g_min);
+}
+
 // First device-detected error wins; later ones are dropped.
 __device__ __forceinline__ void set_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);

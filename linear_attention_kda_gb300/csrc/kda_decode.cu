@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(2 * D)
 decode_step_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, const Tio *__restrict__ v,
                    const Tio *__restrict__ z, const Tio *__restrict__ beta,
                    const float *__restrict__ bias, const float *__restrict__ A_log, float g_min,
-                   float scale, float *__restrict__ state, const int32_t *__restrict__ state_idx,
+                   int kind, float scale, float *__restrict__ state, const int32_t *__restrict__ state_idx,
                    int64_t num_slots, int H, Tio *__restrict__ o, int *err) {
     constexpr int NT = 2 * D;
     constexpr int NW = NT / 32;   // warps
@@ -82,7 +82,7 @@ decode_step_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, const T
     if (tid < D) {
         const float eA = A_log ? expf(A_log[h]) : 1.f;
         const float b = bias ? bias[h * D + tid] : 0.f;
-        const float g = gate_logdecay(ld(z + tok * D + tid), b, eA, g_min);
+        const float g = gate_log(kind, ld(z + tok * D + tid), b, eA, g_min);
         s_alpha[tid] = expf(g);
         s_k[tid] = ld(k + tok * D + tid);
         s_q[tid] = ld(q + tok * D + tid);
@@ -149,7 +149,7 @@ static void launch(const kda_step_args *a, cudaStream_t stream, int *err) {
     const int64_t slots = a->num_slots > 0 ? a->num_slots : a->N;
     decode_step_kernel<D, Tio><<<(unsigned)(a->N * a->H), 2 * D, 0, stream>>>(
         (const Tio *)a->q, (const Tio *)a->k, (const Tio *)a->v, (const Tio *)a->z,
-        (const Tio *)a->beta, a->dt_bias, a->A_log, a->g_min, a->scale, a->state,
+        (const Tio *)a->beta, a->dt_bias, a->A_log, a->g_min, a->gate_kind, a->scale, a->state,
         a->state_indices, slots, a->H, (Tio *)a->o, err);
 }
 

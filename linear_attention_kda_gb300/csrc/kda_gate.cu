@@ -15,7 +15,7 @@ namespace kda {
 
 template <typename T>
 __global__ void gate_elementwise_kernel(const T *__restrict__ z, const float *__restrict__ bias,
-                                        const float *__restrict__ A_log, float g_min, int64_t total,
+                                        const float *__restrict__ A_log, float g_min, int kind, int64_t total,
                                         int H, int dk, float *__restrict__ out) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -23,7 +23,7 @@ __global__ void gate_elementwise_kernel(const T *__restrict__ z, const float *__
         const int h = (int)((i / dk) % H);
         const float b = bias ? bias[h * dk + c] : 0.f;
         const float eA = A_log ? expf(A_log[h]) : 1.f;
-        out[i] = gate_logdecay(ld(z + i), b, eA, g_min);
+        out[i] = gate_log(kind, ld(z + i), b, eA, g_min);
     }
 }
 
@@ -39,7 +39,7 @@ __device__ __forceinline__ int64_t chunk_start_of(const int32_t *cu, int N, int6
 
 template <typename T>
 __global__ void gate_cumsum_kernel(const T *__restrict__ z, const float *__restrict__ bias,
-                                   const float *__restrict__ A_log, float g_min, int64_t Ttot,
+                                   const float *__restrict__ A_log, float g_min, int kind, int64_t Ttot,
                                    int N, const int32_t *__restrict__ cu, int H, int dk, int C,
                                    float *__restrict__ out, int *err) {
     extern __shared__ unsigned char smem_raw[];
@@ -76,7 +76,7 @@ __global__ void gate_cumsum_kernel(const T *__restrict__ z, const float *__restr
         const int64_t t = s0 + i;
         if (is_start[i]) G = 0.f;
         const int64_t idx = (t * H + h) * (int64_t)dk + c;
-        G += gate_logdecay(ld(z + idx), b, eA, g_min);
+        G += gate_log(kind, ld(z + idx), b, eA, g_min);
         if (t >= w0) out[idx] = G;
     }
 }
@@ -96,10 +96,10 @@ kda_status_t kda_launch_gate(const kda_gate_args *a, cudaStream_t stream) {
         const int blocks = (int)(want < 152 * 32 ? want : 152 * 32);
         if (a->dtype == KDA_BF16)
             gate_elementwise_kernel<bf16><<<blocks, threads, 0, stream>>>(
-                (const bf16 *)a->z, a->dt_bias, a->A_log, a->g_min, total, a->H, a->dk, a->out);
+                (const bf16 *)a->z, a->dt_bias, a->A_log, a->g_min, a->gate_kind, total, a->H, a->dk, a->out);
         else
             gate_elementwise_kernel<float><<<blocks, threads, 0, stream>>>(
-                (const float *)a->z, a->dt_bias, a->A_log, a->g_min, total, a->H, a->dk, a->out);
+                (const float *)a->z, a->dt_bias, a->A_log, a->g_min, a->gate_kind, total, a->H, a->dk, a->out);
     } else {
         const int C = a->chunk_size;
         const int threads = a->dk < 128 ? ((a->dk + 31) / 32) * 32 : 128;
@@ -107,11 +107,11 @@ kda_status_t kda_launch_gate(const kda_gate_args *a, cudaStream_t stream) {
         const size_t smem = 2 * (size_t)C;
         if (a->dtype == KDA_BF16)
             gate_cumsum_kernel<bf16><<<grid, threads, smem, stream>>>(
-                (const bf16 *)a->z, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
+                (const bf16 *)a->z, a->dt_bias, a->A_log, a->g_min, a->gate_kind, a->T, (int)a->N, a->cu_seqlens,
                 a->H, a->dk, C, a->out, err);
         else
             gate_cumsum_kernel<float><<<grid, threads, smem, stream>>>(
-                (const float *)a->z, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
+                (const float *)a->z, a->dt_bias, a->A_log, a->g_min, a->gate_kind, a->T, (int)a->N, a->cu_seqlens,
                 a->H, a->dk, C, a->out, err);
     }
     return kda_cuda_status(cudaGetLastError());

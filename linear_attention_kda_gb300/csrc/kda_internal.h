@@ -45,8 +45,10 @@ struct kda_chunk_plan {
     size_t total_bytes;
 };
 
+// gate_kind KDA_GATE_SOFTPLUS always takes the fp32 CUDA-core path (its in-chunk decays are not
+// bounded, so the tensor-core operand images could overflow).
 bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_t dtype, int C,
-                         kda_chunk_plan *plan, const int32_t *cu_seqlens_host = nullptr);
+                         kda_chunk_plan *plan, const int32_t *cu_seqlens_host = nullptr, int gate_kind = 0);
 kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
                                    cudaStream_t stream);
 kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,

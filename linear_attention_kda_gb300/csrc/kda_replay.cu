@@ -72,7 +72,7 @@ template <int D, typename Tio>
 __global__ void __launch_bounds__(2 * D, 2)
 replay_kernel(Tokens<Tio> rt, const int32_t *__restrict__ n_replay, Tokens<Tio> nt,
               const int32_t *__restrict__ n_commit, const float *__restrict__ bias,
-              const float *__restrict__ A_log, float g_min, float scale, float *__restrict__ state,
+              const float *__restrict__ A_log, float g_min, int kind, float scale, float *__restrict__ state,
               const int32_t *__restrict__ state_idx, int64_t num_slots, int64_t n_items, int H,
               Tio *__restrict__ o, int *err) {
     using L = Smem<D, Tio>;
@@ -108,7 +108,7 @@ replay_kernel(Tokens<Tio> rt, const int32_t *__restrict__ n_replay, Tokens<Tio> 
     // one staged channel of token jj of the group: the decay alpha = exp(g) (Eq. 5), k, q, v, and the
     // warp's partial sum of k . q (a warp covers 32 channels of one token)
     auto convert = [&](int jj, float zv, float kv, float qv, float vv, float b, float eA) {
-        FA[0][jj][c_in] = expf(gate_logdecay(zv, b, eA, g_min));
+        FA[0][jj][c_in] = expf(gate_log(kind, zv, b, eA, g_min));
         FA[1][jj][c_in] = kv;
         FA[2][jj][c_in] = qv;
         FA[3][jj][c_in] = vv;
@@ -352,7 +352,7 @@ static kda_status_t launch(const kda_replay_args *a, cudaStream_t stream, int *e
     Tokens<Tio> nt{(const Tio *)a->q, (const Tio *)a->k, (const Tio *)a->z, (const Tio *)a->v,
                    (const Tio *)a->beta, a->M};
     kern<<<grid, 2 * D, L::BYTES, stream>>>(rt, a->R > 0 ? a->n_replay : nullptr, nt, a->n_commit, a->dt_bias,
-                                             a->A_log, a->g_min, a->scale, a->state, a->state_indices, slots,
+                                             a->A_log, a->g_min, a->gate_kind, a->scale, a->state, a->state_indices, slots,
                                              n_items, a->H, (Tio *)a->o, err);
     return kda_cuda_status(cudaGetLastError());
 }

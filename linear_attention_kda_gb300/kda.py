@@ -18,6 +18,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
 
 KDA_F32, KDA_BF16 = 0, 1
+# gate of the log-decay (kda_gate_kind_t): Eq. 5 bounded below by g_min, or the unbounded softplus gate
+GATE_KINDS = {"lower_bound": 0, "softplus": 1}
 _STATUS = {
     0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
     3: "KDA_ERR_UNSUPPORTED_DTYPE", 4: "KDA_ERR_MISALIGNED", 5: "KDA_ERR_WORKSPACE",
@@ -27,7 +29,8 @@ _STATUS = {
 EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step",
             "kda_status_string", "kda_get_device_error", "kda_abi_version",
             "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws",
-            "kda_last_cuda_error", "kda_chunk_fwd_schedule", "kda_output_gate", "kda_recurrent_replay"]
+            "kda_last_cuda_error", "kda_chunk_fwd_schedule", "kda_output_gate", "kda_recurrent_replay",
+            "kda_chunk_fwd_workspace_size_gate"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 _vp = ctypes.c_void_p
@@ -37,7 +40,7 @@ _i64, _i32, _f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
 class GateArgs(ctypes.Structure):
     _fields_ = [("T", _i64), ("N", _i64), ("H", _i32), ("dk", _i32), ("dtype", ctypes.c_int),
                 ("z", _vp), ("dt_bias", _vp), ("A_log", _vp), ("g_min", _f32),
-                ("chunk_size", _i32), ("cu_seqlens", _vp), ("out", _vp)]
+                ("chunk_size", _i32), ("cu_seqlens", _vp), ("out", _vp), ("gate_kind", _i32)]
 
 
 class ChunkArgs(ctypes.Structure):
@@ -46,7 +49,7 @@ class ChunkArgs(ctypes.Structure):
                 ("beta", _vp), ("dt_bias", _vp), ("A_log", _vp), ("g_min", _f32), ("scale", _f32),
                 ("cu_seqlens", _vp), ("cu_seqlens_host", _vp), ("initial_state", _vp),
                 ("final_state", _vp), ("o", _vp), ("chunk_size", _i32),
-                ("out_gate", _vp), ("out_norm_weight", _vp), ("out_norm_eps", _f32)]
+                ("out_gate", _vp), ("out_norm_weight", _vp), ("out_norm_eps", _f32), ("gate_kind", _i32)]
 
 
 class ReplayArgs(ctypes.Structure):
@@ -54,7 +57,7 @@ class ReplayArgs(ctypes.Structure):
                 ("rq", _vp), ("rk", _vp), ("rz", _vp), ("rv", _vp), ("rbeta", _vp), ("n_replay", _vp),
                 ("M", _i32), ("q", _vp), ("k", _vp), ("z", _vp), ("v", _vp), ("beta", _vp), ("n_commit", _vp),
                 ("dt_bias", _vp), ("A_log", _vp), ("g_min", _f32), ("scale", _f32), ("state", _vp),
-                ("state_indices", _vp), ("num_slots", _i64), ("o", _vp)]
+                ("state_indices", _vp), ("num_slots", _i64), ("o", _vp), ("gate_kind", _i32)]
 
 
 class OutputGateArgs(ctypes.Structure):
@@ -66,7 +69,7 @@ class StepArgs(ctypes.Structure):
     _fields_ = [("N", _i64), ("H", _i32), ("dk", _i32), ("dv", _i32), ("dtype", ctypes.c_int),
                 ("q", _vp), ("k", _vp), ("z", _vp), ("v", _vp), ("beta", _vp),
                 ("dt_bias", _vp), ("A_log", _vp), ("g_min", _f32), ("scale", _f32),
-                ("state", _vp), ("state_indices", _vp), ("num_slots", _i64), ("o", _vp)]
+                ("state", _vp), ("state_indices", _vp), ("num_slots", _i64), ("o", _vp), ("gate_kind", _i32)]
 
 
 class KDAError(RuntimeError):
@@ -96,6 +99,8 @@ def load_library(path: Optional[str] = None):
         L.kda_chunk_fwd.restype = ctypes.c_int
         L.kda_chunk_fwd_workspace_size.argtypes = [_i64, _i64, _i32, _i32, _i32, ctypes.c_int, _i32, _vp]
         L.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
+        L.kda_chunk_fwd_workspace_size_gate.argtypes = [_i64, _i64, _i32, _i32, _i32, ctypes.c_int, _i32, _vp, _i32]
+        L.kda_chunk_fwd_workspace_size_gate.restype = ctypes.c_size_t
         L.kda_recurrent_step.argtypes = [ctypes.POINTER(StepArgs), _vp]
         L.kda_recurrent_step.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -133,6 +138,12 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
+def _gate_kind(gate: str) -> int:
+    if gate not in GATE_KINDS:
+        raise ValueError(f"gate must be one of {sorted(GATE_KINDS)}")
+    return GATE_KINDS[gate]
+
+
 def _stream(t: torch.Tensor):
     return torch.cuda.current_stream(t.device).cuda_stream
 
@@ -151,8 +162,10 @@ def _contig(*ts):
 
 
 def gate(z: torch.Tensor, dt_bias=None, A_log=None, g_min: float = -5.0, chunk_size: int = 0,
-         cu_seqlens: Optional[torch.Tensor] = None, n_seq: int = 1, out=None) -> torch.Tensor:
-    """kda_gate: g = g_min * sigmoid(exp(A_log) (z + dt_bias)) (Eq. 5), or its chunk-local cumsum."""
+         cu_seqlens: Optional[torch.Tensor] = None, n_seq: int = 1, out=None,
+         gate: str = "lower_bound") -> torch.Tensor:
+    """kda_gate: g = g_min * sigmoid(exp(A_log) (z + dt_bias)) (Eq. 5), or with gate="softplus"
+    g = -exp(A_log) * softplus(z + dt_bias); or its chunk-local cumsum."""
     L = load_library()
     T, H, dk = z.shape
     _contig(z, dt_bias, A_log, cu_seqlens)
@@ -160,18 +173,20 @@ def gate(z: torch.Tensor, dt_bias=None, A_log=None, g_min: float = -5.0, chunk_s
         out = torch.empty((T, H, dk), dtype=torch.float32, device=z.device)
     a = GateArgs(T=T, N=(cu_seqlens.numel() - 1) if cu_seqlens is not None else n_seq, H=H, dk=dk,
                  dtype=_dtype_code(z), z=_ptr(z), dt_bias=_ptr(dt_bias), A_log=_ptr(A_log),
-                 g_min=g_min, chunk_size=chunk_size, cu_seqlens=_ptr(cu_seqlens), out=_ptr(out))
+                 g_min=g_min, chunk_size=chunk_size, cu_seqlens=_ptr(cu_seqlens), out=_ptr(out),
+                 gate_kind=_gate_kind(gate))
     _check(L.kda_gate(ctypes.byref(a), _stream(z)), "kda_gate")
     return out
 
 
-def chunk_fwd_workspace_size(T, N, H, dk, dv, dtype: torch.dtype, chunk_size=64, cu_seqlens_host=None):
+def chunk_fwd_workspace_size(T, N, H, dk, dv, dtype: torch.dtype, chunk_size=64, cu_seqlens_host=None,
+                             gate: str = "lower_bound"):
     L = load_library()
     code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
     hp = None
     if cu_seqlens_host is not None:
         hp = cu_seqlens_host.data_ptr()
-    return int(L.kda_chunk_fwd_workspace_size(T, N, H, dk, dv, code, chunk_size, hp))
+    return int(L.kda_chunk_fwd_workspace_size_gate(T, N, H, dk, dv, code, chunk_size, hp, _gate_kind(gate)))
 
 
 def chunk_fwd(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0, scale: float = 1.0,
@@ -180,8 +195,10 @@ def chunk_fwd(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0
               output_final_state: bool = False, final_state: Optional[torch.Tensor] = None,
               chunk_size: int = 64, workspace: Optional[torch.Tensor] = None,
               out: Optional[torch.Tensor] = None, out_gate: Optional[torch.Tensor] = None,
-              out_norm_weight: Optional[torch.Tensor] = None, out_norm_eps: float = 1e-6):
+              out_norm_weight: Optional[torch.Tensor] = None, out_norm_eps: float = 1e-6,
+              gate: str = "lower_bound"):
     """kda_chunk_fwd: chunkwise KDA prefill (Eq. 1 evaluated as Eq. 3-4).  Returns (o, final_state).
+    gate="softplus" selects the unbounded gate (run on the fp32 CUDA-core path).
 
     With out_gate ([T, H, dv], the gate pre-activation W_g x), o holds the output epilogue of Eq. 6,
     Sigmoid(out_gate) * RMSNorm(o~) (per-head RMSNorm with weight out_norm_weight [H, dv], eps)."""
@@ -196,7 +213,7 @@ def chunk_fwd(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0
     fs = final_state
     if fs is None and output_final_state:
         fs = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
-    need = chunk_fwd_workspace_size(T, N, H, dk, dv, q.dtype, chunk_size, cu_seqlens_host)
+    need = chunk_fwd_workspace_size(T, N, H, dk, dv, q.dtype, chunk_size, cu_seqlens_host, gate)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
     a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=_dtype_code(q), q=_ptr(q), k=_ptr(k), z=_ptr(z),
@@ -205,7 +222,7 @@ def chunk_fwd(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0
                   cu_seqlens_host=None if cu_seqlens_host is None else cu_seqlens_host.data_ptr(),
                   initial_state=_ptr(initial_state), final_state=_ptr(fs), o=_ptr(o),
                   chunk_size=chunk_size, out_gate=_ptr(out_gate), out_norm_weight=_ptr(out_norm_weight),
-                  out_norm_eps=out_norm_eps)
+                  out_norm_eps=out_norm_eps, gate_kind=_gate_kind(gate))
     _check(L.kda_chunk_fwd(ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(q)),
            "kda_chunk_fwd")
     return o, fs
@@ -225,7 +242,8 @@ def output_gate(o, g, norm_weight=None, eps: float = 1e-6, *, out: Optional[torc
 
 
 def recurrent_step(q, k, v, z, beta, dt_bias, A_log, state, *, g_min: float = -5.0, scale: float = 1.0,
-                   state_indices: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None):
+                   state_indices: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                   gate: str = "lower_bound"):
     """kda_recurrent_step: one decode token per sequence; `state` is updated in place.  Returns o."""
     L = load_library()
     N, H, dk = q.shape
@@ -235,14 +253,14 @@ def recurrent_step(q, k, v, z, beta, dt_bias, A_log, state, *, g_min: float = -5
     a = StepArgs(N=N, H=H, dk=dk, dv=dv, dtype=_dtype_code(q), q=_ptr(q), k=_ptr(k), z=_ptr(z),
                  v=_ptr(v), beta=_ptr(beta), dt_bias=_ptr(dt_bias), A_log=_ptr(A_log), g_min=g_min,
                  scale=scale, state=_ptr(state), state_indices=_ptr(state_indices),
-                 num_slots=state.shape[0], o=_ptr(o))
+                 num_slots=state.shape[0], o=_ptr(o), gate_kind=_gate_kind(gate))
     _check(L.kda_recurrent_step(ctypes.byref(a), _stream(q)), "kda_recurrent_step")
     return o
 
 
 def recurrent_replay(cached, n_replay, new, n_commit, dt_bias, A_log, state, *, g_min: float = -5.0,
                      scale: float = 1.0, state_indices: Optional[torch.Tensor] = None,
-                     out: Optional[torch.Tensor] = None):
+                     out: Optional[torch.Tensor] = None, gate: str = "lower_bound"):
     """kda_recurrent_replay: speculative decoding with replay (section 5.4).
 
     cached: (q, k, z, v, beta) of the cached draft window, [N, R, H, d] / [N, R, H] (or None: R = 0);
@@ -265,7 +283,8 @@ def recurrent_replay(cached, n_replay, new, n_commit, dt_bias, A_log, state, *, 
                    rv=_ptr(rv), rbeta=_ptr(rb), n_replay=_ptr(n_replay), M=M, q=_ptr(q), k=_ptr(k), z=_ptr(z),
                    v=_ptr(v), beta=_ptr(beta), n_commit=_ptr(n_commit), dt_bias=_ptr(dt_bias),
                    A_log=_ptr(A_log), g_min=g_min, scale=scale, state=_ptr(state),
-                   state_indices=_ptr(state_indices), num_slots=state.shape[0], o=_ptr(o))
+                   state_indices=_ptr(state_indices), num_slots=state.shape[0], o=_ptr(o),
+                   gate_kind=_gate_kind(gate))
     _check(L.kda_recurrent_replay(ctypes.byref(a), _stream(q)), "kda_recurrent_replay")
     return o
 
@@ -290,23 +309,27 @@ def set_profile_events(events) -> None:
     _check(L.kda_set_profile_events(arr, len(events)), "kda_set_profile_events")
 
 
-def chunk_fwd_kernel_count(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, cu_seqlens_host=None) -> int:
+def chunk_fwd_kernel_count(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, cu_seqlens_host=None,
+                           gate: str = "lower_bound") -> int:
     """Kernels kda_chunk_fwd launches for these sizes (the split-sequence state pass adds two)."""
     cu = None
     if cu_seqlens_host is not None:
         cu = cu_seqlens_host.to(dtype=torch.int32, device="cpu").contiguous()
     a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=KDA_BF16 if dtype == torch.bfloat16 else KDA_F32,
-                  cu_seqlens_host=None if cu is None else cu.data_ptr(), chunk_size=64)
+                  cu_seqlens_host=None if cu is None else cu.data_ptr(), chunk_size=64,
+                  gate_kind=_gate_kind(gate))
     return int(load_library().kda_chunk_fwd_kernel_count(ctypes.byref(a)))
 
 
-def chunk_fwd_schedule(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, cu_seqlens_host=None) -> dict:
+def chunk_fwd_schedule(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, cu_seqlens_host=None,
+                       gate: str = "lower_bound") -> dict:
     """The schedule kda_chunk_fwd picks for these sizes (see kda_chunk_fwd_schedule in kda.h)."""
     cu = None
     if cu_seqlens_host is not None:
         cu = cu_seqlens_host.to(dtype=torch.int32, device="cpu").contiguous()
     a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=KDA_BF16 if dtype == torch.bfloat16 else KDA_F32,
-                  cu_seqlens_host=None if cu is None else cu.data_ptr(), chunk_size=64)
+                  cu_seqlens_host=None if cu is None else cu.data_ptr(), chunk_size=64,
+                  gate_kind=_gate_kind(gate))
     out = (_i64 * 4)()
     _check(load_library().kda_chunk_fwd_schedule(ctypes.byref(a), out), "kda_chunk_fwd_schedule")
     return {"fused": bool(out[0]), "own_chunks": int(out[1]), "seg_len": int(out[2]), "kernels": int(out[3])}
@@ -316,7 +339,8 @@ def chunk_fwd_static_ws(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: fl
                         scale: float = 1.0, cu_seqlens: Optional[torch.Tensor] = None,
                         cu_seqlens_host: Optional[torch.Tensor] = None, n_seq: int = 1,
                         initial_state: Optional[torch.Tensor] = None,
-                        final_state: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None):
+                        final_state: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                        gate: str = "lower_bound"):
     """kda_chunk_fwd_static_ws: prefill using the library's own fixed scratch buffer.
 
     For callers that must not allocate device scratch: outputs (`out`,
@@ -338,6 +362,6 @@ def chunk_fwd_static_ws(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: fl
                   scale=scale, cu_seqlens=_ptr(cu_seqlens),
                   cu_seqlens_host=None if cu_seqlens_host is None else cu_seqlens_host.data_ptr(),
                   initial_state=_ptr(initial_state), final_state=_ptr(final_state), o=_ptr(o),
-                  chunk_size=64)
+                  chunk_size=64, gate_kind=_gate_kind(gate))
     _check(L.kda_chunk_fwd_static_ws(ctypes.byref(a), _stream(q)), "kda_chunk_fwd_static_ws")
     return o, final_state

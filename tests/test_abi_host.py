@@ -46,7 +46,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.kda_abi_version() == 2
+    assert lib.kda_abi_version() == 3
     for code, name in kda._STATUS.items():
         s = lib.kda_status_string(code).decode()
         assert s and s != "unknown status", name
@@ -132,6 +132,9 @@ def _call_chunk(lib, a, ws=FAKE, ws_bytes=1 << 40):
     (dict(out_gate=FAKE + 16384, out_norm_eps=1e-6), 1),         # gate aliases o
     (dict(out_gate=FAKE + 32776, out_norm_eps=1e-6), 4),
     (dict(out_gate=FAKE + 32768, out_norm_weight=FAKE + 40964, out_norm_eps=1e-6), 4),
+    (dict(gate_kind=2), 1),                                      # no such gate
+    (dict(gate_kind=-1), 1),
+    (dict(gate_kind=1, g_min=0.0, q=None), 1),                   # softplus ignores g_min; q still checked
 ])
 def test_chunk_fwd_rejects(lib, kw, code):
     assert _call_chunk(lib, _chunk(**kw)) == code
@@ -146,6 +149,13 @@ def test_chunk_fwd_workspace_checks(lib):
     assert _call_chunk(lib, a, ws=FAKE + 16, ws_bytes=need) == 4
     assert lib.kda_chunk_fwd_workspace_size(128, 1, 2, 96, 96, kda.KDA_BF16, 64, None) == 0
     assert lib.kda_chunk_fwd_workspace_size(128, 0, 2, 128, 128, kda.KDA_BF16, 64, None) == 0
+    # the plain call is gate kind 0; the softplus gate takes the fp32 path, whose records are larger
+    assert lib.kda_chunk_fwd_workspace_size_gate(128, 1, 2, 128, 128, kda.KDA_BF16, 64, None, 0) == need
+    sp = lib.kda_chunk_fwd_workspace_size_gate(128, 1, 2, 128, 128, kda.KDA_BF16, 64, None, 1)
+    assert sp > need
+    assert sp == lib.kda_chunk_fwd_workspace_size(128, 1, 2, 128, 128, kda.KDA_F32, 64, None)
+    assert lib.kda_chunk_fwd_workspace_size_gate(128, 1, 2, 128, 128, kda.KDA_BF16, 64, None, 3) == 0
+    assert _call_chunk(lib, _chunk(gate_kind=1), ws_bytes=need) == 5
 
 
 def test_chunk_fwd_host_seqlens_validated(lib):
@@ -174,6 +184,8 @@ def _step(**kw):
     (dict(state=FAKE + 65544), 4),
     (dict(beta=FAKE + 8193), 4),
     (dict(g_min=1.0), 1),
+    (dict(gate_kind=7), 1),
+    (dict(gate_kind=1, g_min=1.0, state=None), 1),   # g_min ignored, the state still required
 ])
 def test_recurrent_step_rejects(lib, kw, code):
     assert lib.kda_recurrent_step(ctypes.byref(_step(**kw)), None) == code
@@ -193,6 +205,14 @@ def test_gate_rejects(lib):
     assert lib.kda_gate(ctypes.byref(a), None) == 1
     a.chunk_size = 1000
     assert lib.kda_gate(ctypes.byref(a), None) == 1
+    a.chunk_size = 0
+    a.N = 1
+    a.gate_kind = 5
+    assert lib.kda_gate(ctypes.byref(a), None) == 1
+    a.gate_kind = 1
+    a.g_min = 0.5  # ignored by the softplus gate: the call then fails only on the misaligned z
+    a.z = FAKE + 2
+    assert lib.kda_gate(ctypes.byref(a), None) == 4
 
 
 def _og(**kw):
@@ -240,6 +260,7 @@ def _rp(**kw):
     (dict(rq=FAKE + 8), 4),
     (dict(n_commit=FAKE + 36866), 4),
     (dict(g_min=1.0), 1),
+    (dict(gate_kind=2), 1),
 ])
 def test_recurrent_replay_rejects(lib, kw, code):
     assert lib.kda_recurrent_replay(ctypes.byref(_rp(**kw)), None) == code
