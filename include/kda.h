@@ -205,6 +205,52 @@ typedef struct {
 
 kda_status_t kda_recurrent_replay(const kda_replay_args *args, struct CUstream_st *stream);
 
+/* ------------------------------------------------------------- kda_chunk_bwd
+ * Backward pass of kda_chunk_fwd, for training (the FlashKDA kernels of section 5.1.1 serve
+ * training; the report gives the forward only).  The gradients are the exact derivatives of the
+ * chunkwise form of Eq. 3 and Eq. 4 (which equals Eq. 1): given dL/do and optionally dL/dS_T, it
+ * returns dL/d of q, k, v, z, beta, dt_bias, A_log and the initial state.  Across chunks the
+ * state's adjoint runs backwards, Lambda_in = Diag(gamma^C) Lambda + scale Q^^T dO - W^T dV~ with
+ * dV~ = K~ Lambda + scale A^T dO; every other gradient is local to its chunk (the state entering
+ * it, the Lambda leaving it and dO).  The forward quantities are recomputed (nothing is kept from
+ * kda_chunk_fwd); all arithmetic is fp32 on CUDA cores.  The gate's derivative (either gate kind)
+ * is applied per token; dt_bias and A_log gradients are summed over all tokens.
+ * Supported: as kda_chunk_fwd (d_k = d_v in {64, 128}, chunk_size 64).
+ */
+typedef struct {
+    int64_t T, N;                   /* tokens, sequences (as kda_chunk_fwd) */
+    int32_t H, dk, dv;
+    kda_dtype_t dtype;              /* dtype of every [T, ...] tensor below, inputs and gradients */
+    const void *q, *k, *z;          /* [T, H, dk] forward inputs */
+    const void *v;                  /* [T, H, dv] */
+    const void *beta;               /* [T, H] */
+    const float *dt_bias;           /* [H, dk] or NULL */
+    const float *A_log;             /* [H] or NULL */
+    float g_min, scale;             /* as kda_chunk_fwd */
+    const int32_t *cu_seqlens;      /* [N + 1] device, or NULL for N sequences of T / N tokens */
+    const float *initial_state;     /* [N, H, dk, dv] or NULL (zero) */
+    const void *grad_o;             /* [T, H, dv] dL/do */
+    const float *grad_final_state;  /* [N, H, dk, dv] dL/dS_T, or NULL (zero) */
+    void *grad_q, *grad_k, *grad_z; /* [T, H, dk] outputs (grad_z is dL/dz, the gate's input) */
+    void *grad_v;                   /* [T, H, dv] */
+    void *grad_beta;                /* [T, H] */
+    float *grad_dt_bias;            /* [H, dk], or NULL to skip */
+    float *grad_A_log;              /* [H], or NULL to skip */
+    float *grad_initial_state;      /* [N, H, dk, dv], or NULL to skip */
+    int32_t chunk_size;             /* 64, or 0 for the default */
+    int32_t gate_kind;              /* kda_gate_kind_t */
+} kda_chunk_bwd_args;
+
+/* Bytes of device scratch kda_chunk_bwd needs (0 on invalid sizes): per (chunk, head) about
+ * 0.8 MiB at d = 128 (fp32 records, L, the entering state, the leaving Lambda and per-value-tile
+ * partial sums), independent of dtype and gate kind. */
+size_t kda_chunk_bwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
+                                    int32_t chunk_size);
+
+/* Gradients must not alias the forward inputs or one another.  workspace as kda_chunk_fwd. */
+kda_status_t kda_chunk_bwd(const kda_chunk_bwd_args *args, void *workspace, size_t workspace_bytes,
+                           struct CUstream_st *stream);
+
 /* ----------------------------------------------------------- kda_output_gate
  * The output epilogue of Eq. 6 (section 2.1.1), y_t = W_o[Sigmoid(W_g x_t) * RMSNorm(o~_t)], without
  * the two projections: for every token t and head h,

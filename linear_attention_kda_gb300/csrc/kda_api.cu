@@ -238,6 +238,58 @@ kda_status_t kda_chunk_fwd(const kda_chunk_args *a, void *workspace, size_t work
     return kda_launch_output_gate(&og, (cudaStream_t)stream);
 }
 
+size_t kda_chunk_bwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
+                                    int32_t chunk_size) {
+    if (T < 0 || N < 1 || H < 1 || dk != dv || (dk != 64 && dk != 128)) return 0;
+    if (chunk_size != 0 && chunk_size != 64) return 0;
+    return kda_chunk_bwd_layout_bytes(T, N, H, dk, dv);
+}
+
+kda_status_t kda_chunk_bwd(const kda_chunk_bwd_args *a, void *workspace, size_t workspace_bytes,
+                           struct CUstream_st *stream) {
+    if (!a) return KDA_ERR_INVALID_ARG;
+    if (a->T < 0 || a->N < 1 || a->H < 1) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(a->dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (a->dk != a->dv || (a->dk != 64 && a->dk != 128)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (a->chunk_size != 0 && a->chunk_size != 64) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!gate_ok(a->gate_kind, a->g_min) || !isfinite(a->scale)) return KDA_ERR_INVALID_ARG;
+    if (!a->cu_seqlens && a->T % a->N != 0) return KDA_ERR_INVALID_ARG;
+    if (a->T > INT32_MAX || a->N * (int64_t)a->H > INT32_MAX) return KDA_ERR_UNSUPPORTED_SHAPE;
+    const size_t es = dtype_size(a->dtype);
+    if (a->T > 0) {
+        const void *in[] = {a->q, a->k, a->z, a->v, a->beta, a->grad_o};
+        const void *out[] = {a->grad_q, a->grad_k, a->grad_z, a->grad_v, a->grad_beta};
+        for (const void *p : in)
+            if (!p) return KDA_ERR_INVALID_ARG;
+        for (const void *p : out) {
+            if (!p) return KDA_ERR_INVALID_ARG;
+            for (const void *x : in)
+                if (p == x) return KDA_ERR_INVALID_ARG;
+        }
+        for (int i = 0; i < 5; ++i)
+            for (int j = i + 1; j < 5; ++j)
+                if (out[i] == out[j]) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->z) || !aligned16(a->v) ||
+            !aligned16(a->grad_o) || !aligned16(a->grad_q) || !aligned16(a->grad_k) || !aligned16(a->grad_z) ||
+            !aligned16(a->grad_v) || !aligned_to(a->beta, es) || !aligned_to(a->grad_beta, es))
+            return KDA_ERR_MISALIGNED;
+    }
+    if ((a->initial_state && !aligned16(a->initial_state)) ||
+        (a->grad_final_state && !aligned16(a->grad_final_state)) ||
+        (a->grad_initial_state && !aligned16(a->grad_initial_state)) ||
+        (a->dt_bias && !aligned16(a->dt_bias)) || (a->A_log && !aligned_to(a->A_log, 4)) ||
+        (a->grad_dt_bias && !aligned_to(a->grad_dt_bias, 4)) || (a->grad_A_log && !aligned_to(a->grad_A_log, 4)) ||
+        (a->cu_seqlens && !aligned_to(a->cu_seqlens, 4)))
+        return KDA_ERR_MISALIGNED;
+    const size_t need = kda_chunk_bwd_layout_bytes(a->T, a->N, a->H, a->dk, a->dv);
+    if (need == 0) return KDA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned_to(workspace, 256)) return KDA_ERR_MISALIGNED;
+    kda_status_t st = check_device();
+    if (st != KDA_OK) return st;
+    return kda_launch_chunk_bwd(a, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
 kda_status_t kda_output_gate(const kda_output_gate_args *a, struct CUstream_st *stream) {
     if (!a) return KDA_ERR_INVALID_ARG;
     if (a->T < 0 || a->H < 1) return KDA_ERR_INVALID_ARG;

@@ -1,0 +1,582 @@
+// Backward pass of the chunked prefill (kda_chunk_bwd).  The Kimi K3 report (section 2.1.1, Eq. 3
+// and Eq. 4) gives the forward only; the gradients here are the exact derivatives of that chunkwise
+// form.  Per chunk (rows r of c tokens, state S entering it, Lambda = dL/dS leaving it), with the
+// forward quantities of the fp32 path (G the in-chunk cumulative log-decay, E_ric = e^{G_rc - G_ic},
+// A, L, T = (I + L)^{-1}, W = T diag(b)(Gamma K), U = T diag(b) V, Q^, K~, gamma):
+//     V~ = U - W S,                     dV~ = K~ Lambda + scale A^T dO,
+//     dS_in = Diag(gamma) Lambda + scale Q^^T dO - W^T dV~           (reverse recurrence),
+//     dQ^ = scale dO S^T,  dA = scale dO V~^T,  dK~ = V~ Lambda^T,  dW = -dV~ S^T,
+//     dX_W = T^T dW,  dX_U = T^T dV~,  dL = -(dX_W W^T + dX_U U^T)   (strictly lower),
+// and the elementwise and pairwise derivatives of X_W = diag(b)(Gamma K), X_U = diag(b) V, Q^, K~,
+// gamma, A and L with respect to q, k, v, beta and G; dg is the reverse cumulative sum of dG, and
+// the gate's derivative gives dz, d dt_bias and d A_log.
+//
+// Kernels (all fp32 CUDA-core arithmetic; the forward is recomputed by the fp32 path, which also
+// writes L and the state entering every chunk):
+//   chunk_rev_chain_kernel   one CTA per (sequence, head, 32 value columns): Lambda over the chunks
+//                            in reverse (columns of Lambda evolve independently, as those of S),
+//                            storing the Lambda leaving each chunk;
+//   chunk_bwd_value_kernel   one CTA per (chunk, head, 32 value columns): V~, dV~, dX_U (T^T by
+//                            back substitution), dv, and this tile's share of every contraction over
+//                            the value channels (dQ^, dW, dK~, dA, the X_U part of dL, d gamma,
+//                            the X_U part of d beta), written as partial sums;
+//   chunk_bwd_key_kernel     one CTA per (chunk, head): sums the partials, dX_W = T^T dW, dL, then
+//                            per (row, channel) the pairwise A and L terms, dq, dk, dG; the reverse
+//                            cumulative sum; dz, d beta and per-chunk sums for d dt_bias, d A_log;
+//   bwd_gate_param_kernel    sums the per-chunk gate-parameter gradients per head.
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace bw {
+
+constexpr int NT = 256;   // threads per CTA
+constexpr int TILE = 32;  // value columns per CTA (one per lane)
+
+struct Rec {
+    const float *W, *U, *Q, *K, *A, *gam;
+};
+__device__ __forceinline__ Rec rec_at(const char *base, size_t rec_bytes, int64_t slot, int H, int h, int C,
+                                      int dk, int dv) {
+    const float *r = (const float *)(base + ((size_t)slot * H + h) * rec_bytes);
+    Rec v;
+    v.W = r;
+    v.U = v.W + C * dk;
+    v.Q = v.U + C * dv;
+    v.K = v.Q + C * dk;
+    v.A = v.K + C * dk;
+    v.gam = v.A + C * C;
+    return v;
+}
+
+// chunk slot -> (sequence n, first token t0, valid length len); false past the last chunk
+__device__ __forceinline__ bool locate(const int32_t *chunk_start, const int32_t *cu, int64_t T, int N, int C,
+                                       int64_t slot, int &n, int64_t &t0, int &len) {
+    if (slot >= chunk_start[N]) return false;
+    int lo = 0, hi = N;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (chunk_start[mid] <= slot) lo = mid; else hi = mid;
+    }
+    n = lo;
+    const int64_t s = cu ? (int64_t)cu[n] : (T / N) * n;
+    const int64_t e = cu ? (int64_t)cu[n + 1] : s + T / N;
+    t0 = s + (slot - chunk_start[n]) * (int64_t)C;
+    len = (int)min((int64_t)C, e - t0);
+    return true;
+}
+
+// Partial sums one value tile contributes, per (chunk slot, head, tile), in floats.
+struct Part {
+    int C, dk;
+    __host__ __device__ int dQ() const { return 0; }
+    __host__ __device__ int dW() const { return C * dk; }
+    __host__ __device__ int dK() const { return 2 * C * dk; }
+    __host__ __device__ int dA() const { return 3 * C * dk; }
+    __host__ __device__ int dLu() const { return 3 * C * dk + C * C; }
+    __host__ __device__ int dgam() const { return 3 * C * dk + 2 * C * C; }
+    __host__ __device__ int dbu() const { return 3 * C * dk + 2 * C * C + dk; }
+    __host__ __device__ int size() const { return 3 * C * dk + 2 * C * C + dk + C; }
+};
+
+// ------------------------------------------------------------------ reverse chain over the chunks
+template <typename Tio>
+__global__ void __launch_bounds__(NT)
+chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
+                       int H, int dk, int dv, int C, const char *__restrict__ records, size_t rec_bytes,
+                       float scale, const Tio *__restrict__ d_o, const float *__restrict__ d_final,
+                       float *__restrict__ lam_end, float *__restrict__ d_init) {
+    extern __shared__ float sm[];
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const int j0 = blockIdx.y * TILE;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NWARP = NT / 32;
+    const int PK = dk + 1, PC = C + 1, PS = TILE + 1;
+    float *Ws = sm;               // [C][PK]
+    float *Qs = Ws + C * PK;      // [C][PK]
+    float *Kt = Qs + C * PK;      // [C][PK]
+    float *As = Kt + C * PK;      // [C][PC]
+    float *dOs = As + C * PC;     // [C][PS]
+    float *dVt = dOs + C * PS;    // [C][PS]
+    float *Lm = dVt + C * PS;     // [dk][PS]
+    float *gam = Lm + dk * PS;    // [dk]
+
+    const size_t sbase = ((size_t)n * H + h) * (size_t)dk * dv;
+    for (int e = tid; e < dk * TILE; e += NT) {
+        const int c = e / TILE, j = e % TILE;
+        Lm[c * PS + j] = d_final ? d_final[sbase + (size_t)c * dv + j0 + j] : 0.f;
+    }
+    const int64_t s_tok = cu ? (int64_t)cu[n] : (T / N) * n;
+    const int64_t e_tok = cu ? (int64_t)cu[n + 1] : s_tok + T / N;
+    const int c0 = chunk_start[n], c1 = chunk_start[n + 1];
+    for (int cix = c1 - 1; cix >= c0; --cix) {
+        const int64_t t0 = s_tok + (int64_t)(cix - c0) * C;
+        const int len = (int)min((int64_t)C, e_tok - t0);
+        const Rec rec = rec_at(records, rec_bytes, cix, H, h, C, dk, dv);
+        __syncthreads();  // the previous chunk is done with the buffers; Lambda is final
+        float *lg = lam_end + ((size_t)cix * H + h) * (size_t)dk * dv;
+        for (int e = tid; e < dk * TILE; e += NT) {
+            const int c = e / TILE, j = e % TILE;
+            lg[(size_t)c * dv + j0 + j] = Lm[c * PS + j];
+        }
+        for (int e = tid; e < C * dk; e += NT) {
+            const int r = e / dk, c = e % dk;
+            Ws[r * PK + c] = rec.W[e];
+            Qs[r * PK + c] = rec.Q[e];
+            Kt[r * PK + c] = rec.K[e];
+        }
+        for (int e = tid; e < C * C; e += NT) As[(e / C) * PC + e % C] = rec.A[e];
+        for (int e = tid; e < C * TILE; e += NT) {
+            const int r = e / TILE, j = e % TILE;
+            dOs[r * PS + j] = r < len ? ld(d_o + ((t0 + r) * H + h) * (int64_t)dv + j0 + j) : 0.f;
+        }
+        for (int c = tid; c < dk; c += NT) gam[c] = rec.gam[c];
+        __syncthreads();
+        // dV~ = K~ Lambda + scale A^T dO
+        for (int r = warp; r < len; r += NWARP) {
+            float acc = 0.f, accA = 0.f;
+            for (int c = 0; c < dk; ++c) acc += Kt[r * PK + c] * Lm[c * PS + lane];
+            for (int i = r; i < len; ++i) accA += As[i * PC + r] * dOs[i * PS + lane];
+            dVt[r * PS + lane] = acc + scale * accA;
+        }
+        __syncthreads();
+        // Lambda <- Diag(gamma) Lambda + scale Q^^T dO - W^T dV~  (each entry reads only itself of Lambda)
+        for (int c = warp; c < dk; c += NWARP) {
+            float acc = gam[c] * Lm[c * PS + lane];
+            for (int r = 0; r < len; ++r)
+                acc += scale * Qs[r * PK + c] * dOs[r * PS + lane] - Ws[r * PK + c] * dVt[r * PS + lane];
+            Lm[c * PS + lane] = acc;
+        }
+    }
+    __syncthreads();
+    if (d_init) {
+        for (int e = tid; e < dk * TILE; e += NT) {
+            const int c = e / TILE, j = e % TILE;
+            d_init[sbase + (size_t)c * dv + j0 + j] = Lm[c * PS + j];
+        }
+    }
+}
+
+// ------------------------------------------------------------------ value side, per (chunk, head, tile)
+template <typename Tio>
+__global__ void __launch_bounds__(NT)
+chunk_bwd_value_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
+                       int H, int dk, int dv, int C, const char *__restrict__ records, size_t rec_bytes,
+                       const float *__restrict__ Lbuf, const float *__restrict__ ckpt,
+                       const float *__restrict__ lam_end, float scale, const Tio *__restrict__ v,
+                       const Tio *__restrict__ beta, const Tio *__restrict__ d_o, Tio *__restrict__ grad_v,
+                       float *__restrict__ part) {
+    extern __shared__ float sm[];
+    const int64_t slot = blockIdx.x;
+    const int h = blockIdx.y, tile = blockIdx.z, j0 = tile * TILE;
+    int n, len;
+    int64_t t0;
+    if (!locate(chunk_start, cu, T, N, C, slot, n, t0, len)) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NWARP = NT / 32;
+    const int PK = dk + 1, PC = C + 1, PS = TILE + 1;
+    float *Ws = sm;               // [C][PK]
+    float *Kt = Ws + C * PK;      // [C][PK]
+    float *As = Kt + C * PK;      // [C][PC]
+    float *Ls = As + C * PC;      // [C][PC]
+    float *Ss = Ls + C * PC;      // [dk][PS]
+    float *Lm = Ss + dk * PS;     // [dk][PS]
+    float *dOs = Lm + dk * PS;    // [C][PS]
+    float *Vs = dOs + C * PS;     // [C][PS]  v
+    float *Us = Vs + C * PS;      // [C][PS]
+    float *Vt = Us + C * PS;      // [C][PS]  V~
+    float *dVt = Vt + C * PS;     // [C][PS]  dV~, then dX_U
+    float *bet = dVt + C * PS;    // [C]
+
+    const Rec rec = rec_at(records, rec_bytes, slot, H, h, C, dk, dv);
+    const size_t mbase = ((size_t)slot * H + h) * (size_t)dk * dv;
+    const float *Lg = Lbuf + ((size_t)slot * H + h) * (size_t)C * C;
+    for (int e = tid; e < C * dk; e += NT) {
+        const int r = e / dk, c = e % dk;
+        Ws[r * PK + c] = rec.W[e];
+        Kt[r * PK + c] = rec.K[e];
+    }
+    for (int e = tid; e < C * C; e += NT) {
+        As[(e / C) * PC + e % C] = rec.A[e];
+        Ls[(e / C) * PC + e % C] = Lg[e];
+    }
+    for (int e = tid; e < dk * TILE; e += NT) {
+        const int c = e / TILE, j = e % TILE;
+        Ss[c * PS + j] = ckpt[mbase + (size_t)c * dv + j0 + j];
+        Lm[c * PS + j] = lam_end[mbase + (size_t)c * dv + j0 + j];
+    }
+    for (int e = tid; e < C * TILE; e += NT) {
+        const int r = e / TILE, j = e % TILE;
+        const bool ok = r < len;
+        const int64_t idx = ((t0 + r) * H + h) * (int64_t)dv + j0 + j;
+        dOs[r * PS + j] = ok ? ld(d_o + idx) : 0.f;
+        Vs[r * PS + j] = ok ? ld(v + idx) : 0.f;
+        Us[r * PS + j] = rec.U[r * dv + j0 + j];
+    }
+    for (int r = tid; r < C; r += NT) bet[r] = r < len ? ld(beta + (t0 + r) * H + h) : 0.f;
+    __syncthreads();
+    // V~ = U - W S and dV~ = K~ Lambda + scale A^T dO (zero past len: those rows of U, W, K~, A vanish)
+    for (int r = warp; r < C; r += NWARP) {
+        float vt = Us[r * PS + lane], dvt = 0.f, da = 0.f;
+        for (int c = 0; c < dk; ++c) {
+            vt -= Ws[r * PK + c] * Ss[c * PS + lane];
+            dvt += Kt[r * PK + c] * Lm[c * PS + lane];
+        }
+        for (int i = r; i < len; ++i) da += As[i * PC + r] * dOs[i * PS + lane];
+        Vt[r * PS + lane] = vt;
+        dVt[r * PS + lane] = dvt + scale * da;
+    }
+    __syncthreads();
+    // this tile's share of the contractions over value channels
+    const Part P{C, dk};
+    float *pp = part + (((size_t)slot * H + h) * (size_t)(dv / TILE) + tile) * (size_t)P.size();
+    for (int e = tid; e < C * dk; e += NT) {
+        const int r = e / dk, c = e % dk;
+        float dq = 0.f, dw = 0.f, dkt = 0.f;
+        for (int l = 0; l < TILE; ++l) {
+            const float s = Ss[c * PS + l];
+            dq += dOs[r * PS + l] * s;
+            dw -= dVt[r * PS + l] * s;
+            dkt += Vt[r * PS + l] * Lm[c * PS + l];
+        }
+        pp[P.dQ() + e] = scale * dq;
+        pp[P.dW() + e] = dw;
+        pp[P.dK() + e] = dkt;
+    }
+    for (int e = tid; e < C * C; e += NT) {
+        const int r = e / C, i = e % C;
+        float da = 0.f;
+        if (i <= r)
+            for (int l = 0; l < TILE; ++l) da += dOs[r * PS + l] * Vt[i * PS + l];
+        pp[P.dA() + e] = scale * da;
+    }
+    for (int c = tid; c < dk; c += NT) {
+        float dg = 0.f;
+        for (int l = 0; l < TILE; ++l) dg += Ss[c * PS + l] * Lm[c * PS + l];
+        pp[P.dgam() + c] = dg;
+    }
+    __syncthreads();
+    // dX_U = T^T dV~: back substitution x_r = b_r - sum_{i > r} L_ir x_i, 8 threads per column
+    {
+        const int col = tid >> 3, part8 = tid & 7;
+        for (int r = C - 2; r >= 0; --r) {
+            float acc = 0.f;
+            for (int i = r + 1 + part8; i < C; i += 8) acc += Ls[i * PC + r] * dVt[i * PS + col];
+            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            if (part8 == 0) dVt[r * PS + col] -= acc;
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // dv = beta dX_U;  X_U parts of d beta and dL
+    for (int e = tid; e < len * TILE; e += NT) {
+        const int r = e / TILE, j = e % TILE;
+        st(grad_v + ((t0 + r) * H + h) * (int64_t)dv + j0 + j, bet[r] * dVt[r * PS + j]);
+    }
+    for (int r = tid; r < C; r += NT) {
+        float db = 0.f;
+        for (int l = 0; l < TILE; ++l) db += dVt[r * PS + l] * Vs[r * PS + l];
+        pp[P.dbu() + r] = db;
+    }
+    for (int e = tid; e < C * C; e += NT) {
+        const int r = e / C, i = e % C;
+        float dl = 0.f;
+        if (i < r)
+            for (int l = 0; l < TILE; ++l) dl -= dVt[r * PS + l] * Us[i * PS + l];
+        pp[P.dLu() + e] = dl;
+    }
+}
+
+// ------------------------------------------------------------------ key side, per (chunk, head)
+// Thread t owns channel c = t % dk of rows r = t / dk, t / dk + NT / dk, ...
+template <typename Tio>
+__global__ void __launch_bounds__(NT)
+chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
+                     int H, int dk, int dv, int C, const char *__restrict__ records, size_t rec_bytes,
+                     const float *__restrict__ Lbuf, const float *__restrict__ part, const Tio *__restrict__ q,
+                     const Tio *__restrict__ k, const Tio *__restrict__ z, const Tio *__restrict__ beta,
+                     const float *__restrict__ bias, const float *__restrict__ A_log, float g_min, int kind,
+                     Tio *__restrict__ grad_q, Tio *__restrict__ grad_k, Tio *__restrict__ grad_z,
+                     Tio *__restrict__ grad_beta, float *__restrict__ gate_part) {
+    extern __shared__ float sm[];
+    const int64_t slot = blockIdx.x;
+    const int h = blockIdx.y;
+    int n, len;
+    int64_t t0;
+    if (!locate(chunk_start, cu, T, N, C, slot, n, t0, len)) return;
+    const int tid = threadIdx.x;
+    const int PK = dk + 1, PC = C + 1;
+    const int NR = NT / dk;           // row groups
+    float *qs = sm;                   // [C][PK]
+    float *ks = qs + C * PK;          // [C][PK]
+    float *Gs = ks + C * PK;          // [C][PK]  in-chunk cumulative log-decay
+    float *dX = Gs + C * PK;          // [C][PK]  dW -> dX_W -> per-element d beta terms
+    float *dG = dX + C * PK;          // [C][PK]
+    float *Ls = dG + C * PK;          // [C][PC]
+    float *dLs = Ls + C * PC;         // [C][PC]
+    float *dAs = dLs + C * PC;        // [C][PC]
+    float *bet = dAs + C * PC;        // [C]
+    float *red = bet + C;             // [NR][dk] per-row-group channel sums
+
+    const Part P{C, dk};
+    const int ntile = dv / TILE;
+    const float *pp = part + ((size_t)slot * H + h) * (size_t)ntile * P.size();
+    const float *Lg = Lbuf + ((size_t)slot * H + h) * (size_t)C * C;
+    const float eA = A_log ? expf(A_log[h]) : 1.f;
+    for (int e = tid; e < C * dk; e += NT) {
+        const int r = e / dk, c = e % dk;
+        const bool ok = r < len;
+        const int64_t idx = ((t0 + r) * H + h) * (int64_t)dk + c;
+        qs[r * PK + c] = ok ? ld(q + idx) : 0.f;
+        ks[r * PK + c] = ok ? ld(k + idx) : 0.f;
+        Gs[r * PK + c] = ok ? gate_log(kind, ld(z + idx), bias ? bias[h * dk + c] : 0.f, eA, g_min) : 0.f;
+        float dw = 0.f;
+        for (int t = 0; t < ntile; ++t) dw += pp[(size_t)t * P.size() + P.dW() + e];
+        dX[r * PK + c] = dw;
+    }
+    for (int e = tid; e < C * C; e += NT) {
+        const int r = e / C, i = e % C;
+        float da = 0.f, dl = 0.f;
+        for (int t = 0; t < ntile; ++t) {
+            da += pp[(size_t)t * P.size() + P.dA() + e];
+            dl += pp[(size_t)t * P.size() + P.dLu() + e];
+        }
+        dAs[r * PC + i] = da;
+        dLs[r * PC + i] = dl;
+        Ls[r * PC + i] = Lg[e];
+    }
+    for (int r = tid; r < C; r += NT) bet[r] = r < len ? ld(beta + (t0 + r) * H + h) : 0.f;
+    __syncthreads();
+    for (int c = tid; c < dk; c += NT) {  // cumulative log-decay within the chunk (Eq. 3)
+        float acc = 0.f;
+        for (int r = 0; r < C; ++r) {
+            acc += Gs[r * PK + c];
+            Gs[r * PK + c] = acc;
+        }
+    }
+    // dX_W = T^T dW: back substitution, NT / dk threads per column (adjacent lanes)
+    {
+        const int tpc = NT / dk, col = tid / tpc, sub = tid % tpc;
+        for (int r = C - 2; r >= 0; --r) {
+            float acc = 0.f;
+            for (int i = r + 1 + sub; i < C; i += tpc) acc += Ls[i * PC + r] * dX[i * PK + col];
+            for (int off = tpc >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (sub == 0) dX[r * PK + col] -= acc;
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // dL = (X_U part) - dX_W W^T, strictly lower
+    {
+        const Rec rec = rec_at(records, rec_bytes, slot, H, h, C, dk, dv);
+        for (int e = tid; e < C * C; e += NT) {
+            const int r = e / C, i = e % C;
+            if (i >= r || r >= len) continue;
+            float acc = 0.f;
+            for (int c = 0; c < dk; ++c) acc += dX[r * PK + c] * rec.W[i * dk + c];
+            dLs[r * PC + i] -= acc;
+        }
+    }
+    __syncthreads();
+    // per (row, channel): dq, dk, dG and the d beta terms
+    const int c = tid % dk, rg = tid / dk;
+    float xk_sum = 0.f;  // sum over this thread's rows of dK~ * K~ (flows to G_last)
+    for (int r = rg; r < len; r += NR) {
+        const float Gr = Gs[r * PK + c], Gl = Gs[(C - 1) * PK + c];
+        const float eG = expf(Gr), eL = expf(Gl - Gr);
+        const float qr = qs[r * PK + c], kr = ks[r * PK + c], br = bet[r];
+        float dqh = 0.f, dkt = 0.f;
+        for (int t = 0; t < ntile; ++t) {
+            dqh += pp[(size_t)t * P.size() + P.dQ() + r * dk + c];
+            dkt += pp[(size_t)t * P.size() + P.dK() + r * dk + c];
+        }
+        const float dxw = dX[r * PK + c];
+        float ra = 0.f, rl = 0.f;  // sum_{i <= r} dA_ri k_ic E_ric,  sum_{i < r} dL_ri k_ic E_ric
+        for (int i = 0; i < r; ++i) {
+            const float kE = ks[i * PK + c] * expf(Gr - Gs[i * PK + c]);
+            ra += dAs[r * PC + i] * kE;
+            rl += dLs[r * PC + i] * kE;
+        }
+        ra += dAs[r * PC + r] * kr;
+        float ca = dAs[r * PC + r] * qr, cl = 0.f;  // sum_{r' >= r} dA_r'r q_r'c E, sum_{r' > r} dL_r'r b_r' k_r'c E
+        for (int i = r + 1; i < len; ++i) {
+            const float E = expf(Gs[i * PK + c] - Gr);
+            ca += dAs[i * PC + r] * qs[i * PK + c] * E;
+            cl += dLs[i * PC + r] * bet[i] * ks[i * PK + c] * E;
+        }
+        const float ktil = kr * eL;
+        const float dq = dqh * eG + ra;
+        const float dkk = br * dxw * eG + dkt * eL + ca + br * rl + cl;
+        dG[r * PK + c] = dxw * br * kr * eG + dqh * qr * eG - dkt * ktil + qr * ra - kr * ca + br * kr * rl - kr * cl;
+        dX[r * PK + c] = kr * (eG * dxw + rl);  // this element's share of d beta_r
+        xk_sum += dkt * ktil;
+        const int64_t idx = ((t0 + r) * H + h) * (int64_t)dk + c;
+        st(grad_q + idx, dq);
+        st(grad_k + idx, dkk);
+    }
+    red[rg * dk + c] = xk_sum;
+    __syncthreads();
+    // per channel: G_last collects d gamma * gamma and the K~ terms; dg = reverse cumulative sum of dG;
+    // then the gate's derivative
+    float *gp = gate_part + ((size_t)slot * H + h) * (size_t)(dk + 1);
+    for (int cc = tid; cc < dk; cc += NT) {
+        const Rec rec = rec_at(records, rec_bytes, slot, H, h, C, dk, dv);
+        float dgam = 0.f;
+        for (int t = 0; t < ntile; ++t) dgam += pp[(size_t)t * P.size() + P.dgam() + cc];
+        float run = dgam * rec.gam[cc];
+        for (int g = 0; g < NR; ++g) run += red[g * dk + cc];
+        const float b = bias ? bias[h * dk + cc] : 0.f;
+        float db = 0.f, da = 0.f;
+        for (int r = len - 1; r >= 0; --r) {
+            run += dG[r * PK + cc];
+            const int64_t idx = ((t0 + r) * H + h) * (int64_t)dk + cc;
+            const float zz = ld(z + idx);
+            float dz, dA;
+            if (kind == KDA_GATE_SOFTPLUS) {
+                const float x = zz + b;
+                const float sg = 1.f / (1.f + expf(-x));
+                const float g = gate_log(kind, zz, b, eA, g_min);
+                dz = run * (-eA * sg);
+                dA = run * g;
+            } else {
+                const float x = eA * (zz + b);
+                const float sg = 1.f / (1.f + expf(-x));
+                dz = run * g_min * sg * (1.f - sg) * eA;
+                dA = dz * (zz + b);
+            }
+            st(grad_z + idx, dz);
+            db += dz;
+            da += dA;
+        }
+        gp[cc] = db;
+        red[cc] = da;  // row group 0's slot: read below after the barrier
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float da = 0.f;
+        for (int cc = 0; cc < dk; ++cc) da += red[cc];
+        gp[dk] = da;
+    }
+    for (int r = tid; r < len; r += NT) {  // d beta: X_W and L terms per channel, plus the X_U part
+        float db = 0.f;
+        for (int cc = 0; cc < dk; ++cc) db += dX[r * PK + cc];
+        for (int t = 0; t < ntile; ++t) db += pp[(size_t)t * P.size() + P.dbu() + r];
+        st(grad_beta + (t0 + r) * H + h, db);
+    }
+}
+
+// d dt_bias[h][c] = sum over chunk slots; d A_log[h] likewise
+__global__ void bwd_gate_param_kernel(const float *__restrict__ gate_part, int64_t slots, int H, int dk,
+                                      float *__restrict__ grad_bias, float *__restrict__ grad_alog) {
+    const int h = blockIdx.x;
+    for (int c = threadIdx.x; c <= dk; c += blockDim.x) {
+        float acc = 0.f;
+        for (int64_t s = 0; s < slots; ++s) acc += gate_part[((size_t)s * H + h) * (size_t)(dk + 1) + c];
+        if (c < dk) {
+            if (grad_bias) grad_bias[h * dk + c] = acc;
+        } else if (grad_alog) {
+            grad_alog[h] = acc;
+        }
+    }
+}
+
+}  // namespace bw
+}  // namespace kda
+
+using namespace kda;
+
+namespace {
+
+struct BwdLayout {
+    kda_chunk_plan p;  // chunk table and fp32 records of the forward recomputation
+    int64_t slots;
+    size_t off_L, off_ckpt, off_lam, off_part, off_gate, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool bwd_layout(int64_t T, int64_t N, int H, int dk, int dv, int C, BwdLayout *L) {
+    if (!kda_make_chunk_plan(T, N, H, dk, dv, KDA_F32, C, &L->p, nullptr, 0, true)) return false;
+    const size_t s = (size_t)L->p.max_chunks * H;
+    L->slots = L->p.max_chunks;
+    L->off_L = align256(L->p.total_bytes);
+    L->off_ckpt = align256(L->off_L + s * C * C * sizeof(float));
+    L->off_lam = align256(L->off_ckpt + s * dk * dv * sizeof(float));
+    L->off_part = align256(L->off_lam + s * dk * dv * sizeof(float));
+    const bw::Part P{C, dk};
+    L->off_gate = align256(L->off_part + s * (size_t)(dv / bw::TILE) * P.size() * sizeof(float));
+    L->total = align256(L->off_gate + s * (size_t)(dk + 1) * sizeof(float));
+    return true;
+}
+
+template <typename Tio>
+kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *ws, cudaStream_t stream) {
+    const int C = 64, dk = a->dk, dv = a->dv, H = a->H;
+    char *base = (char *)ws;
+    float *Lbuf = (float *)(base + Ly.off_L), *ckpt = (float *)(base + Ly.off_ckpt);
+    float *lam = (float *)(base + Ly.off_lam), *part = (float *)(base + Ly.off_part);
+    float *gpart = (float *)(base + Ly.off_gate);
+    // 1. the forward again on the fp32 path: records, L and the state entering every chunk
+    kda_chunk_args f{};
+    f.T = a->T; f.N = a->N; f.H = H; f.dk = dk; f.dv = dv; f.dtype = a->dtype;
+    f.q = a->q; f.k = a->k; f.z = a->z; f.v = a->v; f.beta = a->beta;
+    f.dt_bias = a->dt_bias; f.A_log = a->A_log; f.g_min = a->g_min; f.scale = a->scale;
+    f.cu_seqlens = a->cu_seqlens; f.initial_state = a->initial_state; f.chunk_size = 64;
+    f.gate_kind = a->gate_kind;
+    kda_status_t st = kda_launch_chunk_simt_recompute(&f, Ly.p, ws, Lbuf, ckpt, stream);
+    if (st != KDA_OK) return st;
+    const int32_t *chunk_start = (const int32_t *)(base + Ly.p.off_chunk_start);
+    const char *records = base + Ly.p.off_records;
+    const size_t rb = Ly.p.record_bytes;
+    const int PK = dk + 1, PC = C + 1, PS = bw::TILE + 1;
+    // 2. Lambda over the chunks in reverse; d initial_state
+    const size_t smem_rev = sizeof(float) * ((size_t)3 * C * PK + (size_t)C * PC + 2 * (size_t)C * PS +
+                                             (size_t)dk * PS + dk);
+    cudaFuncSetAttribute(bw::chunk_rev_chain_kernel<Tio>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_rev);
+    bw::chunk_rev_chain_kernel<Tio><<<dim3((unsigned)(a->N * H), (unsigned)(dv / bw::TILE)), bw::NT, smem_rev, stream>>>(
+        a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, rb, a->scale, (const Tio *)a->grad_o,
+        a->grad_final_state, lam, a->grad_initial_state);
+    st = kda_cuda_status(cudaGetLastError());
+    if (st != KDA_OK || Ly.slots == 0 || a->T == 0) return st;
+    // 3. value side per (chunk, head, 32 value columns)
+    const size_t smem_val = sizeof(float) * (2 * (size_t)C * PK + 2 * (size_t)C * PC + 2 * (size_t)dk * PS +
+                                             5 * (size_t)C * PS + C);
+    cudaFuncSetAttribute(bw::chunk_bwd_value_kernel<Tio>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_val);
+    bw::chunk_bwd_value_kernel<Tio><<<dim3((unsigned)Ly.slots, (unsigned)H, (unsigned)(dv / bw::TILE)), bw::NT,
+                                      smem_val, stream>>>(
+        a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, rb, Lbuf, ckpt, lam, a->scale,
+        (const Tio *)a->v, (const Tio *)a->beta, (const Tio *)a->grad_o, (Tio *)a->grad_v, part);
+    st = kda_cuda_status(cudaGetLastError());
+    if (st != KDA_OK) return st;
+    // 4. key side per (chunk, head)
+    const size_t smem_key = sizeof(float) * (5 * (size_t)C * PK + 3 * (size_t)C * PC + C + (size_t)bw::NT);
+    cudaFuncSetAttribute(bw::chunk_bwd_key_kernel<Tio>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_key);
+    bw::chunk_bwd_key_kernel<Tio><<<dim3((unsigned)Ly.slots, (unsigned)H), bw::NT, smem_key, stream>>>(
+        a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, rb, Lbuf, part, (const Tio *)a->q,
+        (const Tio *)a->k, (const Tio *)a->z, (const Tio *)a->beta, a->dt_bias, a->A_log, a->g_min, a->gate_kind,
+        (Tio *)a->grad_q, (Tio *)a->grad_k, (Tio *)a->grad_z, (Tio *)a->grad_beta, gpart);
+    st = kda_cuda_status(cudaGetLastError());
+    if (st != KDA_OK) return st;
+    // 5. gate parameters
+    if (a->grad_dt_bias || a->grad_A_log) {
+        bw::bwd_gate_param_kernel<<<(unsigned)H, 128, 0, stream>>>(gpart, Ly.slots, H, dk, a->grad_dt_bias, a->grad_A_log);
+        st = kda_cuda_status(cudaGetLastError());
+    }
+    return st;
+}
+
+}  // namespace
+
+size_t kda_chunk_bwd_layout_bytes(int64_t T, int64_t N, int H, int dk, int dv) {
+    BwdLayout L;
+    return bwd_layout(T, N, H, dk, dv, 64, &L) ? L.total : 0;
+}
+
+kda_status_t kda_launch_chunk_bwd(const kda_chunk_bwd_args *a, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    BwdLayout L;
+    if (!bwd_layout(a->T, a->N, a->H, a->dk, a->dv, 64, &L)) return KDA_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < L.total) return KDA_ERR_WORKSPACE;
+    return a->dtype == KDA_BF16 ? launch_bwd<bf16>(a, L, ws, stream) : launch_bwd<float>(a, L, ws, stream);
+}

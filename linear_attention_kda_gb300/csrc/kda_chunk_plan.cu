@@ -197,13 +197,15 @@ static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int
 }
 
 bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_t dtype, int C,
-                         kda_chunk_plan *p, const int32_t *cu_seqlens_host, int gate_kind) {
+                         kda_chunk_plan *p, const int32_t *cu_seqlens_host, int gate_kind,
+                         bool force_fp32_path) {
     if (T < 0 || N < 1 || H < 1 || C < 1) return false;
     p->T = T; p->N = N; p->H = H; p->dk = dk; p->dv = dv; p->C = C;
     p->max_chunks = (T + N * (int64_t)(C - 1)) / C;
     // bf16 with d_k = d_v = 128 and the bounded gate runs on the tensor cores; everything else on
     // the fp32 CUDA-core path
-    p->path = (dtype == KDA_BF16 && dk == 128 && dv == 128 && C == 64 && gate_kind == KDA_GATE_LOWER_BOUND) ? 1 : 0;
+    p->path = (dtype == KDA_BF16 && dk == 128 && dv == 128 && C == 64 && gate_kind == KDA_GATE_LOWER_BOUND &&
+               !force_fp32_path) ? 1 : 0;
     if (p->path == 1) {
         p->record_bytes = kda_tc_packet_stride();  // bf16 operand images + gamma^C
     } else {

@@ -70,7 +70,7 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
                         const float *__restrict__ bias, const float *__restrict__ A_log, float g_min,
                         int kind, int64_t T, int N, const int32_t *__restrict__ cu,
                         const int32_t *__restrict__ chunk_start, int H, int dk, int dv, int C,
-                        char *__restrict__ records, size_t rec_bytes) {
+                        char *__restrict__ records, size_t rec_bytes, float *__restrict__ Lout) {
     extern __shared__ float sm[];
     const int64_t slot = blockIdx.x;
     const int h = blockIdx.y;
@@ -127,6 +127,10 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
     __syncthreads();
     RecordView rec = record_view(records, rec_bytes, slot, H, h, C, dk, dv);
     for (int e = tid; e < C * C; e += SIMT_THREADS) rec.A[e] = As[(e / C) * PC + e % C];
+    if (Lout) {  // the backward pass reuses L (strictly lower, zeros elsewhere)
+        float *Lg = Lout + ((size_t)slot * H + h) * (size_t)C * C;
+        for (int e = tid; e < C * C; e += SIMT_THREADS) Lg[e] = Ls[(e / C) * PC + e % C];
+    }
     for (int e = tid; e < C * dk; e += SIMT_THREADS) {
         const int r = e / dk, c = e % dk;
         const float G = Gs[r * PK + c], Gl = Gs[(C - 1) * PK + c];  // G is flat past len
@@ -165,7 +169,8 @@ __global__ void __launch_bounds__(SIMT_THREADS)
 chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
                         const int32_t *__restrict__ chunk_start, int H, int dk, int dv, int C,
                         const char *__restrict__ records, size_t rec_bytes, float scale,
-                        const float *initial_state, float *final_state, Tio *__restrict__ o) {
+                        const float *initial_state, float *final_state, Tio *__restrict__ o,
+                        float *__restrict__ ckpt) {
     extern __shared__ float sm[];
     const int n = blockIdx.x / H, h = blockIdx.x % H;
     const int j0 = blockIdx.y * SLICE;
@@ -194,6 +199,13 @@ chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
         const int len = (int)min((int64_t)C, e_tok - t0);
         RecordView rec = record_view((char *)records, rec_bytes, cix, H, h, C, dk, dv);
         __syncthreads();  // previous chunk done with the buffers
+        if (ckpt) {  // the state entering this chunk, for the backward pass
+            float *cg = ckpt + ((size_t)cix * H + h) * (size_t)dk * dv;
+            for (int e = tid; e < dk * SLICE; e += SIMT_THREADS) {
+                const int c = e / SLICE, j = e % SLICE;
+                cg[(size_t)c * dv + j0 + j] = Ss[c * PS + j];
+            }
+        }
         for (int e = tid; e < C * dk; e += SIMT_THREADS) {
             const int r = e / dk, c = e % dk;
             Ws[r * PK + c] = rec.W[e];
@@ -215,7 +227,7 @@ chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
         }
         __syncthreads();
         // O = scale (Q^ S + A V~)
-        for (int r = warp; r < len; r += NWARP) {
+        for (int r = warp; o && r < len; r += NWARP) {
             float acc = 0.f;
             for (int c = 0; c < dk; ++c) acc += Qs[r * PK + c] * Ss[c * PS + lane];
             for (int i = 0; i <= r; ++i) acc += As[r * PC + i] * Vt[i * PS + lane];
@@ -248,8 +260,10 @@ using namespace kda;
 kda_status_t kda_launch_chunk_plan(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
                                    cudaStream_t stream);
 
-kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
-                                   cudaStream_t stream) {
+// The fp32 path; with Lout / ckpt (the backward pass's recomputation) the intra kernel also writes
+// L per (chunk slot, head) and the chain writes the state entering every chunk slot.
+static kda_status_t launch_simt(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws, cudaStream_t stream,
+                                float *Lout, float *ckpt) {
     kda_profile_mark(0, stream);
     kda_status_t st = kda_launch_chunk_plan(a, p, ws, stream);
     if (st != KDA_OK) return st;
@@ -269,13 +283,13 @@ kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan
             chunk_intra_simt_kernel<bf16><<<grid, SIMT_THREADS, smem_intra, stream>>>(
                 (const bf16 *)a->q, (const bf16 *)a->k, (const bf16 *)a->v, (const bf16 *)a->z,
                 (const bf16 *)a->beta, a->dt_bias, a->A_log, a->g_min, a->gate_kind, a->T, (int)a->N, a->cu_seqlens,
-                chunk_start, H, dk, dv, C, records, p.record_bytes);
+                chunk_start, H, dk, dv, C, records, p.record_bytes, Lout);
         } else {
             cudaFuncSetAttribute(chunk_intra_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_intra);
             chunk_intra_simt_kernel<float><<<grid, SIMT_THREADS, smem_intra, stream>>>(
                 (const float *)a->q, (const float *)a->k, (const float *)a->v, (const float *)a->z,
                 (const float *)a->beta, a->dt_bias, a->A_log, a->g_min, a->gate_kind, a->T, (int)a->N, a->cu_seqlens,
-                chunk_start, H, dk, dv, C, records, p.record_bytes);
+                chunk_start, H, dk, dv, C, records, p.record_bytes, Lout);
         }
         {
             const kda_status_t cst = kda_cuda_status(cudaGetLastError());
@@ -288,13 +302,23 @@ kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan
         cudaFuncSetAttribute(chunk_chain_simt_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_chain);
         chunk_chain_simt_kernel<bf16><<<grid2, SIMT_THREADS, smem_chain, stream>>>(
             a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, p.record_bytes,
-            a->scale, a->initial_state, a->final_state, (bf16 *)a->o);
+            a->scale, a->initial_state, a->final_state, (bf16 *)a->o, ckpt);
     } else {
         cudaFuncSetAttribute(chunk_chain_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_chain);
         chunk_chain_simt_kernel<float><<<grid2, SIMT_THREADS, smem_chain, stream>>>(
             a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, p.record_bytes,
-            a->scale, a->initial_state, a->final_state, (float *)a->o);
+            a->scale, a->initial_state, a->final_state, (float *)a->o, ckpt);
     }
     kda_profile_mark(3, stream);
     return kda_cuda_status(cudaGetLastError());
+}
+
+kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
+                                   cudaStream_t stream) {
+    return launch_simt(a, p, ws, stream, nullptr, nullptr);
+}
+
+kda_status_t kda_launch_chunk_simt_recompute(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
+                                             float *Lout, float *ckpt, cudaStream_t stream) {
+    return launch_simt(a, p, ws, stream, Lout, ckpt);
 }

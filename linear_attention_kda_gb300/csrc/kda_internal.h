@@ -48,9 +48,20 @@ struct kda_chunk_plan {
 // gate_kind KDA_GATE_SOFTPLUS always takes the fp32 CUDA-core path (its in-chunk decays are not
 // bounded, so the tensor-core operand images could overflow).
 bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_t dtype, int C,
-                         kda_chunk_plan *plan, const int32_t *cu_seqlens_host = nullptr, int gate_kind = 0);
+                         kda_chunk_plan *plan, const int32_t *cu_seqlens_host = nullptr, int gate_kind = 0,
+                         bool force_fp32_path = false);
 kda_status_t kda_launch_chunk_simt(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
                                    cudaStream_t stream);
 kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
                                  cudaStream_t stream);
+// The fp32 forward again, for the backward pass: records as kda_launch_chunk_simt, plus L per
+// (chunk slot, head) [C][C] into Lout and the state entering each chunk slot [dk][dv] into ckpt;
+// o is written only when a->o is set.
+kda_status_t kda_launch_chunk_simt_recompute(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
+                                             float *Lout, float *ckpt, cudaStream_t stream);
 size_t kda_tc_packet_stride();  // bytes per (chunk, head) packet of the tensor-core path
+
+// Backward pass of the chunked prefill (kda_chunk_bwd.cu): scratch bytes for these sizes (0 if
+// invalid) and the launcher (arguments validated by kda_api.cu).
+size_t kda_chunk_bwd_layout_bytes(int64_t T, int64_t N, int H, int dk, int dv);
+kda_status_t kda_launch_chunk_bwd(const kda_chunk_bwd_args *a, void *ws, size_t ws_bytes, cudaStream_t stream);

@@ -30,7 +30,7 @@ EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_re
             "kda_status_string", "kda_get_device_error", "kda_abi_version",
             "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws",
             "kda_last_cuda_error", "kda_chunk_fwd_schedule", "kda_output_gate", "kda_recurrent_replay",
-            "kda_chunk_fwd_workspace_size_gate"]
+            "kda_chunk_fwd_workspace_size_gate", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 _vp = ctypes.c_void_p
@@ -58,6 +58,15 @@ class ReplayArgs(ctypes.Structure):
                 ("M", _i32), ("q", _vp), ("k", _vp), ("z", _vp), ("v", _vp), ("beta", _vp), ("n_commit", _vp),
                 ("dt_bias", _vp), ("A_log", _vp), ("g_min", _f32), ("scale", _f32), ("state", _vp),
                 ("state_indices", _vp), ("num_slots", _i64), ("o", _vp), ("gate_kind", _i32)]
+
+
+class ChunkBwdArgs(ctypes.Structure):
+    _fields_ = [("T", _i64), ("N", _i64), ("H", _i32), ("dk", _i32), ("dv", _i32), ("dtype", ctypes.c_int),
+                ("q", _vp), ("k", _vp), ("z", _vp), ("v", _vp), ("beta", _vp), ("dt_bias", _vp), ("A_log", _vp),
+                ("g_min", _f32), ("scale", _f32), ("cu_seqlens", _vp), ("initial_state", _vp), ("grad_o", _vp),
+                ("grad_final_state", _vp), ("grad_q", _vp), ("grad_k", _vp), ("grad_z", _vp), ("grad_v", _vp),
+                ("grad_beta", _vp), ("grad_dt_bias", _vp), ("grad_A_log", _vp), ("grad_initial_state", _vp),
+                ("chunk_size", _i32), ("gate_kind", _i32)]
 
 
 class OutputGateArgs(ctypes.Structure):
@@ -101,6 +110,10 @@ def load_library(path: Optional[str] = None):
         L.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
         L.kda_chunk_fwd_workspace_size_gate.argtypes = [_i64, _i64, _i32, _i32, _i32, ctypes.c_int, _i32, _vp, _i32]
         L.kda_chunk_fwd_workspace_size_gate.restype = ctypes.c_size_t
+        L.kda_chunk_bwd_workspace_size.argtypes = [_i64, _i64, _i32, _i32, _i32, _i32]
+        L.kda_chunk_bwd_workspace_size.restype = ctypes.c_size_t
+        L.kda_chunk_bwd.argtypes = [ctypes.POINTER(ChunkBwdArgs), _vp, ctypes.c_size_t, _vp]
+        L.kda_chunk_bwd.restype = ctypes.c_int
         L.kda_recurrent_step.argtypes = [ctypes.POINTER(StepArgs), _vp]
         L.kda_recurrent_step.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -226,6 +239,40 @@ def chunk_fwd(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0
     _check(L.kda_chunk_fwd(ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(q)),
            "kda_chunk_fwd")
     return o, fs
+
+
+def chunk_bwd(q, k, v, z, beta, dt_bias, A_log, grad_o, *, g_min: float = -5.0, scale: float = 1.0,
+              cu_seqlens: Optional[torch.Tensor] = None, n_seq: int = 1,
+              initial_state: Optional[torch.Tensor] = None, grad_final_state: Optional[torch.Tensor] = None,
+              gate: str = "lower_bound", param_grads: bool = True, state_grad: bool = True,
+              workspace: Optional[torch.Tensor] = None) -> dict:
+    """kda_chunk_bwd: gradients of the chunked prefill given grad_o (and grad_final_state).
+
+    Returns a dict with q, k, v, z, beta (dtype of q) and, when asked, dt_bias, A_log (fp32) and
+    initial_state (fp32 [N, H, dk, dv])."""
+    L = load_library()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    _contig(q, k, v, z, beta, dt_bias, A_log, grad_o, cu_seqlens, initial_state, grad_final_state)
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else n_seq
+    g = {n: torch.empty_like(x) for n, x in (("q", q), ("k", k), ("v", v), ("z", z), ("beta", beta))}
+    if param_grads:
+        g["dt_bias"] = torch.zeros((H, dk), dtype=torch.float32, device=q.device)
+        g["A_log"] = torch.zeros((H,), dtype=torch.float32, device=q.device)
+    if state_grad:
+        g["initial_state"] = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    need = int(L.kda_chunk_bwd_workspace_size(T, N, H, dk, dv, 64))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
+    a = ChunkBwdArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=_dtype_code(q), q=_ptr(q), k=_ptr(k), z=_ptr(z), v=_ptr(v),
+                     beta=_ptr(beta), dt_bias=_ptr(dt_bias), A_log=_ptr(A_log), g_min=g_min, scale=scale,
+                     cu_seqlens=_ptr(cu_seqlens), initial_state=_ptr(initial_state), grad_o=_ptr(grad_o),
+                     grad_final_state=_ptr(grad_final_state), grad_q=_ptr(g["q"]), grad_k=_ptr(g["k"]),
+                     grad_z=_ptr(g["z"]), grad_v=_ptr(g["v"]), grad_beta=_ptr(g["beta"]),
+                     grad_dt_bias=_ptr(g.get("dt_bias")), grad_A_log=_ptr(g.get("A_log")),
+                     grad_initial_state=_ptr(g.get("initial_state")), chunk_size=64, gate_kind=_gate_kind(gate))
+    _check(L.kda_chunk_bwd(ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(q)), "kda_chunk_bwd")
+    return g
 
 
 def output_gate(o, g, norm_weight=None, eps: float = 1e-6, *, out: Optional[torch.Tensor] = None):

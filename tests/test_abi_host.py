@@ -64,6 +64,7 @@ int main(void) {
   printf("kda_step_args sizeof %zu\n", sizeof(kda_step_args));
   printf("kda_output_gate_args sizeof %zu\n", sizeof(kda_output_gate_args));
   printf("kda_replay_args sizeof %zu\n", sizeof(kda_replay_args));
+  printf("kda_chunk_bwd_args sizeof %zu\n", sizeof(kda_chunk_bwd_args));
   %FIELDS%
   return 0;
 }
@@ -74,7 +75,7 @@ def test_struct_layout_matches_header(tmp_path):
     fields = []
     for cname, cls in (("kda_gate_args", kda.GateArgs), ("kda_chunk_args", kda.ChunkArgs),
                        ("kda_step_args", kda.StepArgs), ("kda_output_gate_args", kda.OutputGateArgs),
-                       ("kda_replay_args", kda.ReplayArgs)):
+                       ("kda_replay_args", kda.ReplayArgs), ("kda_chunk_bwd_args", kda.ChunkBwdArgs)):
         for f, _ in cls._fields_:
             fields.append(f"F({cname}, {f})")
     src = tmp_path / "layout.c"
@@ -89,7 +90,7 @@ def test_struct_layout_matches_header(tmp_path):
             got[(s, f)] = int(v)
     for cname, cls in (("kda_gate_args", kda.GateArgs), ("kda_chunk_args", kda.ChunkArgs),
                        ("kda_step_args", kda.StepArgs), ("kda_output_gate_args", kda.OutputGateArgs),
-                       ("kda_replay_args", kda.ReplayArgs)):
+                       ("kda_replay_args", kda.ReplayArgs), ("kda_chunk_bwd_args", kda.ChunkBwdArgs)):
         assert got[(cname, "sizeof")] == ctypes.sizeof(cls), cname
         for f, _ in cls._fields_:
             assert got[(cname, f)] == getattr(cls, f).offset, (cname, f)
@@ -283,3 +284,42 @@ def test_valid_args_stop_at_device_check_without_gpu(lib):
     assert lib.kda_recurrent_step(ctypes.byref(_step()), None) == 9
     assert lib.kda_output_gate(ctypes.byref(_og()), None) == 9
     assert lib.kda_recurrent_replay(ctypes.byref(_rp()), None) == 9
+
+
+def _bwd(**kw):
+    base = dict(T=128, N=1, H=2, dk=128, dv=128, dtype=kda.KDA_BF16, q=FAKE, k=FAKE + 1024, z=FAKE + 2048,
+                v=FAKE + 4096, beta=FAKE + 8192, dt_bias=None, A_log=None, g_min=-5.0, scale=1.0, cu_seqlens=None,
+                initial_state=None, grad_o=FAKE + 12288, grad_final_state=None, grad_q=FAKE + 16384,
+                grad_k=FAKE + 20480, grad_z=FAKE + 24576, grad_v=FAKE + 28672, grad_beta=FAKE + 32768,
+                grad_dt_bias=None, grad_A_log=None, grad_initial_state=None, chunk_size=64, gate_kind=0)
+    base.update(kw)
+    return kda.ChunkBwdArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dk=96, dv=96), 2),
+    (dict(chunk_size=16), 2),
+    (dict(dtype=9), 3),
+    (dict(N=0), 1),
+    (dict(T=130, N=4), 1),
+    (dict(g_min=0.0), 1),
+    (dict(gate_kind=4), 1),
+    (dict(grad_o=None), 1),
+    (dict(grad_q=None), 1),
+    (dict(grad_q=FAKE), 1),                # a gradient aliases an input
+    (dict(grad_k=FAKE + 16384), 1),        # two gradients alias
+    (dict(grad_v=FAKE + 28680), 4),
+    (dict(grad_beta=FAKE + 32769), 4),
+    (dict(grad_initial_state=FAKE + 65540), 4),
+])
+def test_chunk_bwd_rejects(lib, kw, code):
+    assert lib.kda_chunk_bwd(ctypes.byref(_bwd(**kw)), FAKE, 1 << 40, None) == code
+
+
+def test_chunk_bwd_workspace(lib):
+    need = lib.kda_chunk_bwd_workspace_size(128, 1, 2, 128, 128, 64)
+    assert need > 2 * 2 * 700 * 1024  # two chunks, two heads, ~0.8 MiB each
+    assert lib.kda_chunk_bwd_workspace_size(128, 1, 2, 96, 96, 64) == 0
+    assert lib.kda_chunk_bwd(ctypes.byref(_bwd()), FAKE, need - 1, None) == 5
+    assert lib.kda_chunk_bwd(ctypes.byref(_bwd()), None, need, None) == 5
+    assert lib.kda_chunk_bwd(ctypes.byref(_bwd()), FAKE + 16, need, None) == 4
