@@ -457,6 +457,80 @@ def run_ours(args, rank, ws, local):
                             "frac": gb / hbm, "bytes": ob, "kernel": "output_gate"}}
         del g_in, w_in, o2
 
+    # ---------------- what the bounded gate buys (section 2.1.1): the same prefill with the unbounded
+    # softplus gate, which has to take the fp32 CUDA-core path (its in-chunk decays are not bounded)
+    gvar = None
+    if not args.no_gate_variant:
+        need_sp = kda.chunk_fwd_workspace_size(T, N, H, D, D, q.dtype, 64, cu_host, gate="softplus")
+        work_sp = torch.empty((need_sp,), dtype=torch.uint8, device=dev)
+        o_sp, fs_sp = torch.empty_like(v), torch.empty_like(fs)
+
+        def step_sp():
+            kda.chunk_fwd(q, k, v, z, beta, b, a, scale=d["scale"], cu_seqlens=d["cu_seqlens"],
+                          cu_seqlens_host=cu_host, final_state=fs_sp, workspace=work_sp, out=o_sp, gate="softplus")
+
+        for _ in range(3):
+            flush.zero_()
+            step_sp()
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        sa, sb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sp_ts = []
+        for _ in range(max(3, min(args.steps, 10))):
+            flush.zero_()
+            sa.record(stream)
+            step_sp()
+            sb.record(stream)
+            sb.synchronize()
+            sp_ts.append(sa.elapsed_time(sb))
+        ms_sp = sum(sp_ts) / len(sp_ts)
+        gvar = {"what": "the same step with g = -exp(A) Softplus(z + b) (unbounded): fp32 CUDA-core path",
+                "softplus_ms_per_step": ms_sp, "lower_bound_ms_per_step": ms,
+                "softplus_tokens_per_s": T / (ms_sp / 1e3), "slowdown": ms_sp / ms,
+                "kernels": kda.chunk_fwd_kernel_count(T, N, H, D, D, q.dtype, cu_host, gate="softplus")}
+        del work_sp, o_sp, fs_sp
+
+    # ---------------- backward pass (training) on the same workload: gradients of q, k, v, z, beta, dt_bias,
+    # A_log from grad_o and grad_final_state (fp32 CUDA cores; the forward is recomputed inside)
+    bwd = None
+    if not args.no_backward:
+        gen = torch.Generator(device=dev).manual_seed(77 + rank)
+        go = torch.randn(o.shape, generator=gen, device=dev).to(o.dtype)
+        gST = torch.randn(fs.shape, generator=gen, device=dev) * 0.1
+        need_b = kda.load_library().kda_chunk_bwd_workspace_size(T, N, H, D, D, 64)
+        work_b = torch.empty((need_b,), dtype=torch.uint8, device=dev)
+
+        def step_b():
+            return kda.chunk_bwd(q, k, v, z, beta, b, a, go, g_min=d["g_min"], scale=d["scale"],
+                                 cu_seqlens=d["cu_seqlens"], grad_final_state=gST, workspace=work_b)
+
+        for _ in range(2):
+            flush.zero_()
+            step_b()
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        nb = 8  # plan, intra, forward chain with checkpoints, reverse chain, value side, key side, gate params
+        evb = [[torch.cuda.Event(enable_timing=True) for _ in range(nb)] for _ in range(max(3, min(args.steps, 10)))]
+        for row in evb:
+            for e in row:
+                e.record(stream)
+        torch.cuda.synchronize()
+        for row in evb:
+            flush.zero_()
+            kda.set_profile_events(row)
+            step_b()
+        kda.set_profile_events([])
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        names_b = ["plan", "intra (fp32 records + L)", "forward chain (entering states)", "reverse chain",
+                   "value side", "key side", "gate parameters"]
+        per_b = [sum(r[i].elapsed_time(r[i + 1]) for r in evb) / len(evb) for i in range(nb - 1)]
+        ms_b = sum(r[0].elapsed_time(r[nb - 1]) for r in evb) / len(evb)
+        bwd = {"what": "kda_chunk_bwd: d q, k, v, z, beta, dt_bias, A_log, S0 from d o and d S_T",
+               "ms_per_step": ms_b, "tokens_per_s": T / (ms_b / 1e3), "vs_forward": ms_b / ms,
+               "kernels_ms": dict(zip(names_b, per_b)), "workspace_bytes": int(need_b)}
+        del go, gST, work_b
+
     # ---------------- decode workload (HBM-bound), 512 in-place steps
     dec = None
     if not args.no_decode:
@@ -559,6 +633,8 @@ def run_ours(args, rank, ws, local):
             "clocks": clocks,
             "decode": dec,
             "epilogue": epi,
+            "gate_variant": gvar,
+            "backward": bwd,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -606,6 +682,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-epilogue", action="store_true")
+    ap.add_argument("--no-gate-variant", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--case", choices=["prefill_small", "prefill_4k", "decode_small"], default=None,
                     help="run a small fixed case for profiler captures instead of the benchmark")
     args = ap.parse_args()

@@ -538,6 +538,7 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
     bw::chunk_rev_chain_kernel<Tio><<<dim3((unsigned)(a->N * H), (unsigned)(dv / bw::TILE)), bw::NT, smem_rev, stream>>>(
         a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, rb, a->scale, (const Tio *)a->grad_o,
         a->grad_final_state, lam, a->grad_initial_state);
+    kda_profile_mark(4, stream);
     st = kda_cuda_status(cudaGetLastError());
     if (st != KDA_OK || Ly.slots == 0 || a->T == 0) return st;
     // 3. value side per (chunk, head, 32 value columns)
@@ -548,6 +549,7 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
                                       smem_val, stream>>>(
         a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, rb, Lbuf, ckpt, lam, a->scale,
         (const Tio *)a->v, (const Tio *)a->beta, (const Tio *)a->grad_o, (Tio *)a->grad_v, part);
+    kda_profile_mark(5, stream);
     st = kda_cuda_status(cudaGetLastError());
     if (st != KDA_OK) return st;
     // 4. key side per (chunk, head)
@@ -557,6 +559,7 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
         a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, rb, Lbuf, part, (const Tio *)a->q,
         (const Tio *)a->k, (const Tio *)a->z, (const Tio *)a->beta, a->dt_bias, a->A_log, a->g_min, a->gate_kind,
         (Tio *)a->grad_q, (Tio *)a->grad_k, (Tio *)a->grad_z, (Tio *)a->grad_beta, gpart);
+    kda_profile_mark(6, stream);
     st = kda_cuda_status(cudaGetLastError());
     if (st != KDA_OK) return st;
     // 5. gate parameters
@@ -564,6 +567,7 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
         bw::bwd_gate_param_kernel<<<(unsigned)H, 128, 0, stream>>>(gpart, Ly.slots, H, dk, a->grad_dt_bias, a->grad_A_log);
         st = kda_cuda_status(cudaGetLastError());
     }
+    kda_profile_mark(7, stream);
     return st;
 }
 

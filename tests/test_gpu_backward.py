@@ -102,3 +102,29 @@ def test_chunk_bwd_optional_outputs_skipped():
     assert set(g) == {"q", "k", "v", "z", "beta"}
     ref = _ref(dict(d, dST=None), "lower_bound")
     assert rel_err(g["q"].cpu().numpy()[:, 0], ref["dq"][:, 0]) <= TOL_F32
+
+
+def test_chunk_bwd_full_prefill_workload_sampled_heads():
+    """The benchmark's workload (T = 4096, H = 32, d = 128, bf16) with the bench's launch: every
+    gradient of two sampled heads (first and last) against exact fp64 gradients of the full sequence."""
+    w = syn.PREFILL_4K
+    dd = syn.make_prefill(w, seed=1)
+    T, H = dd["q"].shape[0], w.H
+    gen = torch.Generator().manual_seed(78)
+    do = torch.randn((T, H, w.d), generator=gen).to(torch.bfloat16)
+    dST = torch.randn((1, H, w.d, w.d), generator=gen) * 0.1
+    g = kda.chunk_bwd(*(dd[n].cuda() for n in ("q", "k", "v", "z", "beta", "dt_bias", "A_log")), do.cuda(),
+                      cu_seqlens=dd["cu_seqlens"].cuda(), grad_final_state=dST.cuda())
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    got = {n: x.float().cpu().numpy() for n, x in g.items()}
+    f = lambda x: x.double().numpy()  # noqa: E731
+    for h in (0, H - 1):
+        r = AG.head_backward(f(dd["q"][:, h]), f(dd["k"][:, h]), f(dd["v"][:, h]), f(dd["z"][:, h]),
+                             f(dd["beta"][:, h]), f(dd["dt_bias"][h]), float(dd["A_log"][h]), None,
+                             f(do[:, h]), f(dST[0, h]))
+        for nm in ("q", "k", "v", "z", "beta"):
+            assert rel_err(got[nm][:, h], r["d" + nm]) <= TOL_BF16, (nm, h)
+        assert rel_err(got["initial_state"][0, h], r["dS0"]) <= TOL_BF16, h
+        assert rel_err(got["dt_bias"][h], r["db"]) <= TOL_BF16, h
+        assert abs(got["A_log"][h] - r["dA_log"]) <= TOL_BF16 * max(1.0, abs(r["dA_log"])), h
