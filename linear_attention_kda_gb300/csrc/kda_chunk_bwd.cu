@@ -16,11 +16,11 @@
 //   chunk_rev_chain_kernel   one CTA per (sequence, head, 32 value columns): Lambda over the chunks
 //                            in reverse (columns of Lambda evolve independently, as those of S),
 //                            storing the Lambda leaving each chunk;
-//   chunk_bwd_value_kernel   one CTA per (chunk, head, 32 value columns): V~, dV~, dX_U (T^T by
-//                            back substitution), dv, and this tile's share of every contraction over
-//                            the value channels (dQ^, dW, dK~, dA, the X_U part of dL, d gamma,
-//                            the X_U part of d beta), written as partial sums;
-//   chunk_bwd_key_kernel     one CTA per (chunk, head): sums the partials, dX_W = T^T dW, dL, then
+//   chunk_bwd_value_kernel_t one CTA of 512 threads per (chunk, head), the value channels 32 at a
+//                            time: V~, dV~, dX_U (T^T by back substitution), dv, and the contractions
+//                            over the value channels (dQ^, dW, dK~, dA, the X_U part of dL, d gamma,
+//                            the X_U part of d beta), accumulated in registers and written once;
+//   chunk_bwd_key_kernel     one CTA per (chunk, head): reads those sums, dX_W = T^T dW, dL, then
 //                            per (row, channel) the pairwise A and L terms, dq, dk, dG; the reverse
 //                            cumulative sum; dz, d beta and per-chunk sums for d dt_bias, d A_log;
 //   bwd_gate_param_kernel    sums the per-chunk gate-parameter gradients per head.
@@ -80,18 +80,21 @@ struct Part {
 };
 
 // ------------------------------------------------------------------ reverse chain over the chunks
-template <typename Tio>
+template <typename Tio, int DK>
 __global__ void __launch_bounds__(NT)
 chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
-                       int H, int dk, int dv, int C, const char *__restrict__ records, size_t rec_bytes,
+                       int H, int dv, const char *__restrict__ records, size_t rec_bytes,
                        float scale, const Tio *__restrict__ d_o, const float *__restrict__ d_final,
                        float *__restrict__ lam_end, float *__restrict__ d_init) {
     extern __shared__ float sm[];
+    constexpr int C = 64, dk = DK;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
     const int j0 = blockIdx.y * TILE;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NWARP = NT / 32;
-    const int PK = dk + 1, PC = C + 1, PS = TILE + 1;
+    constexpr int RW = C / NWARP, CW = DK / NWARP;  // rows of dV~ and of Lambda per warp
+    // 16-byte rows (asynchronous copies, 16-byte broadcast reads); lane-indexed operands are contiguous
+    constexpr int PK = dk + 4, PC = C + 4, PS = TILE + 4;
     float *Ws = sm;               // [C][PK]
     float *Qs = Ws + C * PK;      // [C][PK]
     float *Kt = Qs + C * PK;      // [C][PK]
@@ -102,9 +105,10 @@ chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const i
     float *gam = Lm + dk * PS;    // [dk]
 
     const size_t sbase = ((size_t)n * H + h) * (size_t)dk * dv;
-    for (int e = tid; e < dk * TILE; e += NT) {
-        const int c = e / TILE, j = e % TILE;
-        Lm[c * PS + j] = d_final ? d_final[sbase + (size_t)c * dv + j0 + j] : 0.f;
+    if (d_final) {
+        tile_async(Lm, PS, d_final + sbase + j0, dv, dk, TILE, tid, NT);
+    } else {
+        for (int e = tid; e < dk * TILE; e += NT) Lm[(e / TILE) * PS + e % TILE] = 0.f;
     }
     const int64_t s_tok = cu ? (int64_t)cu[n] : (T / N) * n;
     const int64_t e_tok = cu ? (int64_t)cu[n + 1] : s_tok + T / N;
@@ -113,39 +117,73 @@ chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const i
         const int64_t t0 = s_tok + (int64_t)(cix - c0) * C;
         const int len = (int)min((int64_t)C, e_tok - t0);
         const Rec rec = rec_at(records, rec_bytes, cix, H, h, C, dk, dv);
+        if (tid == 0 && cix > c0)  // the next record in this (reverse) order, into L2 meanwhile
+            prefetch_l2(records + ((size_t)(cix - 1) * H + h) * rec_bytes, (uint32_t)rec_bytes);
+        cp_async_wait_all();
         __syncthreads();  // the previous chunk is done with the buffers; Lambda is final
         float *lg = lam_end + ((size_t)cix * H + h) * (size_t)dk * dv;
         for (int e = tid; e < dk * TILE; e += NT) {
             const int c = e / TILE, j = e % TILE;
             lg[(size_t)c * dv + j0 + j] = Lm[c * PS + j];
         }
-        for (int e = tid; e < C * dk; e += NT) {
-            const int r = e / dk, c = e % dk;
-            Ws[r * PK + c] = rec.W[e];
-            Qs[r * PK + c] = rec.Q[e];
-            Kt[r * PK + c] = rec.K[e];
-        }
-        for (int e = tid; e < C * C; e += NT) As[(e / C) * PC + e % C] = rec.A[e];
+        tile_async(Ws, PK, rec.W, dk, C, dk, tid, NT);
+        tile_async(Qs, PK, rec.Q, dk, C, dk, tid, NT);
+        tile_async(Kt, PK, rec.K, dk, C, dk, tid, NT);
+        tile_async(As, PC, rec.A, C, C, C, tid, NT);
+        tile_async(gam, dk, rec.gam, dk, 1, dk, tid, NT);
+#pragma unroll 8
         for (int e = tid; e < C * TILE; e += NT) {
             const int r = e / TILE, j = e % TILE;
             dOs[r * PS + j] = r < len ? ld(d_o + ((t0 + r) * H + h) * (int64_t)dv + j0 + j) : 0.f;
         }
-        for (int c = tid; c < dk; c += NT) gam[c] = rec.gam[c];
+        cp_async_wait_all();
         __syncthreads();
-        // dV~ = K~ Lambda + scale A^T dO
-        for (int r = warp; r < len; r += NWARP) {
-            float acc = 0.f, accA = 0.f;
-            for (int c = 0; c < dk; ++c) acc += Kt[r * PK + c] * Lm[c * PS + lane];
-            for (int i = r; i < len; ++i) accA += As[i * PC + r] * dOs[i * PS + lane];
-            dVt[r * PS + lane] = acc + scale * accA;
+        // Register-blocked: warp w owns rows [RW w, RW w + RW) of dV~ and rows [CW w, CW w + CW) of
+        // Lambda; lane-indexed operands are read once per reduction index, row operands as 16-byte
+        // broadcasts.
+        const int r0 = warp * RW, cb = warp * CW;
+        {  // dV~ = K~ Lambda + scale A^T dO   (A is zero above its diagonal; rows past len are zero)
+            float acc[RW], acca[RW];
+#pragma unroll
+            for (int i = 0; i < RW; ++i) acc[i] = acca[i] = 0.f;
+            for (int c = 0; c < dk; c += 4) {
+                const float l0 = Lm[c * PS + lane], l1 = Lm[(c + 1) * PS + lane];
+                const float l2 = Lm[(c + 2) * PS + lane], l3 = Lm[(c + 3) * PS + lane];
+#pragma unroll
+                for (int i = 0; i < RW; ++i) {
+                    const float4 k4 = *reinterpret_cast<const float4 *>(&Kt[(r0 + i) * PK + c]);
+                    acc[i] += k4.x * l0 + k4.y * l1 + k4.z * l2 + k4.w * l3;
+                }
+            }
+            for (int i2 = r0; i2 < len; ++i2) {
+                const float d = dOs[i2 * PS + lane];
+                const float4 a0 = *reinterpret_cast<const float4 *>(&As[i2 * PC + r0]);
+                const float4 a1 = *reinterpret_cast<const float4 *>(&As[i2 * PC + r0 + 4]);
+                acca[0] += a0.x * d; acca[1] += a0.y * d; acca[2] += a0.z * d; acca[3] += a0.w * d;
+                acca[4] += a1.x * d; acca[5] += a1.y * d; acca[6] += a1.z * d; acca[7] += a1.w * d;
+            }
+#pragma unroll
+            for (int i = 0; i < RW; ++i) dVt[(r0 + i) * PS + lane] = acc[i] + scale * acca[i];
         }
         __syncthreads();
-        // Lambda <- Diag(gamma) Lambda + scale Q^^T dO - W^T dV~  (each entry reads only itself of Lambda)
-        for (int c = warp; c < dk; c += NWARP) {
-            float acc = gam[c] * Lm[c * PS + lane];
-            for (int r = 0; r < len; ++r)
-                acc += scale * Qs[r * PK + c] * dOs[r * PS + lane] - Ws[r * PK + c] * dVt[r * PS + lane];
-            Lm[c * PS + lane] = acc;
+        {  // Lambda <- Diag(gamma) Lambda + scale Q^^T dO - W^T dV~
+            float lm[CW];
+#pragma unroll
+            for (int i = 0; i < CW; ++i) lm[i] = gam[cb + i] * Lm[(cb + i) * PS + lane];
+            for (int r = 0; r < len; ++r) {
+                const float d = scale * dOs[r * PS + lane], dv2 = dVt[r * PS + lane];
+#pragma unroll
+                for (int j = 0; j < CW; j += 4) {
+                    const float4 q4 = *reinterpret_cast<const float4 *>(&Qs[r * PK + cb + j]);
+                    const float4 w4 = *reinterpret_cast<const float4 *>(&Ws[r * PK + cb + j]);
+                    lm[j] += q4.x * d - w4.x * dv2;
+                    lm[j + 1] += q4.y * d - w4.y * dv2;
+                    lm[j + 2] += q4.z * d - w4.z * dv2;
+                    lm[j + 3] += q4.w * d - w4.w * dv2;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < CW; ++i) Lm[(cb + i) * PS + lane] = lm[i];
         }
     }
     __syncthreads();
@@ -157,29 +195,35 @@ chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const i
     }
 }
 
-// ------------------------------------------------------------------ value side, per (chunk, head, tile)
-template <typename Tio>
-__global__ void __launch_bounds__(NT)
-chunk_bwd_value_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
-                       int H, int dk, int dv, int C, const char *__restrict__ records, size_t rec_bytes,
-                       const float *__restrict__ Lbuf, const float *__restrict__ ckpt,
-                       const float *__restrict__ lam_end, float scale, const Tio *__restrict__ v,
-                       const Tio *__restrict__ beta, const Tio *__restrict__ d_o, Tio *__restrict__ grad_v,
-                       float *__restrict__ part) {
+// ------------------------------------------------------------------ value side, per (chunk, head)
+// 512 threads; the value channels are taken 32 at a time, and every thread keeps its entries of the
+// contractions over them (dQ^, dW, dK~ [C][dk]; dA, dL's X_U part [C][C]) in registers across the
+// tiles, so each (chunk, head) writes them once.
+constexpr int NTV = 512;
+template <int DK>
+__global__ void __launch_bounds__(NTV, 1)
+chunk_bwd_value_kernel_t(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
+                         int H, int dv, const char *__restrict__ records, size_t rec_bytes,
+                         const float *__restrict__ Lbuf, const float *__restrict__ ckpt,
+                         const float *__restrict__ lam_end, float scale, const void *__restrict__ v_,
+                         const void *__restrict__ beta_, const void *__restrict__ d_o_, void *__restrict__ grad_v_,
+                         int bf16_io, float *__restrict__ part) {
+    constexpr int C = 64, dk = DK;
+    constexpr int EK = C * DK / NTV, EC = C * C / NTV;  // entries per thread of the [C][dk] and [C][C] sums
     extern __shared__ float sm[];
     const int64_t slot = blockIdx.x;
-    const int h = blockIdx.y, tile = blockIdx.z, j0 = tile * TILE;
+    const int h = blockIdx.y;
     int n, len;
     int64_t t0;
     if (!locate(chunk_start, cu, T, N, C, slot, n, t0, len)) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int NWARP = NT / 32;
-    const int PK = dk + 1, PC = C + 1, PS = TILE + 1;
+    constexpr int NWARP = NTV / 32;
+    constexpr int PK = dk + 4, PC = C + 4, PS = TILE + 1;
     float *Ws = sm;               // [C][PK]
     float *Kt = Ws + C * PK;      // [C][PK]
     float *As = Kt + C * PK;      // [C][PC]
     float *Ls = As + C * PC;      // [C][PC]
-    float *Ss = Ls + C * PC;      // [dk][PS]
+    float *Ss = Ls + C * PC;      // [dk][PS]  (odd pitch: lanes walk the first index in the sums)
     float *Lm = Ss + dk * PS;     // [dk][PS]
     float *dOs = Lm + dk * PS;    // [C][PS]
     float *Vs = dOs + C * PS;     // [C][PS]  v
@@ -190,103 +234,140 @@ chunk_bwd_value_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const i
 
     const Rec rec = rec_at(records, rec_bytes, slot, H, h, C, dk, dv);
     const size_t mbase = ((size_t)slot * H + h) * (size_t)dk * dv;
-    const float *Lg = Lbuf + ((size_t)slot * H + h) * (size_t)C * C;
-    for (int e = tid; e < C * dk; e += NT) {
-        const int r = e / dk, c = e % dk;
-        Ws[r * PK + c] = rec.W[e];
-        Kt[r * PK + c] = rec.K[e];
-    }
-    for (int e = tid; e < C * C; e += NT) {
-        As[(e / C) * PC + e % C] = rec.A[e];
-        Ls[(e / C) * PC + e % C] = Lg[e];
-    }
-    for (int e = tid; e < dk * TILE; e += NT) {
-        const int c = e / TILE, j = e % TILE;
-        Ss[c * PS + j] = ckpt[mbase + (size_t)c * dv + j0 + j];
-        Lm[c * PS + j] = lam_end[mbase + (size_t)c * dv + j0 + j];
-    }
-    for (int e = tid; e < C * TILE; e += NT) {
-        const int r = e / TILE, j = e % TILE;
-        const bool ok = r < len;
-        const int64_t idx = ((t0 + r) * H + h) * (int64_t)dv + j0 + j;
-        dOs[r * PS + j] = ok ? ld(d_o + idx) : 0.f;
-        Vs[r * PS + j] = ok ? ld(v + idx) : 0.f;
-        Us[r * PS + j] = rec.U[r * dv + j0 + j];
-    }
-    for (int r = tid; r < C; r += NT) bet[r] = r < len ? ld(beta + (t0 + r) * H + h) : 0.f;
-    __syncthreads();
-    // V~ = U - W S and dV~ = K~ Lambda + scale A^T dO (zero past len: those rows of U, W, K~, A vanish)
-    for (int r = warp; r < C; r += NWARP) {
-        float vt = Us[r * PS + lane], dvt = 0.f, da = 0.f;
-        for (int c = 0; c < dk; ++c) {
-            vt -= Ws[r * PK + c] * Ss[c * PS + lane];
-            dvt += Kt[r * PK + c] * Lm[c * PS + lane];
+    tile_async(Ws, PK, rec.W, dk, C, dk, tid, NTV);
+    tile_async(Kt, PK, rec.K, dk, C, dk, tid, NTV);
+    tile_async(As, PC, rec.A, C, C, C, tid, NTV);
+    tile_async(Ls, PC, Lbuf + ((size_t)slot * H + h) * (size_t)C * C, C, C, C, tid, NTV);
+    for (int r = tid; r < C; r += NTV)
+        bet[r] = r < len ? (bf16_io ? ld((const bf16 *)beta_ + (t0 + r) * H + h) : ld((const float *)beta_ + (t0 + r) * H + h)) : 0.f;
+
+    float aq[EK], aw[EK], ak[EK], aa[EC], al[EC], agam = 0.f, abu = 0.f;
+#pragma unroll
+    for (int m = 0; m < EK; ++m) aq[m] = aw[m] = ak[m] = 0.f;
+#pragma unroll
+    for (int m = 0; m < EC; ++m) aa[m] = al[m] = 0.f;
+
+    for (int j0 = 0; j0 < dv; j0 += TILE) {
+        __syncthreads();  // the previous tile is done with the tile buffers
+#pragma unroll 4
+        for (int e = tid; e < dk * TILE; e += NTV) {
+            const int c = e / TILE, j = e % TILE;
+            Ss[c * PS + j] = ckpt[mbase + (size_t)c * dv + j0 + j];
+            Lm[c * PS + j] = lam_end[mbase + (size_t)c * dv + j0 + j];
         }
-        for (int i = r; i < len; ++i) da += As[i * PC + r] * dOs[i * PS + lane];
-        Vt[r * PS + lane] = vt;
-        dVt[r * PS + lane] = dvt + scale * da;
+#pragma unroll 4
+        for (int e = tid; e < C * TILE; e += NTV) {
+            const int r = e / TILE, j = e % TILE;
+            const bool ok = r < len;
+            const int64_t idx = ((t0 + r) * H + h) * (int64_t)dv + j0 + j;
+            if (bf16_io) {
+                dOs[r * PS + j] = ok ? ld((const bf16 *)d_o_ + idx) : 0.f;
+                Vs[r * PS + j] = ok ? ld((const bf16 *)v_ + idx) : 0.f;
+            } else {
+                dOs[r * PS + j] = ok ? ld((const float *)d_o_ + idx) : 0.f;
+                Vs[r * PS + j] = ok ? ld((const float *)v_ + idx) : 0.f;
+            }
+            Us[r * PS + j] = rec.U[r * dv + j0 + j];
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        // V~ = U - W S and dV~ = K~ Lambda + scale A^T dO (zero past len: those rows of U, W, K~, A vanish)
+        for (int r = warp; r < C; r += NWARP) {
+            float vt = Us[r * PS + lane], dvt = 0.f, da = 0.f;
+#pragma unroll 8
+            for (int c = 0; c < dk; ++c) {
+                vt -= Ws[r * PK + c] * Ss[c * PS + lane];
+                dvt += Kt[r * PK + c] * Lm[c * PS + lane];
+            }
+            for (int i = r; i < len; ++i) da += As[i * PC + r] * dOs[i * PS + lane];
+            Vt[r * PS + lane] = vt;
+            dVt[r * PS + lane] = dvt + scale * da;
+        }
+        __syncthreads();
+        // this tile's share of the contractions over value channels
+#pragma unroll
+        for (int m = 0; m < EK; ++m) {
+            const int e = tid + m * NTV, r = e / dk, c = e % dk;
+            float dq = 0.f, dw = 0.f, dkt = 0.f;
+#pragma unroll 8
+            for (int l = 0; l < TILE; ++l) {
+                const float s = Ss[c * PS + l];
+                dq += dOs[r * PS + l] * s;
+                dw -= dVt[r * PS + l] * s;
+                dkt += Vt[r * PS + l] * Lm[c * PS + l];
+            }
+            aq[m] += dq;
+            aw[m] += dw;
+            ak[m] += dkt;
+        }
+#pragma unroll
+        for (int m = 0; m < EC; ++m) {
+            const int e = tid + m * NTV, r = e / C, i = e % C;
+            float da = 0.f;
+            if (i <= r)
+#pragma unroll 8
+                for (int l = 0; l < TILE; ++l) da += dOs[r * PS + l] * Vt[i * PS + l];
+            aa[m] += da;
+        }
+        if (tid < dk) {
+            float dg = 0.f;
+            for (int l = 0; l < TILE; ++l) dg += Ss[tid * PS + l] * Lm[tid * PS + l];
+            agam += dg;
+        }
+        __syncthreads();
+        // dX_U = T^T dV~: back substitution x_r = b_r - sum_{i > r} L_ir x_i, 8 threads per column
+        if (tid < 8 * TILE) {
+            const int col = tid >> 3, part8 = tid & 7;
+            for (int r = C - 2; r >= 0; --r) {
+                float acc = 0.f;
+                for (int i = r + 1 + part8; i < C; i += 8) acc += Ls[i * PC + r] * dVt[i * PS + col];
+                acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                if (part8 == 0) dVt[r * PS + col] -= acc;
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+        // dv = beta dX_U;  X_U parts of d beta and dL
+        for (int e = tid; e < len * TILE; e += NTV) {
+            const int r = e / TILE, j = e % TILE;
+            const int64_t idx = ((t0 + r) * H + h) * (int64_t)dv + j0 + j;
+            if (bf16_io) st((bf16 *)grad_v_ + idx, bet[r] * dVt[r * PS + j]);
+            else st((float *)grad_v_ + idx, bet[r] * dVt[r * PS + j]);
+        }
+        if (tid < C) {
+            float db = 0.f;
+            for (int l = 0; l < TILE; ++l) db += dVt[tid * PS + l] * Vs[tid * PS + l];
+            abu += db;
+        }
+#pragma unroll
+        for (int m = 0; m < EC; ++m) {
+            const int e = tid + m * NTV, r = e / C, i = e % C;
+            float dl = 0.f;
+            if (i < r)
+#pragma unroll 8
+                for (int l = 0; l < TILE; ++l) dl -= dVt[r * PS + l] * Us[i * PS + l];
+            al[m] += dl;
+        }
     }
-    __syncthreads();
-    // this tile's share of the contractions over value channels
     const Part P{C, dk};
-    float *pp = part + (((size_t)slot * H + h) * (size_t)(dv / TILE) + tile) * (size_t)P.size();
-    for (int e = tid; e < C * dk; e += NT) {
-        const int r = e / dk, c = e % dk;
-        float dq = 0.f, dw = 0.f, dkt = 0.f;
-        for (int l = 0; l < TILE; ++l) {
-            const float s = Ss[c * PS + l];
-            dq += dOs[r * PS + l] * s;
-            dw -= dVt[r * PS + l] * s;
-            dkt += Vt[r * PS + l] * Lm[c * PS + l];
-        }
-        pp[P.dQ() + e] = scale * dq;
-        pp[P.dW() + e] = dw;
-        pp[P.dK() + e] = dkt;
+    float *pp = part + ((size_t)slot * H + h) * (size_t)P.size();
+#pragma unroll
+    for (int m = 0; m < EK; ++m) {
+        const int e = tid + m * NTV;
+        pp[P.dQ() + e] = scale * aq[m];
+        pp[P.dW() + e] = aw[m];
+        pp[P.dK() + e] = ak[m];
     }
-    for (int e = tid; e < C * C; e += NT) {
-        const int r = e / C, i = e % C;
-        float da = 0.f;
-        if (i <= r)
-            for (int l = 0; l < TILE; ++l) da += dOs[r * PS + l] * Vt[i * PS + l];
-        pp[P.dA() + e] = scale * da;
+#pragma unroll
+    for (int m = 0; m < EC; ++m) {
+        const int e = tid + m * NTV;
+        pp[P.dA() + e] = scale * aa[m];
+        pp[P.dLu() + e] = al[m];
     }
-    for (int c = tid; c < dk; c += NT) {
-        float dg = 0.f;
-        for (int l = 0; l < TILE; ++l) dg += Ss[c * PS + l] * Lm[c * PS + l];
-        pp[P.dgam() + c] = dg;
-    }
-    __syncthreads();
-    // dX_U = T^T dV~: back substitution x_r = b_r - sum_{i > r} L_ir x_i, 8 threads per column
-    {
-        const int col = tid >> 3, part8 = tid & 7;
-        for (int r = C - 2; r >= 0; --r) {
-            float acc = 0.f;
-            for (int i = r + 1 + part8; i < C; i += 8) acc += Ls[i * PC + r] * dVt[i * PS + col];
-            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            if (part8 == 0) dVt[r * PS + col] -= acc;
-            __syncwarp();
-        }
-    }
-    __syncthreads();
-    // dv = beta dX_U;  X_U parts of d beta and dL
-    for (int e = tid; e < len * TILE; e += NT) {
-        const int r = e / TILE, j = e % TILE;
-        st(grad_v + ((t0 + r) * H + h) * (int64_t)dv + j0 + j, bet[r] * dVt[r * PS + j]);
-    }
-    for (int r = tid; r < C; r += NT) {
-        float db = 0.f;
-        for (int l = 0; l < TILE; ++l) db += dVt[r * PS + l] * Vs[r * PS + l];
-        pp[P.dbu() + r] = db;
-    }
-    for (int e = tid; e < C * C; e += NT) {
-        const int r = e / C, i = e % C;
-        float dl = 0.f;
-        if (i < r)
-            for (int l = 0; l < TILE; ++l) dl -= dVt[r * PS + l] * Us[i * PS + l];
-        pp[P.dLu() + e] = dl;
-    }
+    if (tid < dk) pp[P.dgam() + tid] = agam;
+    if (tid < C) pp[P.dbu() + tid] = abu;
 }
 
 // ------------------------------------------------------------------ key side, per (chunk, head)
@@ -321,10 +402,11 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
     float *red = bet + C;             // [NR][dk] per-row-group channel sums
 
     const Part P{C, dk};
-    const int ntile = dv / TILE;
-    const float *pp = part + ((size_t)slot * H + h) * (size_t)ntile * P.size();
+    constexpr int ntile = 1;  // the value side writes each sum once
+    const float *pp = part + ((size_t)slot * H + h) * (size_t)P.size();
     const float *Lg = Lbuf + ((size_t)slot * H + h) * (size_t)C * C;
     const float eA = A_log ? expf(A_log[h]) : 1.f;
+#pragma unroll 4
     for (int e = tid; e < C * dk; e += NT) {
         const int r = e / dk, c = e % dk;
         const bool ok = r < len;
@@ -336,6 +418,7 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
         for (int t = 0; t < ntile; ++t) dw += pp[(size_t)t * P.size() + P.dW() + e];
         dX[r * PK + c] = dw;
     }
+#pragma unroll 4
     for (int e = tid; e < C * C; e += NT) {
         const int r = e / C, i = e % C;
         float da = 0.f, dl = 0.f;
@@ -506,7 +589,7 @@ bool bwd_layout(int64_t T, int64_t N, int H, int dk, int dv, int C, BwdLayout *L
     L->off_lam = align256(L->off_ckpt + s * dk * dv * sizeof(float));
     L->off_part = align256(L->off_lam + s * dk * dv * sizeof(float));
     const bw::Part P{C, dk};
-    L->off_gate = align256(L->off_part + s * (size_t)(dv / bw::TILE) * P.size() * sizeof(float));
+    L->off_gate = align256(L->off_part + s * (size_t)P.size() * sizeof(float));
     L->total = align256(L->off_gate + s * (size_t)(dk + 1) * sizeof(float));
     return true;
 }
@@ -532,23 +615,40 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
     const size_t rb = Ly.p.record_bytes;
     const int PK = dk + 1, PC = C + 1, PS = bw::TILE + 1;
     // 2. Lambda over the chunks in reverse; d initial_state
-    const size_t smem_rev = sizeof(float) * ((size_t)3 * C * PK + (size_t)C * PC + 2 * (size_t)C * PS +
-                                             (size_t)dk * PS + dk);
-    cudaFuncSetAttribute(bw::chunk_rev_chain_kernel<Tio>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_rev);
-    bw::chunk_rev_chain_kernel<Tio><<<dim3((unsigned)(a->N * H), (unsigned)(dv / bw::TILE)), bw::NT, smem_rev, stream>>>(
-        a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, rb, a->scale, (const Tio *)a->grad_o,
-        a->grad_final_state, lam, a->grad_initial_state);
+    // Ws, Qs, Kt [C][dk + 4]; As [C][C + 4]; dOs, dVt [C][TILE + 4]; Lm [dk][TILE + 4]; gam [dk]
+    const size_t smem_rev = sizeof(float) * ((size_t)3 * C * (dk + 4) + (size_t)C * (C + 4) +
+                                             (2 * (size_t)C + dk) * (bw::TILE + 4) + dk);
+    {
+        auto rev = [&](auto kern) {
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_rev);
+            kern<<<dim3((unsigned)(a->N * H), (unsigned)(dv / bw::TILE)), bw::NT, smem_rev, stream>>>(
+                a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dv, records, rb, a->scale, (const Tio *)a->grad_o,
+                a->grad_final_state, lam, a->grad_initial_state);
+        };
+        if (dk == 128) rev(bw::chunk_rev_chain_kernel<Tio, 128>);
+        else rev(bw::chunk_rev_chain_kernel<Tio, 64>);
+    }
     kda_profile_mark(4, stream);
     st = kda_cuda_status(cudaGetLastError());
     if (st != KDA_OK || Ly.slots == 0 || a->T == 0) return st;
-    // 3. value side per (chunk, head, 32 value columns)
-    const size_t smem_val = sizeof(float) * (2 * (size_t)C * PK + 2 * (size_t)C * PC + 2 * (size_t)dk * PS +
-                                             5 * (size_t)C * PS + C);
-    cudaFuncSetAttribute(bw::chunk_bwd_value_kernel<Tio>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_val);
-    bw::chunk_bwd_value_kernel<Tio><<<dim3((unsigned)Ly.slots, (unsigned)H, (unsigned)(dv / bw::TILE)), bw::NT,
-                                      smem_val, stream>>>(
-        a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, rb, Lbuf, ckpt, lam, a->scale,
-        (const Tio *)a->v, (const Tio *)a->beta, (const Tio *)a->grad_o, (Tio *)a->grad_v, part);
+    // 3. value side per (chunk, head), the value channels 32 at a time
+    {
+        const size_t smem_val = sizeof(float) * (2 * (size_t)C * (dk + 4) + 2 * (size_t)C * (C + 4) +
+                                                 2 * (size_t)dk * (bw::TILE + 1) + 5 * (size_t)C * (bw::TILE + 1) + C);
+        const void *kern = dk == 128 ? (const void *)bw::chunk_bwd_value_kernel_t<128>
+                                     : (const void *)bw::chunk_bwd_value_kernel_t<64>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_val);
+        const dim3 grid((unsigned)Ly.slots, (unsigned)H);
+        const int b16 = a->dtype == KDA_BF16 ? 1 : 0;
+        if (dk == 128)
+            bw::chunk_bwd_value_kernel_t<128><<<grid, bw::NTV, smem_val, stream>>>(
+                a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dv, records, rb, Lbuf, ckpt, lam, a->scale, a->v,
+                a->beta, a->grad_o, a->grad_v, b16, part);
+        else
+            bw::chunk_bwd_value_kernel_t<64><<<grid, bw::NTV, smem_val, stream>>>(
+                a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dv, records, rb, Lbuf, ckpt, lam, a->scale, a->v,
+                a->beta, a->grad_o, a->grad_v, b16, part);
+    }
     kda_profile_mark(5, stream);
     st = kda_cuda_status(cudaGetLastError());
     if (st != KDA_OK) return st;

@@ -164,19 +164,23 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
     for (int e = tid; e < C * dv; e += SIMT_THREADS) rec.U[e] = Vs[(e / dv) * PV + e % dv];
 }
 
-template <typename Tio>
+template <typename Tio, int DK>
 __global__ void __launch_bounds__(SIMT_THREADS)
 chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
-                        const int32_t *__restrict__ chunk_start, int H, int dk, int dv, int C,
+                        const int32_t *__restrict__ chunk_start, int H, int dv, int C_,
                         const char *__restrict__ records, size_t rec_bytes, float scale,
                         const float *initial_state, float *final_state, Tio *__restrict__ o,
                         float *__restrict__ ckpt) {
     extern __shared__ float sm[];
+    constexpr int C = 64, dk = DK;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
     const int j0 = blockIdx.y * SLICE;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NWARP = SIMT_THREADS / 32;
-    const int PK = dk + 1, PC = C + 1, PS = SLICE + 1;
+    constexpr int RW = C / NWARP, CW = DK / NWARP;  // rows of V~ / O and rows of S per warp
+    // row pitches padded to 16 bytes (tiles arrive by 16-byte asynchronous copies, row operands are
+    // read as 16-byte broadcasts); the lane-indexed operands are lane-contiguous: no bank conflicts
+    constexpr int PK = dk + 4, PC = C + 4, PS = SLICE + 4;
     float *Ws = sm;               // [C][PK]
     float *Qs = Ws + C * PK;      // [C][PK]
     float *Kt = Qs + C * PK;      // [C][PK]
@@ -187,9 +191,10 @@ chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
     float *gam = Ss + dk * PS;    // [dk]
 
     const size_t sbase = ((size_t)n * H + h) * (size_t)dk * dv;
-    for (int e = tid; e < dk * SLICE; e += SIMT_THREADS) {
-        const int c = e / SLICE, j = e % SLICE;
-        Ss[c * PS + j] = initial_state ? initial_state[sbase + (size_t)c * dv + j0 + j] : 0.f;
+    if (initial_state) {
+        tile_async(Ss, PS, initial_state + sbase + j0, dv, dk, SLICE, tid, SIMT_THREADS);
+    } else {
+        for (int e = tid; e < dk * SLICE; e += SIMT_THREADS) Ss[(e / SLICE) * PS + e % SLICE] = 0.f;
     }
     const int64_t s_tok = cu ? (int64_t)cu[n] : (T / N) * n;
     const int64_t e_tok = cu ? (int64_t)cu[n + 1] : s_tok + T / N;
@@ -198,7 +203,10 @@ chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
         const int64_t t0 = s_tok + (int64_t)(cix - c0) * C;
         const int len = (int)min((int64_t)C, e_tok - t0);
         RecordView rec = record_view((char *)records, rec_bytes, cix, H, h, C, dk, dv);
-        __syncthreads();  // previous chunk done with the buffers
+        if (tid == 0 && cix + 1 < c1)  // the next chunk's record, into L2 while this one runs
+            prefetch_l2(records + ((size_t)(cix + 1) * H + h) * rec_bytes, (uint32_t)rec_bytes);
+        cp_async_wait_all();
+        __syncthreads();  // previous chunk done with the buffers (and the entering state has landed)
         if (ckpt) {  // the state entering this chunk, for the backward pass
             float *cg = ckpt + ((size_t)cix * H + h) * (size_t)dk * dv;
             for (int e = tid; e < dk * SLICE; e += SIMT_THREADS) {
@@ -206,43 +214,75 @@ chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
                 cg[(size_t)c * dv + j0 + j] = Ss[c * PS + j];
             }
         }
-        for (int e = tid; e < C * dk; e += SIMT_THREADS) {
-            const int r = e / dk, c = e % dk;
-            Ws[r * PK + c] = rec.W[e];
-            Qs[r * PK + c] = rec.Q[e];
-            Kt[r * PK + c] = rec.K[e];
-        }
-        for (int e = tid; e < C * C; e += SIMT_THREADS) As[(e / C) * PC + e % C] = rec.A[e];
-        for (int e = tid; e < C * SLICE; e += SIMT_THREADS) {
-            const int r = e / SLICE, j = e % SLICE;
-            Us[r * PS + j] = rec.U[r * dv + j0 + j];
-        }
-        for (int c = tid; c < dk; c += SIMT_THREADS) gam[c] = rec.gam[c];
+        tile_async(Ws, PK, rec.W, dk, C, dk, tid, SIMT_THREADS);
+        tile_async(Qs, PK, rec.Q, dk, C, dk, tid, SIMT_THREADS);
+        tile_async(Kt, PK, rec.K, dk, C, dk, tid, SIMT_THREADS);
+        tile_async(As, PC, rec.A, C, C, C, tid, SIMT_THREADS);
+        tile_async(Us, PS, rec.U + j0, dv, C, SLICE, tid, SIMT_THREADS);
+        tile_async(gam, dk, rec.gam, dk, 1, dk, tid, SIMT_THREADS);
+        cp_async_wait_all();
         __syncthreads();
-        // V~ = U - W S
-        for (int r = warp; r < C; r += NWARP) {
-            float acc = Us[r * PS + lane];
-            for (int c = 0; c < dk; ++c) acc -= Ws[r * PK + c] * Ss[c * PS + lane];
-            Vt[r * PS + lane] = acc;
+        // Register-blocked products: warp w owns rows [RW w, RW w + RW) of V~ and O and rows
+        // [CW w, CW w + CW) of S; a lane-indexed operand is read once per reduction index for all
+        // of the warp's rows, row operands four at a time as 16-byte broadcasts.
+        const int r0 = warp * RW, cb = warp * CW;
+        {  // V~ = U - W S and the Q^ S part of O
+            float vt[RW], oq[RW];
+#pragma unroll
+            for (int i = 0; i < RW; ++i) {
+                vt[i] = Us[(r0 + i) * PS + lane];
+                oq[i] = 0.f;
+            }
+            for (int c = 0; c < dk; c += 4) {
+                const float s0 = Ss[c * PS + lane], s1 = Ss[(c + 1) * PS + lane];
+                const float s2 = Ss[(c + 2) * PS + lane], s3 = Ss[(c + 3) * PS + lane];
+#pragma unroll
+                for (int i = 0; i < RW; ++i) {
+                    const float4 w = *reinterpret_cast<const float4 *>(&Ws[(r0 + i) * PK + c]);
+                    vt[i] -= w.x * s0 + w.y * s1 + w.z * s2 + w.w * s3;
+                    if (o) {
+                        const float4 q4 = *reinterpret_cast<const float4 *>(&Qs[(r0 + i) * PK + c]);
+                        oq[i] += q4.x * s0 + q4.y * s1 + q4.z * s2 + q4.w * s3;
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < RW; ++i) Vt[(r0 + i) * PS + lane] = vt[i];
+            __syncthreads();
+            if (o) {  // O = scale (Q^ S + A V~); A is zero above its diagonal
+                for (int i0 = 0; i0 < r0 + RW; i0 += 4) {
+                    const float v0 = Vt[i0 * PS + lane], v1 = Vt[(i0 + 1) * PS + lane];
+                    const float v2 = Vt[(i0 + 2) * PS + lane], v3 = Vt[(i0 + 3) * PS + lane];
+#pragma unroll
+                    for (int i = 0; i < RW; ++i) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(&As[(r0 + i) * PC + i0]);
+                        oq[i] += a4.x * v0 + a4.y * v1 + a4.z * v2 + a4.w * v3;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < RW; ++i)
+                    if (r0 + i < len) st(o + ((t0 + r0 + i) * H + h) * (int64_t)dv + j0 + lane, scale * oq[i]);
+            }
         }
-        __syncthreads();
-        // O = scale (Q^ S + A V~)
-        for (int r = warp; o && r < len; r += NWARP) {
-            float acc = 0.f;
-            for (int c = 0; c < dk; ++c) acc += Qs[r * PK + c] * Ss[c * PS + lane];
-            for (int i = 0; i <= r; ++i) acc += As[r * PC + i] * Vt[i * PS + lane];
-            st(o + ((t0 + r) * H + h) * (int64_t)dv + j0 + lane, scale * acc);
+        __syncthreads();  // every read of S in this chunk is done
+        {  // S <- Diag(gamma^C) S + K~^T V~
+            float sn[CW];
+#pragma unroll
+            for (int i = 0; i < CW; ++i) sn[i] = gam[cb + i] * Ss[(cb + i) * PS + lane];
+            for (int r = 0; r < len; ++r) {
+                const float v = Vt[r * PS + lane];
+#pragma unroll
+                for (int j = 0; j < CW; j += 4) {
+                    const float4 k4 = *reinterpret_cast<const float4 *>(&Kt[r * PK + cb + j]);
+                    sn[j] += k4.x * v;
+                    sn[j + 1] += k4.y * v;
+                    sn[j + 2] += k4.z * v;
+                    sn[j + 3] += k4.w * v;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < CW; ++i) Ss[(cb + i) * PS + lane] = sn[i];
         }
-        // S <- Diag(gamma^C) S + K~^T V~   (reads S only in its own column)
-        for (int c = warp; c < dk; c += NWARP) {
-            float acc = gam[c] * Ss[c * PS + lane];
-            for (int r = 0; r < len; ++r) acc += Kt[r * PK + c] * Vt[r * PS + lane];
-            // Other warps may still read S in the output pass: stage the new state in
-            // W's buffer (W is no longer read in this chunk) and copy after the barrier.
-            Ws[c * PS + lane] = acc;  // dk * PS <= C * PK floats
-        }
-        __syncthreads();
-        for (int c = warp; c < dk; c += NWARP) Ss[c * PS + lane] = Ws[c * PS + lane];
     }
     __syncthreads();
     if (final_state) {
@@ -273,8 +313,8 @@ static kda_status_t launch_simt(const kda_chunk_args *a, const kda_chunk_plan &p
     char *records = (char *)ws + p.off_records;
     const size_t smem_intra =
         sizeof(float) * ((size_t)3 * C * (dk + 1) + (size_t)C * (dv + 1) + 2 * (size_t)C * (C + 1) + C);
-    const size_t smem_chain = sizeof(float) * ((size_t)3 * C * (dk + 1) + (size_t)C * (C + 1) +
-                                               2 * (size_t)C * (SLICE + 1) + (size_t)dk * (SLICE + 1) + dk);
+    const size_t smem_chain = sizeof(float) * ((size_t)3 * C * (dk + 4) + (size_t)C * (C + 4) +
+                                               2 * (size_t)C * (SLICE + 4) + (size_t)dk * (SLICE + 4) + dk);
     const bool b16 = a->dtype == KDA_BF16;
     if (p.max_chunks > 0 && a->T > 0) {
         dim3 grid((unsigned)p.max_chunks, (unsigned)H);
@@ -298,16 +338,18 @@ static kda_status_t launch_simt(const kda_chunk_args *a, const kda_chunk_plan &p
     }
     kda_profile_mark(2, stream);
     dim3 grid2((unsigned)(a->N * H), (unsigned)(dv / SLICE));
+    auto chain = [&](auto kern, auto *out) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_chain);
+        kern<<<grid2, SIMT_THREADS, smem_chain, stream>>>(a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dv, C,
+                                                          records, p.record_bytes, a->scale, a->initial_state,
+                                                          a->final_state, out, ckpt);
+    };
     if (b16) {
-        cudaFuncSetAttribute(chunk_chain_simt_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_chain);
-        chunk_chain_simt_kernel<bf16><<<grid2, SIMT_THREADS, smem_chain, stream>>>(
-            a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, p.record_bytes,
-            a->scale, a->initial_state, a->final_state, (bf16 *)a->o, ckpt);
+        if (dk == 128) chain(chunk_chain_simt_kernel<bf16, 128>, (bf16 *)a->o);
+        else chain(chunk_chain_simt_kernel<bf16, 64>, (bf16 *)a->o);
     } else {
-        cudaFuncSetAttribute(chunk_chain_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_chain);
-        chunk_chain_simt_kernel<float><<<grid2, SIMT_THREADS, smem_chain, stream>>>(
-            a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, p.record_bytes,
-            a->scale, a->initial_state, a->final_state, (float *)a->o, ckpt);
+        if (dk == 128) chain(chunk_chain_simt_kernel<float, 128>, (float *)a->o);
+        else chain(chunk_chain_simt_kernel<float, 64>, (float *)a->o);
     }
     kda_profile_mark(3, stream);
     return kda_cuda_status(cudaGetLastError());

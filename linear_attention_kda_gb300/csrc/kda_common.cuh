@@ -36,6 +36,30 @@ __device__ __forceinline__ float gate_log(int kind, float z, float b, float expA
     return gate_logdecay(z, b, expA, g_min);
 }
 
+// 16-byte asynchronous copy global -> shared memory (cached in L2 only): many can be in flight per
+// thread without holding registers; cp_async_wait_all() waits for this thread's copies.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// rows x cols fp32 block from global (row pitch gp floats) to shared memory (row pitch sp floats) by
+// 16-byte copies spread over nt threads; cols, gp, sp multiples of 4 and both bases 16-byte aligned
+__device__ __forceinline__ void tile_async(float *s, int sp, const float *g, int64_t gp, int rows, int cols,
+                                           int tid, int nt) {
+    const int q4 = cols >> 2;
+    for (int e = tid; e < rows * q4; e += nt) {
+        const int r = e / q4, c = (e - r * q4) << 2;
+        cp_async16(s + r * sp + c, g + r * gp + c);
+    }
+}
+
+// Asks L2 to fetch [p, p + bytes) ahead of use (16-byte aligned address, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
 // First device-detected error wins; later ones are dropped.
 __device__ __forceinline__ void set_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
