@@ -20,7 +20,8 @@
 //                            time: V~, dV~, dX_U (T^T by back substitution), dv, and the contractions
 //                            over the value channels (dQ^, dW, dK~, dA, the X_U part of dL, d gamma,
 //                            the X_U part of d beta), accumulated in registers and written once;
-//   chunk_bwd_key_kernel     one CTA per (chunk, head): reads those sums, dX_W = T^T dW, dL, then
+//                            It also solves dX_W = T^T dW and adds dL's X_W part at the end;
+//   chunk_bwd_key_kernel     one CTA per (chunk, head): reads those sums, then
 //                            per (row, channel) the pairwise A and L terms, dq, dk, dG; the reverse
 //                            cumulative sum; dz, d beta and per-chunk sums for d dt_bias, d A_log;
 //   bwd_gate_param_kernel    sums the per-chunk gate-parameter gradients per head.
@@ -196,9 +197,12 @@ chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const i
 }
 
 // ------------------------------------------------------------------ value side, per (chunk, head)
-// 512 threads; the value channels are taken 32 at a time, and every thread keeps its entries of the
-// contractions over them (dQ^, dW, dK~ [C][dk]; dA, dL's X_U part [C][C]) in registers across the
-// tiles, so each (chunk, head) writes them once.
+// 512 threads; the value channels are taken 32 at a time.  Thread t owns rows 4 (t / 32) + [0, 4)
+// and columns t % 32 + 32 j of the contractions over the value channels (dQ^, dW, dK~ [C][dk]; dA
+// and dL [C][C]) and keeps them in registers across the tiles: per reduction index it reads four
+// row values (broadcasts) and its column values (lane-strided rows at an odd pitch: no bank
+// conflicts).  After the last tile it solves dX_W = T^T dW and adds dL's X_W part, -dX_W W^T,
+// while W and L are still in shared memory, and writes every sum once.
 constexpr int NTV = 512;
 template <int DK>
 __global__ void __launch_bounds__(NTV, 1)
@@ -209,7 +213,8 @@ chunk_bwd_value_kernel_t(int64_t T, int N, const int32_t *__restrict__ cu, const
                          const void *__restrict__ beta_, const void *__restrict__ d_o_, void *__restrict__ grad_v_,
                          int bf16_io, float *__restrict__ part) {
     constexpr int C = 64, dk = DK;
-    constexpr int EK = C * DK / NTV, EC = C * C / NTV;  // entries per thread of the [C][dk] and [C][C] sums
+    constexpr int CB = DK / 32, IB = C / 32;  // columns per thread of the [C][dk] and [C][C] sums
+    constexpr int NWARP = NTV / 32, RW = C / NWARP;  // rows of V~ / dV~ per warp (4)
     extern __shared__ float sm[];
     const int64_t slot = blockIdx.x;
     const int h = blockIdx.y;
@@ -217,13 +222,12 @@ chunk_bwd_value_kernel_t(int64_t T, int N, const int32_t *__restrict__ cu, const
     int64_t t0;
     if (!locate(chunk_start, cu, T, N, C, slot, n, t0, len)) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int NWARP = NTV / 32;
-    constexpr int PK = dk + 4, PC = C + 4, PS = TILE + 1;
+    constexpr int PK = dk + 4, PC = C + 4, PS = TILE + 1, PW = dk + 1;
     float *Ws = sm;               // [C][PK]
     float *Kt = Ws + C * PK;      // [C][PK]
     float *As = Kt + C * PK;      // [C][PC]
     float *Ls = As + C * PC;      // [C][PC]
-    float *Ss = Ls + C * PC;      // [dk][PS]  (odd pitch: lanes walk the first index in the sums)
+    float *Ss = Ls + C * PC;      // [dk][PS]
     float *Lm = Ss + dk * PS;     // [dk][PS]
     float *dOs = Lm + dk * PS;    // [C][PS]
     float *Vs = dOs + C * PS;     // [C][PS]  v
@@ -231,6 +235,7 @@ chunk_bwd_value_kernel_t(int64_t T, int N, const int32_t *__restrict__ cu, const
     float *Vt = Us + C * PS;      // [C][PS]  V~
     float *dVt = Vt + C * PS;     // [C][PS]  dV~, then dX_U
     float *bet = dVt + C * PS;    // [C]
+    float *dWs = Ss;              // [C][PW] after the tiles: dW, then dX_W (reuses the tile buffers)
 
     const Rec rec = rec_at(records, rec_bytes, slot, H, h, C, dk, dv);
     const size_t mbase = ((size_t)slot * H + h) * (size_t)dk * dv;
@@ -241,11 +246,15 @@ chunk_bwd_value_kernel_t(int64_t T, int N, const int32_t *__restrict__ cu, const
     for (int r = tid; r < C; r += NTV)
         bet[r] = r < len ? (bf16_io ? ld((const bf16 *)beta_ + (t0 + r) * H + h) : ld((const float *)beta_ + (t0 + r) * H + h)) : 0.f;
 
-    float aq[EK], aw[EK], ak[EK], aa[EC], al[EC], agam = 0.f, abu = 0.f;
+    const int rb = (tid >> 5) * 4;  // this thread's rows of the sums; its columns are lane + 32 j
+    float aq[4][CB], aw[4][CB], ak[4][CB], aa[4][IB], al[4][IB], agam = 0.f, abu = 0.f;
 #pragma unroll
-    for (int m = 0; m < EK; ++m) aq[m] = aw[m] = ak[m] = 0.f;
+    for (int i = 0; i < 4; ++i) {
 #pragma unroll
-    for (int m = 0; m < EC; ++m) aa[m] = al[m] = 0.f;
+        for (int j = 0; j < CB; ++j) aq[i][j] = aw[i][j] = ak[i][j] = 0.f;
+#pragma unroll
+        for (int j = 0; j < IB; ++j) aa[i][j] = al[i][j] = 0.f;
+    }
 
     for (int j0 = 0; j0 < dv; j0 += TILE) {
         __syncthreads();  // the previous tile is done with the tile buffers
@@ -271,43 +280,67 @@ chunk_bwd_value_kernel_t(int64_t T, int N, const int32_t *__restrict__ cu, const
         }
         cp_async_wait_all();
         __syncthreads();
-        // V~ = U - W S and dV~ = K~ Lambda + scale A^T dO (zero past len: those rows of U, W, K~, A vanish)
-        for (int r = warp; r < C; r += NWARP) {
-            float vt = Us[r * PS + lane], dvt = 0.f, da = 0.f;
-#pragma unroll 8
-            for (int c = 0; c < dk; ++c) {
-                vt -= Ws[r * PK + c] * Ss[c * PS + lane];
-                dvt += Kt[r * PK + c] * Lm[c * PS + lane];
+        {  // V~ = U - W S and dV~ = K~ Lambda + scale A^T dO, rows RW w + [0, RW) at column lane
+            const int r0 = warp * RW;
+            float vt[RW], dvt[RW], da[RW];
+#pragma unroll
+            for (int i = 0; i < RW; ++i) {
+                vt[i] = Us[(r0 + i) * PS + lane];
+                dvt[i] = da[i] = 0.f;
             }
-            for (int i = r; i < len; ++i) da += As[i * PC + r] * dOs[i * PS + lane];
-            Vt[r * PS + lane] = vt;
-            dVt[r * PS + lane] = dvt + scale * da;
+            for (int c = 0; c < dk; c += 4) {
+                const float s0 = Ss[c * PS + lane], s1 = Ss[(c + 1) * PS + lane];
+                const float s2 = Ss[(c + 2) * PS + lane], s3 = Ss[(c + 3) * PS + lane];
+                const float l0 = Lm[c * PS + lane], l1 = Lm[(c + 1) * PS + lane];
+                const float l2 = Lm[(c + 2) * PS + lane], l3 = Lm[(c + 3) * PS + lane];
+#pragma unroll
+                for (int i = 0; i < RW; ++i) {
+                    const float4 w = *reinterpret_cast<const float4 *>(&Ws[(r0 + i) * PK + c]);
+                    const float4 k4 = *reinterpret_cast<const float4 *>(&Kt[(r0 + i) * PK + c]);
+                    vt[i] -= w.x * s0 + w.y * s1 + w.z * s2 + w.w * s3;
+                    dvt[i] += k4.x * l0 + k4.y * l1 + k4.z * l2 + k4.w * l3;
+                }
+            }
+            for (int i2 = r0; i2 < len; ++i2) {  // A is zero above its diagonal
+                const float d = dOs[i2 * PS + lane];
+                const float4 a4 = *reinterpret_cast<const float4 *>(&As[i2 * PC + r0]);
+                da[0] += a4.x * d; da[1] += a4.y * d; da[2] += a4.z * d; da[3] += a4.w * d;
+            }
+#pragma unroll
+            for (int i = 0; i < RW; ++i) {
+                Vt[(r0 + i) * PS + lane] = vt[i];
+                dVt[(r0 + i) * PS + lane] = dvt[i] + scale * da[i];
+            }
         }
         __syncthreads();
         // this tile's share of the contractions over value channels
+#pragma unroll 4
+        for (int l = 0; l < TILE; ++l) {
+            float xo[4], xd[4], xv[4], ys[CB], yl[CB], yv[IB];
 #pragma unroll
-        for (int m = 0; m < EK; ++m) {
-            const int e = tid + m * NTV, r = e / dk, c = e % dk;
-            float dq = 0.f, dw = 0.f, dkt = 0.f;
-#pragma unroll 8
-            for (int l = 0; l < TILE; ++l) {
-                const float s = Ss[c * PS + l];
-                dq += dOs[r * PS + l] * s;
-                dw -= dVt[r * PS + l] * s;
-                dkt += Vt[r * PS + l] * Lm[c * PS + l];
+            for (int i = 0; i < 4; ++i) {
+                xo[i] = dOs[(rb + i) * PS + l];
+                xd[i] = dVt[(rb + i) * PS + l];
+                xv[i] = Vt[(rb + i) * PS + l];
             }
-            aq[m] += dq;
-            aw[m] += dw;
-            ak[m] += dkt;
-        }
 #pragma unroll
-        for (int m = 0; m < EC; ++m) {
-            const int e = tid + m * NTV, r = e / C, i = e % C;
-            float da = 0.f;
-            if (i <= r)
-#pragma unroll 8
-                for (int l = 0; l < TILE; ++l) da += dOs[r * PS + l] * Vt[i * PS + l];
-            aa[m] += da;
+            for (int j = 0; j < CB; ++j) {
+                ys[j] = Ss[(lane + 32 * j) * PS + l];
+                yl[j] = Lm[(lane + 32 * j) * PS + l];
+            }
+#pragma unroll
+            for (int j = 0; j < IB; ++j) yv[j] = Vt[(lane + 32 * j) * PS + l];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int j = 0; j < CB; ++j) {
+                    aq[i][j] += xo[i] * ys[j];
+                    aw[i][j] -= xd[i] * ys[j];
+                    ak[i][j] += xv[i] * yl[j];
+                }
+#pragma unroll
+                for (int j = 0; j < IB; ++j) aa[i][j] += xo[i] * yv[j];
+            }
         }
         if (tid < dk) {
             float dg = 0.f;
@@ -341,30 +374,70 @@ chunk_bwd_value_kernel_t(int64_t T, int N, const int32_t *__restrict__ cu, const
             for (int l = 0; l < TILE; ++l) db += dVt[tid * PS + l] * Vs[tid * PS + l];
             abu += db;
         }
+#pragma unroll 4
+        for (int l = 0; l < TILE; ++l) {
+            float xu[4], yu[IB];
 #pragma unroll
-        for (int m = 0; m < EC; ++m) {
-            const int e = tid + m * NTV, r = e / C, i = e % C;
-            float dl = 0.f;
-            if (i < r)
-#pragma unroll 8
-                for (int l = 0; l < TILE; ++l) dl -= dVt[r * PS + l] * Us[i * PS + l];
-            al[m] += dl;
+            for (int i = 0; i < 4; ++i) xu[i] = dVt[(rb + i) * PS + l];
+#pragma unroll
+            for (int j = 0; j < IB; ++j) yu[j] = Us[(lane + 32 * j) * PS + l];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < IB; ++j) al[i][j] -= xu[i] * yu[j];
+        }
+    }
+    // dX_W = T^T dW (columns back-substituted, NTV / dk threads per column), then dL -= dX_W W^T
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < CB; ++j) dWs[(rb + i) * PW + lane + 32 * j] = aw[i][j];
+    __syncthreads();
+    {
+        constexpr int TPC = NTV / DK;
+        const int col = tid / TPC, sub = tid % TPC;
+        for (int r = C - 2; r >= 0; --r) {
+            float acc = 0.f;
+            for (int i = r + 1 + sub; i < C; i += TPC) acc += Ls[i * PC + r] * dWs[i * PW + col];
+#pragma unroll
+            for (int off = TPC >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (sub == 0) dWs[r * PW + col] -= acc;
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    for (int c = 0; c < dk; c += 4) {  // rows of dX_W broadcast, rows of W lane-strided (16-byte reads)
+        float x[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[i][u] = dWs[(rb + i) * PW + c + u];
+#pragma unroll
+        for (int j = 0; j < IB; ++j) {
+            const float4 w = *reinterpret_cast<const float4 *>(&Ws[(lane + 32 * j) * PK + c]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) al[i][j] -= x[i][0] * w.x + x[i][1] * w.y + x[i][2] * w.z + x[i][3] * w.w;
         }
     }
     const Part P{C, dk};
     float *pp = part + ((size_t)slot * H + h) * (size_t)P.size();
 #pragma unroll
-    for (int m = 0; m < EK; ++m) {
-        const int e = tid + m * NTV;
-        pp[P.dQ() + e] = scale * aq[m];
-        pp[P.dW() + e] = aw[m];
-        pp[P.dK() + e] = ak[m];
-    }
+    for (int i = 0; i < 4; ++i) {
+        const int r = rb + i;
 #pragma unroll
-    for (int m = 0; m < EC; ++m) {
-        const int e = tid + m * NTV;
-        pp[P.dA() + e] = scale * aa[m];
-        pp[P.dLu() + e] = al[m];
+        for (int j = 0; j < CB; ++j) {
+            const int e = r * dk + lane + 32 * j;
+            pp[P.dQ() + e] = scale * aq[i][j];
+            pp[P.dW() + e] = dWs[r * PW + lane + 32 * j];  // dX_W
+            pp[P.dK() + e] = ak[i][j];
+        }
+#pragma unroll
+        for (int j = 0; j < IB; ++j) {
+            const int c2 = lane + 32 * j, e = r * C + c2;
+            pp[P.dA() + e] = c2 <= r ? scale * aa[i][j] : 0.f;
+            pp[P.dLu() + e] = c2 < r ? al[i][j] : 0.f;  // the whole dL
+        }
     }
     if (tid < dk) pp[P.dgam() + tid] = agam;
     if (tid < C) pp[P.dbu() + tid] = abu;
@@ -376,7 +449,7 @@ template <typename Tio>
 __global__ void __launch_bounds__(NT)
 chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
                      int H, int dk, int dv, int C, const char *__restrict__ records, size_t rec_bytes,
-                     const float *__restrict__ Lbuf, const float *__restrict__ part, const Tio *__restrict__ q,
+                     const float *__restrict__ part, const Tio *__restrict__ q,
                      const Tio *__restrict__ k, const Tio *__restrict__ z, const Tio *__restrict__ beta,
                      const float *__restrict__ bias, const float *__restrict__ A_log, float g_min, int kind,
                      Tio *__restrict__ grad_q, Tio *__restrict__ grad_k, Tio *__restrict__ grad_z,
@@ -393,18 +466,15 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
     float *qs = sm;                   // [C][PK]
     float *ks = qs + C * PK;          // [C][PK]
     float *Gs = ks + C * PK;          // [C][PK]  in-chunk cumulative log-decay
-    float *dX = Gs + C * PK;          // [C][PK]  dW -> dX_W -> per-element d beta terms
+    float *dX = Gs + C * PK;          // [C][PK]  dX_W, then the per-element d beta terms
     float *dG = dX + C * PK;          // [C][PK]
-    float *Ls = dG + C * PK;          // [C][PC]
-    float *dLs = Ls + C * PC;         // [C][PC]
+    float *dLs = dG + C * PK;         // [C][PC]
     float *dAs = dLs + C * PC;        // [C][PC]
     float *bet = dAs + C * PC;        // [C]
     float *red = bet + C;             // [NR][dk] per-row-group channel sums
 
     const Part P{C, dk};
-    constexpr int ntile = 1;  // the value side writes each sum once
     const float *pp = part + ((size_t)slot * H + h) * (size_t)P.size();
-    const float *Lg = Lbuf + ((size_t)slot * H + h) * (size_t)C * C;
     const float eA = A_log ? expf(A_log[h]) : 1.f;
 #pragma unroll 4
     for (int e = tid; e < C * dk; e += NT) {
@@ -414,21 +484,13 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
         qs[r * PK + c] = ok ? ld(q + idx) : 0.f;
         ks[r * PK + c] = ok ? ld(k + idx) : 0.f;
         Gs[r * PK + c] = ok ? gate_log(kind, ld(z + idx), bias ? bias[h * dk + c] : 0.f, eA, g_min) : 0.f;
-        float dw = 0.f;
-        for (int t = 0; t < ntile; ++t) dw += pp[(size_t)t * P.size() + P.dW() + e];
-        dX[r * PK + c] = dw;
+        dX[r * PK + c] = pp[P.dW() + e];  // dX_W = T^T dW (solved by the value side)
     }
 #pragma unroll 4
     for (int e = tid; e < C * C; e += NT) {
         const int r = e / C, i = e % C;
-        float da = 0.f, dl = 0.f;
-        for (int t = 0; t < ntile; ++t) {
-            da += pp[(size_t)t * P.size() + P.dA() + e];
-            dl += pp[(size_t)t * P.size() + P.dLu() + e];
-        }
-        dAs[r * PC + i] = da;
-        dLs[r * PC + i] = dl;
-        Ls[r * PC + i] = Lg[e];
+        dAs[r * PC + i] = pp[P.dA() + e];
+        dLs[r * PC + i] = pp[P.dLu() + e];  // the whole dL (strictly lower)
     }
     for (int r = tid; r < C; r += NT) bet[r] = r < len ? ld(beta + (t0 + r) * H + h) : 0.f;
     __syncthreads();
@@ -439,29 +501,6 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
             Gs[r * PK + c] = acc;
         }
     }
-    // dX_W = T^T dW: back substitution, NT / dk threads per column (adjacent lanes)
-    {
-        const int tpc = NT / dk, col = tid / tpc, sub = tid % tpc;
-        for (int r = C - 2; r >= 0; --r) {
-            float acc = 0.f;
-            for (int i = r + 1 + sub; i < C; i += tpc) acc += Ls[i * PC + r] * dX[i * PK + col];
-            for (int off = tpc >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (sub == 0) dX[r * PK + col] -= acc;
-            __syncwarp();
-        }
-    }
-    __syncthreads();
-    // dL = (X_U part) - dX_W W^T, strictly lower
-    {
-        const Rec rec = rec_at(records, rec_bytes, slot, H, h, C, dk, dv);
-        for (int e = tid; e < C * C; e += NT) {
-            const int r = e / C, i = e % C;
-            if (i >= r || r >= len) continue;
-            float acc = 0.f;
-            for (int c = 0; c < dk; ++c) acc += dX[r * PK + c] * rec.W[i * dk + c];
-            dLs[r * PC + i] -= acc;
-        }
-    }
     __syncthreads();
     // per (row, channel): dq, dk, dG and the d beta terms
     const int c = tid % dk, rg = tid / dk;
@@ -470,11 +509,7 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
         const float Gr = Gs[r * PK + c], Gl = Gs[(C - 1) * PK + c];
         const float eG = expf(Gr), eL = expf(Gl - Gr);
         const float qr = qs[r * PK + c], kr = ks[r * PK + c], br = bet[r];
-        float dqh = 0.f, dkt = 0.f;
-        for (int t = 0; t < ntile; ++t) {
-            dqh += pp[(size_t)t * P.size() + P.dQ() + r * dk + c];
-            dkt += pp[(size_t)t * P.size() + P.dK() + r * dk + c];
-        }
+        const float dqh = pp[P.dQ() + r * dk + c], dkt = pp[P.dK() + r * dk + c];
         const float dxw = dX[r * PK + c];
         float ra = 0.f, rl = 0.f;  // sum_{i <= r} dA_ri k_ic E_ric,  sum_{i < r} dL_ri k_ic E_ric
         for (int i = 0; i < r; ++i) {
@@ -506,9 +541,7 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
     float *gp = gate_part + ((size_t)slot * H + h) * (size_t)(dk + 1);
     for (int cc = tid; cc < dk; cc += NT) {
         const Rec rec = rec_at(records, rec_bytes, slot, H, h, C, dk, dv);
-        float dgam = 0.f;
-        for (int t = 0; t < ntile; ++t) dgam += pp[(size_t)t * P.size() + P.dgam() + cc];
-        float run = dgam * rec.gam[cc];
+        float run = pp[P.dgam() + cc] * rec.gam[cc];
         for (int g = 0; g < NR; ++g) run += red[g * dk + cc];
         const float b = bias ? bias[h * dk + cc] : 0.f;
         float db = 0.f, da = 0.f;
@@ -545,7 +578,7 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
     for (int r = tid; r < len; r += NT) {  // d beta: X_W and L terms per channel, plus the X_U part
         float db = 0.f;
         for (int cc = 0; cc < dk; ++cc) db += dX[r * PK + cc];
-        for (int t = 0; t < ntile; ++t) db += pp[(size_t)t * P.size() + P.dbu() + r];
+        db += pp[P.dbu() + r];
         st(grad_beta + (t0 + r) * H + h, db);
     }
 }
@@ -613,7 +646,7 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
     const int32_t *chunk_start = (const int32_t *)(base + Ly.p.off_chunk_start);
     const char *records = base + Ly.p.off_records;
     const size_t rb = Ly.p.record_bytes;
-    const int PK = dk + 1, PC = C + 1, PS = bw::TILE + 1;
+    const int PK = dk + 1, PC = C + 1;
     // 2. Lambda over the chunks in reverse; d initial_state
     // Ws, Qs, Kt [C][dk + 4]; As [C][C + 4]; dOs, dVt [C][TILE + 4]; Lm [dk][TILE + 4]; gam [dk]
     const size_t smem_rev = sizeof(float) * ((size_t)3 * C * (dk + 4) + (size_t)C * (C + 4) +
@@ -653,10 +686,10 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
     st = kda_cuda_status(cudaGetLastError());
     if (st != KDA_OK) return st;
     // 4. key side per (chunk, head)
-    const size_t smem_key = sizeof(float) * (5 * (size_t)C * PK + 3 * (size_t)C * PC + C + (size_t)bw::NT);
+    const size_t smem_key = sizeof(float) * (5 * (size_t)C * PK + 2 * (size_t)C * PC + C + (size_t)bw::NT);
     cudaFuncSetAttribute(bw::chunk_bwd_key_kernel<Tio>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_key);
     bw::chunk_bwd_key_kernel<Tio><<<dim3((unsigned)Ly.slots, (unsigned)H), bw::NT, smem_key, stream>>>(
-        a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, rb, Lbuf, part, (const Tio *)a->q,
+        a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, rb, part, (const Tio *)a->q,
         (const Tio *)a->k, (const Tio *)a->z, (const Tio *)a->beta, a->dt_bias, a->A_log, a->g_min, a->gate_kind,
         (Tio *)a->grad_q, (Tio *)a->grad_k, (Tio *)a->grad_z, (Tio *)a->grad_beta, gpart);
     kda_profile_mark(6, stream);
