@@ -494,11 +494,11 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
     }
     for (int r = tid; r < C; r += NT) bet[r] = r < len ? ld(beta + (t0 + r) * H + h) : 0.f;
     __syncthreads();
-    for (int c = tid; c < dk; c += NT) {  // cumulative log-decay within the chunk (Eq. 3)
+    for (int c = tid; c < dk; c += NT) {  // cumulative log-decay within the chunk (Eq. 3), base 2
         float acc = 0.f;
         for (int r = 0; r < C; ++r) {
             acc += Gs[r * PK + c];
-            Gs[r * PK + c] = acc;
+            Gs[r * PK + c] = acc * 1.4426950408889634f;
         }
     }
     __syncthreads();
@@ -507,20 +507,20 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
     float xk_sum = 0.f;  // sum over this thread's rows of dK~ * K~ (flows to G_last)
     for (int r = rg; r < len; r += NR) {
         const float Gr = Gs[r * PK + c], Gl = Gs[(C - 1) * PK + c];
-        const float eG = expf(Gr), eL = expf(Gl - Gr);
+        const float eG = exp2f(Gr), eL = exp2f(Gl - Gr);
         const float qr = qs[r * PK + c], kr = ks[r * PK + c], br = bet[r];
         const float dqh = pp[P.dQ() + r * dk + c], dkt = pp[P.dK() + r * dk + c];
         const float dxw = dX[r * PK + c];
         float ra = 0.f, rl = 0.f;  // sum_{i <= r} dA_ri k_ic E_ric,  sum_{i < r} dL_ri k_ic E_ric
         for (int i = 0; i < r; ++i) {
-            const float kE = ks[i * PK + c] * expf(Gr - Gs[i * PK + c]);
+            const float kE = ks[i * PK + c] * exp2f(Gr - Gs[i * PK + c]);
             ra += dAs[r * PC + i] * kE;
             rl += dLs[r * PC + i] * kE;
         }
         ra += dAs[r * PC + r] * kr;
         float ca = dAs[r * PC + r] * qr, cl = 0.f;  // sum_{r' >= r} dA_r'r q_r'c E, sum_{r' > r} dL_r'r b_r' k_r'c E
         for (int i = r + 1; i < len; ++i) {
-            const float E = expf(Gs[i * PK + c] - Gr);
+            const float E = exp2f(Gs[i * PK + c] - Gr);
             ca += dAs[i * PC + r] * qs[i * PK + c] * E;
             cl += dLs[i * PC + r] * bet[i] * ks[i * PK + c] * E;
         }

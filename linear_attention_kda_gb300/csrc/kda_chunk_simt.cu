@@ -88,6 +88,7 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
     float *bet = As + C * PC;     // [C]
 
     const float eA = A_log ? expf(A_log[h]) : 1.f;
+#pragma unroll 4
     for (int e = tid; e < C * dk; e += SIMT_THREADS) {
         const int r = e / dk, c = e % dk;
         const bool ok = r < len;
@@ -96,33 +97,48 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
         Qs[r * PK + c] = ok ? ld(q + idx) : 0.f;
         Gs[r * PK + c] = ok ? gate_log(kind, ld(z + idx), bias ? bias[h * dk + c] : 0.f, eA, g_min) : 0.f;
     }
+#pragma unroll 8
     for (int e = tid; e < C * dv; e += SIMT_THREADS) {
         const int r = e / dv, c = e % dv;
         Vs[r * PV + c] = r < len ? ld(v + ((t0 + r) * H + h) * (int64_t)dv + c) : 0.f;
     }
     for (int r = tid; r < C; r += SIMT_THREADS) bet[r] = r < len ? ld(beta + (t0 + r) * H + h) : 0.f;
     __syncthreads();
-    for (int c = tid; c < dk; c += SIMT_THREADS) {  // in-chunk cumulative log-decay (Eq. 3)
+    // in-chunk cumulative log-decay (Eq. 3), kept in base 2 (G log2 e) so that every decay below is
+    // one exp2 of a difference
+    for (int c = tid; c < dk; c += SIMT_THREADS) {
         float acc = 0.f;
         for (int r = 0; r < C; ++r) {
             acc += Gs[r * PK + c];
-            Gs[r * PK + c] = acc;
+            Gs[r * PK + c] = acc * 1.4426950408889634f;
         }
     }
     __syncthreads();
-    for (int p = tid; p < C * C; p += SIMT_THREADS) {
-        const int r = p / C, i = p % C;
-        float sl = 0.f, sa = 0.f;
-        if (i <= r) {
+    // A and L, four key rows i per thread sharing the query row r's values; the exponent is clamped at
+    // 0 only so that the block's entries above the diagonal (discarded) cannot overflow
+    for (int it = tid; it < C * (C / 4); it += SIMT_THREADS) {
+        const int r = it / (C / 4), ib = (it % (C / 4)) * 4;
+        if (ib <= r) {
+            float sl[4] = {0.f, 0.f, 0.f, 0.f}, sa[4] = {0.f, 0.f, 0.f, 0.f};
             for (int c = 0; c < dk; ++c) {
-                const float dec = expf(Gs[r * PK + c] - Gs[i * PK + c]);
-                const float ki = Ks[i * PK + c] * dec;
-                sl += Ks[r * PK + c] * ki;
-                sa += Qs[r * PK + c] * ki;
+                const float Gr = Gs[r * PK + c], kr = Ks[r * PK + c], qr = Qs[r * PK + c];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float ki = Ks[(ib + u) * PK + c] * exp2f(fminf(Gr - Gs[(ib + u) * PK + c], 0.f));
+                    sl[u] += kr * ki;
+                    sa[u] += qr * ki;
+                }
             }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = ib + u;
+                Ls[r * PC + i] = (i < r) ? bet[r] * sl[u] : 0.f;
+                As[r * PC + i] = (i <= r) ? sa[u] : 0.f;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) Ls[r * PC + ib + u] = As[r * PC + ib + u] = 0.f;
         }
-        Ls[r * PC + i] = (i < r) ? bet[r] * sl : 0.f;
-        As[r * PC + i] = (i <= r) ? sa : 0.f;
     }
     __syncthreads();
     RecordView rec = record_view(records, rec_bytes, slot, H, h, C, dk, dv);
@@ -133,16 +149,16 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
     }
     for (int e = tid; e < C * dk; e += SIMT_THREADS) {
         const int r = e / dk, c = e % dk;
-        const float G = Gs[r * PK + c], Gl = Gs[(C - 1) * PK + c];  // G is flat past len
-        rec.Q[e] = Qs[r * PK + c] * expf(G);
-        rec.K[e] = Ks[r * PK + c] * expf(Gl - G);
-        if (r == 0) rec.gam[c] = expf(Gl);
+        const float G = Gs[r * PK + c], Gl = Gs[(C - 1) * PK + c];  // base 2; flat past len
+        rec.Q[e] = Qs[r * PK + c] * exp2f(G);
+        rec.K[e] = Ks[r * PK + c] * exp2f(Gl - G);
+        if (r == 0) rec.gam[c] = exp2f(Gl);
     }
     __syncthreads();
     // right-hand sides of the UT transform, in place
     for (int e = tid; e < C * dk; e += SIMT_THREADS) {
         const int r = e / dk, c = e % dk;
-        Ks[r * PK + c] = bet[r] * Ks[r * PK + c] * expf(Gs[r * PK + c]);
+        Ks[r * PK + c] = bet[r] * Ks[r * PK + c] * exp2f(Gs[r * PK + c]);
     }
     for (int e = tid; e < C * dv; e += SIMT_THREADS) {
         const int r = e / dv, c = e % dv;
