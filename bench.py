@@ -646,12 +646,35 @@ def run_case(args):
     prefill_small: B=1, H=8, T=16384, bf16, d=128 (inputs 33.6 MB, packets 155 MB: above L2).
     prefill_4k:    the benchmark's prefill workload, B=1, H=32, T=4096, bf16, d=128.
     decode_small:  N=64 sequences x H=32 heads, d=128, fp32 state 268 MB (above L2), 8 steps.
+    replay_256:    the decode workload's 256 x 32 states, one replay window (3 replayed, 4 new), 3 calls.
+    softplus_4k:   the prefill workload with the softplus gate (fp32 path), 2 calls.
+    backward_4k:   the backward pass on the prefill workload, 2 calls.
     """
     from linear_attention_kda_gb300 import build as kbuild, kda
     kbuild.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.case in ("prefill_small", "prefill_4k"):
+    if args.case == "replay_256":
+        w = syn.DECODE_256
+        Rw, Mw = 3, 4
+        dd = syn.make_decode(w, seed=40, device=dev, steps=Rw + Mw)
+        win = lambda name, a_, b_: dd[name][a_:b_].transpose(0, 1).contiguous()  # noqa: E731
+        cached = tuple(win(n_, 0, Rw) for n_ in ("q", "k", "z", "v", "beta"))
+        new = tuple(win(n_, Rw, Rw + Mw) for n_ in ("q", "k", "z", "v", "beta"))
+        nr = torch.full((w.n_seq,), Rw, dtype=torch.int32, device=dev)
+        nc = torch.ones((w.n_seq,), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            kda.recurrent_replay(cached, nr, new, nc, dd["dt_bias"], dd["A_log"], dd["state"])
+    elif args.case in ("softplus_4k", "backward_4k"):
+        w = WORKLOAD
+        d = syn.make_prefill(w, seed=1, device=dev)
+        args_ = [d[n] for n in ("q", "k", "v", "z", "beta", "dt_bias", "A_log")]
+        for _ in range(2):
+            if args.case == "softplus_4k":
+                kda.chunk_fwd(*args_, cu_seqlens=d["cu_seqlens"], output_final_state=True, gate="softplus")
+            else:
+                kda.chunk_bwd(*args_, torch.ones_like(d["v"]), cu_seqlens=d["cu_seqlens"])
+    elif args.case in ("prefill_small", "prefill_4k"):
         if args.case == "prefill_small":
             w = syn.Workload("prefill_small_bf16_T16384_H8_d128", H=8, d=128, dtype="bf16", seq_len=16384,
                              z_std=1.5, b_range=1.0, alog_std=0.25)
@@ -684,7 +707,8 @@ def main():
     ap.add_argument("--no-epilogue", action="store_true")
     ap.add_argument("--no-gate-variant", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
-    ap.add_argument("--case", choices=["prefill_small", "prefill_4k", "decode_small"], default=None,
+    ap.add_argument("--case", choices=["prefill_small", "prefill_4k", "decode_small", "replay_256", "softplus_4k",
+                                       "backward_4k"], default=None,
                     help="run a small fixed case for profiler captures instead of the benchmark")
     args = ap.parse_args()
     if args.case:
