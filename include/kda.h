@@ -242,14 +242,24 @@ typedef struct {
 } kda_chunk_bwd_args;
 
 /* Bytes of device scratch kda_chunk_bwd needs (0 on invalid sizes): per (chunk, head) about
- * 0.8 MiB at d = 128 (fp32 records, L, the entering state, the leaving Lambda and per-value-tile
- * partial sums), independent of dtype and gate kind. */
+ * 0.42 MiB at d = 128 (fp32 records, L, the entering state, the leaving Lambda and the
+ * chunk-local sums), independent of dtype and gate kind. */
 size_t kda_chunk_bwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
                                     int32_t chunk_size);
 
 /* Gradients must not alias the forward inputs or one another.  workspace as kda_chunk_fwd. */
 kda_status_t kda_chunk_bwd(const kda_chunk_bwd_args *args, void *workspace, size_t workspace_bytes,
                            struct CUstream_st *stream);
+
+/* ------------------------------------------------- kda_selftest_bounded_wait
+ * Not an operation of the paper: a failure-detection self-test.  Launches one CTA that waits on
+ * an mbarrier nothing arrives at, through the bounded wait the tensor-core prefill and replay
+ * kernels use (about one second of the global timer, then give up).  The kernel returns on its
+ * own, sets KDA_ERR_DEVICE_TIMEOUT in the device error word (read it with kda_get_device_error)
+ * and writes the time it waited, in ns, to *elapsed_ns (a device pointer, 8-byte aligned, or NULL).
+ * The context stays usable.  Returns KDA_ERR_CUDA if there is no usable device.
+ */
+kda_status_t kda_selftest_bounded_wait(unsigned long long *elapsed_ns, struct CUstream_st *stream);
 
 /* ----------------------------------------------------------- kda_output_gate
  * The output epilogue of Eq. 6 (section 2.1.1), y_t = W_o[Sigmoid(W_g x_t) * RMSNorm(o~_t)], without

@@ -30,7 +30,8 @@ EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_re
             "kda_status_string", "kda_get_device_error", "kda_abi_version",
             "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws",
             "kda_last_cuda_error", "kda_chunk_fwd_schedule", "kda_output_gate", "kda_recurrent_replay",
-            "kda_chunk_fwd_workspace_size_gate", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size"]
+            "kda_chunk_fwd_workspace_size_gate", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size",
+            "kda_selftest_bounded_wait"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 _vp = ctypes.c_void_p
@@ -114,6 +115,8 @@ def load_library(path: Optional[str] = None):
         L.kda_chunk_bwd_workspace_size.restype = ctypes.c_size_t
         L.kda_chunk_bwd.argtypes = [ctypes.POINTER(ChunkBwdArgs), _vp, ctypes.c_size_t, _vp]
         L.kda_chunk_bwd.restype = ctypes.c_int
+        L.kda_selftest_bounded_wait.argtypes = [_vp, _vp]
+        L.kda_selftest_bounded_wait.restype = ctypes.c_int
         L.kda_recurrent_step.argtypes = [ctypes.POINTER(StepArgs), _vp]
         L.kda_recurrent_step.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -334,6 +337,17 @@ def recurrent_replay(cached, n_replay, new, n_commit, dt_bias, A_log, state, *, 
                    gate_kind=_gate_kind(gate))
     _check(L.kda_recurrent_replay(ctypes.byref(a), _stream(q)), "kda_recurrent_replay")
     return o
+
+
+def selftest_bounded_wait(device=None) -> tuple:
+    """kda_selftest_bounded_wait: a wait nothing completes must give up on its own.  Returns
+    (device error code read afterwards, seconds waited)."""
+    L = load_library()
+    t = torch.zeros((1,), dtype=torch.int64, device=device or "cuda")
+    _check(L.kda_selftest_bounded_wait(_vp(t.data_ptr()), torch.cuda.current_stream(t.device).cuda_stream),
+           "kda_selftest_bounded_wait")
+    code = get_device_error(t.device)
+    return code, int(t.item()) / 1e9
 
 
 def get_device_error(device=None) -> int:

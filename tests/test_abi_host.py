@@ -318,7 +318,7 @@ def test_chunk_bwd_rejects(lib, kw, code):
 
 def test_chunk_bwd_workspace(lib):
     need = lib.kda_chunk_bwd_workspace_size(128, 1, 2, 128, 128, 64)
-    assert need > 2 * 2 * 700 * 1024  # two chunks, two heads, ~0.8 MiB each
+    assert need > 2 * 2 * 400 * 1024  # two chunks, two heads, ~0.42 MiB each
     assert lib.kda_chunk_bwd_workspace_size(128, 1, 2, 96, 96, 64) == 0
     assert lib.kda_chunk_bwd(ctypes.byref(_bwd()), FAKE, need - 1, None) == 5
     assert lib.kda_chunk_bwd(ctypes.byref(_bwd()), None, need, None) == 5

@@ -504,3 +504,17 @@ def test_recurrent_replay_nothing_committed_and_bad_counts():
                          tuple(x.cuda() for x in new), torch.zeros(N, dtype=torch.int32, device="cuda"),
                          d["dt_bias"].cuda(), d["A_log"].cuda(), st)
     assert kda.get_device_error() == 11
+
+
+# ----------------------------------------------------------------------------- failure detection
+
+def test_bounded_wait_gives_up_and_context_stays_usable():
+    """A wait nothing completes (an mbarrier with no arrival, through the bounded wait the kernels
+    use) returns after about a second with KDA_ERR_DEVICE_TIMEOUT; the next call runs normally."""
+    code, secs = kda.selftest_bounded_wait()
+    assert code == 10  # KDA_ERR_DEVICE_TIMEOUT
+    assert 0.5 <= secs <= 10.0, secs
+    assert kda.get_device_error() == 0  # read and cleared
+    d = syn.make_prefill(syn.TINY_F32, seed=0)
+    o, fs = run_prefill(d)
+    compare_prefill(d, o, fs, oracle_prefill(d), TOL_F32)
