@@ -6,10 +6,13 @@
 //
 // Per (sequence, head) state, the layout of the decode step (kda_decode.cu): 2 D threads, warp w
 // holding rows [16 w, 16 w + 16) in registers, lane l holding D / 32 consecutive columns.  The kernel
-// is persistent (two CTAs per SM, each looping over states) and software-pipelined: while a CTA runs
-// the tokens of one state from registers, one warp has already issued the 1-D bulk copies (TMA) that
-// bring the next state and its first 8 tokens' q, k, z, v rows into shared memory, so the state
-// traffic of one item overlaps the arithmetic of the previous one instead of alternating with it.
+// is persistent (two CTAs per SM, each taking a contiguous run of (head, sequence) states in
+// head-major order) and software-pipelined: while a CTA runs the tokens of one state from
+// registers, the next state is on its way by a 1-D bulk copy (TMA) and its first 8 tokens' q, k, z,
+// v rows by 16-byte cp.async copies from every thread, all completing one mbarrier phase, so the
+// state traffic of one item overlaps the arithmetic of the previous one.  Small per-item values
+// (counts, slot, first-group beta) are staged for 32 items at a time and the gate parameters are
+// reloaded only when the head changes: no global load waits on the per-item critical path.
 // Per token
 //     S' = Diag(alpha) S,  p = S'^T k,  r = S'^T q,  e = beta (v - p),
 //     S <- S' + k e^T,     o = scale (r + (k . q) e)
@@ -62,10 +65,16 @@ template <int D, typename Tio> struct Smem {
     static constexpr int E = PR + 2 * NW * D * 4;           // e, [D]
     static constexpr int BETA = E + D * 4;                  // [G]
     static constexpr int KQ = BETA + G * 4;                 // per-warp partial sums of k . q, [G][KQP]
-    static constexpr int META = KQ + G * KQP * 4;           // n_replay, n_commit, valid, pad, slot (int64)
-    static constexpr int BAR = META + 24;                   // one mbarrier (8-byte aligned: META is)
+    // a CTA's items' counts, validity, slot and first-group beta, staged MAXI items at a time
+    static constexpr int MAXI = 32;
+    static constexpr int BNR = KQ + G * KQP * 4;            // int [MAXI]
+    static constexpr int BNC = BNR + MAXI * 4;              // int [MAXI]
+    static constexpr int BVAL = BNC + MAXI * 4;             // int [MAXI]
+    static constexpr int BSLOT = BVAL + MAXI * 4;           // int64 [MAXI]
+    static constexpr int BBETA = BSLOT + MAXI * 8;          // float [MAXI][G]
+    static constexpr int BAR = BBETA + MAXI * G * 4;        // one mbarrier
     static constexpr int BYTES = BAR + 8;
-    static_assert(META % 8 == 0, "slot and barrier need 8-byte alignment");
+    static_assert(BSLOT % 8 == 0 && BAR % 8 == 0, "slots and the barrier need 8-byte alignment");
 };
 
 template <int D, typename Tio>
@@ -92,14 +101,23 @@ replay_kernel(Tokens<Tio> rt, const int32_t *__restrict__ n_replay, Tokens<Tio> 
     float *s_e = reinterpret_cast<float *>(smem + L::E);
     float *s_beta = reinterpret_cast<float *>(smem + L::BETA);
     float(*s_kqp)[KQP] = reinterpret_cast<float(*)[KQP]>(smem + L::KQ);
-    int *meta = reinterpret_cast<int *>(smem + L::META);
-    int64_t *meta_slot = reinterpret_cast<int64_t *>(smem + L::META + 16);
+    constexpr int MAXI = L::MAXI;
+    int *b_nr = reinterpret_cast<int *>(smem + L::BNR);
+    int *b_nc = reinterpret_cast<int *>(smem + L::BNC);
+    int *b_val = reinterpret_cast<int *>(smem + L::BVAL);
+    int64_t *b_slot = reinterpret_cast<int64_t *>(smem + L::BSLOT);
+    float(*b_beta)[G] = reinterpret_cast<float(*)[G]>(smem + L::BBETA);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::BAR);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row0 = warp * RPW, col0 = lane * VW;
     const int c_in = tid % D;  // the channel this thread converts
-    const int64_t step = gridDim.x;
+    // items (head h, sequence n) numbered h-major, it = h N + n; this CTA takes a contiguous run, so its
+    // head (dt_bias, A_log) changes rarely and its sequences' counts and slots can be staged at once
+    const int64_t N_seq = n_items / H;
+    const int64_t base = n_items / gridDim.x, rem = n_items % gridDim.x;
+    const int64_t first = blockIdx.x * base + min((int64_t)blockIdx.x, rem);
+    const int64_t count = base + ((int64_t)blockIdx.x < rem ? 1 : 0);
 
     // token j of sequence n: replayed (cached buffer) for j < nr, new otherwise; [N, L, H] row index
     auto tok_row = [&](int64_t n, int h, int j, int nr) -> int64_t {
@@ -118,84 +136,78 @@ replay_kernel(Tokens<Tio> rt, const int32_t *__restrict__ n_replay, Tokens<Tio> 
         if (lane == 0) s_kqp[jj][c_in / 32] = kq;
     };
 
-    // warp 0 prefetches: counts and slot of the next item to issue (loaded one item ahead of use)
-    int q_nr = 0, q_nc = 0, q_si = 0;  // raw loads: nothing consumes them before the next issue
-    Tio br = Tio(0.f);  // warp 0, lane jj: beta of token jj of the item in flight (converted when used)
-    auto load_meta = [&](int64_t item) {
-        const int64_t n = item / H;
-        if (n_replay) q_nr = n_replay[n];
-        q_nc = n_commit[n];
-        if (state_idx) q_si = state_idx[n];
-    };
-    // bulk copies of the state and of the first G tokens' q, k, z, v rows of `item` into SB / RAW,
-    // completing one phase of `bar`; an item with bad counts or slot is flagged and copies nothing
-    auto issue = [&](int64_t item) {
-        const int64_t n = item / H;
-        const int h = (int)(item % H);
-        const int nr = q_nr, nc = q_nc;
-        const int64_t slot = state_idx ? (int64_t)q_si : n;
-        const bool counts_ok = nr >= 0 && nr <= rt.L && nc >= 0 && nc <= nt.L;
-        const bool slot_ok = slot >= 0 && slot < num_slots;
-        const bool valid = counts_ok && slot_ok;
-        if (lane == 0) {
-            meta[0] = nr;
-            meta[1] = nc;
-            meta[2] = valid;
-            *meta_slot = slot;
+    // counts, validity, slot and first-group beta of items first + k0 .. + MAXI - 1 (two rounds of loads)
+    auto load_batch = [&](int64_t k0) {
+        const int nb = (int)min((int64_t)MAXI, count - k0);
+        if (tid < nb) {
+            const int64_t it = first + k0 + tid, n = it % N_seq;
+            const int nr = n_replay ? n_replay[n] : 0, nc = n_commit[n];
+            const int64_t slot = state_idx ? (int64_t)state_idx[n] : n;
+            const bool counts_ok = nr >= 0 && nr <= rt.L && nc >= 0 && nc <= nt.L;
+            const bool slot_ok = slot >= 0 && slot < num_slots;
             if (!counts_ok) set_error(err, KDA_ERR_BAD_TOKEN_COUNT);
             else if (!slot_ok) set_error(err, KDA_ERR_BAD_STATE_INDEX);
+            b_nr[tid] = nr;
+            b_nc[tid] = nc;
+            b_val[tid] = counts_ok && slot_ok;
+            b_slot[tid] = slot;
         }
-        if (!valid) {
-            if (lane == 0) mbar_arrive(bar);
-            return;
+        __syncthreads();
+        for (int e = tid; e < nb * G; e += NT) {
+            const int kk = e / G, jj = e % G;
+            const int64_t it = first + k0 + kk, n = it % N_seq;
+            const int h = (int)(it / N_seq), nr = b_nr[kk];
+            if (b_val[kk] && jj < min(G, nr + nt.L))
+                b_beta[kk][jj] = ld((jj >= nr ? nt.beta : rt.beta) + tok_row(n, h, jj, nr));
         }
-        const int gn = min(G, nr + nt.L);
-        constexpr uint32_t row_bytes = D * (uint32_t)sizeof(Tio);
-        if (lane == 0) mbar_arrive_expect_tx(bar, D * D * 4 + 4 * gn * row_bytes);
-        __syncwarp();
-        for (int u = lane; u < 1 + 4 * gn; u += 32) {
-            if (u == 0) {
-                bulk_g2s(SB, state + (slot * H + h) * (int64_t)(D * D), D * D * 4, bar);
-            } else {
-                const int t = (u - 1) & 3, jj = (u - 1) >> 2;
+        __syncthreads();
+    };
+    // the state (one 1-D bulk copy by thread 0) and the first G tokens' q, k, z, v rows (16-byte cp.async
+    // granules spread over all threads) of item k, completing one phase of `bar`, which counts thread 0's
+    // arrival with the state's bytes and every thread's cp.async completion; an invalid item copies nothing
+    constexpr int CPR = D * (int)sizeof(Tio) / 16;  // granules per row
+    auto issue = [&](int64_t k) {
+        const int kb = (int)(k % MAXI);
+        const int64_t it = first + k, n = it % N_seq;
+        const int h = (int)(it / N_seq);
+        if (b_val[kb]) {
+            const int nr = b_nr[kb], gn = min(G, nr + nt.L);
+            if (tid == 0) {
+                mbar_arrive_expect_tx(bar, D * D * 4);
+                bulk_g2s(SB, state + (b_slot[kb] * H + h) * (int64_t)(D * D), D * D * 4, bar);
+            }
+            for (int u = tid; u < 4 * gn * CPR; u += NT) {
+                const int t = u / (gn * CPR), r2 = u - t * (gn * CPR), jj = r2 / CPR, part = r2 - jj * CPR;
                 const bool is_new = jj >= nr;
                 const Tio *src = t == 0 ? (is_new ? nt.q : rt.q)
                                : t == 1 ? (is_new ? nt.k : rt.k)
                                : t == 2 ? (is_new ? nt.z : rt.z)
                                         : (is_new ? nt.v : rt.v);
-                bulk_g2s(RAW + (t * G + jj) * D, src + tok_row(n, h, jj, nr) * D, row_bytes, bar);
+                cp_async16(RAW + (t * G + jj) * D + part * (16 / (int)sizeof(Tio)),
+                           src + tok_row(n, h, jj, nr) * D + part * (16 / (int)sizeof(Tio)));
             }
+        } else if (tid == 0) {
+            mbar_arrive(bar);
         }
-        if (lane < gn) br = (lane >= nr ? nt.beta : rt.beta)[tok_row(n, h, lane, nr)];
-    };
-    // dt_bias of this thread's channel and A_log for the head of the item in flight; nothing here
-    // waits for these loads: they are used by the next item
-    float b_nx = 0.f, a_nx = 0.f;
-    auto load_gate = [&](int64_t item) {
-        const int h = (int)(item % H);
-        b_nx = bias ? bias[h * D + c_in] : 0.f;
-        a_nx = A_log ? A_log[h] : 0.f;
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
     };
 
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(bar, 1 + NT);  // thread 0's arrival (with the state's bytes) + every thread's cp.async arrival
         fence_proxy_async();
     }
     __syncthreads();
-    int64_t item = blockIdx.x;
-    if (item < n_items) {
-        if (warp == 0) {
-            load_meta(item);
-            issue(item);
-            if (item + step < n_items) load_meta(item + step);
-        }
-        load_gate(item);
+    if (count > 0) {
+        load_batch(0);
+        issue(0);
     }
+    int h_cur = -1;
+    float b_in = 0.f, eA = 1.f;  // dt_bias of this thread's channel and exp(A) of the current head
 
     uint32_t parity = 0;
-    for (; item < n_items; item += step, parity ^= 1u) {
-        const int64_t n = item / H;
-        const int h = (int)(item % H);
+    for (int64_t kx = 0; kx < count; ++kx, parity ^= 1u) {
+        const int64_t item = first + kx, n = item % N_seq;
+        const int h = (int)(item / N_seq), kb = (int)(kx % MAXI);
         if (!__syncthreads_and(mbar_wait(bar, parity))) {  // bounded: a lost copy cannot hang the GPU
             if (tid == 0) {
                 set_error(err, KDA_ERR_DEVICE_TIMEOUT);
@@ -203,10 +215,14 @@ replay_kernel(Tokens<Tio> rt, const int32_t *__restrict__ n_replay, Tokens<Tio> 
             }
             return;
         }
-        const int nr = meta[0], nc = meta[1];
-        const bool valid = meta[2] != 0;
-        const int64_t slot = *meta_slot;
-        const float b_in = b_nx, eA = expf(a_nx);  // A_log = 0 without A_log: exp(A) = 1
+        const int nr = b_nr[kb], nc = b_nc[kb];
+        const bool valid = b_val[kb] != 0;
+        const int64_t slot = b_slot[kb];
+        if (h != h_cur) {  // a new head: its gate parameters (rare within a CTA's run)
+            h_cur = h;
+            b_in = bias ? bias[h * D + c_in] : 0.f;
+            eA = A_log ? expf(A_log[h]) : 1.f;
+        }
         const int total = nr + nt.L, last_commit = nr + nc - 1;
 
         float2 s[RPW][VP];  // column pairs: the per-token arithmetic runs on packed fp32 pairs
@@ -221,15 +237,12 @@ replay_kernel(Tokens<Tio> rt, const int32_t *__restrict__ n_replay, Tokens<Tio> 
                     convert(jj, ld(RAW + (2 * G + jj) * D + c_in), ld(RAW + (G + jj) * D + c_in),
                             ld(RAW + jj * D + c_in), ld(RAW + (3 * G + jj) * D + c_in), b_in, eA);
             }
-            if (warp == 0 && lane < gn) s_beta[lane] = to_f(br);
+            if (tid < gn) s_beta[tid] = b_beta[kb][tid];
         }
         __syncthreads();  // SB and RAW consumed: the next item's copies may land there
-        if (item + step < n_items) {
-            if (warp == 0) {
-                issue(item + step);
-                if (item + 2 * step < n_items) load_meta(item + 2 * step);
-            }
-            load_gate(item + step);
+        if (kx + 1 < count) {
+            if ((kx + 1) % MAXI == 0) load_batch(kx + 1);  // (this item's staged values are in registers)
+            issue(kx + 1);
         }
         if (!valid) continue;
         float *Sh = state + (slot * H + h) * (int64_t)(D * D);
