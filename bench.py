@@ -531,6 +531,54 @@ def run_ours(args, rank, ws, local):
                "kernels_ms": dict(zip(names_b, per_b)), "workspace_bytes": int(need_b)}
         del go, gST, work_b
 
+    # ---------------- the long prefill workloads (T >= 64K): the varlen batch (32 sequences, ~140K tokens,
+    # initial states) and the 1M-token sequence; inputs far exceed L2, so no flush is needed
+    longw = None
+    if not args.no_long:
+        longw = {}
+        for w_ in (syn.VARLEN_32, syn.LONG_1M):
+            dl = syn.make_prefill(w_, seed=2 if w_ is syn.VARLEN_32 else 3, device=dev)
+            Ls = dl["lengths"]
+            Tl, Nl = sum(Ls), len(Ls)
+            cul = dl["cu_seqlens"].cpu()
+            fsl = torch.empty((Nl, H, D, D), dtype=torch.float32, device=dev)
+            ol = torch.empty_like(dl["v"])
+            wl = torch.empty((kda.chunk_fwd_workspace_size(Tl, Nl, H, D, D, dl["q"].dtype, 64, cul),),
+                             dtype=torch.uint8, device=dev)
+
+            def step_l():
+                kda.chunk_fwd(dl["q"], dl["k"], dl["v"], dl["z"], dl["beta"], dl["dt_bias"], dl["A_log"],
+                              cu_seqlens=dl["cu_seqlens"], cu_seqlens_host=cul, initial_state=dl["initial_state"],
+                              final_state=fsl, workspace=wl, out=ol)
+
+            for _ in range(2):
+                step_l()
+            torch.cuda.synchronize()
+            assert kda.get_device_error() == 0
+            la, lb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            lts = []
+            for _ in range(3):
+                la.record(stream)
+                step_l()
+                lb.record(stream)
+                lb.synchronize()
+                lts.append(la.elapsed_time(lb))
+            msl = sum(lts) / len(lts)
+            fll = prefill_flops(Ls, H, D, D)
+            byl = prefill_bytes(Tl, Nl, H, D, D, 2, dl["initial_state"] is not None, True)
+            tfl = fll["total"] / (msl / 1e3) / 1e12
+            sch = kda.chunk_fwd_schedule(Tl, Nl, H, D, D, dl["q"].dtype, cul)
+            longw[w_.name] = {
+                "tokens": Tl, "sequences": Nl, "ms_per_step": msl, "tokens_per_s": Tl / (msl / 1e3),
+                "tflops": tfl, "tflops_dense_tile": fll["dense_tile"] / (msl / 1e3) / 1e12,
+                "frac_bf16_peak": tfl / tc, "hbm_gbs_algorithmic": byl["total"] / (msl / 1e3) / 1e9,
+                "frac_hbm": byl["total"] / (msl / 1e3) / 1e9 / hbm,
+                "schedule": "fused" if sch["fused"] else ("split state pass, %d chunks per segment" % sch["seg_len"]
+                                                          if sch["seg_len"] else "separate kernels"),
+                "kernels": sch["kernels"]}
+            del dl, fsl, ol, wl
+            torch.cuda.empty_cache()
+
     # ---------------- decode workload (HBM-bound), 512 in-place steps
     dec = None
     if not args.no_decode:
@@ -635,6 +683,7 @@ def run_ours(args, rank, ws, local):
             "epilogue": epi,
             "gate_variant": gvar,
             "backward": bwd,
+            "long_workloads": longw,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -707,6 +756,7 @@ def main():
     ap.add_argument("--no-epilogue", action="store_true")
     ap.add_argument("--no-gate-variant", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--case", choices=["prefill_small", "prefill_4k", "decode_small", "replay_256", "softplus_4k",
                                        "backward_4k"], default=None,
                     help="run a small fixed case for profiler captures instead of the benchmark")
