@@ -27,6 +27,7 @@
 //   bwd_gate_param_kernel    sums the per-chunk gate-parameter gradients per head.
 #include "kda_common.cuh"
 #include "kda_internal.h"
+#include "kda_f32_records.cuh"
 
 namespace kda {
 namespace bw {
@@ -34,40 +35,7 @@ namespace bw {
 constexpr int NT = 256;   // threads per CTA
 constexpr int TILE = 32;  // value columns per CTA (one per lane)
 
-struct Rec {
-    const float *W, *U, *Q, *K, *A, *gam;
-};
-__device__ __forceinline__ Rec rec_at(const char *base, size_t rec_bytes, int64_t slot, int H, int h, int C,
-                                      int dk, int dv) {
-    const float *r = (const float *)(base + ((size_t)slot * H + h) * rec_bytes);
-    Rec v;
-    v.W = r;
-    v.U = v.W + C * dk;
-    v.Q = v.U + C * dv;
-    v.K = v.Q + C * dk;
-    v.A = v.K + C * dk;
-    v.gam = v.A + C * C;
-    return v;
-}
-
-// chunk slot -> (sequence n, first token t0, valid length len); false past the last chunk
-__device__ __forceinline__ bool locate(const int32_t *chunk_start, const int32_t *cu, int64_t T, int N, int C,
-                                       int64_t slot, int &n, int64_t &t0, int &len) {
-    if (slot >= chunk_start[N]) return false;
-    int lo = 0, hi = N;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (chunk_start[mid] <= slot) lo = mid; else hi = mid;
-    }
-    n = lo;
-    const int64_t s = cu ? (int64_t)cu[n] : (T / N) * n;
-    const int64_t e = cu ? (int64_t)cu[n + 1] : s + T / N;
-    t0 = s + (slot - chunk_start[n]) * (int64_t)C;
-    len = (int)min((int64_t)C, e - t0);
-    return true;
-}
-
-// Partial sums one value tile contributes, per (chunk slot, head, tile), in floats.
+// The chunk-local sums the value side writes for the key side, per (chunk slot, head), in floats.
 struct Part {
     int C, dk;
     __host__ __device__ int dQ() const { return 0; }
@@ -117,7 +85,7 @@ chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const i
     for (int cix = c1 - 1; cix >= c0; --cix) {
         const int64_t t0 = s_tok + (int64_t)(cix - c0) * C;
         const int len = (int)min((int64_t)C, e_tok - t0);
-        const Rec rec = rec_at(records, rec_bytes, cix, H, h, C, dk, dv);
+        const F32Record rec = f32_record(records, rec_bytes, cix, H, h, C, dk, dv);
         if (tid == 0 && cix > c0)  // the next record in this (reverse) order, into L2 meanwhile
             prefetch_l2(records + ((size_t)(cix - 1) * H + h) * rec_bytes, (uint32_t)rec_bytes);
         cp_async_wait_all();
@@ -220,7 +188,7 @@ chunk_bwd_value_kernel_t(int64_t T, int N, const int32_t *__restrict__ cu, const
     const int h = blockIdx.y;
     int n, len;
     int64_t t0;
-    if (!locate(chunk_start, cu, T, N, C, slot, n, t0, len)) return;
+    if (!locate_chunk(chunk_start, cu, T, N, C, slot, n, t0, len)) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int PK = dk + 4, PC = C + 4, PS = TILE + 1, PW = dk + 1;
     float *Ws = sm;               // [C][PK]
@@ -237,7 +205,7 @@ chunk_bwd_value_kernel_t(int64_t T, int N, const int32_t *__restrict__ cu, const
     float *bet = dVt + C * PS;    // [C]
     float *dWs = Ss;              // [C][PW] after the tiles: dW, then dX_W (reuses the tile buffers)
 
-    const Rec rec = rec_at(records, rec_bytes, slot, H, h, C, dk, dv);
+    const F32Record rec = f32_record(records, rec_bytes, slot, H, h, C, dk, dv);
     const size_t mbase = ((size_t)slot * H + h) * (size_t)dk * dv;
     tile_async(Ws, PK, rec.W, dk, C, dk, tid, NTV);
     tile_async(Kt, PK, rec.K, dk, C, dk, tid, NTV);
@@ -459,7 +427,7 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
     const int h = blockIdx.y;
     int n, len;
     int64_t t0;
-    if (!locate(chunk_start, cu, T, N, C, slot, n, t0, len)) return;
+    if (!locate_chunk(chunk_start, cu, T, N, C, slot, n, t0, len)) return;
     const int tid = threadIdx.x;
     const int PK = dk + 1, PC = C + 1;
     const int NR = NT / dk;           // row groups
@@ -540,7 +508,7 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
     // then the gate's derivative
     float *gp = gate_part + ((size_t)slot * H + h) * (size_t)(dk + 1);
     for (int cc = tid; cc < dk; cc += NT) {
-        const Rec rec = rec_at(records, rec_bytes, slot, H, h, C, dk, dv);
+        const F32Record rec = f32_record(records, rec_bytes, slot, H, h, C, dk, dv);
         float run = pp[P.dgam() + cc] * rec.gam[cc];
         for (int g = 0; g < NR; ++g) run += red[g * dk + cc];
         const float b = bias ? bias[h * dk + cc] : 0.f;

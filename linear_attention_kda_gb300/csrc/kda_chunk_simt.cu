@@ -23,45 +23,12 @@
 // with g = 0 and beta = 0, which leaves every valid row and the state unchanged.
 #include "kda_common.cuh"
 #include "kda_internal.h"
+#include "kda_f32_records.cuh"
 
 namespace kda {
 
 constexpr int SIMT_THREADS = 256;
 constexpr int SLICE = 32;  // value columns per chain CTA
-
-struct RecordView {
-    float *W, *U, *Q, *K, *A, *gam;
-};
-
-__device__ __forceinline__ RecordView record_view(char *base, size_t rec_bytes, int64_t slot, int H,
-                                                  int h, int C, int dk, int dv) {
-    float *r = (float *)(base + ((size_t)slot * H + h) * rec_bytes);
-    RecordView v;
-    v.W = r;
-    v.U = v.W + C * dk;
-    v.Q = v.U + C * dv;
-    v.K = v.Q + C * dk;
-    v.A = v.K + C * dk;
-    v.gam = v.A + C * C;
-    return v;
-}
-
-// Locates chunk slot -> (sequence n, first token t0, valid length len). Returns false past the end.
-__device__ __forceinline__ bool locate_chunk(const int32_t *chunk_start, const int32_t *cu, int64_t T,
-                                             int N, int C, int64_t slot, int &n, int64_t &t0, int &len) {
-    if (slot >= chunk_start[N]) return false;
-    int lo = 0, hi = N;  // largest n with chunk_start[n] <= slot
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (chunk_start[mid] <= slot) lo = mid; else hi = mid;
-    }
-    n = lo;
-    const int64_t s = cu ? (int64_t)cu[n] : (T / N) * n;
-    const int64_t e = cu ? (int64_t)cu[n + 1] : s + T / N;
-    t0 = s + (slot - chunk_start[n]) * (int64_t)C;
-    len = (int)min((int64_t)C, e - t0);
-    return true;
-}
 
 template <typename Tio>
 __global__ void __launch_bounds__(SIMT_THREADS)
@@ -141,7 +108,7 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
         }
     }
     __syncthreads();
-    RecordView rec = record_view(records, rec_bytes, slot, H, h, C, dk, dv);
+    F32Record rec = f32_record(records, rec_bytes, slot, H, h, C, dk, dv);
     for (int e = tid; e < C * C; e += SIMT_THREADS) rec.A[e] = As[(e / C) * PC + e % C];
     if (Lout) {  // the backward pass reuses L (strictly lower, zeros elsewhere)
         float *Lg = Lout + ((size_t)slot * H + h) * (size_t)C * C;
@@ -218,7 +185,7 @@ chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
     for (int cix = c0; cix < c1; ++cix) {
         const int64_t t0 = s_tok + (int64_t)(cix - c0) * C;
         const int len = (int)min((int64_t)C, e_tok - t0);
-        RecordView rec = record_view((char *)records, rec_bytes, cix, H, h, C, dk, dv);
+        F32Record rec = f32_record(records, rec_bytes, cix, H, h, C, dk, dv);
         if (tid == 0 && cix + 1 < c1)  // the next chunk's record, into L2 while this one runs
             prefetch_l2(records + ((size_t)(cix + 1) * H + h) * rec_bytes, (uint32_t)rec_bytes);
         cp_async_wait_all();

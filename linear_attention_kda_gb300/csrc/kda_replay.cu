@@ -46,9 +46,6 @@ __device__ __forceinline__ void st_row(float *p, const float2 (&x)[VP]) {  // gl
         __stcs(reinterpret_cast<float2 *>(p), x[0]);
 }
 
-__device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
-
 template <typename Tio> struct Tokens {
     const Tio *q, *k, *z, *v, *beta;
     int L;  // tokens per sequence in this buffer
