@@ -307,6 +307,11 @@ __device__ __forceinline__ void element_pass(unsigned char *sm, unsigned char *s
 // Packet publication between CTAs of one (cooperative) launch: the producer releases a flag once the
 // packet's bulk writes have completed; the consumer acquires it before its bulk reads.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// Drops one 128-byte line from L2 without writing it back (its contents become undefined).
+__device__ __forceinline__ void discard_l2(const void *p) {
+    asm volatile("discard.global.L2 [%0], 128;" :: "l"(p) : "memory");
+}
+
 // Flags hold the epoch of the launch that published them (a per-process counter that never repeats),
 // so a workspace needs no clearing between launches.
 __device__ __forceinline__ void flag_release(uint64_t *f, uint64_t epoch) {
@@ -923,9 +928,11 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
             if (!ok) atomicExch(s_fail, 1);
         }
     } else if (warp == 9) {
-        // ------------------------------------------------ packet loads (one thread)
+        // ------------------------------------------------ packet loads (lane 0); once a packet part has
+        // been consumed from its stage, the whole warp drops that part's lines from L2 (this role is its
+        // last reader: the lines are never read again and need no write-back to DRAM)
+        bool ok = true;
         if (lane == 0) {
-            bool ok = true;
             for (int kk = 0; kk < 2 && kk < nc && ok; ++kk) {
                 ok = acquire(kk);
                 if (ok) {
@@ -934,19 +941,30 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                 }
             }
             if (ok && nc > 2 && !flags) bulk_prefetch_l2(packet(2), PK_STRIDE);
-            for (int kk = 0; kk + 2 < nc && ok; ++kk) {
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        for (int kk = 0; kk + 2 < nc && ok; ++kk) {
+            if (lane == 0) {
                 // MMA_U and MMA1 of chunk kk done and gamma_kk read (V~^T of chunk kk written): part 1 of
                 // its stage takes chunk kk + 2
                 ok = mbar_wait_spin(&bar_vt[kk & 1], (kk >> 1) & 1) && acquire(kk + 2);
-                if (!ok) break;
-                load_part1(kk + 2);
-                ok = mbar_wait_spin(&bar_o[kk & 1], (kk >> 1) & 1);  // all MMAs of chunk kk done: part 2
-                if (!ok) break;
-                load_part2(kk + 2);
-                if (kk + 3 < nc && !flags) bulk_prefetch_l2(packet(kk + 3), PK_STRIDE);
+                if (ok) load_part1(kk + 2);
             }
-            if (!ok) atomicExch(s_fail, 1);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            for (int l = lane; l < PK_K / 128; l += 32) discard_l2(packet(kk) + l * 128);  // part 1 (+ pad)
+            if (lane == 0) {
+                ok = mbar_wait_spin(&bar_o[kk & 1], (kk >> 1) & 1);  // all MMAs of chunk kk done: part 2
+                if (ok) {
+                    load_part2(kk + 2);
+                    if (kk + 3 < nc && !flags) bulk_prefetch_l2(packet(kk + 3), PK_STRIDE);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            for (int l = PK_K / 128 + lane; l < PK_STRIDE / 128; l += 32) discard_l2(packet(kk) + l * 128);
         }
+        if (!ok && lane == 0) atomicExch(s_fail, 1);
     } else if (warp >= 12 && warp < 16) {
         // ------------------------------------------------ output warps 12-15 (128 threads, one d_v lane each)
         const int ot = tid - 384;
