@@ -84,8 +84,9 @@ def chunk_lengths_count(lengths, C=64):
 
 def measured_traffic(kernel, p_items):
     """DRAM bytes per launch of `kernel` from the committed ncu record (profiles/traffic_*.json),
-    scaled by the (chunk, head) items of this launch; None if no record exists or the kernel
-    source changed since the capture (sha256 prefix mismatch)."""
+    scaled by the work items of this launch (the record's unit: (chunk, head) items of the prefill,
+    (sequence, head) states of the replay window); None if no record exists or the kernel source
+    changed since the capture (sha256 prefix mismatch)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", f"traffic_{kernel}.json")
     if not os.path.exists(path):
@@ -702,7 +703,8 @@ def run_ours(args, rank, ws, local):
                          "us_per_call": rms * 1e3, "tokens_per_call": DECODE.n_seq * (Rw + Mw),
                          "bytes_per_call": rbytes, "GB_per_s": rgb,
                          "roofline": {"bound": "hbm", "achieved": rgb, "peak": hbm, "unit": "GB/s",
-                                      "frac": rgb / hbm, "kernel": "replay"},
+                                      "frac": rgb / hbm, "kernel": "replay",
+                                      "traffic": measured_traffic("replay", p_items=nh)},
                          "single_steps_us": (Rw + Mw) * dms * 1e3,
                          "speedup_vs_single_steps": (Rw + Mw) * dms / rms}
         del dd2, cached, new
