@@ -87,7 +87,9 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
                              a->cu_seqlens_host, a->gate_kind))
         return 0;
     // either one fused launch (intra-chunk transform and output pass together) or the chunk plan,
-    // then intra-chunk transform, [segment summaries, fold,] output pass
+    // then intra-chunk transform, [segment summaries, fold,] output pass; an empty batch (T = 0)
+    // runs the chunk plan and the output pass alone, which passes the states through
+    if (a->T == 0) return 2;
     const int extra = a->out_gate ? 1 : 0;  // the output epilogue's pass
     if (p.fused) return 1 + extra;
     return (p.split ? 5 : 3) + extra;

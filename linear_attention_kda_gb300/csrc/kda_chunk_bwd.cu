@@ -155,6 +155,7 @@ chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const i
             for (int i = 0; i < CW; ++i) Lm[(cb + i) * PS + lane] = lm[i];
         }
     }
+    cp_async_wait_all();  // a sequence without chunks: the copy of d final_state
     __syncthreads();
     if (d_init) {
         for (int e = tid; e < dk * TILE; e += NT) {
@@ -631,7 +632,15 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
     }
     kda_profile_mark(4, stream);
     st = kda_cuda_status(cudaGetLastError());
-    if (st != KDA_OK || Ly.slots == 0 || a->T == 0) return st;
+    if (st != KDA_OK) return st;
+    if (Ly.slots == 0 || a->T == 0) {  // no tokens: the parameter gradients are zero
+        if (a->grad_dt_bias || a->grad_A_log) {
+            bw::bwd_gate_param_kernel<<<(unsigned)H, 128, 0, stream>>>(gpart, 0, H, dk, a->grad_dt_bias,
+                                                                       a->grad_A_log);
+            st = kda_cuda_status(cudaGetLastError());
+        }
+        return st;
+    }
     // 3. value side per (chunk, head), the value channels 32 at a time
     {
         const size_t smem_val = sizeof(float) * (2 * (size_t)C * (dk + 4) + 2 * (size_t)C * (C + 4) +

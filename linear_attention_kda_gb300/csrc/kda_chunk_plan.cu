@@ -203,9 +203,10 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
     p->T = T; p->N = N; p->H = H; p->dk = dk; p->dv = dv; p->C = C;
     p->max_chunks = (T + N * (int64_t)(C - 1)) / C;
     // bf16 with d_k = d_v = 128 and the bounded gate runs on the tensor cores; everything else on
-    // the fp32 CUDA-core path
-    p->path = (dtype == KDA_BF16 && dk == 128 && dv == 128 && C == 64 && gate_kind == KDA_GATE_LOWER_BOUND &&
-               !force_fp32_path) ? 1 : 0;
+    // the fp32 CUDA-core path, and so does an empty batch (T = 0: no tiles to map, only the states
+    // to pass through)
+    p->path = (T > 0 && dtype == KDA_BF16 && dk == 128 && dv == 128 && C == 64 &&
+               gate_kind == KDA_GATE_LOWER_BOUND && !force_fp32_path) ? 1 : 0;
     if (p->path == 1) {
         p->record_bytes = kda_tc_packet_stride();  // bf16 operand images + gamma^C
     } else {

@@ -267,6 +267,7 @@ chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
             for (int i = 0; i < CW; ++i) Ss[(cb + i) * PS + lane] = sn[i];
         }
     }
+    cp_async_wait_all();  // a sequence without chunks: the initial state's copy
     __syncthreads();
     if (final_state) {
         for (int e = tid; e < dk * SLICE; e += SIMT_THREADS) {

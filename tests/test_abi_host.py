@@ -323,3 +323,17 @@ def test_chunk_bwd_workspace(lib):
     assert lib.kda_chunk_bwd(ctypes.byref(_bwd()), FAKE, need - 1, None) == 5
     assert lib.kda_chunk_bwd(ctypes.byref(_bwd()), None, need, None) == 5
     assert lib.kda_chunk_bwd(ctypes.byref(_bwd()), FAKE + 16, need, None) == 4
+
+
+def test_empty_batch_plan(lib):
+    """An empty batch (T = 0) takes the fp32 path whatever its dtype and head size: the chunk plan
+    and the output pass, which only passes the states through (there are no tiles to map for the
+    tensor-core path).  The epilogue, given, has no tokens to run over."""
+    for dt, d in ((torch.bfloat16, 128), (torch.float32, 64), (torch.bfloat16, 64)):
+        s = kda.chunk_fwd_schedule(0, 3, 32, d, d, dt)
+        assert s == {"fused": False, "own_chunks": 0, "seg_len": 0, "kernels": 2}, (dt, d)
+        assert kda.chunk_fwd_workspace_size(0, 3, 32, d, d, dt) > 0
+    a = kda.ChunkArgs(T=0, N=3, H=32, dk=128, dv=128, dtype=kda.KDA_BF16, chunk_size=64, out_gate=16)
+    assert lib.kda_chunk_fwd_kernel_count(ctypes.byref(a)) == 2
+    # the same sizes with tokens run three kernels on the fp32 path (plan, intra, output pass)
+    assert kda.chunk_fwd_schedule(640, 3, 32, 64, 64, torch.float32)["kernels"] == 3

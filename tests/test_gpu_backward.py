@@ -128,3 +128,34 @@ def test_chunk_bwd_full_prefill_workload_sampled_heads():
         assert rel_err(got["initial_state"][0, h], r["dS0"]) <= TOL_BF16, h
         assert rel_err(got["dt_bias"][h], r["db"]) <= TOL_BF16, h
         assert abs(got["A_log"][h] - r["dA_log"]) <= TOL_BF16 * max(1.0, abs(r["dA_log"])), h
+
+
+def test_chunk_bwd_empty_batch():
+    """T = 0 over two sequences, through the C ABI with NaN-filled gradient buffers.
+    - Eq. 1 takes no step, so S_T = S_0.
+    - d initial_state is then d final_state bit for bit, or zeros without it.
+    - The dt_bias and A_log gradients are zero and are written as such."""
+    import ctypes
+    H, D, N = 2, 64, 2
+    L = kda.load_library()
+    b, a = (x.cuda() for x in syn.make_head_params(H, D, 4, b_range=1.0, alog_std=0.25))
+    dST = (torch.randn((N, H, D, D), generator=torch.Generator().manual_seed(5)) * 0.1).cuda()
+    cu = torch.zeros(N + 1, dtype=torch.int32, device="cuda")
+    need = int(L.kda_chunk_bwd_workspace_size(0, N, H, D, D, 64))
+    ws = torch.empty((max(need, 1),), dtype=torch.uint8, device="cuda")
+    for with_dst in (True, False):
+        nan = float("nan")
+        gdb = torch.full((H, D), nan, device="cuda")
+        gda = torch.full((H,), nan, device="cuda")
+        gS0 = torch.full((N, H, D, D), nan, device="cuda")
+        args = kda.ChunkBwdArgs(T=0, N=N, H=H, dk=D, dv=D, dtype=kda.KDA_F32, dt_bias=b.data_ptr(),
+                                A_log=a.data_ptr(), g_min=-5.0, scale=1.0, cu_seqlens=cu.data_ptr(),
+                                grad_final_state=dST.data_ptr() if with_dst else None,
+                                grad_dt_bias=gdb.data_ptr(), grad_A_log=gda.data_ptr(),
+                                grad_initial_state=gS0.data_ptr(), chunk_size=64, gate_kind=0)
+        assert L.kda_chunk_bwd(ctypes.byref(args), ws.data_ptr(), ws.numel(), None) == 0
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        assert torch.equal(gS0, dST) if with_dst else torch.count_nonzero(gS0.nan_to_num(1.0)).item() == 0
+        assert torch.count_nonzero(gdb.nan_to_num(1.0)).item() == 0
+        assert torch.count_nonzero(gda.nan_to_num(1.0)).item() == 0

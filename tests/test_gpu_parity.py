@@ -170,6 +170,47 @@ def test_final_state_aliases_initial_state():
     compare_prefill(d, o.float().cpu(), st.cpu(), oracle_prefill(d), TOL_BF16)
 
 
+@pytest.mark.parametrize("dtype,D,H", [("bf16", 128, 2), ("bf16", 128, 32), ("f32", 64, 2)])
+def test_empty_sequences_copy_initial_state_exactly(dtype, D, H):
+    """Empty sequences among non-empty ones (Eq. 1 takes no step: S_T = S_0).  Their final state is
+    their initial state bit for bit: on the fused tensor-core launch (6 x 2 chains), the separate
+    tensor-core kernels (6 x 32 chains) and the fp32 path.  The other sequences match the oracle."""
+    w = syn.Workload("e", H=H, d=D, dtype=dtype, seq_len=None, z_std=1.5, b_range=1.0, alog_std=0.25,
+                     s0_std=0.5)
+    lengths = [0, 70, 0, 0, 130, 0]
+    d = _varlen(w, lengths, seed=8)
+    if dtype == "bf16":
+        sch = kda.chunk_fwd_schedule(sum(lengths), len(lengths), H, D, D, torch.bfloat16, d["cu_seqlens"])
+        assert sch["fused"] == (H == 2)
+    o, fs = run_prefill(d)
+    for n, L in enumerate(lengths):
+        if L == 0:
+            assert torch.equal(fs[n], d["initial_state"][n]), n
+    compare_prefill(d, o, fs, oracle_prefill(d), TOL_BF16 if dtype == "bf16" else TOL_F32)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64)])
+def test_empty_batch_passes_states_through(dtype, D):
+    """T = 0 over three sequences (cu_seqlens all zero): the final states are the initial states bit
+    for bit, or zeros without them (the buffer starts as NaN); no token pointer is read."""
+    H, N = 2, 3
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    tok = lambda *s: torch.empty(s, dtype=dt, device="cuda")  # noqa: E731
+    b, a = syn.make_head_params(H, D, 3, b_range=1.0, alog_std=0.25)
+    S0 = syn.make_state(N, H, D, D, 0.5, 3).cuda()
+    cu = torch.zeros(N + 1, dtype=torch.int32)
+    args = (tok(0, H, D), tok(0, H, D), tok(0, H, D), tok(0, H, D), tok(0, H), b.cuda(), a.cuda())
+    o, fs = kda.chunk_fwd(*args, cu_seqlens=cu.cuda(), cu_seqlens_host=cu, initial_state=S0,
+                          output_final_state=True)
+    fz = torch.full((N, H, D, D), float("nan"), device="cuda")
+    kda.chunk_fwd(*args, cu_seqlens=cu.cuda(), final_state=fz)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    assert o.shape == (0, H, D)
+    assert torch.equal(fs, S0)
+    assert not torch.isnan(fz).any() and torch.count_nonzero(fz).item() == 0
+
+
 @pytest.mark.parametrize("split", [1, 64, 100, 129])
 def test_split_resume_matches_one_pass(split):
     """Final state of a prefix passed as the initial state of the rest equals one pass (prefix reuse)."""
