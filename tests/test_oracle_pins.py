@@ -372,6 +372,37 @@ def test_c_oracle_matches_numpy_varlen():
             np.testing.assert_allclose(S_c, S_np[n, h], rtol=1e-12, atol=1e-13)
 
 
+def test_empty_sequences_and_empty_batch():
+    """Eq. 1 over zero tokens takes no step.
+    - An empty sequence's final state is its initial state, exactly, in both codings.
+    - It has no outputs.
+    - The sequences around it come out as if the batch held them alone.
+    - An empty batch (T = 0) only passes every state through."""
+    rng = np.random.default_rng(11)
+    H, d = 2, 4
+    for lengths in ([0, 5, 0, 0, 3, 0], [0, 0, 0]):
+        T = sum(lengths)
+        q, k, v, z = (rng.normal(size=(T, H, d)).astype(np.float32) for _ in range(4))
+        beta = rng.uniform(0.1, 0.9, size=(T, H)).astype(np.float32)
+        b = rng.uniform(-1, 1, size=(H, d)).astype(np.float32)
+        a = rng.normal(0, 0.3, size=H).astype(np.float32)
+        S0 = rng.normal(size=(len(lengths), H, d, d))
+        cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+        o, ST = R.forward(q, k, v, z, beta, b, a, cu, S0=S0)
+        res, _ = c_ref.forward(q, k, v, z, beta, b, a, cu, S0=S0)
+        assert o.shape == (T, H, d)
+        kept = [n for n, L in enumerate(lengths) if L > 0]
+        for n, L in enumerate(lengths):
+            for h in range(H):
+                if L == 0:
+                    assert np.array_equal(ST[n, h], S0[n, h]) and np.array_equal(res[(n, h)][1], S0[n, h])
+                    assert res[(n, h)][0].shape == (0, d)
+        if kept:
+            cu2 = np.concatenate([[0], np.cumsum([lengths[n] for n in kept])]).astype(np.int32)
+            o2, ST2 = R.forward(q, k, v, z, beta, b, a, cu2, S0=S0[kept])
+            assert np.array_equal(o2, o) and np.array_equal(ST2, ST[kept])
+
+
 # ----------------------------------------------------------------------------- mutation tests
 
 def _mut_decay_after(q, k, v, g, beta, S0):
