@@ -337,3 +337,16 @@ def test_empty_batch_plan(lib):
     assert lib.kda_chunk_fwd_kernel_count(ctypes.byref(a)) == 2
     # the same sizes with tokens run three kernels on the fp32 path (plan, intra, output pass)
     assert kda.chunk_fwd_schedule(640, 3, 32, 64, 64, torch.float32)["kernels"] == 3
+
+
+def test_profile_events_validation_and_last_cuda_error(lib):
+    """kda_set_profile_events rejects a negative count, a count above its table and a NULL array
+    with a positive count; (NULL, 0) switches timing off.  kda_last_cuda_error is cleared by reading."""
+    arr = (ctypes.c_void_p * 1)()
+    assert lib.kda_set_profile_events(None, -1) == 1
+    assert lib.kda_set_profile_events(None, 1) == 1
+    assert lib.kda_set_profile_events(arr, 1 << 20) == 1
+    assert lib.kda_set_profile_events(None, 0) == 0
+    lib.kda_last_cuda_error.restype = ctypes.c_int32
+    lib.kda_last_cuda_error()
+    assert lib.kda_last_cuda_error() == 0
