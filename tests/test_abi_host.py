@@ -113,6 +113,7 @@ def _call_chunk(lib, a, ws=FAKE, ws_bytes=1 << 40):
 
 
 @pytest.mark.parametrize("kw,code", [
+    (dict(T=1 << 31), 2),           # token indices are 32-bit: T above INT32_MAX is refused
     (dict(dk=96, dv=96), 2),
     (dict(dk=128, dv=64), 2),
     (dict(chunk_size=32), 2),
@@ -177,6 +178,7 @@ def _step(**kw):
 
 
 @pytest.mark.parametrize("kw,code", [
+    (dict(N=1 << 30, H=4), 2),       # N x H above INT32_MAX
     (dict(dk=32, dv=32), 2),
     (dict(dtype=5), 3),
     (dict(H=0), 1),
@@ -250,6 +252,7 @@ def _rp(**kw):
 
 
 @pytest.mark.parametrize("kw,code", [
+    (dict(N=1 << 20, M=1 << 10, H=4), 2),   # N x window x H above INT32_MAX
     (dict(dk=96, dv=96), 2),
     (dict(dtype=5), 3),
     (dict(M=0), 1),
@@ -297,6 +300,7 @@ def _bwd(**kw):
 
 
 @pytest.mark.parametrize("kw,code", [
+    (dict(T=1 << 31), 2),                  # T above INT32_MAX
     (dict(dk=96, dv=96), 2),
     (dict(chunk_size=16), 2),
     (dict(dtype=9), 3),
