@@ -2,130 +2,133 @@
 //     y[t,h,c] = Sigmoid(g[t,h,c]) * w[h,c] * o[t,h,c] / sqrt(mean_c' o[t,h,c']^2 + eps),
 // the per-head RMSNorm of the recurrent output followed by the data-dependent output gate.
 //
-// One warp per RPW (token, head) rows; each lane holds VPL = dv / 32 consecutive channels of a row (one
-// vector load per tensor), the sum of squares is a warp-shuffle reduction.  All of a warp's loads are
-// issued before the first is used, so that enough bytes are in flight to cover HBM latency.  HBM-bound: o and g are read
-// once, y written once (y may alias o: every element is read before it is written, by the same
-// thread).
+// Every lane moves whole 16-byte vectors: a row (one token, one head) is split over the fewest lanes
+// that hold it in 16-byte pieces (4 to 32 lanes), the sum of squares is a shuffle reduction over those
+// lanes, and a warp issues the loads of four passes (8 to 32 rows) before it uses any, so that enough
+// bytes are in flight to cover HBM latency.  HBM-bound: o and g are read once, y written once (y may
+// alias o: every element is read before it is written, by the same thread).
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
 namespace kda {
 namespace og {
 
-template <int BYTES>
-__device__ __forceinline__ void ld_bytes(const void *p, uint32_t *w) {
-    if constexpr (BYTES == 2) {
-        w[0] = *reinterpret_cast<const unsigned short *>(p);
-    } else if constexpr (BYTES == 4) {
-        w[0] = *reinterpret_cast<const uint32_t *>(p);
-    } else if constexpr (BYTES == 8) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(p);
-        w[0] = v.x; w[1] = v.y;
+// 8 bf16 or 4 fp32 values of one 16-byte vector, as fp32
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4 &u, float *f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f[e] = __uint_as_float(w[e]);
     } else {
 #pragma unroll
-        for (int i = 0; i < BYTES / 16; ++i) {
-            const uint4 v = reinterpret_cast<const uint4 *>(p)[i];
-            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        for (int e = 0; e < 4; ++e) {
+            f[2 * e] = __uint_as_float(w[e] << 16);
+            f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
         }
     }
 }
-template <int BYTES>
-__device__ __forceinline__ void st_bytes(void *p, const uint32_t *w) {
-    if constexpr (BYTES == 2) {
-        *reinterpret_cast<unsigned short *>(p) = (unsigned short)w[0];
-    } else if constexpr (BYTES == 4) {
-        *reinterpret_cast<uint32_t *>(p) = w[0];
-    } else if constexpr (BYTES == 8) {
-        *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
+template <typename T>
+__device__ __forceinline__ uint4 pack16(const float *f) {
+    if constexpr (sizeof(T) == 4) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
     } else {
+        uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < BYTES / 16; ++i)
-            reinterpret_cast<uint4 *>(p)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int e = 0; e < 4; ++e)
+            w[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[2 * e])) |
+                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[2 * e + 1])) << 16);
+        return make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
-// VPL values of type T (bf16 or fp32) as fp32, from / to 32-bit words
-template <typename T, int VPL>
-__device__ __forceinline__ void unpack(const uint32_t *w, float *f) {
-#pragma unroll
-    for (int e = 0; e < VPL; ++e) {
-        if constexpr (sizeof(T) == 4) {
-            f[e] = __uint_as_float(w[e]);
-        } else {
-            const uint32_t x = w[e >> 1];
-            f[e] = __uint_as_float(((e & 1) ? (x & 0xFFFF0000u) : (x << 16)));
-        }
-    }
-}
-template <typename T, int VPL>
-__device__ __forceinline__ void pack(const float *f, uint32_t *w) {
-#pragma unroll
-    for (int e = 0; e < VPL; ++e) {
-        if constexpr (sizeof(T) == 4) {
-            w[e] = __float_as_uint(f[e]);
-        } else {
-            const uint32_t b = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[e]));
-            if (e & 1) w[e >> 1] |= b << 16; else w[e >> 1] = b;
-        }
-    }
-}
+// A row (one token, one head: DV values) is split over LPR lanes, each holding VPL 16-byte vectors;
+// a warp pass covers 32 / LPR rows and a warp issues the loads of PASSES passes before using any.
+constexpr int PASSES = 4;
 
-constexpr int RPW = 4;  // rows per warp: their loads are all issued before any is used
+template <typename T, int DV>
+struct RowSplit {
+    static constexpr int VEC = 16 / (int)sizeof(T);       // values per 16-byte vector
+    static constexpr int NV = DV / VEC;                   // vectors per row
+    static constexpr int LPR = NV < 32 ? NV : 32;         // lanes per row
+    static constexpr int VPL = NV / LPR;                  // vectors per lane
+    static constexpr int RPP = 32 / LPR;                  // rows per warp pass
+    static constexpr int ROWS_PER_BLOCK = 8 * RPP * PASSES;
+    static_assert(NV % LPR == 0 && 32 % LPR == 0, "row split");
+};
 
-template <typename T, int VPL>
+template <typename T, int DV>
 __global__ void __launch_bounds__(256) output_gate_kernel(const T *__restrict__ o, const T *__restrict__ g,
                                                           const float *__restrict__ w, float eps, int64_t rows,
                                                           int H, T *y) {
-    constexpr int DV = 32 * VPL, BYTES = VPL * (int)sizeof(T), WORDS = (BYTES + 3) / 4;
-    const int lane = threadIdx.x & 31;
-    const int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * RPW;
-    uint32_t ow[RPW][WORDS], gw[RPW][WORDS];
+    using RS = RowSplit<T, DV>;
+    constexpr int VEC = RS::VEC, LPR = RS::LPR, VPL = RS::VPL, RPP = RS::RPP;
+    const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
+    const int64_t wrow0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * (RPP * PASSES);
+    const int c0 = li * VPL * VEC;  // first channel of this lane
+    uint4 ov[PASSES][VPL], gv[PASSES][VPL];
 #pragma unroll
-    for (int i = 0; i < RPW; ++i) {
-        if (row0 + i < rows) {
-            const size_t base = (size_t)(row0 + i) * DV + (size_t)VPL * lane;
-            ld_bytes<BYTES>(o + base, ow[i]);
-            ld_bytes<BYTES>(g + base, gw[i]);
+    for (int p = 0; p < PASSES; ++p) {
+        const int64_t row = wrow0 + p * RPP + sub;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            if (row < rows) {
+                const size_t off = (size_t)row * DV + c0 + j * VEC;
+                ov[p][j] = *reinterpret_cast<const uint4 *>(o + off);
+                gv[p][j] = *reinterpret_cast<const uint4 *>(g + off);
+            } else {
+                ov[p][j] = gv[p][j] = make_uint4(0, 0, 0, 0);
+            }
         }
     }
 #pragma unroll
-    for (int i = 0; i < RPW; ++i) {
-        const int64_t row = row0 + i;
-        if (row >= rows) break;  // warp-uniform
-        const int h = (int)(row % H);
-        float ov[VPL], gv[VPL];
-        unpack<T, VPL>(ow[i], ov);
-        unpack<T, VPL>(gw[i], gv);
+    for (int p = 0; p < PASSES; ++p) {
+        const int64_t row = wrow0 + p * RPP + sub;
+        float of[VPL * VEC];
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) unpack16<T>(ov[p][j], of + j * VEC);
         float ss = 0.f;
 #pragma unroll
-        for (int e = 0; e < VPL; ++e) ss = fmaf(ov[e], ov[e], ss);
+        for (int e = 0; e < VPL * VEC; ++e) ss = fmaf(of[e], of[e], ss);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        for (int off = LPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);  // the row's lanes
+        if (row >= rows) continue;  // after the shuffles, which every lane joins
         const float r = rsqrtf(ss * (1.0f / DV) + eps);
-        float yv[VPL];
+        const int h = (int)(row % H);
 #pragma unroll
-        for (int e = 0; e < VPL; ++e) {
-            const float wv = w ? __ldg(w + (size_t)h * DV + VPL * lane + e) : 1.f;
-            yv[e] = __fdividef(ov[e] * r * wv, 1.0f + __expf(-gv[e]));  // 1 + e^{-g} >= 1; inf gives 0
+        for (int j = 0; j < VPL; ++j) {
+            float gf[VEC], yf[VEC], wf[VEC];
+            unpack16<T>(gv[p][j], gf);
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4) {
+                const float4 w4 = w ? __ldg(reinterpret_cast<const float4 *>(w + (size_t)h * DV + c0 + j * VEC + e))
+                                    : make_float4(1.f, 1.f, 1.f, 1.f);
+                wf[e] = w4.x; wf[e + 1] = w4.y; wf[e + 2] = w4.z; wf[e + 3] = w4.w;
+            }
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                yf[e] = __fdividef(of[j * VEC + e] * r * wf[e], 1.0f + __expf(-gf[e]));  // 1 + e^{-g} >= 1; inf gives 0
+            *reinterpret_cast<uint4 *>(y + (size_t)row * DV + c0 + j * VEC) = pack16<T>(yf);
         }
-        uint32_t yw[WORDS];
-        pack<T, VPL>(yv, yw);
-        st_bytes<BYTES>(y + (size_t)row * DV + (size_t)VPL * lane, yw);
     }
+}
+
+template <typename T, int DV>
+static void launch_dv(const kda_output_gate_args *a, int64_t rows, cudaStream_t stream) {
+    constexpr int RB = RowSplit<T, DV>::ROWS_PER_BLOCK;
+    const unsigned grid = (unsigned)((rows + RB - 1) / RB);
+    output_gate_kernel<T, DV><<<grid, 256, 0, stream>>>((const T *)a->o, (const T *)a->g, a->norm_weight, a->eps,
+                                                        rows, a->H, (T *)a->y);
 }
 
 template <typename T>
 static kda_status_t launch_t(const kda_output_gate_args *a, cudaStream_t stream) {
     const int64_t rows = a->T * (int64_t)a->H;
-    const unsigned grid = (unsigned)((rows + 8 * RPW - 1) / (8 * RPW));
-    const T *o = (const T *)a->o, *g = (const T *)a->g;
-    T *y = (T *)a->y;
     switch (a->dv) {
-        case 32: output_gate_kernel<T, 1><<<grid, 256, 0, stream>>>(o, g, a->norm_weight, a->eps, rows, a->H, y); break;
-        case 64: output_gate_kernel<T, 2><<<grid, 256, 0, stream>>>(o, g, a->norm_weight, a->eps, rows, a->H, y); break;
-        case 128: output_gate_kernel<T, 4><<<grid, 256, 0, stream>>>(o, g, a->norm_weight, a->eps, rows, a->H, y); break;
-        case 256: output_gate_kernel<T, 8><<<grid, 256, 0, stream>>>(o, g, a->norm_weight, a->eps, rows, a->H, y); break;
+        case 32: launch_dv<T, 32>(a, rows, stream); break;
+        case 64: launch_dv<T, 64>(a, rows, stream); break;
+        case 128: launch_dv<T, 128>(a, rows, stream); break;
+        case 256: launch_dv<T, 256>(a, rows, stream); break;
         default: return KDA_ERR_UNSUPPORTED_SHAPE;
     }
     return kda_cuda_status(cudaGetLastError());
