@@ -354,3 +354,25 @@ def test_profile_events_validation_and_last_cuda_error(lib):
     lib.kda_last_cuda_error.restype = ctypes.c_int32
     lib.kda_last_cuda_error()
     assert lib.kda_last_cuda_error() == 0
+
+
+def test_schedule_decisions_for_the_workloads(lib):
+    """The latency model's choices for the workloads, on 152 SMs (the host query assumes GB300's
+    count when no device is present):
+    - T = 4096 x H = 32 takes the fused launch, each chain producing its own first 4 chunks;
+    - the 1M-token sequence with 32 heads also takes the fused launch;
+    - with 2 heads it splits the state pass instead (few chains on many SMs);
+    - the varlen batch (32 sequences x 32 heads) takes the separate kernels."""
+    from linear_attention_kda_gb300 import synthetic as syn
+    bf = torch.bfloat16
+    assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, bf) == {"fused": True, "own_chunks": 4, "seg_len": 0,
+                                                                  "kernels": 1}
+    assert kda.chunk_fwd_schedule(1 << 20, 1, 32, 128, 128, bf)["fused"]
+    s = kda.chunk_fwd_schedule(1 << 20, 1, 2, 128, 128, bf)
+    assert not s["fused"] and s["seg_len"] > 0 and s["kernels"] == 5
+    lengths = syn.seq_lengths(syn.VARLEN_32, 1)
+    s = kda.chunk_fwd_schedule(sum(lengths), 32, 32, 128, 128, bf, syn.cu_seqlens_of(lengths))
+    assert s == {"fused": False, "own_chunks": 0, "seg_len": 0, "kernels": 3}
+    # the fp32 path and the softplus gate never take the tensor-core schedules
+    assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, torch.float32)["kernels"] == 3
+    assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, bf, gate="softplus")["kernels"] == 3
