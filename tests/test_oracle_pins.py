@@ -321,6 +321,31 @@ def test_chunked_at_gate_floor_64():
     assert np.linalg.norm(oc - o) <= 1e-10 * np.linalg.norm(o)
 
 
+def test_chunked_with_slow_decay_and_correlated_keys():
+    """The chunked form far from the identity:
+    - slow decays, g about -0.05;
+    - keys sharing a common direction, so the strictly lower L of a 64-token chunk has a spectral
+      norm of several units.
+    It still equals the token recurrence; the UT transform's solve is exact algebra, not a series."""
+    rng = np.random.default_rng(23)
+    T, dk, dv = 200, 32, 16
+    base = rng.normal(size=dk)
+    k = rng.normal(size=(T, dk)) + 1.5 * base
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    q = rng.normal(size=(T, dk))
+    v = rng.normal(size=(T, dv))
+    beta = 1.0 / (1.0 + np.exp(-rng.normal(size=T)))
+    g = -0.05 * rng.uniform(0.5, 1.5, size=(T, dk))
+    S0 = rng.normal(0, 0.1, size=(dk, dv))
+    G = np.cumsum(g[:64], axis=0)
+    L = beta[:64, None] * np.einsum("rc,ic,ric->ri", k[:64], k[:64], np.exp(G[:, None, :] - G[None, :, :]))
+    assert np.linalg.norm(np.tril(L, -1), 2) > 2.0  # the stress is real
+    o, S = R.recurrence(q, k, v, g, beta, S0)
+    oc, Sc = R.chunked(q, k, v, g, beta, S0, C=64)
+    assert np.linalg.norm(oc - o) <= 1e-10 * np.linalg.norm(o)
+    assert np.linalg.norm(Sc - S) <= 1e-10 * np.linalg.norm(S)
+
+
 # ----------------------------------------------------------------------------- KCP (Eq. 17)
 
 def test_segment_composition_equals_one_pass():
