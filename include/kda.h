@@ -200,7 +200,7 @@ typedef struct {
     const float *A_log;            /* [H] or NULL */
     float g_min, scale;            /* as kda_recurrent_step */
     float *state;                  /* [num_slots, H, dk, dv] committed states, updated in place */
-    const int32_t *state_indices;  /* [N] slot of each sequence, or NULL (slot n) */
+    const int32_t *state_indices;  /* [N] slot of each sequence, or NULL (slot n); distinct slots */
     int64_t num_slots;             /* 0 = N */
     void *o;                       /* [N, M, H, dv] outputs of the new tokens */
     int32_t gate_kind;             /* kda_gate_kind_t (0: Eq. 5) */
@@ -329,7 +329,8 @@ typedef struct {
     const float *A_log;            /* [H] or NULL */
     float g_min, scale;
     float *state;                  /* [num_slots, H, dk, dv] fp32, read and written in place */
-    const int32_t *state_indices;  /* [N] state slot of each sequence, or NULL (slot = n) */
+    const int32_t *state_indices;  /* [N] state slot of each sequence, or NULL (slot = n); the
+                                      slots must be distinct (two sequences on one slot race) */
     int64_t num_slots;             /* slots in `state` (0 means N) */
     void *o;                       /* [N, H, dv] */
     int32_t gate_kind;             /* kda_gate_kind_t (0: Eq. 5) */
