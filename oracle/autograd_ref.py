@@ -9,8 +9,7 @@ chunking or reordering beyond the definition.  The restatement is pinned against
 ``numpy_ref.recurrence`` (same forward values) and its gradients against central finite
 differences of ``numpy_ref`` (an independent code path) in the CPU tests.
 
-Only the tests, the package smoke check and the benchmark's CPU leg import this module; the CUDA
-path never does.
+Only the tests and the package smoke check import this module; the CUDA path never does.
 """
 from __future__ import annotations
 
