@@ -662,3 +662,48 @@ def test_gradients_beta_zero_closed_form():
     for t in range(6):
         np.testing.assert_allclose(gr["dq"][t], sc * (np.exp(G[t])[:, None] * c["S0"]) @ c["do"][t], rtol=1e-13, atol=1e-14)
     assert np.all(gr["dk"] == 0) and np.all(gr["dv"] == 0)
+
+
+@pytest.mark.parametrize("gate_kind", ["lower_bound", "softplus"])
+def test_packed_gradients_sum_gate_parameters_over_sequences(gate_kind):
+    """The packed driver ``backward`` (several sequences, several heads): dt_bias and A_log are shared
+    by every sequence of a head, so their gradients are sums over sequences; every other gradient
+    belongs to one (token, head) or one (sequence, head).  All of them against central differences
+    of the packed NumPy forward (``numpy_ref.forward``, an independent code path), on a batch with an
+    empty sequence, so that a per-sequence (rather than summed) or per-head-mixed packing fails."""
+    rng = np.random.default_rng(43)
+    lengths, H, dk, dv = [3, 0, 4, 2], 2, 3, 2
+    T, N = sum(lengths), len(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    k = rng.normal(size=(T, H, dk))
+    k /= np.linalg.norm(k, axis=2, keepdims=True)
+    c = dict(q=rng.normal(size=(T, H, dk)), k=k, v=rng.normal(size=(T, H, dv)), z=rng.normal(0, 1.5, size=(T, H, dk)),
+             beta=rng.uniform(0.1, 0.9, size=(T, H)), dt_bias=rng.uniform(-1, 1, size=(H, dk)),
+             A_log=rng.normal(0, 0.3, size=H), S0=rng.normal(0, 0.3, size=(N, H, dk, dv)))
+    do, dST = rng.normal(size=(T, H, dv)), rng.normal(size=(N, H, dk, dv))
+
+    def loss(cc):
+        o, S = R.forward(cc["q"], cc["k"], cc["v"], cc["z"], cc["beta"], cc["dt_bias"], cc["A_log"], cu, S0=cc["S0"],
+                         g_min=G_MIN, scale=0.8, gate_kind=gate_kind)
+        return float(np.sum(o * do) + np.sum(S * dST))
+
+    gr = AG.backward(c["q"], c["k"], c["v"], c["z"], c["beta"], c["dt_bias"], c["A_log"], cu, do, S0=c["S0"],
+                     dST=dST, g_min=G_MIN, scale=0.8, gate_kind=gate_kind)
+    h = 1e-5
+    for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("z", "dz"), ("beta", "dbeta"),
+                        ("dt_bias", "ddt_bias"), ("A_log", "dA_log"), ("S0", "dS0")):
+        x0 = np.array(c[name], dtype=np.float64)
+        fd = np.zeros_like(x0)
+        for idx in np.ndindex(x0.shape):
+            for sgn in (1.0, -1.0):
+                cc = dict(c)
+                cc[name] = x0.copy()
+                cc[name][idx] += sgn * h
+                fd[idx] += sgn * loss(cc) / (2 * h)
+        np.testing.assert_allclose(gr[gname], fd, rtol=1e-6, atol=1e-8, err_msg=name)
+    # the shared parameters really are sums: each differs from every single sequence's share
+    per_seq = [AG.head_backward(c["q"][a:b, 0], c["k"][a:b, 0], c["v"][a:b, 0], c["z"][a:b, 0], c["beta"][a:b, 0],
+                                c["dt_bias"][0], c["A_log"][0], c["S0"][n, 0], do[a:b, 0], dST[n, 0], G_MIN, 0.8,
+                                gate_kind)["dA_log"] for n, (a, b) in enumerate(zip(cu[:-1], cu[1:]))]
+    assert gr["dA_log"][0] == pytest.approx(sum(per_seq), rel=1e-12)
+    assert all(abs(gr["dA_log"][0] - s) > 1e-6 for s in per_seq if s != 0)
