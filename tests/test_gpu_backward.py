@@ -66,10 +66,12 @@ def _compare(d, got, ref, tol):
                 e = rel_err(x, r)
                 assert np.isfinite(e) and e <= tol, f"d{nm} (seq {n}, head {h}): rel err {e:.3g} > {tol}"
                 worst[nm] = max(worst.get(nm, 0.0), e)
+    # the shared gate parameters: per head (dt_bias row h, A_log[h]), each summed over the sequences
     for nm, rn in (("dt_bias", "ddt_bias"), ("A_log", "dA_log")):
-        e = rel_err(got[nm], ref[rn])
-        assert e <= tol, f"d{nm}: rel err {e:.3g} > {tol}"
-        worst[nm] = e
+        for h in range(H):
+            e = rel_err(np.atleast_1d(got[nm][h]), np.atleast_1d(ref[rn][h]))
+            assert e <= tol, f"d{nm} (head {h}): rel err {e:.3g} > {tol}"
+            worst[nm] = max(worst.get(nm, 0.0), e)
     return worst
 
 
