@@ -1676,7 +1676,18 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
         !make_tile_map(&omap, a->o, a->T, p.H))
         return KDA_ERR_CUDA;
     kda_profile_mark(0, stream);
-    if (p.fused && p.max_chunks > 0 && a->T > 0 && launch_fused(a, p, ws, stream, tm, omap, sms, err)) {
+    // The fused launch publishes packets through flags tagged with a host-side epoch.  A captured
+    // graph would replay one fixed epoch against flags its previous replay left in the same
+    // workspace, so under stream capture (or when the capture state cannot be read) the flag-free
+    // separate kernels run instead.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        (void)cudaGetLastError();
+        cap = cudaStreamCaptureStatusActive;
+    }
+    const bool capturing = cap != cudaStreamCaptureStatusNone;
+    if (p.fused && !capturing && p.max_chunks > 0 && a->T > 0 &&
+        launch_fused(a, p, ws, stream, tm, omap, sms, err)) {
         kda_profile_mark(1, stream);
         return kda_cuda_status(cudaGetLastError());
     }
