@@ -48,7 +48,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
 
-#define KDA_ABI_VERSION 3
+#define KDA_ABI_VERSION 4
 
 typedef enum {
     KDA_OK = 0,
@@ -62,7 +62,8 @@ typedef enum {
     KDA_ERR_BAD_STATE_INDEX = 8,   /* (device) state_indices entry outside [0, num_slots) */
     KDA_ERR_NO_DEVICE = 9,         /* no current CUDA device of compute capability 10.3 */
     KDA_ERR_DEVICE_TIMEOUT = 10,   /* (device) a bounded wait inside a kernel gave up */
-    KDA_ERR_BAD_TOKEN_COUNT = 11   /* (device) n_replay / n_commit entry outside its range */
+    KDA_ERR_BAD_TOKEN_COUNT = 11,  /* (device) n_replay / n_commit entry outside its range */
+    KDA_ERR_NUMERIC = 12           /* (device, debug checks only) an output holds a NaN or an infinity */
 } kda_status_t;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
@@ -161,7 +162,13 @@ size_t kda_chunk_fwd_workspace_size_gate(int64_t T, int64_t N, int32_t H, int32_
 
 /* workspace: device memory of at least kda_chunk_fwd_workspace_size() bytes,
  * 256-byte aligned, owned by the caller; its contents need no initialisation
- * and are garbage afterwards.  Calls that share a workspace must not overlap. */
+ * and are garbage afterwards.  Calls that share a workspace must not overlap.
+ * Stream capture: the fused schedule (kda_chunk_fwd_schedule out[0] = 1)
+ * publishes its per-chunk work through flags tagged with a per-call counter
+ * kept on the host, which a captured graph would freeze; a call made while
+ * `stream` is being captured therefore runs the flag-free separate kernels
+ * (same results, more launches), and its graph may be replayed with new
+ * contents in the same buffers. */
 kda_status_t kda_chunk_fwd(const kda_chunk_args *args, void *workspace, size_t workspace_bytes,
                            struct CUstream_st *stream);
 
@@ -296,13 +303,18 @@ kda_status_t kda_output_gate(const kda_output_gate_args *args, struct CUstream_s
  * KDA_STATIC_WORKSPACE_BYTES that lives inside the library (a file-scope
  * device array, held by every GPU that loads the library until the process
  * exits).  The caller still owns and passes every input and output.
- *   - Limit: problems whose kda_chunk_fwd_workspace_size() exceeds
- *     KDA_STATIC_WORKSPACE_BYTES are rejected with KDA_ERR_WORKSPACE before
- *     anything is launched (bf16 with d = 128 needs about 74 KiB per chunk of
- *     64 tokens per head, so e.g. T = 4096 tokens with 13 heads fit).
+ *   - Limit: problems whose kda_chunk_fwd_workspace_size_gate() for their
+ *     gate kind exceeds KDA_STATIC_WORKSPACE_BYTES are rejected with
+ *     KDA_ERR_WORKSPACE before anything is launched.  The limit depends on the
+ *     gate kind and the dtype: with the bounded gate, bf16 at d = 128 needs
+ *     about 73 KiB per chunk of 64 tokens per head (T = 4096 tokens with 13
+ *     heads fit); the softplus gate and fp32 I/O take the fp32 path, about
+ *     145 KiB per chunk and head at d = 128 (T = 4096 tokens with 7 heads fit).
  *   - Set-up: the first call on each device, made while that device is
- *     current, looks up the buffer's device address; make that first call
- *     before any stream capture.
+ *     current, looks up the buffer's device address and keeps it for the
+ *     life of the process; make that first call before any stream capture.
+ *     A device reset (cudaDeviceReset) invalidates the kept address (and the
+ *     library's device error word): do not call the library across one.
  *   - Sharing: every call on a device uses the same buffer, which keeps the
  *     last call's contents.  Calls whose GPU work overlaps in time (different
  *     streams, or different host threads) race on it and give wrong results:
@@ -352,6 +364,18 @@ int32_t kda_last_cuda_error(void);
 
 int kda_abi_version(void);
 
+/* ------------------------------------------------------------- debug checks
+ * Not an operation of the paper: optional checks for debugging a model.  With KDA_CHECK_FINITE set,
+ * every entry point that writes results (kda_gate, kda_chunk_fwd and kda_chunk_fwd_static_ws,
+ * kda_recurrent_step, kda_recurrent_replay, kda_output_gate, kda_chunk_bwd) launches one more pass
+ * over what it wrote (outputs, final or updated states, gradients) that sets KDA_ERR_NUMERIC in the
+ * device error word (kda_get_device_error) when any value is NaN or infinite.  The pass reads those
+ * results once more from HBM.  Index checks need no switch: cu_seqlens contents, state indices and
+ * replay counts are always checked on the device.  Process-wide; 0 (the default) turns the checks
+ * off.  KDA_ERR_INVALID_ARG for an unknown flag. */
+#define KDA_CHECK_FINITE 1
+kda_status_t kda_set_debug_checks(int32_t flags);
+
 /* ------------------------------------------------------------ instrumentation
  * Optional per-kernel timing.  While set (n_events > 0), kda_chunk_fwd records
  * events[0] on its stream before its first kernel and events[i] right after its
@@ -369,8 +393,8 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *args);
  * entries): out[0] = 1 for the fused launch (intra-chunk transform and output
  * pass in one cooperative kernel), else 0; out[1] = chunks at the start of every
  * sequence that its own output-pass CTAs produce in the fused launch; out[2] =
- * segment length in chunks of the split-sequence state pass (section 5.1.2,
- * Eq. 17 of the Kimi Linear report), 0 when the pass does not run; out[3] =
+ * segment length in chunks of the split-sequence state pass (the Kimi K3
+ * report, section 5.1.2, Eq. 17), 0 when the pass does not run; out[3] =
  * kernels launched.  KDA_ERR_INVALID_ARG on NULL pointers or invalid sizes. */
 kda_status_t kda_chunk_fwd_schedule(const kda_chunk_args *args, int64_t *out);
 

@@ -3,6 +3,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -13,7 +15,7 @@ static __device__ int g_kda_device_error;
 namespace {
 
 constexpr int kMaxDevices = 64;
-int *g_err_ptr[kMaxDevices];  // device address of g_kda_device_error, per device
+std::atomic<int *> g_err_ptr[kMaxDevices];  // device address of g_kda_device_error, per device
 
 // gate_kind is a kda_gate_kind_t; g_min matters (finite, < 0) for the bounded gate only
 bool gate_ok(int32_t kind, float g_min) {
@@ -52,12 +54,14 @@ void kda_profile_mark(int i, cudaStream_t stream) {
 int *kda_device_error_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!g_err_ptr[dev]) {
+    int *e = g_err_ptr[dev].load(std::memory_order_acquire);
+    if (!e) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_kda_device_error) != cudaSuccess) return nullptr;
-        g_err_ptr[dev] = (int *)p;
+        e = (int *)p;
+        g_err_ptr[dev].store(e, std::memory_order_release);
     }
-    return g_err_ptr[dev];
+    return e;
 }
 
 static thread_local int g_last_cuda_error = 0;
@@ -121,6 +125,7 @@ const char *kda_status_string(kda_status_t s) {
         case KDA_ERR_NO_DEVICE: return "no current CUDA device of compute capability 10.3";
         case KDA_ERR_DEVICE_TIMEOUT: return "bounded wait inside a kernel gave up";
         case KDA_ERR_BAD_TOKEN_COUNT: return "n_replay or n_commit entry outside its range";
+        case KDA_ERR_NUMERIC: return "an output holds a NaN or an infinity (debug checks)";
     }
     return "unknown status";
 }
@@ -161,7 +166,10 @@ kda_status_t kda_gate(const kda_gate_args *a, struct CUstream_st *stream) {
         return KDA_ERR_MISALIGNED;
     kda_status_t st = check_device();
     if (st != KDA_OK) return st;
-    return kda_launch_gate(a, (cudaStream_t)stream);
+    st = kda_launch_gate(a, (cudaStream_t)stream);
+    if (st == KDA_OK && (kda_debug_flags() & KDA_CHECK_FINITE))
+        st = kda_check_finite(a->out, a->T * a->H * (int64_t)a->dk, KDA_F32, (cudaStream_t)stream);
+    return st;
 }
 
 static kda_status_t validate_chunk(const kda_chunk_args *a) {
@@ -232,12 +240,20 @@ kda_status_t kda_chunk_fwd(const kda_chunk_args *a, void *workspace, size_t work
     if (st != KDA_OK) return st;
     st = p.path == 1 ? kda_launch_chunk_tc(a, p, workspace, (cudaStream_t)stream)
                      : kda_launch_chunk_simt(a, p, workspace, (cudaStream_t)stream);
-    if (st != KDA_OK || !a->out_gate) return st;
-    // the output epilogue runs as its own HBM-bound pass over o, in place, on all SMs (inside the
-    // output pass it would lengthen the latency-bound chain more than the round trip of o costs)
-    kda_output_gate_args og{a->T, a->H, a->dv, a->dtype, a->o, a->out_gate, a->out_norm_weight,
-                            a->out_norm_eps, a->o};
-    return kda_launch_output_gate(&og, (cudaStream_t)stream);
+    if (st == KDA_OK && a->out_gate) {
+        // the output epilogue runs as its own HBM-bound pass over o, in place, on all SMs (inside the
+        // output pass it would lengthen the latency-bound chain more than the round trip of o costs)
+        kda_output_gate_args og{a->T, a->H, a->dv, a->dtype, a->o, a->out_gate, a->out_norm_weight,
+                                a->out_norm_eps, a->o};
+        st = kda_launch_output_gate(&og, (cudaStream_t)stream);
+    }
+    if (st == KDA_OK && (kda_debug_flags() & KDA_CHECK_FINITE)) {
+        st = kda_check_finite(a->o, a->T * a->H * (int64_t)a->dv, a->dtype, (cudaStream_t)stream);
+        if (st == KDA_OK)
+            st = kda_check_finite(a->final_state, a->N * a->H * (int64_t)a->dk * a->dv, KDA_F32,
+                                  (cudaStream_t)stream);
+    }
+    return st;
 }
 
 size_t kda_chunk_bwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
@@ -289,7 +305,18 @@ kda_status_t kda_chunk_bwd(const kda_chunk_bwd_args *a, void *workspace, size_t 
     if (!aligned_to(workspace, 256)) return KDA_ERR_MISALIGNED;
     kda_status_t st = check_device();
     if (st != KDA_OK) return st;
-    return kda_launch_chunk_bwd(a, workspace, workspace_bytes, (cudaStream_t)stream);
+    st = kda_launch_chunk_bwd(a, workspace, workspace_bytes, (cudaStream_t)stream);
+    if (st == KDA_OK && (kda_debug_flags() & KDA_CHECK_FINITE)) {
+        const int64_t tk = a->T * a->H * (int64_t)a->dk, tv = a->T * a->H * (int64_t)a->dv;
+        const struct { const void *p; int64_t n; kda_dtype_t t; } outs[] = {
+            {a->grad_q, tk, a->dtype}, {a->grad_k, tk, a->dtype}, {a->grad_z, tk, a->dtype},
+            {a->grad_v, tv, a->dtype}, {a->grad_beta, a->T * a->H, a->dtype},
+            {a->grad_dt_bias, (int64_t)a->H * a->dk, KDA_F32}, {a->grad_A_log, a->H, KDA_F32},
+            {a->grad_initial_state, a->N * a->H * (int64_t)a->dk * a->dv, KDA_F32}};
+        for (const auto &x : outs)
+            if (st == KDA_OK && aligned16(x.p)) st = kda_check_finite(x.p, x.n, x.t, (cudaStream_t)stream);
+    }
+    return st;
 }
 
 kda_status_t kda_output_gate(const kda_output_gate_args *a, struct CUstream_st *stream) {
@@ -306,7 +333,10 @@ kda_status_t kda_output_gate(const kda_output_gate_args *a, struct CUstream_st *
         return KDA_ERR_MISALIGNED;
     kda_status_t st = check_device();
     if (st != KDA_OK) return st;
-    return kda_launch_output_gate(a, (cudaStream_t)stream);
+    st = kda_launch_output_gate(a, (cudaStream_t)stream);
+    if (st == KDA_OK && (kda_debug_flags() & KDA_CHECK_FINITE))
+        st = kda_check_finite(a->y, a->T * a->H * (int64_t)a->dv, a->dtype, (cudaStream_t)stream);
+    return st;
 }
 
 kda_status_t kda_recurrent_step(const kda_step_args *a, struct CUstream_st *stream) {
@@ -326,7 +356,14 @@ kda_status_t kda_recurrent_step(const kda_step_args *a, struct CUstream_st *stre
         return KDA_ERR_MISALIGNED;
     kda_status_t st = check_device();
     if (st != KDA_OK) return st;
-    return kda_launch_decode(a, (cudaStream_t)stream);
+    st = kda_launch_decode(a, (cudaStream_t)stream);
+    if (st == KDA_OK && (kda_debug_flags() & KDA_CHECK_FINITE)) {
+        const int64_t slots = a->num_slots ? a->num_slots : a->N;
+        st = kda_check_finite(a->o, a->N * a->H * (int64_t)a->dv, a->dtype, (cudaStream_t)stream);
+        if (st == KDA_OK)
+            st = kda_check_finite(a->state, slots * a->H * (int64_t)a->dk * a->dv, KDA_F32, (cudaStream_t)stream);
+    }
+    return st;
 }
 
 kda_status_t kda_recurrent_replay(const kda_replay_args *a, struct CUstream_st *stream) {
@@ -354,7 +391,14 @@ kda_status_t kda_recurrent_replay(const kda_replay_args *a, struct CUstream_st *
         return KDA_ERR_MISALIGNED;
     kda_status_t st = check_device();
     if (st != KDA_OK) return st;
-    return kda_launch_replay(a, (cudaStream_t)stream);
+    st = kda_launch_replay(a, (cudaStream_t)stream);
+    if (st == KDA_OK && (kda_debug_flags() & KDA_CHECK_FINITE)) {
+        const int64_t slots = a->num_slots ? a->num_slots : a->N;
+        st = kda_check_finite(a->o, a->N * (int64_t)a->M * a->H * a->dv, a->dtype, (cudaStream_t)stream);
+        if (st == KDA_OK)
+            st = kda_check_finite(a->state, slots * a->H * (int64_t)a->dk * a->dv, KDA_F32, (cudaStream_t)stream);
+    }
+    return st;
 }
 
 }  // extern "C"

@@ -10,6 +10,11 @@ void kda_profile_mark(int i, cudaStream_t stream);
 // KDA_OK for cudaSuccess; otherwise records the code for kda_last_cuda_error() and returns KDA_ERR_CUDA.
 kda_status_t kda_cuda_status(cudaError_t e);
 
+// Debug checks (kda_set_debug_checks): the flags in force, and the scan that sets KDA_ERR_NUMERIC in
+// the device error word when [p, p + n) holds a NaN or an infinity (p 16-byte aligned).
+int32_t kda_debug_flags();
+kda_status_t kda_check_finite(const void *p, int64_t n, kda_dtype_t dtype, cudaStream_t stream);
+
 kda_status_t kda_launch_gate(const kda_gate_args *a, cudaStream_t stream);
 kda_status_t kda_launch_output_gate(const kda_output_gate_args *a, cudaStream_t stream);
 kda_status_t kda_launch_decode(const kda_step_args *a, cudaStream_t stream);

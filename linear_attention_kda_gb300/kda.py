@@ -25,13 +25,14 @@ _STATUS = {
     3: "KDA_ERR_UNSUPPORTED_DTYPE", 4: "KDA_ERR_MISALIGNED", 5: "KDA_ERR_WORKSPACE",
     6: "KDA_ERR_CUDA", 7: "KDA_ERR_BAD_SEQLENS", 8: "KDA_ERR_BAD_STATE_INDEX",
     9: "KDA_ERR_NO_DEVICE", 10: "KDA_ERR_DEVICE_TIMEOUT", 11: "KDA_ERR_BAD_TOKEN_COUNT",
+    12: "KDA_ERR_NUMERIC",
 }
 EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step",
             "kda_status_string", "kda_get_device_error", "kda_abi_version",
             "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws",
             "kda_last_cuda_error", "kda_chunk_fwd_schedule", "kda_output_gate", "kda_recurrent_replay",
             "kda_chunk_fwd_workspace_size_gate", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size",
-            "kda_selftest_bounded_wait"]
+            "kda_selftest_bounded_wait", "kda_set_debug_checks"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 _vp = ctypes.c_void_p
@@ -132,6 +133,8 @@ def load_library(path: Optional[str] = None):
         L.kda_chunk_fwd_schedule.restype = ctypes.c_int
         L.kda_chunk_fwd_static_ws.argtypes = [ctypes.POINTER(ChunkArgs), _vp]
         L.kda_chunk_fwd_static_ws.restype = ctypes.c_int
+        L.kda_set_debug_checks.argtypes = [_i32]
+        L.kda_set_debug_checks.restype = ctypes.c_int
         L.kda_recurrent_replay.argtypes = [ctypes.POINTER(ReplayArgs), _vp]
         L.kda_recurrent_replay.restype = ctypes.c_int
         L.kda_output_gate.argtypes = [ctypes.POINTER(OutputGateArgs), _vp]
@@ -354,6 +357,15 @@ def get_device_error(device=None) -> int:
     """Waits for the current stream and returns (and clears) the device error code (0 = none)."""
     L = load_library()
     return int(L.kda_get_device_error(torch.cuda.current_stream(device).cuda_stream))
+
+
+CHECK_FINITE = 1
+
+
+def set_debug_checks(flags: int) -> None:
+    """kda_set_debug_checks: with CHECK_FINITE, every entry point scans what it wrote and sets
+    KDA_ERR_NUMERIC (read with get_device_error) on a NaN or an infinity; 0 turns the checks off."""
+    _check(load_library().kda_set_debug_checks(int(flags)), "kda_set_debug_checks")
 
 
 def status_string(code: int) -> str:

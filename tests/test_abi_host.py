@@ -46,7 +46,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.kda_abi_version() == 3
+    assert lib.kda_abi_version() == 4
     for code, name in kda._STATUS.items():
         s = lib.kda_status_string(code).decode()
         assert s and s != "unknown status", name
@@ -341,6 +341,13 @@ def test_empty_batch_plan(lib):
     assert lib.kda_chunk_fwd_kernel_count(ctypes.byref(a)) == 2
     # the same sizes with tokens run three kernels on the fp32 path (plan, intra, output pass)
     assert kda.chunk_fwd_schedule(640, 3, 32, 64, 64, torch.float32)["kernels"] == 3
+
+
+def test_debug_checks_flags(lib):
+    assert lib.kda_set_debug_checks(2) == 1  # unknown flag: KDA_ERR_INVALID_ARG
+    assert lib.kda_set_debug_checks(-1) == 1
+    assert lib.kda_set_debug_checks(1) == 0
+    assert lib.kda_set_debug_checks(0) == 0
 
 
 def test_profile_events_validation_and_last_cuda_error(lib):

@@ -587,3 +587,73 @@ def test_bounded_wait_gives_up_and_context_stays_usable():
     d = syn.make_prefill(syn.TINY_F32, seed=0)
     o, fs = run_prefill(d)
     compare_prefill(d, o, fs, oracle_prefill(d), TOL_F32)
+
+
+def test_captured_graph_replays_with_new_inputs():
+    """kda_chunk_fwd captured in a CUDA graph, then replayed twice with new contents written into the
+    same input buffers: each replay must match the oracle on its own inputs.  Uncaptured, this
+    workload takes the fused schedule, whose packet flags carry a per-call host counter; the
+    captured call must not depend on it (it runs the flag-free kernels)."""
+    w = syn.PREFILL_4K
+    ds = [syn.make_prefill(w, seed=s) for s in (11, 12)]
+    T, H, D = sum(ds[0]["lengths"]), w.H, w.d
+    cu_host = ds[0]["cu_seqlens"]
+    assert kda.chunk_fwd_schedule(T, 1, H, D, D, torch.bfloat16, cu_host)["fused"]
+    names = ("q", "k", "v", "z", "beta", "dt_bias", "A_log")
+    buf = {n: ds[0][n].cuda() for n in names}
+    cu = cu_host.cuda()
+    o = torch.empty_like(buf["v"])
+    fs = torch.empty((1, H, D, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty((kda.chunk_fwd_workspace_size(T, 1, H, D, D, torch.bfloat16, 64, cu_host),),
+                     dtype=torch.uint8, device="cuda")
+
+    def call():
+        kda.chunk_fwd(*(buf[n] for n in names), g_min=ds[0]["g_min"], scale=ds[0]["scale"], cu_seqlens=cu,
+                      cu_seqlens_host=cu_host, final_state=fs, workspace=ws, out=o)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for d in ds + ds[:1]:
+        for n in names:
+            buf[n].copy_(d[n])
+        graph.replay()
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        worst = compare_prefill(d, o.float().cpu(), fs.cpu(), oracle_prefill(d, heads=None), TOL_BF16)
+        assert worst < TOL_BF16
+
+
+def test_debug_checks_report_non_finite_outputs():
+    """kda_set_debug_checks(KDA_CHECK_FINITE): a NaN in one value vector reaches that head's outputs
+    and state, and the check pass reports KDA_ERR_NUMERIC; clean inputs report nothing, and with the
+    checks off nothing is reported either."""
+    w = syn.Workload("dbg", H=2, d=64, dtype="f32", n_seq=1, seq_len=100, z_std=1.5, b_range=1.0,
+                     alog_std=0.25)
+    d = syn.make_prefill(w, seed=61)
+    try:
+        kda.set_debug_checks(kda.CHECK_FINITE)
+        run_prefill(d)  # asserts no device error
+        d["v"][37, 1, 5] = float("nan")
+        o, fs = kda.chunk_fwd(*(d[n].cuda() for n in ("q", "k", "v", "z", "beta", "dt_bias", "A_log")),
+                              cu_seqlens=d["cu_seqlens"].cuda(), output_final_state=True)
+        assert kda.get_device_error() == 12  # KDA_ERR_NUMERIC
+        assert not torch.isfinite(fs[0, 1]).all() and torch.isfinite(fs[0, 0]).all()
+        st = torch.zeros((3, 2, 64, 64), device="cuda")
+        tok = lambda: torch.randn((3, 2, 64), device="cuda")  # noqa: E731
+        kda.recurrent_step(tok(), tok(), tok(), tok(), torch.rand((3, 2), device="cuda"), None, None, st)
+        assert kda.get_device_error() == 0
+        st[1, 0, 3, 3] = float("inf")
+        kda.recurrent_step(tok(), tok(), tok(), tok(), torch.rand((3, 2), device="cuda"), None, None, st)
+        assert kda.get_device_error() == 12
+    finally:
+        kda.set_debug_checks(0)
+    kda.chunk_fwd(*(d[n].cuda() for n in ("q", "k", "v", "z", "beta", "dt_bias", "A_log")),
+                  cu_seqlens=d["cu_seqlens"].cuda(), output_final_state=True)
+    assert kda.get_device_error() == 0
