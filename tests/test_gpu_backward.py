@@ -66,19 +66,43 @@ def _compare(d, got, ref, tol):
                 e = rel_err(x, r)
                 assert np.isfinite(e) and e <= tol, f"d{nm} (seq {n}, head {h}): rel err {e:.3g} > {tol}"
                 worst[nm] = max(worst.get(nm, 0.0), e)
-    # the shared gate parameters: per head (dt_bias row h, A_log[h]), each summed over the sequences
-    for nm, rn in (("dt_bias", "ddt_bias"), ("A_log", "dA_log")):
-        for h in range(H):
-            e = rel_err(np.atleast_1d(got[nm][h]), np.atleast_1d(ref[rn][h]))
-            assert e <= tol, f"d{nm} (head {h}): rel err {e:.3g} > {tol}"
-            worst[nm] = max(worst.get(nm, 0.0), e)
+    # the shared gate parameters, per head, each a sum over every token of every sequence
+    sb, sa = gate_param_scales(ref["dz"], d["z"], d["dt_bias"], d["A_log"], d.get("gate", "lower_bound"))
+    for h in range(H):
+        eb = float(np.linalg.norm(got["dt_bias"][h] - ref["ddt_bias"][h])) / float(np.linalg.norm(sb[h]))
+        ea = abs(float(got["A_log"][h]) - float(ref["dA_log"][h])) / float(sa[h])
+        assert eb <= tol, f"d dt_bias (head {h}): error {eb:.3g} of the terms' magnitude > {tol}"
+        assert ea <= tol, f"d A_log (head {h}): error {ea:.3g} of the terms' magnitude > {tol}"
+        worst["dt_bias"] = max(worst.get("dt_bias", 0.0), eb)
+        worst["A_log"] = max(worst.get("A_log", 0.0), ea)
     return worst
+
+
+def gate_param_scales(dz, z, dt_bias, A_log, gate):
+    """Magnitudes against which the dt_bias and A_log gradients of each head are measured.
+
+    Both gates are functions of x = z + b, so d/db = sum_t dz_t exactly, and d/dA_log = sum_t,c dz w
+    with w = z + b for Eq. 5 (g = g_min Sigmoid(e^A x): dg/dA = x dg/dz) and w = Softplus(x) / Sigmoid(x)
+    for the softplus gate (g = -e^A Softplus(x): dg/dA = g, dg/dz = -e^A Sigmoid(x)).  These sums can
+    cancel to a tiny fraction of their terms (a ratio near 3000 occurs in the fp32 varlen case), and
+    a cancelling sum has no meaningful relative error of its own: its error is bounded by the
+    tolerance times the sum of the terms' magnitudes.  Returns ([H, d_k] per-channel sum_t |dz|,
+    [H] sum_t,c |dz w|) from the fp64 reference dz."""
+    f = lambda t: t.double().numpy() if isinstance(t, torch.Tensor) else np.asarray(t, np.float64)  # noqa: E731
+    dz = f(dz)
+    x = f(z) + f(dt_bias)[None]
+    if gate == "softplus":
+        w = np.logaddexp(0.0, x) * (1.0 + np.exp(-x))
+    else:
+        w = x
+    return np.abs(dz).sum(0), np.abs(dz * w).sum((0, 2))
 
 
 @pytest.mark.parametrize("gate", ["lower_bound", "softplus"])
 def test_chunk_bwd_f32_varlen_matches_exact_gradients(gate):
     """Ragged batch (1, 63, 64, 65, 130 and an empty sequence) with initial and final state gradients."""
     d = _inputs(2, 64, "f32", [1, 63, 64, 65, 130, 0], seed=51)
+    d["gate"] = gate
     _compare(d, _run(d, gate), _ref(d, gate), TOL_F32)
 
 
@@ -128,8 +152,10 @@ def test_chunk_bwd_full_prefill_workload_sampled_heads():
         for nm in ("q", "k", "v", "z", "beta"):
             assert rel_err(got[nm][:, h], r["d" + nm]) <= TOL_BF16, (nm, h)
         assert rel_err(got["initial_state"][0, h], r["dS0"]) <= TOL_BF16, h
-        assert rel_err(got["dt_bias"][h], r["db"]) <= TOL_BF16, h
-        assert abs(got["A_log"][h] - r["dA_log"]) <= TOL_BF16 * max(1.0, abs(r["dA_log"])), h
+        sb, sa = gate_param_scales(r["dz"][:, None], f(dd["z"][:, h])[:, None], f(dd["dt_bias"][h])[None],
+                                   None, "lower_bound")
+        assert np.linalg.norm(got["dt_bias"][h] - r["db"]) <= TOL_BF16 * np.linalg.norm(sb[0]), h
+        assert abs(got["A_log"][h] - r["dA_log"]) <= TOL_BF16 * sa[0], h
 
 
 def test_chunk_bwd_empty_batch():
