@@ -91,8 +91,8 @@ def chunk_lengths_count(lengths, C=64):
 
 def kernel_names(sch, nk):
     """Names of the kernels kda_chunk_fwd launches under schedule `sch` (kda_chunk_fwd_schedule)."""
-    if sch.get("persistent"):
-        return ["chunk_persist"][:nk] + ["output_gate"] * (nk - 1)
+    if sch.get("team"):
+        return ["chunk_team"] + ["output_gate"] * (nk - 1)
     if sch["fused"]:
         return ["chunk_fused"] + ["output_gate"] * (nk - 1)
     base = ["chunk_plan", "chunk_intra"] + (["chunk_segsum", "chunk_fold"] if sch["seg_len"] else []) + ["chunk_inter"]
@@ -100,8 +100,8 @@ def kernel_names(sch, nk):
 
 
 def schedule_name(sch):
-    if sch.get("persistent"):
-        return "persistent fused (chains from a queue, producers a bounded window ahead)"
+    if sch.get("team"):
+        return "chain teams (1 chain CTA + %d producer CTAs each, producers a bounded window ahead)" % sch["team_producers"]
     if sch["fused"]:
         return "fused"
     return "split state pass, %d chunks per segment" % sch["seg_len"] if sch["seg_len"] else "separate kernels"
@@ -431,7 +431,7 @@ def run_ours(args, rank, ws, local):
     kern_avg = [sum(x) / len(x) for x in kern_ms]
     names = kernel_names(sch, nk)
     dom = max(range(nk), key=lambda j: kern_avg[j])
-    role = {"chunk_intra": "intra", "chunk_fused": "total", "chunk_persist": "total"}.get(names[dom], "inter")
+    role = {"chunk_intra": "intra", "chunk_fused": "total", "chunk_team": "total"}.get(names[dom], "inter")
     bytes_dom, flops_dom = by[role], fl[role]
     t_dom = kern_avg[dom] / 1e3
     # the kernel's algorithmic bound: whichever of its bytes or FLOPs takes longer at peak
@@ -720,13 +720,13 @@ def run_ours(args, rank, ws, local):
             fll = prefill_flops(Ls, H, D, D)
             byl = prefill_bytes(Tl, Nl, H, D, D, 2, dl["initial_state"] is not None, True)
             tfl = fll["total"] / (msl / 1e3) / 1e12
-            sch = kda.chunk_fwd_schedule(Tl, Nl, H, D, D, dl["q"].dtype, cul)
+            sch_l = kda.chunk_fwd_schedule(Tl, Nl, H, D, D, dl["q"].dtype, cul)
             longw[w_.name] = {
                 "tokens": Tl, "sequences": Nl, "ms_per_step": msl, "tokens_per_s": Tl / (msl / 1e3),
                 "tflops": tfl, "tflops_dense_tile": fll["dense_tile"] / (msl / 1e3) / 1e12,
                 "frac_bf16_peak": tfl / tc, "hbm_gbs_algorithmic": byl["total"] / (msl / 1e3) / 1e9,
                 "frac_hbm": byl["total"] / (msl / 1e3) / 1e9 / hbm,
-                "schedule": schedule_name(sch), "kernels": sch["kernels"]}
+                "schedule": schedule_name(sch_l), "kernels": sch_l["kernels"]}
             del dl, fsl, ol, wl
             torch.cuda.empty_cache()
 
@@ -882,6 +882,15 @@ def run_case(args):
                 kda.chunk_fwd(*args_, cu_seqlens=d["cu_seqlens"], output_final_state=True, gate="softplus")
             else:
                 kda.chunk_bwd(*args_, torch.ones_like(d["v"]), cu_seqlens=d["cu_seqlens"])
+    elif args.case == "intra_sep":
+        # 200 sequences x 256 tokens, H = 16 (more sequences than the one-launch schedules take: the
+        # intra-chunk kernel runs alone); inputs 0.84 GB, packets 0.96 GB
+        w = syn.Workload("intra_sep_bf16_N200_T256_H16_d128", H=16, d=128, dtype="bf16", n_seq=200, seq_len=256,
+                         z_std=1.5, b_range=1.0, alog_std=0.25)
+        d = syn.make_prefill(w, seed=1, device=dev)
+        for _ in range(2):
+            kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["dt_bias"], d["A_log"],
+                          cu_seqlens=d["cu_seqlens"], cu_seqlens_host=d["cu_seqlens"].cpu(), output_final_state=True)
     elif args.case in ("prefill_small", "prefill_4k"):
         if args.case == "prefill_small":
             w = syn.Workload("prefill_small_bf16_T16384_H8_d128", H=8, d=128, dtype="bf16", seq_len=16384,
@@ -917,7 +926,7 @@ def main():
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--case", choices=["prefill_small", "prefill_4k", "decode_small", "replay_256", "softplus_4k",
-                                       "backward_4k"], default=None,
+                                       "backward_4k", "intra_sep"], default=None,
                     help="run a small fixed case for profiler captures instead of the benchmark")
     args = ap.parse_args()
     if args.case:

@@ -391,8 +391,11 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *args);
 /* The schedule kda_chunk_fwd picks for these arguments (host only: reads the
  * sizes, dtype and cu_seqlens_host, launches nothing).  out (caller-owned, 4
  * entries): out[0] = 1 for the fused launch (intra-chunk transform and output
- * pass in one cooperative kernel), else 0; out[1] = chunks at the start of every
- * sequence that its own output-pass CTAs produce in the fused launch; out[2] =
+ * pass in one cooperative kernel, one CTA per chain), 2 for the chain-team
+ * launch (one cooperative kernel of teams, each a chain CTA that runs its chains
+ * in turn and out[1] CTAs producing their packets just ahead of it), else 0;
+ * out[1] = chunks at the start of every sequence that its own output-pass CTAs
+ * produce in the fused launch, or producers per team; out[2] =
  * segment length in chunks of the split-sequence state pass (the Kimi K3
  * report, section 5.1.2, Eq. 17), 0 when the pass does not run; out[3] =
  * kernels launched.  KDA_ERR_INVALID_ARG on NULL pointers or invalid sizes. */

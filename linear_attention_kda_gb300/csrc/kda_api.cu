@@ -95,7 +95,7 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
     // runs the chunk plan and the output pass alone, which passes the states through
     if (a->T == 0) return 2;
     const int extra = a->out_gate ? 1 : 0;  // the output epilogue's pass
-    if (p.fused) return 1 + extra;
+    if (p.fused || p.team) return 1 + extra;
     return (p.split ? 5 : 3) + extra;
 }
 
@@ -104,8 +104,8 @@ kda_status_t kda_chunk_fwd_schedule(const kda_chunk_args *a, int64_t *out) {
     kda_chunk_plan p;
     if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p, a->cu_seqlens_host, a->gate_kind))
         return KDA_ERR_INVALID_ARG;
-    out[0] = p.fused;
-    out[1] = p.fused ? p.kpre : 0;
+    out[0] = p.fused ? 1 : (p.team ? 2 : 0);
+    out[1] = p.fused ? p.kpre : (p.team ? p.team_k : 0);
     out[2] = p.split ? p.seg_len : 0;
     out[3] = kda_chunk_fwd_kernel_count(a);
     return KDA_OK;

@@ -128,15 +128,19 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 //    chain first produces its own first kpre chunks, the producers the rest.
 // Uses per-sequence lengths when the host copy of cu_seqlens is given.
 constexpr double T_ITEM = 6.5, T_COLD = 13.5, T_CHAIN = 1.15, T_SUM = 2.3, T_FOLD = 1.8, T_LAUNCH = 4.0;
+constexpr double T_CHAIN_START = 3.0;      // a chain CTA switching to its next chain (team schedule)
+constexpr double TEAM_MAX_CHAINS_HOST = 1024;  // chains per team the producers' table holds
 
 struct tc_schedule {
     int64_t seg_len;  // 1 << 30: no split
     bool fused;
     int kpre;
+    bool team;
+    int teams, team_k;
 };
 
 static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int32_t *cu_host, int sms) {
-    tc_schedule r{(int64_t)1 << 30, false, 0};
+    tc_schedule r{(int64_t)1 << 30, false, 0, false, 0, 0};
     if (T == 0) return r;
     int64_t total = 0, longest = 0;
     auto chunks_of = [&](int64_t n) -> int64_t {
@@ -193,6 +197,29 @@ static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int
             }
         }
     }
+    // chain teams: teams of one chain CTA and k producers; the chains, dealt longest first in snake
+    // order, give every team about the same number of chunk steps
+    if (N <= KDA_FUSED_MAX_SEQS && n_chain > sms / 2 &&
+        (double)n_chain <= (double)(sms / 2) * TEAM_MAX_CHAINS_HOST) {
+        for (int k = 1; k <= 8; ++k) {
+            const int teams = sms / (k + 1);
+            if (teams < 1 || (double)n_chain > (double)teams * TEAM_MAX_CHAINS_HOST) continue;
+            const double per_team = items / teams;  // chunk steps (= packets) per team
+            const double chain = std::max(per_team, (double)longest) * T_CHAIN +
+                                 std::ceil((double)n_chain / teams) * T_CHAIN_START;
+            const double prod = per_team * T_ITEM / k;
+            const double cost = T_COLD + std::max(chain, prod) + T_LAUNCH;
+            if (cost < best) {
+                best = cost;
+                r.team = true;
+                r.teams = teams;
+                r.team_k = k;
+                r.fused = false;
+                r.kpre = 0;
+                r.seg_len = (int64_t)1 << 30;
+            }
+        }
+    }
     return r;
 }
 
@@ -219,6 +246,8 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
     p->split = 0;
     p->fused = 0;
     p->kpre = 0;
+    p->team = 0;
+    p->teams = p->team_k = p->team_window = 0;
     p->seg_len = (int64_t)1 << 30;
     p->max_segs = N;
     if (p->path == 1) {
@@ -229,6 +258,10 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
         p->seg_len = sch.seg_len;
         p->fused = sch.fused ? 1 : 0;
         p->kpre = sch.kpre;
+        p->team = sch.team ? 1 : 0;
+        p->teams = sch.teams;
+        p->team_k = sch.team_k;
+        p->team_window = 4;  // own items a producer may run ahead of its chain
         p->split = p->seg_len < ((int64_t)1 << 30) ? 1 : 0;
         p->max_segs = p->split ? p->max_chunks / p->seg_len + N : N;
     }
@@ -242,6 +275,8 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
     }
     p->off_flags = align_up(end, 256);
     end = p->off_flags + sizeof(uint64_t) * (size_t)p->max_chunks * (size_t)H;
+    p->off_consumed = align_up(end, 256);
+    if (p->team) end = p->off_consumed + sizeof(uint64_t) * (size_t)p->max_chunks * (size_t)H;
     p->total_bytes = align_up(end, 256);
     return true;
 }

@@ -141,26 +141,30 @@ __device__ __forceinline__ bool locate(const int32_t *chunk_start, const int32_t
 
 // =====================================================================================
 // Persistent intra-chunk kernel: one CTA per SM walks the (chunk, head) work items
-// w = slot * H + h.  Warp 16 is the producer: for each item it fetches the q, z, k, v tiles
-// (128-byte-swizzled TMA boxes of 64 tokens x 64 channels, two per tile) and the item's beta,
-// bias and e^{A_log} into one half of a double buffer, while warps 0-15 compute the other item.
+// w = slot * H + h.  Its sixteen consumer warps form two groups of eight; group g takes the CTA's
+// items g, g + 2, g + 4, ... and owns a full set of buffers (a ~100 KB region of shared memory and
+// 256 tensor-memory columns), so that the two groups run out of phase: while one inverts (I + L)
+// (a latency-bound step), the other runs the gate and element pass of its next item (MUFU and
+// shared-memory bound).  Warp 16 + g is group g's producer: it fetches the q, z, k, v tiles
+// (128-byte-swizzled TMA boxes of 64 tokens x 64 channels), the item's beta, bias and e^{A_log},
+// and writes the packet by bulk copies.
 //
 // Tiles stay token-major ([token][channel], the TMA layout) from load to packet: tcgen05 reads a
 // token-major tile as a K-major operand when the contraction runs over channels and, through an
 // MN-major descriptor, as its transpose when it runs over tokens.  Per item:
-//   G1   gate (Eq. 5) and in-chunk cumulative log-decay G (Eq. 3); thread = (channel, half).
-//   G2   element pass; thread = (4 channels, tokens tg + 8 i): every decay factor and operand
-//        image.  Q^ = Q Gamma overwrites q, X = Gamma K overwrites k, K~ = K e^{G_63 - G} takes
-//        the place of z; the row image and two key images feed the next step.
+//   GATE gate (Eq. 5) and in-chunk cumulative log-decay G (Eq. 3); thread = (channel pair,
+//        16-token quarter), G kept in registers.
+//   ELEM element pass, same threads: every decay factor and operand image.  The q and z boxes are
+//        loaded as one 128-row image [q; z]; it becomes the row image [q E; k E] in place.  Keys
+//        scaled to the second reference overwrite k; X = Gamma K goes to its own tile.  Q^ = Q Gamma
+//        and K~ = K e^{G_63 - G} go straight from registers to the packet in global memory.
 //   MMA  A = Tril[(Q Gamma)(K / Gamma)^T] and L = StrictTril[diag(beta)(K Gamma)(K / Gamma)^T]:
-//        one product with M = 128 (64 query rows over 64 key rows), N = 96 (keys scaled to either
+//        M = 128 (64 query rows over 64 key rows), N = 32 + 64 (keys scaled to either
 //        reference), K = 128 channels.
 //   INV  T = (I + L)^{-1} in fp32: 16 x 16 diagonal blocks by substitution, then one 16-row and
 //        one 32-row block merge, T21 = -T22 L21 T11.
-//   MMA  [W | U] = (T diag beta) [X | V], X and V read MN-major (one N = 256 product).
-//   OUT  packet by bulk copies: [W; Q^], K~, A, U, gamma.
-//
-// Warps 0-15 split every phase (16 consumer warps keep the latency-bound phases fed).
+//   MMA  W = (T diag beta) X and U^T = V^T (T diag beta)^T, X and V read MN-major.
+//   OUT  packet: [W; Q^], U^T, gamma, K~, A.
 //
 // Exponent safety.  Each log-decay step lies in (g_min, 0) = (-5, 0), so 16 tokens span less than
 // 80 in the exponent, inside the fp32 / bf16 range of e^{+-88}.  The chunk is cut into two
@@ -171,35 +175,43 @@ __device__ __forceinline__ bool locate(const int32_t *chunk_start, const int32_t
 // the exponential of its own exponent, never a product of two large and small factors, so a key
 // factor that underflows loses at most e^{75 - 87} of a term.  Entries above the diagonal may
 // overflow to inf; they are discarded by selects and never multiplied.
-constexpr int NT2 = 544;      // 16 consumer warps + 1 producer warp
-constexpr int NC2 = 512;      // consumer threads
-constexpr int PRODUCER = 16;  // producer warp
-constexpr uint32_t J_STG_BYTES = 65536;  // 2 stages x [Q | Z | K | V], [64][128] bf16 each (SW128)
-constexpr uint32_t J_TQ = 0, J_TZ = 16384, J_TK = 32768, J_TV = 49152;
-constexpr uint32_t J_G = 2 * J_STG_BYTES;   // fp32 G [64][128]; float4 slot s of row t at s ^ (t % 8)
-constexpr uint32_t J_IMG = J_G + 32768;     // 56 KB working region
-constexpr uint32_t J_ROW = J_IMG;           // row image: q rows over k rows, 128 x 128
-constexpr uint32_t J_KEY = J_IMG + 32768;   // key image, 96 x 128: rows 0-31 = keys 0-31 scaled to p0,
-                                            // rows 32-95 = keys 0-63 scaled to p1
-constexpr int LS = 68;                      // row stride (floats) of the fp32 L and T matrices
-constexpr uint32_t J_L = J_IMG;             // after the A / L product: fp32 L [64][LS]
-constexpr uint32_t J_T = J_IMG + 17408;     // fp32 T [64][LS]
-constexpr uint32_t J_TIMG = J_IMG + 34816;  // (T diag beta) image 64 x 64
-constexpr uint32_t J_AIMG = J_IMG + 43008;  // A image 64 x 64
-constexpr uint32_t J_GAM = J_IMG + 57344;   // gamma fp32 [128]
-constexpr uint32_t J_QTOT = J_GAM + 512;    // G at tokens 15, 31, 47: fp32 [3][128]
-constexpr uint32_t J_BETA = J_QTOT + 2048;  // 2 stages x fp32 [64]
-constexpr uint32_t J_BIAS = J_BETA + 512;   // 2 stages x fp32 [128]
-constexpr uint32_t J_INFO = J_BIAS + 1024;  // 2 stages x {int64 t0, len, h, slot; float eA}
-constexpr uint32_t J_BAR = J_INFO + 128;    // ld[2], pq[2], pw[2], mma, rd
-constexpr uint32_t J_TSLOT = J_BAR + 64;
-constexpr uint32_t J_TBL = J_BAR + 128;     // int32 [J_TBL_N + 1]: producer chunks before each sequence
-constexpr int J_TBL_N = KDA_FUSED_MAX_SEQS;  // sequences the table holds
+constexpr int NT2 = 576;      // 2 consumer groups x 8 warps + 2 producer warps
+constexpr int NCG = 256;      // threads of a consumer group
+constexpr int PRODUCER = 16;  // producer warp of group g: PRODUCER + g
+// Per-group shared-memory region (offsets from the group's base, multiple of 1024)
+constexpr uint32_t GR_QZ = 0;          // 32 KB: TMA boxes q h0 | z h0 | q h1 | z h1 = a K-major 128-row image
+                                       // [q; z]; then the row image [q E; k E]; after the A / L product the
+                                       // fp32 L, T and P of the inverse (which spill into GR_K)
+constexpr uint32_t GR_K = 32768;       // 16 KB: k tile -> keys scaled to p1 (64-row K-major image)
+constexpr uint32_t GR_V = 49152;       // 16 KB: v tile -> U^T image [128 channels][64 tokens]
+constexpr uint32_t GR_X = 65536;       // 16 KB: X = Gamma K (token-major) -> W rows
+constexpr uint32_t GR_K0 = 81920;      // 8 KB: keys 0-31 scaled to p0 (32 rows); then the (T diag beta) image
+constexpr uint32_t GR_A = 90112;       // 8 KB: A image (rows 64-127 of the W product's A operand)
+constexpr uint32_t GR_GAM = 98304;     // gamma^C fp32 [128]
+constexpr uint32_t GR_TOT = GR_GAM + 512;    // quarter sums of the log-decays, fp32 [4][128]
+constexpr uint32_t GR_BETA = GR_TOT + 2048;  // 2 slots x fp32 [64]
+constexpr uint32_t GR_BIAS = GR_BETA + 512;  // 2 slots x fp32 [128]
+constexpr uint32_t GR_INFO = GR_BIAS + 1024; // 2 slots x {int64 t0, len, h, w; float eA} (64 B)
+constexpr uint32_t GR_BAR = GR_INFO + 128;   // mbarriers: ld_qzk, ld_v, a_ready, inv_done, wu_ready, pk_read, mma
+constexpr uint32_t GR_BYTES = 103424;        // 101 KB
+static_assert(GR_BAR + 64 <= GR_BYTES && GR_BYTES % 1024 == 0, "group region");
+// The fp32 L and T of the inverse are kept as SW128 images (fimg below): the tf32 products of its
+// last merge read them in place.
+constexpr uint32_t GR_L = GR_QZ;             // fp32 L image (16 KB)
+constexpr uint32_t GR_T = GR_QZ + 16384;     // fp32 T image (16 KB)
+constexpr uint32_t GR_P = GR_K + 8192;       // P^T (P = L_21 T_11) as a K-major tf32 image, 32 rows (4 KB)
+constexpr uint32_t GR_TT = GR_K + 12288;     // T_11^T as a K-major tf32 image, 32 rows (4 KB)
+constexpr uint32_t J_SH = 2 * GR_BYTES;       // shared by both groups
+constexpr uint32_t J_TSLOT = J_SH;            // TMEM base
+constexpr uint32_t J_TOK = J_SH + 16;         // mbarriers tok[2]: group g may start its gate and element pass
+constexpr uint32_t J_TBL = J_SH + 64;         // int32 [J_TBL_N + 1]: producer chunks before each sequence
+constexpr int J_TBL_N = KDA_FUSED_MAX_SEQS;   // sequences the table holds
 constexpr uint32_t J_CS = J_TBL + 4 * (J_TBL_N + 1);  // fused launch: chunk_start [N + 1]
 constexpr uint32_t J_SS = J_CS + 4 * (J_TBL_N + 1);   //               seg_start [N + 1], then a flag
 constexpr uint32_t J_TOTAL = J_SS + 4 * (J_TBL_N + 2) + 1024;
-// TMEM columns: A / L product (96); later [W | U] (256, lanes 0-63)
-constexpr uint32_t TM_DA = 0, TM_DB = 32, TM_DW = 0, TM_DUT = 128;
+// TMEM columns of a group (base + 256 g): the A / L product in [0, 96); later W in [0, 128) (lanes
+// 0-63) and U^T in [128, 192)
+constexpr uint32_t TM_DA = 0, TM_DW = 0, TM_DUT = 128;
 
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -209,38 +221,31 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// float index of G[t][c] in the swizzled fp32 G tile
-__device__ __forceinline__ int gsw(int t, int c) { return t * 128 + ((((c >> 2) ^ (t & 7)) << 2) | (c & 3)); }
-
-__device__ __forceinline__ void unpack4(const uint2 &u, float *f) {
-    const __nv_bfloat162 *hh = reinterpret_cast<const __nv_bfloat162 *>(&u);
-    const float2 a = __bfloat1622float2(hh[0]), b = __bfloat1622float2(hh[1]);
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-}
-__device__ __forceinline__ uint2 pack4(const float *f) {
-    return make_uint2(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]));
-}
-
 struct TileMaps {
     CUtensorMap q, k, v, z;
 };
 
-// Consumer-group barrier (warps 0-15, named barrier 1) with tcgen05 ordering.
-__device__ __forceinline__ void csync() {
+// Named barrier of consumer group g (ids 1, 2), with tcgen05 ordering.
+__device__ __forceinline__ void gsync(int g) {
     fence_before_sync();
-    named_sync(1, NC2);
+    named_sync(1 + g, NCG);
     fence_after_sync();
 }
-__device__ __forceinline__ bool csync_and(bool pred) {
-    int r;
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.popc.u32 %0, 1, %2, p;\n\t}\n"
-                 : "=r"(r) : "r"((unsigned)pred), "n"(NC2) : "memory");
-    return r == NC2;
+// All threads of group g: true iff pred held in every one of them.
+__device__ __forceinline__ bool gsync_and(int g, bool pred) {
+    return bar_red_popc(1 + g, NCG, pred) == NCG;
 }
-// Waits on an mbarrier from every consumer thread; consumer-uniform result.
-__device__ __forceinline__ bool cwait(uint64_t *bar, uint32_t parity) {
+// Waits on an mbarrier from every thread of group g; group-uniform result.
+__device__ __forceinline__ bool gwait(int g, uint64_t *bar, uint32_t parity) {
     const bool ok = mbar_wait(bar, parity);
-    return csync_and(ok);
+    return gsync_and(g, ok);
+}
+
+// Float index of element (r, c) of a 64 x 64 fp32 matrix kept as a K-major SW128 image: two column
+// blocks of 32 values (8 KB each), rows of 128 bytes, 16-byte chunk j of row r at position j ^ (r % 8).
+// Read by tf32 MMAs as an A operand (rows M, columns K) or, rows being K, as an MN-major B operand.
+__device__ __forceinline__ int fimg(int r, int c) {
+    return ((c >> 5) << 11) + (r << 5) + ((((c & 31) >> 2) ^ (r & 7)) << 2) + (c & 3);
 }
 
 // Partial products of the level-1 block merges of the UT-transform inverse: P[q + 4 a][jc] =
@@ -251,61 +256,24 @@ __device__ __forceinline__ void inv_l1_partial(const float *Lm, const float *Tm,
                                                float *p) {
     float tc[16];
 #pragma unroll
-    for (int k = K0; k < 16; ++k) tc[k] = Tm[(co + k) * LS + co + jc];
+    for (int k = K0; k < 16; ++k) tc[k] = Tm[fimg(co + k, co + jc)];
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-        const float *lr = Lm + (ro + q + 4 * a) * LS + co;
         float acc = 0.f;
 #pragma unroll
         for (int k = K0; k < 16; k += 4) {
-            const float4 l4 = *reinterpret_cast<const float4 *>(lr + k);
+            const float4 l4 = *reinterpret_cast<const float4 *>(Lm + fimg(ro + q + 4 * a, co + k));
             acc += l4.x * tc[k] + l4.y * tc[k + 1] + l4.z * tc[k + 2] + l4.w * tc[k + 3];
         }
         p[a] = acc;
     }
 }
 
-// Element pass for 4 tokens t = tg + 8 i (i = 4 H1 .. 4 H1 + 3) and channels c0 .. c0 + 3.
-template <bool H1>
-__device__ __forceinline__ void element_pass(unsigned char *sm, unsigned char *stg, const float *Gs, int tg,
-                                             int c0, const float *G15, const float *G47, const float *eg15,
-                                             const float *eg47, const float *f63) {
-    const int s4 = c0 >> 2;
-#pragma unroll
-    for (int ii = 0; ii < 4; ++ii) {
-        const int t = tg + 8 * (4 * H1 + ii);
-        const float4 g4 = *reinterpret_cast<const float4 *>(Gs + t * 128 + ((s4 ^ tg) << 2));
-        const float gt[4] = {g4.x, g4.y, g4.z, g4.w};
-        float qf[4], kf[4];
-        unpack4(*reinterpret_cast<const uint2 *>(stg + J_TQ + img_off(64, t, c0)), qf);
-        unpack4(*reinterpret_cast<const uint2 *>(stg + J_TK + img_off(64, t, c0)), kf);
-        float rq[4], rk[4], k0[4], k1[4], qh[4], xk[4], kt[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float dd = (gt[e] - (H1 ? G47[e] : G15[e])) * LOG2E;
-            const float E = ex2_approx(dd);                         // e^{G_t - G_p}
-            const float f1 = ex2_approx((G47[e] - gt[e]) * LOG2E);  // e^{G_p1 - G_t}
-            rq[e] = qf[e] * E;
-            rk[e] = kf[e] * E;
-            k1[e] = kf[e] * f1;
-            k0[e] = H1 ? 0.f : kf[e] * ex2_approx(-dd);             // e^{G_p0 - G_t}
-            const float eg = E * (H1 ? eg47[e] : eg15[e]);           // e^{G_t}
-            qh[e] = qf[e] * eg;
-            xk[e] = kf[e] * eg;
-            kt[e] = kf[e] * (f1 * f63[e]);                           // e^{G_63 - G_t}
-        }
-        *reinterpret_cast<uint2 *>(sm + J_ROW + img_off(128, t, c0)) = pack4(rq);
-        *reinterpret_cast<uint2 *>(sm + J_ROW + img_off(128, 64 + t, c0)) = pack4(rk);
-        *reinterpret_cast<uint2 *>(sm + J_KEY + img_off(96, 32 + t, c0)) = pack4(k1);
-        if (!H1) *reinterpret_cast<uint2 *>(sm + J_KEY + img_off(96, t, c0)) = pack4(k0);
-        *reinterpret_cast<uint2 *>(stg + J_TQ + img_off(64, t, c0)) = pack4(qh);
-        *reinterpret_cast<uint2 *>(stg + J_TK + img_off(64, t, c0)) = pack4(xk);
-        *reinterpret_cast<uint2 *>(stg + J_TZ + img_off(64, t, c0)) = pack4(kt);
-    }
-}
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
 // Packet publication between CTAs of one (cooperative) launch: the producer releases a flag once the
-// packet's bulk writes have completed; the consumer acquires it before its bulk reads.
+// packet's writes have completed; the consumer acquires it before its bulk reads.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 // Drops one 128-byte line from L2 without writing it back (its contents become undefined).
 __device__ __forceinline__ void discard_l2(const void *p) {
@@ -333,23 +301,40 @@ __device__ __forceinline__ bool flag_wait(const uint64_t *f, uint64_t epoch) {
     }
 }
 
+// Team mode of the intra-chunk role (a producer CTA of a chain team): the team's chains in the order
+// its chain CTA runs them, and the number of the team's items (chunks) before each chain.  Producer q of
+// K takes the team's items q, q + K, ...; it starts an item only once the chain has started on the item
+// `window` of its own items earlier, so that packets are read from L2 soon after they are written.
+struct TeamItems {
+    const int32_t *chain;  // [count] n * H + h
+    const int32_t *pre;    // [count + 1]
+    int count, K, q, window;
+    const uint64_t *consumed;  // per item: the launch's epoch once the chain has started on it
+};
+
 // The intra-chunk work of one CTA.  Items (chunk slot, head) are numbered w = slot * H + h.
 //  - own_n < 0, kpre == 0: worker `worker` of `nworkers` takes items worker, worker + nworkers, ...
 //  - own_n < 0, kpre > 0: the same over the items left once the first kpre chunks of every
 //    sequence are taken away (in the same order);
-//  - own_n >= 0: the first kpre chunks of sequence own_n for head own_h.
-// With `flags`, each item's packet is published (flags[item] = epoch) once its writes have completed.
-// In the last mode the CTA keeps its right to allocate tensor memory (its chain runs next).
+//  - own_n >= 0: the first kpre chunks of sequence own_n for head own_h;
+//  - team != nullptr: the items of a chain team (see TeamItems).
+// The CTA's it-th item goes to consumer group it & 1.  With `flags`, each item's packet is published
+// (flags[item] = epoch) once its writes have completed.  In the last mode the CTA keeps its right to
+// allocate tensor memory (its chain runs next).
 __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm, const bf16 *__restrict__ beta,
                                            const float *__restrict__ bias, const float *__restrict__ A_log,
                                            float g_min, int64_t T, int N, const int32_t *__restrict__ cu,
                                            const int32_t *__restrict__ chunk_start, int H,
                                            unsigned char *__restrict__ packets, int *err, int worker, int nworkers,
-                                           uint64_t *flags, uint64_t epoch, int kpre, int own_n, int own_h) {
+                                           uint64_t *flags, uint64_t epoch, int kpre, int own_n, int own_h,
+                                           const TeamItems *team = nullptr) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t *tbl = (int32_t *)(sm + J_TBL);  // kpre > 0: tbl[n] = producer chunks of sequences before n
     int n_items = 0;
-    if (own_n >= 0) {
+    if (team) {
+        const int tot = team->pre[team->count];
+        n_items = team->q < tot ? (tot - team->q + team->K - 1) / team->K : 0;
+    } else if (own_n >= 0) {
         n_items = min(kpre, chunk_start[own_n + 1] - chunk_start[own_n]);
     } else if (kpre > 0) {
         if (warp == 0) {
@@ -376,6 +361,16 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
     }
     if (n_items == 0) return;
     auto w_of = [&](int it) -> int64_t {  // global item index of this CTA's it-th item
+        if (team) {
+            const int k = team->q + it * team->K;
+            int lo = 0, hi = team->count;  // the chain holding team item k: largest m with pre[m] <= k
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (team->pre[mid] <= k) lo = mid; else hi = mid;
+            }
+            const int id = team->chain[lo];
+            return (int64_t)(chunk_start[id / H] + (k - team->pre[lo])) * H + (id % H);
+        }
         if (own_n >= 0) return (int64_t)(chunk_start[own_n] + it) * H + own_h;
         const int64_t k = (int64_t)worker + (int64_t)it * nworkers;
         if (kpre <= 0) return k;
@@ -387,96 +382,115 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
         }
         return (int64_t)(chunk_start[lo] + kpre + (kk - tbl[lo])) * H + (int)(k % H);
     };
-    float *Gs = (float *)(sm + J_G);
-    uint64_t *bar_ld = (uint64_t *)(sm + J_BAR);  // [2] stage loaded
-    uint64_t *bar_pq = bar_ld + 2;                // [2] Q^ and K~ tiles of the stage's item written
-    uint64_t *bar_pw = bar_ld + 4;                // [2] rest of the item's packet written (item done)
-    uint64_t *bar_rd = bar_ld + 7;                // the packet copies of the last item have read shared memory
-    uint64_t *bar_mma = bar_ld + 6;
     uint32_t *tslot = (uint32_t *)(sm + J_TSLOT);
-
-    if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar_ld[i], 1);
-            mbar_init(&bar_pq[i], 1);
-            mbar_init(&bar_pw[i], 1);
-        }
-        mbar_init(bar_mma, 1);
-        mbar_init(bar_rd, 1);
+    if (tid < 2) {
+        uint64_t *b = (uint64_t *)(sm + tid * GR_BYTES + GR_BAR);
+        for (int i = 0; i < 7; ++i) mbar_init(&b[i], 1);
+        mbar_init((uint64_t *)(sm + J_TOK) + tid, 1);
     }
-    if (warp == 0) tmem_alloc(tslot, 256, own_n < 0);
+    if (warp == 0) tmem_alloc(tslot, 512, own_n < 0);
     fence_proxy_async();
     sync_all();
     const uint32_t tb = *tslot;
 
-    if (warp == PRODUCER) {
-        // ------------------------------------------------ producer warp: loads items into the two stages and
+    if (warp >= PRODUCER) {
+        // ------------------------------------------------ producer warp of group g: loads its items and
         // writes their packets (bulk copies from shared memory), publishing each through `flags` once its
-        // writes have completed; a stage is refilled as soon as the copies of its item have read it.
-        auto load_item = [&](int it) {
-            const int64_t w = w_of(it);
-            const int s = it & 1;
+        // writes have completed.  The next item's q, z and k tiles are loaded as soon as the inverse has
+        // freed their buffers, its v tile once the packet copies have read the current item's U^T.
+        const int g = warp - PRODUCER;
+        unsigned char *R = sm + g * GR_BYTES;
+        uint64_t *bar = (uint64_t *)(R + GR_BAR);
+        uint64_t *ld_qzk = bar, *ld_v = bar + 1, *a_ready = bar + 2, *inv_done = bar + 3, *wu_ready = bar + 4,
+                 *pk_read = bar + 5;
+        const int nj = (n_items - g + 1) / 2;  // items it = 2 j + g
+        auto load_qzk = [&](int j) {
+            const int64_t w = w_of(2 * j + g);
+            const int s = j & 1;
             const int64_t slot = w / H;
             const int h = (int)(w % H);
             int n = 0, len = 0;
             int64_t t0 = 0;
             locate(chunk_start, cu, T, N, slot, n, t0, len);
-            float *bet = (float *)(sm + J_BETA) + 64 * s;
-            float *bia = (float *)(sm + J_BIAS) + 128 * s;
+            float *bet = (float *)(R + GR_BETA) + 64 * s;
+            float *bia = (float *)(R + GR_BIAS) + 128 * s;
 #pragma unroll
             for (int r = lane; r < C; r += 32) bet[r] = r < len ? __bfloat162float(beta[(t0 + r) * H + h]) : 0.f;
 #pragma unroll
             for (int c = lane; c < D; c += 32) bia[c] = bias ? bias[h * D + c] : 0.f;
             if (lane == 0) {
-                int64_t *info = (int64_t *)(sm + J_INFO + 64 * s);
+                int64_t *info = (int64_t *)(R + GR_INFO + 64 * s);
                 info[0] = t0;
                 info[1] = len;
                 info[2] = h;
-                info[3] = slot;
+                info[3] = w;
                 *reinterpret_cast<float *>(info + 4) = A_log ? __expf(A_log[h]) : 1.f;
             }
             __threadfence_block();
             __syncwarp();
             if (lane == 0) {
-                unsigned char *stg = sm + s * J_STG_BYTES;
-                mbar_arrive_expect_tx(&bar_ld[s], J_STG_BYTES);
-                const CUtensorMap *maps[4] = {&tm.q, &tm.z, &tm.k, &tm.v};
-#pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    tma_load_3d(stg + 16384 * x, maps[x], 0, h, (int)t0, &bar_ld[s]);
-                    tma_load_3d(stg + 16384 * x + 8192, maps[x], 64, h, (int)t0, &bar_ld[s]);
-                }
+                mbar_arrive_expect_tx(ld_qzk, 6 * 8192);
+                tma_load_3d(R + GR_QZ, &tm.q, 0, h, (int)t0, ld_qzk);
+                tma_load_3d(R + GR_QZ + 8192, &tm.z, 0, h, (int)t0, ld_qzk);
+                tma_load_3d(R + GR_QZ + 16384, &tm.q, 64, h, (int)t0, ld_qzk);
+                tma_load_3d(R + GR_QZ + 24576, &tm.z, 64, h, (int)t0, ld_qzk);
+                tma_load_3d(R + GR_K, &tm.k, 0, h, (int)t0, ld_qzk);
+                tma_load_3d(R + GR_K + 8192, &tm.k, 64, h, (int)t0, ld_qzk);
             }
         };
-        if (n_items > 0) load_item(0);
-        if (n_items > 1) load_item(1);
+        auto load_v = [&](int j) {
+            if (lane == 0) {
+                const int64_t w = w_of(2 * j + g);
+                const int h = (int)(w % H);
+                int n = 0, len = 0;
+                int64_t t0 = 0;
+                locate(chunk_start, cu, T, N, w / H, n, t0, len);
+                mbar_arrive_expect_tx(ld_v, 2 * 8192);
+                tma_load_3d(R + GR_V, &tm.v, 0, h, (int)t0, ld_v);
+                tma_load_3d(R + GR_V + 8192, &tm.v, 64, h, (int)t0, ld_v);
+            }
+        };
+        if (nj > 0) {
+            load_qzk(0);
+            load_v(0);
+        }
         bool ok = true;
-        for (int it = 0; it < n_items && ok; ++it) {
-            const int s = it & 1;
-            const int64_t w = w_of(it);
-            unsigned char *stg = sm + s * J_STG_BYTES;
+        for (int j = 0; j < nj && ok; ++j) {
+            const uint32_t par = j & 1;
+            const int64_t w = w_of(2 * j + g);
             unsigned char *pk = packets + (size_t)w * PK_STRIDE;  // item w = slot * H + h
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar_pq[s], (it >> 1) & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait(a_ready, par));
             if (!ok) break;
             if (lane == 0) {
-                bulk_s2g(pk + PK_WQ + 8192, stg + J_TQ, 8192);  // Q^ rows of the [W; Q^] image
-                bulk_s2g(pk + PK_WQ + 24576, stg + J_TQ + 8192, 8192);
-                bulk_s2g(pk + PK_K, stg + J_TZ, 16384);
+                bulk_s2g(pk + PK_A, R + GR_A, 8192);
                 bulk_commit();
             }
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar_pw[s], (it >> 1) & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait(inv_done, par));
+            if (!ok) break;
+            if (j + 1 < nj) {
+                const int nxt = 2 * (j + 1) + g;
+                if (team && nxt >= team->window) {  // run at most `window` items ahead of the chain
+                    bool okw = true;
+                    if (lane == 0) okw = flag_wait(team->consumed + w_of(nxt - team->window), epoch);
+                    ok = __shfl_sync(0xffffffffu, okw, 0);
+                    if (!ok) break;
+                }
+                load_qzk(j + 1);
+            }
+            ok = __all_sync(0xffffffffu, mbar_wait(wu_ready, par));
             if (!ok) break;
             if (lane == 0) {
-                bulk_s2g(pk + PK_WQ, stg + J_TK, 8192);
-                bulk_s2g(pk + PK_WQ + 16384, stg + J_TK + 8192, 8192);
-                bulk_s2g(pk + PK_U, stg + J_TV, 16384);
-                bulk_s2g(pk + PK_A, sm + J_AIMG, 8192);
-                bulk_s2g(pk + PK_G, sm + J_GAM, 512);
+                bulk_s2g(pk + PK_WQ, R + GR_X, 8192);  // W rows of the [W; Q^] image
+                bulk_s2g(pk + PK_WQ + 16384, R + GR_X + 8192, 8192);
+                bulk_s2g(pk + PK_U, R + GR_V, 16384);
+                bulk_s2g(pk + PK_G, R + GR_GAM, 512);
                 bulk_commit();
                 bulk_wait_read0();
-                mbar_arrive(bar_rd);  // the A image and gamma may be overwritten
+                mbar_arrive(pk_read);  // X, V, A and gamma of this item have been read
             }
-            if (lane == 0) {  // publish before refilling the stage: a chain may be waiting for this packet
+            __syncwarp();
+            if (j + 1 < nj) load_v(j + 1);
+            if (lane == 0) {  // publish: a chain may be waiting for this packet
                 bulk_wait0();
                 if (flags) {
                     fence_proxy_async_global();
@@ -484,152 +498,229 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
                 }
             }
             __syncwarp();
-            if (it + 2 < n_items) load_item(it + 2);
         }
         if (!ok && lane == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     } else {
-        // ------------------------------------------------ consumer warps 0-15
+        // ------------------------------------------------ consumer group g (warps 8 g .. 8 g + 7)
+        const int g = warp >> 3, gt = tid & (NCG - 1), gw = gt >> 5;
+        unsigned char *R = sm + g * GR_BYTES;
+        uint64_t *bar = (uint64_t *)(R + GR_BAR);
+        uint64_t *ld_qzk = bar, *ld_v = bar + 1, *a_ready = bar + 2, *inv_done = bar + 3, *wu_ready = bar + 4,
+                 *pk_read = bar + 5, *bar_mma = bar + 6;
+        const uint32_t tbg = tb + 256u * (uint32_t)g;
+        const int nj = (n_items - g + 1) / 2;
+        // element mapping: channel pair (c0, c0 + 1) of one 64-channel half, 16-token quarter qt
+        const int hw = gw & 1, qt = gw >> 1;
+        const int c0 = 64 * hw + 2 * lane;
+        const uint32_t cpos = (uint32_t)((lane & 3) << 2);  // byte of the pair inside its 16-byte chunk
+        auto roff = [&](int r) -> uint32_t {                  // the pair in row r of a 64-channel block
+            return (uint32_t)(r * 128) + ((((uint32_t)(lane >> 2)) ^ (uint32_t)(r & 7)) << 4) + cpos;
+        };
+        // The two groups take turns at the gate and element pass (MUFU and shared-memory bound), each
+        // starting it once the other has finished its own, so that one group's element pass overlaps
+        // the other's inverse and products instead of competing with its element pass.  Group 0 starts.
+        uint64_t *tok = (uint64_t *)(sm + J_TOK);
         uint32_t mph = 0;
         bool ok = true;
-        int it = 0;
-        for (;; ++it) {
-            if (it >= n_items) break;
-            const int s = it & 1;
-            ok = cwait(&bar_ld[s], (it >> 1) & 1);
+        for (int j = 0; j < nj; ++j) {
+            const uint32_t par = j & 1;
+            const int s = j & 1;
+            if (g == 1) ok = gwait(g, &tok[1], j & 1);               // group 0 has done its item j
+            else if (j > 0) ok = gwait(g, &tok[0], (j - 1) & 1);     // group 1 has done its item j - 1
             if (!ok) break;
-            const int64_t *info = (const int64_t *)(sm + J_INFO + 64 * s);
+            ok = gwait(g, ld_qzk, par);
+            if (!ok) break;
+            const int64_t *info = (const int64_t *)(R + GR_INFO + 64 * s);
             const int len = (int)info[1];
+            const int64_t w = info[3];
             const float eA = *reinterpret_cast<const float *>(info + 4);
-            const float *bet = (const float *)(sm + J_BETA) + 64 * s;
-            const float *bia = (const float *)(sm + J_BIAS) + 128 * s;
-            unsigned char *stg = sm + s * J_STG_BYTES;
+            const float *bet = (const float *)(R + GR_BETA) + 64 * s;
+            const float *bia = (const float *)(R + GR_BIAS) + 128 * s;
+            unsigned char *pk = packets + (size_t)w * PK_STRIDE;
 
-            // ---- G1: gate (Eq. 5) and in-chunk cumulative log-decay (Eq. 3), thread = (channel,
-            //      16-token quarter).  Tokens past the end of the sequence get g = 0 (an exact no-op).
+            // ---- GATE: g = g_min Sigmoid(e^A (z + b)) (Eq. 5), cumulative sums over the quarter
+            float G0[16], G1[16];  // channels c0, c0 + 1; tokens 16 qt + i
             {
-                const int c = tid & 127, qt = tid >> 7;
-                const float bc = bia[c];
-                float gv[16];
+                const float cz = -eA * LOG2E;
+                const float cb0 = cz * bia[c0], cb1 = cz * bia[c0 + 1];
+                const unsigned char *zb = R + GR_QZ + hw * 16384;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float zf =
-                        __bfloat162float(*reinterpret_cast<const bf16 *>(stg + J_TZ + img_off(64, 16 * qt + i, c)));
-                    gv[i] = __fdividef(g_min, 1.0f + __expf(-eA * (zf + bc)));
+                    const int t = 16 * qt + i;
+                    const uint32_t zz = *reinterpret_cast<const uint32_t *>(zb + roff(64 + t));
+                    G0[i] = __fdividef(g_min, 1.0f + ex2_approx(fmaf(bf_lo(zz), cz, cb0)));
+                    G1[i] = __fdividef(g_min, 1.0f + ex2_approx(fmaf(bf_hi(zz), cz, cb1)));
                 }
-                if (len < C) {  // ragged tail (uniform branch, outside the arithmetic above)
+                if (len < C) {  // ragged tail: tokens past the end of the sequence get g = 0 (an exact no-op)
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (16 * qt + i >= len) gv[i] = 0.f;
+                        if (16 * qt + i >= len) G0[i] = G1[i] = 0.f;
                 }
 #pragma unroll
-                for (int i = 1; i < 16; ++i) gv[i] += gv[i - 1];
-                float *qtot = (float *)(sm + J_QTOT);
-                if (qt < 3) qtot[qt * 128 + c] = gv[15];
-                csync();
-                float base = 0.f;
+                for (int i = 1; i < 16; ++i) {
+                    G0[i] += G0[i - 1];
+                    G1[i] += G1[i - 1];
+                }
+                *reinterpret_cast<float2 *>(R + GR_TOT + 4 * (128 * qt + c0)) = make_float2(G0[15], G1[15]);
+            }
+            // all quarter sums written; z read by every thread (its rows are overwritten below); and
+            // (items after the first) the packet copies of the group's previous item have read X and A
+            if (j > 0 && gt == 0) ok = mbar_wait(pk_read, (j - 1) & 1);
+            ok = gsync_and(g, ok);
+            if (!ok) break;
+            float Gr[2], G47[2], eGr[2], f63[2];  // reference G (p0 or p1), G_47, e^{G_ref}, e^{G_63 - G_47}
+            {
+                const float *tot = (const float *)(R + GR_TOT);
+                float2 q4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) q4[u] = *reinterpret_cast<const float2 *>(tot + 128 * u + c0);
+                float base0 = 0.f, base1 = 0.f;
 #pragma unroll
                 for (int u = 0; u < 3; ++u)
-                    if (u < qt) base += qtot[u * 128 + c];
+                    if (u < qt) {
+                        base0 += q4[u].x;
+                        base1 += q4[u].y;
+                    }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) Gs[gsw(16 * qt + i, c)] = gv[i] + base;
-                // the previous item's packet copies have read the A image and gamma buffers
-                if (tid == 0 && it > 0) ok = mbar_wait(bar_rd, (it - 1) & 1);
-                ok = csync_and(ok);
-            }
-            if (!ok) break;
-            // ---- G2: element pass, thread = (channels c0..c0+3, tokens tg + 8 i, one chunk half)
-            {
-                const int tg = lane & 7, cgl = lane >> 3, th = warp >> 3;
-                const int c0 = 16 * (warp & 7) + 4 * cgl, s4 = c0 >> 2;
-                const float4 a15 = *reinterpret_cast<const float4 *>(Gs + 15 * 128 + ((s4 ^ 7) << 2));
-                const float4 a47 = *reinterpret_cast<const float4 *>(Gs + 47 * 128 + ((s4 ^ 7) << 2));
-                const float4 a63 = *reinterpret_cast<const float4 *>(Gs + 63 * 128 + ((s4 ^ 7) << 2));
-                const float G15[4] = {a15.x, a15.y, a15.z, a15.w}, G47[4] = {a47.x, a47.y, a47.z, a47.w};
-                const float G63[4] = {a63.x, a63.y, a63.z, a63.w};
-                float eg15[4], eg47[4], f63[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    eg15[e] = ex2_approx(G15[e] * LOG2E);
-                    eg47[e] = ex2_approx(G47[e] * LOG2E);
-                    f63[e] = ex2_approx((G63[e] - G47[e]) * LOG2E);
+                for (int i = 0; i < 16; ++i) {
+                    G0[i] += base0;
+                    G1[i] += base1;
                 }
-                if (tg == 0 && th == 0)
-                    *reinterpret_cast<float4 *>(sm + J_GAM + 4 * c0) =
-                        make_float4(ex2_approx(G63[0] * LOG2E), ex2_approx(G63[1] * LOG2E),
-                                    ex2_approx(G63[2] * LOG2E), ex2_approx(G63[3] * LOG2E));
-                if (th) element_pass<true>(sm, stg, Gs, tg, c0, G15, G47, eg15, eg47, f63);
-                else element_pass<false>(sm, stg, Gs, tg, c0, G15, G47, eg15, eg47, f63);
+                const float g15[2] = {q4[0].x, q4[0].y};
+                G47[0] = q4[0].x + q4[1].x + q4[2].x;
+                G47[1] = q4[0].y + q4[1].y + q4[2].y;
+                const float g63[2] = {G47[0] + q4[3].x, G47[1] + q4[3].y};
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    Gr[e] = qt < 2 ? g15[e] : G47[e];
+                    eGr[e] = ex2_approx(Gr[e] * LOG2E);
+                    f63[e] = ex2_approx((g63[e] - G47[e]) * LOG2E);
+                }
+                if (qt == 3)
+                    *reinterpret_cast<float2 *>(R + GR_GAM + 4 * c0) =
+                        make_float2(ex2_approx(g63[0] * LOG2E), ex2_approx(g63[1] * LOG2E));
+            }
+            // ---- ELEM: per token t of the quarter and channel e: E = e^{G_t - G_ref}, f1 = e^{G_47 - G_t}
+            //      (keys against the second reference), k0 = e^{G_15 - G_t} (first half only).
+            {
+                unsigned char *qz = R + GR_QZ + hw * 16384;
+                unsigned char *kb = R + GR_K + hw * 8192;
+                unsigned char *k0b = R + GR_K0 + hw * 4096;
+                unsigned char *xb = R + GR_X + hw * 8192;
+                unsigned char *qhat = pk + PK_WQ + hw * 16384;
+                unsigned char *ktil = pk + PK_K + hw * 8192;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t = 16 * qt + i;
+                    const uint32_t o = roff(t);
+                    const uint32_t qq = *reinterpret_cast<const uint32_t *>(qz + o);
+                    const uint32_t kk = *reinterpret_cast<const uint32_t *>(kb + o);
+                    const float qf[2] = {bf_lo(qq), bf_hi(qq)}, kf[2] = {bf_lo(kk), bf_hi(kk)};
+                    const float gt_[2] = {G0[i], G1[i]};
+                    float rq[2], rk[2], k1[2], k0[2], qh[2], xk[2], kt[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float dd = (gt_[e] - Gr[e]) * LOG2E;
+                        const float E = ex2_approx(dd);                          // e^{G_t - G_ref}
+                        const float f1 = ex2_approx((G47[e] - gt_[e]) * LOG2E);  // e^{G_47 - G_t}
+                        rq[e] = qf[e] * E;
+                        rk[e] = kf[e] * E;
+                        k1[e] = kf[e] * f1;
+                        k0[e] = qt < 2 ? kf[e] * ex2_approx(-dd) : 0.f;      // e^{G_15 - G_t}
+                        const float eg = E * eGr[e];                              // e^{G_t}
+                        qh[e] = qf[e] * eg;
+                        xk[e] = kf[e] * eg;
+                        kt[e] = kf[e] * (f1 * f63[e]);                            // e^{G_63 - G_t}
+                    }
+                    *reinterpret_cast<uint32_t *>(qz + o) = pack_bf16(rq[0], rq[1]);
+                    *reinterpret_cast<uint32_t *>(qz + roff(64 + t)) = pack_bf16(rk[0], rk[1]);
+                    *reinterpret_cast<uint32_t *>(kb + o) = pack_bf16(k1[0], k1[1]);
+                    if (qt < 2) *reinterpret_cast<uint32_t *>(k0b + o) = pack_bf16(k0[0], k0[1]);
+                    *reinterpret_cast<uint32_t *>(xb + o) = pack_bf16(xk[0], xk[1]);
+                    *reinterpret_cast<uint32_t *>(qhat + roff(64 + t)) = pack_bf16(qh[0], qh[1]);
+                    *reinterpret_cast<uint32_t *>(ktil + o) = pack_bf16(kt[0], kt[1]);
+                }
             }
             fence_proxy_async();
-            csync();
-            if (tid == 0) {
-                // one product, N = 96: columns 0-31 against keys scaled to p0, 32-95 against keys scaled to p1
-                mma_bf16_k(tb + TM_DA, smem_u32(sm + J_ROW), 128, smem_u32(sm + J_KEY), 96, 8, idesc_bf16(128, 96),
+            gsync(g);
+            if (gt == 0) {
+                // rows over keys 0-31 scaled to p0 (N = 32), then over keys 0-63 scaled to p1 (N = 64)
+                mma_bf16_k(tbg + TM_DA, smem_u32(R + GR_QZ), 128, smem_u32(R + GR_K0), 32, 8, idesc_bf16(128, 32),
                            false);
+                mma_bf16_k(tbg + TM_DA + 32, smem_u32(R + GR_QZ), 128, smem_u32(R + GR_K), 64, 8,
+                           idesc_bf16(128, 64), false);
                 mma_commit(bar_mma);
-                mbar_arrive(&bar_pq[s]);  // Q^ and K~ are in the stage: the producer copies them out
+                // the other group's turn, while it has an item left that waits for this one: group 1's item j
+                // waits for group 0's item j, group 0's item j + 1 for group 1's item j
+                if (g == 0 ? j < n_items / 2 : j + 1 < (n_items + 1) / 2) mbar_arrive(&tok[1 - g]);
             }
-            ok = cwait(bar_mma, mph & 1);
+            ok = gwait(g, bar_mma, mph & 1);
             ++mph;
             if (!ok) break;
             fence_after_sync();
             // ---- A rows -> A image (causal, diagonal kept); L rows -> fp32 (strictly lower, times beta).
             //      Rows of the first half take keys 0-31 from columns 0-31, rows of the second half keys
-            //      0-63 from columns 32-95; the four warps of a TMEM lane quarter split the columns.
-            float *Lm = (float *)(sm + J_L);
-            float *Tm = (float *)(sm + J_T);
+            //      0-63 from columns 32-95; the two warps of a TMEM lane quarter split the columns.
+            float *Lm = (float *)(R + GR_L);
+            float *Tm = (float *)(R + GR_T);
             {
-                const int lq = warp & 3, cp = warp >> 2;
+                const int lq = gw & 3, cp = gw >> 2;
                 const int r = (32 * lq + lane) & 63;  // token row
-                if ((lq & 1) == 0) {
-                    float d[8];
-                    tmem_ld8(tmem_addr(tb + TM_DA, 32 * lq, 8 * cp), d);
-                    if (lq == 0) {
-                        float o[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = (8 * cp + e <= r) ? d[e] : 0.f;
-                        *reinterpret_cast<uint4 *>(sm + J_AIMG + img_chunk_off(64, r, cp)) = pack8(o);
-                        *reinterpret_cast<uint4 *>(sm + J_AIMG + img_chunk_off(64, r, 4 + cp)) = make_uint4(0, 0, 0, 0);
-                    } else {
-                        const float br = bet[r];
-#pragma unroll
-                        for (int e = 0; e < 8; e += 4) {
-                            const int i = 8 * cp + e;
-                            *reinterpret_cast<float4 *>(&Lm[r * LS + i]) =
-                                make_float4((i < r) ? br * d[e] : 0.f, (i + 1 < r) ? br * d[e + 1] : 0.f,
-                                            (i + 2 < r) ? br * d[e + 2] : 0.f, (i + 3 < r) ? br * d[e + 3] : 0.f);
-                        }
-                    }
-                } else {
+                if ((lq & 1) == 0) {                  // rows of the first half: columns [16 cp, 16 cp + 16)
                     float d[16];
-                    tmem_ld16(tmem_addr(tb + TM_DB, 32 * lq, 16 * cp), d);
-                    if (lq == 1) {
+                    tmem_ld16(tmem_addr(tbg + TM_DA, 32 * lq, 16 * cp), d);
+                    if (lq == 0) {
 #pragma unroll
                         for (int jj = 0; jj < 2; ++jj) {
                             const int cj = 2 * cp + jj;
                             float o[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) o[e] = (8 * cj + e <= r) ? d[8 * jj + e] : 0.f;
-                            *reinterpret_cast<uint4 *>(sm + J_AIMG + img_chunk_off(64, r, cj)) = pack8(o);
+                            *reinterpret_cast<uint4 *>(R + GR_A + img_chunk_off(64, r, cj)) = pack8(o);
+                            *reinterpret_cast<uint4 *>(R + GR_A + img_chunk_off(64, r, 4 + cj)) = make_uint4(0, 0, 0, 0);
                         }
                     } else {
                         const float br = bet[r];
 #pragma unroll
                         for (int e = 0; e < 16; e += 4) {
                             const int i = 16 * cp + e;
-                            *reinterpret_cast<float4 *>(&Lm[r * LS + i]) =
+                            *reinterpret_cast<float4 *>(&Lm[fimg(r, i)]) =
+                                make_float4((i < r) ? br * d[e] : 0.f, (i + 1 < r) ? br * d[e + 1] : 0.f,
+                                            (i + 2 < r) ? br * d[e + 2] : 0.f, (i + 3 < r) ? br * d[e + 3] : 0.f);
+                        }
+                    }
+                } else {  // rows of the second half: columns 32 + [32 cp, 32 cp + 32) = keys [32 cp, 32 cp + 32)
+                    float d[32];
+                    tmem_ld32(tmem_addr(tbg + TM_DA + 32, 32 * lq, 32 * cp), d);
+                    if (lq == 1) {
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int cj = 4 * cp + jj;
+                            float o[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) o[e] = (8 * cj + e <= r) ? d[8 * jj + e] : 0.f;
+                            *reinterpret_cast<uint4 *>(R + GR_A + img_chunk_off(64, r, cj)) = pack8(o);
+                        }
+                    } else {
+                        const float br = bet[r];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            const int i = 32 * cp + e;
+                            *reinterpret_cast<float4 *>(&Lm[fimg(r, i)]) =
                                 make_float4((i < r) ? br * d[e] : 0.f, (i + 1 < r) ? br * d[e + 1] : 0.f,
                                             (i + 2 < r) ? br * d[e + 2] : 0.f, (i + 3 < r) ? br * d[e + 3] : 0.f);
                         }
                     }
                 }
             }
-            csync();
+            fence_proxy_async();
+            gsync(g);
+            if (gt == 0) mbar_arrive(a_ready);  // the producer copies the A image out
             // ---- T = (I + L)^{-1}.  Level 0: the four 16 x 16 diagonal blocks, one column per thread,
             //      by forward substitution; the blocks above the diagonal inside each 32-row half are
             //      zeroed so that the merges below can run full-length dot products.
-            if (tid < 64) {
-                const int b = tid >> 4, jc = tid & 15, o0 = 16 * b;
+            if (gt < 64) {
+                const int b = gt >> 4, jc = gt & 15, o0 = 16 * b;
                 float x[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) x[r] = (r == jc) ? 1.f : 0.f;
@@ -637,26 +728,32 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
                 for (int i = 0; i < 15; ++i) {
                     const float xi = x[i];
 #pragma unroll
-                    for (int r = i + 1; r < 16; ++r) x[r] -= Lm[(o0 + r) * LS + o0 + i] * xi;
+                    for (int r = i + 1; r < 16; ++r) x[r] -= Lm[fimg(o0 + r, o0 + i)] * xi;
                 }
 #pragma unroll
-                for (int r = 0; r < 16; ++r) Tm[(o0 + r) * LS + o0 + jc] = x[r];
+                for (int r = 0; r < 16; ++r) Tm[fimg(o0 + r, o0 + jc)] = x[r];
                 if ((b & 1) == 0) {
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) Tm[(o0 + r) * LS + o0 + 16 + jc] = 0.f;
+                    for (int r = 0; r < 16; ++r) Tm[fimg(o0 + r, o0 + 16 + jc)] = 0.f;
+                }
+                if (b < 2) {  // T_11 = T[0:32][0:32] also transposed (the B operand of the level-2 merge)
+                    float *Tt = (float *)(R + GR_TT);
+#pragma unroll
+                    for (int r = 0; r < 16; r += 4) {
+                        *reinterpret_cast<float4 *>(Tt + fimg(o0 + jc, o0 + r)) = make_float4(x[r], x[r + 1], x[r + 2], x[r + 3]);
+                        if (b == 0) *reinterpret_cast<float4 *>(Tt + fimg(16 + jc, r)) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
             }
-            csync();
+            gsync(g);
             // Level 1: T_10 = -T_11 L_10 T_00 inside each 32-row half.  Thread = (half mg, column jc,
             // rows q + 4 a); the four threads of a column share their partial products by shuffles.
-            // T_00 column jc is zero above row jc and T_11 is lower triangular, so the dot products
-            // start at the warp's lowest column and stop at the row.
-            if (tid < 128) {
-                const int mg = tid >> 6, q = lane & 3;
-                const int jc = ((tid >> 5) & 1) * 8 + (lane >> 2);
+            if (gt < 128) {
+                const int mg = gt >> 6, q = lane & 3;
+                const int jc = ((gt >> 5) & 1) * 8 + (lane >> 2);
                 const int ro = 32 * mg + 16, co = 32 * mg;
                 float p[4];
-                if (warp & 1) inv_l1_partial<8>(Lm, Tm, ro, co, q, jc, p);
+                if (gw & 1) inv_l1_partial<8>(Lm, Tm, ro, co, q, jc, p);
                 else inv_l1_partial<0>(Lm, Tm, ro, co, q, jc, p);
                 float pc[16];  // P[:, jc], row q2 + 4 a from lane q2
 #pragma unroll
@@ -665,117 +762,137 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
                     for (int a = 0; a < 4; ++a) pc[q2 + 4 * a] = __shfl_sync(0xffffffffu, p[a], (lane & ~3) | q2);
 #pragma unroll
                 for (int a = 0; a < 4; ++a) {
-                    const float *tr = Tm + (ro + q + 4 * a) * LS + ro;
                     float acc = 0.f;
 #pragma unroll
                     for (int k = 0; k < 4 * (a + 1); k += 4) {
-                        const float4 t4 = *reinterpret_cast<const float4 *>(tr + k);
+                        const float4 t4 = *reinterpret_cast<const float4 *>(Tm + fimg(ro + q + 4 * a, ro + k));
                         acc += t4.x * pc[k] + t4.y * pc[k + 1] + t4.z * pc[k + 2] + t4.w * pc[k + 3];
                     }
-                    Tm[(ro + q + 4 * a) * LS + co + jc] = -acc;
+                    Tm[fimg(ro + q + 4 * a, co + jc)] = -acc;
+                    if (mg == 0) reinterpret_cast<float *>(R + GR_TT)[fimg(co + jc, ro + q + 4 * a)] = -acc;
                 }
             }
-            csync();
-            // Level 2: T_[23][01] = -T_[23][23] L_[23][01] T_[01][01] on 32 x 32 blocks, as two products
-            // through shared memory: P = L_[23][01] T_[01][01], then T_[23][01] = -T_[23][23] P.  Warps 0-7,
-            // thread = (row i, columns 4 jq .. 4 jq + 3), float4 loads.  The triangular factors hold zeros
-            // above their diagonals, so full-length dot products are exact.  P goes to the (not yet
-            // written) T-image area.
-            {
-                float *Pm = (float *)(sm + J_TIMG);  // P [32][36]
-                const int jq = tid & 7, i = tid >> 3;
-                if (tid < 256) {
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float *lr = Lm + (32 + i) * LS;
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4 *>(lr + k);
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float4 t4 = *reinterpret_cast<const float4 *>(Tm + (k + e) * LS + 4 * jq);
-                            acc.x = fmaf(lv[e], t4.x, acc.x);
-                            acc.y = fmaf(lv[e], t4.y, acc.y);
-                            acc.z = fmaf(lv[e], t4.z, acc.z);
-                            acc.w = fmaf(lv[e], t4.w, acc.w);
-                        }
-                    }
-                    *reinterpret_cast<float4 *>(Pm + i * 36 + 4 * jq) = acc;
-                }
-                csync();
-                if (tid < 256) {
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float *tr = Tm + (32 + i) * LS + 32;
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
-                        const float4 t4 = *reinterpret_cast<const float4 *>(tr + k);
-                        const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float4 p4 = *reinterpret_cast<const float4 *>(Pm + (k + e) * 36 + 4 * jq);
-                            acc.x = fmaf(tv[e], p4.x, acc.x);
-                            acc.y = fmaf(tv[e], p4.y, acc.y);
-                            acc.z = fmaf(tv[e], p4.z, acc.z);
-                            acc.w = fmaf(tv[e], p4.w, acc.w);
-                        }
-                    }
-                    *reinterpret_cast<float4 *>(Tm + (32 + i) * LS + 4 * jq) =
-                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-                }
+            // Level 2: T_[23][01] = -T_[23][23] (L_[23][01] T_[01][01]) on 32 x 32 blocks, as two tf32
+            // products on the tensor cores (M = 128, the 32 rows of interest in TMEM lanes 32-63; the other
+            // lanes hold products of rows that are not needed), both operands K-major.  P = L_[23][01] T_[01][01]:
+            // A = L's first column block read as 128 rows (L rows 32-63 are rows 32-63), B = T_[01][01]^T.
+            // Then T_[23][23] P: A = T's second column block read as 128 rows, B = P^T.
+            // Meanwhile the T image is written where it does not depend on this merge.
+            fence_proxy_async();
+            gsync(g);
+            if (gt == 0) {
+                mma_tf32_k32(tbg + 0, smem_u32(R + GR_L), smem_u32(R + GR_TT), idesc_tf32(128, 32), false);
+                mma_commit(bar_mma);
             }
-            csync();
-            // (T diag beta) image: row r, keys 8 jj .. 8 jj + 7; entries above the diagonal are zero
-            {
-                const int r = tid >> 3, jj = tid & 7;
-                const float4 t0v = *reinterpret_cast<const float4 *>(Tm + r * LS + 8 * jj);
-                const float4 t1v = *reinterpret_cast<const float4 *>(Tm + r * LS + 8 * jj + 4);
+            // (T diag beta) image into the dead key-0 image, rows 0-31 and the columns 32-63 of rows 32-63:
+            // item e -> (row r, 8-key chunk jj); entries above the diagonal are zero
+            for (int e = gt; e < 384; e += NCG) {
+                const int r = e < 256 ? (e >> 3) : 32 + ((e - 256) >> 2);
+                const int jj = e < 256 ? (e & 7) : 4 + ((e - 256) & 3);
+                const float4 t0v = *reinterpret_cast<const float4 *>(Tm + fimg(r, 8 * jj));
+                const float4 t1v = *reinterpret_cast<const float4 *>(Tm + fimg(r, 8 * jj + 4));
                 const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
                 float o[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = (8 * jj + e <= r) ? tv[e] * bet[8 * jj + e] : 0.f;
-                *reinterpret_cast<uint4 *>(sm + J_TIMG + img_chunk_off(64, r, jj)) = pack8(o);
+                for (int q = 0; q < 8; ++q) o[q] = (8 * jj + q <= r) ? tv[q] * bet[8 * jj + q] : 0.f;
+                *reinterpret_cast<uint4 *>(R + GR_K0 + img_chunk_off(64, r, jj)) = pack8(o);
+            }
+            ok = gwait(g, bar_mma, mph & 1);
+            ++mph;
+            if (!ok) break;
+            fence_after_sync();
+            const bool mid = (gw & 3) == 1;  // the warps of TMEM lanes 32-63 (rows 32-63), 16 columns each
+            const int c16 = 16 * (gw >> 2);
+            if (mid) {  // P row `lane` (TMEM lane 32 + lane), columns c16 .. c16 + 15 -> column `lane` of P^T
+                float d[16];
+                tmem_ld16(tmem_addr(tbg + c16, 32, 0), d);
+                float *Pt = (float *)(R + GR_P);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) Pt[fimg(c16 + e, lane)] = d[e];
             }
             fence_proxy_async();
-            csync();
-            if (tid == 0) {
-                // W = (T diag beta) X: A = the T image read as 128 rows (rows 64-127 are the A image behind
-                // it and land in unused TMEM lanes), B = X (MN-major).  U^T = V^T (T diag beta)^T: A = V
-                // (MN-major, M = d_v), B = the T image (K-major, 64 rows).
-                mma_bf16_kmn(tb + TM_DW, smem_u32(sm + J_TIMG), 128, smem_u32(stg + J_TK), 8192, 4,
-                             idesc_bf16(128, 128, false, true), false);
-                mma_bf16_mnk(tb + TM_DUT, smem_u32(stg + J_TV), 8192, smem_u32(sm + J_TIMG), 64, 4,
-                             idesc_bf16(128, 64, true, false), false);
+            gsync(g);
+            if (gt == 0) {
+                mma_tf32_k32(tbg + 32, smem_u32(R + GR_T + 8192), smem_u32(R + GR_P), idesc_tf32(128, 32), false);
                 mma_commit(bar_mma);
             }
-            ok = cwait(bar_mma, mph & 1);
+            ok = gwait(g, bar_mma, mph & 1);
+            ++mph;
+            if (!ok) break;
+            fence_after_sync();
+            if (mid) {  // T_[23][01] = -(T_[23][23] P): row 32 + lane, keys c16 .. c16 + 15, times beta, into the T image
+                float d[16];
+                tmem_ld16(tmem_addr(tbg + 32 + c16, 32, 0), d);
+                const int r = 32 + lane;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    float o[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) o[q] = -d[8 * h2 + q] * bet[c16 + 8 * h2 + q];
+                    *reinterpret_cast<uint4 *>(R + GR_K0 + img_chunk_off(64, r, (c16 >> 3) + h2)) = pack8(o);
+                }
+            }
+            fence_proxy_async();
+            gsync(g);
+            if (gt == 0) {
+                mbar_arrive(inv_done);  // L and T are dead: the producer loads the next q, z, k tiles
+                ok = mbar_wait(ld_v, par);
+                if (ok) {
+                    // W = (T diag beta) X: A = the T image read as 128 rows (rows 64-127 are the A image behind
+                    // it and land in unused TMEM lanes), B = X (MN-major).  U^T = V^T (T diag beta)^T: A = V
+                    // (MN-major, M = d_v), B = the T image (K-major, 64 rows).
+                    mma_bf16_kmn(tbg + TM_DW, smem_u32(R + GR_K0), 128, smem_u32(R + GR_X), 8192, 4,
+                                 idesc_bf16(128, 128, false, true), false);
+                    mma_bf16_mnk(tbg + TM_DUT, smem_u32(R + GR_V), 8192, smem_u32(R + GR_K0), 64, 4,
+                                 idesc_bf16(128, 64, true, false), false);
+                    mma_commit(bar_mma);
+                }
+            }
+            ok = gsync_and(g, ok);
+            if (!ok) break;
+            ok = gwait(g, bar_mma, mph & 1);
             ++mph;
             if (!ok) break;
             fence_after_sync();
             // ---- W rows (token-major, TMEM lanes 0-63) into the dead X tile, U^T rows (value channels,
             //      all lanes) into the dead V tile
-            if ((warp & 3) < 2) {
-                const int r = 32 * (warp & 3) + lane, cq = warp >> 2;  // columns [32 cq, 32 cq + 32)
-                float d[32];
-                tmem_ld32(tmem_addr(tb + TM_DW, 32 * (warp & 3), 32 * cq), d);
+            if ((gw & 3) < 2) {
+                const int r = 32 * (gw & 3) + lane, cq = gw >> 2;  // columns [64 cq, 64 cq + 64)
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                    *reinterpret_cast<uint4 *>(stg + J_TK + img_chunk_off(64, r, 4 * cq + jj)) = pack8(d + 8 * jj);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    float d[32];
+                    tmem_ld32(tmem_addr(tbg + TM_DW, 32 * (gw & 3), 64 * cq + 32 * h2), d);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        *reinterpret_cast<uint4 *>(R + GR_X + img_chunk_off(64, r, 8 * cq + 4 * h2 + jj)) =
+                            pack8(d + 8 * jj);
+                }
             }
             {
-                const int vr = 32 * (warp & 3) + lane, tq = warp >> 2;  // tokens [16 tq, 16 tq + 16)
-                float d[16];
-                tmem_ld16(tmem_addr(tb + TM_DUT, 32 * (warp & 3), 16 * tq), d);
-                *reinterpret_cast<uint4 *>(stg + J_TV + img_chunk_off(128, vr, 2 * tq)) = pack8(d);
-                *reinterpret_cast<uint4 *>(stg + J_TV + img_chunk_off(128, vr, 2 * tq + 1)) = pack8(d + 8);
+                const int vr = 32 * (gw & 3) + lane, tq = gw >> 2;  // tokens [32 tq, 32 tq + 32)
+                float d[32];
+                tmem_ld32(tmem_addr(tbg + TM_DUT, 32 * (gw & 3), 32 * tq), d);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    *reinterpret_cast<uint4 *>(R + GR_V + img_chunk_off(128, vr, 4 * tq + jj)) = pack8(d + 8 * jj);
             }
+            // Q^ and K~ went to the packet by plain stores: the group barrier orders them before thread 0's
+            // arrival (release), and the producer's flag store (release, GPU scope) publishes them with the
+            // rest of the packet
             fence_proxy_async();
-            csync();
-            if (tid == 0) mbar_arrive(&bar_pw[s]);  // the item is done: the producer writes its packet
+            gsync(g);
+            if (gt == 0) mbar_arrive(wu_ready);  // the producer writes the rest of the packet
         }
-        if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
+        if (!ok && gt == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     }
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, 256);
+    if (tid < 2) {  // the group regions are reused as plain memory after this role
+        uint64_t *b = (uint64_t *)(sm + tid * GR_BYTES + GR_BAR);
+        for (int i = 0; i < 7; ++i) mbar_inval(&b[i]);
+        mbar_inval((uint64_t *)(sm + J_TOK) + tid);
+    }
+    if (warp == 0) tmem_dealloc(tb, 512);
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(NT2, 1)
@@ -798,8 +915,8 @@ constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 9: packet load
 //   V~     V~^T = U^T - D[:, 0:64] (U^T from the packet) as bf16 pairs into tensor memory
 //   MMA3   S^T += V~^T K~              the decay Diag(gamma) was applied to S^T by the CUDA cores
 //   S      bf16 copy of S_{k+1}^T, then S^T scaled by gamma_{k+1} (per column)
-//   MMA2   D[:, 64:128] += V~^T A^T    O^T = (Q^ S + A V~)^T, issued after MMA1 of chunk k + 1 so that
-//                                      the in-order tensor pipe runs it during the next V~ phase
+//   MMA2   D[:, 64:128] += V~^T A^T    O^T = (Q^ S + A V~)^T, issued after MMA3 of chunk k + 1 so that
+//                                      the in-order tensor pipe runs it behind the next state update
 // The output warps read O^T of chunk k once its MMAs are done, release the D buffer, and store o
 // through a staging tile and TMA.
 // Tensor memory columns: S^T fp32 [0, 128), D buffers [128, 384), bf16 S^T [384, 448), bf16 V~^T
@@ -814,11 +931,13 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                                            const float *__restrict__ seg_in, int H,
                                            const unsigned char *__restrict__ packets, float scale,
                                            const float *initial_state, float *final_state, bf16 *__restrict__ o,
-                                           int *err, int g, int h, const uint64_t *flags, uint64_t epoch) {
-    // segment g of sequence n, head h: chunks [kk0, kk0 + nc) of the sequence
-    if (g >= seg_start[N]) return;
-    int n = 0;
-    {
+                                           int *err, int g, int h, const uint64_t *flags, uint64_t epoch,
+                                           uint64_t *consumed = nullptr, bool relinquish = true) {
+    // segment g of sequence n, head h: chunks [kk0, kk0 + nc) of the sequence (without seg_start, one
+    // segment per sequence: g = n)
+    if (seg_start ? g >= seg_start[N] : g >= N) return;
+    int n = g;
+    if (seg_start) {
         int lo = 0, hi = N;  // largest n with seg_start[n] <= g
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
@@ -826,7 +945,7 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
         }
         n = lo;
     }
-    const int seg_i = g - seg_start[n], nseg = seg_start[n + 1] - seg_start[n];
+    const int seg_i = seg_start ? g - seg_start[n] : 0, nseg = seg_start ? seg_start[n + 1] - seg_start[n] : 1;
     const bool last_seg = (seg_i == nseg - 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lq = warp & 3;           // TMEM lane quarter
@@ -871,7 +990,8 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
         mbar_init(&bar_vt[1], 8);
         *s_fail = 0;
     }
-    if (warp == 0) tmem_alloc(tslot, 512);
+    // a CTA that runs several chains keeps its right to allocate tensor memory
+    if (warp == 0) tmem_alloc(tslot, 512, relinquish);
     fence_proxy_async();  // barrier init visible to the async proxy
     sync_all();
     const uint32_t tb = *tslot;
@@ -880,8 +1000,12 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
     auto stage = [&](int kk) { return sm + (kk & 1) * CS_ST_BYTES; };
     auto acquire = [&](int kk) {  // the packet of chunk kk is published (false: it never was)
         if (flags) {
-            if (!flag_wait(flags + ((size_t)(c_begin + kk) * H + h), epoch)) return false;
+            const size_t item = (size_t)(c_begin + kk) * H + h;
+            if (!flag_wait(flags + item, epoch)) return false;
             fence_proxy_async_global();
+            // its producer may now run further ahead (the mark only paces production; packets are never
+            // reused within a launch)
+            if (consumed) asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(consumed + item), "l"(epoch) : "memory");
         }
         return true;
     };
@@ -916,13 +1040,16 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                 fence_after_sync();
                 mma_ts_k(tDbuf(kk), tb + TM_SB, smem_u32(P + PK_WQ), 128, 8, id1, false);
                 mma_commit(bar_v);
-                if (kk > 0) mma2(kk - 1);
                 ok = mbar_wait_spin(&bar_vt[kk & 1], (kk >> 1) & 1);  // V~^T written, S^T scaled by gamma_kk
                 ok = ok && mbar_wait_spin(&bar_ld2[kk & 1], (kk >> 1) & 1);  // part 2 of packet kk
                 if (!ok) break;
                 fence_after_sync();
                 mma_ts_mn(tb + TM_S, tb + TM_VT + 32 * (kk & 1), smem_u32(P + PK_K), 8192, 4, id3, true);
                 mma_commit(bar_s);
+                // the previous chunk's output product runs behind this chunk's state update (off the
+                // recurrence's critical path); the in-order pipe still finishes it before MMA1 of chunk
+                // kk + 1 rewrites its D buffer or the recurrence warps rewrite its V~ buffer
+                if (kk > 0) mma2(kk - 1);
             }
             if (ok && nc > 0) mma2(nc - 1);
             if (!ok) atomicExch(s_fail, 1);
@@ -1132,7 +1259,11 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
     __syncthreads();
     if (tid == 0 && *(volatile int *)s_fail) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     sync_all();
+    if (tid == 0) {  // the CTA may run another chain over the same shared memory
+        for (int i = 0; i < 13; ++i) mbar_inval(bar_ld1 + i);
+    }
     if (warp == 0) tmem_dealloc(tb, 512);
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(NT3, 1)
@@ -1214,6 +1345,115 @@ chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant
     } else {
         intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, cs, H, packets, err, b - n_chain,
                    (int)gridDim.x - n_chain, flags, epoch, kpre, -1, 0);
+    }
+}
+
+// =====================================================================================
+// Intra-chunk work and the output pass in one launch, for inputs with many chains: the grid is cut into
+// `teams` teams of one chain CTA and K producer CTAs.  The chains (one per sequence and head) are dealt
+// to the teams longest first, in snake order (team 0, 1, ..., T - 1, T - 1, ..., 0, ...), which balances
+// their lengths; a team's chain CTA runs its chains one after another, and its producers produce their
+// chunks in that order, at most `window` of their own items ahead of the chain.  Packets are published
+// through `flags` as in the fused launch and are consumed soon after they are written, so they are read
+// from L2 and dropped from it unwritten.  Launched cooperatively (every CTA resident); every wait is
+// bounded.
+constexpr int TEAM_MAX_CHAINS = 1024;  // chains per team the producers' table holds
+constexpr uint32_t J_TCH = J_SS + 4 * (J_TBL_N + 2);   // team mode: chain table [TEAM_MAX_CHAINS]
+constexpr uint32_t J_TPRE = J_TCH + 4 * TEAM_MAX_CHAINS;  //            item prefix [TEAM_MAX_CHAINS + 1]
+constexpr uint32_t J_TEAM_TOTAL = J_TPRE + 4 * (TEAM_MAX_CHAINS + 1) + 1024;
+
+__global__ void __launch_bounds__(NT2, 1)
+chunk_team_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant__ CUtensorMap omap,
+                     const bf16 *__restrict__ beta, const float *__restrict__ bias, const float *__restrict__ A_log,
+                     float g_min, int64_t T, int N, const int32_t *__restrict__ cu, int H,
+                     unsigned char *__restrict__ packets, float scale, const float *initial_state,
+                     float *final_state, bf16 *__restrict__ o, int *err, int teams, int K, int window,
+                     uint64_t *flags, uint64_t *consumed, uint64_t epoch) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = align1024(smem_raw);
+    const int b = (int)blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int32_t *cs = (int32_t *)(sm + J_CS);    // chunk_start [N + 1]
+    int32_t *perm = (int32_t *)(sm + J_SS);  // sequences by decreasing chunk count
+    int *s_bad = (int *)(sm + J_SS + 4 * (J_TBL_N + 1));
+    if (warp == 0) {  // validate cu_seqlens (0 = c_0 <= ... <= c_N = T) and count chunks per sequence
+        bool bad = false;
+        if (cu) {
+            for (int n = lane; n <= N; n += 32) {
+                const int64_t x = cu[n];
+                bad = bad || (n == 0 && x != 0) || (n == N && x != T) || (n > 0 && x < (int64_t)cu[n - 1]);
+            }
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        int carry = 0;
+        for (int base = 0; base < N; base += 32) {
+            const int m = base + lane;
+            int x = 0;
+            if (m < N && !bad) {
+                const int64_t len = cu ? (int64_t)cu[m + 1] - cu[m] : T / N;
+                x = (int)((len + C - 1) / C);
+            }
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            if (m < N) cs[m + 1] = carry + x;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) {
+            cs[0] = 0;
+            *s_bad = bad ? 1 : 0;
+        }
+    }
+    __syncthreads();
+    if (*(volatile int *)s_bad) {
+        if (b == 0 && tid == 0) set_error(err, KDA_ERR_BAD_SEQLENS);
+        return;
+    }
+    for (int n = tid; n < N; n += blockDim.x) {  // rank by (chunks descending, index ascending)
+        const int cn = cs[n + 1] - cs[n];
+        int r = 0;
+        for (int m = 0; m < N; ++m) {
+            const int cm = cs[m + 1] - cs[m];
+            r += (cm > cn || (cm == cn && m < n)) ? 1 : 0;
+        }
+        perm[r] = n;
+    }
+    __syncthreads();
+    const int t = b / (K + 1), role = b % (K + 1);
+    if (t >= teams) return;
+    const int chains = N * H;
+    auto chain_of = [&](int blk) -> int {  // rank of the team's blk-th chain, or -1
+        const int r = blk * teams + ((blk & 1) ? teams - 1 - t : t);
+        return r < chains ? r : -1;
+    };
+    if (role == 0) {
+        for (int blk = 0;; ++blk) {
+            const int r = chain_of(blk);
+            if (r < 0) break;
+            chain_role(sm, omap, T, N, cu, cs, nullptr, (int64_t)1 << 30, nullptr, H, packets, scale, initial_state,
+                       final_state, o, err, perm[r / H], r % H, flags, epoch, consumed, false);
+        }
+    } else {
+        int32_t *tch = (int32_t *)(sm + J_TCH), *tpre = (int32_t *)(sm + J_TPRE);
+        __shared__ int s_count;
+        if (tid == 0) {
+            int c = 0;
+            tpre[0] = 0;
+            for (int blk = 0; c < TEAM_MAX_CHAINS; ++blk) {
+                const int r = chain_of(blk);
+                if (r < 0) break;
+                const int n = perm[r / H];
+                tch[c] = n * H + r % H;
+                tpre[c + 1] = tpre[c] + (cs[n + 1] - cs[n]);
+                ++c;
+            }
+            s_count = c;
+        }
+        __syncthreads();
+        const TeamItems ti{tch, tpre, s_count, K, role - 1, window, consumed};
+        intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, cs, H, packets, err, 0, 1, flags, epoch, 0, -1, 0,
+                   &ti);
     }
 }
 
@@ -1624,9 +1864,20 @@ static kda_status_t set_smem(const void *kernel, uint32_t bytes) {
 // The fused schedule: one cooperative launch of chains + producers.  Returns false (and clears the
 // launch error) when the device refuses to make every CTA resident; the caller then runs the
 // separate kernels, which need the same workspace.
+// A launch epoch for the packet flags: a per-process counter that never repeats (and is never 0).
+static uint64_t next_launch_epoch() {
+    static std::atomic<uint64_t> next_epoch{0};
+    uint64_t expected = 0;  // first use: start the epochs at a value unlikely to sit in fresh memory
+    if (next_epoch.load() == 0)
+        next_epoch.compare_exchange_strong(
+            expected, ((uint64_t)std::chrono::steady_clock::now().time_since_epoch().count() << 20) | 1u);
+    uint64_t epoch = next_epoch.fetch_add(1);
+    if (epoch == 0) epoch = next_epoch.fetch_add(1);
+    return epoch;
+}
+
 static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws, cudaStream_t stream,
                          const tcp::TileMaps &tm, const CUtensorMap &omap, int sms, int *err) {
-    static std::atomic<uint64_t> next_epoch{0};
     const uint32_t smem = tcp::J_TOTAL > tcp::CS_TOTAL ? tcp::J_TOTAL : tcp::CS_TOTAL;
     if (set_smem((const void *)tcp::chunk_fused_tc_kernel, smem) != KDA_OK) return false;
     int per_sm = 0;
@@ -1634,12 +1885,7 @@ static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void 
             cudaSuccess ||
         per_sm < 1)
         return false;
-    uint64_t expected = 0;  // first use: start the epochs at a value unlikely to sit in fresh memory
-    if (next_epoch.load() == 0)
-        next_epoch.compare_exchange_strong(
-            expected, ((uint64_t)std::chrono::steady_clock::now().time_since_epoch().count() << 20) | 1u);
-    uint64_t epoch = next_epoch.fetch_add(1);
-    if (epoch == 0) epoch = next_epoch.fetch_add(1);
+    uint64_t epoch = next_launch_epoch();
     uint64_t *flags = (uint64_t *)((char *)ws + p.off_flags);
     unsigned char *packets = (unsigned char *)ws + p.off_records;
     const bf16 *beta = (const bf16 *)a->beta;
@@ -1654,6 +1900,39 @@ static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void 
                     &scale, &init, &fin, &o, &err, &n_chain, &flags, &epoch, &kpre};
     if (cudaLaunchCooperativeKernel((const void *)tcp::chunk_fused_tc_kernel, dim3((unsigned)sms), dim3(tcp::NT2),
                                     args, smem, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
+// The chain-team schedule (see chunk_team_tc_kernel).  Returns false (and clears the launch error)
+// when the device refuses to make every CTA resident; the caller then runs the separate kernels.
+static bool launch_team(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws, cudaStream_t stream,
+                        const tcp::TileMaps &tm, const CUtensorMap &omap, int sms, int *err, uint64_t epoch) {
+    const uint32_t smem = tcp::J_TEAM_TOTAL > tcp::CS_TOTAL ? tcp::J_TEAM_TOTAL : tcp::CS_TOTAL;
+    if (set_smem((const void *)tcp::chunk_team_tc_kernel, smem) != KDA_OK) return false;
+    int per_sm = 0;
+    const int grid = p.teams * (p.team_k + 1);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tcp::chunk_team_tc_kernel, tcp::NT2, smem) !=
+            cudaSuccess ||
+        per_sm < 1 || grid > sms * per_sm)
+        return false;
+    uint64_t *flags = (uint64_t *)((char *)ws + p.off_flags);
+    uint64_t *consumed = (uint64_t *)((char *)ws + p.off_consumed);
+    unsigned char *packets = (unsigned char *)ws + p.off_records;
+    const bf16 *beta = (const bf16 *)a->beta;
+    const float *bias = a->dt_bias, *A_log = a->A_log, *init = a->initial_state;
+    float g_min = a->g_min, scale = a->scale;
+    int64_t T = a->T;
+    int N = (int)a->N, H = p.H, teams = p.teams, K = p.team_k, window = p.team_window;
+    const int32_t *cu = a->cu_seqlens;
+    float *fin = a->final_state;
+    bf16 *o = (bf16 *)a->o;
+    void *args[] = {(void *)&tm, (void *)&omap, &beta, &bias, &A_log, &g_min, &T, &N, &cu, &H, &packets, &scale,
+                    &init, &fin, &o, &err, &teams, &K, &window, &flags, &consumed, &epoch};
+    if (cudaLaunchCooperativeKernel((const void *)tcp::chunk_team_tc_kernel, dim3((unsigned)grid), dim3(tcp::NT2), args,
+                                    smem, stream) != cudaSuccess) {
         (void)cudaGetLastError();
         return false;
     }
@@ -1688,6 +1967,11 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     const bool capturing = cap != cudaStreamCaptureStatusNone;
     if (p.fused && !capturing && p.max_chunks > 0 && a->T > 0 &&
         launch_fused(a, p, ws, stream, tm, omap, sms, err)) {
+        kda_profile_mark(1, stream);
+        return kda_cuda_status(cudaGetLastError());
+    }
+    if (p.team && !capturing && p.max_chunks > 0 && a->T > 0 &&
+        launch_team(a, p, ws, stream, tm, omap, sms, err, next_launch_epoch())) {
         kda_profile_mark(1, stream);
         return kda_cuda_status(cudaGetLastError());
     }

@@ -46,7 +46,12 @@ struct kda_chunk_plan {
     // published through 64-bit epoch flags, one per (chunk slot, head).
     int fused;               // (at most KDA_FUSED_MAX_SEQS sequences)
     int kpre;                // fused: chunks at the start of every sequence that its chains produce themselves
+    // Chain teams (tensor-core path, many chains): one cooperative launch of `teams` teams, each a
+    // chain CTA and team_k producer CTAs; producers run at most team_window of their own items ahead.
+    int team;                // 1 if the team schedule runs (then fused = 0)
+    int teams, team_k, team_window;
     size_t off_flags;
+    size_t off_consumed;     // team schedule: per (chunk slot, head), the epoch once its chain has started on it
     size_t total_bytes;
 };
 

@@ -65,6 +65,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn = fals
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::tf32: D fp32, A and B tf32 (fp32 in memory, 10-bit mantissa used), dense.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool a_mn = false, bool b_mn = false) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A(smem desc) * B(smem desc)^T, issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -73,6 +79,22 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
         :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
+// kind::tf32 product of one K-block (K = 32 fp32 values, four K-steps of 8), both operands K-major SW128
+// images (rows of 128 bytes = 32 values along K; each K-step starts 32 bytes further along the rows).
+__device__ __forceinline__ void mma_tf32_k32(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, uint32_t idesc,
+                                             bool accumulate) {
+    const uint64_t da = desc_sw128(a_base), db = desc_sw128(b_base);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n"
+            :: "r"(d_tmem), "l"(da + (uint64_t)((32 * s) >> 4)), "l"(db + (uint64_t)((32 * s) >> 4)), "r"(idesc),
+               "r"((accumulate || s > 0) ? 1u : 0u)
+            : "memory");
+    }
+}
+
 // Full product over K = 16 * ksteps: A image with RA rows, B image with RB rows.  The descriptors
 // of later K-steps differ from the first only in the start-address field (address >> 4, no carry
 // out of its 14 bits for shared-memory addresses), so they are formed by integer adds.
@@ -239,6 +261,10 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int lane, int col) 
 // ---------------------------------------------------------------- mbarriers
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// Invalidates an mbarrier so that its shared memory can be used for something else.
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"

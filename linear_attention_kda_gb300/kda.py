@@ -405,7 +405,8 @@ def chunk_fwd_schedule(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, cu_s
                   gate_kind=_gate_kind(gate))
     out = (_i64 * 4)()
     _check(load_library().kda_chunk_fwd_schedule(ctypes.byref(a), out), "kda_chunk_fwd_schedule")
-    return {"fused": bool(out[0]), "own_chunks": int(out[1]), "seg_len": int(out[2]), "kernels": int(out[3])}
+    return {"fused": out[0] == 1, "team": out[0] == 2, "own_chunks": int(out[1]) if out[0] == 1 else 0,
+            "team_producers": int(out[1]) if out[0] == 2 else 0, "seg_len": int(out[2]), "kernels": int(out[3])}
 
 
 def chunk_fwd_static_ws(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0,

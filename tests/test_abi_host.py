@@ -335,7 +335,8 @@ def test_empty_batch_plan(lib):
     tensor-core path).  The epilogue, given, has no tokens to run over."""
     for dt, d in ((torch.bfloat16, 128), (torch.float32, 64), (torch.bfloat16, 64)):
         s = kda.chunk_fwd_schedule(0, 3, 32, d, d, dt)
-        assert s == {"fused": False, "own_chunks": 0, "seg_len": 0, "kernels": 2}, (dt, d)
+        assert s == {"fused": False, "team": False, "own_chunks": 0, "team_producers": 0, "seg_len": 0,
+                     "kernels": 2}, (dt, d)
         assert kda.chunk_fwd_workspace_size(0, 3, 32, d, d, dt) > 0
     a = kda.ChunkArgs(T=0, N=3, H=32, dk=128, dv=128, dtype=kda.KDA_BF16, chunk_size=64, out_gate=16)
     assert lib.kda_chunk_fwd_kernel_count(ctypes.byref(a)) == 2
@@ -372,14 +373,14 @@ def test_schedule_decisions_for_the_workloads(lib):
     - the varlen batch (32 sequences x 32 heads) takes the separate kernels."""
     from linear_attention_kda_gb300 import synthetic as syn
     bf = torch.bfloat16
-    assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, bf) == {"fused": True, "own_chunks": 4, "seg_len": 0,
-                                                                  "kernels": 1}
+    assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, bf) == {"fused": True, "team": False, "own_chunks": 4,
+                                                                  "team_producers": 0, "seg_len": 0, "kernels": 1}
     assert kda.chunk_fwd_schedule(1 << 20, 1, 32, 128, 128, bf)["fused"]
     s = kda.chunk_fwd_schedule(1 << 20, 1, 2, 128, 128, bf)
     assert not s["fused"] and s["seg_len"] > 0 and s["kernels"] == 5
     lengths = syn.seq_lengths(syn.VARLEN_32, 1)
     s = kda.chunk_fwd_schedule(sum(lengths), 32, 32, 128, 128, bf, syn.cu_seqlens_of(lengths))
-    assert s == {"fused": False, "own_chunks": 0, "seg_len": 0, "kernels": 3}
+    assert s == {"fused": False, "team": False, "own_chunks": 0, "team_producers": 0, "seg_len": 0, "kernels": 3}
     # the fp32 path and the softplus gate never take the tensor-core schedules
     assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, torch.float32)["kernels"] == 3
     assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, bf, gate="softplus")["kernels"] == 3

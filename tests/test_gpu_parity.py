@@ -657,3 +657,53 @@ def test_debug_checks_report_non_finite_outputs():
     kda.chunk_fwd(*(d[n].cuda() for n in ("q", "k", "v", "z", "beta", "dt_bias", "A_log")),
                   cu_seqlens=d["cu_seqlens"].cuda(), output_final_state=True)
     assert kda.get_device_error() == 0
+
+
+def _team_case(seed, lengths, H=8):
+    w = syn.Workload("team", H=H, d=128, dtype="bf16", seq_len=None, z_std=1.5, b_range=1.0,
+                     alog_std=0.25, s0_std=0.02)
+    d = _varlen(w, lengths, seed=seed)
+    sch = kda.chunk_fwd_schedule(sum(lengths), len(lengths), H, 128, 128, torch.bfloat16, d["cu_seqlens"])
+    assert sch["team"] and sch["kernels"] == 1, sch
+    return d
+
+
+def test_team_schedule_varlen_with_states():
+    """The chain-team launch (many chains: 20 sequences x 8 heads) on a ragged batch with empty,
+    one-token, one-chunk and unaligned sequences and initial states: every (sequence, head) against
+    the oracle; an empty sequence's final state is its initial state bit for bit."""
+    rng = np.random.default_rng(71)
+    lengths = [int(x) for x in rng.integers(0, 400, size=20)]
+    lengths[3], lengths[7], lengths[11], lengths[15] = 0, 1, 64, 65
+    d = _team_case(72, lengths)
+    o, fs = run_prefill(d)
+    compare_prefill(d, o, fs, oracle_prefill(d), TOL_BF16)
+    assert torch.equal(fs[3], d["initial_state"][3])
+
+
+def test_team_schedule_final_state_aliases_initial_state():
+    """In-place continuation under the chain-team launch: final_state is initial_state."""
+    rng = np.random.default_rng(73)
+    lengths = [int(x) for x in rng.integers(100, 700, size=24)]
+    d = _team_case(74, lengths)
+    ref = oracle_prefill(d)
+    dev = "cuda"
+    st = d["initial_state"].to(dev).clone()
+    o, _ = kda.chunk_fwd(*(d[n].to(dev) for n in ("q", "k", "v", "z", "beta", "dt_bias", "A_log")),
+                         cu_seqlens=d["cu_seqlens"].to(dev), cu_seqlens_host=d["cu_seqlens"],
+                         initial_state=st, final_state=st)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    compare_prefill(d, o.float().cpu(), st.cpu(), ref, TOL_BF16)
+
+
+def test_team_schedule_bad_cu_seqlens_reports_device_error():
+    """The chain-team launch validates cu_seqlens in every CTA and runs nothing when it is inconsistent."""
+    lengths = [100] * 20
+    d = _team_case(75, lengths)
+    cu = d["cu_seqlens"].clone()
+    cu[6] = int(cu[5]) - 1  # no longer non-decreasing
+    dev = "cuda"
+    kda.chunk_fwd(*(d[n].to(dev) for n in ("q", "k", "v", "z", "beta")), None, None, cu_seqlens=cu.to(dev),
+                  cu_seqlens_host=d["cu_seqlens"], output_final_state=True)
+    assert kda.get_device_error() == 7
