@@ -717,6 +717,30 @@ def run_ours(args, rank, ws, local):
                 lb.synchronize()
                 lts.append(la.elapsed_time(lb))
             msl = sum(lts) / len(lts)
+            epi_l = None
+            if not args.no_epilogue:  # the same step with the Eq. 6 epilogue (applied inside the output pass)
+                gl, wl_ = syn.make_output_gate_inputs(Tl, H, D, "bf16", 35, device=dev)
+
+                def step_le():
+                    kda.chunk_fwd(dl["q"], dl["k"], dl["v"], dl["z"], dl["beta"], dl["dt_bias"], dl["A_log"],
+                                  cu_seqlens=dl["cu_seqlens"], cu_seqlens_host=cul,
+                                  initial_state=dl["initial_state"], final_state=fsl, workspace=wl, out=ol,
+                                  out_gate=gl, out_norm_weight=wl_, out_norm_eps=1e-6)
+
+                step_le()
+                torch.cuda.synchronize()
+                assert kda.get_device_error() == 0
+                ets = []
+                for _ in range(3):
+                    la.record(stream)
+                    step_le()
+                    lb.record(stream)
+                    lb.synchronize()
+                    ets.append(la.elapsed_time(lb))
+                mse = sum(ets) / len(ets)
+                epi_l = {"with_epilogue_ms_per_step": mse, "overhead": mse / msl - 1.0,
+                         "kernels": kda.chunk_fwd_kernel_count(Tl, Nl, H, D, D, dl["q"].dtype, cul, out_gate=True)}
+                del gl, wl_
             fll = prefill_flops(Ls, H, D, D)
             byl = prefill_bytes(Tl, Nl, H, D, D, 2, dl["initial_state"] is not None, True)
             tfl = fll["total"] / (msl / 1e3) / 1e12
@@ -726,7 +750,7 @@ def run_ours(args, rank, ws, local):
                 "tflops": tfl, "tflops_dense_tile": fll["dense_tile"] / (msl / 1e3) / 1e12,
                 "frac_bf16_peak": tfl / tc, "hbm_gbs_algorithmic": byl["total"] / (msl / 1e3) / 1e9,
                 "frac_hbm": byl["total"] / (msl / 1e3) / 1e9 / hbm,
-                "schedule": schedule_name(sch_l), "kernels": sch_l["kernels"]}
+                "schedule": schedule_name(sch_l), "kernels": sch_l["kernels"], "epilogue": epi_l}
             del dl, fsl, ol, wl
             torch.cuda.empty_cache()
 

@@ -140,8 +140,11 @@ typedef struct {
     void *o;                       /* [T, H, dv] output; must not alias an input */
     int32_t chunk_size;            /* 64, or 0 for the default (64) */
     /* Optional output epilogue (Eq. 6 without its projections; see kda_output_gate): when out_gate
-     * is set, o receives Sigmoid(out_gate) * RMSNorm(o~) instead of the recurrent output o~, by a
-     * kda_output_gate pass over o (in place) after the recurrence. */
+     * is set, o receives Sigmoid(out_gate) * RMSNorm(o~) instead of the recurrent output o~ (the norm
+     * taken on o~ rounded to the dtype of o, as kda_output_gate would read it).  The tensor-core path
+     * applies it in its output pass before o is stored, except on the one-launch schedule for chains
+     * shorter than 256 chunks, which (like the fp32 path) runs a kda_output_gate pass over o in place
+     * after the recurrence. */
     const void *out_gate;          /* [T, H, dv], dtype of o, 16-byte aligned, or NULL (no epilogue) */
     const float *out_norm_weight;  /* [H, dv] RMSNorm weight, 16-byte aligned, or NULL (ones) */
     float out_norm_eps;            /* RMSNorm epsilon, > 0 when out_gate is set */
@@ -400,6 +403,19 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *args);
  * report, section 5.1.2, Eq. 17), 0 when the pass does not run; out[3] =
  * kernels launched.  KDA_ERR_INVALID_ARG on NULL pointers or invalid sizes. */
 kda_status_t kda_chunk_fwd_schedule(const kda_chunk_args *args, int64_t *out);
+
+/* Not an operation of the paper: the schedule of the bf16 d = 128 tensor-core prefill, for tests and
+ * measurements.  KDA_SCHEDULE_AUTO (the default) lets the library's latency model choose; the others
+ * force the separate kernels, the fused launch or the chain-team launch when the problem is eligible
+ * for it (fused: sequences x heads + 16 <= SMs; team: at most 159 sequences), else the model's choice
+ * among what remains.  Every schedule computes the same result.  Process-wide; applies to later
+ * calls of kda_chunk_fwd, its workspace size and kda_chunk_fwd_schedule alike.  KDA_ERR_INVALID_ARG
+ * for an unknown mode. */
+#define KDA_SCHEDULE_AUTO 0
+#define KDA_SCHEDULE_SEPARATE 1
+#define KDA_SCHEDULE_FUSED 2
+#define KDA_SCHEDULE_TEAM 3
+kda_status_t kda_set_chunk_schedule(int32_t mode);
 
 #ifdef __cplusplus
 }

@@ -94,7 +94,7 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
     // then intra-chunk transform, [segment summaries, fold,] output pass; an empty batch (T = 0)
     // runs the chunk plan and the output pass alone, which passes the states through
     if (a->T == 0) return 2;
-    const int extra = a->out_gate ? 1 : 0;  // the output epilogue's pass
+    const int extra = (a->out_gate && !(p.path == 1 && p.epi_fused)) ? 1 : 0;  // the output epilogue's own pass
     if (p.fused || p.team) return 1 + extra;
     return (p.split ? 5 : 3) + extra;
 }
@@ -240,9 +240,10 @@ kda_status_t kda_chunk_fwd(const kda_chunk_args *a, void *workspace, size_t work
     if (st != KDA_OK) return st;
     st = p.path == 1 ? kda_launch_chunk_tc(a, p, workspace, (cudaStream_t)stream)
                      : kda_launch_chunk_simt(a, p, workspace, (cudaStream_t)stream);
-    if (st == KDA_OK && a->out_gate) {
-        // the output epilogue runs as its own HBM-bound pass over o, in place, on all SMs (inside the
-        // output pass it would lengthen the latency-bound chain more than the round trip of o costs)
+    if (st == KDA_OK && a->out_gate && !(p.path == 1 && p.epi_fused)) {
+        // the output epilogue as its own HBM-bound pass over o, in place, on all SMs: the fp32 path, and
+        // the fused launch on short chains (inside their output pass it would lengthen the latency-bound
+        // chain more than the round trip of o costs)
         kda_output_gate_args og{a->T, a->H, a->dv, a->dtype, a->o, a->out_gate, a->out_norm_weight,
                                 a->out_norm_eps, a->o};
         st = kda_launch_output_gate(&og, (cudaStream_t)stream);

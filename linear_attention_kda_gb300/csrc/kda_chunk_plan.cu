@@ -11,6 +11,7 @@
 #include "kda_internal.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 namespace kda {
@@ -129,7 +130,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Uses per-sequence lengths when the host copy of cu_seqlens is given.
 constexpr double T_ITEM = 6.5, T_COLD = 13.5, T_CHAIN = 1.15, T_SUM = 2.3, T_FOLD = 1.8, T_LAUNCH = 4.0;
 constexpr double T_CHAIN_START = 3.0;      // a chain CTA switching to its next chain (team schedule)
-constexpr double TEAM_MAX_CHAINS_HOST = 1024;  // chains per team the producers' table holds
+constexpr double TEAM_MAX_CHAINS_HOST = 512;  // chains per team the producers' table holds
 
 struct tc_schedule {
     int64_t seg_len;  // 1 << 30: no split
@@ -139,7 +140,8 @@ struct tc_schedule {
     int teams, team_k;
 };
 
-static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int32_t *cu_host, int sms) {
+static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int32_t *cu_host, int sms,
+                                   int force = KDA_SCHEDULE_AUTO) {
     tc_schedule r{(int64_t)1 << 30, false, 0, false, 0, 0};
     if (T == 0) return r;
     int64_t total = 0, longest = 0;
@@ -158,7 +160,9 @@ static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int
     // unsplit output pass: the longest chain, or the chains' total over the SMs
     const double unsplit = (double)longest > items / sms ? (double)longest : items / sms;
     double best = intra + unsplit * T_CHAIN + 2 * T_LAUNCH;
-    for (int64_t L = 8; L <= (1 << 14); L *= 2) {
+    if (force == KDA_SCHEDULE_SEPARATE) return r;
+    if (force == KDA_SCHEDULE_FUSED || force == KDA_SCHEDULE_TEAM) best = 1e300;  // any eligible one of that kind
+    for (int64_t L = 8; L <= (1 << 14) && force == KDA_SCHEDULE_AUTO; L *= 2) {
         if (L >= longest) break;
         int64_t segs = 0, segs_sum = 0, max_nseg = 0;
         for (int64_t n = 0; n < N; ++n) {
@@ -177,7 +181,7 @@ static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int
         }
     }
     const int64_t n_chain = N * H;
-    if (n_chain + 16 <= sms && N <= KDA_FUSED_MAX_SEQS) {
+    if (n_chain + 16 <= sms && N <= KDA_FUSED_MAX_SEQS && force != KDA_SCHEDULE_TEAM) {
         const double producers = (double)(sms - n_chain);
         for (int kp = 0; kp <= 8; ++kp) {
             double items_p = 0;
@@ -199,7 +203,7 @@ static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int
     }
     // chain teams: teams of one chain CTA and k producers; the chains, dealt longest first in snake
     // order, give every team about the same number of chunk steps
-    if (N <= KDA_FUSED_MAX_SEQS && n_chain > sms / 2 &&
+    if (N <= KDA_FUSED_MAX_SEQS && (n_chain > sms / 2 || force == KDA_SCHEDULE_TEAM) && force != KDA_SCHEDULE_FUSED &&
         (double)n_chain <= (double)(sms / 2) * TEAM_MAX_CHAINS_HOST) {
         for (int k = 1; k <= 8; ++k) {
             const int teams = sms / (k + 1);
@@ -221,6 +225,18 @@ static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int
         }
     }
     return r;
+}
+
+namespace {
+std::atomic<int> g_schedule_override{0};  // kda_set_chunk_schedule
+}
+
+int kda_chunk_schedule_override() { return g_schedule_override.load(std::memory_order_relaxed); }
+
+extern "C" kda_status_t kda_set_chunk_schedule(int32_t mode) {
+    if (mode < KDA_SCHEDULE_AUTO || mode > KDA_SCHEDULE_TEAM) return KDA_ERR_INVALID_ARG;
+    g_schedule_override.store(mode, std::memory_order_relaxed);
+    return KDA_OK;
 }
 
 bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_t dtype, int C,
@@ -248,20 +264,27 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
     p->kpre = 0;
     p->team = 0;
     p->teams = p->team_k = p->team_window = 0;
+    p->epi_fused = 0;
     p->seg_len = (int64_t)1 << 30;
     p->max_segs = N;
     if (p->path == 1) {
         int dev = 0, sms = 152;
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 152;
-        const tc_schedule sch = choose_schedule(T, N, H, C, cu_seqlens_host, sms);
+        const tc_schedule sch = choose_schedule(T, N, H, C, cu_seqlens_host, sms, kda_chunk_schedule_override());
         p->seg_len = sch.seg_len;
         p->fused = sch.fused ? 1 : 0;
         p->kpre = sch.kpre;
         p->team = sch.team ? 1 : 0;
         p->teams = sch.teams;
         p->team_k = sch.team_k;
-        p->team_window = 4;  // own items a producer may run ahead of its chain
+        p->team_window = 6;  // own items a producer may run ahead of its chain
+        int64_t longest = 0;
+        for (int64_t n = 0; n < N; ++n) {
+            const int64_t len = cu_seqlens_host ? (int64_t)cu_seqlens_host[n + 1] - cu_seqlens_host[n] : T / N;
+            longest = std::max(longest, (len + C - 1) / C);
+        }
+        p->epi_fused = (p->fused && longest < 256) ? 0 : 1;
         p->split = p->seg_len < ((int64_t)1 << 30) ? 1 : 0;
         p->max_segs = p->split ? p->max_chunks / p->seg_len + N : N;
     }

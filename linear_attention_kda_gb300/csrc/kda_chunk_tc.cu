@@ -57,7 +57,9 @@ constexpr uint32_t PK_P2 = PK_STRIDE - PK_K;  // bytes of part 2 (at PK_K)
 // the packet after them is prefetched into L2.
 constexpr uint32_t CS_ST_BYTES = PK_STRIDE;            // stage stride (multiple of 1024)
 constexpr uint32_t CS_OIMG = 2 * CS_ST_BYTES;          // o staging, 2 buffers x (64 tokens x 128, 2 x 8 KB)
-constexpr uint32_t CS_BAR = CS_OIMG + 32768;           // 13 mbarriers
+constexpr uint32_t CS_GIMG = CS_OIMG + 32768;          // output epilogue: gate tiles, 2 buffers (same layout)
+constexpr uint32_t CS_W = CS_GIMG + 32768;             // output epilogue: RMSNorm weight of the head, fp32 [128]
+constexpr uint32_t CS_BAR = CS_W + 512;                // 15 mbarriers
 constexpr uint32_t CS_TSLOT = CS_BAR + 128;            // TMEM base, failure flag
 constexpr uint32_t CS_TOTAL = CS_BAR + 192 + 1024;
 static_assert(PK_P1 <= PK_K && PK_P1 % 16 == 0 && PK_P2 % 16 == 0, "packet parts");
@@ -141,20 +143,20 @@ __device__ __forceinline__ bool locate(const int32_t *chunk_start, const int32_t
 
 // =====================================================================================
 // Persistent intra-chunk kernel: one CTA per SM walks the (chunk, head) work items
-// w = slot * H + h.  Its sixteen consumer warps form two groups of eight; group g takes the CTA's
-// items g, g + 2, g + 4, ... and owns a full set of buffers (a ~100 KB region of shared memory and
-// 256 tensor-memory columns), so that the two groups run out of phase: while one inverts (I + L)
-// (a latency-bound step), the other runs the gate and element pass of its next item (MUFU and
-// shared-memory bound).  Warp 16 + g is group g's producer: it fetches the q, z, k, v tiles
-// (128-byte-swizzled TMA boxes of 64 tokens x 64 channels), the item's beta, bias and e^{A_log},
-// and writes the packet by bulk copies.
+// w = slot * H + h.  Its sixteen warps form two groups of eight; group g takes the CTA's items g,
+// g + 2, g + 4, ... and owns a full set of buffers (a ~100 KB region of shared memory and 256
+// tensor-memory columns), so that the two groups run out of phase: while one inverts (I + L) (a
+// latency-bound step), the other runs the gate and element pass of its next item (MUFU and
+// shared-memory bound).  The group's first thread moves its data: the q, z, k, v tiles
+// (128-byte-swizzled TMA boxes of 64 tokens x 64 channels) and the item's beta, bias and e^{A_log}
+// in, the packet out by bulk copies.
 //
 // Tiles stay token-major ([token][channel], the TMA layout) from load to packet: tcgen05 reads a
 // token-major tile as a K-major operand when the contraction runs over channels and, through an
 // MN-major descriptor, as its transpose when it runs over tokens.  Per item:
-//   GATE gate (Eq. 5) and in-chunk cumulative log-decay G (Eq. 3); thread = (channel pair,
-//        16-token quarter), G kept in registers.
-//   ELEM element pass, same threads: every decay factor and operand image.  The q and z boxes are
+//   GATE gate (Eq. 5) and in-chunk cumulative log-decay G (Eq. 3), in base-2 units; thread = (16-byte
+//        chunk of 8 channels, 4 tokens), G kept in registers.
+//   ELEM element pass, same threads: every decay factor and operand image, 16 bytes per access.  The q and z boxes are
 //        loaded as one 128-row image [q; z]; it becomes the row image [q E; k E] in place.  Keys
 //        scaled to the second reference overwrite k; X = Gamma K goes to its own tile.  Q^ = Q Gamma
 //        and K~ = K e^{G_63 - G} go straight from registers to the packet in global memory.
@@ -175,9 +177,8 @@ __device__ __forceinline__ bool locate(const int32_t *chunk_start, const int32_t
 // the exponential of its own exponent, never a product of two large and small factors, so a key
 // factor that underflows loses at most e^{75 - 87} of a term.  Entries above the diagonal may
 // overflow to inf; they are discarded by selects and never multiplied.
-constexpr int NT2 = 576;      // 2 consumer groups x 8 warps + 2 producer warps
+constexpr int NT2 = 512;      // 2 consumer groups x 8 warps
 constexpr int NCG = 256;      // threads of a consumer group
-constexpr int PRODUCER = 16;  // producer warp of group g: PRODUCER + g
 // Per-group shared-memory region (offsets from the group's base, multiple of 1024)
 constexpr uint32_t GR_QZ = 0;          // 32 KB: TMA boxes q h0 | z h0 | q h1 | z h1 = a K-major 128-row image
                                        // [q; z]; then the row image [q E; k E]; after the A / L product the
@@ -191,8 +192,8 @@ constexpr uint32_t GR_GAM = 98304;     // gamma^C fp32 [128]
 constexpr uint32_t GR_TOT = GR_GAM + 512;    // quarter sums of the log-decays, fp32 [4][128]
 constexpr uint32_t GR_BETA = GR_TOT + 2048;  // 2 slots x fp32 [64]
 constexpr uint32_t GR_BIAS = GR_BETA + 512;  // 2 slots x fp32 [128]
-constexpr uint32_t GR_INFO = GR_BIAS + 1024; // 2 slots x {int64 t0, len, h, w; float eA} (64 B)
-constexpr uint32_t GR_BAR = GR_INFO + 128;   // mbarriers: ld_qzk, ld_v, a_ready, inv_done, wu_ready, pk_read, mma
+constexpr uint32_t GR_INFO = GR_BIAS + 1024; // 2 slots x {int64 t0, len, h, w; float e^{A_log}} (64 B)
+constexpr uint32_t GR_BAR = GR_INFO + 128;   // mbarriers: ld_qzk, ld_v, mma
 constexpr uint32_t GR_BYTES = 103424;        // 101 KB
 static_assert(GR_BAR + 64 <= GR_BYTES && GR_BYTES % 1024 == 0, "group region");
 // The fp32 L and T of the inverse are kept as SW128 images (fimg below): the tf32 products of its
@@ -204,11 +205,15 @@ constexpr uint32_t GR_TT = GR_K + 12288;     // T_11^T as a K-major tf32 image, 
 constexpr uint32_t J_SH = 2 * GR_BYTES;       // shared by both groups
 constexpr uint32_t J_TSLOT = J_SH;            // TMEM base
 constexpr uint32_t J_TOK = J_SH + 16;         // mbarriers tok[2]: group g may start its gate and element pass
-constexpr uint32_t J_TBL = J_SH + 64;         // int32 [J_TBL_N + 1]: producer chunks before each sequence
+// Tables a CTA keeps while it runs both roles (fused and team launches): past the shared memory of either
+constexpr uint32_t J_TAB0 = (J_SH + 64 > CS_BAR + 256 ? J_SH + 64 : CS_BAR + 256);
+constexpr uint32_t J_TBL = (J_TAB0 + 63) / 64 * 64;  // int32 [J_TBL_N + 1]: producer chunks before each sequence
 constexpr int J_TBL_N = KDA_FUSED_MAX_SEQS;   // sequences the table holds
 constexpr uint32_t J_CS = J_TBL + 4 * (J_TBL_N + 1);  // fused launch: chunk_start [N + 1]
 constexpr uint32_t J_SS = J_CS + 4 * (J_TBL_N + 1);   //               seg_start [N + 1], then a flag
-constexpr uint32_t J_TOTAL = J_SS + 4 * (J_TBL_N + 2) + 1024;
+constexpr uint32_t J_CU = J_SS + 4 * (J_TBL_N + 2);   // cu_seqlens [N + 1] (and chunk_start in J_CS), so that
+                                                      // the producers locate their items without global loads
+constexpr uint32_t J_TOTAL = J_CU + 4 * (J_TBL_N + 1) + 1024;
 // TMEM columns of a group (base + 256 g): the A / L product in [0, 96); later W in [0, 128) (lanes
 // 0-63) and U^T in [128, 192)
 constexpr uint32_t TM_DA = 0, TM_DW = 0, TM_DUT = 128;
@@ -272,6 +277,25 @@ __device__ __forceinline__ void inv_l1_partial(const float *Lm, const float *Tm,
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
+// Packed fp32 pairs: one instruction computes both lanes (round to nearest even, as the scalar forms).
+__device__ __forceinline__ unsigned long long f2u(float2 a) {
+    return (unsigned long long)__float_as_uint(a.x) | ((unsigned long long)__float_as_uint(a.y) << 32);
+}
+__device__ __forceinline__ float2 u2f(unsigned long long u) {
+    return make_float2(__uint_as_float((uint32_t)u), __uint_as_float((uint32_t)(u >> 32)));
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(r);
+}
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+    unsigned long long r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(r);
+}
+__device__ __forceinline__ uint32_t pack2(float2 a) { return pack_bf16(a.x, a.y); }
+
 // Packet publication between CTAs of one (cooperative) launch: the producer releases a flag once the
 // packet's writes have completed; the consumer acquires it before its bulk reads.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
@@ -290,13 +314,25 @@ __device__ __forceinline__ uint64_t flag_acquire(const uint64_t *f) {
     asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
     return v;
 }
-// Bounded wait (~1 s) for a packet flag to reach this launch's epoch.
+__device__ __forceinline__ uint64_t flag_relaxed(const uint64_t *f) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+    return v;
+}
+// Bounded wait (~1 s) for a packet flag to reach this launch's epoch.  The flag is polled with relaxed
+// loads (an acquiring load per poll would order, and slow, the SM's other memory traffic); the read that
+// sees the epoch is followed by an acquire fence, which orders the caller's later reads after it.
 __device__ __forceinline__ bool flag_wait(const uint64_t *f, uint64_t epoch) {
     if (flag_acquire(f) == epoch) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        for (int i = 0; i < 64; ++i)
-            if (flag_acquire(f) == epoch) return true;
+        for (int i = 0; i < 16; ++i) {
+            if (flag_relaxed(f) == epoch) {
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                return true;
+            }
+            __nanosleep(32);
+        }
         if (globaltimer_ns() - t0 > 1000000000ull) return false;
     }
 }
@@ -385,7 +421,8 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
     uint32_t *tslot = (uint32_t *)(sm + J_TSLOT);
     if (tid < 2) {
         uint64_t *b = (uint64_t *)(sm + tid * GR_BYTES + GR_BAR);
-        for (int i = 0; i < 7; ++i) mbar_init(&b[i], 1);
+        mbar_init(&b[0], 1 + 32);  // ld_qzk: the TMA arrival and one per lane of warp 0 (the item's slot)
+        for (int i = 1; i < 3; ++i) mbar_init(&b[i], 1);
         mbar_init((uint64_t *)(sm + J_TOK) + tid, 1);
     }
     if (warp == 0) tmem_alloc(tslot, 512, own_n < 0);
@@ -393,502 +430,553 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
     sync_all();
     const uint32_t tb = *tslot;
 
-    if (warp >= PRODUCER) {
-        // ------------------------------------------------ producer warp of group g: loads its items and
-        // writes their packets (bulk copies from shared memory), publishing each through `flags` once its
-        // writes have completed.  The next item's q, z and k tiles are loaded as soon as the inverse has
-        // freed their buffers, its v tile once the packet copies have read the current item's U^T.
-        const int g = warp - PRODUCER;
-        unsigned char *R = sm + g * GR_BYTES;
-        uint64_t *bar = (uint64_t *)(R + GR_BAR);
-        uint64_t *ld_qzk = bar, *ld_v = bar + 1, *a_ready = bar + 2, *inv_done = bar + 3, *wu_ready = bar + 4,
-                 *pk_read = bar + 5;
-        const int nj = (n_items - g + 1) / 2;  // items it = 2 j + g
-        auto load_qzk = [&](int j) {
-            const int64_t w = w_of(2 * j + g);
-            const int s = j & 1;
-            const int64_t slot = w / H;
-            const int h = (int)(w % H);
-            int n = 0, len = 0;
-            int64_t t0 = 0;
-            locate(chunk_start, cu, T, N, slot, n, t0, len);
-            float *bet = (float *)(R + GR_BETA) + 64 * s;
-            float *bia = (float *)(R + GR_BIAS) + 128 * s;
-#pragma unroll
-            for (int r = lane; r < C; r += 32) bet[r] = r < len ? __bfloat162float(beta[(t0 + r) * H + h]) : 0.f;
-#pragma unroll
-            for (int c = lane; c < D; c += 32) bia[c] = bias ? bias[h * D + c] : 0.f;
-            if (lane == 0) {
-                int64_t *info = (int64_t *)(R + GR_INFO + 64 * s);
-                info[0] = t0;
-                info[1] = len;
-                info[2] = h;
-                info[3] = w;
-                *reinterpret_cast<float *>(info + 4) = A_log ? __expf(A_log[h]) : 1.f;
-            }
-            __threadfence_block();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive_expect_tx(ld_qzk, 6 * 8192);
-                tma_load_3d(R + GR_QZ, &tm.q, 0, h, (int)t0, ld_qzk);
-                tma_load_3d(R + GR_QZ + 8192, &tm.z, 0, h, (int)t0, ld_qzk);
-                tma_load_3d(R + GR_QZ + 16384, &tm.q, 64, h, (int)t0, ld_qzk);
-                tma_load_3d(R + GR_QZ + 24576, &tm.z, 64, h, (int)t0, ld_qzk);
-                tma_load_3d(R + GR_K, &tm.k, 0, h, (int)t0, ld_qzk);
-                tma_load_3d(R + GR_K + 8192, &tm.k, 64, h, (int)t0, ld_qzk);
-            }
-        };
-        auto load_v = [&](int j) {
-            if (lane == 0) {
-                const int64_t w = w_of(2 * j + g);
-                const int h = (int)(w % H);
-                int n = 0, len = 0;
-                int64_t t0 = 0;
-                locate(chunk_start, cu, T, N, w / H, n, t0, len);
-                mbar_arrive_expect_tx(ld_v, 2 * 8192);
-                tma_load_3d(R + GR_V, &tm.v, 0, h, (int)t0, ld_v);
-                tma_load_3d(R + GR_V + 8192, &tm.v, 64, h, (int)t0, ld_v);
-            }
-        };
-        if (nj > 0) {
-            load_qzk(0);
-            load_v(0);
+    // ------------------------------------------------ consumer group g (warps 8 g .. 8 g + 7).  Its thread 0
+    // also moves the data: the next item's q, z and k tiles are loaded once the inverse has freed their
+    // buffers, its v tile once the packet copies of the previous item have read the U^T image; the
+    // packet's A image, W, U^T and gamma leave by bulk copies, and an item is published (flags) during the
+    // A / L product of the group's next item, when its copies have long completed.
+    const int g = warp >> 3, gt = tid & (NCG - 1), gw = gt >> 5;
+    unsigned char *R = sm + g * GR_BYTES;
+    uint64_t *bar = (uint64_t *)(R + GR_BAR);
+    uint64_t *ld_qzk = bar, *ld_v = bar + 1, *bar_mma = bar + 2;
+    const uint32_t tbg = tb + 256u * (uint32_t)g;
+    const int nj = (n_items - g + 1) / 2;  // items it = 2 j + g
+    // The two groups take turns at the gate and element pass (MUFU and shared-memory bound), each
+    // starting it once the other has finished its own, so that one group's element pass overlaps the
+    // other's inverse and products.  Group 0 starts.
+    uint64_t *tok = (uint64_t *)(sm + J_TOK);
+    uint32_t mph = 0;
+    auto mwait = [&]() -> bool {  // the group's last MMA commit: thread 0 waits, the others sleep at the barrier
+        bool o = true;
+        if (gt == 0) o = mbar_wait(bar_mma, mph & 1);
+        ++mph;
+        return gsync_and(g, o);
+    };
+    // Item j's slot (warp 0 of the group): its location (from the chunk layout), and by asynchronous copies
+    // that complete on the mbarrier of the item's tiles (each lane arrives once its copies have landed): the
+    // 32-bit words holding its beta values (bf16; the gate pass widens them in place), its bias row and
+    // A_log.  Nothing waits on these loads until the item starts; the slot (j & 1) was last used by item j - 2.
+    // The slot's plain stores are ordered before their readers by the group barriers in between.
+    auto fill_slot = [&](int j) {
+        const int s = j & 1;
+        const int64_t w = w_of(2 * j + g);
+        int n = 0, len = 0, h;
+        int64_t t0 = 0, slot;
+        if (w <= 0xffffffffll) {  // 32-bit division where it suffices
+            slot = (int64_t)((uint32_t)w / (uint32_t)H);
+            h = (int)((uint32_t)w - (uint32_t)slot * (uint32_t)H);
+        } else {
+            slot = w / H;
+            h = (int)(w % H);
         }
-        bool ok = true;
-        for (int j = 0; j < nj && ok; ++j) {
-            const uint32_t par = j & 1;
-            const int64_t w = w_of(2 * j + g);
-            unsigned char *pk = packets + (size_t)w * PK_STRIDE;  // item w = slot * H + h
-            ok = __all_sync(0xffffffffu, mbar_wait(a_ready, par));
-            if (!ok) break;
-            if (lane == 0) {
-                bulk_s2g(pk + PK_A, R + GR_A, 8192);
-                bulk_commit();
-            }
-            ok = __all_sync(0xffffffffu, mbar_wait(inv_done, par));
-            if (!ok) break;
-            if (j + 1 < nj) {
-                const int nxt = 2 * (j + 1) + g;
-                if (team && nxt >= team->window) {  // run at most `window` items ahead of the chain
-                    bool okw = true;
-                    if (lane == 0) okw = flag_wait(team->consumed + w_of(nxt - team->window), epoch);
-                    ok = __shfl_sync(0xffffffffu, okw, 0);
-                    if (!ok) break;
-                }
-                load_qzk(j + 1);
-            }
-            ok = __all_sync(0xffffffffu, mbar_wait(wu_ready, par));
-            if (!ok) break;
-            if (lane == 0) {
-                bulk_s2g(pk + PK_WQ, R + GR_X, 8192);  // W rows of the [W; Q^] image
-                bulk_s2g(pk + PK_WQ + 16384, R + GR_X + 8192, 8192);
-                bulk_s2g(pk + PK_U, R + GR_V, 16384);
-                bulk_s2g(pk + PK_G, R + GR_GAM, 512);
-                bulk_commit();
-                bulk_wait_read0();
-                mbar_arrive(pk_read);  // X, V, A and gamma of this item have been read
-            }
-            __syncwarp();
-            if (j + 1 < nj) load_v(j + 1);
-            if (lane == 0) {  // publish: a chain may be waiting for this packet
-                bulk_wait0();
-                if (flags) {
-                    fence_proxy_async_global();
-                    flag_release(flags + w, epoch);
-                }
-            }
-            __syncwarp();
+        locate(chunk_start, cu, T, N, slot, n, t0, len);
+        uint32_t *bw = (uint32_t *)(R + GR_BETA) + 64 * s;
+        float *bia = (float *)(R + GR_BIAS) + 128 * s;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int t = lane + 32 * i;
+            if (t < len)  // the aligned word holding the value: inside the tensor's pages
+                cp_async4(bw + t, (const void *)((uintptr_t)(beta + (t0 + t) * H + h) & ~(uintptr_t)3));
+            else
+                bw[t] = 0u;
         }
-        if (!ok && lane == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
-    } else {
-        // ------------------------------------------------ consumer group g (warps 8 g .. 8 g + 7)
-        const int g = warp >> 3, gt = tid & (NCG - 1), gw = gt >> 5;
-        unsigned char *R = sm + g * GR_BYTES;
-        uint64_t *bar = (uint64_t *)(R + GR_BAR);
-        uint64_t *ld_qzk = bar, *ld_v = bar + 1, *a_ready = bar + 2, *inv_done = bar + 3, *wu_ready = bar + 4,
-                 *pk_read = bar + 5, *bar_mma = bar + 6;
-        const uint32_t tbg = tb + 256u * (uint32_t)g;
-        const int nj = (n_items - g + 1) / 2;
-        // element mapping: channel pair (c0, c0 + 1) of one 64-channel half, 16-token quarter qt
-        const int hw = gw & 1, qt = gw >> 1;
-        const int c0 = 64 * hw + 2 * lane;
-        const uint32_t cpos = (uint32_t)((lane & 3) << 2);  // byte of the pair inside its 16-byte chunk
-        auto roff = [&](int r) -> uint32_t {                  // the pair in row r of a 64-channel block
-            return (uint32_t)(r * 128) + ((((uint32_t)(lane >> 2)) ^ (uint32_t)(r & 7)) << 4) + cpos;
-        };
-        // The two groups take turns at the gate and element pass (MUFU and shared-memory bound), each
-        // starting it once the other has finished its own, so that one group's element pass overlaps
-        // the other's inverse and products instead of competing with its element pass.  Group 0 starts.
-        uint64_t *tok = (uint64_t *)(sm + J_TOK);
-        uint32_t mph = 0;
-        bool ok = true;
-        for (int j = 0; j < nj; ++j) {
-            const uint32_t par = j & 1;
-            const int s = j & 1;
-            if (g == 1) ok = gwait(g, &tok[1], j & 1);               // group 0 has done its item j
-            else if (j > 0) ok = gwait(g, &tok[0], (j - 1) & 1);     // group 1 has done its item j - 1
+        if (bias) cp_async16(bia + 4 * lane, bias + (size_t)h * D + 4 * lane);
+        else reinterpret_cast<float4 *>(bia)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane == 0) {
+            int64_t *info = (int64_t *)(R + GR_INFO + 64 * s);
+            info[0] = t0;
+            info[1] = len;
+            info[2] = h;
+            info[3] = w;
+            float *al = reinterpret_cast<float *>(info + 4);  // A_log (0 without: e^0 = 1)
+            if (A_log) cp_async4(al, A_log + h);
+            else *al = 0.f;
+        }
+        cp_async_arrive_noinc(ld_qzk);
+    };
+    // Item j's q, z, k (and v) tiles by TMA (thread 0, which filled the slot)
+    auto issue_tma = [&](int j, bool with_v) {
+        const int64_t *info = (const int64_t *)(R + GR_INFO + 64 * (j & 1));
+        const int t0 = (int)info[0], h = (int)info[2];
+        mbar_arrive_expect_tx(ld_qzk, 6 * 8192);
+        tma_load_3d(R + GR_QZ, &tm.q, 0, h, t0, ld_qzk);
+        tma_load_3d(R + GR_QZ + 8192, &tm.z, 0, h, t0, ld_qzk);
+        tma_load_3d(R + GR_QZ + 16384, &tm.q, 64, h, t0, ld_qzk);
+        tma_load_3d(R + GR_QZ + 24576, &tm.z, 64, h, t0, ld_qzk);
+        tma_load_3d(R + GR_K, &tm.k, 0, h, t0, ld_qzk);
+        tma_load_3d(R + GR_K + 8192, &tm.k, 64, h, t0, ld_qzk);
+        if (with_v) {
+            mbar_arrive_expect_tx(ld_v, 2 * 8192);
+            tma_load_3d(R + GR_V, &tm.v, 0, h, t0, ld_v);
+            tma_load_3d(R + GR_V + 8192, &tm.v, 64, h, t0, ld_v);
+        }
+    };
+    auto publish = [&](int64_t w) {  // thread 0: the item's packet copies have completed
+        bulk_wait0();
+        if (flags) {
+            fence_proxy_async_global();
+            flag_release(flags + w, epoch);
+        }
+    };
+    bool ok = true;
+    if (gw == 0 && nj > 0) {
+        fill_slot(0);
+        if (lane == 0) issue_tma(0, true);
+    }
+    ok = gsync_and(g, ok);
+    int64_t w_prev = -1;  // the group's previous item, published during the next one
+    // element mapping: 8 channels (one 16-byte chunk cg of 64-channel block hb) x 4 tokens 16 tq + 4 tl + i
+    const int hb = gw & 1, tq = gw >> 1, cg = lane & 7, tl = lane >> 3;
+    const int c0 = 64 * hb + 8 * cg;
+    for (int j = 0; j < nj && ok; ++j) {
+        const uint32_t par = j & 1;
+        const int s = j & 1;
+        if (gt == 0 && j > 0) {
+            // the previous item's copies have read X, A, gamma and the U^T image, so this item's v tile can
+            // take the V buffer (their writes complete later: the packet is published after this item's
+            // A / L product is issued)
+            bulk_wait_read0();
+            const int64_t *ip = (const int64_t *)(R + GR_INFO + 64 * s);
+            mbar_arrive_expect_tx(ld_v, 2 * 8192);
+            tma_load_3d(R + GR_V, &tm.v, 0, (int)ip[2], (int)ip[0], ld_v);
+            tma_load_3d(R + GR_V + 8192, &tm.v, 64, (int)ip[2], (int)ip[0], ld_v);
+        }
+        {
+            bool okt = true;
+            if (gt == 0) {
+                const int it = 2 * j + g;
+                if (team && it >= team->window)  // start at most `window` items ahead of the chain
+                    okt = flag_wait(team->consumed + w_of(it - team->window), epoch);
+                if (!okt) {
+                } else if (g == 1) okt = mbar_wait(&tok[1], j & 1);       // group 0 has done its item j
+                else if (j > 0) okt = mbar_wait(&tok[0], (j - 1) & 1);      // group 1 has done its item j - 1
+            }
+            ok = gsync_and(g, okt);
             if (!ok) break;
-            ok = gwait(g, ld_qzk, par);
-            if (!ok) break;
-            const int64_t *info = (const int64_t *)(R + GR_INFO + 64 * s);
-            const int len = (int)info[1];
-            const int64_t w = info[3];
-            const float eA = *reinterpret_cast<const float *>(info + 4);
-            const float *bet = (const float *)(R + GR_BETA) + 64 * s;
-            const float *bia = (const float *)(R + GR_BIAS) + 128 * s;
-            unsigned char *pk = packets + (size_t)w * PK_STRIDE;
+        }
+        ok = gwait(g, ld_qzk, par);
+        if (!ok) break;
+        const int64_t *info = (const int64_t *)(R + GR_INFO + 64 * s);
+        const int len = (int)info[1];
+        const int64_t w = info[3];
+        const float eA = __expf(*reinterpret_cast<const float *>(info + 4));
+        const float *bet = (const float *)(R + GR_BETA) + 64 * s;
+        const float *bia = (const float *)(R + GR_BIAS) + 128 * s;
+        unsigned char *pk = packets + (size_t)w * PK_STRIDE;
 
-            // ---- GATE: g = g_min Sigmoid(e^A (z + b)) (Eq. 5), cumulative sums over the quarter
-            float G0[16], G1[16];  // channels c0, c0 + 1; tokens 16 qt + i
+        // ---- GATE: g = g_min Sigmoid(e^A (z + b)) (Eq. 5) in base-2 units (times log2 e), prefix sums over
+        //      the thread's 4 tokens, then over the 4 threads of its 16-token quarter (shuffles), then (shared
+        //      memory) over the quarters
+        float G[4][8];
+        {
+            const float cz = -eA * LOG2E, gm = g_min * LOG2E;
+            float cb[8];
             {
-                const float cz = -eA * LOG2E;
-                const float cb0 = cz * bia[c0], cb1 = cz * bia[c0 + 1];
-                const unsigned char *zb = R + GR_QZ + hw * 16384;
+                const float4 b0 = *reinterpret_cast<const float4 *>(bia + c0);
+                const float4 b1 = *reinterpret_cast<const float4 *>(bia + c0 + 4);
+                const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t = 16 * qt + i;
-                    const uint32_t zz = *reinterpret_cast<const uint32_t *>(zb + roff(64 + t));
-                    G0[i] = __fdividef(g_min, 1.0f + ex2_approx(fmaf(bf_lo(zz), cz, cb0)));
-                    G1[i] = __fdividef(g_min, 1.0f + ex2_approx(fmaf(bf_hi(zz), cz, cb1)));
-                }
-                if (len < C) {  // ragged tail: tokens past the end of the sequence get g = 0 (an exact no-op)
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (16 * qt + i >= len) G0[i] = G1[i] = 0.f;
-                }
-#pragma unroll
-                for (int i = 1; i < 16; ++i) {
-                    G0[i] += G0[i - 1];
-                    G1[i] += G1[i - 1];
-                }
-                *reinterpret_cast<float2 *>(R + GR_TOT + 4 * (128 * qt + c0)) = make_float2(G0[15], G1[15]);
+                for (int e = 0; e < 8; ++e) cb[e] = cz * bb[e];
             }
-            // all quarter sums written; z read by every thread (its rows are overwritten below); and
-            // (items after the first) the packet copies of the group's previous item have read X and A
-            if (j > 0 && gt == 0) ok = mbar_wait(pk_read, (j - 1) & 1);
-            ok = gsync_and(g, ok);
-            if (!ok) break;
-            float Gr[2], G47[2], eGr[2], f63[2];  // reference G (p0 or p1), G_47, e^{G_ref}, e^{G_63 - G_47}
-            {
-                const float *tot = (const float *)(R + GR_TOT);
-                float2 q4[4];
+            const unsigned char *zb = R + GR_QZ + hb * 16384;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) q4[u] = *reinterpret_cast<const float2 *>(tot + 128 * u + c0);
-                float base0 = 0.f, base1 = 0.f;
+            for (int i = 0; i < 4; ++i) {
+                const int t = 16 * tq + 4 * tl + i;
+                const uint4 zz = *reinterpret_cast<const uint4 *>(zb + (64 + t) * 128 + ((cg ^ (t & 7)) << 4));
+                const uint32_t zw[4] = {zz.x, zz.y, zz.z, zz.w};
+                const bool live = t < len;  // tokens past the end of the sequence: g = 0 (an exact no-op)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float g0 = __fdividef(gm, 1.0f + ex2_approx(fmaf(bf_lo(zw[e]), cz, cb[2 * e])));
+                    const float g1 = __fdividef(gm, 1.0f + ex2_approx(fmaf(bf_hi(zw[e]), cz, cb[2 * e + 1])));
+                    G[i][2 * e] = live ? g0 : 0.f;
+                    G[i][2 * e + 1] = live ? g1 : 0.f;
+                }
+            }
+#pragma unroll
+            for (int i = 1; i < 4; ++i)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) G[i][e] += G[i - 1][e];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {  // inclusive scan of the thread sums over tl (lanes 8 apart)
+                float x = G[3][e];
+#pragma unroll
+                for (int off = 8; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, off);
+                    if (lane >= off) x += y;
+                }
+                const float base = x - G[3][e];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) G[i][e] += base;
+            }
+            if (tl == 3) {  // the quarter's sums
+                float *tot = (float *)(R + GR_TOT) + 128 * tq + c0;
+                *reinterpret_cast<float4 *>(tot) = make_float4(G[3][0], G[3][1], G[3][2], G[3][3]);
+                *reinterpret_cast<float4 *>(tot + 4) = make_float4(G[3][4], G[3][5], G[3][6], G[3][7]);
+            }
+        }
+        if (gt < 64) {  // beta of token gt: the bf16 half of its word (0 past the end), widened in place
+            uint32_t *bw = (uint32_t *)(R + GR_BETA) + 64 * s;
+            const uint32_t x = bw[gt];
+            const uintptr_t ad = (uintptr_t)(beta + (info[0] + gt) * H + info[2]);
+            reinterpret_cast<float *>(bw)[gt] = __uint_as_float((ad & 2) ? (x & 0xffff0000u) : (x << 16));
+        }
+        ok = gsync_and(g, true);  // quarter sums written; z read by every thread (its rows are rewritten below)
+        float Gr[8], G47[8], eGr[8], f63[8];  // (base 2) reference G (p0 or p1), G_47; e^{G_ref}, e^{G_63 - G_47}
+        {
+            const float *tot = (const float *)(R + GR_TOT);
+            float q4[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(tot + 128 * u + c0);
+                const float4 b4 = *reinterpret_cast<const float4 *>(tot + 128 * u + c0 + 4);
+                q4[u][0] = a4.x; q4[u][1] = a4.y; q4[u][2] = a4.z; q4[u][3] = a4.w;
+                q4[u][4] = b4.x; q4[u][5] = b4.y; q4[u][6] = b4.z; q4[u][7] = b4.w;
+            }
+            float g63[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float base = 0.f;
 #pragma unroll
                 for (int u = 0; u < 3; ++u)
-                    if (u < qt) {
-                        base0 += q4[u].x;
-                        base1 += q4[u].y;
-                    }
+                    if (u < tq) base += q4[u][e];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    G0[i] += base0;
-                    G1[i] += base1;
-                }
-                const float g15[2] = {q4[0].x, q4[0].y};
-                G47[0] = q4[0].x + q4[1].x + q4[2].x;
-                G47[1] = q4[0].y + q4[1].y + q4[2].y;
-                const float g63[2] = {G47[0] + q4[3].x, G47[1] + q4[3].y};
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    Gr[e] = qt < 2 ? g15[e] : G47[e];
-                    eGr[e] = ex2_approx(Gr[e] * LOG2E);
-                    f63[e] = ex2_approx((g63[e] - G47[e]) * LOG2E);
-                }
-                if (qt == 3)
-                    *reinterpret_cast<float2 *>(R + GR_GAM + 4 * c0) =
-                        make_float2(ex2_approx(g63[0] * LOG2E), ex2_approx(g63[1] * LOG2E));
+                for (int i = 0; i < 4; ++i) G[i][e] += base;
+                G47[e] = q4[0][e] + q4[1][e] + q4[2][e];
+                g63[e] = G47[e] + q4[3][e];
+                Gr[e] = tq < 2 ? q4[0][e] : G47[e];
+                eGr[e] = ex2_approx(Gr[e]);
+                f63[e] = ex2_approx(g63[e] - G47[e]);
             }
-            // ---- ELEM: per token t of the quarter and channel e: E = e^{G_t - G_ref}, f1 = e^{G_47 - G_t}
-            //      (keys against the second reference), k0 = e^{G_15 - G_t} (first half only).
-            {
-                unsigned char *qz = R + GR_QZ + hw * 16384;
-                unsigned char *kb = R + GR_K + hw * 8192;
-                unsigned char *k0b = R + GR_K0 + hw * 4096;
-                unsigned char *xb = R + GR_X + hw * 8192;
-                unsigned char *qhat = pk + PK_WQ + hw * 16384;
-                unsigned char *ktil = pk + PK_K + hw * 8192;
+            if (tq == 3 && tl == 3) {
+                float *gam = (float *)(R + GR_GAM) + c0;
+                *reinterpret_cast<float4 *>(gam) =
+                    make_float4(ex2_approx(g63[0]), ex2_approx(g63[1]), ex2_approx(g63[2]), ex2_approx(g63[3]));
+                *reinterpret_cast<float4 *>(gam + 4) =
+                    make_float4(ex2_approx(g63[4]), ex2_approx(g63[5]), ex2_approx(g63[6]), ex2_approx(g63[7]));
+            }
+        }
+        // ---- ELEM: per token t and channel: E = e^{G_t - G_ref}, f1 = e^{G_47 - G_t} (keys against the
+        //      second reference), k0 = e^{G_15 - G_t} (first half only); 16-byte rows of 8 channels
+        {
+            unsigned char *qz = R + GR_QZ + hb * 16384;
+            unsigned char *kb = R + GR_K + hb * 8192;
+            unsigned char *k0b = R + GR_K0 + hb * 4096;
+            unsigned char *xb = R + GR_X + hb * 8192;
+            unsigned char *qhat = pk + PK_WQ + hb * 16384;
+            unsigned char *ktil = pk + PK_K + hb * 8192;
+            // two passes over the thread's tokens (fewer values live at once): the outputs scaled by E, then
+            // those scaled by f1 (k is read again)
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t = 16 * qt + i;
-                    const uint32_t o = roff(t);
-                    const uint32_t qq = *reinterpret_cast<const uint32_t *>(qz + o);
-                    const uint32_t kk = *reinterpret_cast<const uint32_t *>(kb + o);
-                    const float qf[2] = {bf_lo(qq), bf_hi(qq)}, kf[2] = {bf_lo(kk), bf_hi(kk)};
-                    const float gt_[2] = {G0[i], G1[i]};
-                    float rq[2], rk[2], k1[2], k0[2], qh[2], xk[2], kt[2];
+            for (int i = 0; i < 4; ++i) {
+                const int t = 16 * tq + 4 * tl + i;
+                const uint32_t o = (uint32_t)(t * 128 + ((cg ^ (t & 7)) << 4));
+                const uint4 qq = *reinterpret_cast<const uint4 *>(qz + o);
+                const uint4 kk = *reinterpret_cast<const uint4 *>(kb + o);
+                const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w}, kw[4] = {kk.x, kk.y, kk.z, kk.w};
+                uint32_t rq[4], rk[4], qh[4], xk[4];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float dd = (gt_[e] - Gr[e]) * LOG2E;
-                        const float E = ex2_approx(dd);                          // e^{G_t - G_ref}
-                        const float f1 = ex2_approx((G47[e] - gt_[e]) * LOG2E);  // e^{G_47 - G_t}
-                        rq[e] = qf[e] * E;
-                        rk[e] = kf[e] * E;
-                        k1[e] = kf[e] * f1;
-                        k0[e] = qt < 2 ? kf[e] * ex2_approx(-dd) : 0.f;      // e^{G_15 - G_t}
-                        const float eg = E * eGr[e];                              // e^{G_t}
-                        qh[e] = qf[e] * eg;
-                        xk[e] = kf[e] * eg;
-                        kt[e] = kf[e] * (f1 * f63[e]);                            // e^{G_63 - G_t}
-                    }
-                    *reinterpret_cast<uint32_t *>(qz + o) = pack_bf16(rq[0], rq[1]);
-                    *reinterpret_cast<uint32_t *>(qz + roff(64 + t)) = pack_bf16(rk[0], rk[1]);
-                    *reinterpret_cast<uint32_t *>(kb + o) = pack_bf16(k1[0], k1[1]);
-                    if (qt < 2) *reinterpret_cast<uint32_t *>(k0b + o) = pack_bf16(k0[0], k0[1]);
-                    *reinterpret_cast<uint32_t *>(xb + o) = pack_bf16(xk[0], xk[1]);
-                    *reinterpret_cast<uint32_t *>(qhat + roff(64 + t)) = pack_bf16(qh[0], qh[1]);
-                    *reinterpret_cast<uint32_t *>(ktil + o) = pack_bf16(kt[0], kt[1]);
+                for (int e = 0; e < 4; ++e) {
+                    const float2 qf = make_float2(bf_lo(qw[e]), bf_hi(qw[e]));
+                    const float2 kf = make_float2(bf_lo(kw[e]), bf_hi(kw[e]));
+                    const float2 dd = fsub2(make_float2(G[i][2 * e], G[i][2 * e + 1]), make_float2(Gr[2 * e], Gr[2 * e + 1]));
+                    const float2 E = make_float2(ex2_approx(dd.x), ex2_approx(dd.y));  // e^{G_t - G_ref}
+                    const float2 eg = fmul2(E, make_float2(eGr[2 * e], eGr[2 * e + 1]));  // e^{G_t}
+                    rq[e] = pack2(fmul2(qf, E));
+                    rk[e] = pack2(fmul2(kf, E));
+                    qh[e] = pack2(fmul2(qf, eg));
+                    xk[e] = pack2(fmul2(kf, eg));
                 }
+                *reinterpret_cast<uint4 *>(qz + o) = make_uint4(rq[0], rq[1], rq[2], rq[3]);
+                *reinterpret_cast<uint4 *>(qz + 64 * 128 + o) = make_uint4(rk[0], rk[1], rk[2], rk[3]);
+                *reinterpret_cast<uint4 *>(xb + o) = make_uint4(xk[0], xk[1], xk[2], xk[3]);
+                *reinterpret_cast<uint4 *>(qhat + 64 * 128 + o) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
             }
-            fence_proxy_async();
-            gsync(g);
-            if (gt == 0) {
-                // rows over keys 0-31 scaled to p0 (N = 32), then over keys 0-63 scaled to p1 (N = 64)
-                mma_bf16_k(tbg + TM_DA, smem_u32(R + GR_QZ), 128, smem_u32(R + GR_K0), 32, 8, idesc_bf16(128, 32),
-                           false);
-                mma_bf16_k(tbg + TM_DA + 32, smem_u32(R + GR_QZ), 128, smem_u32(R + GR_K), 64, 8,
-                           idesc_bf16(128, 64), false);
-                mma_commit(bar_mma);
-                // the other group's turn, while it has an item left that waits for this one: group 1's item j
-                // waits for group 0's item j, group 0's item j + 1 for group 1's item j
-                if (g == 0 ? j < n_items / 2 : j + 1 < (n_items + 1) / 2) mbar_arrive(&tok[1 - g]);
-            }
-            ok = gwait(g, bar_mma, mph & 1);
-            ++mph;
-            if (!ok) break;
-            fence_after_sync();
-            // ---- A rows -> A image (causal, diagonal kept); L rows -> fp32 (strictly lower, times beta).
-            //      Rows of the first half take keys 0-31 from columns 0-31, rows of the second half keys
-            //      0-63 from columns 32-95; the two warps of a TMEM lane quarter split the columns.
-            float *Lm = (float *)(R + GR_L);
-            float *Tm = (float *)(R + GR_T);
-            {
-                const int lq = gw & 3, cp = gw >> 2;
-                const int r = (32 * lq + lane) & 63;  // token row
-                if ((lq & 1) == 0) {                  // rows of the first half: columns [16 cp, 16 cp + 16)
-                    float d[16];
-                    tmem_ld16(tmem_addr(tbg + TM_DA, 32 * lq, 16 * cp), d);
-                    if (lq == 0) {
 #pragma unroll
-                        for (int jj = 0; jj < 2; ++jj) {
-                            const int cj = 2 * cp + jj;
-                            float o[8];
+            for (int i = 0; i < 4; ++i) {
+                const int t = 16 * tq + 4 * tl + i;
+                const uint32_t o = (uint32_t)(t * 128 + ((cg ^ (t & 7)) << 4));
+                const uint4 kk = *reinterpret_cast<const uint4 *>(kb + o);
+                const uint32_t kw[4] = {kk.x, kk.y, kk.z, kk.w};
+                uint32_t k1[4], k0[4], kt[4];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) o[e] = (8 * cj + e <= r) ? d[8 * jj + e] : 0.f;
-                            *reinterpret_cast<uint4 *>(R + GR_A + img_chunk_off(64, r, cj)) = pack8(o);
-                            *reinterpret_cast<uint4 *>(R + GR_A + img_chunk_off(64, r, 4 + cj)) = make_uint4(0, 0, 0, 0);
-                        }
-                    } else {
-                        const float br = bet[r];
-#pragma unroll
-                        for (int e = 0; e < 16; e += 4) {
-                            const int i = 16 * cp + e;
-                            *reinterpret_cast<float4 *>(&Lm[fimg(r, i)]) =
-                                make_float4((i < r) ? br * d[e] : 0.f, (i + 1 < r) ? br * d[e + 1] : 0.f,
-                                            (i + 2 < r) ? br * d[e + 2] : 0.f, (i + 3 < r) ? br * d[e + 3] : 0.f);
-                        }
-                    }
-                } else {  // rows of the second half: columns 32 + [32 cp, 32 cp + 32) = keys [32 cp, 32 cp + 32)
-                    float d[32];
-                    tmem_ld32(tmem_addr(tbg + TM_DA + 32, 32 * lq, 32 * cp), d);
-                    if (lq == 1) {
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) {
-                            const int cj = 4 * cp + jj;
-                            float o[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) o[e] = (8 * cj + e <= r) ? d[8 * jj + e] : 0.f;
-                            *reinterpret_cast<uint4 *>(R + GR_A + img_chunk_off(64, r, cj)) = pack8(o);
-                        }
-                    } else {
-                        const float br = bet[r];
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4) {
-                            const int i = 32 * cp + e;
-                            *reinterpret_cast<float4 *>(&Lm[fimg(r, i)]) =
-                                make_float4((i < r) ? br * d[e] : 0.f, (i + 1 < r) ? br * d[e + 1] : 0.f,
-                                            (i + 2 < r) ? br * d[e + 2] : 0.f, (i + 3 < r) ? br * d[e + 3] : 0.f);
-                        }
+                for (int e = 0; e < 4; ++e) {
+                    const float2 kf = make_float2(bf_lo(kw[e]), bf_hi(kw[e]));
+                    const float2 gt2 = make_float2(G[i][2 * e], G[i][2 * e + 1]);
+                    const float2 fa = fsub2(make_float2(G47[2 * e], G47[2 * e + 1]), gt2);
+                    const float2 f1 = make_float2(ex2_approx(fa.x), ex2_approx(fa.y));  // e^{G_47 - G_t}
+                    const float2 kf1 = fmul2(kf, f1);
+                    k1[e] = pack2(kf1);
+                    kt[e] = pack2(fmul2(kf1, make_float2(f63[2 * e], f63[2 * e + 1])));  // e^{G_63 - G_t}
+                    if (tq < 2) {  // e^{G_15 - G_t}
+                        const float2 dn = fsub2(make_float2(Gr[2 * e], Gr[2 * e + 1]), gt2);
+                        k0[e] = pack2(fmul2(kf, make_float2(ex2_approx(dn.x), ex2_approx(dn.y))));
                     }
                 }
+                *reinterpret_cast<uint4 *>(kb + o) = make_uint4(k1[0], k1[1], k1[2], k1[3]);
+                if (tq < 2) *reinterpret_cast<uint4 *>(k0b + o) = make_uint4(k0[0], k0[1], k0[2], k0[3]);
+                *reinterpret_cast<uint4 *>(ktil + o) = make_uint4(kt[0], kt[1], kt[2], kt[3]);
             }
-            fence_proxy_async();
-            gsync(g);
-            if (gt == 0) mbar_arrive(a_ready);  // the producer copies the A image out
-            // ---- T = (I + L)^{-1}.  Level 0: the four 16 x 16 diagonal blocks, one column per thread,
-            //      by forward substitution; the blocks above the diagonal inside each 32-row half are
-            //      zeroed so that the merges below can run full-length dot products.
-            if (gt < 64) {
-                const int b = gt >> 4, jc = gt & 15, o0 = 16 * b;
-                float x[16];
+        }
+        fence_proxy_async();
+        gsync(g);
+        if (gt == 0) {
+            // rows over keys 0-31 scaled to p0 (N = 32), then over keys 0-63 scaled to p1 (N = 64)
+            mma_bf16_k(tbg + TM_DA, smem_u32(R + GR_QZ), 128, smem_u32(R + GR_K0), 32, 8, idesc_bf16(128, 32), false);
+            mma_bf16_k(tbg + TM_DA + 32, smem_u32(R + GR_QZ), 128, smem_u32(R + GR_K), 64, 8, idesc_bf16(128, 64),
+                       false);
+            mma_commit(bar_mma);
+            // the other group's turn, while it has an item left that waits for this one: group 1's item j
+            // waits for group 0's item j, group 0's item j + 1 for group 1's item j
+            if (g == 0 ? j < n_items / 2 : j + 1 < (n_items + 1) / 2) mbar_arrive(&tok[1 - g]);
+            if (flags && j > 0) publish(w_prev);  // while the product runs
+        }
+        ok = mwait();
+        if (!ok) break;
+        fence_after_sync();
+        // ---- A rows -> A image (causal, diagonal kept); L rows -> fp32 (strictly lower, times beta).
+        //      Rows of the first half take keys 0-31 from columns 0-31, rows of the second half keys
+        //      0-63 from columns 32-95; the two warps of a TMEM lane quarter split the columns.
+        float *Lm = (float *)(R + GR_L);
+        float *Tm = (float *)(R + GR_T);
+        {
+            const int lq = gw & 3, cp = gw >> 2;
+            const int r = (32 * lq + lane) & 63;  // token row
+            if ((lq & 1) == 0) {                  // rows of the first half: columns [16 cp, 16 cp + 16)
+                float d[16];
+                tmem_ld16(tmem_addr(tbg + TM_DA, 32 * lq, 16 * cp), d);
+                if (lq == 0) {
 #pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = (r == jc) ? 1.f : 0.f;
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int cj = 2 * cp + jj;
+                        float o[8];
 #pragma unroll
-                for (int i = 0; i < 15; ++i) {
-                    const float xi = x[i];
+                        for (int e = 0; e < 8; ++e) o[e] = (8 * cj + e <= r) ? d[8 * jj + e] : 0.f;
+                        *reinterpret_cast<uint4 *>(R + GR_A + img_chunk_off(64, r, cj)) = pack8(o);
+                        *reinterpret_cast<uint4 *>(R + GR_A + img_chunk_off(64, r, 4 + cj)) = make_uint4(0, 0, 0, 0);
+                    }
+                } else {
+                    const float br = bet[r];
 #pragma unroll
-                    for (int r = i + 1; r < 16; ++r) x[r] -= Lm[fimg(o0 + r, o0 + i)] * xi;
+                    for (int e = 0; e < 16; e += 4) {
+                        const int i = 16 * cp + e;
+                        *reinterpret_cast<float4 *>(&Lm[fimg(r, i)]) =
+                            make_float4((i < r) ? br * d[e] : 0.f, (i + 1 < r) ? br * d[e + 1] : 0.f,
+                                        (i + 2 < r) ? br * d[e + 2] : 0.f, (i + 3 < r) ? br * d[e + 3] : 0.f);
+                    }
                 }
+            } else {  // rows of the second half: columns 32 + [32 cp, 32 cp + 32) = keys [32 cp, 32 cp + 32)
+                float d[32];
+                tmem_ld32(tmem_addr(tbg + TM_DA + 32, 32 * lq, 32 * cp), d);
+                if (lq == 1) {
 #pragma unroll
-                for (int r = 0; r < 16; ++r) Tm[fimg(o0 + r, o0 + jc)] = x[r];
-                if ((b & 1) == 0) {
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int cj = 4 * cp + jj;
+                        float o[8];
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) Tm[fimg(o0 + r, o0 + 16 + jc)] = 0.f;
-                }
-                if (b < 2) {  // T_11 = T[0:32][0:32] also transposed (the B operand of the level-2 merge)
-                    float *Tt = (float *)(R + GR_TT);
+                        for (int e = 0; e < 8; ++e) o[e] = (8 * cj + e <= r) ? d[8 * jj + e] : 0.f;
+                        *reinterpret_cast<uint4 *>(R + GR_A + img_chunk_off(64, r, cj)) = pack8(o);
+                    }
+                } else {
+                    const float br = bet[r];
 #pragma unroll
-                    for (int r = 0; r < 16; r += 4) {
-                        *reinterpret_cast<float4 *>(Tt + fimg(o0 + jc, o0 + r)) = make_float4(x[r], x[r + 1], x[r + 2], x[r + 3]);
-                        if (b == 0) *reinterpret_cast<float4 *>(Tt + fimg(16 + jc, r)) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int e = 0; e < 32; e += 4) {
+                        const int i = 32 * cp + e;
+                        *reinterpret_cast<float4 *>(&Lm[fimg(r, i)]) =
+                            make_float4((i < r) ? br * d[e] : 0.f, (i + 1 < r) ? br * d[e + 1] : 0.f,
+                                        (i + 2 < r) ? br * d[e + 2] : 0.f, (i + 3 < r) ? br * d[e + 3] : 0.f);
                     }
                 }
             }
-            gsync(g);
-            // Level 1: T_10 = -T_11 L_10 T_00 inside each 32-row half.  Thread = (half mg, column jc,
-            // rows q + 4 a); the four threads of a column share their partial products by shuffles.
-            if (gt < 128) {
-                const int mg = gt >> 6, q = lane & 3;
-                const int jc = ((gt >> 5) & 1) * 8 + (lane >> 2);
-                const int ro = 32 * mg + 16, co = 32 * mg;
-                float p[4];
-                if (gw & 1) inv_l1_partial<8>(Lm, Tm, ro, co, q, jc, p);
-                else inv_l1_partial<0>(Lm, Tm, ro, co, q, jc, p);
-                float pc[16];  // P[:, jc], row q2 + 4 a from lane q2
+        }
+        fence_proxy_async();
+        gsync(g);
+        if (gt == 0) {  // the A image leaves for the packet
+            bulk_s2g(pk + PK_A, R + GR_A, 8192);
+            bulk_commit();
+        }
+        // ---- T = (I + L)^{-1}.  Level 0: the four 16 x 16 diagonal blocks, one column per thread,
+        //      by forward substitution; the blocks above the diagonal inside each 32-row half are
+        //      zeroed so that the merges below can run full-length dot products.
+        if (gt < 64) {
+            const int b = gt >> 4, jc = gt & 15, o0 = 16 * b;
+            float x[16];
 #pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2)
+            for (int r = 0; r < 16; ++r) x[r] = (r == jc) ? 1.f : 0.f;
 #pragma unroll
-                    for (int a = 0; a < 4; ++a) pc[q2 + 4 * a] = __shfl_sync(0xffffffffu, p[a], (lane & ~3) | q2);
+            for (int i = 0; i < 15; ++i) {
+                const float xi = x[i];
 #pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    float acc = 0.f;
+                for (int r = i + 1; r < 16; ++r) x[r] -= Lm[fimg(o0 + r, o0 + i)] * xi;
+            }
 #pragma unroll
-                    for (int k = 0; k < 4 * (a + 1); k += 4) {
-                        const float4 t4 = *reinterpret_cast<const float4 *>(Tm + fimg(ro + q + 4 * a, ro + k));
-                        acc += t4.x * pc[k] + t4.y * pc[k + 1] + t4.z * pc[k + 2] + t4.w * pc[k + 3];
-                    }
-                    Tm[fimg(ro + q + 4 * a, co + jc)] = -acc;
-                    if (mg == 0) reinterpret_cast<float *>(R + GR_TT)[fimg(co + jc, ro + q + 4 * a)] = -acc;
+            for (int r = 0; r < 16; ++r) Tm[fimg(o0 + r, o0 + jc)] = x[r];
+            if ((b & 1) == 0) {
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tm[fimg(o0 + r, o0 + 16 + jc)] = 0.f;
+            }
+            if (b < 2) {  // T_11 = T[0:32][0:32] also transposed (the B operand of the level-2 merge)
+                float *Tt = (float *)(R + GR_TT);
+#pragma unroll
+                for (int r = 0; r < 16; r += 4) {
+                    *reinterpret_cast<float4 *>(Tt + fimg(o0 + jc, o0 + r)) = make_float4(x[r], x[r + 1], x[r + 2], x[r + 3]);
+                    if (b == 0) *reinterpret_cast<float4 *>(Tt + fimg(16 + jc, r)) = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
-            // Level 2: T_[23][01] = -T_[23][23] (L_[23][01] T_[01][01]) on 32 x 32 blocks, as two tf32
-            // products on the tensor cores (M = 128, the 32 rows of interest in TMEM lanes 32-63; the other
-            // lanes hold products of rows that are not needed), both operands K-major.  P = L_[23][01] T_[01][01]:
-            // A = L's first column block read as 128 rows (L rows 32-63 are rows 32-63), B = T_[01][01]^T.
-            // Then T_[23][23] P: A = T's second column block read as 128 rows, B = P^T.
-            // Meanwhile the T image is written where it does not depend on this merge.
-            fence_proxy_async();
-            gsync(g);
-            if (gt == 0) {
-                mma_tf32_k32(tbg + 0, smem_u32(R + GR_L), smem_u32(R + GR_TT), idesc_tf32(128, 32), false);
-                mma_commit(bar_mma);
+        }
+        gsync(g);
+        // Level 1: T_10 = -T_11 L_10 T_00 inside each 32-row half.  Thread = (half mg, column jc,
+        // rows q + 4 a); the four threads of a column share their partial products by shuffles.
+        if (gt < 128) {
+            const int mg = gt >> 6, q = lane & 3;
+            const int jc = ((gt >> 5) & 1) * 8 + (lane >> 2);
+            const int ro = 32 * mg + 16, co = 32 * mg;
+            float p[4];
+            if (gw & 1) inv_l1_partial<8>(Lm, Tm, ro, co, q, jc, p);
+            else inv_l1_partial<0>(Lm, Tm, ro, co, q, jc, p);
+            float pc[16];  // P[:, jc], row q2 + 4 a from lane q2
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                for (int a = 0; a < 4; ++a) pc[q2 + 4 * a] = __shfl_sync(0xffffffffu, p[a], (lane & ~3) | q2);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                float acc = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4 * (a + 1); k += 4) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(Tm + fimg(ro + q + 4 * a, ro + k));
+                    acc += t4.x * pc[k] + t4.y * pc[k + 1] + t4.z * pc[k + 2] + t4.w * pc[k + 3];
+                }
+                Tm[fimg(ro + q + 4 * a, co + jc)] = -acc;
+                if (mg == 0) reinterpret_cast<float *>(R + GR_TT)[fimg(co + jc, ro + q + 4 * a)] = -acc;
             }
-            // (T diag beta) image into the dead key-0 image, rows 0-31 and the columns 32-63 of rows 32-63:
-            // item e -> (row r, 8-key chunk jj); entries above the diagonal are zero
-            for (int e = gt; e < 384; e += NCG) {
-                const int r = e < 256 ? (e >> 3) : 32 + ((e - 256) >> 2);
-                const int jj = e < 256 ? (e & 7) : 4 + ((e - 256) & 3);
-                const float4 t0v = *reinterpret_cast<const float4 *>(Tm + fimg(r, 8 * jj));
-                const float4 t1v = *reinterpret_cast<const float4 *>(Tm + fimg(r, 8 * jj + 4));
-                const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+        }
+        // Level 2: T_[23][01] = -T_[23][23] (L_[23][01] T_[01][01]) on 32 x 32 blocks, as two tf32
+        // products on the tensor cores (M = 128, the 32 rows of interest in TMEM lanes 32-63; the other
+        // lanes hold products of rows that are not needed), both operands K-major.  P = L_[23][01] T_[01][01]:
+        // A = L's first column block read as 128 rows (L rows 32-63 are rows 32-63), B = T_[01][01]^T.
+        // Then T_[23][23] P: A = T's second column block read as 128 rows, B = P^T.
+        // Meanwhile the T image is written where it does not depend on this merge.
+        fence_proxy_async();
+        gsync(g);
+        if (gt == 0) {
+            mma_tf32_k32(tbg + 0, smem_u32(R + GR_L), smem_u32(R + GR_TT), idesc_tf32(128, 32), false);
+            mma_commit(bar_mma);
+        }
+        // (T diag beta) image into the dead key-0 image, rows 0-31 and the columns 32-63 of rows 32-63:
+        // item e -> (row r, 8-key chunk jj); entries above the diagonal are zero
+        for (int e = gt; e < 384; e += NCG) {
+            const int r = e < 256 ? (e >> 3) : 32 + ((e - 256) >> 2);
+            const int jj = e < 256 ? (e & 7) : 4 + ((e - 256) & 3);
+            const float4 t0v = *reinterpret_cast<const float4 *>(Tm + fimg(r, 8 * jj));
+            const float4 t1v = *reinterpret_cast<const float4 *>(Tm + fimg(r, 8 * jj + 4));
+            const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+            float o[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) o[q] = (8 * jj + q <= r) ? tv[q] * bet[8 * jj + q] : 0.f;
+            *reinterpret_cast<uint4 *>(R + GR_K0 + img_chunk_off(64, r, jj)) = pack8(o);
+        }
+        ok = mwait();
+        if (!ok) break;
+        fence_after_sync();
+        const bool mid = (gw & 3) == 1;  // the warps of TMEM lanes 32-63 (rows 32-63), 16 columns each
+        const int c16 = 16 * (gw >> 2);
+        if (mid) {  // P row `lane` (TMEM lane 32 + lane), columns c16 .. c16 + 15 -> column `lane` of P^T
+            float d[16];
+            tmem_ld16(tmem_addr(tbg + c16, 32, 0), d);
+            float *Pt = (float *)(R + GR_P);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) Pt[fimg(c16 + e, lane)] = d[e];
+        }
+        fence_proxy_async();
+        gsync(g);
+        if (gt == 0) {
+            mma_tf32_k32(tbg + 32, smem_u32(R + GR_T + 8192), smem_u32(R + GR_P), idesc_tf32(128, 32), false);
+            mma_commit(bar_mma);
+        }
+        ok = mwait();
+        if (!ok) break;
+        fence_after_sync();
+        if (mid) {  // T_[23][01] = -(T_[23][23] P): row 32 + lane, keys c16 .. c16 + 15, times beta, into the T image
+            float d[16];
+            tmem_ld16(tmem_addr(tbg + 32 + c16, 32, 0), d);
+            const int r = 32 + lane;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
                 float o[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) o[q] = (8 * jj + q <= r) ? tv[q] * bet[8 * jj + q] : 0.f;
-                *reinterpret_cast<uint4 *>(R + GR_K0 + img_chunk_off(64, r, jj)) = pack8(o);
+                for (int q = 0; q < 8; ++q) o[q] = -d[8 * h2 + q] * bet[c16 + 8 * h2 + q];
+                *reinterpret_cast<uint4 *>(R + GR_K0 + img_chunk_off(64, r, (c16 >> 3) + h2)) = pack8(o);
             }
-            ok = gwait(g, bar_mma, mph & 1);
-            ++mph;
-            if (!ok) break;
-            fence_after_sync();
-            const bool mid = (gw & 3) == 1;  // the warps of TMEM lanes 32-63 (rows 32-63), 16 columns each
-            const int c16 = 16 * (gw >> 2);
-            if (mid) {  // P row `lane` (TMEM lane 32 + lane), columns c16 .. c16 + 15 -> column `lane` of P^T
-                float d[16];
-                tmem_ld16(tmem_addr(tbg + c16, 32, 0), d);
-                float *Pt = (float *)(R + GR_P);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) Pt[fimg(c16 + e, lane)] = d[e];
-            }
-            fence_proxy_async();
-            gsync(g);
-            if (gt == 0) {
-                mma_tf32_k32(tbg + 32, smem_u32(R + GR_T + 8192), smem_u32(R + GR_P), idesc_tf32(128, 32), false);
+        } else if (gw == 0 && j + 1 < nj) {
+            fill_slot(j + 1);  // while warps 1 and 5 read the merge out
+        }
+        fence_proxy_async();
+        gsync(g);
+        bool okm = true;
+        if (gt == 0) {
+            okm = mbar_wait(ld_v, par);
+            if (okm) {
+                // W = (T diag beta) X: A = the T image read as 128 rows (rows 64-127 are the A image behind it
+                // and land in unused TMEM lanes), B = X (MN-major).  U^T = V^T (T diag beta)^T: A = V (MN-major,
+                // M = d_v), B = the T image (K-major, 64 rows).
+                mma_bf16_kmn(tbg + TM_DW, smem_u32(R + GR_K0), 128, smem_u32(R + GR_X), 8192, 4,
+                             idesc_bf16(128, 128, false, true), false);
+                mma_bf16_mnk(tbg + TM_DUT, smem_u32(R + GR_V), 8192, smem_u32(R + GR_K0), 64, 4,
+                             idesc_bf16(128, 64, true, false), false);
                 mma_commit(bar_mma);
             }
-            ok = gwait(g, bar_mma, mph & 1);
-            ++mph;
-            if (!ok) break;
-            fence_after_sync();
-            if (mid) {  // T_[23][01] = -(T_[23][23] P): row 32 + lane, keys c16 .. c16 + 15, times beta, into the T image
-                float d[16];
-                tmem_ld16(tmem_addr(tbg + 32 + c16, 32, 0), d);
-                const int r = 32 + lane;
+        }
+        // L and T are dead: while the products run, the next item's q, z and k tiles come in
+        if (gt == 0 && j + 1 < nj && okm) issue_tma(j + 1, false);
+        ok = gsync_and(g, ok && okm);
+        if (!ok) break;
+        ok = mwait();
+        if (!ok) break;
+        fence_after_sync();
+        // ---- W rows (token-major, TMEM lanes 0-63) into the dead X tile, U^T rows (value channels, all
+        //      lanes) into the dead V tile
+        if ((gw & 3) < 2) {
+            const int r = 32 * (gw & 3) + lane, cq = gw >> 2;  // columns [64 cq, 64 cq + 64)
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    float o[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) o[q] = -d[8 * h2 + q] * bet[c16 + 8 * h2 + q];
-                    *reinterpret_cast<uint4 *>(R + GR_K0 + img_chunk_off(64, r, (c16 >> 3) + h2)) = pack8(o);
-                }
-            }
-            fence_proxy_async();
-            gsync(g);
-            if (gt == 0) {
-                mbar_arrive(inv_done);  // L and T are dead: the producer loads the next q, z, k tiles
-                ok = mbar_wait(ld_v, par);
-                if (ok) {
-                    // W = (T diag beta) X: A = the T image read as 128 rows (rows 64-127 are the A image behind
-                    // it and land in unused TMEM lanes), B = X (MN-major).  U^T = V^T (T diag beta)^T: A = V
-                    // (MN-major, M = d_v), B = the T image (K-major, 64 rows).
-                    mma_bf16_kmn(tbg + TM_DW, smem_u32(R + GR_K0), 128, smem_u32(R + GR_X), 8192, 4,
-                                 idesc_bf16(128, 128, false, true), false);
-                    mma_bf16_mnk(tbg + TM_DUT, smem_u32(R + GR_V), 8192, smem_u32(R + GR_K0), 64, 4,
-                                 idesc_bf16(128, 64, true, false), false);
-                    mma_commit(bar_mma);
-                }
-            }
-            ok = gsync_and(g, ok);
-            if (!ok) break;
-            ok = gwait(g, bar_mma, mph & 1);
-            ++mph;
-            if (!ok) break;
-            fence_after_sync();
-            // ---- W rows (token-major, TMEM lanes 0-63) into the dead X tile, U^T rows (value channels,
-            //      all lanes) into the dead V tile
-            if ((gw & 3) < 2) {
-                const int r = 32 * (gw & 3) + lane, cq = gw >> 2;  // columns [64 cq, 64 cq + 64)
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    float d[32];
-                    tmem_ld32(tmem_addr(tbg + TM_DW, 32 * (gw & 3), 64 * cq + 32 * h2), d);
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        *reinterpret_cast<uint4 *>(R + GR_X + img_chunk_off(64, r, 8 * cq + 4 * h2 + jj)) =
-                            pack8(d + 8 * jj);
-                }
-            }
-            {
-                const int vr = 32 * (gw & 3) + lane, tq = gw >> 2;  // tokens [32 tq, 32 tq + 32)
+            for (int h2 = 0; h2 < 2; ++h2) {
                 float d[32];
-                tmem_ld32(tmem_addr(tbg + TM_DUT, 32 * (gw & 3), 32 * tq), d);
+                tmem_ld32(tmem_addr(tbg + TM_DW, 32 * (gw & 3), 64 * cq + 32 * h2), d);
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
-                    *reinterpret_cast<uint4 *>(R + GR_V + img_chunk_off(128, vr, 4 * tq + jj)) = pack8(d + 8 * jj);
+                    *reinterpret_cast<uint4 *>(R + GR_X + img_chunk_off(64, r, 8 * cq + 4 * h2 + jj)) = pack8(d + 8 * jj);
             }
-            // Q^ and K~ went to the packet by plain stores: the group barrier orders them before thread 0's
-            // arrival (release), and the producer's flag store (release, GPU scope) publishes them with the
-            // rest of the packet
-            fence_proxy_async();
-            gsync(g);
-            if (gt == 0) mbar_arrive(wu_ready);  // the producer writes the rest of the packet
         }
-        if (!ok && gt == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
+        {
+            const int vr = 32 * (gw & 3) + lane, tq2 = gw >> 2;  // tokens [32 tq2, 32 tq2 + 32)
+            float d[32];
+            tmem_ld32(tmem_addr(tbg + TM_DUT, 32 * (gw & 3), 32 * tq2), d);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+                *reinterpret_cast<uint4 *>(R + GR_V + img_chunk_off(128, vr, 4 * tq2 + jj)) = pack8(d + 8 * jj);
+        }
+        // Q^ and K~ went to the packet by plain stores: the group barriers order them before thread 0's flag
+        // store (release, GPU scope), which publishes them with the rest of the packet
+        fence_proxy_async();
+        gsync(g);
+        if (gt == 0) {  // the rest of the packet: W rows of the [W; Q^] image, U^T, gamma
+            bulk_s2g(pk + PK_WQ, R + GR_X, 8192);
+            bulk_s2g(pk + PK_WQ + 16384, R + GR_X + 8192, 8192);
+            bulk_s2g(pk + PK_U, R + GR_V, 16384);
+            bulk_s2g(pk + PK_G, R + GR_GAM, 512);
+            bulk_commit();
+        }
+        w_prev = w;
+    }
+    if (gt == 0) {
+        if (ok && w_prev >= 0) publish(w_prev);
+        if (!ok) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
+        bulk_wait0();
     }
     __syncthreads();
     if (tid < 2) {  // the group regions are reused as plain memory after this role
         uint64_t *b = (uint64_t *)(sm + tid * GR_BYTES + GR_BAR);
-        for (int i = 0; i < 7; ++i) mbar_inval(&b[i]);
+        for (int i = 0; i < 3; ++i) mbar_inval(&b[i]);
         mbar_inval((uint64_t *)(sm + J_TOK) + tid);
     }
     if (warp == 0) tmem_dealloc(tb, 512);
@@ -902,8 +990,20 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
                       const int32_t *__restrict__ chunk_start, int H, unsigned char *__restrict__ packets,
                       int *err) {
     extern __shared__ unsigned char smem_raw[];
-    intra_role(align1024(smem_raw), tm, beta, bias, A_log, g_min, T, N, cu, chunk_start, H, packets, err,
-               (int)blockIdx.x, (int)gridDim.x, nullptr, 0, 0, -1, 0);
+    unsigned char *sm = align1024(smem_raw);
+    const int32_t *cs = chunk_start, *cu_l = cu;
+    if (N <= J_TBL_N) {  // the chunk layout in shared memory: items are located without global loads
+        int32_t *a = (int32_t *)(sm + J_CS), *c = (int32_t *)(sm + J_CU);
+        for (int n = threadIdx.x; n <= N; n += blockDim.x) {
+            a[n] = chunk_start[n];
+            if (cu) c[n] = cu[n];
+        }
+        __syncthreads();
+        cs = a;
+        if (cu) cu_l = c;
+    }
+    intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu_l, cs, H, packets, err, (int)blockIdx.x, (int)gridDim.x,
+               nullptr, 0, 0, -1, 0);
 }
 
 constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 9: packet loads; 12-15: output; 10, 11 idle
@@ -915,8 +1015,9 @@ constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 9: packet load
 //   V~     V~^T = U^T - D[:, 0:64] (U^T from the packet) as bf16 pairs into tensor memory
 //   MMA3   S^T += V~^T K~              the decay Diag(gamma) was applied to S^T by the CUDA cores
 //   S      bf16 copy of S_{k+1}^T, then S^T scaled by gamma_{k+1} (per column)
-//   MMA2   D[:, 64:128] += V~^T A^T    O^T = (Q^ S + A V~)^T, issued after MMA3 of chunk k + 1 so that
-//                                      the in-order tensor pipe runs it behind the next state update
+//   MMA2   D[:, 64:128] += V~^T A^T    O^T = (Q^ S + A V~)^T, issued after MMA1 of chunk k + 1 so that
+//                                      the in-order tensor pipe runs it during the next V~ phase (its
+//                                      completion frees the packet stage for the loader, two chunks ahead)
 // The output warps read O^T of chunk k once its MMAs are done, release the D buffer, and store o
 // through a staging tile and TMA.
 // Tensor memory columns: S^T fp32 [0, 128), D buffers [128, 384), bf16 S^T [384, 448), bf16 V~^T
@@ -932,7 +1033,9 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                                            const unsigned char *__restrict__ packets, float scale,
                                            const float *initial_state, float *final_state, bf16 *__restrict__ o,
                                            int *err, int g, int h, const uint64_t *flags, uint64_t epoch,
-                                           uint64_t *consumed = nullptr, bool relinquish = true) {
+                                           uint64_t *consumed = nullptr, bool relinquish = true,
+                                           const CUtensorMap *gmap = nullptr, const float *epi_w = nullptr,
+                                           float epi_eps = 0.f) {
     // segment g of sequence n, head h: chunks [kk0, kk0 + nc) of the sequence (without seg_start, one
     // segment per sequence: g = n)
     if (seg_start ? g >= seg_start[N] : g >= N) return;
@@ -961,6 +1064,7 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                                                     // recurrence warp); double-buffered so that the
                                                     // loader, which also waits on it, can never see a
                                                     // phase two ahead
+    uint64_t *bar_g = bar_ld1 + 13;                 // [2] output epilogue: gate tile of chunk kk loaded
     uint32_t *tslot = (uint32_t *)(sm + CS_TSLOT);
     int *s_fail = (int *)(sm + CS_TSLOT + 8);
     const int64_t kk0 = (int64_t)seg_i * seg_len;
@@ -988,6 +1092,8 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
         mbar_init(bar_sb, 8);
         mbar_init(&bar_vt[0], 8);
         mbar_init(&bar_vt[1], 8);
+        mbar_init(&bar_g[0], 1);
+        mbar_init(&bar_g[1], 1);
         *s_fail = 0;
     }
     // a CTA that runs several chains keeps its right to allocate tensor memory
@@ -1040,16 +1146,13 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                 fence_after_sync();
                 mma_ts_k(tDbuf(kk), tb + TM_SB, smem_u32(P + PK_WQ), 128, 8, id1, false);
                 mma_commit(bar_v);
+                if (kk > 0) mma2(kk - 1);
                 ok = mbar_wait_spin(&bar_vt[kk & 1], (kk >> 1) & 1);  // V~^T written, S^T scaled by gamma_kk
                 ok = ok && mbar_wait_spin(&bar_ld2[kk & 1], (kk >> 1) & 1);  // part 2 of packet kk
                 if (!ok) break;
                 fence_after_sync();
                 mma_ts_mn(tb + TM_S, tb + TM_VT + 32 * (kk & 1), smem_u32(P + PK_K), 8192, 4, id3, true);
                 mma_commit(bar_s);
-                // the previous chunk's output product runs behind this chunk's state update (off the
-                // recurrence's critical path); the in-order pipe still finishes it before MMA1 of chunk
-                // kk + 1 rewrites its D buffer or the recurrence warps rewrite its V~ buffer
-                if (kk > 0) mma2(kk - 1);
             }
             if (ok && nc > 0) mma2(nc - 1);
             if (!ok) atomicExch(s_fail, 1);
@@ -1093,12 +1196,32 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
         }
         if (!ok && lane == 0) atomicExch(s_fail, 1);
     } else if (warp >= 12 && warp < 16) {
-        // ------------------------------------------------ output warps 12-15 (128 threads, one d_v lane each)
+        // ------------------------------------------------ output warps 12-15 (128 threads, one d_v lane each).
+        // With the output epilogue (Eq. 6 without its projections: y = Sigmoid(g) w o~ / sqrt(mean o~^2 + eps)
+        // per token over the head's d_v channels), o~ goes through the staging tile as bf16, as it would be
+        // stored, and a second pass over the tile (thread = token, 8-channel chunk; the row's 16 chunks
+        // in 16 lanes) normalises and gates it before the store; the gate tiles come in by TMA, two chunks
+        // ahead.  o~ then never leaves the chip.
         const int ot = tid - 384;
+        const bool epi = gmap != nullptr;
         // byte offset of (token t, channel v) in the staging tile (two 64-channel SW128 halves): row part
         const uint32_t vh = (uint32_t)(v >> 6) * 8192 + ((uint32_t)(v & 7) << 1);
         const int vc = (v & 63) >> 3;
         bool ok = true;
+        auto load_g = [&](int kk) {  // gate tile of chunk kk (ot == 0)
+            unsigned char *gt = sm + CS_GIMG + 16384 * (kk & 1);
+            const int64_t tp = s_tok + (int64_t)kk * C;
+            mbar_arrive_expect_tx(&bar_g[kk & 1], 16384);
+            tma_load_3d(gt, gmap, 0, h, (int)tp, &bar_g[kk & 1]);
+            tma_load_3d(gt + 8192, gmap, 64, h, (int)tp, &bar_g[kk & 1]);
+        };
+        if (epi) {
+            float *wv = reinterpret_cast<float *>(sm + CS_W);
+            wv[ot] = epi_w ? epi_w[(size_t)h * D + ot] : 1.f;
+            if (ot == 0) {
+                for (int kk = 0; kk < 2 && kk < nc; ++kk) load_g(kk);
+            }
+        }
         for (int kk = 0; kk < nc && ok; ++kk) {
             ok = mbar_wait(&bar_o[kk & 1], (kk >> 1) & 1);
             if (!ok) break;
@@ -1115,9 +1238,12 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
             mbar_arrive(&bar_free[kk & 1]);  // TMEM buffer read
             const int64_t tp = s_tok + (int64_t)kk * C;
             const int lenp = (int)min((int64_t)C, e_tok - tp);
-            if (lenp == C) {  // full chunk: two 64 x 64 swizzled tiles, two TMA stores (double-buffered)
+            if (lenp == C || epi) {  // through the staging tile (double-buffered)
                 unsigned char *stg = sm + CS_OIMG + 16384 * (kk & 1);
-                if (ot == 0 && kk >= 2) bulk_wait_read1();  // the store of chunk kk - 2 has left this buffer
+                if (ot == 0 && kk >= 2) {
+                    if (lenp == C) bulk_wait_read1();  // the store of chunk kk - 2 has left this buffer
+                    else bulk_wait_read0();
+                }
                 named_sync(2, 128);
 #pragma unroll
                 for (int t = 0; t < 64; ++t) {
@@ -1125,12 +1251,64 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
                     *reinterpret_cast<uint16_t *>(stg + vh + t * 128 + ((vc ^ (t & 7)) << 4)) =
                         (uint16_t)((t & 1) ? (w >> 16) : (w & 0xFFFFu));
                 }
-                fence_proxy_async();
-                named_sync(2, 128);
-                if (ot == 0) {
-                    tma_store_3d(&omap, stg, 0, h, (int)tp);
-                    tma_store_3d(&omap, stg + 8192, 64, h, (int)tp);
-                    bulk_commit();
+                if (epi) {
+                    ok = bar_red_popc(2, 128, mbar_wait(&bar_g[kk & 1], (kk >> 1) & 1)) == 128;
+                    const unsigned char *gtile = sm + CS_GIMG + 16384 * (kk & 1);
+                    const float *wv = reinterpret_cast<const float *>(sm + CS_W);
+                    const int cc = ot & 15;                      // 8-channel chunk of the row
+                    const uint32_t half = (uint32_t)(cc >> 3) * 8192;
+                    float w8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) w8[e] = wv[8 * cc + e];
+#pragma unroll 2
+                    for (int i = 0; i < 8; ++i) {
+                        const int t = (ot >> 4) + 8 * i;         // the 16 lanes of a row share t
+                        const uint32_t off = half + (uint32_t)t * 128 + ((((uint32_t)cc & 7) ^ (uint32_t)(t & 7)) << 4);
+                        const uint4 ov = *reinterpret_cast<const uint4 *>(stg + off);
+                        const uint4 gv = *reinterpret_cast<const uint4 *>(gtile + off);
+                        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw4[4] = {gv.x, gv.y, gv.z, gv.w};
+                        float of[8], gf[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            of[2 * e] = bf_lo(ow[e]);
+                            of[2 * e + 1] = bf_hi(ow[e]);
+                            gf[2 * e] = bf_lo(gw4[e]);
+                            gf[2 * e + 1] = bf_hi(gw4[e]);
+                        }
+                        float ss = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss = fmaf(of[e], of[e], ss);
+#pragma unroll
+                        for (int off2 = 8; off2 > 0; off2 >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off2);
+                        const float r = rsqrtf(ss * (1.0f / D) + epi_eps);
+                        float y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            y[e] = __fdividef(of[e] * r * w8[e], 1.0f + __expf(-gf[e]));  // inf gives 0
+                        *reinterpret_cast<uint4 *>(stg + off) = pack8(y);
+                    }
+                    fence_proxy_async();
+                    named_sync(2, 128);  // the gate tile has been read: chunk kk + 2 takes its buffer
+                    if (ot == 0 && kk + 2 < nc) load_g(kk + 2);
+                } else {
+                    fence_proxy_async();
+                    named_sync(2, 128);
+                }
+                if (lenp == C) {
+                    if (ot == 0) {
+                        tma_store_3d(&omap, stg, 0, h, (int)tp);
+                        tma_store_3d(&omap, stg + 8192, 64, h, (int)tp);
+                        bulk_commit();
+                    }
+                } else {  // the ragged last chunk of a sequence: rows past its end stay untouched
+                    const int cc = ot & 15;
+                    const uint32_t half = (uint32_t)(cc >> 3) * 8192;
+                    for (int i = 0; i < 8; ++i) {
+                        const int t = (ot >> 4) + 8 * i;
+                        if (t < lenp)
+                            *reinterpret_cast<uint4 *>(o + ((tp + t) * H + h) * D + 8 * cc) = *reinterpret_cast<const uint4 *>(
+                                stg + half + (uint32_t)t * 128 + ((((uint32_t)cc & 7) ^ (uint32_t)(t & 7)) << 4));
+                    }
                 }
             } else {  // the ragged last chunk of a sequence: rows past its end stay untouched
                 bf16 *dst = o + (tp * H + h) * D + v;
@@ -1260,7 +1438,7 @@ __device__ __forceinline__ void chain_role(unsigned char *sm, const CUtensorMap 
     if (tid == 0 && *(volatile int *)s_fail) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
     sync_all();
     if (tid == 0) {  // the CTA may run another chain over the same shared memory
-        for (int i = 0; i < 13; ++i) mbar_inval(bar_ld1 + i);
+        for (int i = 0; i < 15; ++i) mbar_inval(bar_ld1 + i);
     }
     if (warp == 0) tmem_dealloc(tb, 512);
     __syncthreads();
@@ -1271,10 +1449,12 @@ chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N
                       const int32_t *__restrict__ chunk_start, const int32_t *__restrict__ seg_start,
                       int64_t seg_len, const float *__restrict__ seg_in, int H,
                       const unsigned char *__restrict__ packets, float scale, const float *initial_state,
-                      float *final_state, bf16 *__restrict__ o, int *err) {
+                      float *final_state, bf16 *__restrict__ o, int *err, const __grid_constant__ CUtensorMap gmap,
+                      int epi, const float *epi_w, float epi_eps) {
     extern __shared__ unsigned char smem_raw[];
     chain_role(align1024(smem_raw), omap, T, N, cu, chunk_start, seg_start, seg_len, seg_in, H, packets, scale,
-               initial_state, final_state, o, err, (int)blockIdx.x, (int)blockIdx.y, nullptr, 0);
+               initial_state, final_state, o, err, (int)blockIdx.x, (int)blockIdx.y, nullptr, 0, nullptr, true,
+               epi ? &gmap : nullptr, epi_w, epi_eps);
 }
 
 // =====================================================================================
@@ -1291,18 +1471,22 @@ chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant
                       float g_min, int64_t T, int N, const int32_t *__restrict__ cu, int H,
                       unsigned char *__restrict__ packets, float scale, const float *initial_state,
                       float *final_state, bf16 *__restrict__ o, int *err, int n_chain, uint64_t *flags,
-                      uint64_t epoch, int kpre) {
+                      uint64_t epoch, int kpre, const __grid_constant__ CUtensorMap gmap, int epi,
+                      const float *epi_w, float epi_eps) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1024(smem_raw);
     const int b = (int)blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t *cs = (int32_t *)(sm + J_CS);  // chunk_start [N + 1]
     int32_t *ss = (int32_t *)(sm + J_SS);  // seg_start [N + 1]: one segment per sequence
+    int32_t *cus = (int32_t *)(sm + J_CU);  // cu_seqlens [N + 1]
+    const int32_t *cu_l = cu ? cus : nullptr;
     int *s_bad = (int *)(sm + J_SS + 4 * (J_TBL_N + 1));
     if (warp == 0) {  // validate cu_seqlens (0 = c_0 <= ... <= c_N = T) and count chunks per sequence
         bool bad = false;
         if (cu) {
             for (int n = lane; n <= N; n += 32) {
                 const int64_t x = cu[n];
+                cus[n] = (int32_t)x;
                 bad = bad || (n == 0 && x != 0) || (n == N && x != T) || (n > 0 && x < (int64_t)cu[n - 1]);
             }
         }
@@ -1336,14 +1520,15 @@ chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant
     }
     if (b < n_chain) {
         if (kpre > 0) {
-            intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, cs, H, packets, err, 0, 1, flags, epoch, kpre,
+            intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu_l, cs, H, packets, err, 0, 1, flags, epoch, kpre,
                        b / H, b % H);
             __syncthreads();
         }
         chain_role(sm, omap, T, N, cu, cs, ss, (int64_t)1 << 30, nullptr, H, packets, scale, initial_state,
-                   final_state, o, err, b / H, b % H, flags, epoch);
+                   final_state, o, err, b / H, b % H, flags, epoch, nullptr, true, epi ? &gmap : nullptr, epi_w,
+                   epi_eps);
     } else {
-        intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, cs, H, packets, err, b - n_chain,
+        intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu_l, cs, H, packets, err, b - n_chain,
                    (int)gridDim.x - n_chain, flags, epoch, kpre, -1, 0);
     }
 }
@@ -1357,8 +1542,8 @@ chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant
 // through `flags` as in the fused launch and are consumed soon after they are written, so they are read
 // from L2 and dropped from it unwritten.  Launched cooperatively (every CTA resident); every wait is
 // bounded.
-constexpr int TEAM_MAX_CHAINS = 1024;  // chains per team the producers' table holds
-constexpr uint32_t J_TCH = J_SS + 4 * (J_TBL_N + 2);   // team mode: chain table [TEAM_MAX_CHAINS]
+constexpr int TEAM_MAX_CHAINS = 512;  // chains per team the producers' table holds
+constexpr uint32_t J_TCH = J_CU + 4 * (J_TBL_N + 1);   // team mode: chain table [TEAM_MAX_CHAINS]
 constexpr uint32_t J_TPRE = J_TCH + 4 * TEAM_MAX_CHAINS;  //            item prefix [TEAM_MAX_CHAINS + 1]
 constexpr uint32_t J_TEAM_TOTAL = J_TPRE + 4 * (TEAM_MAX_CHAINS + 1) + 1024;
 
@@ -1368,18 +1553,22 @@ chunk_team_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant_
                      float g_min, int64_t T, int N, const int32_t *__restrict__ cu, int H,
                      unsigned char *__restrict__ packets, float scale, const float *initial_state,
                      float *final_state, bf16 *__restrict__ o, int *err, int teams, int K, int window,
-                     uint64_t *flags, uint64_t *consumed, uint64_t epoch) {
+                     uint64_t *flags, uint64_t *consumed, uint64_t epoch, const __grid_constant__ CUtensorMap gmap,
+                     int epi, const float *epi_w, float epi_eps) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1024(smem_raw);
     const int b = (int)blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t *cs = (int32_t *)(sm + J_CS);    // chunk_start [N + 1]
     int32_t *perm = (int32_t *)(sm + J_SS);  // sequences by decreasing chunk count
+    int32_t *cus = (int32_t *)(sm + J_CU);   // cu_seqlens [N + 1]
+    const int32_t *cu_l = cu ? cus : nullptr;
     int *s_bad = (int *)(sm + J_SS + 4 * (J_TBL_N + 1));
     if (warp == 0) {  // validate cu_seqlens (0 = c_0 <= ... <= c_N = T) and count chunks per sequence
         bool bad = false;
         if (cu) {
             for (int n = lane; n <= N; n += 32) {
                 const int64_t x = cu[n];
+                cus[n] = (int32_t)x;
                 bad = bad || (n == 0 && x != 0) || (n == N && x != T) || (n > 0 && x < (int64_t)cu[n - 1]);
             }
         }
@@ -1432,7 +1621,8 @@ chunk_team_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant_
             const int r = chain_of(blk);
             if (r < 0) break;
             chain_role(sm, omap, T, N, cu, cs, nullptr, (int64_t)1 << 30, nullptr, H, packets, scale, initial_state,
-                       final_state, o, err, perm[r / H], r % H, flags, epoch, consumed, false);
+                       final_state, o, err, perm[r / H], r % H, flags, epoch, consumed, false,
+                       epi ? &gmap : nullptr, epi_w, epi_eps);
         }
     } else {
         int32_t *tch = (int32_t *)(sm + J_TCH), *tpre = (int32_t *)(sm + J_TPRE);
@@ -1452,7 +1642,7 @@ chunk_team_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant_
         }
         __syncthreads();
         const TeamItems ti{tch, tpre, s_count, K, role - 1, window, consumed};
-        intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu, cs, H, packets, err, 0, 1, flags, epoch, 0, -1, 0,
+        intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu_l, cs, H, packets, err, 0, 1, flags, epoch, 0, -1, 0,
                    &ti);
     }
 }
@@ -1877,7 +2067,8 @@ static uint64_t next_launch_epoch() {
 }
 
 static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws, cudaStream_t stream,
-                         const tcp::TileMaps &tm, const CUtensorMap &omap, int sms, int *err) {
+                         const tcp::TileMaps &tm, const CUtensorMap &omap, int sms, int *err,
+                         const CUtensorMap &gmap, int epi) {
     const uint32_t smem = tcp::J_TOTAL > tcp::CS_TOTAL ? tcp::J_TOTAL : tcp::CS_TOTAL;
     if (set_smem((const void *)tcp::chunk_fused_tc_kernel, smem) != KDA_OK) return false;
     int per_sm = 0;
@@ -1896,8 +2087,11 @@ static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void 
     const int32_t *cu = a->cu_seqlens;
     float *fin = a->final_state;
     bf16 *o = (bf16 *)a->o;
+    const float *epi_w = a->out_norm_weight;
+    float epi_eps = a->out_norm_eps;
     void *args[] = {(void *)&tm, (void *)&omap, &beta, &bias, &A_log, &g_min, &T, &N, &cu, &H, &packets,
-                    &scale, &init, &fin, &o, &err, &n_chain, &flags, &epoch, &kpre};
+                    &scale, &init, &fin, &o, &err, &n_chain, &flags, &epoch, &kpre, (void *)&gmap, &epi, &epi_w,
+                    &epi_eps};
     if (cudaLaunchCooperativeKernel((const void *)tcp::chunk_fused_tc_kernel, dim3((unsigned)sms), dim3(tcp::NT2),
                                     args, smem, stream) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -1909,7 +2103,8 @@ static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void 
 // The chain-team schedule (see chunk_team_tc_kernel).  Returns false (and clears the launch error)
 // when the device refuses to make every CTA resident; the caller then runs the separate kernels.
 static bool launch_team(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws, cudaStream_t stream,
-                        const tcp::TileMaps &tm, const CUtensorMap &omap, int sms, int *err, uint64_t epoch) {
+                        const tcp::TileMaps &tm, const CUtensorMap &omap, int sms, int *err, uint64_t epoch,
+                        const CUtensorMap &gmap, int epi) {
     const uint32_t smem = tcp::J_TEAM_TOTAL > tcp::CS_TOTAL ? tcp::J_TEAM_TOTAL : tcp::CS_TOTAL;
     if (set_smem((const void *)tcp::chunk_team_tc_kernel, smem) != KDA_OK) return false;
     int per_sm = 0;
@@ -1929,8 +2124,11 @@ static bool launch_team(const kda_chunk_args *a, const kda_chunk_plan &p, void *
     const int32_t *cu = a->cu_seqlens;
     float *fin = a->final_state;
     bf16 *o = (bf16 *)a->o;
+    const float *epi_w = a->out_norm_weight;
+    float epi_eps = a->out_norm_eps;
     void *args[] = {(void *)&tm, (void *)&omap, &beta, &bias, &A_log, &g_min, &T, &N, &cu, &H, &packets, &scale,
-                    &init, &fin, &o, &err, &teams, &K, &window, &flags, &consumed, &epoch};
+                    &init, &fin, &o, &err, &teams, &K, &window, &flags, &consumed, &epoch, (void *)&gmap, &epi, &epi_w,
+                    &epi_eps};
     if (cudaLaunchCooperativeKernel((const void *)tcp::chunk_team_tc_kernel, dim3((unsigned)grid), dim3(tcp::NT2), args,
                                     smem, stream) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -1949,10 +2147,11 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     tcp::TileMaps tm;
-    CUtensorMap omap;
+    CUtensorMap omap, gmap;
+    const int epi = (a->out_gate && p.epi_fused) ? 1 : 0;  // the output epilogue runs in the output pass
     if (!make_tile_map(&tm.q, a->q, a->T, p.H) || !make_tile_map(&tm.k, a->k, a->T, p.H) ||
         !make_tile_map(&tm.v, a->v, a->T, p.H) || !make_tile_map(&tm.z, a->z, a->T, p.H) ||
-        !make_tile_map(&omap, a->o, a->T, p.H))
+        !make_tile_map(&omap, a->o, a->T, p.H) || !make_tile_map(&gmap, epi ? a->out_gate : a->o, a->T, p.H))
         return KDA_ERR_CUDA;
     kda_profile_mark(0, stream);
     // The fused launch publishes packets through flags tagged with a host-side epoch.  A captured
@@ -1966,12 +2165,12 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     }
     const bool capturing = cap != cudaStreamCaptureStatusNone;
     if (p.fused && !capturing && p.max_chunks > 0 && a->T > 0 &&
-        launch_fused(a, p, ws, stream, tm, omap, sms, err)) {
+        launch_fused(a, p, ws, stream, tm, omap, sms, err, gmap, epi)) {
         kda_profile_mark(1, stream);
         return kda_cuda_status(cudaGetLastError());
     }
     if (p.team && !capturing && p.max_chunks > 0 && a->T > 0 &&
-        launch_team(a, p, ws, stream, tm, omap, sms, err, next_launch_epoch())) {
+        launch_team(a, p, ws, stream, tm, omap, sms, err, next_launch_epoch(), gmap, epi)) {
         kda_profile_mark(1, stream);
         return kda_cuda_status(cudaGetLastError());
     }
@@ -2015,7 +2214,7 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     if (st != KDA_OK) return st;
     tcp::chunk_inter_tc_kernel<<<dim3((unsigned)p.max_segs, (unsigned)p.H), tcp::NT3, tcp::CS_TOTAL, stream>>>(
         omap, a->T, (int)a->N, a->cu_seqlens, chunk_start, seg_start, p.seg_len, seg_in, p.H, packets, a->scale,
-        a->initial_state, a->final_state, (bf16 *)a->o, err);
+        a->initial_state, a->final_state, (bf16 *)a->o, err, gmap, epi, a->out_norm_weight, a->out_norm_eps);
     kda_profile_mark(mark, stream);
     return kda_cuda_status(cudaGetLastError());
 }

@@ -43,6 +43,17 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
                  :: "r"((uint32_t)__cvta_generic_to_shared(smem_dst)), "l"(gsrc) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// 4-byte asynchronous copy global -> shared memory (both 4-byte aligned).
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(smem_dst)), "l"(gsrc) : "memory");
+}
+// The executing thread's earlier cp.async copies arrive (once, when all have landed) on an mbarrier whose
+// expected count includes this arrival.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(bar)) : "memory");
+}
 
 // rows x cols fp32 block from global (row pitch gp floats) to shared memory (row pitch sp floats) by
 // 16-byte copies spread over nt threads; cols, gp, sp multiples of 4 and both bases 16-byte aligned

@@ -49,11 +49,17 @@ struct kda_chunk_plan {
     // Chain teams (tensor-core path, many chains): one cooperative launch of `teams` teams, each a
     // chain CTA and team_k producer CTAs; producers run at most team_window of their own items ahead.
     int team;                // 1 if the team schedule runs (then fused = 0)
+    // The output epilogue (out_gate) runs inside the output pass instead of as its own pass over o.  Not
+    // for the fused launch on short chains, where the output pass bounds the latency of the call.
+    int epi_fused;
     int teams, team_k, team_window;
     size_t off_flags;
     size_t off_consumed;     // team schedule: per (chunk slot, head), the epoch once its chain has started on it
     size_t total_bytes;
 };
+
+// The schedule forced by kda_set_chunk_schedule (KDA_SCHEDULE_AUTO: the latency model chooses).
+int kda_chunk_schedule_override();
 
 // gate_kind KDA_GATE_SOFTPLUS always takes the fp32 CUDA-core path (its in-chunk decays are not
 // bounded, so the tensor-core operand images could overflow).

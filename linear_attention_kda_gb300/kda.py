@@ -32,7 +32,7 @@ EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_re
             "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws",
             "kda_last_cuda_error", "kda_chunk_fwd_schedule", "kda_output_gate", "kda_recurrent_replay",
             "kda_chunk_fwd_workspace_size_gate", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size",
-            "kda_selftest_bounded_wait", "kda_set_debug_checks"]
+            "kda_selftest_bounded_wait", "kda_set_debug_checks", "kda_set_chunk_schedule"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 _vp = ctypes.c_void_p
@@ -135,6 +135,8 @@ def load_library(path: Optional[str] = None):
         L.kda_chunk_fwd_static_ws.restype = ctypes.c_int
         L.kda_set_debug_checks.argtypes = [_i32]
         L.kda_set_debug_checks.restype = ctypes.c_int
+        L.kda_set_chunk_schedule.argtypes = [_i32]
+        L.kda_set_chunk_schedule.restype = ctypes.c_int
         L.kda_recurrent_replay.argtypes = [ctypes.POINTER(ReplayArgs), _vp]
         L.kda_recurrent_replay.restype = ctypes.c_int
         L.kda_output_gate.argtypes = [ctypes.POINTER(OutputGateArgs), _vp]
@@ -360,6 +362,14 @@ def get_device_error(device=None) -> int:
 
 
 CHECK_FINITE = 1
+SCHEDULES = {"auto": 0, "separate": 1, "fused": 2, "team": 3}
+
+
+def set_chunk_schedule(mode: str) -> None:
+    """kda_set_chunk_schedule: "auto" (the library's latency model), or force "separate", "fused" or
+    "team" where the problem is eligible for it (process-wide; every schedule computes the same result)."""
+    _check(load_library().kda_set_chunk_schedule(SCHEDULES[mode]), "kda_set_chunk_schedule")
+
 
 
 def set_debug_checks(flags: int) -> None:
@@ -383,14 +393,15 @@ def set_profile_events(events) -> None:
 
 
 def chunk_fwd_kernel_count(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, cu_seqlens_host=None,
-                           gate: str = "lower_bound") -> int:
-    """Kernels kda_chunk_fwd launches for these sizes (the split-sequence state pass adds two)."""
+                           gate: str = "lower_bound", out_gate: bool = False) -> int:
+    """Kernels kda_chunk_fwd launches for these sizes (the split-sequence state pass adds two; with
+    out_gate, a separate epilogue pass adds one where the output pass does not apply it)."""
     cu = None
     if cu_seqlens_host is not None:
         cu = cu_seqlens_host.to(dtype=torch.int32, device="cpu").contiguous()
     a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=KDA_BF16 if dtype == torch.bfloat16 else KDA_F32,
                   cu_seqlens_host=None if cu is None else cu.data_ptr(), chunk_size=64,
-                  gate_kind=_gate_kind(gate))
+                  gate_kind=_gate_kind(gate), out_gate=16 if out_gate else None)
     return int(load_library().kda_chunk_fwd_kernel_count(ctypes.byref(a)))
 
 

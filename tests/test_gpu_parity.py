@@ -707,3 +707,50 @@ def test_team_schedule_bad_cu_seqlens_reports_device_error():
     kda.chunk_fwd(*(d[n].to(dev) for n in ("q", "k", "v", "z", "beta")), None, None, cu_seqlens=cu.to(dev),
                   cu_seqlens_host=d["cu_seqlens"], output_final_state=True)
     assert kda.get_device_error() == 7
+
+
+@pytest.mark.parametrize("schedule", ["separate", "team"])
+def test_output_epilogue_inside_the_output_pass(schedule):
+    """The epilogue applied by the output pass itself (separate kernels, chain teams) on a ragged batch
+    with an empty sequence and states: per (sequence, head) against the oracle's recurrence followed by
+    the Eq. 6 epilogue, and equal to the recurrence plus a separate kda_output_gate call."""
+    w_ = syn.Workload("vi", H=8, d=128, dtype="bf16", seq_len=None, z_std=1.5, b_range=1.0,
+                      alog_std=0.25, s0_std=0.02)
+    rng = np.random.default_rng(81)
+    lengths = [int(x) for x in rng.integers(0, 300, size=20)]
+    lengths[2], lengths[9] = 0, 64
+    d = _varlen(w_, lengths, seed=82)
+    T = sum(lengths)
+    g, w = syn.make_output_gate_inputs(T, 8, 128, "bf16", 83)
+    try:
+        kda.set_chunk_schedule(schedule)
+        sch = kda.chunk_fwd_schedule(T, len(lengths), 8, 128, 128, torch.bfloat16, d["cu_seqlens"])
+        assert sch[schedule] if schedule == "team" else not (sch["fused"] or sch["team"])
+        o, fs = run_prefill(d, out_gate=g.cuda(), out_norm_weight=w.cuda(), out_norm_eps=EPS)
+        o_plain, _ = run_prefill(d)
+    finally:
+        kda.set_chunk_schedule("auto")
+    compare_prefill(d, o, fs, _epilogue_ref(d, oracle_prefill(d), g, w), TOL_BF16)
+    y = kda.output_gate(o_plain.to(torch.bfloat16).cuda(), g.cuda(), w.cuda(), EPS).float().cpu()
+    assert rel_err(o.numpy(), y.numpy()) <= 1e-2
+
+
+@pytest.mark.parametrize("schedule", ["fused", "auto"])
+def test_output_epilogue_inside_long_chains(schedule):
+    """Chains of at least 256 chunks apply the epilogue in their output pass: T = 16421 tokens (a ragged
+    last chunk), 4 heads, on the one-launch schedule (forced) and on the schedule the model picks for it
+    (the split state pass: segment summaries, fold, output pass per segment), against the oracle."""
+    w_ = syn.Workload("lo", H=4, d=128, dtype="bf16", n_seq=1, seq_len=16421, z_std=1.5, b_range=1.0,
+                      alog_std=0.25)
+    d = syn.make_prefill(w_, seed=84)
+    T = 16421
+    g, w = syn.make_output_gate_inputs(T, 4, 128, "bf16", 85)
+    try:
+        kda.set_chunk_schedule(schedule)
+        sch = kda.chunk_fwd_schedule(T, 1, 4, 128, 128, torch.bfloat16, d["cu_seqlens"])
+        assert sch["fused"] if schedule == "fused" else sch["seg_len"] > 0
+        assert sch["kernels"] == (1 if schedule == "fused" else 5)  # no separate epilogue pass
+        o, fs = run_prefill(d, out_gate=g.cuda(), out_norm_weight=w.cuda(), out_norm_eps=EPS)
+    finally:
+        kda.set_chunk_schedule("auto")
+    compare_prefill(d, o, fs, _epilogue_ref(d, oracle_prefill(d), g, w), TOL_BF16)
