@@ -207,7 +207,7 @@ static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int
         (double)n_chain <= (double)(sms / 2) * TEAM_MAX_CHAINS_HOST) {
         for (int k = 1; k <= 8; ++k) {
             const int teams = sms / (k + 1);
-            if (teams < 1 || (double)n_chain > (double)teams * TEAM_MAX_CHAINS_HOST) continue;
+            if (teams < 1 || teams > KDA_CTR_MAX || (double)n_chain > (double)teams * TEAM_MAX_CHAINS_HOST) continue;
             const double per_team = items / teams;  // chunk steps (= packets) per team
             const double chain = std::max(per_team, (double)longest) * T_CHAIN +
                                  std::ceil((double)n_chain / teams) * T_CHAIN_START;
@@ -300,6 +300,8 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
     end = p->off_flags + sizeof(uint64_t) * (size_t)p->max_chunks * (size_t)H;
     p->off_consumed = align_up(end, 256);
     if (p->team) end = p->off_consumed + sizeof(uint64_t) * (size_t)p->max_chunks * (size_t)H;
+    p->off_ctr = align_up(end, 256);
+    if (p->path == 1) end = p->off_ctr + sizeof(uint64_t) * KDA_CTR_STRIDE * KDA_CTR_MAX;
     p->total_bytes = align_up(end, 256);
     return true;
 }

@@ -205,6 +205,7 @@ constexpr uint32_t GR_TT = GR_K + 12288;     // T_11^T as a K-major tf32 image, 
 constexpr uint32_t J_SH = 2 * GR_BYTES;       // shared by both groups
 constexpr uint32_t J_TSLOT = J_SH;            // TMEM base
 constexpr uint32_t J_TOK = J_SH + 16;         // mbarriers tok[2]: group g may start its gate and element pass
+constexpr uint32_t J_PAIR = J_SH + 32;        // int64 [4]: items taken from the launch's counter
 // Tables a CTA keeps while it runs both roles (fused and team launches): past the shared memory of either
 constexpr uint32_t J_TAB0 = (J_SH + 64 > CS_BAR + 256 ? J_SH + 64 : CS_BAR + 256);
 constexpr uint32_t J_TBL = (J_TAB0 + 63) / 64 * 64;  // int32 [J_TBL_N + 1]: producer chunks before each sequence
@@ -354,24 +355,27 @@ struct TeamItems {
 //    sequence are taken away (in the same order);
 //  - own_n >= 0: the first kpre chunks of sequence own_n for head own_h;
 //  - team != nullptr: the items of a chain team (see TeamItems).
-// The CTA's it-th item goes to consumer group it & 1.  With `flags`, each item's packet is published
-// (flags[item] = epoch) once its writes have completed.  In the last mode the CTA keeps its right to
-// allocate tensor memory (its chain runs next).
+// Each mode orders its items (k = 0, 1, ...).  Without `ctr` the CTA takes items k = worker,
+// worker + nworkers, ... (a team producer q of K: q, q + K, ...), its it-th item going to consumer group
+// it & 1.  With `ctr` (not for own_n >= 0), the CTA takes pairs of consecutive items, one per group, from
+// a counter shared by the launch, so that CTAs on slower SMs take fewer items; the counter holds
+// (low 32 bits of the epoch) << 32 | items taken, and the first CTA to see a stale tag installs this
+// launch's.  With `flags`, each item's packet is published (flags[item] = epoch) once its writes have
+// completed.  With own_n >= 0 the CTA keeps its right to allocate tensor memory (its chain runs next).
 __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm, const bf16 *__restrict__ beta,
                                            const float *__restrict__ bias, const float *__restrict__ A_log,
                                            float g_min, int64_t T, int N, const int32_t *__restrict__ cu,
                                            const int32_t *__restrict__ chunk_start, int H,
                                            unsigned char *__restrict__ packets, int *err, int worker, int nworkers,
                                            uint64_t *flags, uint64_t epoch, int kpre, int own_n, int own_h,
-                                           const TeamItems *team = nullptr) {
+                                           const TeamItems *team = nullptr, uint64_t *ctr = nullptr) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t *tbl = (int32_t *)(sm + J_TBL);  // kpre > 0: tbl[n] = producer chunks of sequences before n
-    int n_items = 0;
+    int64_t n_all = 0;                       // items of the mode
     if (team) {
-        const int tot = team->pre[team->count];
-        n_items = team->q < tot ? (tot - team->q + team->K - 1) / team->K : 0;
+        n_all = team->pre[team->count];
     } else if (own_n >= 0) {
-        n_items = min(kpre, chunk_start[own_n + 1] - chunk_start[own_n]);
+        n_all = min(kpre, chunk_start[own_n + 1] - chunk_start[own_n]);
     } else if (kpre > 0) {
         if (warp == 0) {
             int carry = 0;
@@ -389,16 +393,54 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
             }
         }
         __syncthreads();
-        const int64_t Wp = (int64_t)tbl[N] * H;
-        n_items = worker < Wp ? (int)((Wp - worker + nworkers - 1) / nworkers) : 0;
+        n_all = (int64_t)tbl[N] * H;
     } else {
-        const int64_t W = (int64_t)chunk_start[N] * H;
-        n_items = worker < W ? (int)((W - worker + nworkers - 1) / nworkers) : 0;
+        n_all = (int64_t)chunk_start[N] * H;
     }
-    if (n_items == 0) return;
-    auto w_of = [&](int it) -> int64_t {  // global item index of this CTA's it-th item
+    const bool dyn = ctr != nullptr && own_n < 0;
+    const int64_t k_first = team ? team->q : (own_n >= 0 ? 0 : worker);
+    const int64_t k_step = team ? team->K : (own_n >= 0 ? 1 : nworkers);
+    const int team_window = team ? team->window * team->K : 0;  // in team items
+    int64_t *pk = (int64_t *)(sm + J_PAIR);  // dynamic: the first item of the CTA's pair j in pk[j & 3]
+    bool ctr_live = false;                   // thread 0: the counter holds this launch's tag
+    auto grab = [&]() -> int64_t {           // thread 0: the first item of the CTA's next pair
+        const uint64_t tag = (uint64_t)(uint32_t)epoch << 32, hi = 0xffffffff00000000ull;
+        unsigned long long *c = reinterpret_cast<unsigned long long *>(ctr);
+        if (!ctr_live) {
+            uint64_t cur = atomicAdd(c, 0ull);
+            for (int i = 0; i < 1024 && (cur & hi) != tag; ++i) {
+                const uint64_t prev = atomicCAS(c, cur, tag | 2ull);
+                if (prev == cur) {
+                    ctr_live = true;
+                    return 0;
+                }
+                cur = prev;
+            }
+            if ((cur & hi) != tag) {
+                set_error(err, KDA_ERR_DEVICE_TIMEOUT);
+                return n_all;
+            }
+            ctr_live = true;
+        }
+        return (int64_t)(atomicAdd(c, 2ull) & 0xffffffffull);
+    };
+    if (dyn) {
+        if (tid == 0) {
+            pk[0] = grab();
+            pk[1] = grab();
+        }
+        __syncthreads();
+        if (pk[0] >= n_all) return;
+    } else if (k_first >= n_all) {
+        return;
+    }
+    auto k_of = [&](int j, int gg) -> int64_t {  // mode item of group gg's j-th item
+        return dyn ? pk[j & 3] + gg : k_first + (int64_t)(2 * j + gg) * k_step;
+    };
+    auto has = [&](int j, int gg) -> bool { return k_of(j, gg) < n_all; };
+    auto w_of = [&](int64_t k64) -> int64_t {  // global item index of the mode's item k
         if (team) {
-            const int k = team->q + it * team->K;
+            const int k = (int)k64;
             int lo = 0, hi = team->count;  // the chain holding team item k: largest m with pre[m] <= k
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
@@ -407,8 +449,8 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
             const int id = team->chain[lo];
             return (int64_t)(chunk_start[id / H] + (k - team->pre[lo])) * H + (id % H);
         }
-        if (own_n >= 0) return (int64_t)(chunk_start[own_n] + it) * H + own_h;
-        const int64_t k = (int64_t)worker + (int64_t)it * nworkers;
+        if (own_n >= 0) return (int64_t)(chunk_start[own_n] + k64) * H + own_h;
+        const int64_t k = k64;
         if (kpre <= 0) return k;
         const int64_t kk = k / H;
         int lo = 0, hi = N;  // the sequence holding producer chunk kk: largest n with tbl[n] <= kk
@@ -440,7 +482,6 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
     uint64_t *bar = (uint64_t *)(R + GR_BAR);
     uint64_t *ld_qzk = bar, *ld_v = bar + 1, *bar_mma = bar + 2;
     const uint32_t tbg = tb + 256u * (uint32_t)g;
-    const int nj = (n_items - g + 1) / 2;  // items it = 2 j + g
     // The two groups take turns at the gate and element pass (MUFU and shared-memory bound), each
     // starting it once the other has finished its own, so that one group's element pass overlaps the
     // other's inverse and products.  Group 0 starts.
@@ -459,7 +500,10 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
     // The slot's plain stores are ordered before their readers by the group barriers in between.
     auto fill_slot = [&](int j) {
         const int s = j & 1;
-        const int64_t w = w_of(2 * j + g);
+        const bool take = dyn && g == 0 && lane == 0 && j >= 1;  // group 0 takes pair j + 1
+        int64_t nxt = 0;
+        if (take) nxt = grab();
+        const int64_t w = w_of(k_of(j, g));
         int n = 0, len = 0, h;
         int64_t t0 = 0, slot;
         if (w <= 0xffffffffll) {  // 32-bit division where it suffices
@@ -493,6 +537,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
             else *al = 0.f;
         }
         cp_async_arrive_noinc(ld_qzk);
+        if (take) pk[(j + 1) & 3] = nxt;
     };
     // Item j's q, z, k (and v) tiles by TMA (thread 0, which filled the slot)
     auto issue_tma = [&](int j, bool with_v) {
@@ -519,7 +564,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
         }
     };
     bool ok = true;
-    if (gw == 0 && nj > 0) {
+    if (gw == 0 && has(0, g)) {
         fill_slot(0);
         if (lane == 0) issue_tma(0, true);
     }
@@ -528,7 +573,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
     // element mapping: 8 channels (one 16-byte chunk cg of 64-channel block hb) x 4 tokens 16 tq + 4 tl + i
     const int hb = gw & 1, tq = gw >> 1, cg = lane & 7, tl = lane >> 3;
     const int c0 = 64 * hb + 8 * cg;
-    for (int j = 0; j < nj && ok; ++j) {
+    for (int j = 0; has(j, g) && ok; ++j) {
         const uint32_t par = j & 1;
         const int s = j & 1;
         if (gt == 0 && j > 0) {
@@ -544,9 +589,9 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
         {
             bool okt = true;
             if (gt == 0) {
-                const int it = 2 * j + g;
-                if (team && it >= team->window)  // start at most `window` items ahead of the chain
-                    okt = flag_wait(team->consumed + w_of(it - team->window), epoch);
+                const int64_t kb = k_of(j, g) - (int64_t)team_window;
+                if (team && kb >= 0)  // start at most `window` items of each producer ahead of the chain
+                    okt = flag_wait(team->consumed + w_of(kb), epoch);
                 if (!okt) {
                 } else if (g == 1) okt = mbar_wait(&tok[1], j & 1);       // group 0 has done its item j
                 else if (j > 0) okt = mbar_wait(&tok[0], (j - 1) & 1);      // group 1 has done its item j - 1
@@ -728,7 +773,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
             mma_commit(bar_mma);
             // the other group's turn, while it has an item left that waits for this one: group 1's item j
             // waits for group 0's item j, group 0's item j + 1 for group 1's item j
-            if (g == 0 ? j < n_items / 2 : j + 1 < (n_items + 1) / 2) mbar_arrive(&tok[1 - g]);
+            if (g == 0 ? has(j, 1) : has(j + 1, 0)) mbar_arrive(&tok[1 - g]);
             if (flags && j > 0) publish(w_prev);  // while the product runs
         }
         ok = mwait();
@@ -908,7 +953,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
                 for (int q = 0; q < 8; ++q) o[q] = -d[8 * h2 + q] * bet[c16 + 8 * h2 + q];
                 *reinterpret_cast<uint4 *>(R + GR_K0 + img_chunk_off(64, r, (c16 >> 3) + h2)) = pack8(o);
             }
-        } else if (gw == 0 && j + 1 < nj) {
+        } else if (gw == 0 && has(j + 1, g)) {
             fill_slot(j + 1);  // while warps 1 and 5 read the merge out
         }
         fence_proxy_async();
@@ -928,7 +973,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
             }
         }
         // L and T are dead: while the products run, the next item's q, z and k tiles come in
-        if (gt == 0 && j + 1 < nj && okm) issue_tma(j + 1, false);
+        if (gt == 0 && has(j + 1, g) && okm) issue_tma(j + 1, false);
         ok = gsync_and(g, ok && okm);
         if (!ok) break;
         ok = mwait();
@@ -988,7 +1033,7 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
                       const float *__restrict__ bias, const float *__restrict__ A_log, float g_min,
                       int64_t T, int N, const int32_t *__restrict__ cu,
                       const int32_t *__restrict__ chunk_start, int H, unsigned char *__restrict__ packets,
-                      int *err) {
+                      int *err, uint64_t *ctr, uint64_t epoch) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1024(smem_raw);
     const int32_t *cs = chunk_start, *cu_l = cu;
@@ -1003,7 +1048,7 @@ chunk_intra_tc_kernel(const __grid_constant__ TileMaps tm, const bf16 *__restric
         if (cu) cu_l = c;
     }
     intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu_l, cs, H, packets, err, (int)blockIdx.x, (int)gridDim.x,
-               nullptr, 0, 0, -1, 0);
+               nullptr, epoch, 0, -1, 0, nullptr, ctr);
 }
 
 constexpr int NT3 = 512;  // warps 0-7: recurrence; 8: MMA issue; 9: packet loads; 12-15: output; 10, 11 idle
@@ -1472,7 +1517,7 @@ chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant
                       unsigned char *__restrict__ packets, float scale, const float *initial_state,
                       float *final_state, bf16 *__restrict__ o, int *err, int n_chain, uint64_t *flags,
                       uint64_t epoch, int kpre, const __grid_constant__ CUtensorMap gmap, int epi,
-                      const float *epi_w, float epi_eps) {
+                      const float *epi_w, float epi_eps, uint64_t *ctr) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1024(smem_raw);
     const int b = (int)blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1529,7 +1574,7 @@ chunk_fused_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant
                    epi_eps);
     } else {
         intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu_l, cs, H, packets, err, b - n_chain,
-                   (int)gridDim.x - n_chain, flags, epoch, kpre, -1, 0);
+                   (int)gridDim.x - n_chain, flags, epoch, kpre, -1, 0, nullptr, ctr);
     }
 }
 
@@ -1554,7 +1599,7 @@ chunk_team_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant_
                      unsigned char *__restrict__ packets, float scale, const float *initial_state,
                      float *final_state, bf16 *__restrict__ o, int *err, int teams, int K, int window,
                      uint64_t *flags, uint64_t *consumed, uint64_t epoch, const __grid_constant__ CUtensorMap gmap,
-                     int epi, const float *epi_w, float epi_eps) {
+                     int epi, const float *epi_w, float epi_eps, uint64_t *ctr) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1024(smem_raw);
     const int b = (int)blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1643,7 +1688,7 @@ chunk_team_tc_kernel(const __grid_constant__ TileMaps tm, const __grid_constant_
         __syncthreads();
         const TeamItems ti{tch, tpre, s_count, K, role - 1, window, consumed};
         intra_role(sm, tm, beta, bias, A_log, g_min, T, N, cu_l, cs, H, packets, err, 0, 1, flags, epoch, 0, -1, 0,
-                   &ti);
+                   &ti, ctr ? ctr + KDA_CTR_STRIDE * t : nullptr);
     }
 }
 
@@ -2089,9 +2134,10 @@ static bool launch_fused(const kda_chunk_args *a, const kda_chunk_plan &p, void 
     bf16 *o = (bf16 *)a->o;
     const float *epi_w = a->out_norm_weight;
     float epi_eps = a->out_norm_eps;
+    uint64_t *ctr = (uint64_t *)((char *)ws + p.off_ctr);
     void *args[] = {(void *)&tm, (void *)&omap, &beta, &bias, &A_log, &g_min, &T, &N, &cu, &H, &packets,
                     &scale, &init, &fin, &o, &err, &n_chain, &flags, &epoch, &kpre, (void *)&gmap, &epi, &epi_w,
-                    &epi_eps};
+                    &epi_eps, &ctr};
     if (cudaLaunchCooperativeKernel((const void *)tcp::chunk_fused_tc_kernel, dim3((unsigned)sms), dim3(tcp::NT2),
                                     args, smem, stream) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -2126,9 +2172,10 @@ static bool launch_team(const kda_chunk_args *a, const kda_chunk_plan &p, void *
     bf16 *o = (bf16 *)a->o;
     const float *epi_w = a->out_norm_weight;
     float epi_eps = a->out_norm_eps;
+    uint64_t *ctr = (uint64_t *)((char *)ws + p.off_ctr);
     void *args[] = {(void *)&tm, (void *)&omap, &beta, &bias, &A_log, &g_min, &T, &N, &cu, &H, &packets, &scale,
                     &init, &fin, &o, &err, &teams, &K, &window, &flags, &consumed, &epoch, (void *)&gmap, &epi, &epi_w,
-                    &epi_eps};
+                    &epi_eps, &ctr};
     if (cudaLaunchCooperativeKernel((const void *)tcp::chunk_team_tc_kernel, dim3((unsigned)grid), dim3(tcp::NT2), args,
                                     smem, stream) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -2183,9 +2230,12 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
         if (st != KDA_OK) return st;
         const int64_t items = p.max_chunks * (int64_t)p.H;
         const unsigned grid = (unsigned)(items < sms ? items : sms);
+        // items are handed out through a launch-tagged counter; a captured graph would replay one tag,
+        // so under capture every CTA takes a fixed share instead
+        uint64_t *ctr = capturing ? nullptr : (uint64_t *)((char *)ws + p.off_ctr);
         tcp::chunk_intra_tc_kernel<<<grid, tcp::NT2, tcp::J_TOTAL, stream>>>(
             tm, (const bf16 *)a->beta, a->dt_bias, a->A_log, a->g_min, a->T, (int)a->N, a->cu_seqlens,
-            chunk_start, p.H, packets, err);
+            chunk_start, p.H, packets, err, ctr, next_launch_epoch());
         st = kda_cuda_status(cudaGetLastError());
         if (st != KDA_OK) return st;
     }

@@ -22,6 +22,8 @@ kda_status_t kda_launch_replay(const kda_replay_args *a, cudaStream_t stream);
 
 // Chunked prefill.  Workspace layout is owned by kda_chunk_plan.cu.
 constexpr int KDA_FUSED_MAX_SEQS = 159;  // sequences the fused schedule's producer item map holds
+constexpr int KDA_CTR_MAX = 128;         // producer item counters (one per chain team, or one)
+constexpr int KDA_CTR_STRIDE = 16;       // uint64 words between counters (one 128-byte line each)
 struct kda_chunk_plan {
     int64_t T, N;
     int H, dk, dv, C;
@@ -55,6 +57,7 @@ struct kda_chunk_plan {
     int teams, team_k, team_window;
     size_t off_flags;
     size_t off_consumed;     // team schedule: per (chunk slot, head), the epoch once its chain has started on it
+    size_t off_ctr;          // tensor-core path: item counters of the producers (KDA_CTR_MAX, 128 bytes apart)
     size_t total_bytes;
 };
 
