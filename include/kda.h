@@ -142,9 +142,9 @@ typedef struct {
     /* Optional output epilogue (Eq. 6 without its projections; see kda_output_gate): when out_gate
      * is set, o receives Sigmoid(out_gate) * RMSNorm(o~) instead of the recurrent output o~ (the norm
      * taken on o~ rounded to the dtype of o, as kda_output_gate would read it).  The tensor-core path
-     * applies it in its output pass before o is stored, except on the one-launch schedule for chains
-     * shorter than 256 chunks, which (like the fp32 path) runs a kda_output_gate pass over o in place
-     * after the recurrence. */
+     * applies it in its output pass before o is stored when the chains run as separate kernels; the
+     * one-launch schedule (whose chains bound the call) and the fp32 path run a kda_output_gate pass
+     * over o in place after the recurrence. */
     const void *out_gate;          /* [T, H, dv], dtype of o, 16-byte aligned, or NULL (no epilogue) */
     const float *out_norm_weight;  /* [H, dv] RMSNorm weight, 16-byte aligned, or NULL (ones) */
     float out_norm_eps;            /* RMSNorm epsilon, > 0 when out_gate is set */
@@ -408,7 +408,8 @@ kda_status_t kda_chunk_fwd_schedule(const kda_chunk_args *args, int64_t *out);
  * measurements.  KDA_SCHEDULE_AUTO (the default) lets the library's latency model choose; the others
  * force the separate kernels, the fused launch or the chain-team launch when the problem is eligible
  * for it (fused: sequences x heads + 16 <= SMs; team: at most 159 sequences), else the model's choice
- * among what remains.  Every schedule computes the same result.  Process-wide; applies to later
+ * among what remains.  The model never picks the chain-team launch: on a GB300 it measured 2-4x
+ * slower than the separate kernels or the fused launch on every workload tried.  Every schedule computes the same result.  Process-wide; applies to later
  * calls of kda_chunk_fwd, its workspace size and kda_chunk_fwd_schedule alike.  KDA_ERR_INVALID_ARG
  * for an unknown mode. */
 #define KDA_SCHEDULE_AUTO 0

@@ -202,8 +202,10 @@ static tc_schedule choose_schedule(int64_t T, int64_t N, int H, int C, const int
         }
     }
     // chain teams: teams of one chain CTA and k producers; the chains, dealt longest first in snake
-    // order, give every team about the same number of chunk steps
-    if (N <= KDA_FUSED_MAX_SEQS && (n_chain > sms / 2 || force == KDA_SCHEDULE_TEAM) && force != KDA_SCHEDULE_FUSED &&
+    // order, give every team about the same number of chunk steps.  Only on request: measured on GB300
+    // (T=4096 x 32 heads, 32 x 4.3K-token varlen batch, T=1M x 32 heads) it is 2-4x slower than the
+    // other schedules, its chain steps waiting on packets that left L2 (see kda_set_chunk_schedule).
+    if (N <= KDA_FUSED_MAX_SEQS && force == KDA_SCHEDULE_TEAM &&
         (double)n_chain <= (double)(sms / 2) * TEAM_MAX_CHAINS_HOST) {
         for (int k = 1; k <= 8; ++k) {
             const int teams = sms / (k + 1);
@@ -279,12 +281,11 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
         p->teams = sch.teams;
         p->team_k = sch.team_k;
         p->team_window = 6;  // own items a producer may run ahead of its chain
-        int64_t longest = 0;
-        for (int64_t n = 0; n < N; ++n) {
-            const int64_t len = cu_seqlens_host ? (int64_t)cu_seqlens_host[n + 1] - cu_seqlens_host[n] : T / N;
-            longest = std::max(longest, (len + C - 1) / C);
-        }
-        p->epi_fused = (p->fused && longest < 256) ? 0 : 1;
+        // the output epilogue inside the output pass adds ~2.8K cycles of output-warp work per chunk: cheaper
+        // than its own pass over o where chains run as separate kernels (a 32 x 4.3K-token batch: +0.39 ms
+        // against +0.62 ms), dearer in the one-launch schedule, whose chains bound the launch (T = 256K x 32
+        // heads: +56 % against +16 %)
+        p->epi_fused = p->fused ? 0 : 1;
         p->split = p->seg_len < ((int64_t)1 << 30) ? 1 : 0;
         p->max_segs = p->split ? p->max_chunks / p->seg_len + N : N;
     }

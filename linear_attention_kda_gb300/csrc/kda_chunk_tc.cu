@@ -476,7 +476,8 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
     // also moves the data: the next item's q, z and k tiles are loaded once the inverse has freed their
     // buffers, its v tile once the packet copies of the previous item have read the U^T image; the
     // packet's A image, W, U^T and gamma leave by bulk copies, and an item is published (flags) during the
-    // A / L product of the group's next item, when its copies have long completed.
+    // A / L product of the group's next item, when its copies have long completed (in a chain team, at
+    // the start of the next item, which may wait for the chain).
     const int g = warp >> 3, gt = tid & (NCG - 1), gw = gt >> 5;
     unsigned char *R = sm + g * GR_BYTES;
     uint64_t *bar = (uint64_t *)(R + GR_BAR);
@@ -589,6 +590,9 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
         {
             bool okt = true;
             if (gt == 0) {
+                // a chain team's producer publishes its previous item before it may wait for the chain
+                // (the chain may be waiting for that very packet)
+                if (team && j > 0) publish(w_prev);
                 const int64_t kb = k_of(j, g) - (int64_t)team_window;
                 if (team && kb >= 0)  // start at most `window` items of each producer ahead of the chain
                     okt = flag_wait(team->consumed + w_of(kb), epoch);
@@ -774,7 +778,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
             // the other group's turn, while it has an item left that waits for this one: group 1's item j
             // waits for group 0's item j, group 0's item j + 1 for group 1's item j
             if (g == 0 ? has(j, 1) : has(j + 1, 0)) mbar_arrive(&tok[1 - g]);
-            if (flags && j > 0) publish(w_prev);  // while the product runs
+            if (flags && !team && j > 0) publish(w_prev);  // while the product runs
         }
         ok = mwait();
         if (!ok) break;

@@ -52,7 +52,7 @@ struct kda_chunk_plan {
     // chain CTA and team_k producer CTAs; producers run at most team_window of their own items ahead.
     int team;                // 1 if the team schedule runs (then fused = 0)
     // The output epilogue (out_gate) runs inside the output pass instead of as its own pass over o.  Not
-    // for the fused launch on short chains, where the output pass bounds the latency of the call.
+    // for the fused launch, whose chains bound the launch.
     int epi_fused;
     int teams, team_k, team_window;
     size_t off_flags;

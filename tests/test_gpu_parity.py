@@ -659,6 +659,14 @@ def test_debug_checks_report_non_finite_outputs():
     assert kda.get_device_error() == 0
 
 
+@pytest.fixture
+def team_schedule():
+    """The chain-team launch runs only when asked for (the model never picks it)."""
+    kda.set_chunk_schedule("team")
+    yield
+    kda.set_chunk_schedule("auto")
+
+
 def _team_case(seed, lengths, H=8):
     w = syn.Workload("team", H=H, d=128, dtype="bf16", seq_len=None, z_std=1.5, b_range=1.0,
                      alog_std=0.25, s0_std=0.02)
@@ -668,7 +676,7 @@ def _team_case(seed, lengths, H=8):
     return d
 
 
-def test_team_schedule_varlen_with_states():
+def test_team_schedule_varlen_with_states(team_schedule):
     """The chain-team launch (many chains: 20 sequences x 8 heads) on a ragged batch with empty,
     one-token, one-chunk and unaligned sequences and initial states: every (sequence, head) against
     the oracle; an empty sequence's final state is its initial state bit for bit."""
@@ -681,7 +689,7 @@ def test_team_schedule_varlen_with_states():
     assert torch.equal(fs[3], d["initial_state"][3])
 
 
-def test_team_schedule_final_state_aliases_initial_state():
+def test_team_schedule_final_state_aliases_initial_state(team_schedule):
     """In-place continuation under the chain-team launch: final_state is initial_state."""
     rng = np.random.default_rng(73)
     lengths = [int(x) for x in rng.integers(100, 700, size=24)]
@@ -697,7 +705,7 @@ def test_team_schedule_final_state_aliases_initial_state():
     compare_prefill(d, o.float().cpu(), st.cpu(), ref, TOL_BF16)
 
 
-def test_team_schedule_bad_cu_seqlens_reports_device_error():
+def test_team_schedule_bad_cu_seqlens_reports_device_error(team_schedule):
     """The chain-team launch validates cu_seqlens in every CTA and runs nothing when it is inconsistent."""
     lengths = [100] * 20
     d = _team_case(75, lengths)
@@ -736,10 +744,11 @@ def test_output_epilogue_inside_the_output_pass(schedule):
 
 
 @pytest.mark.parametrize("schedule", ["fused", "auto"])
-def test_output_epilogue_inside_long_chains(schedule):
-    """Chains of at least 256 chunks apply the epilogue in their output pass: T = 16421 tokens (a ragged
-    last chunk), 4 heads, on the one-launch schedule (forced) and on the schedule the model picks for it
-    (the split state pass: segment summaries, fold, output pass per segment), against the oracle."""
+def test_output_epilogue_on_long_chains(schedule):
+    """The epilogue on long chains: T = 16421 tokens (a ragged last chunk), 4 heads, on the one-launch
+    schedule (forced; the epilogue then runs as its own pass) and on the schedule the model picks for it
+    (the split state pass: segment summaries, fold, output pass per segment applying the epilogue),
+    against the oracle."""
     w_ = syn.Workload("lo", H=4, d=128, dtype="bf16", n_seq=1, seq_len=16421, z_std=1.5, b_range=1.0,
                       alog_std=0.25)
     d = syn.make_prefill(w_, seed=84)
@@ -749,7 +758,9 @@ def test_output_epilogue_inside_long_chains(schedule):
         kda.set_chunk_schedule(schedule)
         sch = kda.chunk_fwd_schedule(T, 1, 4, 128, 128, torch.bfloat16, d["cu_seqlens"])
         assert sch["fused"] if schedule == "fused" else sch["seg_len"] > 0
-        assert sch["kernels"] == (1 if schedule == "fused" else 5)  # no separate epilogue pass
+        assert sch["kernels"] == (1 if schedule == "fused" else 5)
+        n_k = kda.chunk_fwd_kernel_count(T, 1, 4, 128, 128, torch.bfloat16, d["cu_seqlens"], out_gate=True)
+        assert n_k == (2 if schedule == "fused" else 5)  # the one-launch schedule adds the epilogue pass
         o, fs = run_prefill(d, out_gate=g.cuda(), out_norm_weight=w.cuda(), out_norm_eps=EPS)
     finally:
         kda.set_chunk_schedule("auto")
