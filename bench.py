@@ -929,6 +929,14 @@ def run_case(args):
         for _ in range(2):
             kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["dt_bias"], d["A_log"],
                           cu_seqlens=d["cu_seqlens"], cu_seqlens_host=d["cu_seqlens"].cpu(), output_final_state=True)
+    elif args.case == "output_gate":
+        # the Eq. 6 epilogue pass alone on 131072 tokens x 32 heads (o, g, y: 1.07 GB each)
+        w = syn.Workload("output_gate_bf16_T131072_H32_d128", H=32, d=128, dtype="bf16", seq_len=131072)
+        o_ = torch.randn(131072, 32, 128, device=dev).to(torch.bfloat16)
+        g_, w_ = syn.make_output_gate_inputs(131072, 32, 128, "bf16", 5, device=dev)
+        y_ = torch.empty_like(o_)
+        for _ in range(3):
+            kda.output_gate(o_, g_, w_, 1e-6, out=y_)
     elif args.case in ("prefill_small", "prefill_4k"):
         if args.case == "prefill_small":
             w = syn.Workload("prefill_small_bf16_T16384_H8_d128", H=8, d=128, dtype="bf16", seq_len=16384,
@@ -964,7 +972,7 @@ def main():
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--case", choices=["prefill_small", "prefill_4k", "decode_small", "replay_256", "softplus_4k",
-                                       "backward_4k", "intra_sep"], default=None,
+                                       "backward_4k", "intra_sep", "output_gate"], default=None,
                     help="run a small fixed case for profiler captures instead of the benchmark")
     args = ap.parse_args()
     if args.case:
