@@ -423,6 +423,7 @@ def run_ours(args, rank, ws, local):
     step_ms_marked = [ev[i][0].elapsed_time(ev[i][nk]) for i in range(args.steps)]
     kern_ms = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)] for j in range(nk)]
     ms = sum(step_ms) / len(step_ms)
+    step_spread = [min(step_ms), sorted(step_ms)[len(step_ms) // 2], max(step_ms)]
     ms_max = max_over_ranks(ms, ws)
     value = T * ws / (ms_max / 1e3)
     fl = prefill_flops(lengths, H, D, D)
@@ -865,6 +866,7 @@ def run_ours(args, rank, ws, local):
             "frac_hbm_algorithmic": by["total"] / (ms_head / 1e3) / 1e9 / hbm,
             "kernels_ms": dict(zip(names, kern_avg)),
             "ms_per_step_with_kernel_marks": sum(step_ms_marked) / len(step_ms_marked),
+            "step_ms_min_median_max": step_spread,
             "roofline": roof,
             "e2e": {"value": T_head * ws / (e2e_pipe_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_pipe_ms, "wall_ms_per_step": e2e_pipe_wall_ms,
