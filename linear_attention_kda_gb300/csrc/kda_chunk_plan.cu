@@ -19,7 +19,9 @@ namespace kda {
 __global__ void __launch_bounds__(1024)
 chunk_plan_kernel(const int32_t *__restrict__ cu, int64_t T, int N, int C,
                   int32_t *__restrict__ chunk_start, int64_t seg_len, int32_t *__restrict__ seg_start,
-                  int *err) {
+                  int32_t *__restrict__ unit_seg, int *__restrict__ unit_ctr, int *err) {
+    constexpr int MAX_SORT = 4096;  // segments ordered by length; more are taken in index order
+    __shared__ int s_cnt[MAX_SORT];
     __shared__ int s_bad;
     __shared__ int s_warp[32];
     __shared__ int s_carry;
@@ -113,6 +115,30 @@ chunk_plan_kernel(const int32_t *__restrict__ cu, int64_t T, int N, int C,
         __syncthreads();
     }
     if (tid == 0) seg_start[0] = 0;
+    if (!unit_seg) return;
+    // the output pass takes segments longest first (fewer short chains left for the tail), from a
+    // counter this kernel resets
+    __syncthreads();
+    if (tid == 0) *unit_ctr = 0;
+    const int S = seg_start[N];
+    if (S > MAX_SORT) {
+        for (int g = tid; g < S; g += blockDim.x) unit_seg[g] = g;
+        return;
+    }
+    for (int n = tid; n < N; n += blockDim.x) {
+        const int nc = chunk_start[n + 1] - chunk_start[n];
+        for (int g = seg_start[n]; g < seg_start[n + 1]; ++g) {
+            const int64_t left = (int64_t)nc - (int64_t)(g - seg_start[n]) * seg_len;
+            s_cnt[g] = (int)max((int64_t)0, min(seg_len, left));
+        }
+    }
+    __syncthreads();
+    for (int g = tid; g < S; g += blockDim.x) {  // rank by (chunks descending, index ascending)
+        const int c = s_cnt[g];
+        int r = 0;
+        for (int x = 0; x < S; ++x) r += (s_cnt[x] > c || (s_cnt[x] == c && x < g)) ? 1 : 0;
+        unit_seg[r] = g;
+    }
 }
 
 }  // namespace kda
@@ -303,6 +329,8 @@ bool kda_make_chunk_plan(int64_t T, int64_t N, int H, int dk, int dv, kda_dtype_
     if (p->team) end = p->off_consumed + sizeof(uint64_t) * (size_t)p->max_chunks * (size_t)H;
     p->off_ctr = align_up(end, 256);
     if (p->path == 1) end = p->off_ctr + sizeof(uint64_t) * KDA_CTR_STRIDE * KDA_CTR_MAX;
+    p->off_unit = align_up(end, 256);
+    if (p->path == 1) end = p->off_unit + sizeof(int32_t) * (size_t)p->max_segs;
     p->total_bytes = align_up(end, 256);
     return true;
 }
@@ -313,7 +341,9 @@ kda_status_t kda_launch_chunk_plan(const kda_chunk_args *a, const kda_chunk_plan
     if (!err) return KDA_ERR_CUDA;
     int32_t *chunk_start = (int32_t *)((char *)ws + p.off_chunk_start);
     int32_t *seg_start = p.path == 1 ? (int32_t *)((char *)ws + p.off_seg_start) : nullptr;
+    int32_t *unit_seg = p.path == 1 ? (int32_t *)((char *)ws + p.off_unit) : nullptr;
+    int *unit_ctr = p.path == 1 ? (int *)((char *)ws + p.off_ctr + sizeof(uint64_t) * KDA_CTR_STRIDE) : nullptr;
     kda::chunk_plan_kernel<<<1, 1024, 0, stream>>>(a->cu_seqlens, a->T, (int)a->N, p.C, chunk_start,
-                                                    p.seg_len, seg_start, err);
+                                                    p.seg_len, seg_start, unit_seg, unit_ctr, err);
     return kda_cuda_status(cudaGetLastError());
 }

@@ -1499,11 +1499,24 @@ chunk_inter_tc_kernel(const __grid_constant__ CUtensorMap omap, int64_t T, int N
                       int64_t seg_len, const float *__restrict__ seg_in, int H,
                       const unsigned char *__restrict__ packets, float scale, const float *initial_state,
                       float *final_state, bf16 *__restrict__ o, int *err, const __grid_constant__ CUtensorMap gmap,
-                      int epi, const float *epi_w, float epi_eps) {
+                      int epi, const float *epi_w, float epi_eps, const int32_t *__restrict__ unit_seg,
+                      int *unit_ctr) {
+    // persistent: each CTA takes (segment, head) units from the counter, segments longest first
+    // (unit u = segment unit_seg[u / H], head u % H), and keeps its right to allocate tensor memory
     extern __shared__ unsigned char smem_raw[];
-    chain_role(align1024(smem_raw), omap, T, N, cu, chunk_start, seg_start, seg_len, seg_in, H, packets, scale,
-               initial_state, final_state, o, err, (int)blockIdx.x, (int)blockIdx.y, nullptr, 0, nullptr, true,
-               epi ? &gmap : nullptr, epi_w, epi_eps);
+    __shared__ int s_u;
+    const int64_t n_units = (int64_t)seg_start[N] * H;
+    for (;;) {
+        if (threadIdx.x == 0) s_u = atomicAdd(unit_ctr, 1);
+        __syncthreads();
+        const int64_t u = s_u;
+        __syncthreads();  // read before thread 0 takes the next unit
+        if (u >= n_units) break;
+        chain_role(align1024(smem_raw), omap, T, N, cu, chunk_start, seg_start, seg_len, seg_in, H, packets, scale,
+                   initial_state, final_state, o, err, unit_seg[u / H], (int)(u % H), nullptr, 0, nullptr, false,
+                   epi ? &gmap : nullptr, epi_w, epi_eps);
+        if (*(volatile int *)err == KDA_ERR_DEVICE_TIMEOUT) break;  // a wait gave up: stop taking work
+    }
 }
 
 // =====================================================================================
@@ -2266,9 +2279,17 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
     }
     st = set_smem((const void *)tcp::chunk_inter_tc_kernel, tcp::CS_TOTAL);
     if (st != KDA_OK) return st;
-    tcp::chunk_inter_tc_kernel<<<dim3((unsigned)p.max_segs, (unsigned)p.H), tcp::NT3, tcp::CS_TOTAL, stream>>>(
-        omap, a->T, (int)a->N, a->cu_seqlens, chunk_start, seg_start, p.seg_len, seg_in, p.H, packets, a->scale,
-        a->initial_state, a->final_state, (bf16 *)a->o, err, gmap, epi, a->out_norm_weight, a->out_norm_eps);
+    {
+        // one persistent CTA per SM (at most one per unit); the planning kernel reset the unit counter
+        const int64_t units = p.max_segs * (int64_t)p.H;
+        const unsigned grid = (unsigned)(units < sms ? units : sms);
+        const int32_t *unit_seg = (const int32_t *)((char *)ws + p.off_unit);
+        int *unit_ctr = (int *)((char *)ws + p.off_ctr + sizeof(uint64_t) * KDA_CTR_STRIDE);
+        tcp::chunk_inter_tc_kernel<<<grid, tcp::NT3, tcp::CS_TOTAL, stream>>>(
+            omap, a->T, (int)a->N, a->cu_seqlens, chunk_start, seg_start, p.seg_len, seg_in, p.H, packets, a->scale,
+            a->initial_state, a->final_state, (bf16 *)a->o, err, gmap, epi, a->out_norm_weight, a->out_norm_eps,
+            unit_seg, unit_ctr);
+    }
     kda_profile_mark(mark, stream);
     return kda_cuda_status(cudaGetLastError());
 }

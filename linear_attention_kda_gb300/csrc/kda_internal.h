@@ -58,6 +58,7 @@ struct kda_chunk_plan {
     size_t off_flags;
     size_t off_consumed;     // team schedule: per (chunk slot, head), the epoch once its chain has started on it
     size_t off_ctr;          // tensor-core path: item counters of the producers (KDA_CTR_MAX, 128 bytes apart)
+    size_t off_unit;         // tensor-core path: int32 [max_segs] segments in the order the output pass takes them
     size_t total_bytes;
 };
 
