@@ -756,6 +756,37 @@ def run_ours(args, rank, ws, local):
                 epi_l = {"with_epilogue_ms_per_step": mse, "overhead": mse / msl - 1.0,
                          "kernels": kda.chunk_fwd_kernel_count(Tl, Nl, H, D, D, dl["q"].dtype, cul, out_gate=True)}
                 del gl, wl_
+            bwd_l = None
+            if not args.no_backward and Nl == 1:
+                # the backward of the whole sequence in a bounded workspace (32 GiB: segments of one
+                # sequence; the one-pass scratch would be ~209 GiB)
+                del wl
+                torch.cuda.empty_cache()
+                wl = None
+                ws_b = 32 << 30
+                full_b = kda.chunk_bwd_workspace_size(Tl, 1, H, D, D)
+                wsb = torch.empty((min(ws_b, full_b),), dtype=torch.uint8, device=dev)
+                gen = torch.Generator(device=dev).manual_seed(36)
+                dol = torch.randn(ol.shape, generator=gen, device=dev).to(ol.dtype)
+
+                def step_lb():
+                    return kda.chunk_bwd(dl["q"], dl["k"], dl["v"], dl["z"], dl["beta"], dl["dt_bias"], dl["A_log"],
+                                         dol, initial_state=dl["initial_state"], workspace=wsb)
+
+                gb_ = step_lb()
+                torch.cuda.synchronize()
+                assert kda.get_device_error() == 0
+                del gb_
+                la.record(stream)
+                gb_ = step_lb()
+                lb.record(stream)
+                lb.synchronize()
+                msb = la.elapsed_time(lb)
+                bwd_l = {"what": "kda_chunk_bwd of the whole sequence in a 32 GiB workspace (segments)",
+                         "ms_per_step": msb, "tokens_per_s": Tl / (msb / 1e3), "vs_forward": msb / msl,
+                         "workspace_bytes": int(wsb.numel()), "one_pass_workspace_bytes": int(full_b)}
+                del gb_, wsb, dol
+                torch.cuda.empty_cache()
             fll = prefill_flops(Ls, H, D, D)
             byl = prefill_bytes(Tl, Nl, H, D, D, 2, dl["initial_state"] is not None, True)
             tfl = fll["total"] / (msl / 1e3) / 1e12
@@ -765,7 +796,8 @@ def run_ours(args, rank, ws, local):
                 "tflops": tfl, "tflops_dense_tile": fll["dense_tile"] / (msl / 1e3) / 1e12,
                 "frac_bf16_peak": tfl / tc, "hbm_gbs_algorithmic": byl["total"] / (msl / 1e3) / 1e9,
                 "frac_hbm": byl["total"] / (msl / 1e3) / 1e9 / hbm,
-                "schedule": schedule_name(sch_l), "kernels": sch_l["kernels"], "epilogue": epi_l}
+                "schedule": schedule_name(sch_l), "kernels": sch_l["kernels"], "epilogue": epi_l,
+                "backward": bwd_l}
             del dl, fsl, ol, wl
             torch.cuda.empty_cache()
 

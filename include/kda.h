@@ -48,7 +48,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
 
-#define KDA_ABI_VERSION 4
+#define KDA_ABI_VERSION 5
 
 typedef enum {
     KDA_OK = 0,
@@ -256,13 +256,27 @@ typedef struct {
     int32_t gate_kind;              /* kda_gate_kind_t */
 } kda_chunk_bwd_args;
 
-/* Bytes of device scratch kda_chunk_bwd needs (0 on invalid sizes): per (chunk, head) about
- * 0.42 MiB at d = 128 (fp32 records, L, the entering state, the leaving Lambda and the
- * chunk-local sums), independent of dtype and gate kind. */
+/* Bytes of device scratch kda_chunk_bwd needs for one pass over all chunks (0 on invalid sizes):
+ * per (chunk, head) about 0.42 MiB at d = 128 (fp32 records, L, the entering state, the leaving
+ * Lambda and the chunk-local sums), independent of dtype and gate kind. */
 size_t kda_chunk_bwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
                                     int32_t chunk_size);
 
-/* Gradients must not alias the forward inputs or one another.  workspace as kda_chunk_fwd. */
+/* The smallest workspace kda_chunk_bwd accepts (0 on invalid sizes).  For one sequence (N = 1)
+ * longer than 16 chunks this is below kda_chunk_bwd_workspace_size: given less than the one-pass
+ * size, kda_chunk_bwd processes the sequence in segments of the largest power-of-two number of
+ * chunks (at least 16) whose scratch fits.  A forward sweep first stores the state entering each
+ * segment; the segments then run last to first, the gradient of each one's initial state being
+ * the gradient of the previous one's final state (the same recurrence as across chunks,
+ * Section 5.1.2, Eq. 17), and the dt_bias and A_log gradients are the sums of the segments'
+ * sums.  The results equal the one-pass results up to the rounding of those sums.  Extra
+ * workspace: the entering states (64 KiB per head and segment at d = 128).  Other batches
+ * (N > 1) need kda_chunk_bwd_workspace_size. */
+size_t kda_chunk_bwd_workspace_size_min(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
+                                        int32_t chunk_size);
+
+/* Gradients must not alias the forward inputs or one another.  workspace: at least
+ * kda_chunk_bwd_workspace_size_min bytes, 256-byte aligned (KDA_ERR_WORKSPACE otherwise). */
 kda_status_t kda_chunk_bwd(const kda_chunk_bwd_args *args, void *workspace, size_t workspace_bytes,
                            struct CUstream_st *stream);
 

@@ -264,6 +264,13 @@ size_t kda_chunk_bwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk,
     return kda_chunk_bwd_layout_bytes(T, N, H, dk, dv);
 }
 
+size_t kda_chunk_bwd_workspace_size_min(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
+                                        int32_t chunk_size) {
+    if (T < 0 || N < 1 || H < 1 || dk != dv || (dk != 64 && dk != 128)) return 0;
+    if (chunk_size != 0 && chunk_size != 64) return 0;
+    return kda_chunk_bwd_min_layout_bytes(T, N, H, dk, dv);
+}
+
 kda_status_t kda_chunk_bwd(const kda_chunk_bwd_args *a, void *workspace, size_t workspace_bytes,
                            struct CUstream_st *stream) {
     if (!a) return KDA_ERR_INVALID_ARG;
@@ -300,7 +307,7 @@ kda_status_t kda_chunk_bwd(const kda_chunk_bwd_args *a, void *workspace, size_t 
         (a->grad_dt_bias && !aligned_to(a->grad_dt_bias, 4)) || (a->grad_A_log && !aligned_to(a->grad_A_log, 4)) ||
         (a->cu_seqlens && !aligned_to(a->cu_seqlens, 4)))
         return KDA_ERR_MISALIGNED;
-    const size_t need = kda_chunk_bwd_layout_bytes(a->T, a->N, a->H, a->dk, a->dv);
+    const size_t need = kda_chunk_bwd_min_layout_bytes(a->T, a->N, a->H, a->dk, a->dv);
     if (need == 0) return KDA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
     if (!aligned_to(workspace, 256)) return KDA_ERR_MISALIGNED;

@@ -26,6 +26,7 @@
 //                            cumulative sum; dz, d beta and per-chunk sums for d dt_bias, d A_log;
 //   bwd_gate_param_kernel    sums the per-chunk gate-parameter gradients per head.
 #include "kda_common.cuh"
+#include <algorithm>
 #include "kda_internal.h"
 #include "kda_f32_records.cuh"
 
@@ -552,13 +553,16 @@ chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int
     }
 }
 
-// d dt_bias[h][c] = sum over chunk slots; d A_log[h] likewise
-__global__ void bwd_gate_param_kernel(const float *__restrict__ gate_part, int64_t slots, int H, int dk,
+// d dt_bias[h][c] = sum over the chunk slots in use (chunk_start[N] of them; the launch's bound `slots`
+// may be larger, and slots past the last chunk hold no partials); d A_log[h] likewise
+__global__ void bwd_gate_param_kernel(const float *__restrict__ gate_part, int64_t slots,
+                                      const int32_t *__restrict__ chunk_start, int N, int H, int dk,
                                       float *__restrict__ grad_bias, float *__restrict__ grad_alog) {
     const int h = blockIdx.x;
+    const int64_t used = chunk_start ? min(slots, (int64_t)chunk_start[N]) : slots;
     for (int c = threadIdx.x; c <= dk; c += blockDim.x) {
         float acc = 0.f;
-        for (int64_t s = 0; s < slots; ++s) acc += gate_part[((size_t)s * H + h) * (size_t)(dk + 1) + c];
+        for (int64_t s = 0; s < used; ++s) acc += gate_part[((size_t)s * H + h) * (size_t)(dk + 1) + c];
         if (c < dk) {
             if (grad_bias) grad_bias[h * dk + c] = acc;
         } else if (grad_alog) {
@@ -635,7 +639,7 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
     if (st != KDA_OK) return st;
     if (Ly.slots == 0 || a->T == 0) {  // no tokens: the parameter gradients are zero
         if (a->grad_dt_bias || a->grad_A_log) {
-            bw::bwd_gate_param_kernel<<<(unsigned)H, 128, 0, stream>>>(gpart, 0, H, dk, a->grad_dt_bias,
+            bw::bwd_gate_param_kernel<<<(unsigned)H, 128, 0, stream>>>(gpart, 0, nullptr, 0, H, dk, a->grad_dt_bias,
                                                                        a->grad_A_log);
             st = kda_cuda_status(cudaGetLastError());
         }
@@ -674,11 +678,108 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
     if (st != KDA_OK) return st;
     // 5. gate parameters
     if (a->grad_dt_bias || a->grad_A_log) {
-        bw::bwd_gate_param_kernel<<<(unsigned)H, 128, 0, stream>>>(gpart, Ly.slots, H, dk, a->grad_dt_bias, a->grad_A_log);
+        bw::bwd_gate_param_kernel<<<(unsigned)H, 128, 0, stream>>>(gpart, Ly.slots, chunk_start, (int)a->N, H, dk,
+                                                                   a->grad_dt_bias, a->grad_A_log);
         st = kda_cuda_status(cudaGetLastError());
     }
     kda_profile_mark(7, stream);
     return st;
+}
+
+// One long sequence in segments of S chunks, when the whole pass's scratch does not fit: a forward sweep
+// stores the state entering each segment; then the segments run last to first, each a full backward pass
+// over its tokens from its entering state, the gradient of its final state being the gradient of the next
+// segment's initial state (the state's adjoint crosses the boundary exactly as it crosses a chunk boundary
+// inside one pass), and the dt_bias and A_log gradients summed over the segments.  Workspace: one
+// segment's scratch, the entering states [K][H][dk][dv], two adjoint buffers [H][dk][dv] and the gate
+// parameters' per-segment sums.
+struct SegLayout {
+    BwdLayout seg;
+    int64_t S, K;  // chunks per segment, segments
+    size_t off_states, off_carry, off_gpart, total;
+};
+
+bool seg_layout(int64_t T, int H, int dk, int dv, int64_t S, SegLayout *L) {
+    const int64_t seg_tokens = S * 64;
+    if (!bwd_layout(std::min(T, seg_tokens), 1, H, dk, dv, 64, &L->seg)) return false;
+    L->S = S;
+    L->K = (T + seg_tokens - 1) / seg_tokens;
+    const size_t st = (size_t)H * dk * dv * sizeof(float);
+    L->off_states = align256(L->seg.total);
+    L->off_carry = align256(L->off_states + (size_t)L->K * st);
+    L->off_gpart = align256(L->off_carry + 2 * st);
+    L->total = align256(L->off_gpart + (size_t)H * (dk + 1) * sizeof(float));
+    return true;
+}
+
+__global__ void bwd_accumulate_kernel(float *dst, const float *src, int n, int first) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        dst[i] = first ? src[i] : dst[i] + src[i];
+}
+
+template <typename Tio>
+kda_status_t launch_bwd_segmented(const kda_chunk_bwd_args *a, const SegLayout &Ls, void *ws, cudaStream_t stream) {
+    const int H = a->H, dk = a->dk, dv = a->dv;
+    const size_t es = sizeof(Tio), stz = (size_t)H * dk * dv;
+    char *base = (char *)ws;
+    float *states = (float *)(base + Ls.off_states), *carry = (float *)(base + Ls.off_carry);
+    float *gp_bias = (float *)(base + Ls.off_gpart), *gp_alog = gp_bias + (size_t)H * dk;
+    const int64_t seg_tokens = Ls.S * 64;
+    auto seg_len = [&](int64_t k) { return std::min(seg_tokens, a->T - k * seg_tokens); };
+    auto off = [&](const void *p, int64_t k, int width) -> const char * {
+        return p ? (const char *)p + (size_t)(k * seg_tokens) * H * width * es : nullptr;
+    };
+    // forward sweep: the state entering segments 1 .. K - 1 (fp32 path, as the backward recomputes)
+    float *Lbuf = (float *)(base + Ls.seg.off_L), *ckpt = (float *)(base + Ls.seg.off_ckpt);
+    for (int64_t k = 0; k + 1 < Ls.K; ++k) {
+        kda_chunk_args f{};
+        f.T = seg_len(k); f.N = 1; f.H = H; f.dk = dk; f.dv = dv; f.dtype = a->dtype;
+        f.q = off(a->q, k, dk); f.k = off(a->k, k, dk); f.z = off(a->z, k, dk); f.v = off(a->v, k, dv);
+        f.beta = off(a->beta, k, 1);
+        f.dt_bias = a->dt_bias; f.A_log = a->A_log; f.g_min = a->g_min; f.scale = a->scale;
+        f.initial_state = k == 0 ? a->initial_state : states + (size_t)k * stz;
+        f.final_state = states + (size_t)(k + 1) * stz;
+        f.chunk_size = 64; f.gate_kind = a->gate_kind;
+        const kda_status_t st = kda_launch_chunk_simt_recompute(&f, Ls.seg.p, ws, Lbuf, ckpt, stream);
+        if (st != KDA_OK) return st;
+    }
+    // the segments last to first
+    for (int64_t k = Ls.K - 1; k >= 0; --k) {
+        kda_chunk_bwd_args b = *a;
+        b.T = seg_len(k); b.N = 1; b.cu_seqlens = nullptr;
+        b.q = off(a->q, k, dk); b.k = off(a->k, k, dk); b.z = off(a->z, k, dk); b.v = off(a->v, k, dv);
+        b.beta = off(a->beta, k, 1); b.grad_o = off(a->grad_o, k, dv);
+        b.grad_q = (void *)off(a->grad_q, k, dk); b.grad_k = (void *)off(a->grad_k, k, dk);
+        b.grad_z = (void *)off(a->grad_z, k, dk); b.grad_v = (void *)off(a->grad_v, k, dv);
+        b.grad_beta = (void *)off(a->grad_beta, k, 1);
+        b.initial_state = k == 0 ? a->initial_state : states + (size_t)k * stz;
+        b.grad_final_state = k == Ls.K - 1 ? a->grad_final_state : carry + (size_t)((k + 1) & 1) * stz;
+        b.grad_initial_state = k == 0 ? a->grad_initial_state : carry + (size_t)(k & 1) * stz;
+        b.grad_dt_bias = a->grad_dt_bias ? gp_bias : nullptr;
+        b.grad_A_log = a->grad_A_log ? gp_alog : nullptr;
+        kda_status_t st = launch_bwd<Tio>(&b, Ls.seg, ws, stream);
+        if (st != KDA_OK) return st;
+        const int first = k == Ls.K - 1 ? 1 : 0;
+        if (a->grad_dt_bias)
+            bwd_accumulate_kernel<<<(H * dk + 255) / 256, 256, 0, stream>>>(a->grad_dt_bias, gp_bias, H * dk, first);
+        if (a->grad_A_log) bwd_accumulate_kernel<<<1, 256, 0, stream>>>(a->grad_A_log, gp_alog, H, first);
+        st = kda_cuda_status(cudaGetLastError());
+        if (st != KDA_OK) return st;
+    }
+    return KDA_OK;
+}
+
+// Chunks per segment of the segmented pass for this workspace (0: it does not fit, or the pass
+// cannot be segmented): the largest power of two, at least 16, whose layout fits.
+int64_t seg_chunks_for(int64_t T, int64_t N, int H, int dk, int dv, size_t ws_bytes) {
+    if (N != 1 || T <= 16 * 64) return 0;
+    const int64_t chunks = (T + 63) / 64;
+    for (int64_t S = (int64_t)1 << 40; S >= 16; S >>= 1) {
+        if (S >= chunks) continue;
+        SegLayout L;
+        if (seg_layout(T, H, dk, dv, S, &L) && L.total <= ws_bytes) return S;
+    }
+    return 0;
 }
 
 }  // namespace
@@ -688,9 +789,23 @@ size_t kda_chunk_bwd_layout_bytes(int64_t T, int64_t N, int H, int dk, int dv) {
     return bwd_layout(T, N, H, dk, dv, 64, &L) ? L.total : 0;
 }
 
+size_t kda_chunk_bwd_min_layout_bytes(int64_t T, int64_t N, int H, int dk, int dv) {
+    const size_t full = kda_chunk_bwd_layout_bytes(T, N, H, dk, dv);
+    if (N != 1 || T <= 16 * 64) return full;
+    SegLayout L;
+    return seg_layout(T, H, dk, dv, 16, &L) ? std::min(full, L.total) : full;
+}
+
 kda_status_t kda_launch_chunk_bwd(const kda_chunk_bwd_args *a, void *ws, size_t ws_bytes, cudaStream_t stream) {
     BwdLayout L;
     if (!bwd_layout(a->T, a->N, a->H, a->dk, a->dv, 64, &L)) return KDA_ERR_INVALID_ARG;
-    if (!ws || ws_bytes < L.total) return KDA_ERR_WORKSPACE;
-    return a->dtype == KDA_BF16 ? launch_bwd<bf16>(a, L, ws, stream) : launch_bwd<float>(a, L, ws, stream);
+    if (!ws) return KDA_ERR_WORKSPACE;
+    if (ws_bytes >= L.total)
+        return a->dtype == KDA_BF16 ? launch_bwd<bf16>(a, L, ws, stream) : launch_bwd<float>(a, L, ws, stream);
+    const int64_t S = seg_chunks_for(a->T, a->N, a->H, a->dk, a->dv, ws_bytes);
+    if (S == 0) return KDA_ERR_WORKSPACE;
+    SegLayout Ls;
+    if (!seg_layout(a->T, a->H, a->dk, a->dv, S, &Ls)) return KDA_ERR_INVALID_ARG;
+    return a->dtype == KDA_BF16 ? launch_bwd_segmented<bf16>(a, Ls, ws, stream)
+                                : launch_bwd_segmented<float>(a, Ls, ws, stream);
 }

@@ -84,4 +84,7 @@ size_t kda_tc_packet_stride();  // bytes per (chunk, head) packet of the tensor-
 // Backward pass of the chunked prefill (kda_chunk_bwd.cu): scratch bytes for these sizes (0 if
 // invalid) and the launcher (arguments validated by kda_api.cu).
 size_t kda_chunk_bwd_layout_bytes(int64_t T, int64_t N, int H, int dk, int dv);
+// The smallest workspace kda_launch_chunk_bwd accepts: a single sequence longer than 16 chunks runs in
+// segments when the whole pass does not fit (segments of 16 chunks at this size).
+size_t kda_chunk_bwd_min_layout_bytes(int64_t T, int64_t N, int H, int dk, int dv);
 kda_status_t kda_launch_chunk_bwd(const kda_chunk_bwd_args *a, void *ws, size_t ws_bytes, cudaStream_t stream);

@@ -32,7 +32,8 @@ EXPORTED = ["kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_re
             "kda_set_profile_events", "kda_chunk_fwd_kernel_count", "kda_chunk_fwd_static_ws",
             "kda_last_cuda_error", "kda_chunk_fwd_schedule", "kda_output_gate", "kda_recurrent_replay",
             "kda_chunk_fwd_workspace_size_gate", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size",
-            "kda_selftest_bounded_wait", "kda_set_debug_checks", "kda_set_chunk_schedule"]
+            "kda_selftest_bounded_wait", "kda_set_debug_checks", "kda_set_chunk_schedule",
+            "kda_chunk_bwd_workspace_size_min"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 _vp = ctypes.c_void_p
@@ -114,6 +115,8 @@ def load_library(path: Optional[str] = None):
         L.kda_chunk_fwd_workspace_size_gate.restype = ctypes.c_size_t
         L.kda_chunk_bwd_workspace_size.argtypes = [_i64, _i64, _i32, _i32, _i32, _i32]
         L.kda_chunk_bwd_workspace_size.restype = ctypes.c_size_t
+        L.kda_chunk_bwd_workspace_size_min.argtypes = [_i64, _i64, _i32, _i32, _i32, _i32]
+        L.kda_chunk_bwd_workspace_size_min.restype = ctypes.c_size_t
         L.kda_chunk_bwd.argtypes = [ctypes.POINTER(ChunkBwdArgs), _vp, ctypes.c_size_t, _vp]
         L.kda_chunk_bwd.restype = ctypes.c_int
         L.kda_selftest_bounded_wait.argtypes = [_vp, _vp]
@@ -269,8 +272,8 @@ def chunk_bwd(q, k, v, z, beta, dt_bias, A_log, grad_o, *, g_min: float = -5.0, 
         g["A_log"] = torch.zeros((H,), dtype=torch.float32, device=q.device)
     if state_grad:
         g["initial_state"] = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
-    need = int(L.kda_chunk_bwd_workspace_size(T, N, H, dk, dv, 64))
-    if workspace is None or workspace.numel() < need:
+    if workspace is None:  # a given workspace is used as it is (a smaller one segments a long sequence)
+        need = int(L.kda_chunk_bwd_workspace_size(T, N, H, dk, dv, 64))
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
     a = ChunkBwdArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=_dtype_code(q), q=_ptr(q), k=_ptr(k), z=_ptr(z), v=_ptr(v),
                      beta=_ptr(beta), dt_bias=_ptr(dt_bias), A_log=_ptr(A_log), g_min=g_min, scale=scale,
@@ -281,6 +284,14 @@ def chunk_bwd(q, k, v, z, beta, dt_bias, A_log, grad_o, *, g_min: float = -5.0, 
                      grad_initial_state=_ptr(g.get("initial_state")), chunk_size=64, gate_kind=_gate_kind(gate))
     _check(L.kda_chunk_bwd(ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(q)), "kda_chunk_bwd")
     return g
+
+
+def chunk_bwd_workspace_size(T, N, H, dk=128, dv=128, minimum: bool = False) -> int:
+    """kda_chunk_bwd_workspace_size (one pass), or with minimum=True kda_chunk_bwd_workspace_size_min
+    (the smallest workspace kda_chunk_bwd accepts: segments of one long sequence)."""
+    L = load_library()
+    f = L.kda_chunk_bwd_workspace_size_min if minimum else L.kda_chunk_bwd_workspace_size
+    return int(f(T, N, H, dk, dv, 64))
 
 
 def output_gate(o, g, norm_weight=None, eps: float = 1e-6, *, out: Optional[torch.Tensor] = None):

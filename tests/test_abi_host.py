@@ -46,7 +46,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.kda_abi_version() == 4
+    assert lib.kda_abi_version() == 5
     for code, name in kda._STATUS.items():
         s = lib.kda_status_string(code).decode()
         assert s and s != "unknown status", name
@@ -327,6 +327,22 @@ def test_chunk_bwd_workspace(lib):
     assert lib.kda_chunk_bwd(ctypes.byref(_bwd()), FAKE, need - 1, None) == 5
     assert lib.kda_chunk_bwd(ctypes.byref(_bwd()), None, need, None) == 5
     assert lib.kda_chunk_bwd(ctypes.byref(_bwd()), FAKE + 16, need, None) == 4
+
+
+def test_chunk_bwd_minimum_workspace(lib):
+    """One long sequence may run in segments: the minimum is the scratch of a 16-chunk segment plus the
+    segments' entering states, far below the one-pass size at T = 1M (where the one pass would not fit a
+    GPU); batches of several sequences and short sequences need the one-pass size."""
+    lib.kda_chunk_bwd_workspace_size_min.argtypes = [ctypes.c_int64, ctypes.c_int64] + [ctypes.c_int32] * 4
+    lib.kda_chunk_bwd_workspace_size_min.restype = ctypes.c_size_t
+    full = lib.kda_chunk_bwd_workspace_size(1 << 20, 1, 32, 128, 128, 64)
+    small = lib.kda_chunk_bwd_workspace_size_min(1 << 20, 1, 32, 128, 128, 64)
+    assert full > 200 * (1 << 30) and 0 < small < 4 * (1 << 30)
+    assert small >= 1024 * 32 * 128 * 128 * 4  # the entering states of 1024 segments x 32 heads
+    for T, N in ((1 << 20, 2), (1024, 1), (128, 1)):
+        assert lib.kda_chunk_bwd_workspace_size_min(T, N, 32, 128, 128, 64) == \
+            lib.kda_chunk_bwd_workspace_size(T, N, 32, 128, 128, 64)
+    assert lib.kda_chunk_bwd_workspace_size_min(4096, 1, 2, 96, 96, 64) == 0
 
 
 def test_empty_batch_plan(lib):

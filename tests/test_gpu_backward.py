@@ -187,3 +187,62 @@ def test_chunk_bwd_empty_batch():
         assert torch.equal(gS0, dST) if with_dst else torch.count_nonzero(gS0.nan_to_num(1.0)).item() == 0
         assert torch.count_nonzero(gdb.nan_to_num(1.0)).item() == 0
         assert torch.count_nonzero(gda.nan_to_num(1.0)).item() == 0
+
+
+@pytest.mark.parametrize("gate", ["lower_bound", "softplus"])
+def test_chunk_bwd_segmented_long_sequence(gate):
+    """One sequence given less workspace than the one-pass size runs in segments (here the minimum:
+    segments of 16 chunks, so T = 2 x 1024 + 300 tokens makes three, the last ragged): every gradient
+    against the exact fp64 gradients (1e-4, fp32, with S0 and dS_T), and equal to the one-pass result
+    but for the rounding of the per-segment sums of the dt_bias and A_log gradients."""
+    d = _inputs(2, 64, "f32", [2 * 1024 + 300], 91)
+    d["gate"] = gate
+    T, H, D = d["q"].shape
+    full = kda.chunk_bwd_workspace_size(T, 1, H, D, D)
+    small = kda.chunk_bwd_workspace_size(T, 1, H, D, D, minimum=True)
+    assert 0 < small < full
+    dev = {n: d[n].cuda() for n in ("q", "k", "v", "z", "beta", "dt_bias", "A_log", "do")}
+    args = [dev[n] for n in ("q", "k", "v", "z", "beta", "dt_bias", "A_log", "do")]
+    kw = dict(initial_state=d["S0"].cuda(), grad_final_state=d["dST"].cuda(), gate=gate)
+    # workspaces full of NaN: no gradient may depend on scratch the call did not write
+    seg = kda.chunk_bwd(*args, workspace=torch.full((small,), 0xFF, dtype=torch.uint8, device="cuda"), **kw)
+    one = kda.chunk_bwd(*args, workspace=torch.full((full,), 0xFF, dtype=torch.uint8, device="cuda"), **kw)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    seg = {n: x.float().cpu().numpy() for n, x in seg.items()}
+    one = {n: x.float().cpu().numpy() for n, x in one.items()}
+    _compare(d, seg, _ref(d, gate), TOL_F32)
+    for n in ("q", "k", "v", "z", "beta", "initial_state"):
+        assert rel_err(seg[n], one[n]) <= 1e-6, n
+    for n in ("dt_bias", "A_log"):
+        assert np.allclose(seg[n], one[n], rtol=1e-4, atol=1e-5 * float(np.abs(one[n]).max())), n
+
+
+def test_chunk_bwd_workspace_too_small_or_batched():
+    """Below the minimum the call is refused; a batch of several sequences needs the one-pass size."""
+    d = _inputs(2, 64, "f32", [1500, 900], 93)
+    T, H, D = d["q"].shape
+    full = kda.chunk_bwd_workspace_size(T, 2, H, D, D)
+    assert kda.chunk_bwd_workspace_size(T, 2, H, D, D, minimum=True) == full
+    args = [d[n].cuda() for n in ("q", "k", "v", "z", "beta", "dt_bias", "A_log", "do")]
+    with pytest.raises(kda.KDAError, match="KDA_ERR_WORKSPACE"):
+        kda.chunk_bwd(*args, cu_seqlens=d["cu_seqlens"].cuda(),
+                      workspace=torch.empty((full - 256,), dtype=torch.uint8, device="cuda"))
+    small = kda.chunk_bwd_workspace_size(2400, 1, H, D, D, minimum=True)
+    a1 = [x[:2400] if x.dim() >= 2 and x.shape[0] == T else x for x in args]
+    with pytest.raises(kda.KDAError, match="KDA_ERR_WORKSPACE"):
+        kda.chunk_bwd(*a1, workspace=torch.empty((small - 256,), dtype=torch.uint8, device="cuda"))
+
+
+def test_chunk_bwd_varlen_ignores_stale_workspace():
+    """A varlen batch's chunk-slot bound exceeds its chunks; the slots past the last chunk must not
+    reach the dt_bias and A_log sums: the pass on a workspace full of NaN equals the exact gradients."""
+    d = _inputs(2, 64, "f32", [1, 63, 64, 65, 130, 0, 7], 95)
+    T, H, D = d["q"].shape
+    ws = torch.full((kda.chunk_bwd_workspace_size(T, 7, H, D, D),), 0xFF, dtype=torch.uint8, device="cuda")
+    g = kda.chunk_bwd(*(d[n].cuda() for n in ("q", "k", "v", "z", "beta", "dt_bias", "A_log", "do")),
+                      cu_seqlens=d["cu_seqlens"].cuda(), initial_state=d["S0"].cuda(),
+                      grad_final_state=d["dST"].cuda(), workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    _compare(d, {n: x.float().cpu().numpy() for n, x in g.items()}, _ref(d, "lower_bound"), TOL_F32)
