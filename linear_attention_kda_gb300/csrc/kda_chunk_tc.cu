@@ -403,7 +403,8 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
     const int team_window = team ? team->window * team->K : 0;  // in team items
     int64_t *pk = (int64_t *)(sm + J_PAIR);  // dynamic: the first item of the CTA's pair j in pk[j & 3]
     bool ctr_live = false;                   // thread 0: the counter holds this launch's tag
-    auto grab = [&]() -> int64_t {           // thread 0: the first item of the CTA's next pair
+    auto grab = [&]() -> uint64_t {          // thread 0: the counter before this CTA's next pair (low 32 bits:
+                                             // its first item)
         const uint64_t tag = (uint64_t)(uint32_t)epoch << 32, hi = 0xffffffff00000000ull;
         unsigned long long *c = reinterpret_cast<unsigned long long *>(ctr);
         if (!ctr_live) {
@@ -412,22 +413,22 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
                 const uint64_t prev = atomicCAS(c, cur, tag | 2ull);
                 if (prev == cur) {
                     ctr_live = true;
-                    return 0;
+                    return tag;
                 }
                 cur = prev;
             }
             if ((cur & hi) != tag) {
                 set_error(err, KDA_ERR_DEVICE_TIMEOUT);
-                return n_all;
+                return tag | (uint64_t)n_all;
             }
             ctr_live = true;
         }
-        return (int64_t)(atomicAdd(c, 2ull) & 0xffffffffull);
+        return atomicAdd(c, 2ull);
     };
     if (dyn) {
         if (tid == 0) {
-            pk[0] = grab();
-            pk[1] = grab();
+            pk[0] = (int64_t)(grab() & 0xffffffffull);
+            pk[1] = (int64_t)(grab() & 0xffffffffull);
         }
         __syncthreads();
         if (pk[0] >= n_all) return;
@@ -499,10 +500,11 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
     // 32-bit words holding its beta values (bf16; the gate pass widens them in place), its bias row and
     // A_log.  Nothing waits on these loads until the item starts; the slot (j & 1) was last used by item j - 2.
     // The slot's plain stores are ordered before their readers by the group barriers in between.
+    int n_hint = 0;  // warp 0: the sequence of the group's last item
     auto fill_slot = [&](int j) {
         const int s = j & 1;
-        const bool take = dyn && g == 0 && lane == 0 && j >= 1;  // group 0 takes pair j + 1
-        int64_t nxt = 0;
+        const bool take = dyn && g == 0 && lane == 0 && j >= 1;  // group 0 takes pair j + 1 (the
+        uint64_t nxt = 0;                                        // atomic's result is used at the end)
         if (take) nxt = grab();
         const int64_t w = w_of(k_of(j, g));
         int n = 0, len = 0, h;
@@ -514,7 +516,26 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
             slot = w / H;
             h = (int)(w % H);
         }
-        locate(chunk_start, cu, T, N, slot, n, t0, len);
+        // the sequence holding the slot: a group's slots mostly grow, so search forward from the last
+        // one's sequence for a few steps, else bisect
+        n = n_hint;
+        if (slot < chunk_start[n]) n = 0;
+        for (int step = 0; step < 4 && chunk_start[n + 1] <= slot; ++step) ++n;
+        if (chunk_start[n + 1] <= slot) {
+            int lo = n, hi = N;  // largest lo with chunk_start[lo] <= slot
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (chunk_start[mid] <= slot) lo = mid; else hi = mid;
+            }
+            n = lo;
+        }
+        n_hint = n;
+        {
+            const int64_t sb = cu ? (int64_t)cu[n] : (T / N) * n;
+            const int64_t se = cu ? (int64_t)cu[n + 1] : sb + T / N;
+            t0 = sb + (slot - chunk_start[n]) * (int64_t)C;
+            len = (int)min((int64_t)C, se - t0);
+        }
         uint32_t *bw = (uint32_t *)(R + GR_BETA) + 64 * s;
         float *bia = (float *)(R + GR_BIAS) + 128 * s;
 #pragma unroll
@@ -538,7 +559,7 @@ __device__ __forceinline__ void intra_role(unsigned char *sm, const TileMaps &tm
             else *al = 0.f;
         }
         cp_async_arrive_noinc(ld_qzk);
-        if (take) pk[(j + 1) & 3] = nxt;
+        if (take) pk[(j + 1) & 3] = (int64_t)(nxt & 0xffffffffull);
     };
     // Item j's q, z, k (and v) tiles by TMA (thread 0, which filled the slot)
     auto issue_tma = [&](int j, bool with_v) {
