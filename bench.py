@@ -272,6 +272,16 @@ def barrier(ws):
         dist.barrier()
 
 
+def sum_over_ranks(x, ws):
+    """Sum of a per-rank host value (token counts of the ranks' shards)."""
+    if ws <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
 def max_over_ranks(x, ws):
     if ws <= 1:
         return x
@@ -308,7 +318,8 @@ def workload_config(w, lengths, ws):
             "d_k": w.d, "d_v": w.d, "chunk": 64, "io_dtype": w.dtype, "state_dtype": "f32",
             "initial_state": w.s0_std > 0, "final_state": True,
             "l2": "flushed (512 MiB write) before every timed step; inputs exceed L2",
-            "parallelism": f"replicas x{ws}"}
+            "parallelism": f"sequence shards x{ws}" if ws > 1 else "one GPU",
+            "global_sequences": len(lengths) * ws, "tokens_per_rank": int(sum(lengths))}
 
 
 def oracle_sample_units(lengths, H, n_units=ORACLE_SAMPLE_UNITS, seed=5):
@@ -322,7 +333,7 @@ def oracle_sample_units(lengths, H, n_units=ORACLE_SAMPLE_UNITS, seed=5):
 def run_reference(args, rank, ws):
     if rank != 0:
         return
-    d = syn.make_prefill(WORKLOAD, seed=2, device="cpu")
+    d = syn.make_prefill_shard(WORKLOAD, 2, 0, 1, device="cpu")
     lengths = d["lengths"]
     H = WORKLOAD.H
     units, th = oracle_sample_units(lengths, H)
@@ -369,7 +380,9 @@ def run_ours(args, rank, ws, local):
     flush = torch.empty((512 << 20,), dtype=torch.uint8, device=dev)
 
     # ---------------- headline: the varlen batch, inputs resident in HBM
-    d = syn.make_prefill(WORKLOAD, seed=2 + rank, device=dev)
+    # rank r's shard of a global batch of ws x 32 sequences (each sequence drawn from its own seeds, so
+    # it is the same whatever the number of ranks): weak scaling, no data-path collective
+    d = syn.make_prefill_shard(WORKLOAD, 2, rank, ws, device=dev)
     lengths = d["lengths"]
     T, N, H, D = sum(lengths), len(lengths), WORKLOAD.H, WORKLOAD.d
     cu_host = d["cu_seqlens"].cpu()
@@ -425,7 +438,8 @@ def run_ours(args, rank, ws, local):
     ms = sum(step_ms) / len(step_ms)
     step_spread = [min(step_ms), sorted(step_ms)[len(step_ms) // 2], max(step_ms)]
     ms_max = max_over_ranks(ms, ws)
-    value = T * ws / (ms_max / 1e3)
+    T_all = sum_over_ranks(float(T), ws)  # tokens of every rank's shard
+    value = T_all / (ms_max / 1e3)
     fl = prefill_flops(lengths, H, D, D)
     by = prefill_bytes(T, N, H, D, D, 2, s0 is not None, True)
     tflops = fl["total"] / (ms / 1e3) / 1e12
@@ -879,7 +893,7 @@ def run_ours(args, rank, ws, local):
     # ---------------- CPU oracle baseline (rank 0, N = 1 only): a seeded sample of the headline workload
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
-        dc = syn.make_prefill(WORKLOAD, seed=2, device="cpu")
+        dc = syn.make_prefill_shard(WORKLOAD, 2, 0, 1, device="cpu")
         units, th = oracle_sample_units(dc["lengths"], H)
         secs, used, total, reps = cpu_oracle_run(dc, units=units)
         cpu = {"value": th / H / secs, "unit": "tokens/s", "cores": used, "kind": "oracle",
@@ -900,12 +914,12 @@ def run_ours(args, rank, ws, local):
             "ms_per_step_with_kernel_marks": sum(step_ms_marked) / len(step_ms_marked),
             "step_ms_min_median_max": step_spread,
             "roofline": roof,
-            "e2e": {"value": T_head * ws / (e2e_pipe_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": T_all / (e2e_pipe_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_pipe_ms, "wall_ms_per_step": e2e_pipe_wall_ms,
                     "how": "double-buffered: step s+1's inputs (q, k, v, z, beta, initial states) copied from "
                            "pinned host memory while step s computes, step s's o and final states read back "
                            "meanwhile; every step's inputs and results cross the host link",
-                    "serial": {"value": T_head * ws / (e2e_ms / 1e3), "ms_per_step": e2e_ms,
+                    "serial": {"value": T_all / (e2e_ms / 1e3), "ms_per_step": e2e_ms,
                                "how": "copy in, compute, copy out, one step at a time, L2 flushed"}},
             "gpu_launches": nk * args.steps,
             "clocks": clocks,

@@ -166,6 +166,33 @@ def make_prefill(w: Workload, seed: int, device="cpu", *, T_override: Optional[i
                 g_min=-5.0, scale=1.0, chunk=w.chunk)
 
 
+def make_prefill_shard(w: Workload, seed: int, rank: int, world: int, device="cpu"):
+    """Rank `rank`'s share of a global varlen batch of world * w.n_seq sequences: the sequences
+    [rank * n, (rank + 1) * n), n = w.n_seq, as one batch (the inputs of make_prefill, plus `seq_ids`).
+    Every sequence is drawn from its own generators (seeded by the global seed and its index: its
+    length, tokens and initial state), so a sequence is the same whatever the number of ranks; the
+    head parameters are the global seed's."""
+    n = w.n_seq
+    ids = list(range(rank * n, (rank + 1) * n))
+    lengths, parts, states = [], [], []
+    for i in ids:
+        si = seed * 1000003 + 7 * i + 1
+        if w.seq_len is not None:
+            L = int(w.seq_len)
+        else:
+            L = int(torch.randint(w.len_lo, w.len_hi + 1, (1,), generator=_gen(si + 7919, "cpu")))
+        lengths.append(L)
+        parts.append(make_tokens(L, w.H, w.d, w.d, w.dtype, si, z_std=w.z_std, device=device))
+        if w.s0_std > 0:
+            states.append(make_state(1, w.H, w.d, w.d, w.s0_std, si, device))
+    q, k, v, beta, z = (torch.cat([p_[j] for p_ in parts], 0) for j in range(5))
+    b, a = make_head_params(w.H, w.d, seed, b_range=w.b_range, alog_std=w.alog_std)
+    s0 = torch.cat(states, 0) if states else None
+    return dict(q=q, k=k, v=v, beta=beta, z=z, dt_bias=b.to(device), A_log=a.to(device),
+                initial_state=s0, lengths=lengths, cu_seqlens=cu_seqlens_of(lengths).to(device),
+                g_min=-5.0, scale=1.0, chunk=w.chunk, seq_ids=ids)
+
+
 def make_decode(w: Workload, seed: int, device="cpu", *, n_seq: Optional[int] = None,
                 steps: Optional[int] = None):
     """Decode workload: per-step tokens [steps, N, H, d] and the state [N, H, d, d]."""
