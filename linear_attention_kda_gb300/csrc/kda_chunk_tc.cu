@@ -125,31 +125,15 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
     return __syncthreads_and(ok ? 1 : 0) != 0;
 }
 
-__device__ __forceinline__ bool locate(const int32_t *chunk_start, const int32_t *cu, int64_t T, int N,
-                                       int64_t slot, int &n, int64_t &t0, int &len) {
-    if (slot >= chunk_start[N]) return false;
-    int lo = 0, hi = N;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (chunk_start[mid] <= slot) lo = mid; else hi = mid;
-    }
-    n = lo;
-    const int64_t s = cu ? (int64_t)cu[n] : (T / N) * n;
-    const int64_t e = cu ? (int64_t)cu[n + 1] : s + T / N;
-    t0 = s + (slot - chunk_start[n]) * (int64_t)C;
-    len = (int)min((int64_t)C, e - t0);
-    return true;
-}
-
 // =====================================================================================
-// Persistent intra-chunk kernel: one CTA per SM walks the (chunk, head) work items
-// w = slot * H + h.  Its sixteen warps form two groups of eight; group g takes the CTA's items g,
-// g + 2, g + 4, ... and owns a full set of buffers (a ~100 KB region of shared memory and 256
-// tensor-memory columns), so that the two groups run out of phase: while one inverts (I + L) (a
-// latency-bound step), the other runs the gate and element pass of its next item (MUFU and
-// shared-memory bound).  The group's first thread moves its data: the q, z, k, v tiles
-// (128-byte-swizzled TMA boxes of 64 tokens x 64 channels) and the item's beta, bias and e^{A_log}
-// in, the packet out by bulk copies.
+// Persistent intra-chunk kernel: one CTA per SM works through the (chunk, head) items
+// w = slot * H + h, taking them two at a time from a launch-wide counter.  Its sixteen warps form two
+// groups of eight; group g takes the second (g = 1) or first (g = 0) item of each pair and owns a full
+// set of buffers (a ~100 KB region of shared memory and 256 tensor-memory columns), so that the two
+// groups run out of phase: while one inverts (I + L) (a latency-bound step), the other runs the gate
+// and element pass of its next item (MUFU and shared-memory bound).  The group's warp 0 moves its
+// data: the q, z, k, v tiles (128-byte-swizzled TMA boxes of 64 tokens x 64 channels) and the item's
+// beta, bias and A_log in (cp.async), the packet out by bulk copies.
 //
 // Tiles stay token-major ([token][channel], the TMA layout) from load to packet: tcgen05 reads a
 // token-major tile as a K-major operand when the contraction runs over channels and, through an
