@@ -166,12 +166,13 @@ size_t kda_chunk_fwd_workspace_size_gate(int64_t T, int64_t N, int32_t H, int32_
 /* workspace: device memory of at least kda_chunk_fwd_workspace_size() bytes,
  * 256-byte aligned, owned by the caller; its contents need no initialisation
  * and are garbage afterwards.  Calls that share a workspace must not overlap.
- * Stream capture: the fused schedule (kda_chunk_fwd_schedule out[0] = 1)
- * publishes its per-chunk work through flags tagged with a per-call counter
- * kept on the host, which a captured graph would freeze; a call made while
- * `stream` is being captured therefore runs the flag-free separate kernels
- * (same results, more launches), and its graph may be replayed with new
- * contents in the same buffers. */
+ * Stream capture: the one-launch and chain-team schedules publish their
+ * per-chunk work through flags, and the producers take their items from a
+ * counter, both tagged with a per-call number kept on the host, which a captured
+ * graph would freeze; a call made while `stream` is being captured therefore
+ * runs the flag-free separate kernels with a fixed split of the items (same
+ * results, more launches), and its graph may be replayed with new contents in
+ * the same buffers. */
 kda_status_t kda_chunk_fwd(const kda_chunk_args *args, void *workspace, size_t workspace_bytes,
                            struct CUstream_st *stream);
 
