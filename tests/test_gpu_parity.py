@@ -765,3 +765,44 @@ def test_output_epilogue_on_long_chains(schedule):
     finally:
         kda.set_chunk_schedule("auto")
     compare_prefill(d, o, fs, _epilogue_ref(d, oracle_prefill(d), g, w), TOL_BF16)
+
+
+def test_shared_workspace_across_schedules_and_repeated_calls():
+    """One workspace serves interleaved calls of different problems and schedules (separate kernels
+    with the producers' item counter, the one-launch schedule with flags and counter, the split state
+    pass with the output pass's unit counter), twelve times over: every call's result equals the
+    first call of the same problem bit for bit, and the first ones match the oracle.  Counters and
+    flags left in the workspace by one call (tagged with its own number, or reset by the planning
+    kernel) never leak into the next."""
+    w = syn.Workload("ws", H=4, d=128, dtype="bf16", seq_len=None, z_std=1.5, b_range=1.0, alog_std=0.25,
+                     s0_std=0.02)
+    rng = np.random.default_rng(97)
+    cases = []
+    for lengths, mode in (([int(x) for x in rng.integers(1, 700, size=12)], "separate"),
+                          ([2000, 900], "fused"),
+                          ([9000, 130], "auto")):
+        d = _varlen(w, lengths, seed=int(rng.integers(1 << 20)))
+        cases.append((d, mode))
+    size = 0
+    for d, mode in cases:
+        kda.set_chunk_schedule(mode)
+        try:
+            size = max(size, kda.chunk_fwd_workspace_size(sum(d["lengths"]), len(d["lengths"]), 4, 128, 128,
+                                                          torch.bfloat16, 64, d["cu_seqlens"]))
+        finally:
+            kda.set_chunk_schedule("auto")
+    ws = torch.empty((size,), dtype=torch.uint8, device="cuda")
+    first = {}
+    try:
+        for rep in range(12):
+            for i, (d, mode) in enumerate(cases):
+                kda.set_chunk_schedule(mode)
+                o, fs = run_prefill(d, workspace=ws)
+                if rep == 0:
+                    first[i] = (o, fs)
+                    compare_prefill(d, o, fs, oracle_prefill(d), TOL_BF16)
+                else:
+                    assert torch.equal(o, first[i][0]) and torch.equal(fs, first[i][1]), (rep, i, mode)
+    finally:
+        kda.set_chunk_schedule("auto")
+    assert kda.get_device_error() == 0
