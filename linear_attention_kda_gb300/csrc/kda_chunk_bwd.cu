@@ -21,9 +21,9 @@
 //                            over the value channels (dQ^, dW, dK~, dA, the X_U part of dL, d gamma,
 //                            the X_U part of d beta), accumulated in registers and written once;
 //                            It also solves dX_W = T^T dW and adds dL's X_W part at the end;
-//   chunk_bwd_key_kernel     one CTA per (chunk, head): reads those sums, then
-//                            per (row, channel) the pairwise A and L terms, dq, dk, dG; the reverse
-//                            cumulative sum; dz, d beta and per-chunk sums for d dt_bias, d A_log;
+//   chunk_bwd_key_kernel     one CTA per (chunk, head): reads those sums, then per (row, channel)
+//                            the pairwise A and L terms, dq, dk, dG; the reverse cumulative sum;
+//                            dz, d beta and per-chunk sums for d dt_bias, d A_log;
 //   bwd_gate_param_kernel    sums the per-chunk gate-parameter gradients per head.
 #include "kda_common.cuh"
 #include <algorithm>
@@ -414,142 +414,176 @@ chunk_bwd_value_kernel_t(int64_t T, int N, const int32_t *__restrict__ cu, const
 }
 
 // ------------------------------------------------------------------ key side, per (chunk, head)
-// Thread t owns channel c = t % dk of rows r = t / dk, t / dk + NT / dk, ...
-template <typename Tio>
-__global__ void __launch_bounds__(NT)
+// Thread t owns channel c = t % DK of the RPT = C DK / NT consecutive rows (t / DK) RPT + [0, RPT):
+// their in-chunk log-decay (a prefix sum within the rows, then the earlier row groups' totals), their
+// pairwise A and L terms, dq, dk and dG (kept in registers), and afterwards the gate's derivative of
+// the same rows, the reverse cumulative sum of dG reaching them through the later row groups'
+// totals.  q and k sit in shared memory in the I/O type (exact), so that with bf16 I/O two CTAs
+// share an SM.
+template <typename Tio, int DK>
+__global__ void __launch_bounds__(NT, 2)
 chunk_bwd_key_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
-                     int H, int dk, int dv, int C, const char *__restrict__ records, size_t rec_bytes,
+                     int H, int dv, const char *__restrict__ records, size_t rec_bytes,
                      const float *__restrict__ part, const Tio *__restrict__ q,
                      const Tio *__restrict__ k, const Tio *__restrict__ z, const Tio *__restrict__ beta,
                      const float *__restrict__ bias, const float *__restrict__ A_log, float g_min, int kind,
                      Tio *__restrict__ grad_q, Tio *__restrict__ grad_k, Tio *__restrict__ grad_z,
                      Tio *__restrict__ grad_beta, float *__restrict__ gate_part) {
+    constexpr int C = 64, dk = DK;
+    constexpr int NR = NT / DK;   // row groups
+    constexpr int RPT = C / NR;   // rows per thread
+    constexpr int NWC = DK / 32;  // warps per row group (a warp's lanes share their rows)
     extern __shared__ float sm[];
     const int64_t slot = blockIdx.x;
     const int h = blockIdx.y;
     int n, len;
     int64_t t0;
     if (!locate_chunk(chunk_start, cu, T, N, C, slot, n, t0, len)) return;
-    const int tid = threadIdx.x;
-    const int PK = dk + 1, PC = C + 1;
-    const int NR = NT / dk;           // row groups
-    float *qs = sm;                   // [C][PK]
-    float *ks = qs + C * PK;          // [C][PK]
-    float *Gs = ks + C * PK;          // [C][PK]  in-chunk cumulative log-decay
-    float *dX = Gs + C * PK;          // [C][PK]  dX_W, then the per-element d beta terms
-    float *dG = dX + C * PK;          // [C][PK]
-    float *dLs = dG + C * PK;         // [C][PC]
-    float *dAs = dLs + C * PC;        // [C][PC]
-    float *bet = dAs + C * PC;        // [C]
-    float *red = bet + C;             // [NR][dk] per-row-group channel sums
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int c = tid % DK, rg = tid / DK, r0 = rg * RPT;
+    float *Gs = sm;                  // [C][dk]  in-chunk cumulative log-decay (base 2 after the prefix pass)
+    float *dAs = Gs + C * dk;        // [C][C]
+    float *dLs = dAs + C * C;        // [C][C]
+    float *bet = dLs + C * C;        // [C]
+    float *red = bet + C;            // [2][NR][dk] per-row-group channel sums
+    float *dbp = red + 2 * NR * dk;  // [C][NWC] the warps' shares of d beta
+    Tio *qs = reinterpret_cast<Tio *>(dbp + C * NWC);  // [C][dk]
+    Tio *ks = qs + C * dk;                             // [C][dk]
 
     const Part P{C, dk};
     const float *pp = part + ((size_t)slot * H + h) * (size_t)P.size();
+    tile_async(dAs, C, pp + P.dA(), C, C, C, tid, NT);
+    tile_async(dLs, C, pp + P.dLu(), C, C, C, tid, NT);  // the whole dL (strictly lower)
     const float eA = A_log ? expf(A_log[h]) : 1.f;
+    const float bc = bias ? bias[h * dk + c] : 0.f;
+    float gsum = 0.f;
 #pragma unroll 4
-    for (int e = tid; e < C * dk; e += NT) {
-        const int r = e / dk, c = e % dk;
+    for (int m = 0; m < RPT; ++m) {
+        const int r = r0 + m;
         const bool ok = r < len;
         const int64_t idx = ((t0 + r) * H + h) * (int64_t)dk + c;
-        qs[r * PK + c] = ok ? ld(q + idx) : 0.f;
-        ks[r * PK + c] = ok ? ld(k + idx) : 0.f;
-        Gs[r * PK + c] = ok ? gate_log(kind, ld(z + idx), bias ? bias[h * dk + c] : 0.f, eA, g_min) : 0.f;
-        dX[r * PK + c] = pp[P.dW() + e];  // dX_W = T^T dW (solved by the value side)
+        st(qs + r * dk + c, ok ? ld(q + idx) : 0.f);
+        st(ks + r * dk + c, ok ? ld(k + idx) : 0.f);
+        gsum += ok ? gate_log(kind, ld(z + idx), bc, eA, g_min) : 0.f;
+        Gs[r * dk + c] = gsum;
     }
-#pragma unroll 4
-    for (int e = tid; e < C * C; e += NT) {
-        const int r = e / C, i = e % C;
-        dAs[r * PC + i] = pp[P.dA() + e];
-        dLs[r * PC + i] = pp[P.dLu() + e];  // the whole dL (strictly lower)
-    }
+    red[rg * dk + c] = gsum;
     for (int r = tid; r < C; r += NT) bet[r] = r < len ? ld(beta + (t0 + r) * H + h) : 0.f;
+    cp_async_wait_all();
     __syncthreads();
-    for (int c = tid; c < dk; c += NT) {  // cumulative log-decay within the chunk (Eq. 3), base 2
-        float acc = 0.f;
-        for (int r = 0; r < C; ++r) {
-            acc += Gs[r * PK + c];
-            Gs[r * PK + c] = acc * 1.4426950408889634f;
+    {  // cumulative log-decay within the chunk (Eq. 3), base 2
+        float off = 0.f;
+        for (int g = 0; g < rg; ++g) off += red[g * dk + c];
+#pragma unroll 4
+        for (int m = 0; m < RPT; ++m) {
+            const int r = r0 + m;
+            Gs[r * dk + c] = (Gs[r * dk + c] + off) * 1.4426950408889634f;
         }
     }
     __syncthreads();
     // per (row, channel): dq, dk, dG and the d beta terms
-    const int c = tid % dk, rg = tid / dk;
-    float xk_sum = 0.f;  // sum over this thread's rows of dK~ * K~ (flows to G_last)
-    for (int r = rg; r < len; r += NR) {
-        const float Gr = Gs[r * PK + c], Gl = Gs[(C - 1) * PK + c];
-        const float eG = exp2f(Gr), eL = exp2f(Gl - Gr);
-        const float qr = qs[r * PK + c], kr = ks[r * PK + c], br = bet[r];
-        const float dqh = pp[P.dQ() + r * dk + c], dkt = pp[P.dK() + r * dk + c];
-        const float dxw = dX[r * PK + c];
-        float ra = 0.f, rl = 0.f;  // sum_{i <= r} dA_ri k_ic E_ric,  sum_{i < r} dL_ri k_ic E_ric
-        for (int i = 0; i < r; ++i) {
-            const float kE = ks[i * PK + c] * exp2f(Gr - Gs[i * PK + c]);
-            ra += dAs[r * PC + i] * kE;
-            rl += dLs[r * PC + i] * kE;
+    const float Gl = Gs[(C - 1) * dk + c];
+    float dGr[RPT];
+    float xk_sum = 0.f, gtot = 0.f;  // sums over this thread's rows of dK~ * K~ (flows to G_last) and of dG
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) {
+        const int r = r0 + m;
+        float dg = 0.f, dbt = 0.f;
+        if (r < len) {
+            const float Gr = Gs[r * dk + c];
+            const float eG = exp2f(Gr), eL = exp2f(Gl - Gr);
+            const float qr = ld(qs + r * dk + c), kr = ld(ks + r * dk + c), br = bet[r];
+            const float dqh = pp[P.dQ() + r * dk + c], dkt = pp[P.dK() + r * dk + c];
+            const float dxw = pp[P.dW() + r * dk + c];  // dX_W = T^T dW (solved by the value side)
+            float ra = 0.f, rl = 0.f;  // sum_{i <= r} dA_ri k_ic E_ric,  sum_{i < r} dL_ri k_ic E_ric
+            for (int i = 0; i < r; ++i) {
+                const float kE = ld(ks + i * dk + c) * exp2f(Gr - Gs[i * dk + c]);
+                ra += dAs[r * C + i] * kE;
+                rl += dLs[r * C + i] * kE;
+            }
+            ra += dAs[r * C + r] * kr;
+            // sum_{r' >= r} dA_r'r q_r'c E,  sum_{r' > r} dL_r'r b_r' k_r'c E
+            float ca = dAs[r * C + r] * qr, cl = 0.f;
+            for (int i = r + 1; i < len; ++i) {
+                const float E = exp2f(Gs[i * dk + c] - Gr);
+                ca += dAs[i * C + r] * ld(qs + i * dk + c) * E;
+                cl += dLs[i * C + r] * bet[i] * ld(ks + i * dk + c) * E;
+            }
+            const float ktil = kr * eL;
+            const float dq = dqh * eG + ra;
+            const float dkk = br * dxw * eG + dkt * eL + ca + br * rl + cl;
+            dg = dxw * br * kr * eG + dqh * qr * eG - dkt * ktil + qr * ra - kr * ca + br * kr * rl - kr * cl;
+            dbt = kr * (eG * dxw + rl);  // this element's share of d beta_r
+            xk_sum += dkt * ktil;
+            const int64_t idx = ((t0 + r) * H + h) * (int64_t)dk + c;
+            st(grad_q + idx, dq);
+            st(grad_k + idx, dkk);
         }
-        ra += dAs[r * PC + r] * kr;
-        float ca = dAs[r * PC + r] * qr, cl = 0.f;  // sum_{r' >= r} dA_r'r q_r'c E, sum_{r' > r} dL_r'r b_r' k_r'c E
-        for (int i = r + 1; i < len; ++i) {
-            const float E = exp2f(Gs[i * PK + c] - Gr);
-            ca += dAs[i * PC + r] * qs[i * PK + c] * E;
-            cl += dLs[i * PC + r] * bet[i] * ks[i * PK + c] * E;
-        }
-        const float ktil = kr * eL;
-        const float dq = dqh * eG + ra;
-        const float dkk = br * dxw * eG + dkt * eL + ca + br * rl + cl;
-        dG[r * PK + c] = dxw * br * kr * eG + dqh * qr * eG - dkt * ktil + qr * ra - kr * ca + br * kr * rl - kr * cl;
-        dX[r * PK + c] = kr * (eG * dxw + rl);  // this element's share of d beta_r
-        xk_sum += dkt * ktil;
-        const int64_t idx = ((t0 + r) * H + h) * (int64_t)dk + c;
-        st(grad_q + idx, dq);
-        st(grad_k + idx, dkk);
+        dGr[m] = dg;
+        gtot += dg;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dbt += __shfl_xor_sync(0xffffffffu, dbt, off);
+        if (lane == 0) dbp[r * NWC + (c >> 5)] = dbt;
     }
     red[rg * dk + c] = xk_sum;
+    red[(NR + rg) * dk + c] = gtot;
     __syncthreads();
-    // per channel: G_last collects d gamma * gamma and the K~ terms; dg = reverse cumulative sum of dG;
-    // then the gate's derivative
-    float *gp = gate_part + ((size_t)slot * H + h) * (size_t)(dk + 1);
-    for (int cc = tid; cc < dk; cc += NT) {
+    // G_last collects d gamma * gamma and the K~ terms of every row; dg of row r = that plus the sum of
+    // dG over the rows r' >= r; then the gate's derivative
+    float run;
+    {
         const F32Record rec = f32_record(records, rec_bytes, slot, H, h, C, dk, dv);
-        float run = pp[P.dgam() + cc] * rec.gam[cc];
-        for (int g = 0; g < NR; ++g) run += red[g * dk + cc];
-        const float b = bias ? bias[h * dk + cc] : 0.f;
-        float db = 0.f, da = 0.f;
-        for (int r = len - 1; r >= 0; --r) {
-            run += dG[r * PK + cc];
-            const int64_t idx = ((t0 + r) * H + h) * (int64_t)dk + cc;
+        run = pp[P.dgam() + c] * rec.gam[c];
+        for (int g = 0; g < NR; ++g) run += red[g * dk + c];
+        for (int g = rg + 1; g < NR; ++g) run += red[(NR + g) * dk + c];
+    }
+    float db = 0.f, da = 0.f;
+#pragma unroll
+    for (int m = RPT - 1; m >= 0; --m) {
+        const int r = r0 + m;
+        run += dGr[m];
+        if (r < len) {
+            const int64_t idx = ((t0 + r) * H + h) * (int64_t)dk + c;
             const float zz = ld(z + idx);
             float dz, dA;
             if (kind == KDA_GATE_SOFTPLUS) {
-                const float x = zz + b;
+                const float x = zz + bc;
                 const float sg = 1.f / (1.f + expf(-x));
-                const float g = gate_log(kind, zz, b, eA, g_min);
+                const float g = gate_log(kind, zz, bc, eA, g_min);
                 dz = run * (-eA * sg);
                 dA = run * g;
             } else {
-                const float x = eA * (zz + b);
+                const float x = eA * (zz + bc);
                 const float sg = 1.f / (1.f + expf(-x));
                 dz = run * g_min * sg * (1.f - sg) * eA;
-                dA = dz * (zz + b);
+                dA = dz * (zz + bc);
             }
             st(grad_z + idx, dz);
             db += dz;
             da += dA;
         }
-        gp[cc] = db;
-        red[cc] = da;  // row group 0's slot: read below after the barrier
     }
+    __syncthreads();  // every thread has read red
+    red[rg * dk + c] = db;
+    red[(NR + rg) * dk + c] = da;
     __syncthreads();
-    if (tid == 0) {
-        float da = 0.f;
-        for (int cc = 0; cc < dk; ++cc) da += red[cc];
-        gp[dk] = da;
+    float *gp = gate_part + ((size_t)slot * H + h) * (size_t)(dk + 1);
+    if (tid < dk) {
+        float s = 0.f;
+        for (int g = 0; g < NR; ++g) s += red[g * dk + tid];
+        gp[tid] = s;
+    } else if (tid < dk + 32) {
+        float s = 0.f;
+        for (int e = lane; e < NR * dk; e += 32) s += red[NR * dk + e];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) gp[dk] = s;
     }
     for (int r = tid; r < len; r += NT) {  // d beta: X_W and L terms per channel, plus the X_U part
-        float db = 0.f;
-        for (int cc = 0; cc < dk; ++cc) db += dX[r * PK + cc];
-        db += pp[P.dbu() + r];
-        st(grad_beta + (t0 + r) * H + h, db);
+        float s = pp[P.dbu() + r];
+#pragma unroll
+        for (int w = 0; w < NWC; ++w) s += dbp[r * NWC + w];
+        st(grad_beta + (t0 + r) * H + h, s);
     }
 }
 
@@ -619,7 +653,6 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
     const int32_t *chunk_start = (const int32_t *)(base + Ly.p.off_chunk_start);
     const char *records = base + Ly.p.off_records;
     const size_t rb = Ly.p.record_bytes;
-    const int PK = dk + 1, PC = C + 1;
     // 2. Lambda over the chunks in reverse; d initial_state
     // Ws, Qs, Kt [C][dk + 4]; As [C][C + 4]; dOs, dVt [C][TILE + 4]; Lm [dk][TILE + 4]; gam [dk]
     const size_t smem_rev = sizeof(float) * ((size_t)3 * C * (dk + 4) + (size_t)C * (C + 4) +
@@ -666,13 +699,21 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
     kda_profile_mark(5, stream);
     st = kda_cuda_status(cudaGetLastError());
     if (st != KDA_OK) return st;
-    // 4. key side per (chunk, head)
-    const size_t smem_key = sizeof(float) * (5 * (size_t)C * PK + 2 * (size_t)C * PC + C + (size_t)bw::NT);
-    cudaFuncSetAttribute(bw::chunk_bwd_key_kernel<Tio>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_key);
-    bw::chunk_bwd_key_kernel<Tio><<<dim3((unsigned)Ly.slots, (unsigned)H), bw::NT, smem_key, stream>>>(
-        a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dk, dv, C, records, rb, part, (const Tio *)a->q,
-        (const Tio *)a->k, (const Tio *)a->z, (const Tio *)a->beta, a->dt_bias, a->A_log, a->g_min, a->gate_kind,
-        (Tio *)a->grad_q, (Tio *)a->grad_k, (Tio *)a->grad_z, (Tio *)a->grad_beta, gpart);
+    // 4. key side per (chunk, head): Gs [C][dk], dA and dL [C][C], bet [C], red [2][NT / dk][dk],
+    // dbp [C][dk / 32] fp32; q and k [C][dk] in the I/O type
+    const size_t smem_key = sizeof(float) * ((size_t)C * dk + 2 * (size_t)C * C + C + 2 * (size_t)bw::NT +
+                                             (size_t)C * (dk / 32)) + 2 * sizeof(Tio) * (size_t)C * dk;
+    {
+        auto key = [&](auto kern) {
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_key);
+            kern<<<dim3((unsigned)Ly.slots, (unsigned)H), bw::NT, smem_key, stream>>>(
+                a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dv, records, rb, part, (const Tio *)a->q,
+                (const Tio *)a->k, (const Tio *)a->z, (const Tio *)a->beta, a->dt_bias, a->A_log, a->g_min,
+                a->gate_kind, (Tio *)a->grad_q, (Tio *)a->grad_k, (Tio *)a->grad_z, (Tio *)a->grad_beta, gpart);
+        };
+        if (dk == 128) key(bw::chunk_bwd_key_kernel<Tio, 128>);
+        else key(bw::chunk_bwd_key_kernel<Tio, 64>);
+    }
     kda_profile_mark(6, stream);
     st = kda_cuda_status(cudaGetLastError());
     if (st != KDA_OK) return st;
