@@ -29,6 +29,7 @@
 #include <algorithm>
 #include "kda_internal.h"
 #include "kda_f32_records.cuh"
+#include "tc_util.cuh"
 
 namespace kda {
 namespace bw {
@@ -413,6 +414,430 @@ chunk_bwd_value_kernel_t(int64_t T, int N, const int32_t *__restrict__ cu, const
     if (tid < C) pp[P.dbu() + tid] = abu;
 }
 
+// ------------------------------------------------------------------ value side on the tensor cores
+// bf16 I/O with d_k = d_v = 128: one 256-thread CTA per (chunk, head); the value-channel contractions
+// are tcgen05 products (bf16 operand images in shared memory, fp32 accumulators in tensor memory),
+// each computed transposed so that its 128 rows are channels (one TMEM lane each) and its 64
+// columns the chunk's tokens:
+//   first:  V~^T = U^T - S^T W^T,  dV~^T = Lambda^T K~^T + dO^T (scale A),  dQ^^T = S dO^T
+//   second: dW^T = -S dV~^T,  dK~^T = Lambda V~^T,  [V~; U] dO^T,  [V~; U] dX_U^T
+//   third:  [K~; W] dX_W^T accumulated onto the last one
+// The stacked products give dA^T (the rows of V~) and the X_U and X_W parts of dL^T (the rows of U
+// and W); their other halves are not used.  A thread that owns a channel (a TMEM lane) holds one
+// column of dV~ or dW in registers, so both solves with T^T = (I + L^T)^{-1} are back substitutions
+// in registers, and it writes the solved column as one 128-byte row of an MN-major operand image.
+// S and Lambda are stored once: an image with rows c and K-blocks of 64 value channels is also the
+// MN-major image of S^T (rows k = c holding 64 consecutive value channels).
+namespace vt {
+constexpr uint32_t SIMG = 0;          // S: rows c (128) x 128 value channels, K-major, blocks of 16 KB
+constexpr uint32_t LIMG = 32768;      // Lambda, the same
+constexpr uint32_t KWIMG = 65536;     // rows 0..63 K~, rows 64..127 W (x 128 key channels), K-major
+constexpr uint32_t DOIMG = 98304;     // dO: rows r (64) x 128 value channels, K-major, blocks of 8 KB
+constexpr uint32_t AIMG = 114688;     // scale A: rows i (64) x 64 tokens r
+constexpr uint32_t VUIMG = 122880;    // MN-major over tokens: group 0 V~, group 1 U, rows j (128), 16 KB each
+constexpr uint32_t DVIMG = 155648;    // dV~: rows j (128) x 64 tokens
+constexpr uint32_t DXUIMG = 172032;   // dX_U: rows j x 64 tokens
+constexpr uint32_t DXWIMG = 188416;   // dX_W: rows c x 64 tokens
+constexpr uint32_t LF = 204800;       // L, fp32 [64][64], strictly lower
+constexpr uint32_t BET = LF + 16384;  // beta [64]
+constexpr uint32_t RED = BET + 256;   // [4][64] the channel warps' shares of d beta (X_U part)
+constexpr uint32_t DGAM = RED + 1024; // d gamma [128]
+constexpr uint32_t BAR = DGAM + 512;  // 3 mbarriers
+constexpr uint32_t TSLOT = BAR + 32;  // TMEM base
+constexpr uint32_t TOTAL = TSLOT + 16 + 1024;  // + alignment of the base to 1024 bytes
+}  // namespace vt
+
+__device__ __forceinline__ unsigned char *vt_align1024(unsigned char *p) {
+    const uint32_t s = tc::smem_u32(p);
+    return p + ((1024u - (s & 1023u)) & 1023u);
+}
+__device__ __forceinline__ uint4 vt_pack8(const float *f) {
+    return make_uint4(tc::pack_bf16(f[0], f[1]), tc::pack_bf16(f[2], f[3]), tc::pack_bf16(f[4], f[5]),
+                      tc::pack_bf16(f[6], f[7]));
+}
+__device__ __forceinline__ void vt_load8(const float *p, float *f) {
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void vt_sync() {
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+}
+// Waits on an mbarrier from every thread (bounded); a CTA-uniform "all ok".
+__device__ __forceinline__ bool vt_wait(uint64_t *bar, uint32_t parity) {
+    const bool ok = tc::mbar_wait(bar, parity);
+    const bool all = __syncthreads_and(ok ? 1 : 0) != 0;
+    tc::fence_after_sync();
+    return all;
+}
+// x <- (I + L^T)^{-1} x for L strictly lower ([64][64] fp32, shared memory), x the 64 fp32 columns
+// [tcol, tcol + 64) of this thread's TMEM lane, in place: x_r -= sum_{i > r} L_ir x_i, by blocks of 16 rows
+// from the last up (a block's own triangle in registers, then its updates of the earlier blocks).  The
+// block loops run at run time, so the code stays small; the warp executes it together.
+__device__ __forceinline__ void vt_solve_ut_tmem(uint32_t tcol, const float *L) {
+    for (int b = 3; b >= 0; --b) {
+        float xb[16];
+        tc::tmem_ld16(tcol + 16 * b, xb);
+        const float *Lb = L + 16 * b * 64 + 16 * b;  // L[16 b + ii][16 b + rr]
+#pragma unroll
+        for (int ii = 15; ii >= 1; --ii) {
+            const float xi = xb[ii];
+#pragma unroll
+            for (int rr = 0; rr < ii; rr += 4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(Lb + ii * 64 + rr);
+                xb[rr] -= l4.x * xi;
+                if (rr + 1 < ii) xb[rr + 1] -= l4.y * xi;
+                if (rr + 2 < ii) xb[rr + 2] -= l4.z * xi;
+                if (rr + 3 < ii) xb[rr + 3] -= l4.w * xi;
+            }
+        }
+        tc::tmem_st16(tcol + 16 * b, xb);
+#pragma unroll 1
+        for (int b2 = 0; b2 < b; ++b2) {
+            float xc[16];
+            tc::tmem_ld16(tcol + 16 * b2, xc);
+            const float *Lc = L + 16 * b * 64 + 16 * b2;  // L[16 b + ii][16 b2 + rr]
+#pragma unroll
+            for (int ii = 0; ii < 16; ++ii) {
+#pragma unroll
+                for (int rr = 0; rr < 16; rr += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(Lc + ii * 64 + rr);
+                    xc[rr] -= l4.x * xb[ii];
+                    xc[rr + 1] -= l4.y * xb[ii];
+                    xc[rr + 2] -= l4.z * xb[ii];
+                    xc[rr + 3] -= l4.w * xb[ii];
+                }
+            }
+            tc::tmem_st16(tcol + 16 * b2, xc);
+        }
+        tc::tmem_st_wait();
+    }
+}
+// Sums x[0..63] over the warp's lanes by halving exchanges; returns b such that x[0], x[1] then hold
+// the sums of entries b, b + 1 (each lane a different pair).
+__device__ __forceinline__ int vt_reduce_scatter64(float *x, int lane) {
+    int b = 0;
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+        const int o = 16 >> step, half = 32 >> step;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < half; ++k) {
+            const float send = up ? x[k] : x[k + half];
+            const float keep = up ? x[k + half] : x[k];
+            x[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+        if (up) b += half;
+    }
+    return b;
+}
+
+// Asks L2 for what item (slot, h) reads: S, Lambda, L, the record's W, U, K~ and A, and its rows of
+// dO and v (warp 0; the item is in the sequence table).
+__device__ __forceinline__ void vt_prefetch_item(int64_t slot, int h, int64_t t0, int len, int H,
+                                                 const char *records, size_t rec_bytes, const float *Lbuf,
+                                                 const float *ckpt, const float *lam_end, const bf16 *v,
+                                                 const bf16 *d_o, int lane) {
+    constexpr int C = 64, D = 128;
+    const size_t mbase = ((size_t)slot * H + h) * (size_t)D * D;
+    const F32Record rec = f32_record(records, rec_bytes, slot, H, h, C, D, D);
+    if (lane == 0) {
+        prefetch_l2(ckpt + mbase, D * D * 4);
+        prefetch_l2(lam_end + mbase, D * D * 4);
+        prefetch_l2(rec.W, 2 * C * D * 4);         // W, U
+        prefetch_l2(rec.K, (C * D + C * C) * 4);   // K~, A
+        prefetch_l2(Lbuf + ((size_t)slot * H + h) * (size_t)C * C, C * C * 4);
+    }
+    for (int r = lane; r < len; r += 32) {
+        const int64_t idx = ((t0 + r) * H + h) * (int64_t)D;
+        prefetch_l2(d_o + idx, D * 2);
+        prefetch_l2(v + idx, D * 2);
+    }
+}
+
+// Persistent: CTA b takes the items (slot, head) w = b, b + gridDim.x, ... (slot = w / H), and asks L2
+// for its next item while it works on the current one.
+__global__ void __launch_bounds__(256, 1)
+chunk_bwd_value_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
+                          int H, const char *__restrict__ records, size_t rec_bytes,
+                          const float *__restrict__ Lbuf, const float *__restrict__ ckpt,
+                          const float *__restrict__ lam_end, float scale, const bf16 *__restrict__ v,
+                          const bf16 *__restrict__ beta, const bf16 *__restrict__ d_o, bf16 *__restrict__ grad_v,
+                          float *__restrict__ part, int *err) {
+    using namespace tc;
+    constexpr int C = 64, D = 128;
+    extern __shared__ unsigned char vt_raw[];
+    unsigned char *sm = vt_align1024(vt_raw);
+    const int64_t items = (int64_t)chunk_start[N] * H;
+    if ((int64_t)blockIdx.x >= items) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lq = (warp & 3) * 32, row = lq + lane;  // TMEM lane quarter of this warp; this thread's lane
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + vt::BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + vt::TSLOT);
+    float *Lf = reinterpret_cast<float *>(sm + vt::LF), *bet = reinterpret_cast<float *>(sm + vt::BET);
+    float *red = reinterpret_cast<float *>(sm + vt::RED), *dgam = reinterpret_cast<float *>(sm + vt::DGAM);
+    const Part P{C, D};
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init(&bar[2], 1);
+    }
+    if (warp == 0) tmem_alloc(tslot, 256);
+    fence_proxy_async();
+    vt_sync();
+    const uint32_t tb = *tslot;
+    const uint32_t s0 = smem_u32(sm);
+    auto where = [&](int64_t w, int64_t &slot, int &h, int64_t &t0, int &len) {
+        slot = w / H;
+        h = (int)(w - slot * H);
+        int n;
+        locate_chunk(chunk_start, cu, T, N, C, slot, n, t0, len);
+    };
+    bool ok = true;
+    uint32_t ph = 0;
+    {
+        int64_t slot, t0;
+        int h, len;
+        where(blockIdx.x, slot, h, t0, len);
+        if (warp == 0) vt_prefetch_item(slot, h, t0, len, H, records, rec_bytes, Lbuf, ckpt, lam_end, v, d_o, lane);
+    }
+    for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ph ^= 1u) {
+        int64_t slot, t0;
+        int h, len;
+        where(w, slot, h, t0, len);
+        if (warp == 0 && w + gridDim.x < items) {
+            int64_t s2, t2;
+            int h2, l2;
+            where(w + gridDim.x, s2, h2, t2, l2);
+            vt_prefetch_item(s2, h2, t2, l2, H, records, rec_bytes, Lbuf, ckpt, lam_end, v, d_o, lane);
+        }
+        float *pp = part + ((size_t)slot * H + h) * (size_t)P.size();
+        const F32Record rec = f32_record(records, rec_bytes, slot, H, h, C, D, D);
+        const size_t mbase = ((size_t)slot * H + h) * (size_t)D * D;
+
+        // operand images; each loop's loads are issued before its stores
+        tile_async(Lf, C, Lbuf + ((size_t)slot * H + h) * (size_t)C * C, C, C, C, tid, 256);
+#pragma unroll 1
+        for (int bq = 0; bq < 2; ++bq) {  // S and Lambda; d gamma = row sums of S o Lambda
+            float sv[4][8], lv[4][8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int e = tid + 256 * (4 * bq + q), c = e >> 4, jc = e & 15;
+                vt_load8(ckpt + mbase + (size_t)c * D + 8 * jc, sv[q]);
+                vt_load8(lam_end + mbase + (size_t)c * D + 8 * jc, lv[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int e = tid + 256 * (4 * bq + q), c = e >> 4, jc = e & 15;
+                const uint32_t off = img_chunk_off(128, c, jc);
+                *reinterpret_cast<uint4 *>(sm + vt::SIMG + off) = vt_pack8(sv[q]);
+                *reinterpret_cast<uint4 *>(sm + vt::LIMG + off) = vt_pack8(lv[q]);
+                float dot = 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) dot += sv[q][u] * lv[q][u];
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                if ((lane & 15) == 0) dgam[c] = dot;
+            }
+        }
+        {  // K~ (rows 0..63) and W (rows 64..127)
+            float x[8][8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int e = tid + 256 * q, r = e >> 4, jc = e & 15;
+                vt_load8((r < C ? rec.K + (size_t)r * D : rec.W + (size_t)(r - C) * D) + 8 * jc, x[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int e = tid + 256 * q, r = e >> 4, jc = e & 15;
+                *reinterpret_cast<uint4 *>(sm + vt::KWIMG + img_chunk_off(128, r, jc)) = vt_pack8(x[q]);
+            }
+        }
+        {  // dO (zero past the sequence), scale A (rows i), U transposed (row j holds U[0..63][j])
+            uint4 uo[4];
+            float xa[2][8], xu[4][8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int e = tid + 256 * q, r = e >> 4, jc = e & 15;
+                uo[q] = make_uint4(0u, 0u, 0u, 0u);
+                if (r < len) uo[q] = *reinterpret_cast<const uint4 *>(d_o + ((t0 + r) * H + h) * (int64_t)D + 8 * jc);
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int e = tid + 256 * q, i = e >> 3, rc = e & 7;
+                vt_load8(rec.A + (size_t)i * C + 8 * rc, xa[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int e = tid + 256 * q, j = e & 127, ic = e >> 7;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) xu[q][u] = rec.U[(size_t)(8 * ic + u) * D + j];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int e = tid + 256 * q, r = e >> 4, jc = e & 15;
+                *reinterpret_cast<uint4 *>(sm + vt::DOIMG + img_chunk_off(64, r, jc)) = uo[q];
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int e = tid + 256 * q, i = e >> 3, rc = e & 7;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) xa[q][u] *= scale;
+                *reinterpret_cast<uint4 *>(sm + vt::AIMG + img_chunk_off(64, i, rc)) = vt_pack8(xa[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int e = tid + 256 * q, j = e & 127, ic = e >> 7;
+                *reinterpret_cast<uint4 *>(sm + vt::VUIMG + 16384 + img_chunk_off(128, j, ic)) = vt_pack8(xu[q]);
+            }
+        }
+        if (tid < C) bet[tid] = tid < len ? ld(beta + (t0 + tid) * H + h) : 0.f;
+        cp_async_wait_all();
+        fence_proxy_async();
+        vt_sync();
+
+        if (tid == 0) {
+            mma_bf16_mnk(tb + 0, s0 + vt::SIMG, 16384, s0 + vt::KWIMG + 8192, 128, 8, idesc_bf16(128, 64, true, false),
+                         false);
+            mma_bf16_mnk(tb + 64, s0 + vt::LIMG, 16384, s0 + vt::KWIMG, 128, 8, idesc_bf16(128, 64, true, false),
+                         false);
+            mma_bf16_mnmn(tb + 64, s0 + vt::DOIMG, 8192, s0 + vt::AIMG, 8192, 4, idesc_bf16(128, 64, true, true),
+                          true);
+            mma_bf16_k(tb + 128, s0 + vt::SIMG, 128, s0 + vt::DOIMG, 64, 8, idesc_bf16(128, 64), false);
+            mma_commit(&bar[0]);
+        }
+        ok = vt_wait(&bar[0], ph);
+        if (!ok) break;
+        if (warp < 4) {  // value channel j = row
+            const int j = row;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {  // V~ = U - W S, column j -> row j of the V~ group
+                float d[32];
+                tmem_ld32(tmem_addr(tb + 0, lq, 32 * hf), d);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) d[u] = rec.U[(size_t)(32 * hf + u) * D + j] - d[u];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4 *>(sm + vt::VUIMG + img_chunk_off(128, j, 4 * hf + q)) =
+                        vt_pack8(d + 8 * q);
+            }
+            float x[64];
+            tmem_ld32(tmem_addr(tb + 64, lq, 0), x);
+            tmem_ld32(tmem_addr(tb + 64, lq, 32), x + 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4 *>(sm + vt::DVIMG + img_chunk_off(128, j, q)) = vt_pack8(x + 8 * q);
+            vt_solve_ut_tmem(tmem_addr(tb + 64, lq, 0), Lf);  // dX_U = T^T dV~
+            tmem_ld32(tmem_addr(tb + 64, lq, 0), x);
+            tmem_ld32(tmem_addr(tb + 64, lq, 32), x + 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4 *>(sm + vt::DXUIMG + img_chunk_off(128, j, q)) = vt_pack8(x + 8 * q);
+#pragma unroll
+            for (int r0 = 0; r0 < C; r0 += 16) {  // dv = beta dX_U; the X_U part of d beta, sum_j dX_U v
+                float vv[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    vv[u] = r0 + u < len ? ld(v + ((t0 + r0 + u) * H + h) * (int64_t)D + j) : 0.f;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int r = r0 + u;
+                    if (r < len) st(grad_v + ((t0 + r) * H + h) * (int64_t)D + j, bet[r] * x[r]);
+                    x[r] *= vv[u];
+                }
+            }
+            const int b = vt_reduce_scatter64(x, lane);
+            red[warp * 64 + b] = x[0];
+            red[warp * 64 + b + 1] = x[1];
+        } else {  // key channel c = row: dQ^ = scale dO S^T
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float d[32];
+                tmem_ld32(tmem_addr(tb + 128, lq, 32 * hf), d);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) pp[P.dQ() + (32 * hf + u) * D + row] = scale * d[u];
+            }
+        }
+        fence_proxy_async();
+        vt_sync();
+        if (tid == 0) {
+            mma_bf16_kmn(tb + 0, s0 + vt::SIMG, 128, s0 + vt::DVIMG, 16384, 8, idesc_bf16(128, 64, false, true),
+                         false);
+            mma_bf16_kmn(tb + 64, s0 + vt::LIMG, 128, s0 + vt::VUIMG, 16384, 8, idesc_bf16(128, 64, false, true),
+                         false);
+            mma_bf16_mnk(tb + 128, s0 + vt::VUIMG, 16384, s0 + vt::DOIMG, 64, 8, idesc_bf16(128, 64, true, false),
+                         false);
+            mma_bf16_mnmn(tb + 192, s0 + vt::VUIMG, 16384, s0 + vt::DXUIMG, 16384, 8,
+                          idesc_bf16(128, 64, true, true), false);
+            mma_commit(&bar[1]);
+        }
+        ok = vt_wait(&bar[1], ph);
+        if (!ok) break;
+        if (warp < 4) {  // key channel c = row: dX_W = T^T dW, dW = -(S dV~^T)^T
+            float x[64];
+            vt_solve_ut_tmem(tmem_addr(tb + 0, lq, 0), Lf);  // linear: solve S dV~^T, then negate
+            tmem_ld32(tmem_addr(tb + 0, lq, 0), x);
+            tmem_ld32(tmem_addr(tb + 0, lq, 32), x + 32);
+#pragma unroll
+            for (int r = 0; r < C; ++r) x[r] = -x[r];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4 *>(sm + vt::DXWIMG + img_chunk_off(128, row, q)) = vt_pack8(x + 8 * q);
+#pragma unroll
+            for (int r = 0; r < C; ++r) pp[P.dW() + r * D + row] = x[r];
+        } else {  // dK~ = V~ Lambda^T; the rows of V~ in [V~; U] dO^T give dA
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float d[32];
+                tmem_ld32(tmem_addr(tb + 64, lq, 32 * hf), d);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) pp[P.dK() + (32 * hf + u) * D + row] = d[u];
+            }
+            if (warp < 6) {  // i = row < 64: dA[r][i] = scale (dO V~^T)[r][i] for i <= r
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    float d[32];
+                    tmem_ld32(tmem_addr(tb + 128, lq, 32 * hf), d);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        const int r = 32 * hf + u;
+                        pp[P.dA() + r * C + row] = row <= r ? scale * d[u] : 0.f;
+                    }
+                }
+            }
+        }
+        fence_proxy_async();
+        vt_sync();
+        if (tid == 0) {
+            mma_bf16_kmn(tb + 192, s0 + vt::KWIMG, 128, s0 + vt::DXWIMG, 16384, 8, idesc_bf16(128, 64, false, true),
+                         true);
+            mma_commit(&bar[2]);
+        }
+        ok = vt_wait(&bar[2], ph);
+        if (!ok) break;
+        if (warp >= 6) {  // i = row - 64: dL[r][i] = -(dX_U U^T + dX_W W^T)[r][i] for i < r
+            const int i = row - 64;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float d[32];
+                tmem_ld32(tmem_addr(tb + 192, lq, 32 * hf), d);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int r = 32 * hf + u;
+                    pp[P.dLu() + r * C + i] = i < r ? -d[u] : 0.f;
+                }
+            }
+        }
+        if (tid < D) pp[P.dgam() + tid] = dgam[tid];
+        if (tid < C) pp[P.dbu() + tid] = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
+        vt_sync();  // every read of this item's images and tensor memory is done
+    }
+    if (!ok && tid == 0) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
+    vt_sync();
+    if (warp == 0) tmem_dealloc(tb, 256);
+}
+
 // ------------------------------------------------------------------ key side, per (chunk, head)
 // Thread t owns channel c = t % DK of the RPT = C DK / NT consecutive rows (t / DK) RPT + [0, RPT):
 // their in-chunk log-decay (a prefix sum within the rows, then the earlier row groups' totals), their
@@ -678,8 +1103,19 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
         }
         return st;
     }
-    // 3. value side per (chunk, head), the value channels 32 at a time
-    {
+    // 3. value side per (chunk, head): on the tensor cores for bf16 I/O at d_k = d_v = 128 (dO read in
+    // 16-byte pieces), else on CUDA cores, the value channels 32 at a time
+    if (a->dtype == KDA_BF16 && dk == 128 && dv == 128 && ((uintptr_t)a->grad_o & 15) == 0) {
+        cudaFuncSetAttribute(bw::chunk_bwd_value_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bw::vt::TOTAL);
+        int dev = 0, sms = 148;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int64_t items = Ly.slots * H;
+        bw::chunk_bwd_value_tc_kernel<<<(unsigned)std::min<int64_t>(sms, items), 256, bw::vt::TOTAL, stream>>>(
+            a->T, (int)a->N, a->cu_seqlens, chunk_start, H, records, rb, Lbuf, ckpt, lam, a->scale,
+            (const bf16 *)a->v, (const bf16 *)a->beta, (const bf16 *)a->grad_o, (bf16 *)a->grad_v, part,
+            kda_device_error_ptr());
+    } else {
         const size_t smem_val = sizeof(float) * (2 * (size_t)C * (dk + 4) + 2 * (size_t)C * (C + 4) +
                                                  2 * (size_t)dk * (bw::TILE + 1) + 5 * (size_t)C * (bw::TILE + 1) + C);
         const void *kern = dk == 128 ? (const void *)bw::chunk_bwd_value_kernel_t<128>
