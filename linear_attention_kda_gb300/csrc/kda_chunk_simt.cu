@@ -22,6 +22,7 @@
 // Tokens past the end of a sequence inside its last chunk are loaded as zeros
 // with g = 0 and beta = 0, which leaves every valid row and the state unchanged.
 #include "kda_common.cuh"
+#include <algorithm>
 #include "kda_internal.h"
 #include "kda_f32_records.cuh"
 
@@ -30,8 +31,11 @@ namespace kda {
 constexpr int SIMT_THREADS = 256;
 constexpr int SLICE = 32;  // value columns per chain CTA
 
+// One CTA per (chunk, head).  Shared memory holds k, G and q (then v, in q's place, once the records
+// that need q are written) and L, ~113 KB at d = 128, so that two CTAs share an SM; A goes straight to
+// the record.
 template <typename Tio>
-__global__ void __launch_bounds__(SIMT_THREADS)
+__global__ void __launch_bounds__(SIMT_THREADS, 2)
 chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, const Tio *__restrict__ v,
                         const Tio *__restrict__ z, const Tio *__restrict__ beta,
                         const float *__restrict__ bias, const float *__restrict__ A_log, float g_min,
@@ -45,15 +49,18 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
     int64_t t0;
     if (!locate_chunk(chunk_start, cu, T, N, C, slot, n, t0, len)) return;
     const int tid = threadIdx.x;
-    const int PK = dk + 1, PV = dv + 1, PC = C + 1;
+    const int PK = dk + 1, PV = dv + 1, PC = C;
     float *Ks = sm;               // [C][PK]
-    float *Qs = Ks + C * PK;      // [C][PK]
-    float *Gs = Qs + C * PK;      // [C][PK]
-    float *Vs = Gs + C * PK;      // [C][PV]
-    float *Ls = Vs + C * PV;      // [C][PC]
-    float *As = Ls + C * PC;      // [C][PC]
-    float *bet = As + C * PC;     // [C]
+    float *Gs = Ks + C * PK;      // [C][PK]
+    float *Qs = Gs + C * PK;      // [C][PK]  q, then v ([C][PV]) in the same place
+    float *Vs = Qs;
+    float *Ls = Qs + C * max(PK, PV);  // [C][PC]
+    auto bet = [&](int r) { return r < len ? ld(beta + (t0 + r) * H + h) : 0.f; };
 
+    for (int r = tid; r < len; r += SIMT_THREADS) {  // v is read after A and L: ask L2 for it now
+        const char *row = reinterpret_cast<const char *>(v + ((t0 + r) * H + h) * (int64_t)dv);
+        for (int o = 0; o < dv * (int)sizeof(Tio); o += 128) asm volatile("prefetch.global.L2 [%0];" :: "l"(row + o));
+    }
     const float eA = A_log ? expf(A_log[h]) : 1.f;
 #pragma unroll 4
     for (int e = tid; e < C * dk; e += SIMT_THREADS) {
@@ -64,12 +71,6 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
         Qs[r * PK + c] = ok ? ld(q + idx) : 0.f;
         Gs[r * PK + c] = ok ? gate_log(kind, ld(z + idx), bias ? bias[h * dk + c] : 0.f, eA, g_min) : 0.f;
     }
-#pragma unroll 8
-    for (int e = tid; e < C * dv; e += SIMT_THREADS) {
-        const int r = e / dv, c = e % dv;
-        Vs[r * PV + c] = r < len ? ld(v + ((t0 + r) * H + h) * (int64_t)dv + c) : 0.f;
-    }
-    for (int r = tid; r < C; r += SIMT_THREADS) bet[r] = r < len ? ld(beta + (t0 + r) * H + h) : 0.f;
     __syncthreads();
     // in-chunk cumulative log-decay (Eq. 3), kept in base 2 (G log2 e) so that every decay below is
     // one exp2 of a difference
@@ -81,10 +82,12 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
         }
     }
     __syncthreads();
+    F32Record rec = f32_record(records, rec_bytes, slot, H, h, C, dk, dv);
     // A and L, four key rows i per thread sharing the query row r's values; the exponent is clamped at
     // 0 only so that the block's entries above the diagonal (discarded) cannot overflow
     for (int it = tid; it < C * (C / 4); it += SIMT_THREADS) {
         const int r = it / (C / 4), ib = (it % (C / 4)) * 4;
+        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f), l4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (ib <= r) {
             float sl[4] = {0.f, 0.f, 0.f, 0.f}, sa[4] = {0.f, 0.f, 0.f, 0.f};
             for (int c = 0; c < dk; ++c) {
@@ -96,23 +99,18 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
                     sa[u] += qr * ki;
                 }
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = ib + u;
-                Ls[r * PC + i] = (i < r) ? bet[r] * sl[u] : 0.f;
-                As[r * PC + i] = (i <= r) ? sa[u] : 0.f;
-            }
-        } else {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) Ls[r * PC + ib + u] = As[r * PC + ib + u] = 0.f;
+            const float br = bet(r);
+            l4 = make_float4(ib < r ? br * sl[0] : 0.f, ib + 1 < r ? br * sl[1] : 0.f,
+                             ib + 2 < r ? br * sl[2] : 0.f, ib + 3 < r ? br * sl[3] : 0.f);
+            a4 = make_float4(sa[0], ib + 1 <= r ? sa[1] : 0.f, ib + 2 <= r ? sa[2] : 0.f, ib + 3 <= r ? sa[3] : 0.f);
         }
+        *reinterpret_cast<float4 *>(Ls + r * PC + ib) = l4;
+        *reinterpret_cast<float4 *>(rec.A + r * C + ib) = a4;
     }
     __syncthreads();
-    F32Record rec = f32_record(records, rec_bytes, slot, H, h, C, dk, dv);
-    for (int e = tid; e < C * C; e += SIMT_THREADS) rec.A[e] = As[(e / C) * PC + e % C];
     if (Lout) {  // the backward pass reuses L (strictly lower, zeros elsewhere)
         float *Lg = Lout + ((size_t)slot * H + h) * (size_t)C * C;
-        for (int e = tid; e < C * C; e += SIMT_THREADS) Lg[e] = Ls[(e / C) * PC + e % C];
+        for (int e = tid; e < C * C; e += SIMT_THREADS) Lg[e] = Ls[e];
     }
     for (int e = tid; e < C * dk; e += SIMT_THREADS) {
         const int r = e / dk, c = e % dk;
@@ -121,15 +119,16 @@ chunk_intra_simt_kernel(const Tio *__restrict__ q, const Tio *__restrict__ k, co
         rec.K[e] = Ks[r * PK + c] * exp2f(Gl - G);
         if (r == 0) rec.gam[c] = exp2f(Gl);
     }
-    __syncthreads();
+    __syncthreads();  // q is no longer needed: v takes its place
     // right-hand sides of the UT transform, in place
     for (int e = tid; e < C * dk; e += SIMT_THREADS) {
         const int r = e / dk, c = e % dk;
-        Ks[r * PK + c] = bet[r] * Ks[r * PK + c] * exp2f(Gs[r * PK + c]);
+        Ks[r * PK + c] = bet(r) * Ks[r * PK + c] * exp2f(Gs[r * PK + c]);
     }
+#pragma unroll 8
     for (int e = tid; e < C * dv; e += SIMT_THREADS) {
         const int r = e / dv, c = e % dv;
-        Vs[r * PV + c] *= bet[r];
+        Vs[r * PV + c] = r < len ? bet(r) * ld(v + ((t0 + r) * H + h) * (int64_t)dv + c) : 0.f;
     }
     __syncthreads();
     // forward substitution (I + L) X = RHS, one column per thread
@@ -296,7 +295,7 @@ static kda_status_t launch_simt(const kda_chunk_args *a, const kda_chunk_plan &p
     const int32_t *chunk_start = (const int32_t *)((char *)ws + p.off_chunk_start);
     char *records = (char *)ws + p.off_records;
     const size_t smem_intra =
-        sizeof(float) * ((size_t)3 * C * (dk + 1) + (size_t)C * (dv + 1) + 2 * (size_t)C * (C + 1) + C);
+        sizeof(float) * ((size_t)2 * C * (dk + 1) + (size_t)C * (std::max(dk, dv) + 1) + (size_t)C * C);
     const size_t smem_chain = sizeof(float) * ((size_t)3 * C * (dk + 4) + (size_t)C * (C + 4) +
                                                2 * (size_t)C * (SLICE + 4) + (size_t)dk * (SLICE + 4) + dk);
     const bool b16 = a->dtype == KDA_BF16;
