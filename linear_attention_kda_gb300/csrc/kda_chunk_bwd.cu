@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(NT)
 chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
                        int H, int dv, const char *__restrict__ records, size_t rec_bytes,
                        float scale, const Tio *__restrict__ d_o, const float *__restrict__ d_final,
-                       float *__restrict__ lam_end, float *__restrict__ d_init) {
+                       float *__restrict__ lam_end, float *__restrict__ d_init, int staged) {
     extern __shared__ float sm[];
     constexpr int C = 64, dk = DK;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
@@ -66,6 +66,7 @@ chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const i
     constexpr int RW = C / NWARP, CW = DK / NWARP;  // rows of dV~ and of Lambda per warp
     // 16-byte rows (asynchronous copies, 16-byte broadcast reads); lane-indexed operands are contiguous
     constexpr int PK = dk + 4, PC = C + 4, PS = TILE + 4;
+    constexpr int RAW = TILE * (int)sizeof(Tio) / 16;  // 16-byte pieces of a row of dO's slice
     float *Ws = sm;               // [C][PK]
     float *Qs = Ws + C * PK;      // [C][PK]
     float *Kt = Qs + C * PK;      // [C][PK]
@@ -74,41 +75,71 @@ chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const i
     float *dVt = dOs + C * PS;    // [C][PS]
     float *Lm = dVt + C * PS;     // [dk][PS]
     float *gam = Lm + dk * PS;    // [dk]
+    Tio *dOraw = reinterpret_cast<Tio *>(gam + dk);  // [C][TILE] dO as stored, the next chunk's
 
     const size_t sbase = ((size_t)n * H + h) * (size_t)dk * dv;
+    const int64_t s_tok = cu ? (int64_t)cu[n] : (T / N) * n;
+    const int64_t e_tok = cu ? (int64_t)cu[n + 1] : s_tok + T / N;
+    const int c0 = chunk_start[n], c1 = chunk_start[n + 1];
+    auto first_tok = [&](int cix) { return s_tok + (int64_t)(cix - c0) * C; };
+    auto length = [&](int cix) { return (int)min((int64_t)C, e_tok - first_tok(cix)); };
+    // A chunk's tiles come in three groups of asynchronous copies, each issued as soon as the previous
+    // chunk's copy has been read for the last time: its dO slice (as stored), K~ and A after the dV~
+    // phase, Q^, W and gamma after the Lambda phase.
+    auto issue_do = [&](int cix) {
+        if (!staged) return;
+        const int64_t t0 = first_tok(cix);
+        const int len = length(cix);
+        for (int e = tid; e < len * RAW; e += NT) {
+            const int r = e / RAW, pc = e % RAW;
+            cp_async16(reinterpret_cast<char *>(dOraw) + (r * RAW + pc) * 16,
+                       reinterpret_cast<const char *>(d_o + ((t0 + r) * H + h) * (int64_t)dv + j0) + pc * 16);
+        }
+    };
+    auto issue_ka = [&](int cix) {
+        const F32Record rec = f32_record(records, rec_bytes, cix, H, h, C, dk, dv);
+        tile_async(Kt, PK, rec.K, dk, C, dk, tid, NT);
+        tile_async(As, PC, rec.A, C, C, C, tid, NT);
+    };
+    auto issue_qw = [&](int cix) {
+        const F32Record rec = f32_record(records, rec_bytes, cix, H, h, C, dk, dv);
+        tile_async(Ws, PK, rec.W, dk, C, dk, tid, NT);
+        tile_async(Qs, PK, rec.Q, dk, C, dk, tid, NT);
+        tile_async(gam, dk, rec.gam, dk, 1, dk, tid, NT);
+    };
     if (d_final) {
         tile_async(Lm, PS, d_final + sbase + j0, dv, dk, TILE, tid, NT);
     } else {
         for (int e = tid; e < dk * TILE; e += NT) Lm[(e / TILE) * PS + e % TILE] = 0.f;
     }
-    const int64_t s_tok = cu ? (int64_t)cu[n] : (T / N) * n;
-    const int64_t e_tok = cu ? (int64_t)cu[n + 1] : s_tok + T / N;
-    const int c0 = chunk_start[n], c1 = chunk_start[n + 1];
+    if (c1 > c0) {
+        issue_do(c1 - 1);
+        issue_ka(c1 - 1);
+    }
+    cp_async_commit();
+    if (c1 > c0) issue_qw(c1 - 1);
+    cp_async_commit();
     for (int cix = c1 - 1; cix >= c0; --cix) {
-        const int64_t t0 = s_tok + (int64_t)(cix - c0) * C;
-        const int len = (int)min((int64_t)C, e_tok - t0);
-        const F32Record rec = f32_record(records, rec_bytes, cix, H, h, C, dk, dv);
+        const int64_t t0 = first_tok(cix);
+        const int len = length(cix);
         if (tid == 0 && cix > c0)  // the next record in this (reverse) order, into L2 meanwhile
             prefetch_l2(records + ((size_t)(cix - 1) * H + h) * rec_bytes, (uint32_t)rec_bytes);
-        cp_async_wait_all();
-        __syncthreads();  // the previous chunk is done with the buffers; Lambda is final
+        cp_async_wait_group1();  // this chunk's dO, K~ and A (and, the first time, d final_state)
+        __syncthreads();         // the previous chunk is done with dOs; Lambda is final
         float *lg = lam_end + ((size_t)cix * H + h) * (size_t)dk * dv;
         for (int e = tid; e < dk * TILE; e += NT) {
             const int c = e / TILE, j = e % TILE;
             lg[(size_t)c * dv + j0 + j] = Lm[c * PS + j];
         }
-        tile_async(Ws, PK, rec.W, dk, C, dk, tid, NT);
-        tile_async(Qs, PK, rec.Q, dk, C, dk, tid, NT);
-        tile_async(Kt, PK, rec.K, dk, C, dk, tid, NT);
-        tile_async(As, PC, rec.A, C, C, C, tid, NT);
-        tile_async(gam, dk, rec.gam, dk, 1, dk, tid, NT);
 #pragma unroll 8
         for (int e = tid; e < C * TILE; e += NT) {
             const int r = e / TILE, j = e % TILE;
-            dOs[r * PS + j] = r < len ? ld(d_o + ((t0 + r) * H + h) * (int64_t)dv + j0 + j) : 0.f;
+            dOs[r * PS + j] = r >= len ? 0.f
+                              : staged ? ld(dOraw + r * TILE + j)
+                                       : ld(d_o + ((t0 + r) * H + h) * (int64_t)dv + j0 + j);
         }
-        cp_async_wait_all();
-        __syncthreads();
+        __syncthreads();  // dO converted: the staging buffer is free
+        if (cix > c0) issue_do(cix - 1);
         // Register-blocked: warp w owns rows [RW w, RW w + RW) of dV~ and rows [CW w, CW w + CW) of
         // Lambda; lane-indexed operands are read once per reduction index, row operands as 16-byte
         // broadcasts.
@@ -136,6 +167,10 @@ chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const i
 #pragma unroll
             for (int i = 0; i < RW; ++i) dVt[(r0 + i) * PS + lane] = acc[i] + scale * acca[i];
         }
+        __syncthreads();  // K~ and A are free
+        if (cix > c0) issue_ka(cix - 1);
+        cp_async_commit();
+        cp_async_wait_group1();  // this chunk's Q^, W and gamma (the group just closed may still fly)
         __syncthreads();
         {  // Lambda <- Diag(gamma) Lambda + scale Q^^T dO - W^T dV~
             float lm[CW];
@@ -156,6 +191,9 @@ chunk_rev_chain_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const i
 #pragma unroll
             for (int i = 0; i < CW; ++i) Lm[(cb + i) * PS + lane] = lm[i];
         }
+        __syncthreads();  // Q^, W and gamma are free
+        if (cix > c0) issue_qw(cix - 1);
+        cp_async_commit();
     }
     cp_async_wait_all();  // a sequence without chunks: the copy of d final_state
     __syncthreads();
@@ -1080,14 +1118,17 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
     const size_t rb = Ly.p.record_bytes;
     // 2. Lambda over the chunks in reverse; d initial_state
     // Ws, Qs, Kt [C][dk + 4]; As [C][C + 4]; dOs, dVt [C][TILE + 4]; Lm [dk][TILE + 4]; gam [dk]
+    // + the staging buffer of the next chunk's dO slice [C][TILE] in the I/O type
     const size_t smem_rev = sizeof(float) * ((size_t)3 * C * (dk + 4) + (size_t)C * (C + 4) +
-                                             (2 * (size_t)C + dk) * (bw::TILE + 4) + dk);
+                                             (2 * (size_t)C + dk) * (bw::TILE + 4) + dk) +
+                            sizeof(Tio) * (size_t)C * bw::TILE;
+    const int staged = ((uintptr_t)a->grad_o & 15) == 0 ? 1 : 0;  // dO rows copied in 16-byte pieces
     {
         auto rev = [&](auto kern) {
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_rev);
             kern<<<dim3((unsigned)(a->N * H), (unsigned)(dv / bw::TILE)), bw::NT, smem_rev, stream>>>(
                 a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dv, records, rb, a->scale, (const Tio *)a->grad_o,
-                a->grad_final_state, lam, a->grad_initial_state);
+                a->grad_final_state, lam, a->grad_initial_state, staged);
         };
         if (dk == 128) rev(bw::chunk_rev_chain_kernel<Tio, 128>);
         else rev(bw::chunk_rev_chain_kernel<Tio, 64>);

@@ -173,22 +173,42 @@ chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
     float *gam = Ss + dk * PS;    // [dk]
 
     const size_t sbase = ((size_t)n * H + h) * (size_t)dk * dv;
+    const int64_t s_tok = cu ? (int64_t)cu[n] : (T / N) * n;
+    const int64_t e_tok = cu ? (int64_t)cu[n + 1] : s_tok + T / N;
+    const int c0 = chunk_start[n], c1 = chunk_start[n + 1];
+    // A chunk's tiles come in two groups of asynchronous copies, each issued as soon as the phase that
+    // last read the previous chunk's copy is done: W, U (and Q^, A with outputs) after the V~ / O phase,
+    // K~ and gamma after the state update.
+    auto issue_vo = [&](int cix) {
+        const F32Record rec = f32_record(records, rec_bytes, cix, H, h, C, dk, dv);
+        tile_async(Ws, PK, rec.W, dk, C, dk, tid, SIMT_THREADS);
+        tile_async(Us, PS, rec.U + j0, dv, C, SLICE, tid, SIMT_THREADS);
+        if (o) {
+            tile_async(Qs, PK, rec.Q, dk, C, dk, tid, SIMT_THREADS);
+            tile_async(As, PC, rec.A, C, C, C, tid, SIMT_THREADS);
+        }
+    };
+    auto issue_s = [&](int cix) {
+        const F32Record rec = f32_record(records, rec_bytes, cix, H, h, C, dk, dv);
+        tile_async(Kt, PK, rec.K, dk, C, dk, tid, SIMT_THREADS);
+        tile_async(gam, dk, rec.gam, dk, 1, dk, tid, SIMT_THREADS);
+    };
     if (initial_state) {
         tile_async(Ss, PS, initial_state + sbase + j0, dv, dk, SLICE, tid, SIMT_THREADS);
     } else {
         for (int e = tid; e < dk * SLICE; e += SIMT_THREADS) Ss[(e / SLICE) * PS + e % SLICE] = 0.f;
     }
-    const int64_t s_tok = cu ? (int64_t)cu[n] : (T / N) * n;
-    const int64_t e_tok = cu ? (int64_t)cu[n + 1] : s_tok + T / N;
-    const int c0 = chunk_start[n], c1 = chunk_start[n + 1];
+    if (c0 < c1) issue_vo(c0);
+    cp_async_commit();
+    if (c0 < c1) issue_s(c0);
+    cp_async_commit();
     for (int cix = c0; cix < c1; ++cix) {
         const int64_t t0 = s_tok + (int64_t)(cix - c0) * C;
         const int len = (int)min((int64_t)C, e_tok - t0);
-        F32Record rec = f32_record(records, rec_bytes, cix, H, h, C, dk, dv);
         if (tid == 0 && cix + 1 < c1)  // the next chunk's record, into L2 while this one runs
             prefetch_l2(records + ((size_t)(cix + 1) * H + h) * rec_bytes, (uint32_t)rec_bytes);
-        cp_async_wait_all();
-        __syncthreads();  // previous chunk done with the buffers (and the entering state has landed)
+        cp_async_wait_group1();  // this chunk's W, U (, Q^, A) and, the first time, the entering state
+        __syncthreads();
         if (ckpt) {  // the state entering this chunk, for the backward pass
             float *cg = ckpt + ((size_t)cix * H + h) * (size_t)dk * dv;
             for (int e = tid; e < dk * SLICE; e += SIMT_THREADS) {
@@ -196,14 +216,6 @@ chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
                 cg[(size_t)c * dv + j0 + j] = Ss[c * PS + j];
             }
         }
-        tile_async(Ws, PK, rec.W, dk, C, dk, tid, SIMT_THREADS);
-        tile_async(Qs, PK, rec.Q, dk, C, dk, tid, SIMT_THREADS);
-        tile_async(Kt, PK, rec.K, dk, C, dk, tid, SIMT_THREADS);
-        tile_async(As, PC, rec.A, C, C, C, tid, SIMT_THREADS);
-        tile_async(Us, PS, rec.U + j0, dv, C, SLICE, tid, SIMT_THREADS);
-        tile_async(gam, dk, rec.gam, dk, 1, dk, tid, SIMT_THREADS);
-        cp_async_wait_all();
-        __syncthreads();
         // Register-blocked products: warp w owns rows [RW w, RW w + RW) of V~ and O and rows
         // [CW w, CW w + CW) of S; a lane-indexed operand is read once per reduction index for all
         // of the warp's rows, row operands four at a time as 16-byte broadcasts.
@@ -246,7 +258,11 @@ chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
                     if (r0 + i < len) st(o + ((t0 + r0 + i) * H + h) * (int64_t)dv + j0 + lane, scale * oq[i]);
             }
         }
-        __syncthreads();  // every read of S in this chunk is done
+        __syncthreads();  // every read of S, W, U, Q^ and A in this chunk is done
+        if (cix + 1 < c1) issue_vo(cix + 1);
+        cp_async_commit();
+        cp_async_wait_group1();  // this chunk's K~ and gamma
+        __syncthreads();
         {  // S <- Diag(gamma^C) S + K~^T V~
             float sn[CW];
 #pragma unroll
@@ -265,6 +281,9 @@ chunk_chain_simt_kernel(int64_t T, int N, const int32_t *__restrict__ cu,
 #pragma unroll
             for (int i = 0; i < CW; ++i) Ss[(cb + i) * PS + lane] = sn[i];
         }
+        __syncthreads();  // K~ and gamma are free
+        if (cix + 1 < c1) issue_s(cix + 1);
+        cp_async_commit();
     }
     cp_async_wait_all();  // a sequence without chunks: the initial state's copy
     __syncthreads();

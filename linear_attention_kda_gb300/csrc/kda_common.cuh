@@ -43,6 +43,10 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
                  :: "r"((uint32_t)__cvta_generic_to_shared(smem_dst)), "l"(gsrc) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Closes this thread's current group of cp.async copies (an empty group is allowed); wait_group1 waits
+// until at most the newest group is still in flight.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 // 4-byte asynchronous copy global -> shared memory (both 4-byte aligned).
 __device__ __forceinline__ void cp_async4(void *smem_dst, const void *gsrc) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
