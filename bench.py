@@ -941,8 +941,8 @@ def run_case(args):
     prefill_4k:    the benchmark's prefill workload, B=1, H=32, T=4096, bf16, d=128.
     decode_small:  N=64 sequences x H=32 heads, d=128, fp32 state 268 MB (above L2), 8 steps.
     replay_256:    the decode workload's 256 x 32 states, one replay window (3 replayed, 4 new), 3 calls.
-    softplus_4k:   the prefill workload with the softplus gate (fp32 path), 2 calls.
-    backward_4k:   the backward pass on the prefill workload, 2 calls.
+    softplus_4k:   the T=4096 prefill workload with the softplus gate (fp32 path), 2 calls.
+    backward_4k:   the backward pass on the T=4096 prefill workload, 2 calls.
     """
     from linear_attention_kda_gb300 import build as kbuild, kda
     kbuild.build()
@@ -960,7 +960,7 @@ def run_case(args):
         for _ in range(3):
             kda.recurrent_replay(cached, nr, new, nc, dd["dt_bias"], dd["A_log"], dd["state"])
     elif args.case in ("softplus_4k", "backward_4k"):
-        w = WORKLOAD
+        w = syn.PREFILL_4K
         d = syn.make_prefill(w, seed=1, device=dev)
         args_ = [d[n] for n in ("q", "k", "v", "z", "beta", "dt_bias", "A_log")]
         for _ in range(2):
