@@ -549,6 +549,44 @@ def run_ours(args, rank, ws, local):
     e2e_pipe_wall_ms = (time.perf_counter() - t0_) * 1e3 / args.steps
     del dev_in, dev_in2, pin, o2_, fs2_
     T_head, ms_head = T, ms
+
+    # ---------------- the backward pass on the same batch (one-pass workspace, ~0.42 MiB per chunk-head)
+    bwd_batch = None
+    if not args.no_backward:
+        del work
+        torch.cuda.empty_cache()
+        work = None
+        gen = torch.Generator(device=dev).manual_seed(79 + rank)
+        go_h = torch.randn(o.shape, generator=gen, device=dev).to(o.dtype)
+        gST_h = torch.randn(fs.shape, generator=gen, device=dev) * 0.1
+        need_h = kda.chunk_bwd_workspace_size(T, N, H, D, D)
+        work_h = torch.empty((need_h,), dtype=torch.uint8, device=dev)
+
+        def step_bh():
+            return kda.chunk_bwd(q, k, v, z, beta, b, a, go_h, g_min=d["g_min"], scale=d["scale"],
+                                 cu_seqlens=d["cu_seqlens"], initial_state=s0, grad_final_state=gST_h,
+                                 workspace=work_h)
+
+        for _ in range(2):
+            g_ = step_bh()
+            del g_
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        ha, hb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hts = []
+        for _ in range(3):
+            ha.record(stream)
+            g_ = step_bh()
+            hb.record(stream)
+            hb.synchronize()
+            hts.append(ha.elapsed_time(hb))
+            del g_
+        msbh = max_over_ranks(sum(hts) / len(hts), ws)
+        bwd_batch = {"what": "kda_chunk_bwd on the headline batch: d q, k, v, z, beta, dt_bias, A_log, S0 "
+                             "from d o and d S_T (inputs larger than L2)",
+                     "ms_per_step": msbh, "tokens_per_s": T / (msbh / 1e3), "vs_forward": msbh / ms,
+                     "workspace_bytes": int(need_h)}
+        del go_h, gST_h, work_h
     del q, k, v, z, beta, d, o, fs, work
     torch.cuda.empty_cache()
 
@@ -928,6 +966,7 @@ def run_ours(args, rank, ws, local):
             "epilogue": epi,
             "gate_variant": gvar,
             "backward": bwd,
+            "backward_batch": bwd_batch,
             "long_workloads": longw,
             "cpu_baseline": cpu,
         }

@@ -876,6 +876,386 @@ chunk_bwd_value_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, cons
     if (warp == 0) tmem_dealloc(tb, 256);
 }
 
+// ------------------------------------------------------------------ reverse chain on the tensor cores
+// bf16 I/O with d_k = d_v = 128: one 256-thread CTA per (sequence, head) keeps Lambda^T (rows = value
+// channels j = TMEM lanes, columns = key channels c) in tensor memory, fp32, and per chunk, last to first:
+//   writes Lambda (leaving the chunk) to lam_end and as a bf16 image, scales it by gamma in place, then
+//   dV~^T = Lambda^T K~^T + dO^T (scale A)          (into TMEM columns 128..191)
+//   Lambda^T += dO^T (scale Q^) + (-dV~^T) W          (two accumulating products)
+// Warps 4-7 turn the fp32 records of the chunks ahead into bf16 operand images (two buffers: the
+// chunk after next is filled while this one runs; a buffer is released by the commit that follows
+// the last product reading it); warps 0-3 move Lambda and dV~ between TMEM and shared memory, and
+// their first thread issues the products.
+namespace rc {
+constexpr uint32_t KI = 0, QI = 16384, WI = 32768, DI = 49152, AI = 65536, GM = 73728;  // within a buffer
+constexpr uint32_t BUF = 74752;            // one chunk's images: K~, scale Q^, W, dO (rows r, 16 KB each),
+                                           // scale A (rows i, 8 KB), gamma (fp32 [128])
+constexpr uint32_t LIMG = 2 * BUF;         // Lambda^T, bf16, K-major: rows j (128), two blocks of 64 c
+constexpr uint32_t DVIMG = LIMG + 32768;   // -dV~^T, bf16, K-major: rows j (128), 64 tokens
+constexpr uint32_t BAR = DVIMG + 16384;    // full[2], empty[2], mma1, mma2
+constexpr uint32_t TSLOT = BAR + 64;       // TMEM base
+constexpr uint32_t FAIL = TSLOT + 8;       // a bounded wait gave up
+constexpr uint32_t TOTAL = FAIL + 8 + 1024;
+}  // namespace rc
+
+// And-reduction of v over the n threads of named barrier id (also a barrier among them).
+__device__ __forceinline__ bool rc_all(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}\n"
+                 : "=r"(r) : "r"((uint32_t)v), "r"(id), "r"(n) : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void rc_bar(int id, int n) { asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory"); }
+// Bounded wait on an mbarrier phase that also gives up once the other role has failed.
+__device__ __forceinline__ bool rc_wait(uint64_t *bar, uint32_t parity, volatile int *fail) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = tc::globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (tc::mbar_try_wait(bar, parity)) return true;
+        if (*fail) return false;
+        if (tc::globaltimer_ns() - t0 > 1000000000ull) {
+            *fail = 1;
+            return false;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256, 1)
+chunk_rev_chain_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
+                          int H, const char *__restrict__ records, size_t rec_bytes, float scale,
+                          const bf16 *__restrict__ d_o, const float *__restrict__ d_final,
+                          float *__restrict__ lam_end, float *__restrict__ d_init, int *err) {
+    using namespace tc;
+    constexpr int C = 64, D = 128;
+    extern __shared__ unsigned char rc_raw[];
+    unsigned char *sm = vt_align1024(rc_raw);
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lq = (warp & 3) * 32, row = lq + lane;  // TMEM lane quarter of this warp; this thread's lane
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + rc::BAR), *empty = full + 2, *bmma1 = full + 4,
+             *bmma2 = full + 5;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + rc::TSLOT);
+    volatile int *fail = reinterpret_cast<volatile int *>(sm + rc::FAIL);
+    const int64_t s_tok = cu ? (int64_t)cu[n] : (T / N) * n;
+    const int64_t e_tok = cu ? (int64_t)cu[n + 1] : s_tok + T / N;
+    const int c0 = chunk_start[n], c1 = chunk_start[n + 1];
+    const int nst = c1 - c0;
+    const size_t sbase = ((size_t)n * H + h) * (size_t)D * D;
+    if (tid == 0) {
+        mbar_init(&full[0], 128);
+        mbar_init(&full[1], 128);
+        mbar_init(&empty[0], 1);
+        mbar_init(&empty[1], 1);
+        mbar_init(bmma1, 1);
+        mbar_init(bmma2, 1);
+        *fail = 0;
+    }
+    if (warp == 0) tmem_alloc(tslot, 256);
+    fence_proxy_async();
+    vt_sync();
+    const uint32_t tb = *tslot;  // Lambda^T: columns [0, 128); dV~^T: [128, 192)
+
+    if (warp < 4) {
+        // Lambda^T <- d final_state^T (or 0)
+#pragma unroll 1
+        for (int cb = 0; cb < D; cb += 16) {
+            float x[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) x[u] = d_final ? d_final[sbase + (size_t)(cb + u) * D + row] : 0.f;
+            tmem_st16(tmem_addr(tb, lq, cb), x);
+        }
+        tmem_st_wait();
+        bool ok = true;
+        for (int s = 0; s < nst; ++s) {
+            const int cix = c1 - 1 - s, b = s & 1;
+            unsigned char *B = sm + b * rc::BUF;
+            ok = rc_all(1, 128, rc_wait(&full[b], (s >> 1) & 1, fail));
+            if (!ok) break;
+            // Lambda leaving this chunk: to lam_end and the image; then Diag(gamma) Lambda in place
+            const float *gam = reinterpret_cast<const float *>(B + rc::GM);
+            float *lg = lam_end + ((size_t)cix * H + h) * (size_t)D * D;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                float x[32];
+                tmem_ld32(tmem_addr(tb, lq, 32 * q), x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) lg[(size_t)(32 * q + u) * D + row] = x[u];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint4 *>(sm + rc::LIMG + img_chunk_off(128, row, 4 * q + k)) = vt_pack8(x + 8 * k);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) x[u] *= gam[32 * q + u];
+                tmem_st32(tmem_addr(tb, lq, 32 * q), x);
+            }
+            tmem_st_wait();
+            fence_proxy_async();
+            fence_before_sync();
+            rc_bar(1, 128);
+            fence_after_sync();
+            const uint32_t sb = smem_u32(B), s0 = smem_u32(sm);
+            if (tid == 0) {
+                mma_bf16_k(tb + 128, s0 + rc::LIMG, 128, sb + rc::KI, 64, 8, idesc_bf16(128, 64), false);
+                mma_bf16_mnmn(tb + 128, sb + rc::DI, 8192, sb + rc::AI, 8192, 4, idesc_bf16(128, 64, true, true), true);
+                mma_bf16_mnmn(tb + 0, sb + rc::DI, 8192, sb + rc::QI, 8192, 4, idesc_bf16(128, 128, true, true), true);
+                mma_commit(bmma1);
+            }
+            ok = rc_all(1, 128, rc_wait(bmma1, s & 1, fail));
+            if (!ok) break;
+            fence_after_sync();
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {  // -dV~^T, row j of the image
+                float x[32];
+                tmem_ld32(tmem_addr(tb + 128, lq, 32 * hf), x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) x[u] = -x[u];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint4 *>(sm + rc::DVIMG + img_chunk_off(128, row, 4 * hf + k)) = vt_pack8(x + 8 * k);
+            }
+            fence_proxy_async();
+            fence_before_sync();
+            rc_bar(1, 128);
+            fence_after_sync();
+            if (tid == 0) {
+                mma_bf16_kmn(tb + 0, s0 + rc::DVIMG, 128, sb + rc::WI, 8192, 4, idesc_bf16(128, 128, false, true), true);
+                mma_commit(&empty[b]);  // this chunk's images are read by nothing after these products
+                mma_commit(bmma2);
+            }
+            ok = rc_all(1, 128, rc_wait(bmma2, s & 1, fail));
+            if (!ok) break;
+            fence_after_sync();
+        }
+        if (ok && d_init) {  // d S0 = Lambda entering the sequence
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                float x[32];
+                tmem_ld32(tmem_addr(tb, lq, 32 * q), x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) d_init[sbase + (size_t)(32 * q + u) * D + row] = x[u];
+            }
+        }
+    } else {  // fill warps
+        const int ft = tid - 128;
+        for (int s = 0; s < nst; ++s) {
+            const int cix = c1 - 1 - s, b = s & 1;
+            if (s >= 2 && !rc_all(2, 128, rc_wait(&empty[b], ((s >> 1) - 1) & 1, fail))) break;
+            if (ft == 0 && cix - 2 >= c0)  // the record two chunks on, into L2
+                prefetch_l2(records + ((size_t)(cix - 2) * H + h) * rec_bytes, (uint32_t)rec_bytes);
+            unsigned char *B = sm + b * rc::BUF;
+            const F32Record rec = f32_record(records, rec_bytes, cix, H, h, C, D, D);
+            const int64_t t0 = s_tok + (int64_t)(cix - c0) * C;
+            const int len = (int)min((int64_t)C, e_tok - t0);
+#pragma unroll 2
+            for (int q = 0; q < 8; ++q) {  // K~, scale Q^, W: rows r, 8 channels per piece
+                const int e = ft + 128 * q, r = e >> 4, jc = e & 15;
+                float xk[8], xq[8], xw[8];
+                vt_load8(rec.K + (size_t)r * D + 8 * jc, xk);
+                vt_load8(rec.Q + (size_t)r * D + 8 * jc, xq);
+                vt_load8(rec.W + (size_t)r * D + 8 * jc, xw);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) xq[u] *= scale;
+                const uint32_t off = img_chunk_off(64, r, jc);
+                *reinterpret_cast<uint4 *>(B + rc::KI + off) = vt_pack8(xk);
+                *reinterpret_cast<uint4 *>(B + rc::QI + off) = vt_pack8(xq);
+                *reinterpret_cast<uint4 *>(B + rc::WI + off) = vt_pack8(xw);
+            }
+            {
+                uint4 uo[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {  // dO, zero past the sequence
+                    const int e = ft + 128 * q, r = e >> 4, jc = e & 15;
+                    uo[q] = make_uint4(0u, 0u, 0u, 0u);
+                    if (r < len) uo[q] = *reinterpret_cast<const uint4 *>(d_o + ((t0 + r) * H + h) * (int64_t)D + 8 * jc);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int e = ft + 128 * q, r = e >> 4, jc = e & 15;
+                    *reinterpret_cast<uint4 *>(B + rc::DI + img_chunk_off(64, r, jc)) = uo[q];
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // scale A, rows i
+                const int e = ft + 128 * q, i = e >> 3, rcn = e & 7;
+                float x[8];
+                vt_load8(rec.A + (size_t)i * C + 8 * rcn, x);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] *= scale;
+                *reinterpret_cast<uint4 *>(B + rc::AI + img_chunk_off(64, i, rcn)) = vt_pack8(x);
+            }
+            reinterpret_cast<float *>(B + rc::GM)[ft] = rec.gam[ft];
+            fence_proxy_async();
+            mbar_arrive(&full[b]);
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && *fail) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
+    fence_after_sync();
+    if (warp == 0) tmem_dealloc(tb, 256);
+}
+
+// ------------------------------------------------------------------ forward chain with checkpoints on the tensor cores
+// The backward pass's recomputation of the state entering every chunk (no outputs), bf16 I/O with
+// d_k = d_v = 128: one 256-thread CTA per (sequence, head) keeps S^T (rows = value channels j = TMEM
+// lanes, columns = key channels c) in tensor memory, fp32, and per chunk writes S (entering it) to
+// the checkpoints and as a bf16 image, scales it by gamma in place, then
+//   V~^T = U^T - S^T W^T         (S^T W^T into TMEM columns 128..191; U from the fp32 record)
+//   S^T += V~^T K~               (accumulating product)
+// Warps 4-7 fill two buffers of the chunks ahead (W and K~ as bf16 images, U fp32, gamma); warps 0-3
+// move S and V~ between TMEM and shared memory, and their first thread issues the products.
+namespace fc {
+constexpr uint32_t WI = 0, KI = 16384, UF = 32768, GM = 65536;  // within a buffer
+constexpr uint32_t BUF = 67584;           // W, K~ (rows r, bf16, 16 KB each), U fp32 [64][128], gamma [128]
+constexpr uint32_t SIMG = 2 * BUF;        // S^T, bf16, K-major: rows j (128), two blocks of 64 c
+constexpr uint32_t VIMG = SIMG + 32768;   // V~^T, bf16, K-major: rows j (128), 64 tokens
+constexpr uint32_t BAR = VIMG + 16384;    // full[2], empty[2], mma1, mma2
+constexpr uint32_t TSLOT = BAR + 64;
+constexpr uint32_t FAIL = TSLOT + 8;
+constexpr uint32_t TOTAL = FAIL + 8 + 1024;
+}  // namespace fc
+
+__global__ void __launch_bounds__(256, 1)
+chunk_chain_ckpt_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_start,
+                           int H, const char *__restrict__ records, size_t rec_bytes,
+                           const float *__restrict__ initial_state, float *__restrict__ final_state,
+                           float *__restrict__ ckpt, int *err) {
+    using namespace tc;
+    constexpr int C = 64, D = 128;
+    extern __shared__ unsigned char fc_raw[];
+    unsigned char *sm = vt_align1024(fc_raw);
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lq = (warp & 3) * 32, row = lq + lane;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + fc::BAR), *empty = full + 2, *bmma1 = full + 4,
+             *bmma2 = full + 5;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + fc::TSLOT);
+    volatile int *fail = reinterpret_cast<volatile int *>(sm + fc::FAIL);
+    const int c0 = chunk_start[n], c1 = chunk_start[n + 1];
+    const int nst = c1 - c0;
+    const size_t sbase = ((size_t)n * H + h) * (size_t)D * D;
+    if (tid == 0) {
+        mbar_init(&full[0], 128);
+        mbar_init(&full[1], 128);
+        mbar_init(&empty[0], 1);
+        mbar_init(&empty[1], 1);
+        mbar_init(bmma1, 1);
+        mbar_init(bmma2, 1);
+        *fail = 0;
+    }
+    if (warp == 0) tmem_alloc(tslot, 256);
+    fence_proxy_async();
+    vt_sync();
+    const uint32_t tb = *tslot;  // S^T: columns [0, 128); S^T W^T: [128, 192)
+
+    if (warp < 4) {
+#pragma unroll 1
+        for (int cb = 0; cb < D; cb += 16) {  // S^T <- S0^T (or 0)
+            float x[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) x[u] = initial_state ? initial_state[sbase + (size_t)(cb + u) * D + row] : 0.f;
+            tmem_st16(tmem_addr(tb, lq, cb), x);
+        }
+        tmem_st_wait();
+        bool ok = true;
+        for (int s = 0; s < nst; ++s) {
+            const int cix = c0 + s, b = s & 1;
+            unsigned char *B = sm + b * fc::BUF;
+            ok = rc_all(1, 128, rc_wait(&full[b], (s >> 1) & 1, fail));
+            if (!ok) break;
+            const float *gam = reinterpret_cast<const float *>(B + fc::GM);
+            float *cg = ckpt + ((size_t)cix * H + h) * (size_t)D * D;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {  // S entering the chunk: checkpoint, image, then Diag(gamma) S
+                float x[32];
+                tmem_ld32(tmem_addr(tb, lq, 32 * q), x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) cg[(size_t)(32 * q + u) * D + row] = x[u];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint4 *>(sm + fc::SIMG + img_chunk_off(128, row, 4 * q + k)) = vt_pack8(x + 8 * k);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) x[u] *= gam[32 * q + u];
+                tmem_st32(tmem_addr(tb, lq, 32 * q), x);
+            }
+            tmem_st_wait();
+            fence_proxy_async();
+            fence_before_sync();
+            rc_bar(1, 128);
+            fence_after_sync();
+            const uint32_t sb = smem_u32(B), s0 = smem_u32(sm);
+            if (tid == 0) {
+                mma_bf16_k(tb + 128, s0 + fc::SIMG, 128, sb + fc::WI, 64, 8, idesc_bf16(128, 64), false);
+                mma_commit(bmma1);
+            }
+            ok = rc_all(1, 128, rc_wait(bmma1, s & 1, fail));
+            if (!ok) break;
+            fence_after_sync();
+            const float *Uf = reinterpret_cast<const float *>(B + fc::UF);
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {  // V~^T = U^T - S^T W^T, row j of the image
+                float x[32];
+                tmem_ld32(tmem_addr(tb + 128, lq, 32 * hf), x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) x[u] = Uf[(32 * hf + u) * D + row] - x[u];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint4 *>(sm + fc::VIMG + img_chunk_off(128, row, 4 * hf + k)) = vt_pack8(x + 8 * k);
+            }
+            fence_proxy_async();
+            fence_before_sync();
+            rc_bar(1, 128);
+            fence_after_sync();
+            if (tid == 0) {
+                mma_bf16_kmn(tb + 0, s0 + fc::VIMG, 128, sb + fc::KI, 8192, 4, idesc_bf16(128, 128, false, true), true);
+                mma_commit(&empty[b]);
+                mma_commit(bmma2);
+            }
+            ok = rc_all(1, 128, rc_wait(bmma2, s & 1, fail));
+            if (!ok) break;
+            fence_after_sync();
+        }
+        if (ok && final_state) {
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                float x[32];
+                tmem_ld32(tmem_addr(tb, lq, 32 * q), x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) final_state[sbase + (size_t)(32 * q + u) * D + row] = x[u];
+            }
+        }
+    } else {  // fill warps
+        const int ft = tid - 128;
+        for (int s = 0; s < nst; ++s) {
+            const int cix = c0 + s, b = s & 1;
+            if (s >= 2 && !rc_all(2, 128, rc_wait(&empty[b], ((s >> 1) - 1) & 1, fail))) break;
+            if (ft == 0 && cix + 2 < c1)
+                prefetch_l2(records + ((size_t)(cix + 2) * H + h) * rec_bytes, (uint32_t)rec_bytes);
+            unsigned char *B = sm + b * fc::BUF;
+            const F32Record rec = f32_record(records, rec_bytes, cix, H, h, C, D, D);
+            tile_async(reinterpret_cast<float *>(B + fc::UF), D, rec.U, D, C, D, ft, 128);
+#pragma unroll 2
+            for (int q = 0; q < 8; ++q) {  // W, K~: rows r, 8 channels per piece
+                const int e = ft + 128 * q, r = e >> 4, jc = e & 15;
+                float xw[8], xk[8];
+                vt_load8(rec.W + (size_t)r * D + 8 * jc, xw);
+                vt_load8(rec.K + (size_t)r * D + 8 * jc, xk);
+                const uint32_t off = img_chunk_off(64, r, jc);
+                *reinterpret_cast<uint4 *>(B + fc::WI + off) = vt_pack8(xw);
+                *reinterpret_cast<uint4 *>(B + fc::KI + off) = vt_pack8(xk);
+            }
+            reinterpret_cast<float *>(B + fc::GM)[ft] = rec.gam[ft];
+            cp_async_wait_all();
+            fence_proxy_async();
+            mbar_arrive(&full[b]);
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && *fail) set_error(err, KDA_ERR_DEVICE_TIMEOUT);
+    fence_after_sync();
+    if (warp == 0) tmem_dealloc(tb, 256);
+}
+
 // ------------------------------------------------------------------ key side, per (chunk, head)
 // Thread t owns channel c = t % DK of the RPT = C DK / NT consecutive rows (t / DK) RPT + [0, RPT):
 // their in-chunk log-decay (a prefix sum within the rows, then the earlier row groups' totals), their
@@ -1073,6 +1453,19 @@ __global__ void bwd_gate_param_kernel(const float *__restrict__ gate_part, int64
 
 using namespace kda;
 
+// The backward pass's forward chain (checkpoints, final state, no outputs) on the tensor cores when the
+// problem allows it (bf16, d_k = d_v = 128); false otherwise (the caller then runs the CUDA-core chain).
+bool kda_launch_chain_ckpt_tc(const kda_chunk_args *a, const int32_t *chunk_start, const char *records,
+                              size_t rec_bytes, float *ckpt, cudaStream_t stream) {
+    if (!ckpt || a->dtype != KDA_BF16 || a->dk != 128 || a->dv != 128 || a->o) return false;
+    cudaFuncSetAttribute(bw::chunk_chain_ckpt_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)bw::fc::TOTAL);
+    bw::chunk_chain_ckpt_tc_kernel<<<(unsigned)(a->N * a->H), 256, bw::fc::TOTAL, stream>>>(
+        a->T, (int)a->N, a->cu_seqlens, chunk_start, a->H, records, rec_bytes, a->initial_state, a->final_state,
+        ckpt, kda_device_error_ptr());
+    return true;
+}
+
 namespace {
 
 struct BwdLayout {
@@ -1130,8 +1523,17 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
                 a->T, (int)a->N, a->cu_seqlens, chunk_start, H, dv, records, rb, a->scale, (const Tio *)a->grad_o,
                 a->grad_final_state, lam, a->grad_initial_state, staged);
         };
-        if (dk == 128) rev(bw::chunk_rev_chain_kernel<Tio, 128>);
-        else rev(bw::chunk_rev_chain_kernel<Tio, 64>);
+        if (a->dtype == KDA_BF16 && dk == 128 && dv == 128 && staged) {  // on the tensor cores
+            cudaFuncSetAttribute(bw::chunk_rev_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bw::rc::TOTAL);
+            bw::chunk_rev_chain_tc_kernel<<<(unsigned)(a->N * H), 256, bw::rc::TOTAL, stream>>>(
+                a->T, (int)a->N, a->cu_seqlens, chunk_start, H, records, rb, a->scale, (const bf16 *)a->grad_o,
+                a->grad_final_state, lam, a->grad_initial_state, kda_device_error_ptr());
+        } else if (dk == 128) {
+            rev(bw::chunk_rev_chain_kernel<Tio, 128>);
+        } else {
+            rev(bw::chunk_rev_chain_kernel<Tio, 64>);
+        }
     }
     kda_profile_mark(4, stream);
     st = kda_cuda_status(cudaGetLastError());

@@ -339,6 +339,10 @@ static kda_status_t launch_simt(const kda_chunk_args *a, const kda_chunk_plan &p
         }
     }
     kda_profile_mark(2, stream);
+    if (kda_launch_chain_ckpt_tc(a, chunk_start, records, p.record_bytes, ckpt, stream)) {
+        kda_profile_mark(3, stream);
+        return kda_cuda_status(cudaGetLastError());
+    }
     dim3 grid2((unsigned)(a->N * H), (unsigned)(dv / SLICE));
     auto chain = [&](auto kern, auto *out) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_chain);

@@ -77,6 +77,10 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
 // The fp32 forward again, for the backward pass: records as kda_launch_chunk_simt, plus L per
 // (chunk slot, head) [C][C] into Lout and the state entering each chunk slot [dk][dv] into ckpt;
 // o is written only when a->o is set.
+// The backward pass's forward chain (checkpoints) on the tensor cores: launched and true when the problem
+// allows it (bf16, d_k = d_v = 128, no outputs, checkpoints requested), else false.
+bool kda_launch_chain_ckpt_tc(const kda_chunk_args *a, const int32_t *chunk_start, const char *records,
+                              size_t rec_bytes, float *ckpt, cudaStream_t stream);
 kda_status_t kda_launch_chunk_simt_recompute(const kda_chunk_args *a, const kda_chunk_plan &p, void *ws,
                                              float *Lout, float *ckpt, cudaStream_t stream);
 size_t kda_tc_packet_stride();  // bytes per (chunk, head) packet of the tensor-core path
