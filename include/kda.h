@@ -158,7 +158,10 @@ size_t kda_chunk_fwd_workspace_size(int64_t T, int64_t N, int32_t H, int32_t dk,
                                     kda_dtype_t dtype, int32_t chunk_size,
                                     const int32_t *cu_seqlens_host);
 /* The same for a given gate kind (kda_chunk_fwd_workspace_size is gate_kind 0; the softplus gate
- * takes the fp32 path, whose records are larger for bf16 d = 128). */
+ * takes the fp32 path, whose records are larger for bf16 d = 128).  The bf16 d = 128 tensor-core
+ * prefill scales rows and keys by e^{G_r - G_p} against references at most 16 tokens away, exact while
+ * 16 |g_min| stays inside fp32 range: with the bounded gate and g_min < -5.5 kda_chunk_fwd runs the
+ * fp32 path instead, whose workspace is this function's value for KDA_GATE_SOFTPLUS. */
 size_t kda_chunk_fwd_workspace_size_gate(int64_t T, int64_t N, int32_t H, int32_t dk, int32_t dv,
                                          kda_dtype_t dtype, int32_t chunk_size,
                                          const int32_t *cu_seqlens_host, int32_t gate_kind);
@@ -321,8 +324,9 @@ kda_status_t kda_output_gate(const kda_output_gate_args *args, struct CUstream_s
  * KDA_STATIC_WORKSPACE_BYTES that lives inside the library (a file-scope
  * device array, held by every GPU that loads the library until the process
  * exits).  The caller still owns and passes every input and output.
- *   - Limit: problems whose kda_chunk_fwd_workspace_size_gate() for their
- *     gate kind exceeds KDA_STATIC_WORKSPACE_BYTES are rejected with
+ *   - Limit: problems whose kda_chunk_fwd_workspace_size_gate() for the path
+ *     they take (their gate kind; KDA_GATE_SOFTPLUS's size for a bounded gate
+ *     with g_min < -5.5) exceeds KDA_STATIC_WORKSPACE_BYTES are rejected with
  *     KDA_ERR_WORKSPACE before anything is launched.  The limit depends on the
  *     gate kind and the dtype: with the bounded gate, bf16 at d = 128 needs
  *     about 73 KiB per chunk of 64 tokens per head (T = 4096 tokens with 13

@@ -88,7 +88,7 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
     if (!a) return 0;
     kda_chunk_plan p;
     if (!kda_make_chunk_plan(a->T, a->N > 0 ? a->N : 1, a->H > 0 ? a->H : 1, a->dk, a->dv, a->dtype, 64, &p,
-                             a->cu_seqlens_host, a->gate_kind))
+                             a->cu_seqlens_host, a->gate_kind, kda_gate_needs_fp32_path(a->gate_kind, a->g_min)))
         return 0;
     // either one fused launch (intra-chunk transform and output pass together) or the chunk plan,
     // then intra-chunk transform, [segment summaries, fold,] output pass; an empty batch (T = 0)
@@ -102,7 +102,8 @@ int32_t kda_chunk_fwd_kernel_count(const kda_chunk_args *a) {
 kda_status_t kda_chunk_fwd_schedule(const kda_chunk_args *a, int64_t *out) {
     if (!a || !out || a->T < 0 || a->N < 1 || a->H < 1) return KDA_ERR_INVALID_ARG;
     kda_chunk_plan p;
-    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p, a->cu_seqlens_host, a->gate_kind))
+    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p, a->cu_seqlens_host, a->gate_kind,
+                             kda_gate_needs_fp32_path(a->gate_kind, a->g_min)))
         return KDA_ERR_INVALID_ARG;
     out[0] = p.fused ? 1 : (p.team ? 2 : 0);
     out[1] = p.fused ? p.kpre : (p.team ? p.team_k : 0);
@@ -232,7 +233,8 @@ kda_status_t kda_chunk_fwd(const kda_chunk_args *a, void *workspace, size_t work
     kda_status_t st = validate_chunk(a);
     if (st != KDA_OK) return st;
     kda_chunk_plan p;
-    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p, a->cu_seqlens_host, a->gate_kind))
+    if (!kda_make_chunk_plan(a->T, a->N, a->H, a->dk, a->dv, a->dtype, 64, &p, a->cu_seqlens_host, a->gate_kind,
+                             kda_gate_needs_fp32_path(a->gate_kind, a->g_min)))
         return KDA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < p.total_bytes) return KDA_ERR_WORKSPACE;
     if (!aligned_to(workspace, 256)) return KDA_ERR_MISALIGNED;

@@ -77,6 +77,19 @@ kda_status_t kda_launch_chunk_tc(const kda_chunk_args *a, const kda_chunk_plan &
 // The fp32 forward again, for the backward pass: records as kda_launch_chunk_simt, plus L per
 // (chunk slot, head) [C][C] into Lout and the state entering each chunk slot [dk][dv] into ckpt;
 // o is written only when a->o is set.
+// The bf16 tensor-core prefill scales the rows and keys of a 64-token chunk by e^{G_r - G_p} against
+// references p at most 16 tokens away, so every such exponent is at most 16 |g_min| in size: inside
+// fp32 / bf16 range (e^88.7) for g_min >= -5.5 (the report uses -5).  A bounded gate with a lower g_min
+// runs on the fp32 path, whose decays are exp(G_r - G_i) <= 1 for every gate.
+constexpr float KDA_TC_MIN_G_MIN = -5.5f;
+inline bool kda_gate_needs_fp32_path(int gate_kind, float g_min) {
+    return gate_kind == KDA_GATE_LOWER_BOUND && !(g_min >= KDA_TC_MIN_G_MIN);
+}
+// The gate kind whose kda_chunk_fwd_workspace_size_gate fits a call: the softplus gate's (the fp32
+// path's) for a bounded gate below KDA_TC_MIN_G_MIN.
+inline int kda_workspace_gate(int gate_kind, float g_min) {
+    return kda_gate_needs_fp32_path(gate_kind, g_min) ? (int)KDA_GATE_SOFTPLUS : gate_kind;
+}
 // The backward pass's forward chain (checkpoints) on the tensor cores: launched and true when the problem
 // allows it (bf16, d_k = d_v = 128, no outputs, checkpoints requested), else false.
 bool kda_launch_chain_ckpt_tc(const kda_chunk_args *a, const int32_t *chunk_start, const char *records,

@@ -29,10 +29,11 @@ std::atomic<void *> g_static_ws_ptr[kMaxDev];  // device address of g_kda_static
 
 extern "C" kda_status_t kda_chunk_fwd_static_ws(const kda_chunk_args *args, struct CUstream_st *stream) {
     if (!args) return KDA_ERR_INVALID_ARG;
-    // sized for the gate kind: the softplus gate takes the fp32 path, whose records are larger
+    // sized for the path the call takes: the softplus gate, and the bounded gate below
+    // KDA_TC_MIN_G_MIN, run on the fp32 path, whose records are larger
     const size_t need = kda_chunk_fwd_workspace_size_gate(args->T, args->N, args->H, args->dk, args->dv,
                                                           args->dtype, args->chunk_size, args->cu_seqlens_host,
-                                                          args->gate_kind);
+                                                          kda_workspace_gate(args->gate_kind, args->g_min));
     if (need == 0) return kda_chunk_fwd(args, nullptr, 0, stream);  // invalid sizes: same status as kda_chunk_fwd
     if (need > (size_t)KDA_STATIC_WORKSPACE_BYTES) return KDA_ERR_WORKSPACE;  // problem too large for the buffer
     int dev = -1;

@@ -203,9 +203,17 @@ def gate(z: torch.Tensor, dt_bias=None, A_log=None, g_min: float = -5.0, chunk_s
     return out
 
 
+# below this g_min the bounded gate's bf16 d = 128 prefill runs on the fp32 path (kda.h)
+TC_MIN_G_MIN = -5.5
+
+
 def chunk_fwd_workspace_size(T, N, H, dk, dv, dtype: torch.dtype, chunk_size=64, cu_seqlens_host=None,
-                             gate: str = "lower_bound"):
+                             gate: str = "lower_bound", g_min: float = -5.0):
+    """kda_chunk_fwd_workspace_size_gate for the path the call takes (the fp32 path's size, that of the
+    softplus gate, for a bounded gate with g_min below TC_MIN_G_MIN)."""
     L = load_library()
+    if gate == "lower_bound" and not g_min >= TC_MIN_G_MIN:
+        gate = "softplus"
     code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
     hp = None
     if cu_seqlens_host is not None:
@@ -237,7 +245,7 @@ def chunk_fwd(q, k, v, z, beta, dt_bias=None, A_log=None, *, g_min: float = -5.0
     fs = final_state
     if fs is None and output_final_state:
         fs = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
-    need = chunk_fwd_workspace_size(T, N, H, dk, dv, q.dtype, chunk_size, cu_seqlens_host, gate)
+    need = chunk_fwd_workspace_size(T, N, H, dk, dv, q.dtype, chunk_size, cu_seqlens_host, gate, g_min)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
     a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=_dtype_code(q), q=_ptr(q), k=_ptr(k), z=_ptr(z),
@@ -404,7 +412,7 @@ def set_profile_events(events) -> None:
 
 
 def chunk_fwd_kernel_count(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, cu_seqlens_host=None,
-                           gate: str = "lower_bound", out_gate: bool = False) -> int:
+                           gate: str = "lower_bound", out_gate: bool = False, g_min: float = -5.0) -> int:
     """Kernels kda_chunk_fwd launches for these sizes (the split-sequence state pass adds two; with
     out_gate, a separate epilogue pass adds one where the output pass does not apply it)."""
     cu = None
@@ -412,19 +420,19 @@ def chunk_fwd_kernel_count(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, 
         cu = cu_seqlens_host.to(dtype=torch.int32, device="cpu").contiguous()
     a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=KDA_BF16 if dtype == torch.bfloat16 else KDA_F32,
                   cu_seqlens_host=None if cu is None else cu.data_ptr(), chunk_size=64,
-                  gate_kind=_gate_kind(gate), out_gate=16 if out_gate else None)
+                  gate_kind=_gate_kind(gate), out_gate=16 if out_gate else None, g_min=g_min)
     return int(load_library().kda_chunk_fwd_kernel_count(ctypes.byref(a)))
 
 
 def chunk_fwd_schedule(T=0, N=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, cu_seqlens_host=None,
-                       gate: str = "lower_bound") -> dict:
+                       gate: str = "lower_bound", g_min: float = -5.0) -> dict:
     """The schedule kda_chunk_fwd picks for these sizes (see kda_chunk_fwd_schedule in kda.h)."""
     cu = None
     if cu_seqlens_host is not None:
         cu = cu_seqlens_host.to(dtype=torch.int32, device="cpu").contiguous()
     a = ChunkArgs(T=T, N=N, H=H, dk=dk, dv=dv, dtype=KDA_BF16 if dtype == torch.bfloat16 else KDA_F32,
                   cu_seqlens_host=None if cu is None else cu.data_ptr(), chunk_size=64,
-                  gate_kind=_gate_kind(gate))
+                  gate_kind=_gate_kind(gate), g_min=g_min)
     out = (_i64 * 4)()
     _check(load_library().kda_chunk_fwd_schedule(ctypes.byref(a), out), "kda_chunk_fwd_schedule")
     return {"fused": out[0] == 1, "team": out[0] == 2, "own_chunks": int(out[1]) if out[0] == 1 else 0,

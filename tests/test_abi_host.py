@@ -158,6 +158,13 @@ def test_chunk_fwd_workspace_checks(lib):
     assert sp == lib.kda_chunk_fwd_workspace_size(128, 1, 2, 128, 128, kda.KDA_F32, 64, None)
     assert lib.kda_chunk_fwd_workspace_size_gate(128, 1, 2, 128, 128, kda.KDA_BF16, 64, None, 3) == 0
     assert _call_chunk(lib, _chunk(gate_kind=1), ws_bytes=need) == 5
+    # a bounded gate below g_min = -5.5 runs on the fp32 path (16 tokens of decay would leave fp32 range in
+    # the tensor-core path's scaled images): it needs the fp32 path's workspace
+    assert _call_chunk(lib, _chunk(g_min=-8.0), ws_bytes=need) == 5
+    assert _call_chunk(lib, _chunk(g_min=-8.0), ws=FAKE + 16, ws_bytes=sp) == 4  # size accepted, then alignment
+    assert _call_chunk(lib, _chunk(g_min=-5.5), ws=FAKE + 16, ws_bytes=need) == 4
+    assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, torch.bfloat16, g_min=-8.0)["kernels"] == 3
+    assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, torch.bfloat16, g_min=-5.0)["fused"]
 
 
 def test_chunk_fwd_host_seqlens_validated(lib):

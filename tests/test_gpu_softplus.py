@@ -138,3 +138,23 @@ def test_recurrent_replay_softplus_matches_oracle():
                                     d["state"][n, h].double().numpy())
             assert rel_err(o[n, :, h].numpy(), o_ref) <= TOL_BF16, (n, h)
             assert rel_err(st[n, h].cpu().numpy(), S_ref) <= TOL_BF16, (n, h)
+
+
+def test_bounded_gate_below_tensor_core_range_runs_fp32_path():
+    """Eq. 5 with g_min = -8 and bf16 d = 128: the tensor-core prefill scales rows and keys by
+    e^{G_r - G_p} against references up to 16 tokens away, which leaves fp32 range once 16 |g_min|
+    exceeds ~88, so kda_chunk_fwd takes the fp32 path (3 kernels, the fp32 path's workspace).  The
+    logits are shifted so that most decays sit near the bound; results against the fp64 oracle."""
+    from tests.gpu_util import oracle_prefill
+    d = _varlen(2, 128, "bf16", [200, 77, 64], seed=63)
+    d["z"] = (d["z"].float() + 4.0).to(d["z"].dtype)
+    d["g_min"] = -8.0
+    assert kda.chunk_fwd_kernel_count(sum(d["lengths"]), 3, 2, 128, 128, torch.bfloat16, d["cu_seqlens"],
+                                      g_min=-8.0) == 3
+    assert kda.chunk_fwd_workspace_size(sum(d["lengths"]), 3, 2, 128, 128, torch.bfloat16, 64, d["cu_seqlens"],
+                                        g_min=-8.0) == \
+        kda.chunk_fwd_workspace_size(sum(d["lengths"]), 3, 2, 128, 128, torch.bfloat16, 64, d["cu_seqlens"],
+                                     gate="softplus")
+    o, fs = run_prefill(d)
+    assert torch.isfinite(o).all() and torch.isfinite(fs).all()
+    compare_prefill(d, o, fs, oracle_prefill(d), TOL_BF16)
