@@ -550,43 +550,6 @@ def run_ours(args, rank, ws, local):
     del dev_in, dev_in2, pin, o2_, fs2_
     T_head, ms_head = T, ms
 
-    # ---------------- the backward pass on the same batch (one-pass workspace, ~0.42 MiB per chunk-head)
-    bwd_batch = None
-    if not args.no_backward:
-        del work
-        torch.cuda.empty_cache()
-        work = None
-        gen = torch.Generator(device=dev).manual_seed(79 + rank)
-        go_h = torch.randn(o.shape, generator=gen, device=dev).to(o.dtype)
-        gST_h = torch.randn(fs.shape, generator=gen, device=dev) * 0.1
-        need_h = kda.chunk_bwd_workspace_size(T, N, H, D, D)
-        work_h = torch.empty((need_h,), dtype=torch.uint8, device=dev)
-
-        def step_bh():
-            return kda.chunk_bwd(q, k, v, z, beta, b, a, go_h, g_min=d["g_min"], scale=d["scale"],
-                                 cu_seqlens=d["cu_seqlens"], initial_state=s0, grad_final_state=gST_h,
-                                 workspace=work_h)
-
-        for _ in range(2):
-            g_ = step_bh()
-            del g_
-        torch.cuda.synchronize()
-        assert kda.get_device_error() == 0
-        ha, hb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        hts = []
-        for _ in range(3):
-            ha.record(stream)
-            g_ = step_bh()
-            hb.record(stream)
-            hb.synchronize()
-            hts.append(ha.elapsed_time(hb))
-            del g_
-        msbh = max_over_ranks(sum(hts) / len(hts), ws)
-        bwd_batch = {"what": "kda_chunk_bwd on the headline batch: d q, k, v, z, beta, dt_bias, A_log, S0 "
-                             "from d o and d S_T (inputs larger than L2)",
-                     "ms_per_step": msbh, "tokens_per_s": T / (msbh / 1e3), "vs_forward": msbh / ms,
-                     "workspace_bytes": int(need_h)}
-        del go_h, gST_h, work_h
     del q, k, v, z, beta, d, o, fs, work
     torch.cuda.empty_cache()
 
@@ -927,6 +890,46 @@ def run_ours(args, rank, ws, local):
                          "single_steps_us": (Rw + Mw) * dms * 1e3,
                          "speedup_vs_single_steps": (Rw + Mw) * dms / rms}
         del dd2, cached, new
+
+    # ---------------- the backward pass on the headline batch (one-pass workspace, ~0.42 MiB per chunk-head);
+    # last, so that its 32 GB scratch does not shape the placement of the buffers timed above
+    bwd_batch = None
+    if not args.no_backward:
+        db = syn.make_prefill_shard(WORKLOAD, 2, rank, ws, device=dev)
+        Tb, Nb = sum(db["lengths"]), len(db["lengths"])
+        qb, kb, vb, zb, betab = (db[n] for n in ("q", "k", "v", "z", "beta"))
+        gen = torch.Generator(device=dev).manual_seed(79 + rank)
+        go_h = torch.randn(vb.shape, generator=gen, device=dev).to(vb.dtype)
+        gST_h = torch.randn((Nb, H, D, D), generator=gen, device=dev) * 0.1
+        need_h = kda.chunk_bwd_workspace_size(Tb, Nb, H, D, D)
+        work_h = torch.empty((need_h,), dtype=torch.uint8, device=dev)
+
+        def step_bh():
+            return kda.chunk_bwd(qb, kb, vb, zb, betab, db["dt_bias"], db["A_log"], go_h, g_min=db["g_min"],
+                                 scale=db["scale"], cu_seqlens=db["cu_seqlens"], initial_state=db["initial_state"],
+                                 grad_final_state=gST_h, workspace=work_h)
+
+        for _ in range(2):
+            g_ = step_bh()
+            del g_
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        ha, hb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hts = []
+        for _ in range(3):
+            ha.record(stream)
+            g_ = step_bh()
+            hb.record(stream)
+            hb.synchronize()
+            hts.append(ha.elapsed_time(hb))
+            del g_
+        msbh = max_over_ranks(sum(hts) / len(hts), ws)
+        bwd_batch = {"what": "kda_chunk_bwd on the headline batch: d q, k, v, z, beta, dt_bias, A_log, S0 "
+                             "from d o and d S_T (inputs larger than L2)",
+                     "ms_per_step": msbh, "tokens_per_s": Tb / (msbh / 1e3), "vs_forward": msbh / ms_head,
+                     "workspace_bytes": int(need_h)}
+        del go_h, gST_h, work_h, qb, kb, vb, zb, betab, db
+        torch.cuda.empty_cache()
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only): a seeded sample of the headline workload
     cpu = None
