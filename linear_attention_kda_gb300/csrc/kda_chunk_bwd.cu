@@ -1234,15 +1234,21 @@ chunk_chain_ckpt_tc_kernel(int64_t T, int N, const int32_t *__restrict__ cu, con
             unsigned char *B = sm + b * fc::BUF;
             const F32Record rec = f32_record(records, rec_bytes, cix, H, h, C, D, D);
             tile_async(reinterpret_cast<float *>(B + fc::UF), D, rec.U, D, C, D, ft, 128);
-#pragma unroll 2
-            for (int q = 0; q < 8; ++q) {  // W, K~: rows r, 8 channels per piece
-                const int e = ft + 128 * q, r = e >> 4, jc = e & 15;
-                float xw[8], xk[8];
-                vt_load8(rec.W + (size_t)r * D + 8 * jc, xw);
-                vt_load8(rec.K + (size_t)r * D + 8 * jc, xk);
-                const uint32_t off = img_chunk_off(64, r, jc);
-                *reinterpret_cast<uint4 *>(B + fc::WI + off) = vt_pack8(xw);
-                *reinterpret_cast<uint4 *>(B + fc::KI + off) = vt_pack8(xk);
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {  // W, then K~: rows r, pieces of 8 channels, loads before stores
+                const float *src = m == 0 ? rec.W : rec.K;
+                float x[8][8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int e = ft + 128 * q, r = e >> 4, jc = e & 15;
+                    vt_load8(src + (size_t)r * D + 8 * jc, x[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int e = ft + 128 * q, r = e >> 4, jc = e & 15;
+                    *reinterpret_cast<uint4 *>(B + (m == 0 ? fc::WI : fc::KI) + img_chunk_off(64, r, jc)) =
+                        vt_pack8(x[q]);
+                }
             }
             reinterpret_cast<float *>(B + fc::GM)[ft] = rec.gam[ft];
             cp_async_wait_all();

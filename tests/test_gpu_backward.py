@@ -111,6 +111,14 @@ def test_chunk_bwd_bf16_d128_matches_exact_gradients():
     _compare(d, _run(d, "lower_bound"), _ref(d, "lower_bound"), TOL_BF16)
 
 
+def test_chunk_bwd_bf16_d128_ragged_with_empty_sequence():
+    """The tensor-core chains and value side on a ragged bf16 batch: an empty sequence (no chunks:
+    d initial_state is d final_state passed through), one token, exactly one chunk, a chunk and one
+    token, and two and a half chunks."""
+    d = _inputs(2, 128, "bf16", [0, 1, 64, 65, 160], seed=57)
+    _compare(d, _run(d, "lower_bound"), _ref(d, "lower_bound"), TOL_BF16)
+
+
 def test_chunk_bwd_f32_d128_equal_lengths_without_states():
     """Two sequences of 96 tokens given by N alone (no cu_seqlens), zero initial state, no final-state
     gradient: d initial_state is then the full adjoint of the state entering each sequence."""
