@@ -92,3 +92,8 @@ def test_static_workspace_rejects_oversized_problem(cuda_ok):
                        scale=1.0, cu_seqlens=None, cu_seqlens_host=None, initial_state=None, final_state=None,
                        o=o.data_ptr(), chunk_size=64, gate_kind=1)
     assert L.kda_chunk_fwd_static_ws(ctypes.byref(a2), None) == 5
+    # so is the bounded gate below g_min = -5.5, which runs on the same fp32 path
+    a2.gate_kind, a2.g_min = 0, -8.0
+    assert L.kda_chunk_fwd_static_ws(ctypes.byref(a2), None) == 5
+    torch.cuda.synchronize()
+    assert bool((o.float() == 7.0).all())
