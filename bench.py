@@ -674,7 +674,8 @@ def run_ours(args, rank, ws, local):
         del work_sp, o_sp, fs_sp
 
     # ---------------- backward pass (training) on the same workload: gradients of q, k, v, z, beta, dt_bias,
-    # A_log from grad_o and grad_final_state (fp32 CUDA cores; the forward is recomputed inside)
+    # A_log from grad_o and grad_final_state (the forward recomputed inside; chains and value side on the
+    # tensor cores for this bf16 d = 128 workload)
     bwd = None
     if not args.no_backward:
         gen = torch.Generator(device=dev).manual_seed(77 + rank)

@@ -114,8 +114,8 @@ kda_status_t kda_gate(const kda_gate_args *args, struct CUstream_st *stream);
  * the last chunk of a sequence may be shorter.
  *
  * Supported: d_k = d_v in {64, 128}; chunk_size 64 (0 selects 64).
- * bf16 with d_k = d_v = 128 runs on the tensor cores (tcgen05); every other
- * case runs on the fp32 CUDA-core path.
+ * bf16 with d_k = d_v = 128 runs on the tensor cores (tcgen05) with the bounded
+ * gate and g_min >= -5.5; every other case runs on the fp32 CUDA-core path.
  * Empty sequences are allowed: their final state is their initial state (zero
  * without one), copied exactly.  An empty batch (T = 0) does only that and
  * reads no token pointer.
@@ -230,7 +230,9 @@ kda_status_t kda_recurrent_replay(const kda_replay_args *args, struct CUstream_s
  * state's adjoint runs backwards, Lambda_in = Diag(gamma^C) Lambda + scale Q^^T dO - W^T dV~ with
  * dV~ = K~ Lambda + scale A^T dO; every other gradient is local to its chunk (the state entering
  * it, the Lambda leaving it and dO).  The forward quantities are recomputed (nothing is kept from
- * kda_chunk_fwd); all arithmetic is fp32 on CUDA cores.  The gate's derivative (either gate kind)
+ * kda_chunk_fwd): the chunk-local quantities in fp32 on CUDA cores; with bf16 I/O at d_k = d_v = 128
+ * the two chains and the value-channel contractions are tcgen05 products of bf16 operand images with
+ * fp32 accumulation (fp32 I/O stays in fp32 throughout).  The gate's derivative (either gate kind)
  * is applied per token; dt_bias and A_log gradients are summed over all tokens
  * (and written, as zeros, when there are none: T = 0).  For an empty sequence the
  * initial state's gradient is its final state's (zero without one).

@@ -11,16 +11,19 @@
 // gamma, A and L with respect to q, k, v, beta and G; dg is the reverse cumulative sum of dG, and
 // the gate's derivative gives dz, d dt_bias and d A_log.
 //
-// Kernels (all fp32 CUDA-core arithmetic; the forward is recomputed by the fp32 path, which also
-// writes L and the state entering every chunk):
+// Kernels.  The forward is recomputed by the fp32 path's intra-chunk kernel, which also writes L; the
+// state entering every chunk comes from its chain or, for bf16 at d = 128, from
+// chunk_chain_ckpt_tc_kernel (S^T in tensor memory).  Then:
 //   chunk_rev_chain_kernel   one CTA per (sequence, head, 32 value columns): Lambda over the chunks
 //                            in reverse (columns of Lambda evolve independently, as those of S),
-//                            storing the Lambda leaving each chunk;
+//                            storing the Lambda leaving each chunk; for bf16 at d = 128
+//                            chunk_rev_chain_tc_kernel instead, Lambda^T in tensor memory;
 //   chunk_bwd_value_kernel_t one CTA of 512 threads per (chunk, head), the value channels 32 at a
 //                            time: V~, dV~, dX_U (T^T by back substitution), dv, and the contractions
 //                            over the value channels (dQ^, dW, dK~, dA, the X_U part of dL, d gamma,
 //                            the X_U part of d beta), accumulated in registers and written once;
-//                            It also solves dX_W = T^T dW and adds dL's X_W part at the end;
+//                            it also solves dX_W = T^T dW and adds dL's X_W part at the end; for bf16
+//                            at d = 128 chunk_bwd_value_tc_kernel instead (tcgen05 products);
 //   chunk_bwd_key_kernel     one CTA per (chunk, head): reads those sums, then per (row, channel)
 //                            the pairwise A and L terms, dq, dk, dG; the reverse cumulative sum;
 //                            dz, d beta and per-chunk sums for d dt_bias, d A_log;
