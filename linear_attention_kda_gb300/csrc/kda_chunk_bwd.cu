@@ -1555,9 +1555,10 @@ kda_status_t launch_bwd(const kda_chunk_bwd_args *a, const BwdLayout &Ly, void *
         }
         return st;
     }
-    // 3. value side per (chunk, head): on the tensor cores for bf16 I/O at d_k = d_v = 128 (dO read in
-    // 16-byte pieces), else on CUDA cores, the value channels 32 at a time
-    if (a->dtype == KDA_BF16 && dk == 128 && dv == 128 && ((uintptr_t)a->grad_o & 15) == 0) {
+    // 3. value side per (chunk, head): on the tensor cores for bf16 I/O at d_k = d_v = 128 (dO read, and the
+    // rows of dO and v prefetched, in 16-byte pieces), else on CUDA cores, the value channels 32 at a time
+    if (a->dtype == KDA_BF16 && dk == 128 && dv == 128 && ((uintptr_t)a->grad_o & 15) == 0 &&
+        ((uintptr_t)a->v & 15) == 0) {
         cudaFuncSetAttribute(bw::chunk_bwd_value_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)bw::vt::TOTAL);
         int dev = 0, sms = 148;
