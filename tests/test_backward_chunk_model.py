@@ -26,8 +26,50 @@ def _bf(x, on):
     return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
 
 
-def chunk_backward(q, k, v, z, beta, b, A_log, do, dST=None, g_min=-5.0, scale=1.0, C=64, rounded=False):
-    """Gradients of sum(o * do) + sum(S_T * dST) for one (sequence, head), chunk by chunk (Eq. 3-4 form)."""
+def _tf32(x):
+    """Round to 10 mantissa bits (nearest, ties to even), fp32 exponent range."""
+    a = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    a = ((a + 0xFFF + ((a >> 13) & 1)) >> 13) << 13
+    return a.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _key_terms_factorised(dA, dL, Q, K, B, G, fmt):
+    """The key side's four sums as products of scaled operand images, with the decays split against
+    two half references (p0 = 15 for rows 0..31, p1 = 47 for rows 32..63): every factor is the
+    exponential of at most 16 tokens of decay, or at most 1.  fmt: operand rounding, 'bf16' or 'tf32'."""
+    C = Q.shape[0]
+    rnd = (lambda x: _bf(x, True)) if fmt == "bf16" else _tf32
+    low = np.tril(np.ones((C, C)), -1)
+    h0 = np.arange(C) < 32
+    p0, p1 = 15, 47
+
+    def img(X, p, rows, sign):  # X_i e^{sign (G_p - G_i)} on `rows`, zero elsewhere
+        out = np.zeros_like(X)
+        out[rows] = X[rows] * np.exp(sign * (G[p] - G[rows]))
+        return rnd(out)
+
+    k0, k1 = img(K, p0, h0, 1), img(K, p1, np.ones(C, bool), 1)
+    q0, q1 = img(Q, p0, h0, -1), img(Q, p1, ~h0, -1)
+    bk0, bk1 = img(B[:, None] * K, p0, h0, -1), img(B[:, None] * K, p1, ~h0, -1)
+    dAl, dLl = rnd(dA * low), rnd(dL * low)
+    ra, rl, ca, cl = (np.zeros_like(K) for _ in range(4))
+    for r in range(C):
+        p, kk = (p0, k0) if r < 32 else (p1, k1)
+        er = np.exp(G[r] - G[p])
+        ra[r], rl[r] = er * (dAl[r] @ kk), er * (dLl[r] @ kk)
+        ca[r] = np.exp(G[p1] - G[r]) * (dAl[:, r] @ q1)
+        cl[r] = np.exp(G[p1] - G[r]) * (dLl[:, r] @ bk1)
+        if r < 32:
+            ca[r] += np.exp(G[p0] - G[r]) * (dAl[:, r] @ q0)
+            cl[r] += np.exp(G[p0] - G[r]) * (dLl[:, r] @ bk0)
+    return ra + np.diag(dA)[:, None] * K, rl, ca + np.diag(dA)[:, None] * Q, cl
+
+
+def chunk_backward(q, k, v, z, beta, b, A_log, do, dST=None, g_min=-5.0, scale=1.0, C=64, rounded=False,
+                   key_fmt=None):
+    """Gradients of sum(o * do) + sum(S_T * dST) for one (sequence, head), chunk by chunk (Eq. 3-4 form).
+    rounded: bf16 operands at the tensor-core kernels' rounding points; key_fmt: the key side's sums as
+    factorised products with 'bf16' or 'tf32' operands (None: the kernels' direct pairwise form)."""
     T, dk = q.shape
     dv = v.shape[1]
     eA = np.exp(A_log)
@@ -85,10 +127,13 @@ def chunk_backward(q, k, v, z, beta, b, A_log, do, dST=None, g_min=-5.0, scale=1
         dgam = np.sum(ckpt[ci] * lam[ci], 1)
         # key side
         Q, K, B, G, E = R['Q'], R['K'], R['B'], R['G'], R['E']
-        ra = np.einsum('ri,ic,ric->rc', dA * low, K, E) + np.diag(dA)[:, None] * K
-        rl = np.einsum('ri,ic,ric->rc', dL * low, K, E)
-        ca = np.einsum('ir,ic,ric->rc', dA * low, Q, 1.0 / E) + np.diag(dA)[:, None] * Q
-        cl = np.einsum('ir,i,ic,ric->rc', dL * low, B, K, 1.0 / E)
+        if key_fmt:
+            ra, rl, ca, cl = _key_terms_factorised(dA, dL, Q, K, B, G, key_fmt)
+        else:
+            ra = np.einsum('ri,ic,ric->rc', dA * low, K, E) + np.diag(dA)[:, None] * K
+            rl = np.einsum('ri,ic,ric->rc', dL * low, K, E)
+            ca = np.einsum('ir,ic,ric->rc', dA * low, Q, 1.0 / E) + np.diag(dA)[:, None] * Q
+            cl = np.einsum('ir,i,ic,ric->rc', dL * low, B, K, 1.0 / E)
         eG, eL = np.exp(G), np.exp(G[-1] - G)
         ktil = K * eL
         dG = (dXW * B[:, None] * K * eG + dQh * Q * eG - dKt * ktil + Q * ra - K * ca + B[:, None] * K * rl
@@ -136,3 +181,14 @@ def test_tensor_core_rounding_points_leave_headroom():
     for n in ("dq", "dk", "dv", "dz", "dbeta", "dS0"):
         e = _rel(got[n], ref[n])
         assert 1e-5 < e <= 5e-3, (n, e)
+
+
+def test_factorised_key_side_needs_tf32():
+    """The key side as factorised products (a tensor-core design): exact in fp64 terms, but dG sums
+    seven partly cancelling terms, so its operand precision shows in dz: bf16 operands exceed the
+    bf16 tolerance, tf32 operands stay inside it (with the other tensor-core rounding points on)."""
+    args, dST = _case(200, 128, 52)
+    ref = AG.head_backward(*args[:7], None, args[7], dST)
+    e_bf = _rel(chunk_backward(*args, dST=dST, rounded=True, key_fmt="bf16")["dz"], ref["dz"])
+    e_tf = _rel(chunk_backward(*args, dST=dST, rounded=True, key_fmt="tf32")["dz"], ref["dz"])
+    assert e_bf > 1e-2 and e_tf <= 5e-3, (e_bf, e_tf)
