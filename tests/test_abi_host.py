@@ -12,6 +12,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 import torch
 
@@ -165,6 +166,12 @@ def test_chunk_fwd_workspace_checks(lib):
     assert _call_chunk(lib, _chunk(g_min=-5.5), ws=FAKE + 16, ws_bytes=need) == 4
     assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, torch.bfloat16, g_min=-8.0)["kernels"] == 3
     assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, torch.bfloat16, g_min=-5.0)["fused"]
+    # the boundary: -5.5 itself stays on the tensor cores, the next float below it does not
+    below = float(np.nextafter(np.float32(-5.5), np.float32(-6.0)))
+    assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, torch.bfloat16, g_min=-5.5)["fused"]
+    assert kda.chunk_fwd_schedule(4096, 1, 32, 128, 128, torch.bfloat16, g_min=below)["kernels"] == 3
+    assert kda.chunk_fwd_workspace_size(4096, 1, 32, 128, 128, torch.bfloat16, g_min=below) == \
+        kda.chunk_fwd_workspace_size(4096, 1, 32, 128, 128, torch.bfloat16, gate="softplus")
 
 
 def test_chunk_fwd_host_seqlens_validated(lib):
